@@ -1,0 +1,152 @@
+"""ctypes front end of the CPU oracle (sage_oracle.c).
+
+TEST INFRASTRUCTURE ONLY: imported by the tests, the smoke check and the bench's
+CPU-baseline leg, never by the library.  It shares no code with the CUDA path.
+
+All arrays are float64 numpy arrays of one head, [N, D] token-major.  The
+quantizer mask selects which quantizers are on (QM_ALL = the low-bit scheme,
+0 = exact fp64 attention through the same code).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+QM_QK, QM_V, QM_P, QM_DO, QM_DS, QM_F32 = 1, 2, 4, 8, 16, 32
+QM_ALL = 63
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sage_oracle.c")
+_OUT = os.path.join(_HERE, "_build", "libsage_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle (plain C, OpenMP, IEEE operations only)."""
+    os.makedirs(os.path.dirname(_OUT), exist_ok=True)
+    if force or not os.path.exists(_OUT) or os.path.getmtime(_OUT) < os.path.getmtime(_SRC):
+        tmp = _OUT + f".{os.getpid()}.tmp"
+        cmd = ["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
+               "-fexcess-precision=standard", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _OUT)
+    return _OUT
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = build()
+            L = ctypes.CDLL(path)
+            dp = ctypes.POINTER(ctypes.c_double)
+            fp = ctypes.POINTER(ctypes.c_float)
+            i = ctypes.c_int
+            L.sage_oracle_e4m3.restype = ctypes.c_double
+            L.sage_oracle_e4m3.argtypes = [ctypes.c_double]
+            L.sage_oracle_e4m3_f32.argtypes = [fp, fp, ctypes.c_long]
+            L.sage_oracle_to_bf16.argtypes = [dp, dp, ctypes.c_long]
+            L.sage_oracle_quantize.argtypes = [i, i, dp, dp, dp, i, i, i] + [dp] * 11
+            L.sage_oracle_fwd.argtypes = [i, i, i, ctypes.c_double, i] + [dp] * 6 + [dp, fp, dp]
+            L.sage_oracle_bwd.argtypes = [i, i, i, ctypes.c_double, i, i] + [dp] * 12 + [dp] * 4
+            _lib = L
+    return _lib
+
+
+def _d(a):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _f(a):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_float))
+
+
+def _c64(x):
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def e4m3(x: np.ndarray) -> np.ndarray:
+    """e4m3 rounding (nearest even, saturating) of fp32 values."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    y = np.empty_like(x)
+    lib().sage_oracle_e4m3_f32(_f(x), _f(y), x.size)
+    return y
+
+
+def to_bf16(x: np.ndarray) -> np.ndarray:
+    """fp64 -> fp32 -> bf16 (both nearest even), returned as float64 values."""
+    x = _c64(x)
+    y = np.empty_like(x)
+    lib().sage_oracle_to_bf16(_d(x), _d(y), x.size)
+    return y
+
+
+def quantize(q, k, v, qk_norm, k_smooth, qmask=QM_ALL) -> dict:
+    q, k, v = _c64(q), _c64(k), _c64(v)
+    N, D = q.shape
+    o = {n: np.zeros((N, D)) for n in ("qn", "kn", "qx", "kx", "vx")}
+    o.update(qr=np.zeros(N), kr=np.zeros(N), kmean=np.zeros(D),
+             sq=np.zeros(max(1, -(-N // 128))), sk=np.zeros(max(1, -(-N // 64))), sv=np.zeros(D))
+    rc = lib().sage_oracle_quantize(N, D, _d(q), _d(k), _d(v), int(qk_norm), int(k_smooth), int(qmask),
+                                    _d(o["qn"]), _d(o["qr"]), _d(o["kn"]), _d(o["kr"]), _d(o["kmean"]),
+                                    _d(o["qx"]), _d(o["sq"]), _d(o["kx"]), _d(o["sk"]),
+                                    _d(o["vx"]), _d(o["sv"]))
+    if rc:
+        raise RuntimeError(f"oracle quantize failed ({rc})")
+    return o
+
+
+def forward(qz: dict, causal, sm_scale, qmask=QM_ALL) -> dict:
+    N, D = qz["qx"].shape
+    O64 = np.zeros((N, D))
+    O32 = np.zeros((N, D), dtype=np.float32)
+    L = np.zeros(N)
+    rc = lib().sage_oracle_fwd(N, D, int(causal), float(sm_scale), int(qmask),
+                               _d(qz["qx"]), _d(qz["sq"]), _d(qz["kx"]), _d(qz["sk"]),
+                               _d(qz["vx"]), _d(qz["sv"]), _d(O64), _f(O32), _d(L))
+    if rc:
+        raise RuntimeError(f"oracle forward failed ({rc})")
+    return {"O64": O64, "O32": O32, "Obf": to_bf16(O64), "LSE64": L,
+            "LSE32": L.astype(np.float32)}
+
+
+def backward(qz: dict, v, do, O, LSE, causal, sm_scale, qk_norm, qmask=QM_ALL) -> dict:
+    v, do, O, LSE = _c64(v), _c64(do), _c64(O), _c64(LSE)
+    N, D = v.shape
+    dQ, dK, dV = np.zeros((N, D)), np.zeros((N, D)), np.zeros((N, D))
+    Dv = np.zeros(N)
+    rc = lib().sage_oracle_bwd(N, D, int(causal), float(sm_scale), int(qk_norm), int(qmask),
+                               _d(v), _d(do), _d(O), _d(LSE),
+                               _d(qz["qx"]), _d(qz["sq"]), _d(qz["kx"]), _d(qz["sk"]),
+                               _d(qz["qn"]), _d(qz["qr"]), _d(qz["kn"]), _d(qz["kr"]),
+                               _d(dQ), _d(dK), _d(dV), _d(Dv))
+    if rc:
+        raise RuntimeError(f"oracle backward failed ({rc})")
+    return {"dQ64": dQ, "dK64": dK, "dV64": dV, "dQbf": to_bf16(dQ), "dKbf": to_bf16(dK),
+            "dVbf": to_bf16(dV), "Dvec": Dv}
+
+
+def run_head(q, k, v, do, causal, sm_scale, qk_norm=False, k_smooth=True, qmask=QM_ALL,
+             backward_pass=True) -> dict:
+    """Quantize, forward and (optionally) backward of one head.
+
+    In the low-bit scheme (F32 bit on) the backward consumes the forward's bf16 O
+    and fp32 LSE, as a training step would; with exact arithmetic it consumes
+    the fp64 values.
+    """
+    qz = quantize(q, k, v, qk_norm, k_smooth, qmask)
+    fw = forward(qz, causal, sm_scale, qmask)
+    out = dict(qz)
+    out.update(fw)
+    if backward_pass:
+        if qmask & QM_F32:
+            O_used, L_used = fw["Obf"], fw["LSE32"].astype(np.float64)
+        else:
+            O_used, L_used = fw["O64"], fw["LSE64"]
+        out.update(backward(qz, v, do, O_used, L_used, causal, sm_scale, qk_norm, qmask))
+    return out

@@ -1,0 +1,484 @@
+/*
+ * CPU oracle of SageBwd-style low-bit attention (forward and backward).
+ *
+ * TEST INFRASTRUCTURE ONLY.  The tests, the smoke check and the bench's CPU
+ * baseline leg are the only callers.  It shares no code, header, table or
+ * constant with the CUDA path and never calls it.
+ *
+ * What it computes, and where that is defined:
+ *  - "SageBwd: A Trainable Low-bit Attention" (euno.news summary, Methodology
+ *    1-2): six of the seven attention matmuls run quantized (QK^T and PV in the
+ *    forward; S recompute, dV, dQ, dK in the backward); the softmax-gradient
+ *    matmul dP = dO V^T stays in high precision.  Methodology 4 / Results:
+ *    QK-norm (unit-norm q and k per token before the dot product) and
+ *    K-smoothing.  K-smoothing is read as subtracting the per-(b,h) channel mean
+ *    of K over tokens, the only softmax-invariant reading of "smoothing K".
+ *  - "Attn-QAT: 4-Bit Attention With Quantization-Aware Training" (gist.science
+ *    summary, Methodology, principle 1): the backward recomputes P from the
+ *    saved log-sum-exp L in the same low precision as the forward.
+ *  - "ThriftAttention" (gist.science summary, Methodology step 2): the
+ *    FlashAttention-2 online softmax that merges key tiles into one output.
+ *  - The quantization granularity (Q per 128-token block, K per 64-token block,
+ *    symmetric INT8 with scale max|x|/127; FP8 e4m3 for P, V and dO) is the
+ *    plainest scheme consistent with those pages; they print no formula for it.
+ *
+ * Precision: softmax, accumulations and the dP matmul in fp64; integer dot
+ * products of the INT8 codes exact; every value the scheme stores in fp32 (the
+ * scales, the normalised q/k, the smoothed k, the logits, the probabilities
+ * before FP8 rounding) rounded to fp32 with round-to-nearest-even.  Build with
+ * -ffp-contract=off and without -ffast-math so that each written operation is
+ * one IEEE operation.
+ *
+ * Quantizer mask (qmask): each bit switches one quantizer on; all bits off
+ * turns the same code into exact fp64 attention, which the tests compare with
+ * textbook attention and finite differences.
+ *
+ * Parity status: every function below is pinned by the CPU tests (e4m3 rounding
+ * exhaustively against a library cast; the quantizers-off path against library
+ * attention and autograd and against finite differences; the quantized path on
+ * inputs it must reproduce exactly; invariants).  The exact FP8/INT8 codes on
+ * random inputs have no printed worked example to pin them to.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define QM_QK 1   /* INT8 codes for Q and K (forward QK^T, backward S, dQ, dK) */
+#define QM_V 2    /* e4m3 codes for V (forward PV) */
+#define QM_P 4    /* e4m3 codes for P (forward PV, backward dV and dS) */
+#define QM_DO 8   /* e4m3 codes for dO (backward dV) */
+#define QM_DS 16  /* INT8 codes for dS (backward dQ, dK) */
+#define QM_F32 32 /* fp32 rounding of the stored intermediate values */
+
+#define QBLK 128  /* Q tokens per INT8 scale */
+#define KBLK 64   /* K tokens per INT8 scale */
+#define TILE 128  /* keys per online-softmax step */
+
+static const double LOG2E = 1.4426950408889634074;
+static const double LN2 = 0.69314718055994530942;
+
+static inline double r32(int on, double x) { return on ? (double)(float)x : x; }
+
+/* OCP FP8 E4M3 (bias 7, no infinities, max 448, subnormal step 2^-9):
+ * round to nearest, ties to even, saturating to +-448. */
+double sage_oracle_e4m3(double x)
+{
+    double a = fabs(x);
+    if (a != a) return x;
+    if (a >= 448.0) return copysign(448.0, x);
+    if (a == 0.0) return x;
+    int e;
+    frexp(a, &e);          /* a = f * 2^e, f in [0.5, 1) */
+    int E = e - 1;         /* floor(log2 a) */
+    if (E < -6) E = -6;    /* subnormals share the quantum of the lowest binade */
+    double quantum = ldexp(1.0, E - 3);
+    double r = nearbyint(a / quantum) * quantum;
+    if (r > 448.0) r = 448.0;
+    return copysign(r, x);
+}
+
+void sage_oracle_e4m3_f32(const float *x, float *y, long n)
+{
+#pragma omp parallel for schedule(static)
+    for (long i = 0; i < n; ++i) y[i] = (float)sage_oracle_e4m3((double)x[i]);
+}
+
+/* fp64 -> fp32 (nearest even) -> bf16 (nearest even), returned as a double */
+static double bf16_round(double x)
+{
+    float f = (float)x;
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7f800000u) != 0x7f800000u) u += 0x7fffu + ((u >> 16) & 1u);
+    u &= 0xffff0000u;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+void sage_oracle_to_bf16(const double *x, double *y, long n)
+{
+    for (long i = 0; i < n; ++i) y[i] = bf16_round(x[i]);
+}
+
+/* Symmetric per-block INT8: scale = max|x| / 127 over `blk` consecutive tokens
+ * (all D channels), code = round-half-even(x / scale) clamped to [-127, 127]. */
+static void block_int8(const double *x, int N, int D, int blk, int on, int f32,
+                       double *codes, double *scales)
+{
+    int nb = (N + blk - 1) / blk;
+    for (int b = 0; b < nb; ++b) {
+        int t0 = b * blk, t1 = t0 + blk < N ? t0 + blk : N;
+        if (!on) {
+            scales[b] = 1.0;
+            memcpy(codes + (size_t)t0 * D, x + (size_t)t0 * D, sizeof(double) * (size_t)(t1 - t0) * D);
+            continue;
+        }
+        double a = 0.0;
+        for (size_t i = (size_t)t0 * D; i < (size_t)t1 * D; ++i) a = fmax(a, fabs(x[i]));
+        double s = r32(f32, a / 127.0);
+        scales[b] = a > 0.0 ? s : 0.0;
+        for (size_t i = (size_t)t0 * D; i < (size_t)t1 * D; ++i) {
+            if (a == 0.0) { codes[i] = 0.0; continue; }
+            double c = nearbyint(r32(f32, x[i] / s));
+            codes[i] = c > 127.0 ? 127.0 : (c < -127.0 ? -127.0 : c);
+        }
+    }
+}
+
+/* Per-channel e4m3: scale = max_t |x[t,d]| / 448, code = e4m3(x / scale). */
+static void channel_e4m3(const double *x, int N, int D, int on, int f32,
+                         double *codes, double *scales)
+{
+    for (int d = 0; d < D; ++d) {
+        if (!on) {
+            scales[d] = 1.0;
+            for (int t = 0; t < N; ++t) codes[(size_t)t * D + d] = x[(size_t)t * D + d];
+            continue;
+        }
+        double a = 0.0;
+        for (int t = 0; t < N; ++t) a = fmax(a, fabs(x[(size_t)t * D + d]));
+        double s = r32(f32, a / 448.0);
+        scales[d] = a > 0.0 ? s : 0.0;
+        for (int t = 0; t < N; ++t) {
+            size_t i = (size_t)t * D + d;
+            codes[i] = a > 0.0 ? sage_oracle_e4m3(r32(f32, x[i] / s)) : 0.0;
+        }
+    }
+}
+
+/* Per-token L2 normalisation: sigma = sum x^2 (fp64, exact for bf16 inputs),
+ * r = 1 / sqrt(sigma) (r = 0 for an all-zero token), x' = x * r. */
+static void l2_normalise(const double *x, int N, int D, int f32, double *xn, double *r)
+{
+    for (int t = 0; t < N; ++t) {
+        const double *row = x + (size_t)t * D;
+        double s = 0.0;
+        for (int d = 0; d < D; ++d) s += row[d] * row[d];
+        double sig = r32(f32, s);
+        double rt = sig > 0.0 ? r32(f32, 1.0 / r32(f32, sqrt(sig))) : 0.0;
+        r[t] = rt;
+        for (int d = 0; d < D; ++d) xn[(size_t)t * D + d] = r32(f32, row[d] * rt);
+    }
+}
+
+/*
+ * Quantize one head.  Inputs Q, K, V are [N, D] (row-major, token-major).
+ * Outputs: qn/kn the (optionally) normalised q', k' [N, D]; qr/kr the 1/||x||
+ * factors [N] (1 when QK-norm is off); kmean [D] (0 when smoothing is off);
+ * qx/kx INT8 codes [N, D] with scales sq [ceil(N/128)], sk [ceil(N/64)];
+ * vx e4m3 codes [N, D] with per-channel scales sv [D].
+ */
+int sage_oracle_quantize(int N, int D, const double *Q, const double *K, const double *V,
+                         int qk_norm, int k_smooth, int qmask,
+                         double *qn, double *qr, double *kn, double *kr, double *kmean,
+                         double *qx, double *sq, double *kx, double *sk,
+                         double *vx, double *sv)
+{
+    if (N < 0 || D <= 0) return 1;
+    int f32 = (qmask & QM_F32) != 0;
+    size_t E = (size_t)N * D;
+    if (qk_norm) {
+        l2_normalise(Q, N, D, f32, qn, qr);
+        l2_normalise(K, N, D, f32, kn, kr);
+    } else {
+        memcpy(qn, Q, sizeof(double) * E);
+        memcpy(kn, K, sizeof(double) * E);
+        for (int t = 0; t < N; ++t) qr[t] = kr[t] = 1.0;
+    }
+    double *ks = (double *)malloc(sizeof(double) * (E ? E : 1));
+    if (!ks) return 2;
+    for (int d = 0; d < D; ++d) {
+        double m = 0.0;
+        if (k_smooth && N > 0) {
+            double s = 0.0;
+            for (int t = 0; t < N; ++t) s += kn[(size_t)t * D + d];
+            m = r32(f32, s / N);
+        }
+        kmean[d] = m;
+        for (int t = 0; t < N; ++t) {
+            size_t i = (size_t)t * D + d;
+            ks[i] = k_smooth ? r32(f32, kn[i] - m) : kn[i];
+        }
+    }
+    block_int8(qn, N, D, QBLK, (qmask & QM_QK) != 0, f32, qx, sq);
+    block_int8(ks, N, D, KBLK, (qmask & QM_QK) != 0, f32, kx, sk);
+    channel_e4m3(V, N, D, (qmask & QM_V) != 0, f32, vx, sv);
+    free(ks);
+    return 0;
+}
+
+/* log2-domain logit of query i against key j: (sum_d qx*kx) * c, with
+ * c = RN(RN(sq_I * sk_J) * alpha), alpha = RN(sm_scale * log2 e).  With INT8
+ * codes every product and partial sum is an integer below 2^53, so the fp64
+ * sum is the exact integer dot product. */
+static inline double logit2(const double *qrow, const double *krow, int D, double c, int f32)
+{
+    double acc = 0.0;
+    for (int d = 0; d < D; ++d) acc += qrow[d] * krow[d];
+    return r32(f32, acc * c);
+}
+
+static inline double qk_factor(double sqI, double skJ, double alpha, int f32)
+{
+    return r32(f32, r32(f32, sqI * skJ) * alpha);
+}
+
+/*
+ * Forward for one head: online softmax over ascending 128-key tiles.
+ * Per row and tile: m' = max(m, max_j S2_ij); p~ = RN32(2^(S2 - m')) (fp64
+ * exp2); p8 = e4m3(RN32(448 p~)); l = l 2^(m - m') + sum p~;
+ * A = A 2^(m - m') + sum p8 v8.  Finish: O = A sv / (448 l), LSE = ln2 (m + log2 l).
+ * Outputs O64 [N, D], O32 [N, D] (float), LSE64 [N].
+ */
+int sage_oracle_fwd(int N, int D, int causal, double sm_scale, int qmask,
+                    const double *qx, const double *sq, const double *kx, const double *sk,
+                    const double *vx, const double *sv,
+                    double *O64, float *O32, double *LSE64)
+{
+    if (N < 0 || D <= 0) return 1;
+    int f32 = (qmask & QM_F32) != 0;
+    int qp = (qmask & QM_P) != 0;
+    double alpha = r32(f32, sm_scale * LOG2E);
+    int err = 0;
+#pragma omp parallel
+    {
+        double *A = (double *)malloc(sizeof(double) * D);
+        double *s2 = (double *)malloc(sizeof(double) * TILE);
+        if (!A || !s2) {
+#pragma omp atomic write
+            err = 2;
+        }
+#pragma omp for schedule(dynamic, 8)
+        for (int i = 0; i < N; ++i) {
+            if (!A || !s2) continue;
+            const double *qrow = qx + (size_t)i * D;
+            double m = -INFINITY, l = 0.0;
+            for (int d = 0; d < D; ++d) A[d] = 0.0;
+            for (int j0 = 0; j0 < N; j0 += TILE) {
+                int j1 = j0 + TILE < N ? j0 + TILE : N;
+                if (causal && j1 > i + 1) j1 = i + 1;
+                if (j1 <= j0) break;
+                double mt = -INFINITY;
+                for (int j = j0; j < j1; ++j) {
+                    double c = qk_factor(sq[i / QBLK], sk[j / KBLK], alpha, f32);
+                    s2[j - j0] = logit2(qrow, kx + (size_t)j * D, D, c, f32);
+                    mt = fmax(mt, s2[j - j0]);
+                }
+                double mn = fmax(m, mt);
+                double corr = (m == -INFINITY) ? 0.0 : exp2(m - mn);
+                l *= corr;
+                for (int d = 0; d < D; ++d) A[d] *= corr;
+                for (int j = j0; j < j1; ++j) {
+                    double pt = r32(f32, exp2(s2[j - j0] - mn));
+                    double p8 = qp ? sage_oracle_e4m3(r32(f32, 448.0 * pt)) : 448.0 * pt;
+                    l += pt;
+                    const double *vrow = vx + (size_t)j * D;
+                    for (int d = 0; d < D; ++d) A[d] += p8 * vrow[d];
+                }
+                m = mn;
+            }
+            for (int d = 0; d < D; ++d) {
+                double o = A[d] * sv[d] / (448.0 * l);
+                O64[(size_t)i * D + d] = o;
+                O32[(size_t)i * D + d] = (float)o;
+            }
+            LSE64[i] = LN2 * (m + log2(l));
+        }
+        free(A);
+        free(s2);
+    }
+    return err;
+}
+
+/* One (128-query block I, 64-key block J) tile of the backward.
+ * P = RN32(2^(S2 - RN32(LSE log2 e))), p8 = e4m3(RN32(448 P)), P^ = p8 / 448,
+ * dP = dO V^T (fp64, unquantized), dS = RN32(P^ (dP - Dvec)),
+ * dS8 = INT8 of dS with one scale max|dS|/127 for the tile.
+ * p8t/ds8t are [QBLK][KBLK]; returns the tile's dS scale. */
+static double bwd_tile(int I, int J, int N, int D, int causal, double alpha, int qmask,
+                       const double *qx, const double *sq, const double *kx, const double *sk,
+                       const double *V, const double *dO, const double *lse2, const double *Dv,
+                       double *p8t, double *ds8t)
+{
+    int f32 = (qmask & QM_F32) != 0;
+    int i0 = I * QBLK, i1 = i0 + QBLK < N ? i0 + QBLK : N;
+    int j0 = J * KBLK, j1 = j0 + KBLK < N ? j0 + KBLK : N;
+    double amax = 0.0;
+    double c = qk_factor(sq[I], sk[J], alpha, f32);
+    for (int i = i0; i < i1; ++i) {
+        for (int j = j0; j < j1; ++j) {
+            double *pp = p8t + (size_t)(i - i0) * KBLK + (j - j0);
+            double *dd = ds8t + (size_t)(i - i0) * KBLK + (j - j0);
+            if (causal && j > i) { *pp = 0.0; *dd = 0.0; continue; }
+            double s2 = logit2(qx + (size_t)i * D, kx + (size_t)j * D, D, c, f32);
+            double P = r32(f32, exp2(s2 - lse2[i]));
+            double p8 = (qmask & QM_P) ? sage_oracle_e4m3(r32(f32, 448.0 * P)) : 448.0 * P;
+            double dp = 0.0;
+            for (int d = 0; d < D; ++d) dp += dO[(size_t)i * D + d] * V[(size_t)j * D + d];
+            double ds = r32(f32, (p8 / 448.0) * (dp - Dv[i]));
+            *pp = p8;
+            *dd = ds;
+            amax = fmax(amax, fabs(ds));
+        }
+    }
+    if (!(qmask & QM_DS)) return 1.0;
+    double s = amax > 0.0 ? r32(f32, amax / 127.0) : 0.0;
+    for (int i = i0; i < i1; ++i)
+        for (int j = j0; j < j1; ++j) {
+            double *dd = ds8t + (size_t)(i - i0) * KBLK + (j - j0);
+            if (s == 0.0) { *dd = 0.0; continue; }
+            double q = nearbyint(r32(f32, *dd / s));
+            *dd = q > 127.0 ? 127.0 : (q < -127.0 ? -127.0 : q);
+        }
+    return s;
+}
+
+/* dx = r (dx' - x' (x' . dx')): gradient through x' = x / ||x||. */
+static void l2_normalise_grad(double *g, const double *xn, const double *r, int N, int D)
+{
+    for (int t = 0; t < N; ++t) {
+        double *gr = g + (size_t)t * D;
+        const double *xr = xn + (size_t)t * D;
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += xr[d] * gr[d];
+        for (int d = 0; d < D; ++d) gr[d] = r[t] * (gr[d] - xr[d] * dot);
+    }
+}
+
+/*
+ * Backward for one head.  V, dO are the unquantized inputs [N, D]; O the
+ * forward output used for Dvec_i = sum_d dO O; LSE the forward's natural-log
+ * LSE [N].  Codes and scales as returned by sage_oracle_quantize.
+ * dV_j  = (s_dO,d / 448) sum_i p8_ij dO8_id
+ * dQ_i += RN32(s_dS sk_J) sum_j dS8_ij kx_jd          (per tile)
+ * dK_j += RN32(s_dS sq_I) sum_i dS8_ij qx_id          (per tile)
+ * then dQ, dK scaled by sm_scale, and passed back through QK-norm; the
+ * K-smoothing Jacobian (I - 11^T/N) is applied as the identity: the exact dS
+ * rows sum to zero, so the smoothed-K gradient already has zero token mean.
+ * Outputs dQ, dK, dV [N, D] and Dvec [N] in fp64.
+ */
+int sage_oracle_bwd(int N, int D, int causal, double sm_scale, int qk_norm, int qmask,
+                    const double *V, const double *dO, const double *O, const double *LSE,
+                    const double *qx, const double *sq, const double *kx, const double *sk,
+                    const double *qn, const double *qr, const double *kn, const double *kr,
+                    double *dQ, double *dK, double *dV, double *Dvec)
+{
+    if (N < 0 || D <= 0) return 1;
+    int f32 = (qmask & QM_F32) != 0;
+    double alpha = r32(f32, sm_scale * LOG2E);
+    size_t E = (size_t)N * D;
+    double *lse2 = (double *)malloc(sizeof(double) * (N ? N : 1));
+    double *do8 = (double *)malloc(sizeof(double) * (E ? E : 1));
+    double *sdo = (double *)malloc(sizeof(double) * D);
+    if (!lse2 || !do8 || !sdo) { free(lse2); free(do8); free(sdo); return 2; }
+
+    for (int i = 0; i < N; ++i) {
+        double s = 0.0;
+        for (int d = 0; d < D; ++d) s += dO[(size_t)i * D + d] * O[(size_t)i * D + d];
+        Dvec[i] = s;
+        lse2[i] = r32(f32, LSE[i] * LOG2E);
+    }
+    channel_e4m3(dO, N, D, (qmask & QM_DO) != 0, f32, do8, sdo);
+    memset(dQ, 0, sizeof(double) * E);
+    memset(dK, 0, sizeof(double) * E);
+    memset(dV, 0, sizeof(double) * E);
+    int nI = (N + QBLK - 1) / QBLK, nJ = (N + KBLK - 1) / KBLK;
+    int err = 0;
+
+    /* dQ: one query block per task, all key blocks in order */
+#pragma omp parallel
+    {
+        double *p8t = (double *)malloc(sizeof(double) * QBLK * KBLK);
+        double *ds8t = (double *)malloc(sizeof(double) * QBLK * KBLK);
+        double *acc = (double *)malloc(sizeof(double) * 2 * D);
+        double *acc2 = acc ? acc + D : NULL;
+        if (!p8t || !ds8t || !acc) {
+#pragma omp atomic write
+            err = 2;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int I = 0; I < nI; ++I) {
+            if (!p8t || !ds8t || !acc) continue;
+            int i0 = I * QBLK, i1 = i0 + QBLK < N ? i0 + QBLK : N;
+            for (int J = 0; J < nJ; ++J) {
+                if (causal && J * KBLK > i1 - 1) break;
+                double s = bwd_tile(I, J, N, D, causal, alpha, qmask, qx, sq, kx, sk, V, dO,
+                                    lse2, Dvec, p8t, ds8t);
+                double c = r32(f32, s * sk[J]);
+                int j0 = J * KBLK, j1 = j0 + KBLK < N ? j0 + KBLK : N;
+                for (int i = i0; i < i1; ++i) {
+                    /* acc_d = sum_j dS8_ij kx_jd, j ascending */
+                    for (int d = 0; d < D; ++d) acc[d] = 0.0;
+                    for (int j = j0; j < j1; ++j) {
+                        double t = ds8t[(size_t)(i - i0) * KBLK + (j - j0)];
+                        const double *kr_ = kx + (size_t)j * D;
+                        for (int d = 0; d < D; ++d) acc[d] += t * kr_[d];
+                    }
+                    for (int d = 0; d < D; ++d) dQ[(size_t)i * D + d] += c * acc[d];
+                }
+            }
+        }
+        free(p8t);
+        free(ds8t);
+        free(acc);
+        (void)acc2;
+    }
+    /* dK, dV: one key block per task, all query blocks in order */
+#pragma omp parallel
+    {
+        double *p8t = (double *)malloc(sizeof(double) * QBLK * KBLK);
+        double *ds8t = (double *)malloc(sizeof(double) * QBLK * KBLK);
+        double *acc = (double *)malloc(sizeof(double) * 2 * D);
+        double *acc2 = acc ? acc + D : NULL;
+        if (!p8t || !ds8t || !acc) {
+#pragma omp atomic write
+            err = 2;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int J = 0; J < nJ; ++J) {
+            if (!p8t || !ds8t || !acc) continue;
+            int j0 = J * KBLK, j1 = j0 + KBLK < N ? j0 + KBLK : N;
+            for (int I = 0; I < nI; ++I) {
+                int i0 = I * QBLK, i1 = i0 + QBLK < N ? i0 + QBLK : N;
+                if (causal && j0 > i1 - 1) continue;
+                double s = bwd_tile(I, J, N, D, causal, alpha, qmask, qx, sq, kx, sk, V, dO,
+                                    lse2, Dvec, p8t, ds8t);
+                double c = r32(f32, s * sq[I]);
+                for (int j = j0; j < j1; ++j) {
+                    /* acck_d = sum_i dS8_ij qx_id, accv_d = sum_i p8_ij dO8_id, i ascending */
+                    for (int d = 0; d < D; ++d) { acc[d] = 0.0; acc2[d] = 0.0; }
+                    for (int i = i0; i < i1; ++i) {
+                        size_t t = (size_t)(i - i0) * KBLK + (j - j0);
+                        double a = ds8t[t], p = p8t[t];
+                        const double *qrow = qx + (size_t)i * D, *orow = do8 + (size_t)i * D;
+                        for (int d = 0; d < D; ++d) {
+                            acc[d] += a * qrow[d];
+                            acc2[d] += p * orow[d];
+                        }
+                    }
+                    for (int d = 0; d < D; ++d) {
+                        dK[(size_t)j * D + d] += c * acc[d];
+                        dV[(size_t)j * D + d] += (sdo[d] / 448.0) * acc2[d];
+                    }
+                }
+            }
+        }
+        free(p8t);
+        free(ds8t);
+        free(acc);
+        (void)acc2;
+    }
+    for (size_t i = 0; i < E; ++i) {
+        dQ[i] *= sm_scale;
+        dK[i] *= sm_scale;
+    }
+    if (qk_norm) {
+        l2_normalise_grad(dQ, qn, qr, N, D);
+        l2_normalise_grad(dK, kn, kr, N, D);
+    }
+    free(lse2);
+    free(do8);
+    free(sdo);
+    return err;
+}
