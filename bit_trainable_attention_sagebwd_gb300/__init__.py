@@ -1,0 +1,242 @@
+"""GB300 (sm_103a) low-bit attention for training: the SageBwd scheme.
+
+The compute path is the CUDA library libsage_attn.so (include/sage_attn.h).  This
+module only marshals arguments to it: the ctypes functions carry the C names
+(sage_attn_quantize, sage_attn_fwd, sage_attn_bwd, ...), and the torch helpers
+below allocate device memory, read the current stream and call them.  There is
+no CPU fallback: without the built library every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+from . import workloads  # noqa: F401  (seeded synthetic inputs)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsage_attn.so")
+
+SAGE_OK, SAGE_ERR_INVALID_ARG, SAGE_ERR_UNSUPPORTED, SAGE_ERR_CUDA, SAGE_ERR_TIMEOUT = 0, 1, 2, 3, 4
+
+# names declared in include/sage_attn.h
+ABI_FUNCTIONS = ("sage_attn_ws_bytes", "sage_attn_bwd_ws_bytes", "sage_attn_quantize", "sage_attn_fwd",
+                 "sage_attn_bwd", "sage_attn_ws_views", "sage_attn_get_status", "sage_attn_selftest_wait",
+                 "sage_attn_status_str", "sage_attn_timer_enable", "sage_attn_timer_read")
+
+
+class SageError(RuntimeError):
+    def __init__(self, fn, code):
+        super().__init__(f"{fn} failed: {code} ({status_str(code)})")
+        self.code = code
+
+
+class sage_ws_views(ctypes.Structure):
+    _fields_ = [("qc", ctypes.c_void_p), ("kc", ctypes.c_void_p), ("v8t", ctypes.c_void_p),
+                ("sq", ctypes.c_void_p), ("sk", ctypes.c_void_p), ("sv", ctypes.c_void_p),
+                ("kmean", ctypes.c_void_p), ("qr", ctypes.c_void_p), ("kr", ctypes.c_void_p),
+                ("status", ctypes.c_void_p), ("n_pad", ctypes.c_int)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib():
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"CUDA library not built: {LIB_PATH} (run __graft_entry__.build())")
+            L = ctypes.CDLL(LIB_PATH)
+            i, sz, vp, fp, u64 = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float, ctypes.c_ulonglong
+            L.sage_attn_ws_bytes.restype = sz
+            L.sage_attn_ws_bytes.argtypes = [i, i, i, i]
+            L.sage_attn_bwd_ws_bytes.restype = sz
+            L.sage_attn_bwd_ws_bytes.argtypes = [i, i, i, i]
+            L.sage_attn_quantize.argtypes = [vp, vp, vp, i, i, i, i, i, i, vp, sz, vp]
+            L.sage_attn_fwd.argtypes = [vp, vp, vp, vp, i, i, i, i, i, fp, vp]
+            L.sage_attn_bwd.argtypes = [vp] * 11 + [sz] + [i] * 7 + [fp, vp]
+            L.sage_attn_ws_views.argtypes = [vp, i, i, i, i, ctypes.POINTER(sage_ws_views)]
+            L.sage_attn_get_status.argtypes = [vp, vp]
+            L.sage_attn_selftest_wait.argtypes = [vp, u64, vp]
+            L.sage_attn_timer_enable.argtypes = [i]
+            L.sage_attn_timer_read.argtypes = [ctypes.c_char_p, ctypes.POINTER(ctypes.c_double),
+                                               ctypes.POINTER(ctypes.c_int)]
+            L.sage_attn_status_str.restype = ctypes.c_char_p
+            L.sage_attn_status_str.argtypes = [i]
+            _lib = L
+    return _lib
+
+
+# ----------------------------------------------------------- C names, as is
+
+def sage_attn_ws_bytes(B, H, N, D):
+    return lib().sage_attn_ws_bytes(B, H, N, D)
+
+
+def sage_attn_bwd_ws_bytes(B, H, N, D):
+    return lib().sage_attn_bwd_ws_bytes(B, H, N, D)
+
+
+def sage_attn_quantize(Q, K, V, B, H, N, D, qk_norm, k_smooth, ws, ws_bytes, stream):
+    return lib().sage_attn_quantize(Q, K, V, B, H, N, D, int(qk_norm), int(k_smooth), ws, ws_bytes, stream)
+
+
+def sage_attn_fwd(ws, O, LSE, O32, B, H, N, D, causal, sm_scale, stream):
+    return lib().sage_attn_fwd(ws, O, LSE, O32, B, H, N, D, int(causal), float(sm_scale), stream)
+
+
+def sage_attn_bwd(Q, K, V, O, LSE, dO, dQ, dK, dV, ws, bwd_ws, bwd_ws_bytes, B, H, N, D, causal, qk_norm,
+                  k_smooth, sm_scale, stream):
+    return lib().sage_attn_bwd(Q, K, V, O, LSE, dO, dQ, dK, dV, ws, bwd_ws, bwd_ws_bytes, B, H, N, D,
+                               int(causal), int(qk_norm), int(k_smooth), float(sm_scale), stream)
+
+
+def sage_attn_ws_views(ws, B, H, N, D) -> sage_ws_views:
+    v = sage_ws_views()
+    rc = lib().sage_attn_ws_views(ws, B, H, N, D, ctypes.byref(v))
+    if rc:
+        raise SageError("sage_attn_ws_views", rc)
+    return v
+
+
+def sage_attn_get_status(ws, stream):
+    return lib().sage_attn_get_status(ws, stream)
+
+
+def sage_attn_selftest_wait(ws, budget_ns, stream):
+    return lib().sage_attn_selftest_wait(ws, int(budget_ns), stream)
+
+
+def sage_attn_timer_enable(on):
+    return lib().sage_attn_timer_enable(int(on))
+
+
+def sage_attn_timer_read(kernel: str):
+    """(total ms, launches) of the timed launches of `kernel` since the last read."""
+    ms, n = ctypes.c_double(0.0), ctypes.c_int(0)
+    rc = lib().sage_attn_timer_read(kernel.encode(), ctypes.byref(ms), ctypes.byref(n))
+    if rc:
+        raise SageError("sage_attn_timer_read", rc)
+    return ms.value, n.value
+
+
+def status_str(code) -> str:
+    try:
+        return lib().sage_attn_status_str(int(code)).decode()
+    except RuntimeError:
+        return str(code)
+
+
+# ------------------------------------------------------------- torch helpers
+
+def _check(fn, rc):
+    if rc != SAGE_OK:
+        raise SageError(fn, rc)
+
+
+def _stream_ptr(stream=None):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _shape(q):
+    B, H, N, D = q.shape
+    return B, H, N, D
+
+
+def alloc_ws(B, H, N, D, device="cuda"):
+    import torch
+    n = sage_attn_ws_bytes(B, H, N, D)
+    if n == 0:
+        raise SageError("sage_attn_ws_bytes", SAGE_ERR_UNSUPPORTED)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def alloc_bwd_ws(B, H, N, D, device="cuda"):
+    import torch
+    n = sage_attn_bwd_ws_bytes(B, H, N, D)
+    if n == 0:
+        raise SageError("sage_attn_bwd_ws_bytes", SAGE_ERR_UNSUPPORTED)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def quantize(q, k, v, qk_norm=False, k_smooth=True, ws=None, stream=None):
+    """Quantize pass on bf16 [B, H, N, D] CUDA tensors; returns the workspace tensor."""
+    B, H, N, D = _shape(q)
+    if ws is None:
+        ws = alloc_ws(B, H, N, D, q.device)
+    _check("sage_attn_quantize", sage_attn_quantize(_ptr(q), _ptr(k), _ptr(v), B, H, N, D, qk_norm, k_smooth,
+                                                    _ptr(ws), ws.numel(), _stream_ptr(stream)))
+    return ws
+
+
+def forward(ws, B, H, N, D, causal, sm_scale=None, o=None, lse=None, o32=False, device="cuda", stream=None):
+    """Forward from a quantize workspace; returns (O bf16, LSE fp32[, O32 fp32])."""
+    import torch
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    if o is None:
+        o = torch.empty((B, H, N, D), dtype=torch.bfloat16, device=device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    O32 = torch.empty((B, H, N, D), dtype=torch.float32, device=device) if o32 is True else (o32 or None)
+    _check("sage_attn_fwd", sage_attn_fwd(_ptr(ws), _ptr(o), _ptr(lse), _ptr(O32), B, H, N, D, causal,
+                                          sm_scale, _stream_ptr(stream)))
+    return (o, lse, O32) if O32 is not None else (o, lse)
+
+
+def backward(q, k, v, o, lse, do, ws, causal, qk_norm=False, k_smooth=True, sm_scale=None, bwd_ws=None,
+             dq=None, dk=None, dv=None, stream=None):
+    """Backward; returns (dQ, dK, dV) bf16."""
+    import torch
+    B, H, N, D = _shape(q)
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    if bwd_ws is None:
+        bwd_ws = alloc_bwd_ws(B, H, N, D, q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check("sage_attn_bwd", sage_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq),
+                                          _ptr(dk), _ptr(dv), _ptr(ws), _ptr(bwd_ws), bwd_ws.numel(), B, H, N,
+                                          D, causal, qk_norm, k_smooth, sm_scale, _stream_ptr(stream)))
+    return dq, dk, dv
+
+
+def get_status(ws, stream=None) -> int:
+    return sage_attn_get_status(_ptr(ws), _stream_ptr(stream))
+
+
+def ws_tensors(ws, B, H, N, D) -> dict:
+    """Views of a quantize workspace as torch tensors (for inspection and tests)."""
+    import torch
+    v = sage_attn_ws_views(_ptr(ws), B, H, N, D)
+    base = ws.data_ptr()
+    np_ = v.n_pad
+    bh = B * H
+
+    def view(ptr, n_bytes, dtype, shape):
+        off = ptr - base
+        return ws[off:off + n_bytes].view(dtype).view(shape)
+
+    return {
+        "qc": view(v.qc, bh * np_ * D * 2, torch.bfloat16, (B, H, np_, D)),
+        "kc": view(v.kc, bh * np_ * D * 2, torch.bfloat16, (B, H, np_, D)),
+        "v8t": view(v.v8t, bh * D * np_, torch.uint8, (B, H, D, np_)),
+        "sq": view(v.sq, bh * (np_ // 128) * 4, torch.float32, (B, H, np_ // 128)),
+        "sk": view(v.sk, bh * (np_ // 64) * 4, torch.float32, (B, H, np_ // 64)),
+        "sv": view(v.sv, bh * D * 4, torch.float32, (B, H, D)),
+        "kmean": view(v.kmean, bh * D * 4, torch.float32, (B, H, D)),
+        "qr": view(v.qr, bh * np_ * 4, torch.float32, (B, H, np_)),
+        "kr": view(v.kr, bh * np_ * 4, torch.float32, (B, H, np_)),
+        "n_pad": np_,
+    }

@@ -1,0 +1,690 @@
+// Backward of SageBwd-style low-bit attention on tcgen05 tensor cores.
+//
+// "SageBwd: A Trainable Low-bit Attention" (euno.news summary), Methodology 2:
+// the backward keeps the forward's quantization; only the softmax-gradient
+// matmul dP = dO V^T stays in high precision (bf16 operands, fp32 accumulate).
+// "Attn-QAT: 4-Bit Attention With Quantization-Aware Training" (gist.science
+// summary), Methodology, principle 1: P is recomputed from the saved LSE and
+// rounded to e4m3 exactly as the forward rounds it.
+//
+// Kernels (all on the caller's stream):
+//   bwd_pre    per (head, 128-query block): D_i = sum_d dO*O, LSE*log2(e) (+inf on
+//              padded rows), partial channel maxima of |dO|, zeroed dQ accumulator
+//   bwd_docomb per head: dO channel scales max|dO|/448
+//   bwd_do8    per (head, 128-query block): e4m3 codes of dO, channel-major
+//   bwd_main   per (head, 128-key block), looping over query blocks:
+//                S^T  = K8 Q8^T        kind::f16 (bf16-held INT8 codes, exact)
+//                dP^T = V dO^T         kind::f16 (bf16)
+//                P^T  = e4m3(448 * 2^(S2 - LSE2)) / 448;  dS^T = P^T (dP^T - D)
+//                dV  += P8^T dO8       kind::f8f6f4
+//                dS  -> INT8, one scale per (128 query x 64 key) tile
+//                dK_part = dS8^T Q8    kind::f16, scaled per tile, summed in registers
+//                dQ_part = dS8 K8      kind::f16 per 64-key half, scaled, fp32 atomics
+//              dV and dK (x sm_scale, through QK-norm) written at the end
+//   bwd_dq     per query row: dQ = sm_scale * acc, through QK-norm, to bf16
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "../../include/sage_attn.h"
+#include "kernels.h"
+#include "layout.h"
+#include "ptx.cuh"
+#include "timer.h"
+#include "tmap.h"
+
+namespace sage {
+
+namespace {
+
+constexpr float kLog2_448 = 8.807354922057604f;
+constexpr int kPreThreads = 256;
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 t = __bfloat1622float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
+// ------------------------------------------------------------------ bwd_pre
+template <int D>
+__global__ void __launch_bounds__(kPreThreads) bwd_pre_kernel(const __nv_bfloat16* __restrict__ O,
+                                                               const __nv_bfloat16* __restrict__ dO,
+                                                               const float* __restrict__ LSE, int N,
+                                                               float* __restrict__ dvec, float* __restrict__ lse2,
+                                                               float* __restrict__ dopart,
+                                                               float* __restrict__ dqacc) {
+  constexpr int TPR = D / 8, RPP = kPreThreads / TPR, PASSES = 128 / RPP;
+  const int blk = blockIdx.x, bh = blockIdx.y, nb = gridDim.x, np = nb * 128;
+  const int tid = threadIdx.x, g = tid % TPR, ro = tid / TPR;
+  const size_t head = (size_t)bh * N * D;
+  float am[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) am[i] = 0.f;
+#pragma unroll
+  for (int p = 0; p < PASSES; ++p) {
+    const int r = p * RPP + ro, t = blk * 128 + r;
+    uint4 uo = make_uint4(0, 0, 0, 0), ud = make_uint4(0, 0, 0, 0);
+    if (t < N) {
+      uo = __ldg(reinterpret_cast<const uint4*>(O + head + (size_t)t * D) + g);
+      ud = __ldg(reinterpret_cast<const uint4*>(dO + head + (size_t)t * D) + g);
+    }
+    float o[8], d[8];
+    unpack8(uo, o);
+    unpack8(ud, d);
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      s = fmaf(o[i], d[i], s);
+      am[i] = fmaxf(am[i], fabsf(d[i]));
+    }
+#pragma unroll
+    for (int m = TPR / 2; m >= 1; m >>= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
+    if (g == 0) {
+      dvec[(size_t)bh * np + t] = t < N ? s : 0.f;
+      lse2[(size_t)bh * np + t] =
+          t < N ? (float)((double)LSE[(size_t)bh * N + t] * 1.4426950408889634074) : INFINITY;
+    }
+    float4* z = reinterpret_cast<float4*>(dqacc + ((size_t)bh * np + t) * D + g * 8);
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  __shared__ float s_max[RPP][D];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) s_max[ro][g * 8 + i] = am[i];
+  __syncthreads();
+  if (tid < D) {
+    float m = 0.f;
+    for (int r = 0; r < RPP; ++r) m = fmaxf(m, s_max[r][tid]);
+    dopart[((size_t)bh * nb + blk) * D + tid] = m;
+  }
+}
+
+__global__ void bwd_docomb_kernel(const float* __restrict__ dopart, int D, int nb, float* __restrict__ sdo) {
+  const int bh = blockIdx.x, d = threadIdx.x;
+  if (d >= D) return;
+  float m = 0.f;
+  for (int b = 0; b < nb; ++b) m = fmaxf(m, dopart[((size_t)bh * nb + b) * D + d]);
+  sdo[(size_t)bh * D + d] = m > 0.f ? __fdiv_rn(m, 448.0f) : 0.f;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kPreThreads) bwd_do8_kernel(const __nv_bfloat16* __restrict__ dO, int N,
+                                                               const float* __restrict__ sdo,
+                                                               uint8_t* __restrict__ do8t) {
+  constexpr int TPR = D / 8, RPP = kPreThreads / TPR, PASSES = 128 / RPP;
+  const int blk = blockIdx.x, bh = blockIdx.y, nb = gridDim.x, np = nb * 128;
+  const int tid = threadIdx.x, g = tid % TPR, ro = tid / TPR;
+  const size_t head = (size_t)bh * N * D;
+  __shared__ __align__(16) uint8_t s8[D][128];
+  float sc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) sc[i] = sdo[(size_t)bh * D + g * 8 + i];
+#pragma unroll
+  for (int p = 0; p < PASSES; ++p) {
+    const int row = p * RPP + ro, t = blk * 128 + row;
+    uint4 u = make_uint4(0, 0, 0, 0);
+    if (t < N) u = __ldg(reinterpret_cast<const uint4*>(dO + head + (size_t)t * D) + g);
+    float x[8];
+    unpack8(u, x);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int d = g * 8 + i;
+      const float y = sc[i] > 0.f ? __fdiv_rn(x[i], sc[i]) : 0.f;
+      s8[d][row ^ (((d >> 3) & 15) << 2)] = __nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3);
+    }
+  }
+  __syncthreads();
+  for (int idx = tid; idx < D * 8; idx += kPreThreads) {
+    const int d = idx >> 3, c = idx & 7, f = ((d >> 3) & 15) << 2;
+    uint4 val;
+    val.x = *reinterpret_cast<const uint32_t*>(&s8[d][(c * 16 + 0) ^ f]);
+    val.y = *reinterpret_cast<const uint32_t*>(&s8[d][(c * 16 + 4) ^ f]);
+    val.z = *reinterpret_cast<const uint32_t*>(&s8[d][(c * 16 + 8) ^ f]);
+    val.w = *reinterpret_cast<const uint32_t*>(&s8[d][(c * 16 + 12) ^ f]);
+    reinterpret_cast<uint4*>(do8t + ((size_t)bh * D + d) * np + blk * 128)[c] = val;
+  }
+}
+
+// ------------------------------------------------------------------ bwd_main
+template <int D>
+struct BwdSmem {
+  uint8_t k[128 * D * 2];    // K codes of this key block (resident)
+  uint8_t v[128 * D * 2];    // V bf16 of this key block (resident)
+  uint8_t q[128 * D * 2];    // Q codes of the current query block
+  uint8_t dob[128 * D * 2];  // dO bf16 of the current query block
+  uint8_t do8[D * 128];      // dO e4m3 codes, channel-major
+  uint8_t p[128 * 128];      // P^T e4m3, key rows
+  uint8_t ds[128 * 128 * 2]; // dS^T INT8 codes in bf16, key rows
+  float bias[128];           // log2(448) - LSE2_i of the current query block
+  float dvec[128];
+  float smax[4];
+  uint64_t bar_kv;
+  uint64_t bar_q_full, bar_do_full, bar_do8_full;
+  uint64_t bar_q_free, bar_do_free, bar_do8_free;
+  uint64_t bar_sdp, bar_p, bar_ds, bar_part, bar_free;
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct BwdParams {
+  int N, np, nqb, causal, qk_norm;
+  float alpha, sm_scale;
+  const float* sq;
+  const float* sk;
+  const float* sdo;
+  const float* lse2;
+  const float* dvec;
+  const __nv_bfloat16* K;
+  const float* kr;
+  float* dqacc;
+  __nv_bfloat16* dK;
+  __nv_bfloat16* dV;
+  int* status;
+};
+
+__device__ __forceinline__ void named_bar_compute() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+template <int D>
+__global__ void __launch_bounds__(256, 1)
+    bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_do8, const BwdParams prm) {
+  extern __shared__ uint8_t smem_raw[];
+  BwdSmem<D>& sm = *reinterpret_cast<BwdSmem<D>*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int kb = blockIdx.x, bh = blockIdx.y;
+  const int I0 = prm.causal ? kb : 0;
+  const int n_it = prm.nqb - I0;
+  constexpr uint32_t kCols = 512;
+  constexpr uint32_t cS = 0, cDP = 128, cDV = 256, cDQB = 384;  // TMEM column bases
+  constexpr uint32_t kTile = 128 * D * 2;
+
+  if (tid == 0) {
+    mbar_init(&sm.bar_kv, 1);
+    mbar_init(&sm.bar_q_full, 1);
+    mbar_init(&sm.bar_do_full, 1);
+    mbar_init(&sm.bar_do8_full, 1);
+    mbar_init(&sm.bar_q_free, 1);
+    mbar_init(&sm.bar_do_free, 1);
+    mbar_init(&sm.bar_do8_free, 1);
+    mbar_init(&sm.bar_sdp, 1);
+    mbar_init(&sm.bar_p, 128);
+    mbar_init(&sm.bar_ds, 128);
+    mbar_init(&sm.bar_part, 1);
+    mbar_init(&sm.bar_free, 128);
+    sm.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem_base, kCols);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  volatile int* abort = &sm.abort;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- producer
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+    tma_prefetch_desc(&tm_do8);
+    mbar_arrive_expect_tx(&sm.bar_kv, 2 * kTile);
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c) {
+      tma_load_3d(sm.k + c * 16384, &tm_k, c * 64, kb * 128, bh, &sm.bar_kv);
+      tma_load_3d(sm.v + c * 16384, &tm_v, c * 64, kb * 128, bh, &sm.bar_kv);
+    }
+    for (int it = 0; it < n_it; ++it) {
+      const int I = I0 + it;
+      if (it > 0 && !mbar_wait(&sm.bar_do_free, (it - 1) & 1, abort)) break;
+      mbar_arrive_expect_tx(&sm.bar_do_full, kTile);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) tma_load_3d(sm.dob + c * 16384, &tm_do, c * 64, I * 128, bh, &sm.bar_do_full);
+      if (it > 0 && !mbar_wait(&sm.bar_q_free, (it - 1) & 1, abort)) break;
+      mbar_arrive_expect_tx(&sm.bar_q_full, kTile);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) tma_load_3d(sm.q + c * 16384, &tm_q, c * 64, I * 128, bh, &sm.bar_q_full);
+      if (it > 0 && !mbar_wait(&sm.bar_do8_free, (it - 1) & 1, abort)) break;
+      mbar_arrive_expect_tx(&sm.bar_do8_full, D * 128);
+      tma_load_3d(sm.do8, &tm_do8, I * 128, 0, bh, &sm.bar_do8_full);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- UMMA issuer
+    constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);   // S^T, dP^T
+    constexpr uint32_t id_dv = idesc_e4m3(128, D);                   // dV
+    constexpr uint32_t id_dk = idesc_bf16(128, D, false, true);      // dK: A K-major, B MN-major
+    constexpr uint32_t id_dq = idesc_bf16(128, D, true, true);       // dQ: A, B MN-major
+    const uint32_t a_k = smem_u32(sm.k), a_v = smem_u32(sm.v), a_q = smem_u32(sm.q), a_do = smem_u32(sm.dob);
+    const uint32_t a_do8 = smem_u32(sm.do8), a_p = smem_u32(sm.p), a_ds = smem_u32(sm.ds);
+    bool ok = mbar_wait(&sm.bar_kv, 0, abort);
+    for (int it = 0; ok && it < n_it; ++it) {
+      const uint32_t ph = it & 1;
+      if (!mbar_wait(&sm.bar_q_full, ph, abort) || !mbar_wait(&sm.bar_do_full, ph, abort)) break;
+      if (it > 0 && !mbar_wait(&sm.bar_free, (it - 1) & 1, abort)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+        umma_bf16(tmem + cS, sdesc_sw128(a_k + off, 16, 1024), sdesc_sw128(a_q + off, 16, 1024), id_s, kk > 0);
+      }
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+        umma_bf16(tmem + cDP, sdesc_sw128(a_v + off, 16, 1024), sdesc_sw128(a_do + off, 16, 1024), id_s, kk > 0);
+      }
+      umma_commit(&sm.bar_sdp);
+      umma_commit(&sm.bar_do_free);
+      if (!mbar_wait(&sm.bar_p, ph, abort) || !mbar_wait(&sm.bar_do8_full, ph, abort)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        umma_f8(tmem + cDV, sdesc_sw128(a_p + kk * 32, 16, 1024), sdesc_sw128(a_do8 + kk * 32, 16, 1024), id_dv,
+                (it > 0 || kk > 0));
+      umma_commit(&sm.bar_do8_free);
+      if (!mbar_wait(&sm.bar_ds, ph, abort)) break;
+      tc_fence_after();
+      // dK_part[key, d] = sum_q dS^T[key, q] Q[q, d]
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t offa = (kk >> 2) * 16384 + (kk & 3) * 32;
+        umma_bf16(tmem + cS, sdesc_sw128(a_ds + offa, 16, 1024), sdesc_sw128(a_q + kk * 2048, 16384, 1024), id_dk,
+                  kk > 0);
+      }
+      // dQ halves: [q, d] = sum_{key in half} dS[q, key] K[key, d]
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        umma_bf16(tmem + cDP, sdesc_sw128(a_ds + kk * 2048, 16384, 1024), sdesc_sw128(a_k + kk * 2048, 16384, 1024),
+                  id_dq, kk > 0);
+#pragma unroll
+      for (int kk = 4; kk < 8; ++kk)
+        umma_bf16(tmem + cDQB, sdesc_sw128(a_ds + kk * 2048, 16384, 1024),
+                  sdesc_sw128(a_k + kk * 2048, 16384, 1024), id_dq, kk > 4);
+      umma_commit(&sm.bar_part);
+      umma_commit(&sm.bar_q_free);
+    }
+  } else if (warp >= 4) {
+    // ---------------- compute: thread t owns key row t (TMEM lane t)
+    const int t = tid - 128;
+    const int key = kb * 128 + t;
+    const bool key_ok = key < prm.N;
+    const int half = t >> 6;
+    const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
+    const float* skh = prm.sk + (size_t)bh * prm.nqb * 2;
+    const float sk_mine = skh[2 * kb + half];
+    const float sk0 = skh[2 * kb], sk1 = skh[2 * kb + 1];
+    float dk[D];
+#pragma unroll
+    for (int d = 0; d < D; ++d) dk[d] = 0.f;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int I = I0 + it;
+      const uint32_t ph = it & 1;
+      {
+        const size_t r = (size_t)bh * prm.np + I * 128 + t;
+        sm.bias[t] = kLog2_448 - prm.lse2[r];
+        sm.dvec[t] = prm.dvec[r];
+      }
+      named_bar_compute();
+      const float sqI = prm.sq[(size_t)bh * prm.nqb + I];
+      const float cs = __fmul_rn(__fmul_rn(sqI, sk_mine), prm.alpha);
+      const bool diag = prm.causal && I == kb;
+      if (!mbar_wait(&sm.bar_sdp, ph, abort)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // ---- P^T row: e4m3(448 * 2^(S2 - LSE2)), masked entries 0
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t s[32];
+        tmem_ld32(tmem + lane_base + cS + c * 32, s);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          float p[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int qi = c * 32 + e + u;
+            float v = ex2(fmaf(__uint_as_float(s[e + u]), cs, sm.bias[qi]));
+            if (!key_ok || (diag && qi < t)) v = 0.f;
+            p[u] = v;
+          }
+          const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(p[0], p[1]), __NV_SATFINITE, __NV_E4M3);
+          const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(p[2], p[3]), __NV_SATFINITE, __NV_E4M3);
+          pk[(c * 32 + e) >> 2] = (uint32_t)lo | ((uint32_t)hi << 16);
+        }
+      }
+      {
+        uint8_t* prow = sm.p + (t >> 3) * 1024 + (t & 7) * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(prow + ((c ^ (t & 7)) << 4)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&sm.bar_p);
+      // ---- dS^T = P^ (dP^T - D), kept in TMEM (over dP^T) until the tile max is known
+      float amax = 0.f;
+      const uint8_t* prow_rd = sm.p + (t >> 3) * 1024 + (t & 7) * 128;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t dp[32];
+        tmem_ld32(tmem + lane_base + cDP + c * 32, dp);
+        // this row's 32 P codes of the chunk, read back from the swizzled tile
+        uint32_t pw[8];
+        {
+          const uint4 a = *reinterpret_cast<const uint4*>(prow_rd + (((2 * c) ^ (t & 7)) << 4));
+          const uint4 b = *reinterpret_cast<const uint4*>(prow_rd + (((2 * c + 1) ^ (t & 7)) << 4));
+          pw[0] = a.x; pw[1] = a.y; pw[2] = a.z; pw[3] = a.w;
+          pw[4] = b.x; pw[5] = b.y; pw[6] = b.z; pw[7] = b.w;
+        }
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const int qi = c * 32 + e;
+          const uint32_t w = pw[e >> 2] >> ((e & 3) * 8);
+          const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xffffu), __NV_E4M3);
+          const float2 pf = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+          const float d0 = (pf.x * (1.0f / 448.0f)) * (__uint_as_float(dp[e]) - sm.dvec[qi]);
+          const float d1 = (pf.y * (1.0f / 448.0f)) * (__uint_as_float(dp[e + 1]) - sm.dvec[qi + 1]);
+          amax = fmaxf(amax, fmaxf(fabsf(d0), fabsf(d1)));
+          dp[e] = __float_as_uint(d0);
+          dp[e + 1] = __float_as_uint(d1);
+        }
+        tmem_st32(tmem + lane_base + cDP + c * 32, dp);
+      }
+      tmem_st_wait();
+#pragma unroll
+      for (int m = 16; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+      if (lane == 0) sm.smax[warp - 4] = amax;
+      named_bar_compute();
+      const float a0 = fmaxf(sm.smax[0], sm.smax[1]), a1 = fmaxf(sm.smax[2], sm.smax[3]);
+      const float sds0 = a0 > 0.f ? __fdiv_rn(a0, 127.0f) : 0.f;
+      const float sds1 = a1 > 0.f ? __fdiv_rn(a1, 127.0f) : 0.f;
+      const float sds = half ? sds1 : sds0;
+      const float inv = sds > 0.f ? 1.0f / sds : 0.f;
+      // ---- dS^T codes -> shared memory (bf16 containers, 128B-swizzled key rows)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t dsv[32];
+        tmem_ld32(tmem + lane_base + cDP + c * 32, dsv);
+        tmem_ld_wait();
+        uint32_t packed[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          int c0 = __float2int_rn(__uint_as_float(dsv[e]) * inv);
+          int c1 = __float2int_rn(__uint_as_float(dsv[e + 1]) * inv);
+          c0 = max(-127, min(127, c0));
+          c1 = max(-127, min(127, c1));
+          const __nv_bfloat162 h = __floats2bfloat162_rn((float)c0, (float)c1);
+          packed[e >> 1] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        // queries [32c, 32c+32): block c/2, bytes (c&1)*64 .. +64 of the 128-byte row
+        uint8_t* rowp = sm.ds + (c >> 1) * 16384 + (t >> 3) * 1024 + (t & 7) * 128;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int chunk = (c & 1) * 4 + u;
+          *reinterpret_cast<uint4*>(rowp + ((chunk ^ (t & 7)) << 4)) =
+              make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&sm.bar_ds);
+      if (!mbar_wait(&sm.bar_part, ph, abort)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // ---- dK += RN(s_dS * s_q) * part
+      const float ck = __fmul_rn(sds, sqI);
+#pragma unroll
+      for (int c = 0; c < D; c += 32) {
+        uint32_t pv[32];
+        tmem_ld32(tmem + lane_base + cS + c, pv);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) dk[c + e] = fmaf(ck, __uint_as_float(pv[e]), dk[c + e]);
+      }
+      // ---- dQ (query row t of block I) += ca * half0 + cb * half1
+      const float ca = __fmul_rn(sds0, sk0), cb = __fmul_rn(sds1, sk1);
+      const int qrow = I * 128 + t;
+      const bool q_ok = qrow < prm.N;
+      float* dst = prm.dqacc + ((size_t)bh * prm.np + qrow) * D;
+      // the TMEM loads are warp-collective: every lane issues them, only live rows add
+#pragma unroll
+      for (int c = 0; c < D; c += 16) {
+        uint32_t va[16], vb[16];
+        tmem_ld16(tmem + lane_base + cDP + c, va);
+        tmem_ld16(tmem + lane_base + cDQB + c, vb);
+        tmem_ld_wait();
+        if (q_ok) {
+#pragma unroll
+          for (int e = 0; e < 16; e += 4) {
+            float4 add;
+            add.x = fmaf(ca, __uint_as_float(va[e]), cb * __uint_as_float(vb[e]));
+            add.y = fmaf(ca, __uint_as_float(va[e + 1]), cb * __uint_as_float(vb[e + 1]));
+            add.z = fmaf(ca, __uint_as_float(va[e + 2]), cb * __uint_as_float(vb[e + 2]));
+            add.w = fmaf(ca, __uint_as_float(va[e + 3]), cb * __uint_as_float(vb[e + 3]));
+            atomicAdd(reinterpret_cast<float4*>(dst + c + e), add);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&sm.bar_free);
+    }
+    // ---------------- epilogue: dV and dK rows of this key block
+    if (ok) {
+      tc_fence_after();
+      const size_t orow = ((size_t)bh * prm.N + key) * D;
+      const float* sdoh = prm.sdo + (size_t)bh * D;
+#pragma unroll
+      for (int c = 0; c < D; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + cDV + c, v);
+        tmem_ld_wait();
+        if (key_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(prm.dV + orow + c);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint4 u;
+            __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int d0 = c + 8 * i + 2 * e;
+              h[e] = __floats2bfloat162_rn(__uint_as_float(v[8 * i + 2 * e]) * (sdoh[d0] * (1.0f / 448.0f)),
+                                           __uint_as_float(v[8 * i + 2 * e + 1]) * (sdoh[d0 + 1] * (1.0f / 448.0f)));
+            }
+            dst[i] = u;
+          }
+        }
+      }
+      if (key_ok) {
+#pragma unroll
+        for (int d = 0; d < D; ++d) dk[d] *= prm.sm_scale;
+        if (prm.qk_norm) {
+          // dk = r (dk' - k' (k' . dk')), k' = RN(k r) as the quantize pass formed it
+          const float r = prm.kr[(size_t)bh * prm.np + key];
+          const uint4* krow = reinterpret_cast<const uint4*>(prm.K + orow);
+          float dot = 0.f;
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) {
+            float f[8];
+            unpack8(__ldg(krow + c), f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) dot = fmaf(__fmul_rn(f[e], r), dk[c * 8 + e], dot);
+          }
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) {
+            float f[8];
+            unpack8(__ldg(krow + c), f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) dk[c * 8 + e] = r * (dk[c * 8 + e] - __fmul_rn(f[e], r) * dot);
+          }
+        }
+        uint4* dst = reinterpret_cast<uint4*>(prm.dK + orow);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+          uint4 u;
+          __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) h[e] = __floats2bfloat162_rn(dk[c * 8 + 2 * e], dk[c * 8 + 2 * e + 1]);
+          dst[c] = u;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, kCols);
+  if (tid == 0 && sm.abort) atomicExch(prm.status, kDevTimeout);
+}
+
+// ------------------------------------------------------------------ bwd_dq
+template <int D>
+__global__ void __launch_bounds__(kPreThreads) bwd_dq_kernel(const float* __restrict__ dqacc,
+                                                              const __nv_bfloat16* __restrict__ Q,
+                                                              const float* __restrict__ qr, int N, int np,
+                                                              int qk_norm, float sm_scale,
+                                                              __nv_bfloat16* __restrict__ dQ) {
+  constexpr int TPR = D / 8, RPP = kPreThreads / TPR;
+  const int bh = blockIdx.y;
+  const int tid = threadIdx.x, g = tid % TPR, ro = tid / TPR;
+  const int t = blockIdx.x * RPP + ro;
+  const bool live = t < N;  // no early exit: the row's lanes shuffle together below
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+  if (live) {
+    const float4* src = reinterpret_cast<const float4*>(dqacc + ((size_t)bh * np + t) * D + g * 8);
+    a = src[0];
+    b = src[1];
+  }
+  float x[8] = {a.x * sm_scale, a.y * sm_scale, a.z * sm_scale, a.w * sm_scale,
+                b.x * sm_scale, b.y * sm_scale, b.z * sm_scale, b.w * sm_scale};
+  const size_t row = ((size_t)bh * N + t) * D;
+  if (qk_norm) {
+    const float r = live ? qr[(size_t)bh * np + t] : 0.f;
+    float qn[8];
+    unpack8(live ? __ldg(reinterpret_cast<const uint4*>(Q + row) + g) : make_uint4(0, 0, 0, 0), qn);
+    float dot = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      qn[i] = __fmul_rn(qn[i], r);
+      dot = fmaf(qn[i], x[i], dot);
+    }
+#pragma unroll
+    for (int m = TPR / 2; m >= 1; m >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, m, TPR);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = r * (x[i] - qn[i] * dot);
+  }
+  uint4 u;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) h[e] = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+  if (live) reinterpret_cast<uint4*>(dQ + row)[g] = u;
+}
+
+template <int D>
+int launch_main_t(const CUtensorMap& tk, const CUtensorMap& tq, const CUtensorMap& tv, const CUtensorMap& tdo,
+                  const CUtensorMap& tdo8, const BwdParams& p, int BH, cudaStream_t st) {
+  size_t smem = sizeof(BwdSmem<D>) + 1024;
+  if (smem < 120 * 1024) smem = 120 * 1024;  // one CTA per SM: it holds all 512 TMEM columns
+  auto kern = bwd_main_kernel<D>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 3;
+  ScopedTimer timer("bwd_main", st);
+  kern<<<dim3(p.nqb, BH), 256, smem, st>>>(tk, tq, tv, tdo, tdo8, p);
+  return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
+
+}  // namespace
+
+int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO,
+               void* dQ, void* dK, void* dV, const void* ws, void* bwd_ws, int B, int H, int N, int D, int causal,
+               int qk_norm, int k_smooth, float sm_scale, cudaStream_t st) {
+  (void)k_smooth;  // the smoothing Jacobian is applied as the identity (dS rows sum to zero)
+  const QuantWs QL = quant_ws_layout(B, H, N, D);
+  const BwdWs BL = bwd_ws_layout(B, H, N, D);
+  const uint8_t* w = static_cast<const uint8_t*>(ws);
+  uint8_t* bw = static_cast<uint8_t*>(bwd_ws);
+  const int BH = B * H, np = QL.np, nb = np / 128;
+  float* dvec = reinterpret_cast<float*>(bw + BL.dvec);
+  float* lse2 = reinterpret_cast<float*>(bw + BL.lse2);
+  float* dopart = reinterpret_cast<float*>(bw + BL.dopart);
+  float* sdo = reinterpret_cast<float*>(bw + BL.sdo);
+  float* dqacc = reinterpret_cast<float*>(bw + BL.dqacc);
+  uint8_t* do8t = bw + BL.do8t;
+  auto* o = static_cast<const __nv_bfloat16*>(O);
+  auto* dob = static_cast<const __nv_bfloat16*>(dO);
+  const dim3 g(nb, BH);
+  {
+  ScopedTimer timer("bwd_pre", st);
+  if (D == 128) {
+    bwd_pre_kernel<128><<<g, kPreThreads, 0, st>>>(o, dob, LSE, N, dvec, lse2, dopart, dqacc);
+  } else {
+    bwd_pre_kernel<64><<<g, kPreThreads, 0, st>>>(o, dob, LSE, N, dvec, lse2, dopart, dqacc);
+  }
+  bwd_docomb_kernel<<<BH, 128, 0, st>>>(dopart, D, nb, sdo);
+  if (D == 128)
+    bwd_do8_kernel<128><<<g, kPreThreads, 0, st>>>(dob, N, sdo, do8t);
+  else
+    bwd_do8_kernel<64><<<g, kPreThreads, 0, st>>>(dob, N, sdo, do8t);
+  }
+  if (cudaGetLastError() != cudaSuccess) return 3;
+
+  CUtensorMap tk, tq, tv, tdo, tdo8;
+  if (!make_tmap_3d(&tk, w + QL.kc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, np, BH, 64, 128)) return 3;
+  if (!make_tmap_3d(&tq, w + QL.qc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, np, BH, 64, 128)) return 3;
+  if (!make_tmap_3d(&tv, V, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, N, BH, 64, 128)) return 3;
+  if (!make_tmap_3d(&tdo, dO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, N, BH, 64, 128)) return 3;
+  if (!make_tmap_3d(&tdo8, do8t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, np, D, BH, 128, D)) return 3;
+  BwdParams p;
+  p.N = N;
+  p.np = np;
+  p.nqb = nb;
+  p.causal = causal;
+  p.qk_norm = qk_norm;
+  p.alpha = (float)((double)sm_scale * 1.4426950408889634074);
+  p.sm_scale = sm_scale;
+  p.sq = reinterpret_cast<const float*>(w + QL.sq);
+  p.sk = reinterpret_cast<const float*>(w + QL.sk);
+  p.sdo = sdo;
+  p.lse2 = lse2;
+  p.dvec = dvec;
+  p.K = static_cast<const __nv_bfloat16*>(K);
+  p.kr = reinterpret_cast<const float*>(w + QL.kr);
+  p.dqacc = dqacc;
+  p.dK = static_cast<__nv_bfloat16*>(dK);
+  p.dV = static_cast<__nv_bfloat16*>(dV);
+  p.status = reinterpret_cast<int*>(const_cast<uint8_t*>(w) + QL.status);
+  int rc = D == 128 ? launch_main_t<128>(tk, tq, tv, tdo, tdo8, p, BH, st)
+                    : launch_main_t<64>(tk, tq, tv, tdo, tdo8, p, BH, st);
+  if (rc) return rc;
+  const float* qr = reinterpret_cast<const float*>(w + QL.qr);
+  auto* q = static_cast<const __nv_bfloat16*>(Q);
+  auto* dq = static_cast<__nv_bfloat16*>(dQ);
+  constexpr int rpp128 = kPreThreads / 16, rpp64 = kPreThreads / 8;
+  ScopedTimer timer("bwd_dq", st);
+  if (D == 128)
+    bwd_dq_kernel<128><<<dim3((N + rpp128 - 1) / rpp128, BH), kPreThreads, 0, st>>>(dqacc, q, qr, N, np, qk_norm,
+                                                                                      sm_scale, dq);
+  else
+    bwd_dq_kernel<64><<<dim3((N + rpp64 - 1) / rpp64, BH), kPreThreads, 0, st>>>(dqacc, q, qr, N, np, qk_norm,
+                                                                                   sm_scale, dq);
+  return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
+
+}  // namespace sage

@@ -1,0 +1,17 @@
+// Internal launchers (host side); each returns 0 or a sage_status code.
+#pragma once
+
+#include <cuda_runtime.h>
+
+namespace sage {
+
+int launch_quantize(const void* Q, const void* K, const void* V, int B, int H, int N, int D, int qk_norm,
+                    int k_smooth, void* ws, cudaStream_t st);
+int launch_fwd(const void* ws, void* O, float* LSE, float* O32, int B, int H, int N, int D, int causal,
+               float sm_scale, cudaStream_t st);
+int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO,
+               void* dQ, void* dK, void* dV, const void* ws, void* bwd_ws, int B, int H, int N, int D,
+               int causal, int qk_norm, int k_smooth, float sm_scale, cudaStream_t st);
+int launch_selftest_wait(void* ws, unsigned long long budget_ns, cudaStream_t st);
+
+}  // namespace sage

@@ -1,0 +1,68 @@
+// Workspace layouts (device memory owned by the caller, carved by the library).
+// Every section starts on a 256-byte boundary.  Np = N rounded up to 128.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+namespace sage {
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+inline int pad128(int n) { return (n + 127) / 128 * 128; }
+
+struct QuantWs {
+  // byte offsets
+  size_t status, qc, kc, v8t, sq, sk, sv, kmean, qr, kr, kpart, vpart, total;
+  int np;
+};
+
+// quantize workspace: codes and scales the forward and backward read, and the
+// per-128-token partial sums that the smoothing mean and the V scales come from
+inline QuantWs quant_ws_layout(int B, int H, int N, int D) {
+  QuantWs L{};
+  const size_t bh = (size_t)B * H;
+  const int np = pad128(N);
+  const size_t nb = np / 128;
+  size_t o = 0;
+  L.status = o; o = align256(o + 256);
+  L.qc = o;     o = align256(o + bh * np * D * 2);
+  L.kc = o;     o = align256(o + bh * np * D * 2);
+  L.v8t = o;    o = align256(o + bh * D * np);
+  L.sq = o;     o = align256(o + bh * nb * 4);
+  L.sk = o;     o = align256(o + bh * nb * 2 * 4);
+  L.sv = o;     o = align256(o + bh * D * 4);
+  L.kmean = o;  o = align256(o + bh * D * 4);
+  L.qr = o;     o = align256(o + bh * np * 4);
+  L.kr = o;     o = align256(o + bh * np * 4);
+  L.kpart = o;  o = align256(o + bh * nb * D * 8);  // fp64 partial column sums of k'
+  L.vpart = o;  o = align256(o + bh * nb * D * 4);  // partial channel max |V|
+  L.total = o;
+  L.np = np;
+  return L;
+}
+
+struct BwdWs {
+  size_t dvec, lse2, do8t, sdo, dopart, dqacc, total;
+  int np;
+};
+
+// backward scratch: D_i, LSE*log2(e) (+inf on padded rows), FP8 dO codes
+// (channel-major), their channel scales and partial maxima, fp32 dQ accumulator
+inline BwdWs bwd_ws_layout(int B, int H, int N, int D) {
+  BwdWs L{};
+  const size_t bh = (size_t)B * H;
+  const int np = pad128(N);
+  const size_t nb = np / 128;
+  size_t o = 0;
+  L.dvec = o;   o = align256(o + bh * np * 4);
+  L.lse2 = o;   o = align256(o + bh * np * 4);
+  L.do8t = o;   o = align256(o + bh * D * np);
+  L.sdo = o;    o = align256(o + bh * D * 4);
+  L.dopart = o; o = align256(o + bh * nb * D * 4);
+  L.dqacc = o;  o = align256(o + bh * np * D * 4);
+  L.total = o;
+  L.np = np;
+  return L;
+}
+
+}  // namespace sage

@@ -1,0 +1,165 @@
+/*
+ * sage_attn.h -- C ABI of the GB300 (sm_103a) low-bit attention library:
+ * the SageBwd scheme's quantize pass, forward and backward for training.
+ *
+ * What the calls compute
+ * ----------------------
+ * "SageBwd: A Trainable Low-bit Attention" (euno.news summary), Methodology 1-2:
+ * six of the seven matmuls of an attention block run in low precision -- QK^T and
+ * PV in the forward, the S recompute, dV, dQ and dK in the backward -- while the
+ * softmax-gradient matmul dP = dO V^T stays in high precision (bf16 here).
+ * Methodology 4 and Results: QK-norm (each query and key scaled to unit L2 norm
+ * before the dot product) and K-smoothing (read here as subtracting the per-head
+ * channel mean of K over tokens, which leaves the softmax unchanged).
+ * "Attn-QAT: 4-Bit Attention With Quantization-Aware Training" (gist.science
+ * summary), Methodology, principle 1: the backward recomputes P from the saved
+ * log-sum-exp in the forward's low precision.  "ThriftAttention" (gist.science
+ * summary), Methodology step 2: the FlashAttention-2 online softmax over key tiles.
+ *
+ * Number formats (the pages give no formulas; these are the plainest reading):
+ *   Q: INT8, one fp32 scale max|q'|/127 per 128-token block (all channels);
+ *   K: INT8, one fp32 scale max|k''|/127 per 64-token block;
+ *   V, dO: FP8 e4m3, one fp32 scale max|x|/448 per (head, channel);
+ *   P: FP8 e4m3 with the static scale 1/448 (probabilities relative to the
+ *      running row maximum are at most 1);
+ *   dS: INT8, one scale max|dS|/127 per (128-query x 64-key) tile.
+ * INT8 products accumulate exactly (the codes sit in bf16 containers and every
+ * partial sum is an integer below 2^24, exact in the fp32 accumulator).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Tensors Q, K, V, O, dO, dQ, dK, dV: bf16, contiguous [B, H, N, D] (D fastest),
+ *    device memory owned by the caller, 16-byte aligned.  LSE: fp32 [B, H, N],
+ *    natural log.  O32 (optional): fp32 [B, H, N, D].
+ *  - Supported shapes: B, H >= 1; N >= 1 (any value; tiles are padded internally);
+ *    D in {64, 128}; queries and keys share N.  Other shapes: SAGE_ERR_UNSUPPORTED.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call is
+ *    asynchronous on that stream, allocates nothing and never synchronises,
+ *    except sage_attn_get_status.
+ *  - Argument errors are returned synchronously before anything is launched.
+ *  - Workspaces are device memory the caller allocates with at least the size the
+ *    *_ws_bytes call reports; their contents are owned by the library between
+ *    sage_attn_quantize and the last forward/backward that reads them.
+ *  - Every device-side wait is bounded; a wait that runs out records
+ *    SAGE_ERR_TIMEOUT in the workspace status word (read with
+ *    sage_attn_get_status) and the kernel returns.
+ *  - The forward is deterministic.  dQ is accumulated with fp32 atomics across
+ *    key blocks, so its last bits depend on the order of those atomics.
+ */
+#ifndef SAGE_ATTN_H
+#define SAGE_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SAGE_OK = 0,
+  SAGE_ERR_INVALID_ARG = 1, /* null or misaligned pointer, bad size, workspace too small */
+  SAGE_ERR_UNSUPPORTED = 2, /* shape outside the supported set */
+  SAGE_ERR_CUDA = 3,        /* a CUDA runtime call failed (launch, attribute, tensor map) */
+  SAGE_ERR_TIMEOUT = 4      /* a device-side wait ran out of its time budget */
+} sage_status;
+
+/* Pointers into a quantize workspace (for inspection and parity tests).
+ * Np = N rounded up to a multiple of 128; rows past N hold zero codes. */
+typedef struct sage_ws_views {
+  void *qc;      /* bf16 [B*H, Np, D]: INT8 codes of q' (bf16 containers)           */
+  void *kc;      /* bf16 [B*H, Np, D]: INT8 codes of k'' (smoothed, bf16 containers) */
+  void *v8t;     /* e4m3 [B*H, D, Np]: FP8 codes of V, channel-major                 */
+  float *sq;     /* [B*H, Np/128] Q block scales                                     */
+  float *sk;     /* [B*H, Np/64]  K block scales                                     */
+  float *sv;     /* [B*H, D]      V channel scales                                   */
+  float *kmean;  /* [B*H, D]      channel mean of k' (0 without K-smoothing)         */
+  float *qr;     /* [B*H, Np]     1/||q|| per token (1 without QK-norm)              */
+  float *kr;     /* [B*H, Np]     1/||k|| per token (1 without QK-norm)              */
+  int *status;   /* device status word                                               */
+  int n_pad;     /* Np                                                               */
+} sage_ws_views;
+
+/* Bytes of the quantize workspace for this shape (0 if unsupported). It holds the
+ * codes and scales the forward and backward read, plus the status word. */
+size_t sage_attn_ws_bytes(int B, int H, int N, int D);
+
+/* Bytes of the backward scratch for this shape (0 if unsupported): the row terms
+ * D_i = rowsum(dO * O) and LSE*log2(e), the FP8 codes of dO, and the fp32 dQ
+ * accumulator. */
+size_t sage_attn_bwd_ws_bytes(int B, int H, int N, int D);
+
+/*
+ * Quantize pass (SageBwd summary, Methodology 1 and 4).
+ * Reads Q, K, V; optionally L2-normalises q and k per token (qk_norm != 0);
+ * optionally subtracts the per-(b,h) channel mean of k over the N tokens
+ * (k_smooth != 0); writes the INT8 codes and scales of q' and k'' and the FP8
+ * codes and scales of V into `ws`, and clears the status word.
+ * Rounding: every scale and quotient is a correctly rounded fp32 operation;
+ * codes round half to even; the norms and means are the fp32 rounding of the
+ * exact sums.
+ */
+int sage_attn_quantize(const void *Q, const void *K, const void *V, int B, int H, int N, int D,
+                       int qk_norm, int k_smooth, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Forward (SageBwd summary, Methodology 1; ThriftAttention summary, Methodology 2).
+ * S = (q8 k8^T) * sq * sk * sm_scale computed exactly in integers and scaled in
+ * fp32; causal (causal != 0) masks keys j > i; online softmax over 128-key tiles
+ * with the running maximum; P = 2^(S*log2e - m) rounded to e4m3 after scaling by
+ * 448; O = (P8 V8) * sv / (448 l).  Writes O (bf16), LSE (fp32, natural log) and,
+ * if O32 is not NULL, O in fp32 before the bf16 rounding.
+ * sm_scale <= 0 selects 1/sqrt(D).  `ws` comes from sage_attn_quantize with the
+ * same B, H, N, D.
+ */
+int sage_attn_fwd(const void *ws, void *O, float *LSE, float *O32, int B, int H, int N, int D,
+                  int causal, float sm_scale, void *stream);
+
+/*
+ * Backward (SageBwd summary, Methodology 2; Attn-QAT summary, principle 1).
+ * D_i = sum_d dO*O; P recomputed from LSE and rounded to e4m3 exactly as in the
+ * forward; dP = dO V^T in bf16 with fp32 accumulation (the one unquantized
+ * matmul); dS = P (dP - D_i); dV = P8^T dO8 (FP8); dS to INT8 per 128x64 tile;
+ * dQ = dS8 k8 and dK = dS8^T q8 (exact integer sums, scaled per tile); then
+ * dQ, dK times sm_scale and back through QK-norm when qk_norm != 0.  K-smoothing
+ * passes dK through unchanged (the exact dS rows sum to zero).
+ * Q, K, V, dO are the same inputs the forward saw; O and LSE the forward's outputs;
+ * `ws` the quantize workspace; `bwd_ws` scratch of sage_attn_bwd_ws_bytes.
+ * Writes dQ, dK, dV (bf16).
+ */
+int sage_attn_bwd(const void *Q, const void *K, const void *V, const void *O, const float *LSE,
+                  const void *dO, void *dQ, void *dK, void *dV, const void *ws, void *bwd_ws,
+                  size_t bwd_ws_bytes, int B, int H, int N, int D, int causal, int qk_norm,
+                  int k_smooth, float sm_scale, void *stream);
+
+/* Fill `views` with the device pointers inside a quantize workspace. */
+int sage_attn_ws_views(void *ws, int B, int H, int N, int D, sage_ws_views *views);
+
+/* Synchronise `stream`, read and clear the workspace status word.  Returns SAGE_OK
+ * or SAGE_ERR_TIMEOUT (or SAGE_ERR_CUDA if the read itself failed). */
+int sage_attn_get_status(void *ws, void *stream);
+
+/* Self-test of the bounded wait: launches one CTA that waits on a barrier nothing
+ * arrives at, with a budget of `budget_ns` nanoseconds (capped at 1 s); the kernel
+ * gives up, records SAGE_ERR_TIMEOUT in the status word of `ws` and returns. */
+int sage_attn_selftest_wait(void *ws, unsigned long long budget_ns, void *stream);
+
+/* Kernel timing for benchmarks.  While enabled (on != 0) the library brackets
+ * each launch group with CUDA events recorded on the launching stream: "quantize"
+ * (the three quantize kernels), "fwd", "bwd_pre" (D_i, LSE*log2e, dO codes),
+ * "bwd_main" and "bwd_dq".  Costs two event records per group; off by default. */
+int sage_attn_timer_enable(int on);
+
+/* Synchronise the events recorded for `kernel` since the last read, store their
+ * summed duration (ms) and number of launches, and forget them.  Unknown names
+ * give zero. */
+int sage_attn_timer_read(const char *kernel, double *total_ms, int *launches);
+
+/* Static description of a status code. */
+const char *sage_attn_status_str(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SAGE_ATTN_H */

@@ -208,16 +208,18 @@ int sage_oracle_quantize(int N, int D, const double *Q, const double *K, const d
     return 0;
 }
 
-/* log2-domain logit of query i against key j: (sum_d qx*kx) * c, with
- * c = RN(RN(sq_I * sk_J) * alpha), alpha = RN(sm_scale * log2 e).  With INT8
- * codes every product and partial sum is an integer below 2^53, so the fp64
- * sum is the exact integer dot product. */
-static inline double logit2(const double *qrow, const double *krow, int D, double c, int f32)
+/* sum_d qx*kx.  With INT8 codes every product and partial sum is an integer
+ * below 2^53, so this fp64 sum is the exact integer dot product. */
+static inline double dot(const double *qrow, const double *krow, int D)
 {
     double acc = 0.0;
     for (int d = 0; d < D; ++d) acc += qrow[d] * krow[d];
-    return r32(f32, acc * c);
+    return acc;
 }
+
+/* The dequantization factor of a (query block, key block) pair is
+ * c = RN(RN(sq_I * sk_J) * alpha), alpha = RN(sm_scale * log2 e): the
+ * log2-domain logit is acc * c. */
 
 static inline double qk_factor(double sqI, double skJ, double alpha, int f32)
 {
@@ -226,9 +228,13 @@ static inline double qk_factor(double sqI, double skJ, double alpha, int f32)
 
 /*
  * Forward for one head: online softmax over ascending 128-key tiles.
- * Per row and tile: m' = max(m, max_j S2_ij); p~ = RN32(2^(S2 - m')) (fp64
- * exp2); p8 = e4m3(RN32(448 p~)); l = l 2^(m - m') + sum p~;
- * A = A 2^(m - m') + sum p8 v8.  Finish: O = A sv / (448 l), LSE = ln2 (m + log2 l).
+ * Per row and tile, with acc_ij the integer dot product and c the tile's
+ * dequantization factor (S2 = acc c, log2 units):
+ *   m' = max(m, max_j RN32(acc_ij c));
+ *   t = RN32(acc_ij c - m')  (one rounding of the exact value);
+ *   p~ = RN32(2^t) (fp64 exp2);  p8 = e4m3(RN32(448 p~));
+ *   l = l 2^(m - m') + sum p~;  A = A 2^(m - m') + sum p8 v8.
+ * Finish: O = A sv / (448 l), LSE = ln2 (m + log2 l).
  * Outputs O64 [N, D], O32 [N, D] (float), LSE64 [N].
  */
 int sage_oracle_fwd(int N, int D, int causal, double sm_scale, int qmask,
@@ -244,7 +250,7 @@ int sage_oracle_fwd(int N, int D, int causal, double sm_scale, int qmask,
 #pragma omp parallel
     {
         double *A = (double *)malloc(sizeof(double) * D);
-        double *s2 = (double *)malloc(sizeof(double) * TILE);
+        double *s2 = (double *)malloc(sizeof(double) * 2 * TILE);  /* acc, c per key */
         if (!A || !s2) {
 #pragma omp atomic write
             err = 2;
@@ -260,17 +266,20 @@ int sage_oracle_fwd(int N, int D, int causal, double sm_scale, int qmask,
                 if (causal && j1 > i + 1) j1 = i + 1;
                 if (j1 <= j0) break;
                 double mt = -INFINITY;
+                double *acc = s2, *cj = s2 + TILE;
                 for (int j = j0; j < j1; ++j) {
                     double c = qk_factor(sq[i / QBLK], sk[j / KBLK], alpha, f32);
-                    s2[j - j0] = logit2(qrow, kx + (size_t)j * D, D, c, f32);
-                    mt = fmax(mt, s2[j - j0]);
+                    acc[j - j0] = dot(qrow, kx + (size_t)j * D, D);
+                    cj[j - j0] = c;
+                    mt = fmax(mt, r32(f32, acc[j - j0] * c));
                 }
                 double mn = fmax(m, mt);
                 double corr = (m == -INFINITY) ? 0.0 : exp2(m - mn);
                 l *= corr;
                 for (int d = 0; d < D; ++d) A[d] *= corr;
                 for (int j = j0; j < j1; ++j) {
-                    double pt = r32(f32, exp2(s2[j - j0] - mn));
+                    double t = r32(f32, acc[j - j0] * cj[j - j0] - mn);
+                    double pt = r32(f32, exp2(t));
                     double p8 = qp ? sage_oracle_e4m3(r32(f32, 448.0 * pt)) : 448.0 * pt;
                     l += pt;
                     const double *vrow = vx + (size_t)j * D;
@@ -292,7 +301,7 @@ int sage_oracle_fwd(int N, int D, int causal, double sm_scale, int qmask,
 }
 
 /* One (128-query block I, 64-key block J) tile of the backward.
- * P = RN32(2^(S2 - RN32(LSE log2 e))), p8 = e4m3(RN32(448 P)), P^ = p8 / 448,
+ * P = RN32(2^RN32(acc c - RN32(LSE log2 e))), p8 = e4m3(RN32(448 P)), P^ = p8 / 448,
  * dP = dO V^T (fp64, unquantized), dS = RN32(P^ (dP - Dvec)),
  * dS8 = INT8 of dS with one scale max|dS|/127 for the tile.
  * p8t/ds8t are [QBLK][KBLK]; returns the tile's dS scale. */
@@ -311,8 +320,8 @@ static double bwd_tile(int I, int J, int N, int D, int causal, double alpha, int
             double *pp = p8t + (size_t)(i - i0) * KBLK + (j - j0);
             double *dd = ds8t + (size_t)(i - i0) * KBLK + (j - j0);
             if (causal && j > i) { *pp = 0.0; *dd = 0.0; continue; }
-            double s2 = logit2(qx + (size_t)i * D, kx + (size_t)j * D, D, c, f32);
-            double P = r32(f32, exp2(s2 - lse2[i]));
+            double acc = dot(qx + (size_t)i * D, kx + (size_t)j * D, D);
+            double P = r32(f32, exp2(r32(f32, acc * c - lse2[i])));
             double p8 = (qmask & QM_P) ? sage_oracle_e4m3(r32(f32, 448.0 * P)) : 448.0 * P;
             double dp = 0.0;
             for (int d = 0; d < D; ++d) dp += dO[(size_t)i * D + d] * V[(size_t)j * D + d];

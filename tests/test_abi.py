@@ -1,0 +1,76 @@
+"""The C ABI library loads without a GPU, exports every function include/sage_attn.h
+declares, sizes its workspaces, and rejects bad arguments before launching."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import bit_trainable_attention_sagebwd_gb300 as sa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bit_trainable_attention_sagebwd_gb300 import build
+    build.build()
+    return sa.lib()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "sage_attn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sage_attn_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_function(lib):
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), f"{n} not exported"
+    assert set(names) == set(sa.ABI_FUNCTIONS)
+
+
+def test_workspace_sizes(lib):
+    for (B, H, N, D) in [(1, 2, 256, 64), (4, 16, 2048, 128), (1, 32, 32768, 128), (1, 1, 1, 64), (2, 3, 333, 128)]:
+        n = sa.sage_attn_ws_bytes(B, H, N, D)
+        np_ = (N + 127) // 128 * 128
+        # at least the codes: two bf16 containers and one e4m3 tensor
+        assert n >= B * H * np_ * D * 5
+        assert n % 256 == 0
+        assert sa.sage_attn_bwd_ws_bytes(B, H, N, D) >= B * H * np_ * D * 5
+    for bad in [(1, 1, 128, 96), (0, 1, 128, 64), (1, 1, 0, 64), (1, 1, 128, 256)]:
+        assert sa.sage_attn_ws_bytes(*bad) == 0
+        assert sa.sage_attn_bwd_ws_bytes(*bad) == 0
+
+
+def test_argument_errors_return_before_launch(lib):
+    null = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(0x10000)  # aligned, never dereferenced: the checks fail first
+    odd = ctypes.c_void_p(0x10001)
+    assert sa.sage_attn_quantize(null, fake, fake, 1, 1, 128, 64, 0, 1, fake, 1 << 30, null) == sa.SAGE_ERR_INVALID_ARG
+    assert sa.sage_attn_quantize(odd, fake, fake, 1, 1, 128, 64, 0, 1, fake, 1 << 30, null) == sa.SAGE_ERR_INVALID_ARG
+    assert sa.sage_attn_quantize(fake, fake, fake, 1, 1, 128, 96, 0, 1, fake, 1 << 30, null) == sa.SAGE_ERR_UNSUPPORTED
+    assert sa.sage_attn_quantize(fake, fake, fake, 1, 1, 128, 64, 0, 1, fake, 16, null) == sa.SAGE_ERR_INVALID_ARG
+    assert sa.sage_attn_fwd(fake, fake, null, null, 1, 1, 128, 64, 1, 0.125, null) == sa.SAGE_ERR_INVALID_ARG
+    assert sa.sage_attn_fwd(fake, fake, fake, odd, 1, 1, 128, 64, 1, 0.125, null) == sa.SAGE_ERR_INVALID_ARG
+    assert sa.sage_attn_fwd(fake, fake, fake, null, 1, 1, 128, 64, 1, float("nan"), null) == sa.SAGE_ERR_INVALID_ARG
+    assert sa.sage_attn_fwd(fake, fake, fake, null, 1, 1, 128, 80, 1, 0.125, null) == sa.SAGE_ERR_UNSUPPORTED
+    args = [fake] * 11
+    assert sa.sage_attn_bwd(*args[:10], fake, 16, 1, 1, 128, 64, 1, 0, 1, 0.125, null) == sa.SAGE_ERR_INVALID_ARG
+    a2 = list(args)
+    a2[6] = odd
+    assert sa.sage_attn_bwd(*a2[:10], fake, 1 << 40, 1, 1, 128, 64, 1, 0, 1, 0.125, null) == sa.SAGE_ERR_INVALID_ARG
+    with pytest.raises(sa.SageError):
+        sa.sage_attn_ws_views(fake, 1, 1, 128, 96)
+    assert sa.status_str(sa.SAGE_ERR_TIMEOUT) == "device wait timed out"
+
+
+def test_ws_views_offsets(lib):
+    base = 1 << 20
+    v = sa.sage_attn_ws_views(ctypes.c_void_p(base), 2, 3, 333, 128)
+    assert v.n_pad == 384
+    ptrs = [v.status, v.qc, v.kc, v.v8t, v.sq, v.sk, v.sv, v.kmean, v.qr, v.kr]
+    assert ptrs == sorted(ptrs) and all((p - base) % 256 == 0 for p in ptrs)
+    assert v.kc - v.qc >= 6 * 384 * 128 * 2

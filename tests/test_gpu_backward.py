@@ -1,0 +1,44 @@
+"""Backward parity of the CUDA path (through the C ABI) against the CPU oracle:
+relative L2 error of dQ, dK, dV at most 1e-2 per head (the stated tolerance),
+plus the forward checks on the same run."""
+import pytest
+
+from bit_trainable_attention_sagebwd_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [
+    wl.custom(1, 2, 333, 64, True, seed=20, kind="k_offset2", name="n333_d64_causal"),
+    wl.custom(1, 2, 700, 128, True, qk_norm=True, sm_scale=16.0, seed=21, name="n700_d128_causal_qknorm"),
+    wl.custom(2, 1, 250, 128, False, seed=22, kind="k_outlier20", name="n250_d128_outliers"),
+    wl.custom(1, 1, 1, 64, False, seed=23, name="n1_d64"),
+    wl.custom(1, 1, 64, 128, True, seed=24, name="n64_d128_causal"),
+    wl.custom(1, 1, 512, 64, False, qk_norm=True, sm_scale=8.0, seed=25, kind="k_offset3", name="n512_d64_qknorm"),
+    wl.custom(1, 2, 640, 128, True, seed=26, kind="student_t3", name="n640_d128_student"),
+    wl.custom(1, 1, 129, 128, False, k_smooth=False, seed=27, name="n129_d128_nosmooth"),
+]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=[w.name for w in SMALL])
+def test_backward_small(w):
+    import parity
+    x = wl.all_inputs(w)
+    g = parity.run_gpu(w, x, backward=True)
+    for bh in range(w.bh):
+        r = parity.oracle_head(w, x, bh, backward=True)
+        parity.check_forward_head(w, g, bh, r)
+        parity.check_backward_head(w, g, bh, r)
+
+
+@pytest.mark.parametrize("name", list(wl.WORKLOADS))
+def test_backward_full_size(name):
+    """Full-size workloads in the bench's launch configuration; the oracle computes
+    one head (two for the small workload)."""
+    import parity
+    w = wl.WORKLOADS[name]
+    x = wl.all_inputs(w)
+    g = parity.run_gpu(w, x, backward=True)
+    heads = range(w.bh) if w.bh <= 4 else [w.bh - 1]
+    for bh in heads:
+        r = parity.oracle_head(w, x, bh, backward=True)
+        parity.check_backward_head(w, g, bh, r)

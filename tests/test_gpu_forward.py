@@ -1,0 +1,46 @@
+"""Quantize + forward parity of the CUDA path (through the C ABI) against the CPU oracle.
+
+Codes and scales must match bit for bit; O32 within 2e-3 max abs error; LSE
+within 1e-4 (relative to max(1, |LSE|)); bf16 O must be the rounding of O32."""
+import pytest
+
+from bit_trainable_attention_sagebwd_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [
+    wl.custom(1, 2, 333, 64, True, seed=10, kind="k_offset2", name="n333_d64_causal"),
+    wl.custom(1, 2, 700, 128, True, qk_norm=True, sm_scale=16.0, seed=11, name="n700_d128_causal_qknorm"),
+    wl.custom(2, 1, 250, 128, False, seed=12, kind="k_outlier20", name="n250_d128_outliers"),
+    wl.custom(1, 1, 1, 64, False, seed=13, name="n1_d64"),
+    wl.custom(1, 1, 64, 128, True, seed=14, name="n64_d128_causal"),
+    wl.custom(1, 1, 512, 64, False, seed=15, kind="k_offset3", name="n512_d64_offset3"),
+    wl.custom(1, 2, 640, 128, True, seed=16, kind="student_t3", name="n640_d128_student"),
+    wl.custom(1, 1, 129, 128, False, k_smooth=False, seed=17, name="n129_d128_nosmooth"),
+]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=[w.name for w in SMALL])
+def test_quantize_forward_small(w):
+    import parity
+    x = wl.all_inputs(w)
+    g = parity.run_gpu(w, x, backward=False)
+    for bh in range(w.bh):
+        r = parity.oracle_head(w, x, bh, backward=False)
+        parity.check_quantize_head(w, g, bh, r)
+        parity.check_forward_head(w, g, bh, r)
+
+
+@pytest.mark.parametrize("name", list(wl.WORKLOADS))
+def test_quantize_forward_full_size(name):
+    """Full-size workloads in the bench's launch configuration; the oracle computes
+    the first and last head (every head for the small one)."""
+    import parity
+    w = wl.WORKLOADS[name]
+    x = wl.all_inputs(w)
+    g = parity.run_gpu(w, x, backward=False)
+    heads = range(w.bh) if w.bh <= 4 else [0, w.bh - 1]
+    for bh in heads:
+        r = parity.oracle_head(w, x, bh, backward=False)
+        parity.check_quantize_head(w, g, bh, r)
+        parity.check_forward_head(w, g, bh, r)
