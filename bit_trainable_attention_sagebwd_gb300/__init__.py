@@ -23,7 +23,8 @@ SAGE_OK, SAGE_ERR_INVALID_ARG, SAGE_ERR_UNSUPPORTED, SAGE_ERR_CUDA, SAGE_ERR_TIM
 # names declared in include/sage_attn.h
 ABI_FUNCTIONS = ("sage_attn_ws_bytes", "sage_attn_bwd_ws_bytes", "sage_attn_quantize", "sage_attn_fwd",
                  "sage_attn_bwd", "sage_attn_ws_views", "sage_attn_get_status", "sage_attn_selftest_wait",
-                 "sage_attn_status_str", "sage_attn_timer_enable", "sage_attn_timer_read")
+                 "sage_attn_status_str", "sage_attn_timer_enable", "sage_attn_timer_read",
+                 "sage_attn_bwd_noalloc")
 
 
 class SageError(RuntimeError):
@@ -62,6 +63,7 @@ def lib():
             L.sage_attn_ws_views.argtypes = [vp, i, i, i, i, ctypes.POINTER(sage_ws_views)]
             L.sage_attn_get_status.argtypes = [vp, vp]
             L.sage_attn_selftest_wait.argtypes = [vp, u64, vp]
+            L.sage_attn_bwd_noalloc.argtypes = [vp] * 10 + [i] * 7 + [fp, vp]
             L.sage_attn_timer_enable.argtypes = [i]
             L.sage_attn_timer_read.argtypes = [ctypes.c_char_p, ctypes.POINTER(ctypes.c_double),
                                                ctypes.POINTER(ctypes.c_int)]
@@ -93,6 +95,12 @@ def sage_attn_bwd(Q, K, V, O, LSE, dO, dQ, dK, dV, ws, bwd_ws, bwd_ws_bytes, B, 
                   k_smooth, sm_scale, stream):
     return lib().sage_attn_bwd(Q, K, V, O, LSE, dO, dQ, dK, dV, ws, bwd_ws, bwd_ws_bytes, B, H, N, D,
                                int(causal), int(qk_norm), int(k_smooth), float(sm_scale), stream)
+
+
+def sage_attn_bwd_noalloc(Q, K, V, O, LSE, dO, dQ, dK, dV, ws, B, H, N, D, causal, qk_norm, k_smooth, sm_scale,
+                          stream):
+    return lib().sage_attn_bwd_noalloc(Q, K, V, O, LSE, dO, dQ, dK, dV, ws, B, H, N, D, int(causal),
+                                       int(qk_norm), int(k_smooth), float(sm_scale), stream)
 
 
 def sage_attn_ws_views(ws, B, H, N, D) -> sage_ws_views:

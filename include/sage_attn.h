@@ -144,6 +144,33 @@ int sage_attn_get_status(void *ws, void *stream);
  * gives up, records SAGE_ERR_TIMEOUT in the status word of `ws` and returns. */
 int sage_attn_selftest_wait(void *ws, unsigned long long budget_ns, void *stream);
 
+/* Size of the library-owned scratch array used by sage_attn_bwd_noalloc. */
+#define SAGE_ATTN_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * Backward without a caller-supplied scratch buffer.  The pages have no
+ * counterpart to this call; it exists for callers that cannot allocate device
+ * memory: code running while a CUDA graph is being captured (where a fresh
+ * allocation is not allowed), hosts whose memory pool owns every device byte and
+ * forbids allocations from extensions, and real-time or embedded deployments
+ * that allocate nothing after start-up.  They still pass the inputs, outputs and
+ * the quantize workspace, exactly as for sage_attn_bwd, and get the same result.
+ *
+ * The scratch is one fixed array of SAGE_ATTN_NOALLOC_SCRATCH_BYTES inside the
+ * library; every GPU that loads the library holds it until the process exits.
+ * Shapes whose scratch (sage_attn_bwd_ws_bytes) exceeds it are rejected with
+ * SAGE_ERR_UNSUPPORTED before anything is launched.  The call allocates nothing.
+ * Its first call on a device looks up the array's device address with that
+ * device current; make that first call before any stream capture.
+ * Every call shares the one array and each call clears what must start at zero,
+ * so calls are independent in sequence, but calls that overlap on the GPU (on
+ * different streams, or from several threads) race on the array.
+ */
+int sage_attn_bwd_noalloc(const void *Q, const void *K, const void *V, const void *O, const float *LSE,
+                          const void *dO, void *dQ, void *dK, void *dV, const void *ws, int B, int H,
+                          int N, int D, int causal, int qk_norm, int k_smooth, float sm_scale,
+                          void *stream);
+
 /* Kernel timing for benchmarks.  While enabled (on != 0) the library brackets
  * each launch group with CUDA events recorded on the launching stream: "quantize"
  * (the three quantize kernels), "fwd", "bwd_pre" (D_i, LSE*log2e, dO codes),
