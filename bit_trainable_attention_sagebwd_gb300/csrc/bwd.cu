@@ -161,17 +161,17 @@ template <int D>
 struct BwdSmem {
   uint8_t k[128 * D * 2];    // K codes of this key block (resident)
   uint8_t v[128 * D * 2];    // V bf16 of this key block (resident)
-  uint8_t q[128 * D * 2];    // Q codes of the current query block
+  uint8_t q[2][128 * D * 2]; // Q codes of the current and next query blocks
   uint8_t dob[128 * D * 2];  // dO bf16 of the current query block
   uint8_t do8[D * 128];      // dO e4m3 codes, channel-major
   uint8_t p[128 * 128];      // P^T e4m3, key rows
   uint8_t ds[128 * 128 * 2]; // dS^T INT8 codes in bf16, key rows
-  float bias[128];           // log2(448) - LSE2_i of the current query block
-  float dvec[128];
-  float smax[4];
+  __align__(16) float bias[128];  // log2(448) - LSE2_i of the current query block
+  __align__(16) float dvec[128];
+  float smax[8];
   uint64_t bar_kv;
-  uint64_t bar_q_full, bar_do_full, bar_do8_full;
-  uint64_t bar_q_free, bar_do_free, bar_do8_free;
+  uint64_t bar_q_full[2], bar_do_full, bar_do8_full;
+  uint64_t bar_q_free[2], bar_do_free, bar_do8_free;
   uint64_t bar_sdp, bar_p, bar_ds, bar_part, bar_free;
   uint32_t tmem_base;
   int abort;
@@ -193,10 +193,20 @@ struct BwdParams {
   int* status;
 };
 
-__device__ __forceinline__ void named_bar_compute() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// the 256 threads of the two compute warpgroups
+__device__ __forceinline__ void named_bar_compute() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23: x + M - M rounds x to an integer (ties to even)
+
+// One CTA per (head, 128-key block), looping over the query blocks that see it.
+//   warps 0-3, 4-7 : compute warpgroups g = 0, 1; thread t of a group owns key row t
+//                    (TMEM lane t) and query columns [64g, 64g + 64) of it, and D/2
+//                    of the dK/dQ/dV columns
+//   warp 8 lane 0  : TMA producer;  warp 9 : TMEM allocator, lane 0 issues the UMMAs
+// TMEM columns: [0,128) S^T, then dK_part; [128,256) dP^T, then dS, then dQ half 0;
+// [256,256+D) dV; [384,384+D) dQ half 1.
 template <int D>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_do8, const BwdParams prm) {
@@ -209,24 +219,27 @@ __global__ void __launch_bounds__(256, 1)
   constexpr uint32_t kCols = 512;
   constexpr uint32_t cS = 0, cDP = 128, cDV = 256, cDQB = 384;  // TMEM column bases
   constexpr uint32_t kTile = 128 * D * 2;
+  constexpr int DH = D / 2;  // dK/dQ/dV columns per compute warpgroup
 
   if (tid == 0) {
     mbar_init(&sm.bar_kv, 1);
-    mbar_init(&sm.bar_q_full, 1);
+    mbar_init(&sm.bar_q_full[0], 1);
+    mbar_init(&sm.bar_q_full[1], 1);
     mbar_init(&sm.bar_do_full, 1);
     mbar_init(&sm.bar_do8_full, 1);
-    mbar_init(&sm.bar_q_free, 1);
+    mbar_init(&sm.bar_q_free[0], 1);
+    mbar_init(&sm.bar_q_free[1], 1);
     mbar_init(&sm.bar_do_free, 1);
     mbar_init(&sm.bar_do8_free, 1);
     mbar_init(&sm.bar_sdp, 1);
-    mbar_init(&sm.bar_p, 128);
-    mbar_init(&sm.bar_ds, 128);
+    mbar_init(&sm.bar_p, 256);
+    mbar_init(&sm.bar_ds, 256);
     mbar_init(&sm.bar_part, 1);
-    mbar_init(&sm.bar_free, 128);
+    mbar_init(&sm.bar_free, 256);
     sm.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == 9) {
     tmem_alloc(&sm.tmem_base, kCols);
     tmem_relinquish();
   }
@@ -235,7 +248,7 @@ __global__ void __launch_bounds__(256, 1)
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort = &sm.abort;
 
-  if (warp == 0 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     // ---------------- producer
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_q);
@@ -254,26 +267,29 @@ __global__ void __launch_bounds__(256, 1)
       mbar_arrive_expect_tx(&sm.bar_do_full, kTile);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) tma_load_3d(sm.dob + c * 16384, &tm_do, c * 64, I * 128, bh, &sm.bar_do_full);
-      if (it > 0 && !mbar_wait(&sm.bar_q_free, (it - 1) & 1, abort)) break;
-      mbar_arrive_expect_tx(&sm.bar_q_full, kTile);
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) tma_load_3d(sm.q + c * 16384, &tm_q, c * 64, I * 128, bh, &sm.bar_q_full);
       if (it > 0 && !mbar_wait(&sm.bar_do8_free, (it - 1) & 1, abort)) break;
       mbar_arrive_expect_tx(&sm.bar_do8_full, D * 128);
       tma_load_3d(sm.do8, &tm_do8, I * 128, 0, bh, &sm.bar_do8_full);
+      const int qs = it & 1;
+      if (it > 1 && !mbar_wait(&sm.bar_q_free[qs], ((it >> 1) - 1) & 1, abort)) break;
+      mbar_arrive_expect_tx(&sm.bar_q_full[qs], kTile);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c)
+        tma_load_3d(sm.q[qs] + c * 16384, &tm_q, c * 64, I * 128, bh, &sm.bar_q_full[qs]);
     }
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 9 && lane == 0) {
     // ---------------- UMMA issuer
     constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);   // S^T, dP^T
     constexpr uint32_t id_dv = idesc_e4m3(128, D);                   // dV
     constexpr uint32_t id_dk = idesc_bf16(128, D, false, true);      // dK: A K-major, B MN-major
     constexpr uint32_t id_dq = idesc_bf16(128, D, true, true);       // dQ: A, B MN-major
-    const uint32_t a_k = smem_u32(sm.k), a_v = smem_u32(sm.v), a_q = smem_u32(sm.q), a_do = smem_u32(sm.dob);
+    const uint32_t a_k = smem_u32(sm.k), a_v = smem_u32(sm.v), a_do = smem_u32(sm.dob);
     const uint32_t a_do8 = smem_u32(sm.do8), a_p = smem_u32(sm.p), a_ds = smem_u32(sm.ds);
     bool ok = mbar_wait(&sm.bar_kv, 0, abort);
     for (int it = 0; ok && it < n_it; ++it) {
       const uint32_t ph = it & 1;
-      if (!mbar_wait(&sm.bar_q_full, ph, abort) || !mbar_wait(&sm.bar_do_full, ph, abort)) break;
+      const uint32_t a_q = smem_u32(sm.q[it & 1]);
+      if (!mbar_wait(&sm.bar_q_full[it & 1], (it >> 1) & 1, abort) || !mbar_wait(&sm.bar_do_full, ph, abort)) break;
       if (it > 0 && !mbar_wait(&sm.bar_free, (it - 1) & 1, abort)) break;
       tc_fence_after();
 #pragma unroll
@@ -314,26 +330,31 @@ __global__ void __launch_bounds__(256, 1)
         umma_bf16(tmem + cDQB, sdesc_sw128(a_ds + kk * 2048, 16384, 1024),
                   sdesc_sw128(a_k + kk * 2048, 16384, 1024), id_dq, kk > 4);
       umma_commit(&sm.bar_part);
-      umma_commit(&sm.bar_q_free);
+      umma_commit(&sm.bar_q_free[it & 1]);
     }
-  } else if (warp >= 4) {
-    // ---------------- compute: thread t owns key row t (TMEM lane t)
-    const int t = tid - 128;
+  } else if (warp < 8) {
+    // ---------------- compute: warpgroup g, thread t owns key row t
+    const int g = warp >> 2;
+    const int t = tid & 127;
     const int key = kb * 128 + t;
     const bool key_ok = key < prm.N;
-    const int half = t >> 6;
-    const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
+    const int half = t >> 6;  // 64-key block of this row within the CTA's 128 keys
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const float* skh = prm.sk + (size_t)bh * prm.nqb * 2;
     const float sk_mine = skh[2 * kb + half];
     const float sk0 = skh[2 * kb], sk1 = skh[2 * kb + 1];
-    float dk[D];
+    const uint32_t qcol = (uint32_t)(64 * g);  // this group's 64 query columns
+    const uint32_t dcol = (uint32_t)(DH * g);  // this group's D/2 output columns
+    uint8_t* prow = sm.p + (t >> 3) * 1024 + (t & 7) * 128;
+    uint8_t* dsrow = sm.ds + g * 16384 + (t >> 3) * 1024 + (t & 7) * 128;
+    float dk[DH];
 #pragma unroll
-    for (int d = 0; d < D; ++d) dk[d] = 0.f;
+    for (int d = 0; d < DH; ++d) dk[d] = 0.f;
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int I = I0 + it;
       const uint32_t ph = it & 1;
-      {
+      if (g == 0) {
         const size_t r = (size_t)bh * prm.np + I * 128 + t;
         sm.bias[t] = kLog2_448 - prm.lse2[r];
         sm.dvec[t] = prm.dvec[r];
@@ -347,101 +368,94 @@ __global__ void __launch_bounds__(256, 1)
         break;
       }
       tc_fence_after();
-      // ---- P^T row: e4m3(448 * 2^(S2 - LSE2)), masked entries 0
-      uint32_t pk[32];
+      // ---- P^T: e4m3(448 * 2^(S2 - LSE2)) for query columns [qcol, qcol + 64), in two
+      // 32-column chunks; codes go straight to the swizzled P tile
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t s[32];
-        tmem_ld32(tmem + lane_base + cS + c * 32, s);
-        tmem_ld_wait();
+      for (int c = 0; c < 2; ++c) {
+        uint32_t sv[32];
+        tmem_ld32(tmem + lane_base + cS + qcol + 32 * c, sv);
+        tmem_wait32(sv);
+        uint32_t pw[8];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
           float p[4];
+          const float4 b4 = *reinterpret_cast<const float4*>(&sm.bias[qcol + 32 * c + e]);
+          const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const int qi = c * 32 + e + u;
-            float v = ex2(fmaf(__uint_as_float(s[e + u]), cs, sm.bias[qi]));
+            const int qi = (int)qcol + 32 * c + e + u;
+            float v = ex2(fmaf(__uint_as_float(sv[e + u]), cs, bb[u]));
             if (!key_ok || (diag && qi < t)) v = 0.f;
             p[u] = v;
           }
           const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(p[0], p[1]), __NV_SATFINITE, __NV_E4M3);
           const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(p[2], p[3]), __NV_SATFINITE, __NV_E4M3);
-          pk[(c * 32 + e) >> 2] = (uint32_t)lo | ((uint32_t)hi << 16);
+          pw[e >> 2] = (uint32_t)lo | ((uint32_t)hi << 16);
         }
-      }
-      {
-        uint8_t* prow = sm.p + (t >> 3) * 1024 + (t & 7) * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(prow + ((c ^ (t & 7)) << 4)) =
-              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        const int u0 = 4 * g + 2 * c;  // 16-byte units of this chunk in the 128-byte row
+        *reinterpret_cast<uint4*>(prow + ((u0 ^ (t & 7)) << 4)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+        *reinterpret_cast<uint4*>(prow + (((u0 + 1) ^ (t & 7)) << 4)) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
       }
       fence_proxy_async_smem();
       mbar_arrive(&sm.bar_p);
-      // ---- dS^T = P^ (dP^T - D), kept in TMEM (over dP^T) until the tile max is known
+      // ---- dS^T * 448 = p8 (dP^T - D), kept in TMEM (over dP^T) until the tile max is known
       float amax = 0.f;
-      const uint8_t* prow_rd = sm.p + (t >> 3) * 1024 + (t & 7) * 128;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t dp[32];
-        tmem_ld32(tmem + lane_base + cDP + c * 32, dp);
-        // this row's 32 P codes of the chunk, read back from the swizzled tile
-        uint32_t pw[8];
-        {
-          const uint4 a = *reinterpret_cast<const uint4*>(prow_rd + (((2 * c) ^ (t & 7)) << 4));
-          const uint4 b = *reinterpret_cast<const uint4*>(prow_rd + (((2 * c + 1) ^ (t & 7)) << 4));
-          pw[0] = a.x; pw[1] = a.y; pw[2] = a.z; pw[3] = a.w;
-          pw[4] = b.x; pw[5] = b.y; pw[6] = b.z; pw[7] = b.w;
-        }
-        tmem_ld_wait();
+      for (int c = 0; c < 2; ++c) {
+        uint32_t dv[32];
+        tmem_ld32(tmem + lane_base + cDP + qcol + 32 * c, dv);
+        const int u0 = 4 * g + 2 * c;
+        const uint4 pa = *reinterpret_cast<const uint4*>(prow + ((u0 ^ (t & 7)) << 4));
+        const uint4 pb = *reinterpret_cast<const uint4*>(prow + (((u0 + 1) ^ (t & 7)) << 4));
+        const uint32_t pw[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+        tmem_wait32(dv);
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const int qi = c * 32 + e;
+          const float2 dd = *reinterpret_cast<const float2*>(&sm.dvec[qcol + 32 * c + e]);
           const uint32_t w = pw[e >> 2] >> ((e & 3) * 8);
           const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xffffu), __NV_E4M3);
           const float2 pf = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-          const float d0 = (pf.x * (1.0f / 448.0f)) * (__uint_as_float(dp[e]) - sm.dvec[qi]);
-          const float d1 = (pf.y * (1.0f / 448.0f)) * (__uint_as_float(dp[e + 1]) - sm.dvec[qi + 1]);
-          amax = fmaxf(amax, fmaxf(fabsf(d0), fabsf(d1)));
-          dp[e] = __float_as_uint(d0);
-          dp[e + 1] = __float_as_uint(d1);
+          const float x0 = pf.x * (__uint_as_float(dv[e]) - dd.x);
+          const float x1 = pf.y * (__uint_as_float(dv[e + 1]) - dd.y);
+          amax = fmaxf(amax, fmaxf(fabsf(x0), fabsf(x1)));
+          dv[e] = __float_as_uint(x0);
+          dv[e + 1] = __float_as_uint(x1);
         }
-        tmem_st32(tmem + lane_base + cDP + c * 32, dp);
+        tmem_st32(tmem + lane_base + cDP + qcol + 32 * c, dv);
       }
       tmem_st_wait();
 #pragma unroll
       for (int m = 16; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
-      if (lane == 0) sm.smax[warp - 4] = amax;
+      if (lane == 0) sm.smax[warp] = amax;
       named_bar_compute();
-      const float a0 = fmaxf(sm.smax[0], sm.smax[1]), a1 = fmaxf(sm.smax[2], sm.smax[3]);
-      const float sds0 = a0 > 0.f ? __fdiv_rn(a0, 127.0f) : 0.f;
-      const float sds1 = a1 > 0.f ? __fdiv_rn(a1, 127.0f) : 0.f;
-      const float sds = half ? sds1 : sds0;
-      const float inv = sds > 0.f ? 1.0f / sds : 0.f;
-      // ---- dS^T codes -> shared memory (bf16 containers, 128B-swizzled key rows)
+      // tile max over the 64 key rows of each half and all 128 queries (both groups)
+      const float a0 = fmaxf(fmaxf(sm.smax[0], sm.smax[1]), fmaxf(sm.smax[4], sm.smax[5]));
+      const float a1 = fmaxf(fmaxf(sm.smax[2], sm.smax[3]), fmaxf(sm.smax[6], sm.smax[7]));
+      // values are 448 * dS: scale s_dS = max|dS| / 127
+      const float sds0 = a0 > 0.f ? __fdiv_rn(a0 * (1.0f / 448.0f), 127.0f) : 0.f;
+      const float sds1 = a1 > 0.f ? __fdiv_rn(a1 * (1.0f / 448.0f), 127.0f) : 0.f;
+      const float amine = half ? a1 : a0;
+      const float inv = amine > 0.f ? 127.0f / amine : 0.f;  // code = rint(448 dS * 127 / max|448 dS|)
+      // ---- dS^T codes -> shared memory (bf16 containers, 128B-swizzled key rows, block g)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t dsv[32];
-        tmem_ld32(tmem + lane_base + cDP + c * 32, dsv);
-        tmem_ld_wait();
+      for (int c = 0; c < 2; ++c) {
+        uint32_t dv[32];
+        tmem_ld32(tmem + lane_base + cDP + qcol + 32 * c, dv);
+        tmem_wait32(dv);
         uint32_t packed[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          int c0 = __float2int_rn(__uint_as_float(dsv[e]) * inv);
-          int c1 = __float2int_rn(__uint_as_float(dsv[e + 1]) * inv);
-          c0 = max(-127, min(127, c0));
-          c1 = max(-127, min(127, c1));
-          const __nv_bfloat162 h = __floats2bfloat162_rn((float)c0, (float)c1);
-          packed[e >> 1] = *reinterpret_cast<const uint32_t*>(&h);
+          // round to the nearest integer (ties to even) without leaving the fp32 pipe;
+          // |448 dS * inv| <= 127 (plus rounding), so no clamp is needed
+          const float c0 = fmaf(__uint_as_float(dv[e]), inv, kRoundMagic) - kRoundMagic;
+          const float c1 = fmaf(__uint_as_float(dv[e + 1]), inv, kRoundMagic) - kRoundMagic;
+          const __nv_bfloat162 hv = __floats2bfloat162_rn(c0, c1);
+          packed[e >> 1] = *reinterpret_cast<const uint32_t*>(&hv);
         }
-        // queries [32c, 32c+32): block c/2, bytes (c&1)*64 .. +64 of the 128-byte row
-        uint8_t* rowp = sm.ds + (c >> 1) * 16384 + (t >> 3) * 1024 + (t & 7) * 128;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int chunk = (c & 1) * 4 + u;
-          *reinterpret_cast<uint4*>(rowp + ((chunk ^ (t & 7)) << 4)) =
+        for (int u = 0; u < 4; ++u)
+          *reinterpret_cast<uint4*>(dsrow + (((4 * c + u) ^ (t & 7)) << 4)) =
               make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
-        }
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -451,28 +465,34 @@ __global__ void __launch_bounds__(256, 1)
         break;
       }
       tc_fence_after();
-      // ---- dK += RN(s_dS * s_q) * part
-      const float ck = __fmul_rn(sds, sqI);
+      // ---- dK += RN(s_dS * s_q) * part (this group's D/2 columns)
+      const float ck = __fmul_rn(half ? sds1 : sds0, sqI);
 #pragma unroll
-      for (int c = 0; c < D; c += 32) {
-        uint32_t pv[32];
-        tmem_ld32(tmem + lane_base + cS + c, pv);
-        tmem_ld_wait();
+      for (int c = 0; c < DH; c += 16) {
+        uint32_t pv[16];
+        tmem_ld16(tmem + lane_base + cS + dcol + c, pv);
+        tmem_wait16(pv);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) dk[c + e] = fmaf(ck, __uint_as_float(pv[e]), dk[c + e]);
+        for (int e = 0; e < 16; ++e) dk[c + e] = fmaf(ck, __uint_as_float(pv[e]), dk[c + e]);
       }
-      // ---- dQ (query row t of block I) += ca * half0 + cb * half1
+      // ---- dQ (query row t of block I) += ca * half0 + cb * half1, this group's D/2 columns
       const float ca = __fmul_rn(sds0, sk0), cb = __fmul_rn(sds1, sk1);
       const int qrow = I * 128 + t;
       const bool q_ok = qrow < prm.N;
-      float* dst = prm.dqacc + ((size_t)bh * prm.np + qrow) * D;
-      // the TMEM loads are warp-collective: every lane issues them, only live rows add
+      float* dst = prm.dqacc + ((size_t)bh * prm.np + qrow) * D + dcol;
 #pragma unroll
-      for (int c = 0; c < D; c += 16) {
+      for (int c = 0; c < DH; c += 16) {
         uint32_t va[16], vb[16];
-        tmem_ld16(tmem + lane_base + cDP + c, va);
-        tmem_ld16(tmem + lane_base + cDQB + c, vb);
+        tmem_ld16(tmem + lane_base + cDP + dcol + c, va);
+        tmem_ld16(tmem + lane_base + cDQB + dcol + c, vb);
         tmem_ld_wait();
+        reg_fence16(va);
+        reg_fence16(vb);
+        if (c + 16 >= DH) {
+          // every TMEM read of this iteration is done: let the next S/dP MMAs start
+          tc_fence_before();
+          mbar_arrive(&sm.bar_free);
+        }
         if (q_ok) {
 #pragma unroll
           for (int e = 0; e < 16; e += 4) {
@@ -485,61 +505,49 @@ __global__ void __launch_bounds__(256, 1)
           }
         }
       }
-      tc_fence_before();
-      mbar_arrive(&sm.bar_free);
     }
-    // ---------------- epilogue: dV and dK rows of this key block
+    // ---------------- epilogue: dV and dK rows of this key block, this group's columns
     if (ok) {
       tc_fence_after();
       const size_t orow = ((size_t)bh * prm.N + key) * D;
-      const float* sdoh = prm.sdo + (size_t)bh * D;
 #pragma unroll
-      for (int c = 0; c < D; c += 32) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_base + cDV + c, v);
-        tmem_ld_wait();
+      for (int d = 0; d < DH; ++d) dk[d] *= prm.sm_scale;
+      float r = 0.f;
+      const uint4* krow = reinterpret_cast<const uint4*>(prm.K + orow + dcol);
+      if (prm.qk_norm) {
+        // dk = r (dk' - k' (k' . dk')), k' = RN(k r): the dot spans both groups' columns
+        r = key_ok ? prm.kr[(size_t)bh * prm.np + key] : 0.f;
+        float dot = 0.f;
         if (key_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(prm.dV + orow + c);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint4 u;
-            __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int d0 = c + 8 * i + 2 * e;
-              h[e] = __floats2bfloat162_rn(__uint_as_float(v[8 * i + 2 * e]) * (sdoh[d0] * (1.0f / 448.0f)),
-                                           __uint_as_float(v[8 * i + 2 * e + 1]) * (sdoh[d0 + 1] * (1.0f / 448.0f)));
-            }
-            dst[i] = u;
-          }
-        }
-      }
-      if (key_ok) {
-#pragma unroll
-        for (int d = 0; d < D; ++d) dk[d] *= prm.sm_scale;
-        if (prm.qk_norm) {
-          // dk = r (dk' - k' (k' . dk')), k' = RN(k r) as the quantize pass formed it
-          const float r = prm.kr[(size_t)bh * prm.np + key];
-          const uint4* krow = reinterpret_cast<const uint4*>(prm.K + orow);
-          float dot = 0.f;
-#pragma unroll
-          for (int c = 0; c < D / 8; ++c) {
+          for (int c = 0; c < DH / 8; ++c) {
             float f[8];
             unpack8(__ldg(krow + c), f);
 #pragma unroll
             for (int e = 0; e < 8; ++e) dot = fmaf(__fmul_rn(f[e], r), dk[c * 8 + e], dot);
           }
+        }
+        // add the two groups' partial dot products through the (now idle) per-query rows
+        named_bar_compute();
+        if (g == 1) sm.dvec[t] = dot;
+        named_bar_compute();
+        if (g == 0) sm.bias[t] = dot + sm.dvec[t];
+        named_bar_compute();
+        dot = sm.bias[t];
+        if (key_ok) {
 #pragma unroll
-          for (int c = 0; c < D / 8; ++c) {
+          for (int c = 0; c < DH / 8; ++c) {
             float f[8];
             unpack8(__ldg(krow + c), f);
 #pragma unroll
             for (int e = 0; e < 8; ++e) dk[c * 8 + e] = r * (dk[c * 8 + e] - __fmul_rn(f[e], r) * dot);
           }
         }
-        uint4* dst = reinterpret_cast<uint4*>(prm.dK + orow);
+      }
+      if (key_ok) {
+        uint4* dst = reinterpret_cast<uint4*>(prm.dK + orow + dcol);
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
+        for (int c = 0; c < DH / 8; ++c) {
           uint4 u;
           __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
 #pragma unroll
@@ -547,11 +555,33 @@ __global__ void __launch_bounds__(256, 1)
           dst[c] = u;
         }
       }
+      const float* sdoh = prm.sdo + (size_t)bh * D;
+#pragma unroll
+      for (int c = 0; c < DH; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + cDV + dcol + c, v);
+        tmem_wait32(v);
+        if (key_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(prm.dV + orow + dcol + c);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint4 u;
+            __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int d0 = dcol + c + 8 * i + 2 * e;
+              h[e] = __floats2bfloat162_rn(__uint_as_float(v[8 * i + 2 * e]) * (sdoh[d0] * (1.0f / 448.0f)),
+                                           __uint_as_float(v[8 * i + 2 * e + 1]) * (sdoh[d0 + 1] * (1.0f / 448.0f)));
+            }
+            dst[i] = u;
+          }
+        }
+      }
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, kCols);
+  if (warp == 9) tmem_dealloc(tmem, kCols);
   if (tid == 0 && sm.abort) atomicExch(prm.status, kDevTimeout);
 }
 
@@ -606,7 +636,7 @@ int launch_main_t(const CUtensorMap& tk, const CUtensorMap& tq, const CUtensorMa
   auto kern = bwd_main_kernel<D>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 3;
   ScopedTimer timer("bwd_main", st);
-  kern<<<dim3(p.nqb, BH), 256, smem, st>>>(tk, tq, tv, tdo, tdo8, p);
+  kern<<<dim3(p.nqb, BH), 384, smem, st>>>(tk, tq, tv, tdo, tdo8, p);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 

@@ -32,21 +32,20 @@ constexpr float kLog2_448 = 8.807354922057604f;  // log2(448)
 
 template <int D>
 struct FwdSmem {
-  uint8_t q[128 * D * 2];
-  uint8_t k[kKStages][128 * D * 2];
-  uint8_t v[kVStages][D * 128];
-  uint8_t p[2][128 * 128];
+  uint8_t q[2][128 * D * 2];        // query tiles A and B (bf16 containers of INT8 codes)
+  uint8_t k[kKStages][128 * D * 2];  // key tiles
+  uint8_t v[kVStages][D * 128];      // value tiles (e4m3, channel-major)
+  uint8_t p[2][128 * 128];           // P of tiles A and B (e4m3, 128B-swizzled K-major)
   uint64_t bar_q;
   uint64_t bar_k_full[kKStages], bar_k_empty[kKStages];
   uint64_t bar_v_full[kVStages], bar_v_empty[kVStages];
-  uint64_t bar_s_full[2], bar_p_full[2];
-  uint64_t bar_o;
+  uint64_t bar_s_full[2], bar_p_full[2], bar_o_done[2];
   uint32_t tmem_base;
   int abort;
 };
 
 struct FwdParams {
-  int N, np, nqb;
+  int N, np, nqb, npairs;
   float alpha;  // RN(sm_scale * log2 e)
   const float* sq;
   const float* sk;
@@ -62,35 +61,265 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// two fp32 lanes in one 64-bit register: each lane is an ordinary IEEE fp32 op
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2split(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 
 // The e4m3 code of x = RN(448 * RN(2^t)) flips where x crosses a rounding
 // midpoint of e4m3: fp32 mantissa bit 19 set and bits 18..0 clear.  The fast
-// value 448 * ex2.approx(t) is within a few ulps of x, so a code is trusted
-// unless the fast value lies within kBandUlps of such a midpoint; those few are
-// recomputed with a correctly rounded exp2.  band_key(x) <= kBandMax marks them.
-constexpr uint32_t kBandUlps = 16;
+// value 448 * ex2.approx(t) is within 2 ulps of x (measured over 2^26 values of
+// t in [-16, 0]), so a code is trusted unless the fast value lies within
+// kBandUlps of such a midpoint; those few are recomputed with a correctly
+// rounded exp2.  band_key(x) <= kBandMax marks them.
+constexpr uint32_t kBandUlps = 8;
 constexpr uint32_t kBandC = (kBandUlps - 0x80000u) << 12;
 constexpr uint32_t kBandMax = (2u * kBandUlps) << 12;
 __device__ __forceinline__ uint32_t band_key(float x) { return __float_as_uint(x) * 4096u + kBandC; }
 
-// e4m3 code of RN(448 * RN(2^t)) with 2^t evaluated in fp64 and rounded once
+
+// e4m3 code of RN(448 * RN(2^t)) with 2^t evaluated in fp64 and rounded once.
+// Out of line with a scalar argument: the rare path adds little code.
 __device__ __noinline__ uint32_t exact_p_code(float t) {
   const float pt = (float)exp2((double)t);
   return (uint32_t)__nv_cvt_float_to_fp8(__fmul_rn(448.0f, pt), __NV_SATFINITE, __NV_E4M3);
 }
 
+__device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float d) {
+  const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+// Softmax of one 128-query tile (tile X of the CTA), run by one warpgroup.
+// Thread t owns query row t (TMEM lane t).
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(256, 1)
+__device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParams& prm, int X, int qb, int bh,
+                                                  uint32_t tmem, volatile int* abort) {
+  const int t = threadIdx.x - 128 * X;
+  const int warp_in_wg = t >> 5;
+  const int row = qb * 128 + t;
+  const uint32_t lane_base = (uint32_t)(warp_in_wg * 32) << 16;
+  const uint32_t s_col = tmem + lane_base + (uint32_t)(X * 128);
+  const uint32_t o_col = tmem + lane_base + 256u + (uint32_t)(X * D);
+  const int n_tiles = CAUSAL ? qb + 1 : prm.nqb;
+  const float s_q = prm.sq[(size_t)bh * prm.nqb + qb];
+  const float* skh = prm.sk + (size_t)bh * prm.nqb * 2;
+  uint8_t* prow = sm.p[X] + (t >> 3) * 1024 + (t & 7) * 128;
+  float m = -INFINITY, l = 0.f;
+  bool ok = true;
+  for (int j = 0; j < n_tiles; ++j) {
+    if (!mbar_wait(&sm.bar_s_full[X], j & 1, abort)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    const float c0 = __fmul_rn(__fmul_rn(s_q, skh[2 * j]), prm.alpha);
+    const float c1 = __fmul_rn(__fmul_rn(s_q, skh[2 * j + 1]), prm.alpha);
+    const int kbase = j * 128;
+    const bool masked_tile = (kbase + 128 > prm.N) || (CAUSAL && j == qb);
+    int lim = prm.N - kbase;  // keys [0, lim) of the tile are valid
+    if (CAUSAL && j == qb) lim = min(lim, t + 1);
+    // ---- S row in two 64-key halves (sh = two 32-column loads): the max pass ends
+    // with half 1 in registers; the exp pass uses it, then reloads half 0
+    uint32_t sh[2][32];
+    float mxh[2];
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+      tmem_ld32(s_col + h * 64, sh[0]);
+      tmem_ld32(s_col + h * 64 + 32, sh[1]);
+      tmem_ld_wait();
+      reg_fence32(sh[0]);
+      reg_fence32(sh[1]);
+      float a = -INFINITY;
+      const int hl = lim - h * 64;  // valid keys of this half (masked tiles)
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float v0 = __uint_as_float(sh[q][e]), v1 = __uint_as_float(sh[q][e + 1]);
+          if (masked_tile) {
+            v0 = (q * 32 + e < hl) ? v0 : -INFINITY;
+            v1 = (q * 32 + e + 1 < hl) ? v1 : -INFINITY;
+          }
+          a = max3(a, v0, v1);
+        }
+      mxh[h] = a;
+    }
+    // the log2-domain logit is acc * c with c >= 0, so its maximum is max(acc) * c
+    const float mt0 = mxh[0] == -INFINITY ? -INFINITY : __fmul_rn(mxh[0], c0);
+    const float mt1 = mxh[1] == -INFINITY ? -INFINITY : __fmul_rn(mxh[1], c1);
+    const float m_new = max3(m, mt0, mt1);
+    const float corr = (m == -INFINITY) ? 0.f : ex2(m - m_new);
+    // ---- PV of the previous tile must be complete before P is overwritten and O rescaled
+    if (j > 0) {
+      if (!mbar_wait(&sm.bar_o_done[X], (j - 1) & 1, abort)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+    }
+    // ---- t = RN(acc*c - m_new) (one FMA), x = 448 * 2^t, e4m3 codes -> shared memory
+    const uint64_t neg_m2 = f2(-m_new, -m_new);
+    const uint64_t k448 = f2(448.f, 448.f);
+    uint64_t lsum = f2(0.f, 0.f);
+#pragma unroll 1
+    for (int h = 1; h >= 0; --h) {
+      if (h == 0) {
+        tmem_ld32(s_col, sh[0]);
+        tmem_ld32(s_col + 32, sh[1]);
+        tmem_ld_wait();
+        reg_fence32(sh[0]);
+        reg_fence32(sh[1]);
+      }
+      const float cc = h == 0 ? c0 : c1;
+      const uint64_t cc2 = f2(cc, cc);
+      const int hl = lim - h * 64;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        struct {
+          uint32_t w[8];
+        } w;
+        uint32_t band = ~0u;
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          float x[4];
+#pragma unroll
+          for (int u = 0; u < 4; u += 2) {
+            float t0, t1;
+            f2split(ffma2(f2(__uint_as_float(sh[q][e + u]), __uint_as_float(sh[q][e + u + 1])), cc2, neg_m2), t0,
+                    t1);
+            f2split(fmul2(f2(ex2(t0), ex2(t1)), k448), x[u], x[u + 1]);
+            if (masked_tile) {
+              x[u] = (q * 32 + e + u < hl) ? x[u] : 0.f;
+              x[u + 1] = (q * 32 + e + u + 1 < hl) ? x[u + 1] : 0.f;
+            }
+            lsum = fadd2(lsum, f2(x[u], x[u + 1]));
+            band = min(band, min(band_key(x[u]), band_key(x[u + 1])));
+          }
+          w.w[e >> 2] = pack4_e4m3(x[0], x[1], x[2], x[3]);
+        }
+        // rare: codes whose fast value is near an e4m3 midpoint are redone exactly
+        if (band <= kBandMax) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float tt = fmaf(__uint_as_float(sh[q][e]), cc, -m_new);
+            const float xv = ex2(tt) * 448.f;
+            if (band_key(xv) <= kBandMax && (!masked_tile || q * 32 + e < hl)) {
+              const uint32_t code = exact_p_code(tt);
+              w.w[e >> 2] = (w.w[e >> 2] & ~(0xffu << ((e & 3) * 8))) | (code << ((e & 3) * 8));
+            }
+          }
+        }
+        const int c = 2 * h + q;  // 32-key chunk of the row: 16-byte units 2c, 2c+1
+        *reinterpret_cast<uint4*>(prow + (((2 * c) ^ (t & 7)) << 4)) = make_uint4(w.w[0], w.w[1], w.w[2], w.w[3]);
+        *reinterpret_cast<uint4*>(prow + (((2 * c + 1) ^ (t & 7)) << 4)) =
+            make_uint4(w.w[4], w.w[5], w.w[6], w.w[7]);
+      }
+    }
+    if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        uint32_t o[32];
+        tmem_ld32(o_col + c, o);
+        tmem_wait32(o);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+        tmem_st32(o_col + c, o);
+      }
+      tmem_st_wait();
+    }
+    float la, lb;
+    f2split(lsum, la, lb);
+    l = fmaf(l, corr, la + lb);
+    m = m_new;
+    fence_proxy_async_smem();
+    tc_fence_before();
+    mbar_arrive(&sm.bar_p_full[X]);
+  }
+  // ---- epilogue: O = A * sv / l (l sums 448 p~), LSE = ln2 (m + log2(l / 448))
+  if (ok && mbar_wait(&sm.bar_o_done[X], (n_tiles - 1) & 1, abort)) {
+    tc_fence_after();
+    const float inv_l = 1.0f / l;
+    const bool live = row < prm.N;
+    const size_t obase = ((size_t)bh * prm.N + row) * D;
+    const float* svh = prm.sv + (size_t)bh * D;
+#pragma unroll 1
+    for (int c = 0; c < D; c += 32) {
+      uint32_t o[32];
+      tmem_ld32(o_col + c, o);
+      tmem_wait32(o);
+      float f[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(o[i]) * (svh[c + i] * inv_l);
+      if (live) {
+        uint4* dst = reinterpret_cast<uint4*>(prm.O + obase + c);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint4 u;
+          __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) h[e] = __floats2bfloat162_rn(f[8 * i + 2 * e], f[8 * i + 2 * e + 1]);
+          dst[i] = u;
+        }
+        if (prm.O32) {
+          float4* d32 = reinterpret_cast<float4*>(prm.O32 + obase + c);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) d32[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+        }
+      }
+    }
+    if (live) prm.LSE[(size_t)bh * prm.N + row] = (m + (log2f(l) - kLog2_448)) * 0.69314718055994531f;
+  }
+}
+
+// One CTA per (head, pair of 128-query blocks A = 2c, B = 2c + 1).  Warpgroups
+// 0 and 1 run the softmax of tiles A and B; warp 8 loads K and V tiles with
+// TMA; warp 9 allocates TMEM and issues the UMMAs in the order
+//   S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) ...
+// so the tensor core works on one tile while the other tile's softmax runs.
+// TMEM columns: S_A [0,128), S_B [128,256), O_A [256,256+D), O_B [256+D,256+2D).
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(384, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdParams prm) {
   extern __shared__ uint8_t smem_raw[];
   FwdSmem<D>& sm = *reinterpret_cast<FwdSmem<D>*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.y;
-  const int qb = CAUSAL ? (prm.nqb - 1 - (int)blockIdx.x) : (int)blockIdx.x;
-  const int n_tiles = CAUSAL ? qb + 1 : prm.nqb;
+  const int pc = CAUSAL ? (prm.npairs - 1 - (int)blockIdx.x) : (int)blockIdx.x;
+  const int qbA = 2 * pc, qbB = 2 * pc + 1;
+  const bool hasB = qbB < prm.nqb;
+  // KV tiles: tile A needs [0, lastA], tile B [0, lastB]
+  const int lastA = CAUSAL ? qbA : prm.nqb - 1;
+  const int lastB = hasB ? (CAUSAL ? qbB : prm.nqb - 1) : -1;
+  const int n_kv = (lastB > lastA ? lastB : lastA) + 1;
   constexpr uint32_t kTmemCols = 512;
-  constexpr uint32_t kOCol = 256;
 
   if (tid == 0) {
     mbar_init(&sm.bar_q, 1);
@@ -102,15 +331,15 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(&sm.bar_v_full[s], 1);
       mbar_init(&sm.bar_v_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&sm.bar_s_full[s], 1);
-      mbar_init(&sm.bar_p_full[s], 128);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&sm.bar_s_full[x], 1);
+      mbar_init(&sm.bar_p_full[x], 128);
+      mbar_init(&sm.bar_o_done[x], 1);
     }
-    mbar_init(&sm.bar_o, 1);
     sm.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == 9) {
     tmem_alloc(&sm.tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -119,234 +348,87 @@ __global__ void __launch_bounds__(256, 1)
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort = &sm.abort;
 
-  if (warp == 0 && lane == 0) {
-    // ---------------- producer: Q once, then K tiles
+  if (warp < 4) {
+    softmax_tile_loop<D, CAUSAL>(sm, prm, 0, qbA, bh, tmem, abort);
+  } else if (warp < 8) {
+    if (hasB) softmax_tile_loop<D, CAUSAL>(sm, prm, 1, qbB, bh, tmem, abort);
+  } else if (warp == 8 && lane == 0) {
+    // ---------------- producer: Q tiles once, then K and V tiles
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
-    mbar_arrive_expect_tx(&sm.bar_q, 128 * D * 2);
+    tma_prefetch_desc(&tm_v);
+    mbar_arrive_expect_tx(&sm.bar_q, (hasB ? 2 : 1) * 128 * D * 2);
 #pragma unroll
-    for (int c = 0; c < D / 64; ++c) tma_load_3d(sm.q + c * 16384, &tm_q, c * 64, qb * 128, bh, &sm.bar_q);
-    for (int j = 0; j < n_tiles; ++j) {
+    for (int c = 0; c < D / 64; ++c) {
+      tma_load_3d(sm.q[0] + c * 16384, &tm_q, c * 64, qbA * 128, bh, &sm.bar_q);
+      if (hasB) tma_load_3d(sm.q[1] + c * 16384, &tm_q, c * 64, qbB * 128, bh, &sm.bar_q);
+    }
+    for (int j = 0; j < n_kv; ++j) {
       const int s = j % kKStages;
       if (j >= kKStages && !mbar_wait(&sm.bar_k_empty[s], ((j / kKStages) - 1) & 1, abort)) break;
       mbar_arrive_expect_tx(&sm.bar_k_full[s], 128 * D * 2);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c)
         tma_load_3d(sm.k[s] + c * 16384, &tm_k, c * 64, j * 128, bh, &sm.bar_k_full[s]);
+      const int vs = j % kVStages;
+      if (j >= kVStages && !mbar_wait(&sm.bar_v_empty[vs], ((j / kVStages) - 1) & 1, abort)) break;
+      mbar_arrive_expect_tx(&sm.bar_v_full[vs], D * 128);
+      tma_load_3d(sm.v[vs], &tm_v, j * 128, 0, bh, &sm.bar_v_full[vs]);
     }
-  } else if (warp == 2 && lane == 0) {
-    // ---------------- producer: V tiles
-    tma_prefetch_desc(&tm_v);
-    for (int j = 0; j < n_tiles; ++j) {
-      const int s = j % kVStages;
-      if (j >= kVStages && !mbar_wait(&sm.bar_v_empty[s], ((j / kVStages) - 1) & 1, abort)) break;
-      mbar_arrive_expect_tx(&sm.bar_v_full[s], D * 128);
-      tma_load_3d(sm.v[s], &tm_v, j * 128, 0, bh, &sm.bar_v_full[s]);
-    }
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 9 && lane == 0) {
     // ---------------- UMMA issuer
     constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
     constexpr uint32_t idesc_o = idesc_e4m3(128, D);
-    const uint32_t q_addr = smem_u32(sm.q);
-    auto issue_s = [&](int j) -> bool {
-      const int s = j % kKStages;
-      if (!mbar_wait(&sm.bar_k_full[s], (j / kKStages) & 1, abort)) return false;
-      tc_fence_after();
-      const uint32_t k_addr = smem_u32(sm.k[s]);
-      const uint32_t d_col = tmem + (uint32_t)((j & 1) * 128);
+    auto issue_s = [&](int X, int j) {
+      const uint32_t q_addr = smem_u32(sm.q[X]);
+      const uint32_t k_addr = smem_u32(sm.k[j % kKStages]);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-        umma_bf16(d_col, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), idesc_s,
-                  kk > 0);
+        umma_bf16(tmem + (uint32_t)(X * 128), sdesc_sw128(q_addr + off, 16, 1024),
+                  sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0);
       }
-      umma_commit(&sm.bar_s_full[j & 1]);
-      umma_commit(&sm.bar_k_empty[s]);
-      return true;
+      umma_commit(&sm.bar_s_full[X]);
     };
-    bool ok = mbar_wait(&sm.bar_q, 0, abort) && issue_s(0);
-    for (int j = 0; ok && j < n_tiles; ++j) {
-      if (j + 1 < n_tiles && !issue_s(j + 1)) break;
-      const int vs = j % kVStages;
-      if (!mbar_wait(&sm.bar_p_full[j & 1], (j >> 1) & 1, abort)) break;
-      if (!mbar_wait(&sm.bar_v_full[vs], (j / kVStages) & 1, abort)) break;
-      tc_fence_after();
-      const uint32_t p_addr = smem_u32(sm.p[j & 1]);
-      const uint32_t v_addr = smem_u32(sm.v[vs]);
+    auto issue_pv = [&](int X, int j, int first) {
+      const uint32_t p_addr = smem_u32(sm.p[X]);
+      const uint32_t v_addr = smem_u32(sm.v[j % kVStages]);
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        umma_f8(tmem + kOCol, sdesc_sw128(p_addr + kk * 32, 16, 1024), sdesc_sw128(v_addr + kk * 32, 16, 1024),
-                idesc_o, (j > 0 || kk > 0));
-      }
-      umma_commit(&sm.bar_o);
-      umma_commit(&sm.bar_v_empty[vs]);
+      for (int kk = 0; kk < 4; ++kk)
+        umma_f8(tmem + 256u + (uint32_t)(X * D), sdesc_sw128(p_addr + kk * 32, 16, 1024),
+                sdesc_sw128(v_addr + kk * 32, 16, 1024), idesc_o, (!first || kk > 0));
+      umma_commit(&sm.bar_o_done[X]);
+    };
+    bool ok = mbar_wait(&sm.bar_q, 0, abort) && mbar_wait(&sm.bar_k_full[0], 0, abort);
+    if (ok) {
+      tc_fence_after();
+      issue_s(0, 0);
+      if (lastB >= 0) issue_s(1, 0);
+      umma_commit(&sm.bar_k_empty[0]);
     }
-  } else if (warp >= 4) {
-    // ---------------- softmax: one query row per thread
-    const int t = tid - 128;
-    const int row = qb * 128 + t;
-    const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
-    const float s_q = prm.sq[(size_t)bh * prm.nqb + qb];
-    const float* skh = prm.sk + (size_t)bh * prm.nqb * 2;
-    float m = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      if (!mbar_wait(&sm.bar_s_full[j & 1], (j >> 1) & 1, abort)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float s[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        tmem_ld32(tmem + lane_base + (uint32_t)((j & 1) * 128 + c * 32),
-                  *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
-      tmem_ld_wait();
-      const float c0 = __fmul_rn(__fmul_rn(s_q, skh[2 * j]), prm.alpha);
-      const float c1 = __fmul_rn(__fmul_rn(s_q, skh[2 * j + 1]), prm.alpha);
-      const int kbase = j * 128;
-      // keys past the sequence end (last tile) or after the query (causal diagonal)
-      const bool masked_tile = (kbase + 128 > prm.N) || (CAUSAL && j == qb);
-      int lim = prm.N - kbase;  // keys [0, lim) of the tile are valid
-      if (CAUSAL && j == qb) lim = min(lim, t + 1);
-      float mx0 = -INFINITY, mx1 = -INFINITY;
-      if (masked_tile) {
-#pragma unroll
-        for (int i = 0; i < 64; ++i) mx0 = fmaxf(mx0, i < lim ? s[i] : -INFINITY);
-#pragma unroll
-        for (int i = 64; i < 128; ++i) mx1 = fmaxf(mx1, i < lim ? s[i] : -INFINITY);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 64; ++i) mx0 = fmaxf(mx0, s[i]);
-#pragma unroll
-        for (int i = 64; i < 128; ++i) mx1 = fmaxf(mx1, s[i]);
-      }
-      // the log2-domain logit is acc * c with c >= 0, so its maximum is max(acc) * c
-      const float mt0 = mx0 == -INFINITY ? -INFINITY : __fmul_rn(mx0, c0);
-      const float mt1 = mx1 == -INFINITY ? -INFINITY : __fmul_rn(mx1, c1);
-      const float m_new = fmaxf(m, fmaxf(mt0, mt1));
-      const float corr = (m == -INFINITY) ? 0.f : ex2(m - m_new);
-      // t = RN(acc*c - m_new) in one FMA; x = 448 * 2^t (to be rounded to e4m3)
-      const float neg_m = -m_new;
-      float lt = 0.f;
-      uint32_t pk[32];
-      uint32_t band[4] = {~0u, ~0u, ~0u, ~0u};  // per 32-key chunk: min band key
-#pragma unroll
-      for (int i = 0; i < 128; i += 4) {
-        const float c = i < 64 ? c0 : c1;
-        float p0 = ex2(fmaf(s[i], c, neg_m)) * 448.f;
-        float p1 = ex2(fmaf(s[i + 1], c, neg_m)) * 448.f;
-        float p2 = ex2(fmaf(s[i + 2], c, neg_m)) * 448.f;
-        float p3 = ex2(fmaf(s[i + 3], c, neg_m)) * 448.f;
-        if (masked_tile) {
-          p0 = i < lim ? p0 : 0.f;
-          p1 = i + 1 < lim ? p1 : 0.f;
-          p2 = i + 2 < lim ? p2 : 0.f;
-          p3 = i + 3 < lim ? p3 : 0.f;
-        }
-        band[i >> 5] = min(band[i >> 5], min(min(band_key(p0), band_key(p1)), min(band_key(p2), band_key(p3))));
-        lt += (p0 + p1) + (p2 + p3);
-        const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(p0, p1), __NV_SATFINITE, __NV_E4M3);
-        const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(p2, p3), __NV_SATFINITE, __NV_E4M3);
-        pk[i >> 2] = (uint32_t)lo | ((uint32_t)hi << 16);
-      }
-      // rare: codes whose fast value is near an e4m3 midpoint are redone exactly
-      // (S is still in TMEM: reload the flagged 32-key chunk rather than keep it live)
-      if (__any_sync(0xffffffffu, min(min(band[0], band[1]), min(band[2], band[3])) <= kBandMax)) {
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          if (__any_sync(0xffffffffu, band[cc] <= kBandMax)) {
-            uint32_t sr[32];
-            tmem_ld32(tmem + lane_base + (uint32_t)((j & 1) * 128 + cc * 32), sr);
-            tmem_ld_wait();
-            if (band[cc] <= kBandMax) {
-              const float c = cc < 2 ? c0 : c1;
-#pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                const int i = cc * 32 + e;
-                const float tt = fmaf(__uint_as_float(sr[e]), c, neg_m);
-                const float x = ex2(tt) * 448.f;
-                const bool valid = !masked_tile || i < lim;
-                if (valid && band_key(x) <= kBandMax) {
-                  const uint32_t code = exact_p_code(tt);
-                  pk[i >> 2] = (pk[i >> 2] & ~(0xffu << ((i & 3) * 8))) | (code << ((i & 3) * 8));
-                }
-              }
-            }
-          }
-        }
-      }
-      l = fmaf(l, corr, lt);
-      m = m_new;
-      // P row -> shared memory, 128B-swizzled K-major layout (row t, 128 key bytes)
-      uint8_t* prow = sm.p[j & 1] + (t >> 3) * 1024 + (t & 7) * 128;
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(prow + ((c ^ (t & 7)) << 4)) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-      fence_proxy_async_smem();
-      if (j > 0) {
-        // PV_{j-1} must be complete before O is rescaled (and before the P buffer
-        // it read is overwritten next iteration)
-        if (!mbar_wait(&sm.bar_o, (j - 1) & 1, abort)) {
+    for (int j = 0; ok && j < n_kv; ++j) {
+      const bool nextk = j + 1 < n_kv;
+      if (nextk && !mbar_wait(&sm.bar_k_full[(j + 1) % kKStages], ((j + 1) / kKStages) & 1, abort)) break;
+      if (!mbar_wait(&sm.bar_v_full[j % kVStages], (j / kVStages) & 1, abort)) break;
+      for (int X = 0; X < 2; ++X) {
+        const int last = X == 0 ? lastA : lastB;
+        if (j > last) continue;
+        if (!mbar_wait(&sm.bar_p_full[X], j & 1, abort)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, corr != 1.f)) {
-#pragma unroll
-          for (int c = 0; c < D; c += 32) {
-            uint32_t o[32];
-            tmem_ld32(tmem + lane_base + kOCol + c, o);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
-            tmem_st32(tmem + lane_base + kOCol + c, o);
-          }
-          tmem_st_wait();
-        }
+        issue_pv(X, j, j == 0);
+        if (j + 1 <= last) issue_s(X, j + 1);
       }
-      tc_fence_before();
-      mbar_arrive(&sm.bar_p_full[j & 1]);
-    }
-    // ---------------- epilogue: O = A * sv / l, LSE
-    if (ok && mbar_wait(&sm.bar_o, (n_tiles - 1) & 1, abort)) {
-      tc_fence_after();
-      const float inv_l = 1.0f / l;
-      const bool live = row < prm.N;
-      const size_t obase = ((size_t)bh * prm.N + row) * D;
-      const float* svh = prm.sv + (size_t)bh * D;
-#pragma unroll
-      for (int c = 0; c < D; c += 32) {
-        uint32_t o[32];
-        tmem_ld32(tmem + lane_base + kOCol + c, o);
-        tmem_ld_wait();
-        float f[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(o[i]) * (svh[c + i] * inv_l);
-        if (live) {
-          uint4* dst = reinterpret_cast<uint4*>(prm.O + obase + c);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint4 u;
-            __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) h[e] = __floats2bfloat162_rn(f[8 * i + 2 * e], f[8 * i + 2 * e + 1]);
-            dst[i] = u;
-          }
-          if (prm.O32) {
-            float4* d32 = reinterpret_cast<float4*>(prm.O32 + obase + c);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) d32[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
-          }
-        }
-      }
-      if (live) prm.LSE[(size_t)bh * prm.N + row] = (m + (log2f(l) - kLog2_448)) * 0.69314718055994531f;
+      if (!ok) break;
+      umma_commit(&sm.bar_v_empty[j % kVStages]);
+      if (nextk) umma_commit(&sm.bar_k_empty[(j + 1) % kKStages]);
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 9) tmem_dealloc(tmem, kTmemCols);
   if (tid == 0 && sm.abort) atomicExch(prm.status, kDevTimeout);
 }
 
@@ -358,7 +440,7 @@ int launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
   auto kern = fwd_kernel<D, CAUSAL>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 3;
   ScopedTimer timer("fwd", st);
-  kern<<<dim3(p.nqb, BH), 256, smem, st>>>(tq, tk, tv, p);
+  kern<<<dim3(p.npairs, BH), 384, smem, st>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 
@@ -377,6 +459,7 @@ int launch_fwd(const void* ws, void* O, float* LSE, float* O32, int B, int H, in
   p.N = N;
   p.np = np;
   p.nqb = np / 128;
+  p.npairs = (p.nqb + 1) / 2;
   p.alpha = (float)((double)sm_scale * 1.4426950408889634074);
   p.sq = reinterpret_cast<const float*>(w + L.sq);
   p.sk = reinterpret_cast<const float*>(w + L.sk);
