@@ -61,7 +61,7 @@ template <int D>
 __global__ void __launch_bounds__(kPreThreads) bwd_pre_kernel(const __nv_bfloat16* __restrict__ O,
                                                                const __nv_bfloat16* __restrict__ dO,
                                                                const float* __restrict__ LSE, int N,
-                                                               float* __restrict__ dvec, float* __restrict__ lse2,
+                                                               float* __restrict__ dvec, float* __restrict__ bias,
                                                                float* __restrict__ dopart,
                                                                float* __restrict__ dqacc) {
   constexpr int TPR = D / 8, RPP = kPreThreads / TPR, PASSES = 128 / RPP;
@@ -92,12 +92,16 @@ __global__ void __launch_bounds__(kPreThreads) bwd_pre_kernel(const __nv_bfloat1
     for (int m = TPR / 2; m >= 1; m >>= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
     if (g == 0) {
       dvec[(size_t)bh * np + t] = t < N ? s : 0.f;
-      lse2[(size_t)bh * np + t] =
-          t < N ? (float)((double)LSE[(size_t)bh * N + t] * 1.4426950408889634074) : INFINITY;
+      // P = 2^(S2 - LSE log2 e) is formed as 2^(S2 + bias) / 448 with bias = log2(448) - LSE log2 e;
+      // padded rows get bias = -inf, hence P = 0
+      bias[(size_t)bh * np + t] =
+          t < N ? kLog2_448 - (float)((double)LSE[(size_t)bh * N + t] * 1.4426950408889634074) : -INFINITY;
     }
-    float4* z = reinterpret_cast<float4*>(dqacc + ((size_t)bh * np + t) * D + g * 8);
-    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  // zero this block's columns of the feature-major dQ accumulator [bh][d][token]
+  for (int idx = tid; idx < D * 32; idx += kPreThreads) {
+    const int d = idx >> 5, c = idx & 31;
+    reinterpret_cast<float4*>(dqacc + ((size_t)bh * D + d) * np + blk * 128)[c] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   __shared__ float s_max[RPP][D];
 #pragma unroll
@@ -166,8 +170,8 @@ struct BwdSmem {
   uint8_t do8[D * 128];      // dO e4m3 codes, channel-major
   uint8_t p[128 * 128];      // P^T e4m3, key rows
   uint8_t ds[128 * 128 * 2]; // dS^T INT8 codes in bf16, key rows
-  __align__(16) float bias[128];  // log2(448) - LSE2_i of the current query block
-  __align__(16) float dvec[128];
+  __align__(16) float bias[2][128];  // log2(448) - LSE_i log2(e), per Q buffer
+  __align__(16) float dvec[2][128];  // D_i, per Q buffer
   float smax[8];
   uint64_t bar_kv;
   uint64_t bar_q_full[2], bar_do_full, bar_do8_full;
@@ -183,7 +187,7 @@ struct BwdParams {
   const float* sq;
   const float* sk;
   const float* sdo;
-  const float* lse2;
+  const float* bias;
   const float* dvec;
   const __nv_bfloat16* K;
   const float* kr;
@@ -210,8 +214,14 @@ __global__ void __launch_bounds__(384, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_do8, const BwdParams prm) {
-  extern __shared__ uint8_t smem_raw[];
-  BwdSmem<D>& sm = *reinterpret_cast<BwdSmem<D>*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  // the tile buffers need 1024-byte alignment (128-byte swizzle atoms); the layout
+  // fills almost all of the 227 KB, so the base is used as is and checked
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if ((smem_u32(smem_raw) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicExch(prm.status, kDevSetup);
+    return;
+  }
+  BwdSmem<D>& sm = *reinterpret_cast<BwdSmem<D>*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int kb = blockIdx.x, bh = blockIdx.y;
   const int I0 = prm.causal ? kb : 0;
@@ -272,10 +282,13 @@ __global__ void __launch_bounds__(384, 1)
       tma_load_3d(sm.do8, &tm_do8, I * 128, 0, bh, &sm.bar_do8_full);
       const int qs = it & 1;
       if (it > 1 && !mbar_wait(&sm.bar_q_free[qs], ((it >> 1) - 1) & 1, abort)) break;
-      mbar_arrive_expect_tx(&sm.bar_q_full[qs], kTile);
+      mbar_arrive_expect_tx(&sm.bar_q_full[qs], kTile + 1024);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c)
         tma_load_3d(sm.q[qs] + c * 16384, &tm_q, c * 64, I * 128, bh, &sm.bar_q_full[qs]);
+      // the query block's bias and D_i rows travel with its Q tile
+      bulk_load(sm.bias[qs], prm.bias + (size_t)bh * prm.np + I * 128, 512, &sm.bar_q_full[qs]);
+      bulk_load(sm.dvec[qs], prm.dvec + (size_t)bh * prm.np + I * 128, 512, &sm.bar_q_full[qs]);
     }
   } else if (warp == 9 && lane == 0) {
     // ---------------- UMMA issuer
@@ -354,12 +367,13 @@ __global__ void __launch_bounds__(384, 1)
     for (int it = 0; it < n_it; ++it) {
       const int I = I0 + it;
       const uint32_t ph = it & 1;
-      if (g == 0) {
-        const size_t r = (size_t)bh * prm.np + I * 128 + t;
-        sm.bias[t] = kLog2_448 - prm.lse2[r];
-        sm.dvec[t] = prm.dvec[r];
+      const int qs = it & 1;
+      const float* s_bias = sm.bias[qs];
+      const float* s_dvec = sm.dvec[qs];
+      if (!mbar_wait(&sm.bar_q_full[qs], (it >> 1) & 1, abort)) {
+        ok = false;
+        break;
       }
-      named_bar_compute();
       const float sqI = prm.sq[(size_t)bh * prm.nqb + I];
       const float cs = __fmul_rn(__fmul_rn(sqI, sk_mine), prm.alpha);
       const bool diag = prm.causal && I == kb;
@@ -368,62 +382,72 @@ __global__ void __launch_bounds__(384, 1)
         break;
       }
       tc_fence_after();
-      // ---- P^T: e4m3(448 * 2^(S2 - LSE2)) for query columns [qcol, qcol + 64), in two
-      // 32-column chunks; codes go straight to the swizzled P tile
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t sv[32];
-        tmem_ld32(tmem + lane_base + cS + qcol + 32 * c, sv);
-        tmem_wait32(sv);
-        uint32_t pw[8];
-#pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          float p[4];
-          const float4 b4 = *reinterpret_cast<const float4*>(&sm.bias[qcol + 32 * c + e]);
-          const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int qi = (int)qcol + 32 * c + e + u;
-            float v = ex2(fmaf(__uint_as_float(sv[e + u]), cs, bb[u]));
-            if (!key_ok || (diag && qi < t)) v = 0.f;
-            p[u] = v;
-          }
-          const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(p[0], p[1]), __NV_SATFINITE, __NV_E4M3);
-          const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(p[2], p[3]), __NV_SATFINITE, __NV_E4M3);
-          pw[e >> 2] = (uint32_t)lo | ((uint32_t)hi << 16);
-        }
-        const int u0 = 4 * g + 2 * c;  // 16-byte units of this chunk in the 128-byte row
-        *reinterpret_cast<uint4*>(prow + ((u0 ^ (t & 7)) << 4)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-        *reinterpret_cast<uint4*>(prow + (((u0 + 1) ^ (t & 7)) << 4)) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(&sm.bar_p);
-      // ---- dS^T * 448 = p8 (dP^T - D), kept in TMEM (over dP^T) until the tile max is known
+      // ---- P^T = e4m3(448 * 2^(S2 - LSE2)) and dS^T * 448 = p8 (dP^T - D) for query columns
+      // [qcol, qcol + 64), in 32-column chunks.  TMEM loads are software-pipelined: the next
+      // chunk's load is issued before the current chunk is processed (wait::ld waits for all
+      // of this thread's loads, so each wait then covers a load that overlapped compute).
       float amax = 0.f;
+      {
+        uint32_t bufA[32], bufB[32];
+        auto p_chunk = [&](const uint32_t (&sv)[32], int c) {
+          uint32_t pw[8];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t dv[32];
-        tmem_ld32(tmem + lane_base + cDP + qcol + 32 * c, dv);
-        const int u0 = 4 * g + 2 * c;
-        const uint4 pa = *reinterpret_cast<const uint4*>(prow + ((u0 ^ (t & 7)) << 4));
-        const uint4 pb = *reinterpret_cast<const uint4*>(prow + (((u0 + 1) ^ (t & 7)) << 4));
-        const uint32_t pw[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
-        tmem_wait32(dv);
+          for (int e = 0; e < 32; e += 4) {
+            float p[4];
+            const float4 b4 = *reinterpret_cast<const float4*>(&s_bias[qcol + 32 * c + e]);
+            const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float2 dd = *reinterpret_cast<const float2*>(&sm.dvec[qcol + 32 * c + e]);
-          const uint32_t w = pw[e >> 2] >> ((e & 3) * 8);
-          const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xffffu), __NV_E4M3);
-          const float2 pf = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-          const float x0 = pf.x * (__uint_as_float(dv[e]) - dd.x);
-          const float x1 = pf.y * (__uint_as_float(dv[e + 1]) - dd.y);
-          amax = fmaxf(amax, fmaxf(fabsf(x0), fabsf(x1)));
-          dv[e] = __float_as_uint(x0);
-          dv[e + 1] = __float_as_uint(x1);
-        }
-        tmem_st32(tmem + lane_base + cDP + qcol + 32 * c, dv);
+            for (int u = 0; u < 4; ++u) {
+              const int qi = (int)qcol + 32 * c + e + u;
+              float v = ex2(fmaf(__uint_as_float(sv[e + u]), cs, bb[u]));
+              if (!key_ok || (diag && qi < t)) v = 0.f;
+              p[u] = v;
+            }
+            const __nv_fp8x2_storage_t lo =
+                __nv_cvt_float2_to_fp8x2(make_float2(p[0], p[1]), __NV_SATFINITE, __NV_E4M3);
+            const __nv_fp8x2_storage_t hi =
+                __nv_cvt_float2_to_fp8x2(make_float2(p[2], p[3]), __NV_SATFINITE, __NV_E4M3);
+            pw[e >> 2] = (uint32_t)lo | ((uint32_t)hi << 16);
+          }
+          const int u0 = 4 * g + 2 * c;  // 16-byte units of this chunk in the 128-byte row
+          *reinterpret_cast<uint4*>(prow + ((u0 ^ (t & 7)) << 4)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+          *reinterpret_cast<uint4*>(prow + (((u0 + 1) ^ (t & 7)) << 4)) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
+        };
+        auto ds_chunk = [&](uint32_t (&dv)[32], int c) {
+          const int u0 = 4 * g + 2 * c;
+          const uint4 pa = *reinterpret_cast<const uint4*>(prow + ((u0 ^ (t & 7)) << 4));
+          const uint4 pb = *reinterpret_cast<const uint4*>(prow + (((u0 + 1) ^ (t & 7)) << 4));
+          const uint32_t pw[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float2 dd = *reinterpret_cast<const float2*>(&s_dvec[qcol + 32 * c + e]);
+            const uint32_t w = pw[e >> 2] >> ((e & 3) * 8);
+            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xffffu), __NV_E4M3);
+            const float2 pf = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+            const float x0 = pf.x * (__uint_as_float(dv[e]) - dd.x);
+            const float x1 = pf.y * (__uint_as_float(dv[e + 1]) - dd.y);
+            amax = fmaxf(amax, fmaxf(fabsf(x0), fabsf(x1)));
+            dv[e] = __float_as_uint(x0);
+            dv[e + 1] = __float_as_uint(x1);
+          }
+          tmem_st32(tmem + lane_base + cDP + qcol + 32 * c, dv);
+        };
+        tmem_ld32(tmem + lane_base + cS + qcol, bufA);
+        tmem_wait32(bufA);
+        tmem_ld32(tmem + lane_base + cS + qcol + 32, bufB);
+        p_chunk(bufA, 0);
+        tmem_wait32(bufB);
+        tmem_ld32(tmem + lane_base + cDP + qcol, bufA);
+        p_chunk(bufB, 1);
+        fence_proxy_async_smem();
+        mbar_arrive(&sm.bar_p);
+        tmem_wait32(bufA);
+        tmem_ld32(tmem + lane_base + cDP + qcol + 32, bufB);
+        ds_chunk(bufA, 0);
+        tmem_wait32(bufB);
+        ds_chunk(bufB, 1);
+        tmem_st_wait();
       }
-      tmem_st_wait();
 #pragma unroll
       for (int m = 16; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
       if (lane == 0) sm.smax[warp] = amax;
@@ -437,25 +461,30 @@ __global__ void __launch_bounds__(384, 1)
       const float amine = half ? a1 : a0;
       const float inv = amine > 0.f ? 127.0f / amine : 0.f;  // code = rint(448 dS * 127 / max|448 dS|)
       // ---- dS^T codes -> shared memory (bf16 containers, 128B-swizzled key rows, block g)
+      {
+        uint32_t bufA[32], bufB[32];
+        auto code_chunk = [&](const uint32_t (&dv)[32], int c) {
+          uint32_t packed[16];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t dv[32];
-        tmem_ld32(tmem + lane_base + cDP + qcol + 32 * c, dv);
-        tmem_wait32(dv);
-        uint32_t packed[16];
+          for (int e = 0; e < 32; e += 2) {
+            // round to the nearest integer (ties to even) without leaving the fp32 pipe;
+            // |448 dS * inv| <= 127 (plus rounding), so no clamp is needed
+            const float c0 = fmaf(__uint_as_float(dv[e]), inv, kRoundMagic) - kRoundMagic;
+            const float c1 = fmaf(__uint_as_float(dv[e + 1]), inv, kRoundMagic) - kRoundMagic;
+            const __nv_bfloat162 hv = __floats2bfloat162_rn(c0, c1);
+            packed[e >> 1] = *reinterpret_cast<const uint32_t*>(&hv);
+          }
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          // round to the nearest integer (ties to even) without leaving the fp32 pipe;
-          // |448 dS * inv| <= 127 (plus rounding), so no clamp is needed
-          const float c0 = fmaf(__uint_as_float(dv[e]), inv, kRoundMagic) - kRoundMagic;
-          const float c1 = fmaf(__uint_as_float(dv[e + 1]), inv, kRoundMagic) - kRoundMagic;
-          const __nv_bfloat162 hv = __floats2bfloat162_rn(c0, c1);
-          packed[e >> 1] = *reinterpret_cast<const uint32_t*>(&hv);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          *reinterpret_cast<uint4*>(dsrow + (((4 * c + u) ^ (t & 7)) << 4)) =
-              make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
+          for (int u = 0; u < 4; ++u)
+            *reinterpret_cast<uint4*>(dsrow + (((4 * c + u) ^ (t & 7)) << 4)) =
+                make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
+        };
+        tmem_ld32(tmem + lane_base + cDP + qcol, bufA);
+        tmem_wait32(bufA);
+        tmem_ld32(tmem + lane_base + cDP + qcol + 32, bufB);
+        code_chunk(bufA, 0);
+        tmem_wait32(bufB);
+        code_chunk(bufB, 1);
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -465,43 +494,59 @@ __global__ void __launch_bounds__(384, 1)
         break;
       }
       tc_fence_after();
-      // ---- dK += RN(s_dS * s_q) * part (this group's D/2 columns)
+      // ---- dK += RN(s_dS * s_q) * part;  dQ (query row t of block I) += ca * half0 + cb * half1
+      // (this group's D/2 columns), TMEM loads pipelined as above
       const float ck = __fmul_rn(half ? sds1 : sds0, sqI);
-#pragma unroll
-      for (int c = 0; c < DH; c += 16) {
-        uint32_t pv[16];
-        tmem_ld16(tmem + lane_base + cS + dcol + c, pv);
-        tmem_wait16(pv);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) dk[c + e] = fmaf(ck, __uint_as_float(pv[e]), dk[c + e]);
-      }
-      // ---- dQ (query row t of block I) += ca * half0 + cb * half1, this group's D/2 columns
       const float ca = __fmul_rn(sds0, sk0), cb = __fmul_rn(sds1, sk1);
       const int qrow = I * 128 + t;
       const bool q_ok = qrow < prm.N;
-      float* dst = prm.dqacc + ((size_t)bh * prm.np + qrow) * D + dcol;
+      // feature-major accumulator: the 32 lanes of a warp add 32 consecutive queries of
+      // one feature, one 128-byte line per reduction instruction
+      float* dst = prm.dqacc + ((size_t)bh * D + dcol) * prm.np + qrow;
+      {
+        uint32_t kA[16], kB[16];
+        tmem_ld16(tmem + lane_base + cS + dcol, kA);
+        tmem_wait16(kA);
 #pragma unroll
-      for (int c = 0; c < DH; c += 16) {
-        uint32_t va[16], vb[16];
-        tmem_ld16(tmem + lane_base + cDP + dcol + c, va);
-        tmem_ld16(tmem + lane_base + cDQB + dcol + c, vb);
-        tmem_ld_wait();
-        reg_fence16(va);
-        reg_fence16(vb);
-        if (c + 16 >= DH) {
-          // every TMEM read of this iteration is done: let the next S/dP MMAs start
-          tc_fence_before();
-          mbar_arrive(&sm.bar_free);
+        for (int c = 0; c < DH; c += 32) {
+          tmem_ld16(tmem + lane_base + cS + dcol + c + 16, kB);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) dk[c + e] = fmaf(ck, __uint_as_float(kA[e]), dk[c + e]);
+          tmem_wait16(kB);
+          if (c + 32 < DH) tmem_ld16(tmem + lane_base + cS + dcol + c + 32, kA);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) dk[c + 16 + e] = fmaf(ck, __uint_as_float(kB[e]), dk[c + 16 + e]);
+          if (c + 32 < DH) tmem_wait16(kA);
         }
-        if (q_ok) {
+      }
+      {
+        uint32_t va[2][16], vb[2][16];
+        tmem_ld16(tmem + lane_base + cDP + dcol, va[0]);
+        tmem_ld16(tmem + lane_base + cDQB + dcol, vb[0]);
+        tmem_ld_wait();
+        reg_fence16(va[0]);
+        reg_fence16(vb[0]);
 #pragma unroll
-          for (int e = 0; e < 16; e += 4) {
-            float4 add;
-            add.x = fmaf(ca, __uint_as_float(va[e]), cb * __uint_as_float(vb[e]));
-            add.y = fmaf(ca, __uint_as_float(va[e + 1]), cb * __uint_as_float(vb[e + 1]));
-            add.z = fmaf(ca, __uint_as_float(va[e + 2]), cb * __uint_as_float(vb[e + 2]));
-            add.w = fmaf(ca, __uint_as_float(va[e + 3]), cb * __uint_as_float(vb[e + 3]));
-            atomicAdd(reinterpret_cast<float4*>(dst + c + e), add);
+        for (int c = 0; c < DH; c += 16) {
+          const int cur = (c >> 4) & 1;
+          if (c + 16 < DH) {
+            tmem_ld16(tmem + lane_base + cDP + dcol + c + 16, va[cur ^ 1]);
+            tmem_ld16(tmem + lane_base + cDQB + dcol + c + 16, vb[cur ^ 1]);
+          } else {
+            // every TMEM read of this iteration is done: let the next S/dP MMAs start
+            tc_fence_before();
+            mbar_arrive(&sm.bar_free);
+          }
+          if (q_ok) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              atomicAdd(dst + (size_t)(c + e) * prm.np,
+                        fmaf(ca, __uint_as_float(va[cur][e]), cb * __uint_as_float(vb[cur][e])));
+          }
+          if (c + 16 < DH) {
+            tmem_ld_wait();
+            reg_fence16(va[cur ^ 1]);
+            reg_fence16(vb[cur ^ 1]);
           }
         }
       }
@@ -529,11 +574,11 @@ __global__ void __launch_bounds__(384, 1)
         }
         // add the two groups' partial dot products through the (now idle) per-query rows
         named_bar_compute();
-        if (g == 1) sm.dvec[t] = dot;
+        if (g == 1) sm.dvec[0][t] = dot;
         named_bar_compute();
-        if (g == 0) sm.bias[t] = dot + sm.dvec[t];
+        if (g == 0) sm.bias[0][t] = dot + sm.dvec[0][t];
         named_bar_compute();
-        dot = sm.bias[t];
+        dot = sm.bias[0][t];
         if (key_ok) {
 #pragma unroll
           for (int c = 0; c < DH / 8; ++c) {
@@ -586,52 +631,58 @@ __global__ void __launch_bounds__(384, 1)
 }
 
 // ------------------------------------------------------------------ bwd_dq
+// 64 tokens per CTA: the feature-major accumulator is read along tokens (coalesced),
+// transposed through shared memory, scaled, passed through QK-norm, written as bf16 rows.
 template <int D>
 __global__ void __launch_bounds__(kPreThreads) bwd_dq_kernel(const float* __restrict__ dqacc,
                                                               const __nv_bfloat16* __restrict__ Q,
                                                               const float* __restrict__ qr, int N, int np,
                                                               int qk_norm, float sm_scale,
                                                               __nv_bfloat16* __restrict__ dQ) {
-  constexpr int TPR = D / 8, RPP = kPreThreads / TPR;
-  const int bh = blockIdx.y;
+  constexpr int TPR = D / 8, RPP = kPreThreads / TPR, TOK = 64;
+  __shared__ float tile[D][TOK + 1];
+  const int bh = blockIdx.y, t0 = blockIdx.x * TOK;
   const int tid = threadIdx.x, g = tid % TPR, ro = tid / TPR;
-  const int t = blockIdx.x * RPP + ro;
-  const bool live = t < N;  // no early exit: the row's lanes shuffle together below
-  float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-  if (live) {
-    const float4* src = reinterpret_cast<const float4*>(dqacc + ((size_t)bh * np + t) * D + g * 8);
-    a = src[0];
-    b = src[1];
+  for (int idx = tid; idx < D * TOK; idx += kPreThreads) {
+    const int d = idx / TOK, c = idx % TOK;
+    tile[d][c] = dqacc[((size_t)bh * D + d) * np + t0 + c];
   }
-  float x[8] = {a.x * sm_scale, a.y * sm_scale, a.z * sm_scale, a.w * sm_scale,
-                b.x * sm_scale, b.y * sm_scale, b.z * sm_scale, b.w * sm_scale};
-  const size_t row = ((size_t)bh * N + t) * D;
-  if (qk_norm) {
-    const float r = live ? qr[(size_t)bh * np + t] : 0.f;
-    float qn[8];
-    unpack8(live ? __ldg(reinterpret_cast<const uint4*>(Q + row) + g) : make_uint4(0, 0, 0, 0), qn);
-    float dot = 0.f;
+  __syncthreads();
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      qn[i] = __fmul_rn(qn[i], r);
-      dot = fmaf(qn[i], x[i], dot);
+  for (int p = 0; p < TOK / RPP; ++p) {
+    const int r = p * RPP + ro, t = t0 + r;
+    const bool live = t < N;  // no early exit: the row's lanes shuffle together below
+    float x[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = tile[g * 8 + i][r] * sm_scale;
+    const size_t row = ((size_t)bh * N + t) * D;
+    if (qk_norm) {
+      const float rr = live ? qr[(size_t)bh * np + t] : 0.f;
+      float qn[8];
+      unpack8(live ? __ldg(reinterpret_cast<const uint4*>(Q + row) + g) : make_uint4(0, 0, 0, 0), qn);
+      float dot = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        qn[i] = __fmul_rn(qn[i], rr);
+        dot = fmaf(qn[i], x[i], dot);
+      }
+#pragma unroll
+      for (int m = TPR / 2; m >= 1; m >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, m, TPR);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[i] = rr * (x[i] - qn[i] * dot);
     }
+    uint4 u;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
 #pragma unroll
-    for (int m = TPR / 2; m >= 1; m >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, m, TPR);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) x[i] = r * (x[i] - qn[i] * dot);
+    for (int e = 0; e < 4; ++e) h[e] = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+    if (live) reinterpret_cast<uint4*>(dQ + row)[g] = u;
   }
-  uint4 u;
-  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
-#pragma unroll
-  for (int e = 0; e < 4; ++e) h[e] = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
-  if (live) reinterpret_cast<uint4*>(dQ + row)[g] = u;
 }
 
 template <int D>
 int launch_main_t(const CUtensorMap& tk, const CUtensorMap& tq, const CUtensorMap& tv, const CUtensorMap& tdo,
                   const CUtensorMap& tdo8, const BwdParams& p, int BH, cudaStream_t st) {
-  size_t smem = sizeof(BwdSmem<D>) + 1024;
+  size_t smem = sizeof(BwdSmem<D>);
   if (smem < 120 * 1024) smem = 120 * 1024;  // one CTA per SM: it holds all 512 TMEM columns
   auto kern = bwd_main_kernel<D>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 3;
@@ -652,7 +703,7 @@ int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const
   uint8_t* bw = static_cast<uint8_t*>(bwd_ws);
   const int BH = B * H, np = QL.np, nb = np / 128;
   float* dvec = reinterpret_cast<float*>(bw + BL.dvec);
-  float* lse2 = reinterpret_cast<float*>(bw + BL.lse2);
+  float* biasv = reinterpret_cast<float*>(bw + BL.bias);
   float* dopart = reinterpret_cast<float*>(bw + BL.dopart);
   float* sdo = reinterpret_cast<float*>(bw + BL.sdo);
   float* dqacc = reinterpret_cast<float*>(bw + BL.dqacc);
@@ -663,9 +714,9 @@ int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const
   {
   ScopedTimer timer("bwd_pre", st);
   if (D == 128) {
-    bwd_pre_kernel<128><<<g, kPreThreads, 0, st>>>(o, dob, LSE, N, dvec, lse2, dopart, dqacc);
+    bwd_pre_kernel<128><<<g, kPreThreads, 0, st>>>(o, dob, LSE, N, dvec, biasv, dopart, dqacc);
   } else {
-    bwd_pre_kernel<64><<<g, kPreThreads, 0, st>>>(o, dob, LSE, N, dvec, lse2, dopart, dqacc);
+    bwd_pre_kernel<64><<<g, kPreThreads, 0, st>>>(o, dob, LSE, N, dvec, biasv, dopart, dqacc);
   }
   bwd_docomb_kernel<<<BH, 128, 0, st>>>(dopart, D, nb, sdo);
   if (D == 128)
@@ -692,7 +743,7 @@ int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const
   p.sq = reinterpret_cast<const float*>(w + QL.sq);
   p.sk = reinterpret_cast<const float*>(w + QL.sk);
   p.sdo = sdo;
-  p.lse2 = lse2;
+  p.bias = biasv;
   p.dvec = dvec;
   p.K = static_cast<const __nv_bfloat16*>(K);
   p.kr = reinterpret_cast<const float*>(w + QL.kr);
@@ -706,14 +757,11 @@ int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const
   const float* qr = reinterpret_cast<const float*>(w + QL.qr);
   auto* q = static_cast<const __nv_bfloat16*>(Q);
   auto* dq = static_cast<__nv_bfloat16*>(dQ);
-  constexpr int rpp128 = kPreThreads / 16, rpp64 = kPreThreads / 8;
   ScopedTimer timer("bwd_dq", st);
   if (D == 128)
-    bwd_dq_kernel<128><<<dim3((N + rpp128 - 1) / rpp128, BH), kPreThreads, 0, st>>>(dqacc, q, qr, N, np, qk_norm,
-                                                                                      sm_scale, dq);
+    bwd_dq_kernel<128><<<dim3(np / 64, BH), kPreThreads, 0, st>>>(dqacc, q, qr, N, np, qk_norm, sm_scale, dq);
   else
-    bwd_dq_kernel<64><<<dim3((N + rpp64 - 1) / rpp64, BH), kPreThreads, 0, st>>>(dqacc, q, qr, N, np, qk_norm,
-                                                                                   sm_scale, dq);
+    bwd_dq_kernel<64><<<dim3(np / 64, BH), kPreThreads, 0, st>>>(dqacc, q, qr, N, np, qk_norm, sm_scale, dq);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 

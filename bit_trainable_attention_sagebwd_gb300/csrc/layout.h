@@ -42,12 +42,13 @@ inline QuantWs quant_ws_layout(int B, int H, int N, int D) {
 }
 
 struct BwdWs {
-  size_t dvec, lse2, do8t, sdo, dopart, dqacc, total;
+  size_t dvec, bias, do8t, sdo, dopart, dqacc, total;
   int np;
 };
 
-// backward scratch: D_i, LSE*log2(e) (+inf on padded rows), FP8 dO codes
+// backward scratch: D_i, log2(448) - LSE*log2(e) (-inf on padded rows), FP8 dO codes
 // (channel-major), their channel scales and partial maxima, fp32 dQ accumulator
+// (feature-major [BH, D, Np] so that reductions from query rows coalesce)
 inline BwdWs bwd_ws_layout(int B, int H, int N, int D) {
   BwdWs L{};
   const size_t bh = (size_t)B * H;
@@ -55,7 +56,7 @@ inline BwdWs bwd_ws_layout(int B, int H, int N, int D) {
   const size_t nb = np / 128;
   size_t o = 0;
   L.dvec = o;   o = align256(o + bh * np * 4);
-  L.lse2 = o;   o = align256(o + bh * np * 4);
+  L.bias = o;   o = align256(o + bh * np * 4);
   L.do8t = o;   o = align256(o + bh * D * np);
   L.sdo = o;    o = align256(o + bh * D * 4);
   L.dopart = o; o = align256(o + bh * nb * D * 4);

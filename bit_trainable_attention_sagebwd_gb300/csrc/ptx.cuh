@@ -11,7 +11,7 @@
 namespace sage {
 
 // device-side status codes (kept in the workspace header word)
-enum : int { kDevOk = 0, kDevTimeout = 4 };
+enum : int { kDevOk = 0, kDevTimeout = 4, kDevSetup = 5 };
 
 // Wall-clock budget of one wait; generous next to any single tile of work.
 #ifndef SAGE_WAIT_NS
@@ -90,6 +90,13 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
       "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
       : "memory");
+}
+// plain bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16)
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
 }
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
