@@ -364,9 +364,13 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
     for (int d = 0; d < DH; ++d) dk[d] = 0.f;
     bool ok = true;
+    float sq_next = prm.sq[(size_t)bh * prm.nqb + I0];
     for (int it = 0; it < n_it; ++it) {
       const int I = I0 + it;
       const uint32_t ph = it & 1;
+      // the query block's scale was fetched an iteration early (global latency off the path)
+      const float sqI = sq_next;
+      if (it + 1 < n_it) sq_next = prm.sq[(size_t)bh * prm.nqb + I + 1];
       const int qs = it & 1;
       const float* s_bias = sm.bias[qs];
       const float* s_dvec = sm.dvec[qs];
@@ -374,7 +378,6 @@ __global__ void __launch_bounds__(384, 1)
         ok = false;
         break;
       }
-      const float sqI = prm.sq[(size_t)bh * prm.nqb + I];
       const float cs = __fmul_rn(__fmul_rn(sqI, sk_mine), prm.alpha);
       const bool diag = prm.causal && I == kb;
       if (!mbar_wait(&sm.bar_sdp, ph, abort)) {
@@ -389,6 +392,10 @@ __global__ void __launch_bounds__(384, 1)
       float amax = 0.f;
       {
         uint32_t bufA[32], bufB[32];
+        // rows of padded keys and the causal diagonal block need a mask; warps with
+        // neither take the unmasked path
+        const bool any_mask = __any_sync(0xffffffffu, !key_ok || diag);
+        const int mask_lim = !key_ok ? 128 : (diag ? t : 0);  // queries qi < mask_lim are masked
         auto p_chunk = [&](const uint32_t (&sv)[32], int c) {
           uint32_t pw[8];
 #pragma unroll
@@ -397,11 +404,11 @@ __global__ void __launch_bounds__(384, 1)
             const float4 b4 = *reinterpret_cast<const float4*>(&s_bias[qcol + 32 * c + e]);
             const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int qi = (int)qcol + 32 * c + e + u;
-              float v = ex2(fmaf(__uint_as_float(sv[e + u]), cs, bb[u]));
-              if (!key_ok || (diag && qi < t)) v = 0.f;
-              p[u] = v;
+            for (int u = 0; u < 4; ++u) p[u] = ex2(fmaf(__uint_as_float(sv[e + u]), cs, bb[u]));
+            if (any_mask) {
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                if ((int)qcol + 32 * c + e + u < mask_lim) p[u] = 0.f;
             }
             const __nv_fp8x2_storage_t lo =
                 __nv_cvt_float2_to_fp8x2(make_float2(p[0], p[1]), __NV_SATFINITE, __NV_E4M3);

@@ -174,7 +174,9 @@ __global__ void kcombine_kernel(const double* __restrict__ kpart, const float* _
   sv[(size_t)bh * D + d] = m > 0.f ? __fdiv_rn(m, 448.0f) : 0.f;
 }
 
-// quantize: per (head, 128-token block).
+// quantize: per (head, 128-token block, tensor): blockIdx.z = 0 for Q, 1 for K, 2 for V.
+// Each thread issues all of its 128-bit loads before any arithmetic (values stay
+// packed bf16 until used) so that a CTA keeps a whole 32 KB block in flight.
 template <int D>
 __global__ void __launch_bounds__(kThreads) quantize_kernel(
     const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K,
@@ -183,7 +185,7 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(
     uint8_t* __restrict__ v8t, float* __restrict__ sq, float* __restrict__ sk, float* __restrict__ qr,
     float* __restrict__ kr, int* __restrict__ status) {
   constexpr int TPR = D / 8, RPP = kThreads / TPR, PASSES = 128 / RPP;
-  const int blk = blockIdx.x, bh = blockIdx.y, nb = gridDim.x, np = nb * 128;
+  const int blk = blockIdx.x, bh = blockIdx.y, which = blockIdx.z, nb = gridDim.x, np = nb * 128;
   const int tid = threadIdx.x, g = tid % TPR, ro = tid / TPR, warp = tid >> 5, lane = tid & 31;
   const size_t head = (size_t)bh * N * D;
   const size_t phead = (size_t)bh * np * D;
@@ -191,67 +193,73 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(
   // V codes transposed: row d holds the block's 128 tokens; 4-byte groups are
   // permuted by (d / 8) so the byte stores of one warp fall in distinct banks
   __shared__ __align__(16) uint8_t s_v8[D][128];
-  if (blk == 0 && bh == 0 && tid == 0) *status = 0;
+  if (blk == 0 && bh == 0 && which == 0 && tid == 0) *status = 0;
 
-  float x[PASSES][8];
-  // ---- Q: optional norm, block max, codes
-  float amax = 0.f;
+  const __nv_bfloat16* src = which == 0 ? Q : (which == 1 ? K : V);
+  uint4 raw[PASSES];
 #pragma unroll
   for (int p = 0; p < PASSES; ++p) {
     const int t = blk * 128 + p * RPP + ro;
-    uint4 u = make_uint4(0, 0, 0, 0);
-    if (t < N) u = __ldg(reinterpret_cast<const uint4*>(Q + head + (size_t)t * D) + g);
-    unpack8(u, x[p]);
-    float r = 1.f;
-    if (qk_norm) {
-      r = inv_norm<TPR>(x[p]);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) x[p][i] = __fmul_rn(x[p][i], r);
-    }
-    if (g == 0) qr[(size_t)bh * np + blk * 128 + p * RPP + ro] = r;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[p][i]));
+    raw[p] = t < N ? __ldg(reinterpret_cast<const uint4*>(src + head + (size_t)t * D) + g) : make_uint4(0, 0, 0, 0);
   }
-  amax = warp_max(amax);
-  if (lane == 0) s_red[0][warp] = amax;
-  __syncthreads();
-  amax = 0.f;
-#pragma unroll
-  for (int w = 0; w < kThreads / 32; ++w) amax = fmaxf(amax, s_red[0][w]);
-  const float s_q = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 0.f;
-  if (tid == 0) sq[(size_t)bh * nb + blk] = s_q;
-#pragma unroll
-  for (int p = 0; p < PASSES; ++p) {
-    float c[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) c[i] = (float)int8_code(x[p][i], s_q);
-    reinterpret_cast<uint4*>(qc + phead + (size_t)(blk * 128 + p * RPP + ro) * D)[g] = pack8_bf16(c);
-  }
-  __syncthreads();
 
-  // ---- K: optional norm, minus channel mean, two 64-token block maxima, codes
+  if (which == 2) {
+    // ---- V: e4m3 codes with channel scales, transposed through shared memory
+    float svv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) svv[i] = sv[(size_t)bh * D + g * 8 + i];
+#pragma unroll
+    for (int p = 0; p < PASSES; ++p) {
+      const int row = p * RPP + ro;
+      float v[8];
+      unpack8(raw[p], v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float y = svv[i] > 0.f ? __fdiv_rn(v[i], svv[i]) : 0.f;
+        const int d = g * 8 + i;
+        // round to nearest even, saturating to +-448
+        s_v8[d][row ^ (((d >> 3) & 15) << 2)] = __nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3);
+      }
+    }
+    __syncthreads();
+    // D rows of 128 bytes: 16 bytes per thread per step
+    for (int idx = tid; idx < D * 8; idx += kThreads) {
+      const int d = idx >> 3, c = idx & 7, f = ((d >> 3) & 15) << 2;
+      uint4 val;
+      val.x = *reinterpret_cast<const uint32_t*>(&s_v8[d][(c * 16 + 0) ^ f]);
+      val.y = *reinterpret_cast<const uint32_t*>(&s_v8[d][(c * 16 + 4) ^ f]);
+      val.z = *reinterpret_cast<const uint32_t*>(&s_v8[d][(c * 16 + 8) ^ f]);
+      val.w = *reinterpret_cast<const uint32_t*>(&s_v8[d][(c * 16 + 12) ^ f]);
+      reinterpret_cast<uint4*>(v8t + ((size_t)bh * D + d) * np + blk * 128)[c] = val;
+    }
+    return;
+  }
+
+  // ---- Q (which == 0): optional norm, one 128-token block max;
+  //      K (which == 1): optional norm, minus the channel mean, two 64-token block maxima
+  const bool isk = which == 1;
   float km[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) km[i] = k_smooth ? kmean[(size_t)bh * D + g * 8 + i] : 0.f;
+  for (int i = 0; i < 8; ++i) km[i] = (isk && k_smooth) ? kmean[(size_t)bh * D + g * 8 + i] : 0.f;
+  float* rout = isk ? kr : qr;
+  float x[PASSES][8];
   float am[2] = {0.f, 0.f};
 #pragma unroll
   for (int p = 0; p < PASSES; ++p) {
     const int t = blk * 128 + p * RPP + ro;
-    uint4 u = make_uint4(0, 0, 0, 0);
-    if (t < N) u = __ldg(reinterpret_cast<const uint4*>(K + head + (size_t)t * D) + g);
-    unpack8(u, x[p]);
+    unpack8(raw[p], x[p]);
     float r = 1.f;
     if (qk_norm) {
       r = inv_norm<TPR>(x[p]);
 #pragma unroll
       for (int i = 0; i < 8; ++i) x[p][i] = __fmul_rn(x[p][i], r);
     }
-    if (g == 0) kr[(size_t)bh * np + blk * 128 + p * RPP + ro] = r;
-    const int half = (p * RPP + ro) >= 64;
+    if (g == 0) rout[(size_t)bh * np + blk * 128 + p * RPP + ro] = r;
+    const int hsel = isk && (p * RPP + ro) >= 64;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      x[p][i] = (t < N) ? (k_smooth ? __fsub_rn(x[p][i], km[i]) : x[p][i]) : 0.f;
-      am[half] = fmaxf(am[half], fabsf(x[p][i]));
+      if (isk) x[p][i] = (t < N) ? (k_smooth ? __fsub_rn(x[p][i], km[i]) : x[p][i]) : 0.f;
+      am[hsel] = fmaxf(am[hsel], fabsf(x[p][i]));
     }
   }
   am[0] = warp_max(am[0]);
@@ -261,53 +269,27 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(
     s_red[1][warp] = am[1];
   }
   __syncthreads();
-  float s_k[2];
+  float sc[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     float a = 0.f;
 #pragma unroll
     for (int w = 0; w < kThreads / 32; ++w) a = fmaxf(a, s_red[h][w]);
-    s_k[h] = a > 0.f ? __fdiv_rn(a, 127.0f) : 0.f;
+    sc[h] = a > 0.f ? __fdiv_rn(a, 127.0f) : 0.f;
   }
-  if (tid < 2) sk[(size_t)bh * nb * 2 + blk * 2 + tid] = s_k[tid];
+  if (!isk) {
+    if (tid == 0) sq[(size_t)bh * nb + blk] = sc[0];
+  } else if (tid < 2) {
+    sk[(size_t)bh * nb * 2 + blk * 2 + tid] = sc[tid];
+  }
+  __nv_bfloat16* dst = isk ? kc : qc;
 #pragma unroll
   for (int p = 0; p < PASSES; ++p) {
-    const float s = s_k[(p * RPP + ro) >= 64];
+    const float s = isk ? sc[(p * RPP + ro) >= 64] : sc[0];
     float c[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) c[i] = (float)int8_code(x[p][i], s);
-    reinterpret_cast<uint4*>(kc + phead + (size_t)(blk * 128 + p * RPP + ro) * D)[g] = pack8_bf16(c);
-  }
-
-  // ---- V: e4m3 codes with channel scales, transposed through shared memory
-  float svv[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) svv[i] = sv[(size_t)bh * D + g * 8 + i];
-#pragma unroll
-  for (int p = 0; p < PASSES; ++p) {
-    const int row = p * RPP + ro, t = blk * 128 + row;
-    uint4 u = make_uint4(0, 0, 0, 0);
-    if (t < N) u = __ldg(reinterpret_cast<const uint4*>(V + head + (size_t)t * D) + g);
-    float v[8];
-    unpack8(u, v);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float y = svv[i] > 0.f ? __fdiv_rn(v[i], svv[i]) : 0.f;
-      const int d = g * 8 + i;
-      // round to nearest even, saturating to +-448
-      s_v8[d][row ^ (((d >> 3) & 15) << 2)] = __nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3);
-    }
-  }
-  __syncthreads();
-  // D rows of 128 bytes: 16 bytes per thread per step
-  for (int idx = tid; idx < D * 8; idx += kThreads) {
-    const int d = idx >> 3, c = idx & 7, f = ((d >> 3) & 15) << 2;
-    uint4 val;
-    val.x = *reinterpret_cast<const uint32_t*>(&s_v8[d][(c * 16 + 0) ^ f]);
-    val.y = *reinterpret_cast<const uint32_t*>(&s_v8[d][(c * 16 + 4) ^ f]);
-    val.z = *reinterpret_cast<const uint32_t*>(&s_v8[d][(c * 16 + 8) ^ f]);
-    val.w = *reinterpret_cast<const uint32_t*>(&s_v8[d][(c * 16 + 12) ^ f]);
-    reinterpret_cast<uint4*>(v8t + ((size_t)bh * D + d) * np + blk * 128)[c] = val;
+    reinterpret_cast<uint4*>(dst + phead + (size_t)(blk * 128 + p * RPP + ro) * D)[g] = pack8_bf16(c);
   }
 }
 
@@ -319,6 +301,7 @@ int launch_quantize(const void* Q, const void* K, const void* V, int B, int H, i
   uint8_t* w = static_cast<uint8_t*>(ws);
   const int nb = L.np / 128;
   const dim3 grid(nb, B * H);
+  const dim3 qgrid(nb, B * H, 3);
   auto* q = static_cast<const __nv_bfloat16*>(Q);
   auto* k = static_cast<const __nv_bfloat16*>(K);
   auto* v = static_cast<const __nv_bfloat16*>(V);
@@ -333,7 +316,7 @@ int launch_quantize(const void* Q, const void* K, const void* V, int B, int H, i
     kstats_kernel<64><<<grid, kThreads, 0, st>>>(k, v, N, qk_norm, kpart, vpart);
   kcombine_kernel<<<B * H, 128, 0, st>>>(kpart, vpart, N, D, nb, k_smooth, kmean, sv);
   auto args = [&](auto kern) {
-    kern<<<grid, kThreads, 0, st>>>(q, k, v, N, qk_norm, k_smooth, kmean, sv,
+    kern<<<qgrid, kThreads, 0, st>>>(q, k, v, N, qk_norm, k_smooth, kmean, sv,
                                     reinterpret_cast<__nv_bfloat16*>(w + L.qc),
                                     reinterpret_cast<__nv_bfloat16*>(w + L.kc), w + L.v8t,
                                     reinterpret_cast<float*>(w + L.sq), reinterpret_cast<float*>(w + L.sk),
