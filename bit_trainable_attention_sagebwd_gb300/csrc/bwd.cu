@@ -22,6 +22,7 @@
 //                dQ_part = dS8 K8      kind::f16 per 64-key half, scaled, fp32 atomics
 //              dV and dK (x sm_scale, through QK-norm) written at the end
 //   bwd_dq     per query row: dQ = sm_scale * acc, through QK-norm, to bf16
+#include <cstddef>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -39,6 +40,10 @@ namespace {
 
 constexpr float kLog2_448 = 8.807354922057604f;
 constexpr int kPreThreads = 256;
+#ifndef SAGE_BWD_GROUPS
+#define SAGE_BWD_GROUPS 2
+#endif
+constexpr int kBwdGroups = SAGE_BWD_GROUPS;  // compute warpgroups of the main backward kernel
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -172,7 +177,7 @@ struct BwdSmem {
   uint8_t ds[128 * 128 * 2]; // dS^T INT8 codes in bf16, key rows
   __align__(16) float bias[2][128];  // log2(448) - LSE_i log2(e), per Q buffer
   __align__(16) float dvec[2][128];  // D_i, per Q buffer
-  float smax[8];
+  float smax[16];
   uint64_t bar_kv;
   uint64_t bar_q_full[2], bar_do_full, bar_do8_full;
   uint64_t bar_q_free[2], bar_do_free, bar_do8_free;
@@ -197,20 +202,23 @@ struct BwdParams {
   int* status;
 };
 
-// the 256 threads of the two compute warpgroups
-__device__ __forceinline__ void named_bar_compute() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// named barrier 1 over the compute warpgroups only
+template <int NWG>
+__device__ __forceinline__ void named_bar_compute() {
+  asm volatile("bar.sync 1, %0;" ::"n"(NWG * 128) : "memory");
+}
 
 constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23: x + M - M rounds x to an integer (ties to even)
 
 // One CTA per (head, 128-key block), looping over the query blocks that see it.
-//   warps 0-3, 4-7 : compute warpgroups g = 0, 1; thread t of a group owns key row t
-//                    (TMEM lane t) and query columns [64g, 64g + 64) of it, and D/2
-//                    of the dK/dQ/dV columns
-//   warp 8 lane 0  : TMA producer;  warp 9 : TMEM allocator, lane 0 issues the UMMAs
+//   warps 0 .. 4*NWG-1 : NWG compute warpgroups; thread t of group g owns key row t (TMEM
+//                        lane t), query columns [QC*g, QC*g + QC) of it (QC = 128/NWG) and
+//                        output columns [DG*g, DG*g + DG) of dK, dQ, dV (DG = D/NWG)
+//   warp 4*NWG lane 0  : TMA producer;  warp 4*NWG+1 : TMEM allocator, lane 0 issues UMMAs
 // TMEM columns: [0,128) S^T, then dK_part; [128,256) dP^T, then dS, then dQ half 0;
 // [256,256+D) dV; [384,384+D) dQ half 1.
-template <int D>
-__global__ void __launch_bounds__(384, 1)
+template <int D, int NWG>
+__global__ void __launch_bounds__((NWG + 1) * 128, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_do8, const BwdParams prm) {
@@ -222,6 +230,10 @@ __global__ void __launch_bounds__(384, 1)
     return;
   }
   BwdSmem<D>& sm = *reinterpret_cast<BwdSmem<D>*>(smem_raw);
+  constexpr int NC = NWG * 128;  // compute threads
+  constexpr int QC = 128 / NWG;  // query columns per compute thread
+  constexpr int DG = D / NWG;    // output columns per compute thread
+  constexpr int WPROD = 4 * NWG, WMMA = 4 * NWG + 1;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int kb = blockIdx.x, bh = blockIdx.y;
   const int I0 = prm.causal ? kb : 0;
@@ -229,7 +241,6 @@ __global__ void __launch_bounds__(384, 1)
   constexpr uint32_t kCols = 512;
   constexpr uint32_t cS = 0, cDP = 128, cDV = 256, cDQB = 384;  // TMEM column bases
   constexpr uint32_t kTile = 128 * D * 2;
-  constexpr int DH = D / 2;  // dK/dQ/dV columns per compute warpgroup
 
   if (tid == 0) {
     mbar_init(&sm.bar_kv, 1);
@@ -242,14 +253,14 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&sm.bar_do_free, 1);
     mbar_init(&sm.bar_do8_free, 1);
     mbar_init(&sm.bar_sdp, 1);
-    mbar_init(&sm.bar_p, 256);
-    mbar_init(&sm.bar_ds, 256);
+    mbar_init(&sm.bar_p, NC);
+    mbar_init(&sm.bar_ds, NC);
     mbar_init(&sm.bar_part, 1);
-    mbar_init(&sm.bar_free, 256);
+    mbar_init(&sm.bar_free, NC);
     sm.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == WMMA) {
     tmem_alloc(&sm.tmem_base, kCols);
     tmem_relinquish();
   }
@@ -258,7 +269,7 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort = &sm.abort;
 
-  if (warp == 8 && lane == 0) {
+  if (warp == WPROD && lane == 0) {
     // ---------------- producer
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_q);
@@ -290,7 +301,7 @@ __global__ void __launch_bounds__(384, 1)
       bulk_load(sm.bias[qs], prm.bias + (size_t)bh * prm.np + I * 128, 512, &sm.bar_q_full[qs]);
       bulk_load(sm.dvec[qs], prm.dvec + (size_t)bh * prm.np + I * 128, 512, &sm.bar_q_full[qs]);
     }
-  } else if (warp == 9 && lane == 0) {
+  } else if (warp == WMMA && lane == 0) {
     // ---------------- UMMA issuer
     constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);   // S^T, dP^T
     constexpr uint32_t id_dv = idesc_e4m3(128, D);                   // dV
@@ -345,7 +356,7 @@ __global__ void __launch_bounds__(384, 1)
       umma_commit(&sm.bar_part);
       umma_commit(&sm.bar_q_free[it & 1]);
     }
-  } else if (warp < 8) {
+  } else if (warp < 4 * NWG) {
     // ---------------- compute: warpgroup g, thread t owns key row t
     const int g = warp >> 2;
     const int t = tid & 127;
@@ -356,13 +367,15 @@ __global__ void __launch_bounds__(384, 1)
     const float* skh = prm.sk + (size_t)bh * prm.nqb * 2;
     const float sk_mine = skh[2 * kb + half];
     const float sk0 = skh[2 * kb], sk1 = skh[2 * kb + 1];
-    const uint32_t qcol = (uint32_t)(64 * g);  // this group's 64 query columns
-    const uint32_t dcol = (uint32_t)(DH * g);  // this group's D/2 output columns
+    const uint32_t qcol = (uint32_t)(QC * g);
+    const uint32_t dcol = (uint32_t)(DG * g);
     uint8_t* prow = sm.p + (t >> 3) * 1024 + (t & 7) * 128;
-    uint8_t* dsrow = sm.ds + g * 16384 + (t >> 3) * 1024 + (t & 7) * 128;
-    float dk[DH];
+    // dS^T row: query columns [qcol, qcol + QC) sit in 64-query block qcol/64, bytes 2*(qcol%64) on
+    uint8_t* dsrow = sm.ds + (qcol >> 6) * 16384 + (t >> 3) * 1024 + (t & 7) * 128;
+    const int ds_u0 = (int)((qcol & 63) * 2) >> 4;  // first 16-byte unit of this group in the row
+    float dk[DG];
 #pragma unroll
-    for (int d = 0; d < DH; ++d) dk[d] = 0.f;
+    for (int d = 0; d < DG; ++d) dk[d] = 0.f;
     bool ok = true;
     float sq_next = prm.sq[(size_t)bh * prm.nqb + I0];
     for (int it = 0; it < n_it; ++it) {
@@ -385,17 +398,17 @@ __global__ void __launch_bounds__(384, 1)
         break;
       }
       tc_fence_after();
-      // ---- P^T = e4m3(448 * 2^(S2 - LSE2)) and dS^T * 448 = p8 (dP^T - D) for query columns
-      // [qcol, qcol + 64), in 32-column chunks.  TMEM loads are software-pipelined: the next
-      // chunk's load is issued before the current chunk is processed (wait::ld waits for all
-      // of this thread's loads, so each wait then covers a load that overlapped compute).
+      // rows of padded keys and the causal diagonal block need a mask; warps with
+      // neither take the unmasked path
+      const bool any_mask = __any_sync(0xffffffffu, !key_ok || diag);
+      const int mask_lim = !key_ok ? 128 : (diag ? t : 0);  // queries qi < mask_lim are masked
+      // ---- P^T = e4m3(448 * 2^(S2 - LSE2)) and dS^T * 448 = p8 (dP^T - D) on this thread's
+      // query columns, 32 at a time.  TMEM loads are software-pipelined: the next chunk's load
+      // is issued before the current chunk is processed (wait::ld waits for all of this
+      // thread's loads, so each wait covers a load that overlapped compute).
       float amax = 0.f;
       {
         uint32_t bufA[32], bufB[32];
-        // rows of padded keys and the causal diagonal block need a mask; warps with
-        // neither take the unmasked path
-        const bool any_mask = __any_sync(0xffffffffu, !key_ok || diag);
-        const int mask_lim = !key_ok ? 128 : (diag ? t : 0);  // queries qi < mask_lim are masked
         auto p_chunk = [&](const uint32_t (&sv)[32], int c) {
           uint32_t pw[8];
 #pragma unroll
@@ -416,12 +429,12 @@ __global__ void __launch_bounds__(384, 1)
                 __nv_cvt_float2_to_fp8x2(make_float2(p[2], p[3]), __NV_SATFINITE, __NV_E4M3);
             pw[e >> 2] = (uint32_t)lo | ((uint32_t)hi << 16);
           }
-          const int u0 = 4 * g + 2 * c;  // 16-byte units of this chunk in the 128-byte row
+          const int u0 = (int)(qcol >> 4) + 2 * c;  // 16-byte units of this chunk in the 128-byte row
           *reinterpret_cast<uint4*>(prow + ((u0 ^ (t & 7)) << 4)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
           *reinterpret_cast<uint4*>(prow + (((u0 + 1) ^ (t & 7)) << 4)) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
         };
         auto ds_chunk = [&](uint32_t (&dv)[32], int c) {
-          const int u0 = 4 * g + 2 * c;
+          const int u0 = (int)(qcol >> 4) + 2 * c;
           const uint4 pa = *reinterpret_cast<const uint4*>(prow + ((u0 ^ (t & 7)) << 4));
           const uint4 pb = *reinterpret_cast<const uint4*>(prow + (((u0 + 1) ^ (t & 7)) << 4));
           const uint32_t pw[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
@@ -439,37 +452,53 @@ __global__ void __launch_bounds__(384, 1)
           }
           tmem_st32(tmem + lane_base + cDP + qcol + 32 * c, dv);
         };
-        tmem_ld32(tmem + lane_base + cS + qcol, bufA);
-        tmem_wait32(bufA);
-        tmem_ld32(tmem + lane_base + cS + qcol + 32, bufB);
-        p_chunk(bufA, 0);
-        tmem_wait32(bufB);
-        tmem_ld32(tmem + lane_base + cDP + qcol, bufA);
-        p_chunk(bufB, 1);
-        fence_proxy_async_smem();
-        mbar_arrive(&sm.bar_p);
-        tmem_wait32(bufA);
-        tmem_ld32(tmem + lane_base + cDP + qcol + 32, bufB);
-        ds_chunk(bufA, 0);
-        tmem_wait32(bufB);
-        ds_chunk(bufB, 1);
+        if constexpr (QC == 64) {
+          tmem_ld32(tmem + lane_base + cS + qcol, bufA);
+          tmem_wait32(bufA);
+          tmem_ld32(tmem + lane_base + cS + qcol + 32, bufB);
+          p_chunk(bufA, 0);
+          tmem_wait32(bufB);
+          tmem_ld32(tmem + lane_base + cDP + qcol, bufA);
+          p_chunk(bufB, 1);
+          fence_proxy_async_smem();
+          mbar_arrive(&sm.bar_p);
+          tmem_wait32(bufA);
+          tmem_ld32(tmem + lane_base + cDP + qcol + 32, bufB);
+          ds_chunk(bufA, 0);
+          tmem_wait32(bufB);
+          ds_chunk(bufB, 1);
+        } else {
+          tmem_ld32(tmem + lane_base + cS + qcol, bufA);
+          tmem_wait32(bufA);
+          tmem_ld32(tmem + lane_base + cDP + qcol, bufB);
+          p_chunk(bufA, 0);
+          fence_proxy_async_smem();
+          mbar_arrive(&sm.bar_p);
+          tmem_wait32(bufB);
+          ds_chunk(bufB, 0);
+        }
         tmem_st_wait();
       }
 #pragma unroll
       for (int m = 16; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
       if (lane == 0) sm.smax[warp] = amax;
-      named_bar_compute();
-      // tile max over the 64 key rows of each half and all 128 queries (both groups)
-      const float a0 = fmaxf(fmaxf(sm.smax[0], sm.smax[1]), fmaxf(sm.smax[4], sm.smax[5]));
-      const float a1 = fmaxf(fmaxf(sm.smax[2], sm.smax[3]), fmaxf(sm.smax[6], sm.smax[7]));
+      named_bar_compute<NWG>();
+      // tile max over the 64 key rows of each half and all 128 queries (every group)
+      float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+      for (int w = 0; w < 4 * NWG; ++w) {
+        if ((w & 3) < 2)
+          a0 = fmaxf(a0, sm.smax[w]);
+        else
+          a1 = fmaxf(a1, sm.smax[w]);
+      }
       // values are 448 * dS: scale s_dS = max|dS| / 127
       const float sds0 = a0 > 0.f ? __fdiv_rn(a0 * (1.0f / 448.0f), 127.0f) : 0.f;
       const float sds1 = a1 > 0.f ? __fdiv_rn(a1 * (1.0f / 448.0f), 127.0f) : 0.f;
       const float amine = half ? a1 : a0;
       const float inv = amine > 0.f ? 127.0f / amine : 0.f;  // code = rint(448 dS * 127 / max|448 dS|)
-      // ---- dS^T codes -> shared memory (bf16 containers, 128B-swizzled key rows, block g)
+      // ---- dS^T codes -> shared memory (bf16 containers, 128B-swizzled key rows)
       {
-        uint32_t bufA[32], bufB[32];
         auto code_chunk = [&](const uint32_t (&dv)[32], int c) {
           uint32_t packed[16];
 #pragma unroll
@@ -483,15 +512,22 @@ __global__ void __launch_bounds__(384, 1)
           }
 #pragma unroll
           for (int u = 0; u < 4; ++u)
-            *reinterpret_cast<uint4*>(dsrow + (((4 * c + u) ^ (t & 7)) << 4)) =
+            *reinterpret_cast<uint4*>(dsrow + (((ds_u0 + 4 * c + u) ^ (t & 7)) << 4)) =
                 make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
         };
-        tmem_ld32(tmem + lane_base + cDP + qcol, bufA);
-        tmem_wait32(bufA);
-        tmem_ld32(tmem + lane_base + cDP + qcol + 32, bufB);
-        code_chunk(bufA, 0);
-        tmem_wait32(bufB);
-        code_chunk(bufB, 1);
+        uint32_t bufA[32], bufB[32];
+        if constexpr (QC == 64) {
+          tmem_ld32(tmem + lane_base + cDP + qcol, bufA);
+          tmem_wait32(bufA);
+          tmem_ld32(tmem + lane_base + cDP + qcol + 32, bufB);
+          code_chunk(bufA, 0);
+          tmem_wait32(bufB);
+          code_chunk(bufB, 1);
+        } else {
+          tmem_ld32(tmem + lane_base + cDP + qcol, bufA);
+          tmem_wait32(bufA);
+          code_chunk(bufA, 0);
+        }
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -502,7 +538,7 @@ __global__ void __launch_bounds__(384, 1)
       }
       tc_fence_after();
       // ---- dK += RN(s_dS * s_q) * part;  dQ (query row t of block I) += ca * half0 + cb * half1
-      // (this group's D/2 columns), TMEM loads pipelined as above
+      // (this group's DG columns), TMEM loads pipelined as above
       const float ck = __fmul_rn(half ? sds1 : sds0, sqI);
       const float ca = __fmul_rn(sds0, sk0), cb = __fmul_rn(sds1, sk1);
       const int qrow = I * 128 + t;
@@ -515,15 +551,15 @@ __global__ void __launch_bounds__(384, 1)
         tmem_ld16(tmem + lane_base + cS + dcol, kA);
         tmem_wait16(kA);
 #pragma unroll
-        for (int c = 0; c < DH; c += 32) {
+        for (int c = 0; c < DG; c += 32) {
           tmem_ld16(tmem + lane_base + cS + dcol + c + 16, kB);
 #pragma unroll
           for (int e = 0; e < 16; ++e) dk[c + e] = fmaf(ck, __uint_as_float(kA[e]), dk[c + e]);
           tmem_wait16(kB);
-          if (c + 32 < DH) tmem_ld16(tmem + lane_base + cS + dcol + c + 32, kA);
+          if (c + 32 < DG) tmem_ld16(tmem + lane_base + cS + dcol + c + 32, kA);
 #pragma unroll
           for (int e = 0; e < 16; ++e) dk[c + 16 + e] = fmaf(ck, __uint_as_float(kB[e]), dk[c + 16 + e]);
-          if (c + 32 < DH) tmem_wait16(kA);
+          if (c + 32 < DG) tmem_wait16(kA);
         }
       }
       {
@@ -534,9 +570,9 @@ __global__ void __launch_bounds__(384, 1)
         reg_fence16(va[0]);
         reg_fence16(vb[0]);
 #pragma unroll
-        for (int c = 0; c < DH; c += 16) {
+        for (int c = 0; c < DG; c += 16) {
           const int cur = (c >> 4) & 1;
-          if (c + 16 < DH) {
+          if (c + 16 < DG) {
             tmem_ld16(tmem + lane_base + cDP + dcol + c + 16, va[cur ^ 1]);
             tmem_ld16(tmem + lane_base + cDQB + dcol + c + 16, vb[cur ^ 1]);
           } else {
@@ -550,7 +586,7 @@ __global__ void __launch_bounds__(384, 1)
               atomicAdd(dst + (size_t)(c + e) * prm.np,
                         fmaf(ca, __uint_as_float(va[cur][e]), cb * __uint_as_float(vb[cur][e])));
           }
-          if (c + 16 < DH) {
+          if (c + 16 < DG) {
             tmem_ld_wait();
             reg_fence16(va[cur ^ 1]);
             reg_fence16(vb[cur ^ 1]);
@@ -558,37 +594,40 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
     }
-    // ---------------- epilogue: dV and dK rows of this key block, this group's columns
+    // ---------------- epilogue: dK then dV rows of this key block, this group's columns
     if (ok) {
       tc_fence_after();
       const size_t orow = ((size_t)bh * prm.N + key) * D;
 #pragma unroll
-      for (int d = 0; d < DH; ++d) dk[d] *= prm.sm_scale;
-      float r = 0.f;
+      for (int d = 0; d < DG; ++d) dk[d] *= prm.sm_scale;
       const uint4* krow = reinterpret_cast<const uint4*>(prm.K + orow + dcol);
       if (prm.qk_norm) {
-        // dk = r (dk' - k' (k' . dk')), k' = RN(k r): the dot spans both groups' columns
-        r = key_ok ? prm.kr[(size_t)bh * prm.np + key] : 0.f;
+        // dk = r (dk' - k' (k' . dk')), k' = RN(k r): the dot spans every group's columns
+        const float r = key_ok ? prm.kr[(size_t)bh * prm.np + key] : 0.f;
         float dot = 0.f;
         if (key_ok) {
 #pragma unroll
-          for (int c = 0; c < DH / 8; ++c) {
+          for (int c = 0; c < DG / 8; ++c) {
             float f[8];
             unpack8(__ldg(krow + c), f);
 #pragma unroll
             for (int e = 0; e < 8; ++e) dot = fmaf(__fmul_rn(f[e], r), dk[c * 8 + e], dot);
           }
         }
-        // add the two groups' partial dot products through the (now idle) per-query rows
-        named_bar_compute();
-        if (g == 1) sm.dvec[0][t] = dot;
-        named_bar_compute();
-        if (g == 0) sm.bias[0][t] = dot + sm.dvec[0][t];
-        named_bar_compute();
-        dot = sm.bias[0][t];
+        // partial dot products through the (now idle) per-query rows: bias and dvec are
+        // adjacent, 4 x 128 floats in all
+        static_assert(offsetof(BwdSmem<D>, dvec) == offsetof(BwdSmem<D>, bias) + sizeof(sm.bias) && NWG <= 4,
+                      "exchange buffer layout");
+        float* xch = &sm.bias[0][0];
+        named_bar_compute<NWG>();
+        xch[g * 128 + t] = dot;
+        named_bar_compute<NWG>();
+        dot = 0.f;
+#pragma unroll
+        for (int q = 0; q < NWG; ++q) dot += xch[q * 128 + t];
         if (key_ok) {
 #pragma unroll
-          for (int c = 0; c < DH / 8; ++c) {
+          for (int c = 0; c < DG / 8; ++c) {
             float f[8];
             unpack8(__ldg(krow + c), f);
 #pragma unroll
@@ -597,26 +636,26 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       if (key_ok) {
-        uint4* dst = reinterpret_cast<uint4*>(prm.dK + orow + dcol);
+        uint4* dstk = reinterpret_cast<uint4*>(prm.dK + orow + dcol);
 #pragma unroll
-        for (int c = 0; c < DH / 8; ++c) {
+        for (int c = 0; c < DG / 8; ++c) {
           uint4 u;
           __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
 #pragma unroll
           for (int e = 0; e < 4; ++e) h[e] = __floats2bfloat162_rn(dk[c * 8 + 2 * e], dk[c * 8 + 2 * e + 1]);
-          dst[c] = u;
+          dstk[c] = u;
         }
       }
       const float* sdoh = prm.sdo + (size_t)bh * D;
 #pragma unroll
-      for (int c = 0; c < DH; c += 32) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_base + cDV + dcol + c, v);
-        tmem_wait32(v);
+      for (int c = 0; c < DG; c += 16) {
+        uint32_t v[16];
+        tmem_ld16(tmem + lane_base + cDV + dcol + c, v);
+        tmem_wait16(v);
         if (key_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(prm.dV + orow + dcol + c);
+          uint4* dstv = reinterpret_cast<uint4*>(prm.dV + orow + dcol + c);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
+          for (int i = 0; i < 2; ++i) {
             uint4 u;
             __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
 #pragma unroll
@@ -625,7 +664,7 @@ __global__ void __launch_bounds__(384, 1)
               h[e] = __floats2bfloat162_rn(__uint_as_float(v[8 * i + 2 * e]) * (sdoh[d0] * (1.0f / 448.0f)),
                                            __uint_as_float(v[8 * i + 2 * e + 1]) * (sdoh[d0 + 1] * (1.0f / 448.0f)));
             }
-            dst[i] = u;
+            dstv[i] = u;
           }
         }
       }
@@ -633,7 +672,7 @@ __global__ void __launch_bounds__(384, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) tmem_dealloc(tmem, kCols);
+  if (warp == WMMA) tmem_dealloc(tmem, kCols);
   if (tid == 0 && sm.abort) atomicExch(prm.status, kDevTimeout);
 }
 
@@ -686,15 +725,15 @@ __global__ void __launch_bounds__(kPreThreads) bwd_dq_kernel(const float* __rest
   }
 }
 
-template <int D>
+template <int D, int NWG>
 int launch_main_t(const CUtensorMap& tk, const CUtensorMap& tq, const CUtensorMap& tv, const CUtensorMap& tdo,
                   const CUtensorMap& tdo8, const BwdParams& p, int BH, cudaStream_t st) {
   size_t smem = sizeof(BwdSmem<D>);
   if (smem < 120 * 1024) smem = 120 * 1024;  // one CTA per SM: it holds all 512 TMEM columns
-  auto kern = bwd_main_kernel<D>;
+  auto kern = bwd_main_kernel<D, NWG>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 3;
   ScopedTimer timer("bwd_main", st);
-  kern<<<dim3(p.nqb, BH), 384, smem, st>>>(tk, tq, tv, tdo, tdo8, p);
+  kern<<<dim3(p.nqb, BH), (NWG + 1) * 128, smem, st>>>(tk, tq, tv, tdo, tdo8, p);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 
@@ -758,8 +797,8 @@ int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const
   p.dK = static_cast<__nv_bfloat16*>(dK);
   p.dV = static_cast<__nv_bfloat16*>(dV);
   p.status = reinterpret_cast<int*>(const_cast<uint8_t*>(w) + QL.status);
-  int rc = D == 128 ? launch_main_t<128>(tk, tq, tv, tdo, tdo8, p, BH, st)
-                    : launch_main_t<64>(tk, tq, tv, tdo, tdo8, p, BH, st);
+  int rc = D == 128 ? launch_main_t<128, kBwdGroups>(tk, tq, tv, tdo, tdo8, p, BH, st)
+                    : launch_main_t<64, kBwdGroups>(tk, tq, tv, tdo, tdo8, p, BH, st);
   if (rc) return rc;
   const float* qr = reinterpret_cast<const float*>(w + QL.qr);
   auto* q = static_cast<const __nv_bfloat16*>(Q);
