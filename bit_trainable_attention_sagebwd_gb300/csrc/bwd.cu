@@ -19,7 +19,8 @@
 //                dV  += P8^T dO8       kind::f8f6f4
 //                dS  -> INT8, one scale per (128 query x 64 key) tile
 //                dK_part = dS8^T Q8    kind::f16, scaled per tile, summed in registers
-//                dQ_part = dS8 K8      kind::f16 per 64-key half, scaled, fp32 atomics
+//                dQ_part = dS8 K8      kind::f16 per 64-key half, scaled, staged in shared
+//                                      memory and added to the fp32 accumulator by TMA reduce
 //              dV and dK (x sm_scale, through QK-norm) written at the end
 //   bwd_dq     per query row: dQ = sm_scale * acc, through QK-norm, to bf16
 #include <cstddef>
@@ -207,6 +208,10 @@ template <int NWG>
 __device__ __forceinline__ void named_bar_compute() {
   asm volatile("bar.sync 1, %0;" ::"n"(NWG * 128) : "memory");
 }
+// named barrier 2 + g over compute warpgroup g
+__device__ __forceinline__ void named_bar_group(int g) {
+  asm volatile("bar.sync %0, 128;" ::"r"(2 + g) : "memory");
+}
 
 constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23: x + M - M rounds x to an integer (ties to even)
 
@@ -217,11 +222,16 @@ constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23: x + M - M rounds x to
 //   warp 4*NWG lane 0  : TMA producer;  warp 4*NWG+1 : TMEM allocator, lane 0 issues UMMAs
 // TMEM columns: [0,128) S^T, then dK_part; [128,256) dP^T, then dS, then dQ half 0;
 // [256,256+D) dV; [384,384+D) dQ half 1.
+// dQ staging: each group writes its scaled dQ part as [32 features][128 queries] fp32
+// boxes (16 KB) into shared memory the next MMAs do not read: the dS^T blocks, then the
+// halves of the Q buffer just consumed; one thread per group adds them to the feature-major
+// accumulator with TMA reduce and, once the boxes are read, frees the Q buffer.
 template <int D, int NWG>
 __global__ void __launch_bounds__((NWG + 1) * 128, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const __grid_constant__ CUtensorMap tm_do8, const BwdParams prm) {
+                    const __grid_constant__ CUtensorMap tm_do8, const __grid_constant__ CUtensorMap tm_dq,
+                    const BwdParams prm) {
   // the tile buffers need 1024-byte alignment (128-byte swizzle atoms); the layout
   // fills almost all of the 227 KB, so the base is used as is and checked
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -248,8 +258,8 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
     mbar_init(&sm.bar_q_full[1], 1);
     mbar_init(&sm.bar_do_full, 1);
     mbar_init(&sm.bar_do8_full, 1);
-    mbar_init(&sm.bar_q_free[0], 1);
-    mbar_init(&sm.bar_q_free[1], 1);
+    mbar_init(&sm.bar_q_free[0], NWG);  // one arrival per group once its dQ boxes are read
+    mbar_init(&sm.bar_q_free[1], NWG);
     mbar_init(&sm.bar_do_free, 1);
     mbar_init(&sm.bar_do8_free, 1);
     mbar_init(&sm.bar_sdp, 1);
@@ -276,6 +286,7 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_do);
     tma_prefetch_desc(&tm_do8);
+    tma_prefetch_desc(&tm_dq);
     mbar_arrive_expect_tx(&sm.bar_kv, 2 * kTile);
 #pragma unroll
     for (int c = 0; c < D / 64; ++c) {
@@ -354,7 +365,6 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
         umma_bf16(tmem + cDQB, sdesc_sw128(a_ds + kk * 2048, 16384, 1024),
                   sdesc_sw128(a_k + kk * 2048, 16384, 1024), id_dq, kk > 4);
       umma_commit(&sm.bar_part);
-      umma_commit(&sm.bar_q_free[it & 1]);
     }
   } else if (warp < 4 * NWG) {
     // ---------------- compute: warpgroup g, thread t owns key row t
@@ -376,6 +386,8 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
     float dk[DG];
 #pragma unroll
     for (int d = 0; d < DG; ++d) dk[d] = 0.f;
+    static_assert(NWG * (DG / 32) <= 4 && DG % 32 == 0, "dQ staging slots");
+    int pending_qs = -1;  // Q buffer whose dQ boxes are still being read by TMA (elected thread)
     bool ok = true;
     float sq_next = prm.sq[(size_t)bh * prm.nqb + I0];
     for (int it = 0; it < n_it; ++it) {
@@ -482,6 +494,13 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
 #pragma unroll
       for (int m = 16; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
       if (lane == 0) sm.smax[warp] = amax;
+      // the previous iteration's dQ boxes must be read before dS^T is rewritten below and
+      // before the producer refills that Q buffer
+      if (t == 0 && pending_qs >= 0) {
+        bulk_wait_read_all();
+        mbar_arrive(&sm.bar_q_free[pending_qs]);
+        pending_qs = -1;
+      }
       named_bar_compute<NWG>();
       // tile max over the 64 key rows of each half and all 128 queries (every group)
       float a0 = 0.f, a1 = 0.f;
@@ -541,11 +560,6 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
       // (this group's DG columns), TMEM loads pipelined as above
       const float ck = __fmul_rn(half ? sds1 : sds0, sqI);
       const float ca = __fmul_rn(sds0, sk0), cb = __fmul_rn(sds1, sk1);
-      const int qrow = I * 128 + t;
-      const bool q_ok = qrow < prm.N;
-      // feature-major accumulator: the 32 lanes of a warp add 32 consecutive queries of
-      // one feature, one 128-byte line per reduction instruction
-      float* dst = prm.dqacc + ((size_t)bh * D + dcol) * prm.np + qrow;
       {
         uint32_t kA[16], kB[16];
         tmem_ld16(tmem + lane_base + cS + dcol, kA);
@@ -563,6 +577,11 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
         }
       }
       {
+        // staging slot of box b (features dcol + 32b ..): 0,1 -> dS^T blocks, 2,3 -> halves of q[qs]
+        auto slot = [&](int b) -> float* {
+          const int sidx = g * (DG / 32) + b;
+          return reinterpret_cast<float*>(sidx < 2 ? sm.ds + sidx * 16384 : sm.q[qs] + (sidx - 2) * 16384);
+        };
         uint32_t va[2][16], vb[2][16];
         tmem_ld16(tmem + lane_base + cDP + dcol, va[0]);
         tmem_ld16(tmem + lane_base + cDQB + dcol, vb[0]);
@@ -580,20 +599,29 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
             tc_fence_before();
             mbar_arrive(&sm.bar_free);
           }
-          if (q_ok) {
+          // box row = feature, column = query row t: a warp stores 128 contiguous bytes
+          float* box = slot(c >> 5) + (c & 31) * 128 + t;
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-              atomicAdd(dst + (size_t)(c + e) * prm.np,
-                        fmaf(ca, __uint_as_float(va[cur][e]), cb * __uint_as_float(vb[cur][e])));
-          }
+          for (int e = 0; e < 16; ++e)
+            box[e * 128] = fmaf(ca, __uint_as_float(va[cur][e]), cb * __uint_as_float(vb[cur][e]));
           if (c + 16 < DG) {
             tmem_ld_wait();
             reg_fence16(va[cur ^ 1]);
             reg_fence16(vb[cur ^ 1]);
           }
         }
+        fence_proxy_async_smem();
+        named_bar_group(g);
+        if (t == 0) {
+#pragma unroll
+          for (int b = 0; b < DG / 32; ++b) tma_reduce_add_3d(&tm_dq, slot(b), I * 128, (int)dcol + 32 * b, bh);
+          bulk_commit();
+          pending_qs = qs;
+        }
       }
     }
+    // the last reductions must complete before the CTA's shared memory goes away
+    if (t == 0) bulk_wait_all();
     // ---------------- epilogue: dK then dV rows of this key block, this group's columns
     if (ok) {
       tc_fence_after();
@@ -727,13 +755,13 @@ __global__ void __launch_bounds__(kPreThreads) bwd_dq_kernel(const float* __rest
 
 template <int D, int NWG>
 int launch_main_t(const CUtensorMap& tk, const CUtensorMap& tq, const CUtensorMap& tv, const CUtensorMap& tdo,
-                  const CUtensorMap& tdo8, const BwdParams& p, int BH, cudaStream_t st) {
+                  const CUtensorMap& tdo8, const CUtensorMap& tdq, const BwdParams& p, int BH, cudaStream_t st) {
   size_t smem = sizeof(BwdSmem<D>);
   if (smem < 120 * 1024) smem = 120 * 1024;  // one CTA per SM: it holds all 512 TMEM columns
   auto kern = bwd_main_kernel<D, NWG>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 3;
   ScopedTimer timer("bwd_main", st);
-  kern<<<dim3(p.nqb, BH), (NWG + 1) * 128, smem, st>>>(tk, tq, tv, tdo, tdo8, p);
+  kern<<<dim3(p.nqb, BH), (NWG + 1) * 128, smem, st>>>(tk, tq, tv, tdo, tdo8, tdq, p);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 
@@ -778,6 +806,10 @@ int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const
   if (!make_tmap_3d(&tv, V, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, N, BH, 64, 128)) return 3;
   if (!make_tmap_3d(&tdo, dO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, N, BH, 64, 128)) return 3;
   if (!make_tmap_3d(&tdo8, do8t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, np, D, BH, 128, D)) return 3;
+  // dQ accumulator [BH][D][np] fp32, boxes of 32 features x 128 queries, unswizzled
+  CUtensorMap tdq;
+  if (!make_tmap_3d(&tdq, dqacc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, np, D, BH, 128, 32, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return 3;
   BwdParams p;
   p.N = N;
   p.np = np;
@@ -797,8 +829,8 @@ int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const
   p.dK = static_cast<__nv_bfloat16*>(dK);
   p.dV = static_cast<__nv_bfloat16*>(dV);
   p.status = reinterpret_cast<int*>(const_cast<uint8_t*>(w) + QL.status);
-  int rc = D == 128 ? launch_main_t<128, kBwdGroups>(tk, tq, tv, tdo, tdo8, p, BH, st)
-                    : launch_main_t<64, kBwdGroups>(tk, tq, tv, tdo, tdo8, p, BH, st);
+  int rc = D == 128 ? launch_main_t<128, kBwdGroups>(tk, tq, tv, tdo, tdo8, tdq, p, BH, st)
+                    : launch_main_t<64, kBwdGroups>(tk, tq, tv, tdo, tdo8, tdq, p, BH, st);
   if (rc) return rc;
   const float* qr = reinterpret_cast<const float*>(w + QL.qr);
   auto* q = static_cast<const __nv_bfloat16*>(Q);
