@@ -182,7 +182,7 @@ struct BwdSmem {
   uint64_t bar_kv;
   uint64_t bar_q_full[2], bar_do_full, bar_do8_full;
   uint64_t bar_q_free[2], bar_do_free, bar_do8_free;
-  uint64_t bar_sdp, bar_p, bar_ds, bar_part, bar_free;
+  uint64_t bar_s, bar_dp, bar_p, bar_ds, bar_dk, bar_part, bar_free_s, bar_free_dp;
   uint32_t tmem_base;
   int abort;
 };
@@ -262,11 +262,14 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
     mbar_init(&sm.bar_q_free[1], NWG);
     mbar_init(&sm.bar_do_free, 1);
     mbar_init(&sm.bar_do8_free, 1);
-    mbar_init(&sm.bar_sdp, 1);
+    mbar_init(&sm.bar_s, 1);
+    mbar_init(&sm.bar_dp, 1);
+    mbar_init(&sm.bar_dk, 1);
     mbar_init(&sm.bar_p, NC);
     mbar_init(&sm.bar_ds, NC);
     mbar_init(&sm.bar_part, 1);
-    mbar_init(&sm.bar_free, NC);
+    mbar_init(&sm.bar_free_s, NC);
+    mbar_init(&sm.bar_free_dp, NC);
     sm.abort = 0;
     fence_mbar_init();
   }
@@ -324,20 +327,27 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
     for (int it = 0; ok && it < n_it; ++it) {
       const uint32_t ph = it & 1;
       const uint32_t a_q = smem_u32(sm.q[it & 1]);
-      if (!mbar_wait(&sm.bar_q_full[it & 1], (it >> 1) & 1, abort) || !mbar_wait(&sm.bar_do_full, ph, abort)) break;
-      if (it > 0 && !mbar_wait(&sm.bar_free, (it - 1) & 1, abort)) break;
+      // S^T(it) goes in as soon as the previous dK part has been read out of its columns,
+      // dP^T(it) once the previous dQ halves have been read: both overlap the compute
+      // warps' work on iteration it - 1
+      if (!mbar_wait(&sm.bar_q_full[it & 1], (it >> 1) & 1, abort)) break;
+      if (it > 0 && !mbar_wait(&sm.bar_free_s, (it - 1) & 1, abort)) break;
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
         umma_bf16(tmem + cS, sdesc_sw128(a_k + off, 16, 1024), sdesc_sw128(a_q + off, 16, 1024), id_s, kk > 0);
       }
+      umma_commit(&sm.bar_s);
+      if (!mbar_wait(&sm.bar_do_full, ph, abort)) break;
+      if (it > 0 && !mbar_wait(&sm.bar_free_dp, (it - 1) & 1, abort)) break;
+      tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
         umma_bf16(tmem + cDP, sdesc_sw128(a_v + off, 16, 1024), sdesc_sw128(a_do + off, 16, 1024), id_s, kk > 0);
       }
-      umma_commit(&sm.bar_sdp);
+      umma_commit(&sm.bar_dp);
       umma_commit(&sm.bar_do_free);
       if (!mbar_wait(&sm.bar_p, ph, abort) || !mbar_wait(&sm.bar_do8_full, ph, abort)) break;
       tc_fence_after();
@@ -355,6 +365,7 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
         umma_bf16(tmem + cS, sdesc_sw128(a_ds + offa, 16, 1024), sdesc_sw128(a_q + kk * 2048, 16384, 1024), id_dk,
                   kk > 0);
       }
+      umma_commit(&sm.bar_dk);
       // dQ halves: [q, d] = sum_{key in half} dS[q, key] K[key, d]
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
@@ -405,7 +416,7 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
       }
       const float cs = __fmul_rn(__fmul_rn(sqI, sk_mine), prm.alpha);
       const bool diag = prm.causal && I == kb;
-      if (!mbar_wait(&sm.bar_sdp, ph, abort)) {
+      if (!mbar_wait(&sm.bar_s, ph, abort)) {
         ok = false;
         break;
       }
@@ -470,10 +481,15 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
           tmem_ld32(tmem + lane_base + cS + qcol + 32, bufB);
           p_chunk(bufA, 0);
           tmem_wait32(bufB);
-          tmem_ld32(tmem + lane_base + cDP + qcol, bufA);
           p_chunk(bufB, 1);
           fence_proxy_async_smem();
           mbar_arrive(&sm.bar_p);
+          if (!mbar_wait(&sm.bar_dp, ph, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          tmem_ld32(tmem + lane_base + cDP + qcol, bufA);
           tmem_wait32(bufA);
           tmem_ld32(tmem + lane_base + cDP + qcol + 32, bufB);
           ds_chunk(bufA, 0);
@@ -482,10 +498,15 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
         } else {
           tmem_ld32(tmem + lane_base + cS + qcol, bufA);
           tmem_wait32(bufA);
-          tmem_ld32(tmem + lane_base + cDP + qcol, bufB);
           p_chunk(bufA, 0);
           fence_proxy_async_smem();
           mbar_arrive(&sm.bar_p);
+          if (!mbar_wait(&sm.bar_dp, ph, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          tmem_ld32(tmem + lane_base + cDP + qcol, bufB);
           tmem_wait32(bufB);
           ds_chunk(bufB, 0);
         }
@@ -551,7 +572,7 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&sm.bar_ds);
-      if (!mbar_wait(&sm.bar_part, ph, abort)) {
+      if (!mbar_wait(&sm.bar_dk, ph, abort)) {
         ok = false;
         break;
       }
@@ -576,6 +597,14 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
           if (c + 32 < DG) tmem_wait16(kA);
         }
       }
+      // the dK part is in registers: the next S^T may overwrite its columns
+      tc_fence_before();
+      mbar_arrive(&sm.bar_free_s);
+      if (!mbar_wait(&sm.bar_part, ph, abort)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
       {
         // staging slot of box b (features dcol + 32b ..): 0,1 -> dS^T blocks, 2,3 -> halves of q[qs]
         auto slot = [&](int b) -> float* {
@@ -595,9 +624,9 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
             tmem_ld16(tmem + lane_base + cDP + dcol + c + 16, va[cur ^ 1]);
             tmem_ld16(tmem + lane_base + cDQB + dcol + c + 16, vb[cur ^ 1]);
           } else {
-            // every TMEM read of this iteration is done: let the next S/dP MMAs start
+            // every TMEM read of this iteration is done: the next dP^T may start
             tc_fence_before();
-            mbar_arrive(&sm.bar_free);
+            mbar_arrive(&sm.bar_free_dp);
           }
           // box row = feature, column = query row t: a warp stores 128 contiguous bytes
           float* box = slot(c >> 5) + (c & 31) * 128 + t;
