@@ -281,103 +281,111 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort = &sm.abort;
+  // the producer/MMA warpgroup needs few registers: hand them to the compute groups
+  // (launch: 168 x 128 per group; after: kRegsIssue + NWG x kRegsCompute per 128 threads)
+  constexpr uint32_t kRegsIssue = 80, kRegsCompute = NWG == 2 ? 208 : 168;
+  static_assert(kRegsIssue + NWG * kRegsCompute <= (NWG + 1) * 168, "register split exceeds the launch budget");
 
-  if (warp == WPROD && lane == 0) {
-    // ---------------- producer
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_v);
-    tma_prefetch_desc(&tm_do);
-    tma_prefetch_desc(&tm_do8);
-    tma_prefetch_desc(&tm_dq);
-    mbar_arrive_expect_tx(&sm.bar_kv, 2 * kTile);
-#pragma unroll
-    for (int c = 0; c < D / 64; ++c) {
-      tma_load_3d(sm.k + c * 16384, &tm_k, c * 64, kb * 128, bh, &sm.bar_kv);
-      tma_load_3d(sm.v + c * 16384, &tm_v, c * 64, kb * 128, bh, &sm.bar_kv);
-    }
-    for (int it = 0; it < n_it; ++it) {
-      const int I = I0 + it;
-      if (it > 0 && !mbar_wait(&sm.bar_do_free, (it - 1) & 1, abort)) break;
-      mbar_arrive_expect_tx(&sm.bar_do_full, kTile);
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) tma_load_3d(sm.dob + c * 16384, &tm_do, c * 64, I * 128, bh, &sm.bar_do_full);
-      if (it > 0 && !mbar_wait(&sm.bar_do8_free, (it - 1) & 1, abort)) break;
-      mbar_arrive_expect_tx(&sm.bar_do8_full, D * 128);
-      tma_load_3d(sm.do8, &tm_do8, I * 128, 0, bh, &sm.bar_do8_full);
-      const int qs = it & 1;
-      if (it > 1 && !mbar_wait(&sm.bar_q_free[qs], ((it >> 1) - 1) & 1, abort)) break;
-      mbar_arrive_expect_tx(&sm.bar_q_full[qs], kTile + 1024);
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_3d(sm.q[qs] + c * 16384, &tm_q, c * 64, I * 128, bh, &sm.bar_q_full[qs]);
-      // the query block's bias and D_i rows travel with its Q tile
-      bulk_load(sm.bias[qs], prm.bias + (size_t)bh * prm.np + I * 128, 512, &sm.bar_q_full[qs]);
-      bulk_load(sm.dvec[qs], prm.dvec + (size_t)bh * prm.np + I * 128, 512, &sm.bar_q_full[qs]);
-    }
-  } else if (warp == WMMA && lane == 0) {
-    // ---------------- UMMA issuer
-    constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);   // S^T, dP^T
-    constexpr uint32_t id_dv = idesc_e4m3(128, D);                   // dV
-    constexpr uint32_t id_dk = idesc_bf16(128, D, false, true);      // dK: A K-major, B MN-major
-    constexpr uint32_t id_dq = idesc_bf16(128, D, true, true);       // dQ: A, B MN-major
-    const uint32_t a_k = smem_u32(sm.k), a_v = smem_u32(sm.v), a_do = smem_u32(sm.dob);
-    const uint32_t a_do8 = smem_u32(sm.do8), a_p = smem_u32(sm.p), a_ds = smem_u32(sm.ds);
-    bool ok = mbar_wait(&sm.bar_kv, 0, abort);
-    for (int it = 0; ok && it < n_it; ++it) {
-      const uint32_t ph = it & 1;
-      const uint32_t a_q = smem_u32(sm.q[it & 1]);
-      // S^T(it) goes in as soon as the previous dK part has been read out of its columns,
-      // dP^T(it) once the previous dQ halves have been read: both overlap the compute
-      // warps' work on iteration it - 1
-      if (!mbar_wait(&sm.bar_q_full[it & 1], (it >> 1) & 1, abort)) break;
-      if (it > 0 && !mbar_wait(&sm.bar_free_s, (it - 1) & 1, abort)) break;
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-        umma_bf16(tmem + cS, sdesc_sw128(a_k + off, 16, 1024), sdesc_sw128(a_q + off, 16, 1024), id_s, kk > 0);
+  if (warp >= 4 * NWG) {
+    regs_decrease<kRegsIssue>();
+    if (warp == WPROD && lane == 0) {
+      // ---------------- producer
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      tma_prefetch_desc(&tm_do8);
+      tma_prefetch_desc(&tm_dq);
+      mbar_arrive_expect_tx(&sm.bar_kv, 2 * kTile);
+  #pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_3d(sm.k + c * 16384, &tm_k, c * 64, kb * 128, bh, &sm.bar_kv);
+        tma_load_3d(sm.v + c * 16384, &tm_v, c * 64, kb * 128, bh, &sm.bar_kv);
       }
-      umma_commit(&sm.bar_s);
-      if (!mbar_wait(&sm.bar_do_full, ph, abort)) break;
-      if (it > 0 && !mbar_wait(&sm.bar_free_dp, (it - 1) & 1, abort)) break;
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-        umma_bf16(tmem + cDP, sdesc_sw128(a_v + off, 16, 1024), sdesc_sw128(a_do + off, 16, 1024), id_s, kk > 0);
+      for (int it = 0; it < n_it; ++it) {
+        const int I = I0 + it;
+        if (it > 0 && !mbar_wait(&sm.bar_do_free, (it - 1) & 1, abort)) break;
+        mbar_arrive_expect_tx(&sm.bar_do_full, kTile);
+  #pragma unroll
+        for (int c = 0; c < D / 64; ++c) tma_load_3d(sm.dob + c * 16384, &tm_do, c * 64, I * 128, bh, &sm.bar_do_full);
+        if (it > 0 && !mbar_wait(&sm.bar_do8_free, (it - 1) & 1, abort)) break;
+        mbar_arrive_expect_tx(&sm.bar_do8_full, D * 128);
+        tma_load_3d(sm.do8, &tm_do8, I * 128, 0, bh, &sm.bar_do8_full);
+        const int qs = it & 1;
+        if (it > 1 && !mbar_wait(&sm.bar_q_free[qs], ((it >> 1) - 1) & 1, abort)) break;
+        mbar_arrive_expect_tx(&sm.bar_q_full[qs], kTile + 1024);
+  #pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(sm.q[qs] + c * 16384, &tm_q, c * 64, I * 128, bh, &sm.bar_q_full[qs]);
+        // the query block's bias and D_i rows travel with its Q tile
+        bulk_load(sm.bias[qs], prm.bias + (size_t)bh * prm.np + I * 128, 512, &sm.bar_q_full[qs]);
+        bulk_load(sm.dvec[qs], prm.dvec + (size_t)bh * prm.np + I * 128, 512, &sm.bar_q_full[qs]);
       }
-      umma_commit(&sm.bar_dp);
-      umma_commit(&sm.bar_do_free);
-      if (!mbar_wait(&sm.bar_p, ph, abort) || !mbar_wait(&sm.bar_do8_full, ph, abort)) break;
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        umma_f8(tmem + cDV, sdesc_sw128(a_p + kk * 32, 16, 1024), sdesc_sw128(a_do8 + kk * 32, 16, 1024), id_dv,
-                (it > 0 || kk > 0));
-      umma_commit(&sm.bar_do8_free);
-      if (!mbar_wait(&sm.bar_ds, ph, abort)) break;
-      tc_fence_after();
-      // dK_part[key, d] = sum_q dS^T[key, q] Q[q, d]
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t offa = (kk >> 2) * 16384 + (kk & 3) * 32;
-        umma_bf16(tmem + cS, sdesc_sw128(a_ds + offa, 16, 1024), sdesc_sw128(a_q + kk * 2048, 16384, 1024), id_dk,
-                  kk > 0);
+    } else if (warp == WMMA && lane == 0) {
+      // ---------------- UMMA issuer
+      constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);   // S^T, dP^T
+      constexpr uint32_t id_dv = idesc_e4m3(128, D);                   // dV
+      constexpr uint32_t id_dk = idesc_bf16(128, D, false, true);      // dK: A K-major, B MN-major
+      constexpr uint32_t id_dq = idesc_bf16(128, D, true, true);       // dQ: A, B MN-major
+      const uint32_t a_k = smem_u32(sm.k), a_v = smem_u32(sm.v), a_do = smem_u32(sm.dob);
+      const uint32_t a_do8 = smem_u32(sm.do8), a_p = smem_u32(sm.p), a_ds = smem_u32(sm.ds);
+      bool ok = mbar_wait(&sm.bar_kv, 0, abort);
+      for (int it = 0; ok && it < n_it; ++it) {
+        const uint32_t ph = it & 1;
+        const uint32_t a_q = smem_u32(sm.q[it & 1]);
+        // S^T(it) goes in as soon as the previous dK part has been read out of its columns,
+        // dP^T(it) once the previous dQ halves have been read: both overlap the compute
+        // warps' work on iteration it - 1
+        if (!mbar_wait(&sm.bar_q_full[it & 1], (it >> 1) & 1, abort)) break;
+        if (it > 0 && !mbar_wait(&sm.bar_free_s, (it - 1) & 1, abort)) break;
+        tc_fence_after();
+  #pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          umma_bf16(tmem + cS, sdesc_sw128(a_k + off, 16, 1024), sdesc_sw128(a_q + off, 16, 1024), id_s, kk > 0);
+        }
+        umma_commit(&sm.bar_s);
+        if (!mbar_wait(&sm.bar_do_full, ph, abort)) break;
+        if (it > 0 && !mbar_wait(&sm.bar_free_dp, (it - 1) & 1, abort)) break;
+        tc_fence_after();
+  #pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          umma_bf16(tmem + cDP, sdesc_sw128(a_v + off, 16, 1024), sdesc_sw128(a_do + off, 16, 1024), id_s, kk > 0);
+        }
+        umma_commit(&sm.bar_dp);
+        umma_commit(&sm.bar_do_free);
+        if (!mbar_wait(&sm.bar_p, ph, abort) || !mbar_wait(&sm.bar_do8_full, ph, abort)) break;
+        tc_fence_after();
+  #pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_f8(tmem + cDV, sdesc_sw128(a_p + kk * 32, 16, 1024), sdesc_sw128(a_do8 + kk * 32, 16, 1024), id_dv,
+                  (it > 0 || kk > 0));
+        umma_commit(&sm.bar_do8_free);
+        if (!mbar_wait(&sm.bar_ds, ph, abort)) break;
+        tc_fence_after();
+        // dK_part[key, d] = sum_q dS^T[key, q] Q[q, d]
+  #pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t offa = (kk >> 2) * 16384 + (kk & 3) * 32;
+          umma_bf16(tmem + cS, sdesc_sw128(a_ds + offa, 16, 1024), sdesc_sw128(a_q + kk * 2048, 16384, 1024), id_dk,
+                    kk > 0);
+        }
+        umma_commit(&sm.bar_dk);
+        // dQ halves: [q, d] = sum_{key in half} dS[q, key] K[key, d]
+  #pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16(tmem + cDP, sdesc_sw128(a_ds + kk * 2048, 16384, 1024), sdesc_sw128(a_k + kk * 2048, 16384, 1024),
+                    id_dq, kk > 0);
+  #pragma unroll
+        for (int kk = 4; kk < 8; ++kk)
+          umma_bf16(tmem + cDQB, sdesc_sw128(a_ds + kk * 2048, 16384, 1024),
+                    sdesc_sw128(a_k + kk * 2048, 16384, 1024), id_dq, kk > 4);
+        umma_commit(&sm.bar_part);
       }
-      umma_commit(&sm.bar_dk);
-      // dQ halves: [q, d] = sum_{key in half} dS[q, key] K[key, d]
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        umma_bf16(tmem + cDP, sdesc_sw128(a_ds + kk * 2048, 16384, 1024), sdesc_sw128(a_k + kk * 2048, 16384, 1024),
-                  id_dq, kk > 0);
-#pragma unroll
-      for (int kk = 4; kk < 8; ++kk)
-        umma_bf16(tmem + cDQB, sdesc_sw128(a_ds + kk * 2048, 16384, 1024),
-                  sdesc_sw128(a_k + kk * 2048, 16384, 1024), id_dq, kk > 4);
-      umma_commit(&sm.bar_part);
     }
-  } else if (warp < 4 * NWG) {
+  } else {
+    regs_increase<kRegsCompute>();
     // ---------------- compute: warpgroup g, thread t owns key row t
     const int g = warp >> 2;
     const int t = tid & 127;
