@@ -433,22 +433,30 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
       // neither take the unmasked path
       const bool any_mask = __any_sync(0xffffffffu, !key_ok || diag);
       const int mask_lim = !key_ok ? 128 : (diag ? t : 0);  // queries qi < mask_lim are masked
-      // ---- P^T = e4m3(448 * 2^(S2 - LSE2)) and dS^T * 448 = p8 (dP^T - D) on this thread's
-      // query columns, 32 at a time.  TMEM loads are software-pipelined: the next chunk's load
-      // is issued before the current chunk is processed (wait::ld waits for all of this
-      // thread's loads, so each wait covers a load that overlapped compute).
-      float amax = 0.f;
+      // ---- P^T = e4m3(448 * 2^(S2 - LSE2)) on this thread's QC query columns, 32 per chunk.
+      // The codes go to shared memory for the dV MMA and stay in registers for dS.
+      constexpr int NCH = QC / 32;
+      uint32_t buf[NCH][32];
+      uint32_t pw[NCH][8];
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) tmem_ld32(tmem + lane_base + cS + qcol + 32 * c, buf[c]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) reg_fence32(buf[c]);
       {
-        uint32_t bufA[32], bufB[32];
-        auto p_chunk = [&](const uint32_t (&sv)[32], int c) {
-          uint32_t pw[8];
+        const uint64_t cs2 = f2(cs, cs);
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
 #pragma unroll
           for (int e = 0; e < 32; e += 4) {
-            float p[4];
             const float4 b4 = *reinterpret_cast<const float4*>(&s_bias[qcol + 32 * c + e]);
-            const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
+            float p[4];
+            f2split(ffma2(f2(__uint_as_float(buf[c][e]), __uint_as_float(buf[c][e + 1])), cs2, f2(b4.x, b4.y)), p[0],
+                    p[1]);
+            f2split(ffma2(f2(__uint_as_float(buf[c][e + 2]), __uint_as_float(buf[c][e + 3])), cs2, f2(b4.z, b4.w)),
+                    p[2], p[3]);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) p[u] = ex2(fmaf(__uint_as_float(sv[e + u]), cs, bb[u]));
+            for (int u = 0; u < 4; ++u) p[u] = ex2(p[u]);
             if (any_mask) {
 #pragma unroll
               for (int u = 0; u < 4; ++u)
@@ -458,67 +466,51 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
                 __nv_cvt_float2_to_fp8x2(make_float2(p[0], p[1]), __NV_SATFINITE, __NV_E4M3);
             const __nv_fp8x2_storage_t hi =
                 __nv_cvt_float2_to_fp8x2(make_float2(p[2], p[3]), __NV_SATFINITE, __NV_E4M3);
-            pw[e >> 2] = (uint32_t)lo | ((uint32_t)hi << 16);
+            pw[c][e >> 2] = (uint32_t)lo | ((uint32_t)hi << 16);
           }
           const int u0 = (int)(qcol >> 4) + 2 * c;  // 16-byte units of this chunk in the 128-byte row
-          *reinterpret_cast<uint4*>(prow + ((u0 ^ (t & 7)) << 4)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-          *reinterpret_cast<uint4*>(prow + (((u0 + 1) ^ (t & 7)) << 4)) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
-        };
-        auto ds_chunk = [&](uint32_t (&dv)[32], int c) {
-          const int u0 = (int)(qcol >> 4) + 2 * c;
-          const uint4 pa = *reinterpret_cast<const uint4*>(prow + ((u0 ^ (t & 7)) << 4));
-          const uint4 pb = *reinterpret_cast<const uint4*>(prow + (((u0 + 1) ^ (t & 7)) << 4));
-          const uint32_t pw[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float2 dd = *reinterpret_cast<const float2*>(&s_dvec[qcol + 32 * c + e]);
-            const uint32_t w = pw[e >> 2] >> ((e & 3) * 8);
-            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xffffu), __NV_E4M3);
-            const float2 pf = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-            const float x0 = pf.x * (__uint_as_float(dv[e]) - dd.x);
-            const float x1 = pf.y * (__uint_as_float(dv[e + 1]) - dd.y);
-            amax = fmaxf(amax, fmaxf(fabsf(x0), fabsf(x1)));
-            dv[e] = __float_as_uint(x0);
-            dv[e + 1] = __float_as_uint(x1);
-          }
-          tmem_st32(tmem + lane_base + cDP + qcol + 32 * c, dv);
-        };
-        if constexpr (QC == 64) {
-          tmem_ld32(tmem + lane_base + cS + qcol, bufA);
-          tmem_wait32(bufA);
-          tmem_ld32(tmem + lane_base + cS + qcol + 32, bufB);
-          p_chunk(bufA, 0);
-          tmem_wait32(bufB);
-          p_chunk(bufB, 1);
-          fence_proxy_async_smem();
-          mbar_arrive(&sm.bar_p);
-          if (!mbar_wait(&sm.bar_dp, ph, abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          tmem_ld32(tmem + lane_base + cDP + qcol, bufA);
-          tmem_wait32(bufA);
-          tmem_ld32(tmem + lane_base + cDP + qcol + 32, bufB);
-          ds_chunk(bufA, 0);
-          tmem_wait32(bufB);
-          ds_chunk(bufB, 1);
-        } else {
-          tmem_ld32(tmem + lane_base + cS + qcol, bufA);
-          tmem_wait32(bufA);
-          p_chunk(bufA, 0);
-          fence_proxy_async_smem();
-          mbar_arrive(&sm.bar_p);
-          if (!mbar_wait(&sm.bar_dp, ph, abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          tmem_ld32(tmem + lane_base + cDP + qcol, bufB);
-          tmem_wait32(bufB);
-          ds_chunk(bufB, 0);
+          *reinterpret_cast<uint4*>(prow + ((u0 ^ (t & 7)) << 4)) =
+              make_uint4(pw[c][0], pw[c][1], pw[c][2], pw[c][3]);
+          *reinterpret_cast<uint4*>(prow + (((u0 + 1) ^ (t & 7)) << 4)) =
+              make_uint4(pw[c][4], pw[c][5], pw[c][6], pw[c][7]);
         }
-        tmem_st_wait();
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&sm.bar_p);
+      // ---- dS^T * 448 = p8 (dP^T - D), kept in registers until the tile scale is known
+      if (!mbar_wait(&sm.bar_dp, ph, abort)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) tmem_ld32(tmem + lane_base + cDP + qcol + 32 * c, buf[c]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) reg_fence32(buf[c]);
+      float amax = 0.f;
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(&s_dvec[qcol + 32 * c + e]);
+          const uint32_t w = pw[c][e >> 2];
+          const __half2_raw h01 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xffffu), __NV_E4M3);
+          const __half2_raw h23 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
+          const float2 p01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+          const float2 p23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+          float x[4];
+          f2split(fmul2(f2(p01.x, p01.y),
+                        fsub2(f2(__uint_as_float(buf[c][e]), __uint_as_float(buf[c][e + 1])), f2(d4.x, d4.y))),
+                  x[0], x[1]);
+          f2split(fmul2(f2(p23.x, p23.y),
+                        fsub2(f2(__uint_as_float(buf[c][e + 2]), __uint_as_float(buf[c][e + 3])), f2(d4.z, d4.w))),
+                  x[2], x[3]);
+          amax = max3(amax, fabsf(x[0]), fabsf(x[1]));
+          amax = max3(amax, fabsf(x[2]), fabsf(x[3]));
+#pragma unroll
+          for (int u = 0; u < 4; ++u) buf[c][e + u] = __float_as_uint(x[u]);
+        }
       }
 #pragma unroll
       for (int m = 16; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
@@ -540,21 +532,21 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
         else
           a1 = fmaxf(a1, sm.smax[w]);
       }
-      // values are 448 * dS: scale s_dS = max|dS| / 127
-      const float sds0 = a0 > 0.f ? __fdiv_rn(a0 * (1.0f / 448.0f), 127.0f) : 0.f;
-      const float sds1 = a1 > 0.f ? __fdiv_rn(a1 * (1.0f / 448.0f), 127.0f) : 0.f;
       const float amine = half ? a1 : a0;
       const float inv = amine > 0.f ? 127.0f / amine : 0.f;  // code = rint(448 dS * 127 / max|448 dS|)
-      // ---- dS^T codes -> shared memory (bf16 containers, 128B-swizzled key rows)
+      // ---- dS^T codes -> shared memory (bf16 containers, 128B-swizzled key rows).  Rounding to
+      // the nearest integer (ties to even) stays in the fp32 pipe: RN(x * inv + 1.5 * 2^23) - 1.5 * 2^23;
+      // |x * inv| <= 127 (plus rounding), so no clamp is needed
       {
-        auto code_chunk = [&](const uint32_t (&dv)[32], int c) {
+        const uint64_t inv2 = f2(inv, inv), magic2 = f2(kRoundMagic, kRoundMagic);
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
           uint32_t packed[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            // round to the nearest integer (ties to even) without leaving the fp32 pipe;
-            // |448 dS * inv| <= 127 (plus rounding), so no clamp is needed
-            const float c0 = fmaf(__uint_as_float(dv[e]), inv, kRoundMagic) - kRoundMagic;
-            const float c1 = fmaf(__uint_as_float(dv[e + 1]), inv, kRoundMagic) - kRoundMagic;
+            float c0, c1;
+            f2split(fsub2(ffma2(f2(__uint_as_float(buf[c][e]), __uint_as_float(buf[c][e + 1])), inv2, magic2), magic2),
+                    c0, c1);
             const __nv_bfloat162 hv = __floats2bfloat162_rn(c0, c1);
             packed[e >> 1] = *reinterpret_cast<const uint32_t*>(&hv);
           }
@@ -562,24 +554,14 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
           for (int u = 0; u < 4; ++u)
             *reinterpret_cast<uint4*>(dsrow + (((ds_u0 + 4 * c + u) ^ (t & 7)) << 4)) =
                 make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
-        };
-        uint32_t bufA[32], bufB[32];
-        if constexpr (QC == 64) {
-          tmem_ld32(tmem + lane_base + cDP + qcol, bufA);
-          tmem_wait32(bufA);
-          tmem_ld32(tmem + lane_base + cDP + qcol + 32, bufB);
-          code_chunk(bufA, 0);
-          tmem_wait32(bufB);
-          code_chunk(bufB, 1);
-        } else {
-          tmem_ld32(tmem + lane_base + cDP + qcol, bufA);
-          tmem_wait32(bufA);
-          code_chunk(bufA, 0);
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&sm.bar_ds);
+      // values are 448 * dS: scale s_dS = max|dS| / 127
+      const float sds0 = a0 > 0.f ? __fdiv_rn(a0 * (1.0f / 448.0f), 127.0f) : 0.f;
+      const float sds1 = a1 > 0.f ? __fdiv_rn(a1 * (1.0f / 448.0f), 127.0f) : 0.f;
       if (!mbar_wait(&sm.bar_dk, ph, abort)) {
         ok = false;
         break;
