@@ -8,15 +8,15 @@
 // rounded to e4m3 exactly as the forward rounds it.
 //
 // Kernels (all on the caller's stream):
-//   bwd_pre    per (head, 128-query block): D_i = sum_d dO*O, LSE*log2(e) (+inf on
-//              padded rows), partial channel maxima of |dO|, zeroed dQ accumulator
+//   bwd_pre    per (head, 128-query block): D_i = sum_d dO*O, log2(448) - LSE*log2(e)
+//              (-inf on padded rows), partial channel maxima of |dO|, zeroed dQ accumulator
 //   bwd_docomb per head: dO channel scales max|dO|/448
 //   bwd_do8    per (head, 128-query block): e4m3 codes of dO, channel-major
 //   bwd_main   per (head, 128-key block), looping over query blocks:
-//                S^T  = K8 Q8^T        kind::f16 (bf16-held INT8 codes, exact)
-//                dP^T = V dO^T         kind::f16 (bf16)
-//                P^T  = e4m3(448 * 2^(S2 - LSE2)) / 448;  dS^T = P^T (dP^T - D)
-//                dV  += P8^T dO8       kind::f8f6f4
+//                S  = Q8 K8^T          kind::f16 (bf16-held INT8 codes, exact)
+//                dP = dO V^T           kind::f16 (bf16)
+//                P  = e4m3(448 * 2^(S2 - LSE2)) / 448;  dS = P (dP - D)
+//                dV  += P8^T dO8       kind::f8f6f4, P read transposed from its query rows
 //                dS  -> INT8, one scale per (128 query x 64 key) tile
 //                dK_part = dS8^T Q8    kind::f16, scaled per tile, summed in registers
 //                dQ_part = dS8 K8      kind::f16 per 64-key half, scaled, staged in shared
@@ -41,10 +41,6 @@ namespace {
 
 constexpr float kLog2_448 = 8.807354922057604f;
 constexpr int kPreThreads = 256;
-#ifndef SAGE_BWD_GROUPS
-#define SAGE_BWD_GROUPS 2
-#endif
-constexpr int kBwdGroups = SAGE_BWD_GROUPS;  // compute warpgroups of the main backward kernel
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -174,15 +170,15 @@ struct BwdSmem {
   uint8_t q[2][128 * D * 2]; // Q codes of the current and next query blocks
   uint8_t dob[128 * D * 2];  // dO bf16 of the current query block
   uint8_t do8[D * 128];      // dO e4m3 codes, channel-major
-  uint8_t p[128 * 128];      // P^T e4m3, key rows
-  uint8_t ds[128 * 128 * 2]; // dS^T INT8 codes in bf16, key rows
+  uint8_t p[128 * 128];      // P e4m3, query rows of 128 keys
+  uint8_t ds[128 * 128 * 2]; // dS INT8 codes in bf16, query rows; keys [0,64) then [64,128)
   __align__(16) float bias[2][128];  // log2(448) - LSE_i log2(e), per Q buffer
   __align__(16) float dvec[2][128];  // D_i, per Q buffer
-  float smax[16];
+  float smax[8];             // per compute warp: max |448 dS| over its rows of its group's keys
   uint64_t bar_kv;
   uint64_t bar_q_full[2], bar_do_full, bar_do8_full;
   uint64_t bar_q_free[2], bar_do_free, bar_do8_free;
-  uint64_t bar_s, bar_dp, bar_p, bar_ds, bar_dk, bar_part, bar_free_s, bar_free_dp;
+  uint64_t bar_s, bar_dp, bar_p, bar_ds[2], bar_dk, bar_part, bar_free_s, bar_free_dp;
   uint32_t tmem_base;
   int abort;
 };
@@ -197,17 +193,13 @@ struct BwdParams {
   const float* dvec;
   const __nv_bfloat16* K;
   const float* kr;
-  float* dqacc;
   __nv_bfloat16* dK;
   __nv_bfloat16* dV;
   int* status;
 };
 
-// named barrier 1 over the compute warpgroups only
-template <int NWG>
-__device__ __forceinline__ void named_bar_compute() {
-  asm volatile("bar.sync 1, %0;" ::"n"(NWG * 128) : "memory");
-}
+// named barrier 1 over both compute warpgroups
+__device__ __forceinline__ void named_bar_compute() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 // named barrier 2 + g over compute warpgroup g
 __device__ __forceinline__ void named_bar_group(int g) {
   asm volatile("bar.sync %0, 128;" ::"r"(2 + g) : "memory");
@@ -216,18 +208,21 @@ __device__ __forceinline__ void named_bar_group(int g) {
 constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23: x + M - M rounds x to an integer (ties to even)
 
 // One CTA per (head, 128-key block), looping over the query blocks that see it.
-//   warps 0 .. 4*NWG-1 : NWG compute warpgroups; thread t of group g owns key row t (TMEM
-//                        lane t), query columns [QC*g, QC*g + QC) of it (QC = 128/NWG) and
-//                        output columns [DG*g, DG*g + DG) of dK, dQ, dV (DG = D/NWG)
-//   warp 4*NWG lane 0  : TMA producer;  warp 4*NWG+1 : TMEM allocator, lane 0 issues UMMAs
-// TMEM columns: [0,128) S^T, then dK_part; [128,256) dP^T, then dS, then dQ half 0;
-// [256,256+D) dV; [384,384+D) dQ half 1.
+//   warps 0-7 : two compute warpgroups.  In the P and dS phases thread t of group g owns query
+//               row t (TMEM lane t of S and dP) and the keys of K block g (columns [64g, 64g+64)):
+//               the row's LSE and D_i are then scalars, and each group's dS tile (128 queries x
+//               64 keys) is quantized with its own scale.  In the epilogues thread t reads TMEM
+//               lane t of dK_part and dV (key row t) or of dQ (query row t), output columns
+//               [DG*g, DG*g + DG) (DG = D/2).
+//   warp 8 lane 0: TMA producer;  warp 9: TMEM allocator, lane 0 issues UMMAs.
+// TMEM columns: [0,128) S, then dK_part; [128,256) dP, then dQ of keys [64,128);
+// [256,256+D) dV; [384,384+D) dQ of keys [0,64).
 // dQ staging: each group writes its scaled dQ part as [32 features][128 queries] fp32
-// boxes (16 KB) into shared memory the next MMAs do not read: the dS^T blocks, then the
-// halves of the Q buffer just consumed; one thread per group adds them to the feature-major
+// boxes (16 KB) into shared memory the next MMAs do not read (its own dS block, then half
+// of the Q buffer just consumed); one thread per group adds them to the feature-major
 // accumulator with TMA reduce and, once the boxes are read, frees the Q buffer.
-template <int D, int NWG>
-__global__ void __launch_bounds__((NWG + 1) * 128, 1)
+template <int D>
+__global__ void __launch_bounds__(384, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_do8, const __grid_constant__ CUtensorMap tm_dq,
@@ -240,16 +235,14 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
     return;
   }
   BwdSmem<D>& sm = *reinterpret_cast<BwdSmem<D>*>(smem_raw);
-  constexpr int NC = NWG * 128;  // compute threads
-  constexpr int QC = 128 / NWG;  // query columns per compute thread
-  constexpr int DG = D / NWG;    // output columns per compute thread
-  constexpr int WPROD = 4 * NWG, WMMA = 4 * NWG + 1;
+  constexpr int DG = D / 2;  // output columns per compute thread
+  constexpr int WPROD = 8, WMMA = 9;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int kb = blockIdx.x, bh = blockIdx.y;
   const int I0 = prm.causal ? kb : 0;
   const int n_it = prm.nqb - I0;
   constexpr uint32_t kCols = 512;
-  constexpr uint32_t cS = 0, cDP = 128, cDV = 256, cDQB = 384;  // TMEM column bases
+  constexpr uint32_t cS = 0, cDP = 128, cDV = 256, cDQ0 = 384, cDQ1 = 128;  // TMEM column bases
   constexpr uint32_t kTile = 128 * D * 2;
 
   if (tid == 0) {
@@ -258,18 +251,19 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
     mbar_init(&sm.bar_q_full[1], 1);
     mbar_init(&sm.bar_do_full, 1);
     mbar_init(&sm.bar_do8_full, 1);
-    mbar_init(&sm.bar_q_free[0], NWG);  // one arrival per group once its dQ boxes are read
-    mbar_init(&sm.bar_q_free[1], NWG);
+    mbar_init(&sm.bar_q_free[0], 2);  // one arrival per group once its dQ boxes are read
+    mbar_init(&sm.bar_q_free[1], 2);
     mbar_init(&sm.bar_do_free, 1);
     mbar_init(&sm.bar_do8_free, 1);
     mbar_init(&sm.bar_s, 1);
     mbar_init(&sm.bar_dp, 1);
+    mbar_init(&sm.bar_p, 256);
+    mbar_init(&sm.bar_ds[0], 128);
+    mbar_init(&sm.bar_ds[1], 128);
     mbar_init(&sm.bar_dk, 1);
-    mbar_init(&sm.bar_p, NC);
-    mbar_init(&sm.bar_ds, NC);
     mbar_init(&sm.bar_part, 1);
-    mbar_init(&sm.bar_free_s, NC);
-    mbar_init(&sm.bar_free_dp, NC);
+    mbar_init(&sm.bar_free_s, 256);
+    mbar_init(&sm.bar_free_dp, 256);
     sm.abort = 0;
     fence_mbar_init();
   }
@@ -282,11 +276,11 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort = &sm.abort;
   // the producer/MMA warpgroup needs few registers: hand them to the compute groups
-  // (launch: 168 x 128 per group; after: kRegsIssue + NWG x kRegsCompute per 128 threads)
-  constexpr uint32_t kRegsIssue = 80, kRegsCompute = NWG == 2 ? 208 : 168;
-  static_assert(kRegsIssue + NWG * kRegsCompute <= (NWG + 1) * 168, "register split exceeds the launch budget");
+  // (launch: 168 x 384; after: 80 x 128 + 208 x 256)
+  constexpr uint32_t kRegsIssue = 80, kRegsCompute = 208;
+  static_assert(kRegsIssue + 2 * kRegsCompute <= 3 * 168, "register split exceeds the launch budget");
 
-  if (warp >= 4 * NWG) {
+  if (warp >= 8) {
     regs_decrease<kRegsIssue>();
     if (warp == WPROD && lane == 0) {
       // ---------------- producer
@@ -297,7 +291,7 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
       tma_prefetch_desc(&tm_do8);
       tma_prefetch_desc(&tm_dq);
       mbar_arrive_expect_tx(&sm.bar_kv, 2 * kTile);
-  #pragma unroll
+#pragma unroll
       for (int c = 0; c < D / 64; ++c) {
         tma_load_3d(sm.k + c * 16384, &tm_k, c * 64, kb * 128, bh, &sm.bar_kv);
         tma_load_3d(sm.v + c * 16384, &tm_v, c * 64, kb * 128, bh, &sm.bar_kv);
@@ -306,15 +300,16 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
         const int I = I0 + it;
         if (it > 0 && !mbar_wait(&sm.bar_do_free, (it - 1) & 1, abort)) break;
         mbar_arrive_expect_tx(&sm.bar_do_full, kTile);
-  #pragma unroll
-        for (int c = 0; c < D / 64; ++c) tma_load_3d(sm.dob + c * 16384, &tm_do, c * 64, I * 128, bh, &sm.bar_do_full);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(sm.dob + c * 16384, &tm_do, c * 64, I * 128, bh, &sm.bar_do_full);
         if (it > 0 && !mbar_wait(&sm.bar_do8_free, (it - 1) & 1, abort)) break;
         mbar_arrive_expect_tx(&sm.bar_do8_full, D * 128);
         tma_load_3d(sm.do8, &tm_do8, I * 128, 0, bh, &sm.bar_do8_full);
         const int qs = it & 1;
         if (it > 1 && !mbar_wait(&sm.bar_q_free[qs], ((it >> 1) - 1) & 1, abort)) break;
         mbar_arrive_expect_tx(&sm.bar_q_full[qs], kTile + 1024);
-  #pragma unroll
+#pragma unroll
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d(sm.q[qs] + c * 16384, &tm_q, c * 64, I * 128, bh, &sm.bar_q_full[qs]);
         // the query block's bias and D_i rows travel with its Q tile
@@ -323,90 +318,95 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
       }
     } else if (warp == WMMA && lane == 0) {
       // ---------------- UMMA issuer
-      constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);   // S^T, dP^T
-      constexpr uint32_t id_dv = idesc_e4m3(128, D);                   // dV
-      constexpr uint32_t id_dk = idesc_bf16(128, D, false, true);      // dK: A K-major, B MN-major
-      constexpr uint32_t id_dq = idesc_bf16(128, D, true, true);       // dQ: A, B MN-major
+      constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);  // S = Q K^T, dP = dO V^T
+      constexpr uint32_t id_dv = idesc_e4m3(128, D, true);            // dV = P^T dO8: A from query rows
+      constexpr uint32_t id_dk = idesc_bf16(128, D, true, true);      // dK = dS^T Q: A from query rows
+      constexpr uint32_t id_dq = idesc_bf16(128, D, false, true);     // dQ = dS K: B from key rows
       const uint32_t a_k = smem_u32(sm.k), a_v = smem_u32(sm.v), a_do = smem_u32(sm.dob);
       const uint32_t a_do8 = smem_u32(sm.do8), a_p = smem_u32(sm.p), a_ds = smem_u32(sm.ds);
       bool ok = mbar_wait(&sm.bar_kv, 0, abort);
       for (int it = 0; ok && it < n_it; ++it) {
         const uint32_t ph = it & 1;
         const uint32_t a_q = smem_u32(sm.q[it & 1]);
-        // S^T(it) goes in as soon as the previous dK part has been read out of its columns,
-        // dP^T(it) once the previous dQ halves have been read: both overlap the compute
+        // S(it) goes in as soon as the previous dK part has been read out of its columns,
+        // dP(it) once the previous dQ halves have been read: both overlap the compute
         // warps' work on iteration it - 1
         if (!mbar_wait(&sm.bar_q_full[it & 1], (it >> 1) & 1, abort)) break;
         if (it > 0 && !mbar_wait(&sm.bar_free_s, (it - 1) & 1, abort)) break;
         tc_fence_after();
-  #pragma unroll
+#pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_bf16(tmem + cS, sdesc_sw128(a_k + off, 16, 1024), sdesc_sw128(a_q + off, 16, 1024), id_s, kk > 0);
+          umma_bf16(tmem + cS, sdesc_sw128(a_q + off, 16, 1024), sdesc_sw128(a_k + off, 16, 1024), id_s, kk > 0);
         }
         umma_commit(&sm.bar_s);
         if (!mbar_wait(&sm.bar_do_full, ph, abort)) break;
         if (it > 0 && !mbar_wait(&sm.bar_free_dp, (it - 1) & 1, abort)) break;
         tc_fence_after();
-  #pragma unroll
+#pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_bf16(tmem + cDP, sdesc_sw128(a_v + off, 16, 1024), sdesc_sw128(a_do + off, 16, 1024), id_s, kk > 0);
+          umma_bf16(tmem + cDP, sdesc_sw128(a_do + off, 16, 1024), sdesc_sw128(a_v + off, 16, 1024), id_s,
+                    kk > 0);
         }
         umma_commit(&sm.bar_dp);
         umma_commit(&sm.bar_do_free);
         if (!mbar_wait(&sm.bar_p, ph, abort) || !mbar_wait(&sm.bar_do8_full, ph, abort)) break;
         tc_fence_after();
-  #pragma unroll
+        // dV[key, d] += sum_q P[q, key] dO8[q, d]: 32 query rows per step
+#pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          umma_f8(tmem + cDV, sdesc_sw128(a_p + kk * 32, 16, 1024), sdesc_sw128(a_do8 + kk * 32, 16, 1024), id_dv,
-                  (it > 0 || kk > 0));
+          umma_f8(tmem + cDV, sdesc_sw128(a_p + kk * 4096, 16384, 1024), sdesc_sw128(a_do8 + kk * 32, 16, 1024),
+                  id_dv, (it > 0 || kk > 0));
         umma_commit(&sm.bar_do8_free);
-        if (!mbar_wait(&sm.bar_ds, ph, abort)) break;
+        // dQ of keys [0,64) once group 0's codes are in: [q, d] = sum_key dS[q, key] K[key, d]
+        if (!mbar_wait(&sm.bar_ds[0], ph, abort)) break;
         tc_fence_after();
-        // dK_part[key, d] = sum_q dS^T[key, q] Q[q, d]
-  #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t offa = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_bf16(tmem + cS, sdesc_sw128(a_ds + offa, 16, 1024), sdesc_sw128(a_q + kk * 2048, 16384, 1024), id_dk,
-                    kk > 0);
-        }
-        umma_commit(&sm.bar_dk);
-        // dQ halves: [q, d] = sum_{key in half} dS[q, key] K[key, d]
-  #pragma unroll
+#pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          umma_bf16(tmem + cDP, sdesc_sw128(a_ds + kk * 2048, 16384, 1024), sdesc_sw128(a_k + kk * 2048, 16384, 1024),
+          umma_bf16(tmem + cDQ0, sdesc_sw128(a_ds + kk * 32, 16, 1024), sdesc_sw128(a_k + kk * 2048, 16384, 1024),
                     id_dq, kk > 0);
-  #pragma unroll
-        for (int kk = 4; kk < 8; ++kk)
-          umma_bf16(tmem + cDQB, sdesc_sw128(a_ds + kk * 2048, 16384, 1024),
-                    sdesc_sw128(a_k + kk * 2048, 16384, 1024), id_dq, kk > 4);
+        if (!mbar_wait(&sm.bar_ds[1], ph, abort)) break;
+        tc_fence_after();
+        // dK_part[key, d] = sum_q dS[q, key] Q[q, d]
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16(tmem + cS, sdesc_sw128(a_ds + kk * 2048, 16384, 1024), sdesc_sw128(a_q + kk * 2048, 16384, 1024),
+                    id_dk, kk > 0);
+        umma_commit(&sm.bar_dk);
+        // dQ of keys [64,128), into the dP columns (both groups have read dP by now)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16(tmem + cDQ1, sdesc_sw128(a_ds + 16384 + kk * 32, 16, 1024),
+                    sdesc_sw128(a_k + 8192 + kk * 2048, 16384, 1024), id_dq, kk > 0);
         umma_commit(&sm.bar_part);
       }
     }
   } else {
     regs_increase<kRegsCompute>();
-    // ---------------- compute: warpgroup g, thread t owns key row t
+    // ---------------- compute: group g, thread t
     const int g = warp >> 2;
     const int t = tid & 127;
-    const int key = kb * 128 + t;
-    const bool key_ok = key < prm.N;
-    const int half = t >> 6;  // 64-key block of this row within the CTA's 128 keys
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const int key = kb * 128 + t;  // key row of the epilogues
+    const bool key_ok = key < prm.N;
     const float* skh = prm.sk + (size_t)bh * prm.nqb * 2;
-    const float sk_mine = skh[2 * kb + half];
     const float sk0 = skh[2 * kb], sk1 = skh[2 * kb + 1];
-    const uint32_t qcol = (uint32_t)(QC * g);
+    const float sk_mine = g ? sk1 : sk0;  // scale of this group's 64-key block
+    const uint32_t kcol = (uint32_t)(64 * g);  // first key column of this group
     const uint32_t dcol = (uint32_t)(DG * g);
+    // P row t: keys [64g, 64g + 64) are 16-byte units 4g .. 4g+3 of the 128-byte row
     uint8_t* prow = sm.p + (t >> 3) * 1024 + (t & 7) * 128;
-    // dS^T row: query columns [qcol, qcol + QC) sit in 64-query block qcol/64, bytes 2*(qcol%64) on
-    uint8_t* dsrow = sm.ds + (qcol >> 6) * 16384 + (t >> 3) * 1024 + (t & 7) * 128;
-    const int ds_u0 = (int)((qcol & 63) * 2) >> 4;  // first 16-byte unit of this group in the row
+    // dS row t of this group's 64-key block: 128 bytes, units 0..7
+    uint8_t* dsrow = sm.ds + g * 16384 + (t >> 3) * 1024 + (t & 7) * 128;
+    // keys of this block that exist: columns kc >= klim_pad are padding
+    const int klim_pad = min(128, prm.N - kb * 128);
     float dk[DG];
 #pragma unroll
     for (int d = 0; d < DG; ++d) dk[d] = 0.f;
-    static_assert(NWG * (DG / 32) <= 4 && DG % 32 == 0, "dQ staging slots");
     int pending_qs = -1;  // Q buffer whose dQ boxes are still being read by TMA (elected thread)
+    // a wait that times out raises the abort flag; from then on this thread skips its waits
+    // but still runs every iteration, so no thread is left behind at a named barrier
     bool ok = true;
     float sq_next = prm.sq[(size_t)bh * prm.nqb + I0];
     for (int it = 0; it < n_it; ++it) {
@@ -416,51 +416,40 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
       const float sqI = sq_next;
       if (it + 1 < n_it) sq_next = prm.sq[(size_t)bh * prm.nqb + I + 1];
       const int qs = it & 1;
-      const float* s_bias = sm.bias[qs];
-      const float* s_dvec = sm.dvec[qs];
-      if (!mbar_wait(&sm.bar_q_full[qs], (it >> 1) & 1, abort)) {
-        ok = false;
-        break;
-      }
+      ok = ok && mbar_wait(&sm.bar_q_full[qs], (it >> 1) & 1, abort);
+      // this query row's scalars: P = 2^(S2 - LSE2) is formed as 2^(S2 + bias) / 448
+      const float bias_t = sm.bias[qs][t];
+      const float dvec_t = sm.dvec[qs][t];
       const float cs = __fmul_rn(__fmul_rn(sqI, sk_mine), prm.alpha);
-      const bool diag = prm.causal && I == kb;
-      if (!mbar_wait(&sm.bar_s, ph, abort)) {
-        ok = false;
-        break;
-      }
+      // masked key columns kc >= klim: padding, and keys after this query on the diagonal block
+      const int klim = (prm.causal && I == kb) ? min(klim_pad, t + 1) : klim_pad;
+      const bool any_mask = __any_sync(0xffffffffu, klim < (int)kcol + 64);
+      ok = ok && mbar_wait(&sm.bar_s, ph, abort);
       tc_fence_after();
-      // rows of padded keys and the causal diagonal block need a mask; warps with
-      // neither take the unmasked path
-      const bool any_mask = __any_sync(0xffffffffu, !key_ok || diag);
-      const int mask_lim = !key_ok ? 128 : (diag ? t : 0);  // queries qi < mask_lim are masked
-      // ---- P^T = e4m3(448 * 2^(S2 - LSE2)) on this thread's QC query columns, 32 per chunk.
-      // The codes go to shared memory for the dV MMA and stay in registers for dS.
-      constexpr int NCH = QC / 32;
-      uint32_t buf[NCH][32];
-      uint32_t pw[NCH][8];
+      // ---- P = e4m3(448 * 2^(S2 - LSE2)) on this row's 64 keys, 32 per chunk.  The codes go
+      // to shared memory for the dV MMA and stay in registers for dS.
+      uint32_t buf[2][32];
+      uint32_t pw[2][8];
 #pragma unroll
-      for (int c = 0; c < NCH; ++c) tmem_ld32(tmem + lane_base + cS + qcol + 32 * c, buf[c]);
+      for (int c = 0; c < 2; ++c) tmem_ld32(tmem + lane_base + cS + kcol + 32 * c, buf[c]);
       tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < NCH; ++c) reg_fence32(buf[c]);
+      for (int c = 0; c < 2; ++c) reg_fence32(buf[c]);
       {
-        const uint64_t cs2 = f2(cs, cs);
+        const uint64_t cs2 = f2(cs, cs), b2 = f2(bias_t, bias_t);
 #pragma unroll
-        for (int c = 0; c < NCH; ++c) {
+        for (int c = 0; c < 2; ++c) {
 #pragma unroll
           for (int e = 0; e < 32; e += 4) {
-            const float4 b4 = *reinterpret_cast<const float4*>(&s_bias[qcol + 32 * c + e]);
             float p[4];
-            f2split(ffma2(f2(__uint_as_float(buf[c][e]), __uint_as_float(buf[c][e + 1])), cs2, f2(b4.x, b4.y)), p[0],
-                    p[1]);
-            f2split(ffma2(f2(__uint_as_float(buf[c][e + 2]), __uint_as_float(buf[c][e + 3])), cs2, f2(b4.z, b4.w)),
-                    p[2], p[3]);
+            f2split(ffma2(f2(__uint_as_float(buf[c][e]), __uint_as_float(buf[c][e + 1])), cs2, b2), p[0], p[1]);
+            f2split(ffma2(f2(__uint_as_float(buf[c][e + 2]), __uint_as_float(buf[c][e + 3])), cs2, b2), p[2], p[3]);
 #pragma unroll
             for (int u = 0; u < 4; ++u) p[u] = ex2(p[u]);
             if (any_mask) {
 #pragma unroll
               for (int u = 0; u < 4; ++u)
-                if ((int)qcol + 32 * c + e + u < mask_lim) p[u] = 0.f;
+                if ((int)kcol + 32 * c + e + u >= klim) p[u] = 0.f;
             }
             const __nv_fp8x2_storage_t lo =
                 __nv_cvt_float2_to_fp8x2(make_float2(p[0], p[1]), __NV_SATFINITE, __NV_E4M3);
@@ -468,7 +457,7 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
                 __nv_cvt_float2_to_fp8x2(make_float2(p[2], p[3]), __NV_SATFINITE, __NV_E4M3);
             pw[c][e >> 2] = (uint32_t)lo | ((uint32_t)hi << 16);
           }
-          const int u0 = (int)(qcol >> 4) + 2 * c;  // 16-byte units of this chunk in the 128-byte row
+          const int u0 = 4 * g + 2 * c;
           *reinterpret_cast<uint4*>(prow + ((u0 ^ (t & 7)) << 4)) =
               make_uint4(pw[c][0], pw[c][1], pw[c][2], pw[c][3]);
           *reinterpret_cast<uint4*>(prow + (((u0 + 1) ^ (t & 7)) << 4)) =
@@ -477,70 +466,60 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
       }
       fence_proxy_async_smem();
       mbar_arrive(&sm.bar_p);
-      // ---- dS^T * 448 = p8 (dP^T - D), kept in registers until the tile scale is known
-      if (!mbar_wait(&sm.bar_dp, ph, abort)) {
-        ok = false;
-        break;
-      }
+      // ---- 448 dS = p8 (dP - D_i), kept in registers until the tile scale is known
+      ok = ok && mbar_wait(&sm.bar_dp, ph, abort);
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < NCH; ++c) tmem_ld32(tmem + lane_base + cDP + qcol + 32 * c, buf[c]);
+      for (int c = 0; c < 2; ++c) tmem_ld32(tmem + lane_base + cDP + kcol + 32 * c, buf[c]);
       tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < NCH; ++c) reg_fence32(buf[c]);
+      for (int c = 0; c < 2; ++c) reg_fence32(buf[c]);
       float amax = 0.f;
+      {
+        const uint64_t d2 = f2(dvec_t, dvec_t);
 #pragma unroll
-      for (int c = 0; c < NCH; ++c) {
+        for (int c = 0; c < 2; ++c) {
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(&s_dvec[qcol + 32 * c + e]);
-          const uint32_t w = pw[c][e >> 2];
-          const __half2_raw h01 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xffffu), __NV_E4M3);
-          const __half2_raw h23 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
-          const float2 p01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
-          const float2 p23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
-          float x[4];
-          f2split(fmul2(f2(p01.x, p01.y),
-                        fsub2(f2(__uint_as_float(buf[c][e]), __uint_as_float(buf[c][e + 1])), f2(d4.x, d4.y))),
-                  x[0], x[1]);
-          f2split(fmul2(f2(p23.x, p23.y),
-                        fsub2(f2(__uint_as_float(buf[c][e + 2]), __uint_as_float(buf[c][e + 3])), f2(d4.z, d4.w))),
-                  x[2], x[3]);
-          amax = max3(amax, fabsf(x[0]), fabsf(x[1]));
-          amax = max3(amax, fabsf(x[2]), fabsf(x[3]));
+          for (int e = 0; e < 32; e += 4) {
+            const uint32_t w = pw[c][e >> 2];
+            const __half2_raw h01 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xffffu), __NV_E4M3);
+            const __half2_raw h23 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
+            const float2 p01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+            const float2 p23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+            float x[4];
+            f2split(fmul2(f2(p01.x, p01.y), fsub2(f2(__uint_as_float(buf[c][e]), __uint_as_float(buf[c][e + 1])), d2)),
+                    x[0], x[1]);
+            f2split(fmul2(f2(p23.x, p23.y),
+                          fsub2(f2(__uint_as_float(buf[c][e + 2]), __uint_as_float(buf[c][e + 3])), d2)),
+                    x[2], x[3]);
+            amax = max3(amax, fabsf(x[0]), fabsf(x[1]));
+            amax = max3(amax, fabsf(x[2]), fabsf(x[3]));
 #pragma unroll
-          for (int u = 0; u < 4; ++u) buf[c][e + u] = __float_as_uint(x[u]);
+            for (int u = 0; u < 4; ++u) buf[c][e + u] = __float_as_uint(x[u]);
+          }
         }
       }
 #pragma unroll
       for (int m = 16; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
       if (lane == 0) sm.smax[warp] = amax;
-      // the previous iteration's dQ boxes must be read before dS^T is rewritten below and
-      // before the producer refills that Q buffer
+      // the previous iteration's dQ boxes (this group's dS block and Q half) must be read
+      // before the block is rewritten below and before the producer refills that Q buffer
       if (t == 0 && pending_qs >= 0) {
         bulk_wait_read_all();
         mbar_arrive(&sm.bar_q_free[pending_qs]);
         pending_qs = -1;
       }
-      named_bar_compute<NWG>();
-      // tile max over the 64 key rows of each half and all 128 queries (every group)
-      float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-      for (int w = 0; w < 4 * NWG; ++w) {
-        if ((w & 3) < 2)
-          a0 = fmaxf(a0, sm.smax[w]);
-        else
-          a1 = fmaxf(a1, sm.smax[w]);
-      }
-      const float amine = half ? a1 : a0;
+      named_bar_group(g);
+      // the group's tile (128 queries x 64 keys) max; values are 448 dS
+      const float amine = fmaxf(fmaxf(sm.smax[4 * g], sm.smax[4 * g + 1]), fmaxf(sm.smax[4 * g + 2], sm.smax[4 * g + 3]));
       const float inv = amine > 0.f ? 127.0f / amine : 0.f;  // code = rint(448 dS * 127 / max|448 dS|)
-      // ---- dS^T codes -> shared memory (bf16 containers, 128B-swizzled key rows).  Rounding to
+      // ---- dS codes -> shared memory (bf16 containers, 128B-swizzled query rows).  Rounding to
       // the nearest integer (ties to even) stays in the fp32 pipe: RN(x * inv + 1.5 * 2^23) - 1.5 * 2^23;
       // |x * inv| <= 127 (plus rounding), so no clamp is needed
       {
         const uint64_t inv2 = f2(inv, inv), magic2 = f2(kRoundMagic, kRoundMagic);
 #pragma unroll
-        for (int c = 0; c < NCH; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t packed[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
@@ -552,24 +531,25 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
           }
 #pragma unroll
           for (int u = 0; u < 4; ++u)
-            *reinterpret_cast<uint4*>(dsrow + (((ds_u0 + 4 * c + u) ^ (t & 7)) << 4)) =
+            *reinterpret_cast<uint4*>(dsrow + (((4 * c + u) ^ (t & 7)) << 4)) =
                 make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&sm.bar_ds);
+      mbar_arrive(&sm.bar_ds[g]);
+      // ---- dK += RN(s_dS * s_q) * part (key row t);  dQ (query row t) += ca * part0 + cb * part1
+      ok = ok && mbar_wait(&sm.bar_dk, ph, abort);
+      tc_fence_after();
+      // the other group's tile max: its codes are in (bar_dk completed after both groups' codes),
+      // and the waits below make its smax writes visible here
+      ok = ok && mbar_wait(&sm.bar_ds[0], ph, abort) && mbar_wait(&sm.bar_ds[1], ph, abort);
+      const float a0 = fmaxf(fmaxf(sm.smax[0], sm.smax[1]), fmaxf(sm.smax[2], sm.smax[3]));
+      const float a1 = fmaxf(fmaxf(sm.smax[4], sm.smax[5]), fmaxf(sm.smax[6], sm.smax[7]));
       // values are 448 * dS: scale s_dS = max|dS| / 127
       const float sds0 = a0 > 0.f ? __fdiv_rn(a0 * (1.0f / 448.0f), 127.0f) : 0.f;
       const float sds1 = a1 > 0.f ? __fdiv_rn(a1 * (1.0f / 448.0f), 127.0f) : 0.f;
-      if (!mbar_wait(&sm.bar_dk, ph, abort)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      // ---- dK += RN(s_dS * s_q) * part;  dQ (query row t of block I) += ca * half0 + cb * half1
-      // (this group's DG columns), TMEM loads pipelined as above
-      const float ck = __fmul_rn(half ? sds1 : sds0, sqI);
+      const float ck = __fmul_rn(t >> 6 ? sds1 : sds0, sqI);
       const float ca = __fmul_rn(sds0, sk0), cb = __fmul_rn(sds1, sk1);
       {
         uint32_t kA[16], kB[16];
@@ -587,23 +567,19 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
           if (c + 32 < DG) tmem_wait16(kA);
         }
       }
-      // the dK part is in registers: the next S^T may overwrite its columns
+      // the dK part is in registers: the next S may overwrite its columns
       tc_fence_before();
       mbar_arrive(&sm.bar_free_s);
-      if (!mbar_wait(&sm.bar_part, ph, abort)) {
-        ok = false;
-        break;
-      }
+      ok = ok && mbar_wait(&sm.bar_part, ph, abort);
       tc_fence_after();
       {
-        // staging slot of box b (features dcol + 32b ..): 0,1 -> dS^T blocks, 2,3 -> halves of q[qs]
+        // staging slot of box b (features dcol + 32b ..): this group's dS block, then half g of q[qs]
         auto slot = [&](int b) -> float* {
-          const int sidx = g * (DG / 32) + b;
-          return reinterpret_cast<float*>(sidx < 2 ? sm.ds + sidx * 16384 : sm.q[qs] + (sidx - 2) * 16384);
+          return reinterpret_cast<float*>(b == 0 ? sm.ds + g * 16384 : sm.q[qs] + g * 16384);
         };
         uint32_t va[2][16], vb[2][16];
-        tmem_ld16(tmem + lane_base + cDP + dcol, va[0]);
-        tmem_ld16(tmem + lane_base + cDQB + dcol, vb[0]);
+        tmem_ld16(tmem + lane_base + cDQ0 + dcol, va[0]);
+        tmem_ld16(tmem + lane_base + cDQ1 + dcol, vb[0]);
         tmem_ld_wait();
         reg_fence16(va[0]);
         reg_fence16(vb[0]);
@@ -611,10 +587,10 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
         for (int c = 0; c < DG; c += 16) {
           const int cur = (c >> 4) & 1;
           if (c + 16 < DG) {
-            tmem_ld16(tmem + lane_base + cDP + dcol + c + 16, va[cur ^ 1]);
-            tmem_ld16(tmem + lane_base + cDQB + dcol + c + 16, vb[cur ^ 1]);
+            tmem_ld16(tmem + lane_base + cDQ0 + dcol + c + 16, va[cur ^ 1]);
+            tmem_ld16(tmem + lane_base + cDQ1 + dcol + c + 16, vb[cur ^ 1]);
           } else {
-            // every TMEM read of this iteration is done: the next dP^T may start
+            // every TMEM read of this iteration is done: the next dP may start
             tc_fence_before();
             mbar_arrive(&sm.bar_free_dp);
           }
@@ -642,14 +618,16 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
     // the last reductions must complete before the CTA's shared memory goes away
     if (t == 0) bulk_wait_all();
     // ---------------- epilogue: dK then dV rows of this key block, this group's columns
-    if (ok) {
+    // (after a timed-out wait the results are not stored, but every thread still takes part
+    // in the barriers below)
+    {
       tc_fence_after();
       const size_t orow = ((size_t)bh * prm.N + key) * D;
 #pragma unroll
       for (int d = 0; d < DG; ++d) dk[d] *= prm.sm_scale;
       const uint4* krow = reinterpret_cast<const uint4*>(prm.K + orow + dcol);
       if (prm.qk_norm) {
-        // dk = r (dk' - k' (k' . dk')), k' = RN(k r): the dot spans every group's columns
+        // dk = r (dk' - k' (k' . dk')), k' = RN(k r): the dot spans both groups' columns
         const float r = key_ok ? prm.kr[(size_t)bh * prm.np + key] : 0.f;
         float dot = 0.f;
         if (key_ok) {
@@ -661,17 +639,12 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
             for (int e = 0; e < 8; ++e) dot = fmaf(__fmul_rn(f[e], r), dk[c * 8 + e], dot);
           }
         }
-        // partial dot products through the (now idle) per-query rows: bias and dvec are
-        // adjacent, 4 x 128 floats in all
-        static_assert(offsetof(BwdSmem<D>, dvec) == offsetof(BwdSmem<D>, bias) + sizeof(sm.bias) && NWG <= 4,
-                      "exchange buffer layout");
+        // partial dot products through the (now idle) bias rows
         float* xch = &sm.bias[0][0];
-        named_bar_compute<NWG>();
+        named_bar_compute();
         xch[g * 128 + t] = dot;
-        named_bar_compute<NWG>();
-        dot = 0.f;
-#pragma unroll
-        for (int q = 0; q < NWG; ++q) dot += xch[q * 128 + t];
+        named_bar_compute();
+        dot = xch[t] + xch[128 + t];
         if (key_ok) {
 #pragma unroll
           for (int c = 0; c < DG / 8; ++c) {
@@ -682,7 +655,7 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
           }
         }
       }
-      if (key_ok) {
+      if (key_ok && ok) {
         uint4* dstk = reinterpret_cast<uint4*>(prm.dK + orow + dcol);
 #pragma unroll
         for (int c = 0; c < DG / 8; ++c) {
@@ -699,7 +672,7 @@ __global__ void __launch_bounds__((NWG + 1) * 128, 1)
         uint32_t v[16];
         tmem_ld16(tmem + lane_base + cDV + dcol + c, v);
         tmem_wait16(v);
-        if (key_ok) {
+        if (key_ok && ok) {
           uint4* dstv = reinterpret_cast<uint4*>(prm.dV + orow + dcol + c);
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
@@ -772,15 +745,15 @@ __global__ void __launch_bounds__(kPreThreads) bwd_dq_kernel(const float* __rest
   }
 }
 
-template <int D, int NWG>
+template <int D>
 int launch_main_t(const CUtensorMap& tk, const CUtensorMap& tq, const CUtensorMap& tv, const CUtensorMap& tdo,
                   const CUtensorMap& tdo8, const CUtensorMap& tdq, const BwdParams& p, int BH, cudaStream_t st) {
   size_t smem = sizeof(BwdSmem<D>);
   if (smem < 120 * 1024) smem = 120 * 1024;  // one CTA per SM: it holds all 512 TMEM columns
-  auto kern = bwd_main_kernel<D, NWG>;
+  auto kern = bwd_main_kernel<D>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 3;
   ScopedTimer timer("bwd_main", st);
-  kern<<<dim3(p.nqb, BH), (NWG + 1) * 128, smem, st>>>(tk, tq, tv, tdo, tdo8, tdq, p);
+  kern<<<dim3(p.nqb, BH), 384, smem, st>>>(tk, tq, tv, tdo, tdo8, tdq, p);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 
@@ -844,12 +817,11 @@ int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const
   p.dvec = dvec;
   p.K = static_cast<const __nv_bfloat16*>(K);
   p.kr = reinterpret_cast<const float*>(w + QL.kr);
-  p.dqacc = dqacc;
   p.dK = static_cast<__nv_bfloat16*>(dK);
   p.dV = static_cast<__nv_bfloat16*>(dV);
   p.status = reinterpret_cast<int*>(const_cast<uint8_t*>(w) + QL.status);
-  int rc = D == 128 ? launch_main_t<128, kBwdGroups>(tk, tq, tv, tdo, tdo8, tdq, p, BH, st)
-                    : launch_main_t<64, kBwdGroups>(tk, tq, tv, tdo, tdo8, tdq, p, BH, st);
+  int rc = D == 128 ? launch_main_t<128>(tk, tq, tv, tdo, tdo8, tdq, p, BH, st)
+                    : launch_main_t<64>(tk, tq, tv, tdo, tdo8, tdq, p, BH, st);
   if (rc) return rc;
   const float* qr = reinterpret_cast<const float*>(w + QL.qr);
   auto* q = static_cast<const __nv_bfloat16*>(Q);

@@ -299,11 +299,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
          | ((uint32_t)(N >> 3) << 17)          // N / 8
          | ((uint32_t)(M >> 4) << 24);         // M / 16
 }
-__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
-  return (1u << 4)                     // D = F32
-         | (0u << 7) | (0u << 10)      // A = B = E4M3
-         | ((uint32_t)(N >> 3) << 17)  // N / 8
-         | ((uint32_t)(M >> 4) << 24); // M / 16
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool a_mn_major = false) {
+  return (1u << 4)                         // D = F32
+         | (0u << 7) | (0u << 10)          // A = B = E4M3
+         | ((a_mn_major ? 1u : 0u) << 15)  // A major-ness
+         | ((uint32_t)(N >> 3) << 17)      // N / 8
+         | ((uint32_t)(M >> 4) << 24);     // M / 16
 }
 
 // byte offset of element (row, byte-in-row) inside a 128B-swizzled block of rows
