@@ -80,6 +80,20 @@ __device__ __noinline__ uint32_t exact_p_code(float t) {
   return (uint32_t)__nv_cvt_float_to_fp8(__fmul_rn(448.0f, pt), __NV_SATFINITE, __NV_E4M3);
 }
 
+// a[e] for a run-time e, by a tree of selects (a stays in registers)
+__device__ __forceinline__ uint32_t pick32(const uint32_t (&a)[32], int e) {
+  uint32_t b[16], c[8], d[4], f[2];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) b[i] = (e & 16) ? a[i + 16] : a[i];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) c[i] = (e & 8) ? b[i + 8] : b[i];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d[i] = (e & 4) ? c[i + 4] : c[i];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) f[i] = (e & 2) ? d[i + 2] : d[i];
+  return (e & 1) ? f[1] : f[0];
+}
+
 __device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float d) {
   const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
   const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
@@ -103,14 +117,18 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
   uint8_t* prow = sm.p[X] + (t >> 3) * 1024 + (t & 7) * 128;
   float m = -INFINITY, l = 0.f;
   bool ok = true;
+  // the K-block scales of a tile are fetched one tile early (global latency off the path)
+  float2 sk_next = *reinterpret_cast<const float2*>(skh);
   for (int j = 0; j < n_tiles; ++j) {
+    const float2 skj = sk_next;
+    if (j + 1 < n_tiles) sk_next = *reinterpret_cast<const float2*>(skh + 2 * (j + 1));
     if (!mbar_wait(&sm.bar_s_full[X], j & 1, abort)) {
       ok = false;
       break;
     }
     tc_fence_after();
-    const float c0 = __fmul_rn(__fmul_rn(s_q, skh[2 * j]), prm.alpha);
-    const float c1 = __fmul_rn(__fmul_rn(s_q, skh[2 * j + 1]), prm.alpha);
+    const float c0 = __fmul_rn(__fmul_rn(s_q, skj.x), prm.alpha);
+    const float c1 = __fmul_rn(__fmul_rn(s_q, skj.y), prm.alpha);
     const int kbase = j * 128;
     const bool masked_tile = (kbase + 128 > prm.N) || (CAUSAL && j == qb);
     int lim = prm.N - kbase;  // keys [0, lim) of the tile are valid
@@ -172,9 +190,7 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
       const int hl = lim - h * 64;
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
-        struct {
-          uint32_t w[8];
-        } w;
+        uint32_t w[8];
         uint32_t band = ~0u;
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
@@ -192,24 +208,24 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
             lsum = fadd2(lsum, f2(x[u], x[u + 1]));
             band = min(band, min(band_key(x[u]), band_key(x[u + 1])));
           }
-          w.w[e >> 2] = pack4_e4m3(x[0], x[1], x[2], x[3]);
+          w[e >> 2] = pack4_e4m3(x[0], x[1], x[2], x[3]);
         }
-        // rare: codes whose fast value is near an e4m3 midpoint are redone exactly
+        const int c = 2 * h + q;  // 32-key chunk of the row: 16-byte units 2c, 2c+1
+        *reinterpret_cast<uint4*>(prow + (((2 * c) ^ (t & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(prow + (((2 * c + 1) ^ (t & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+        // rare: codes whose fast value is near an e4m3 midpoint are redone exactly and
+        // patched in shared memory (a short loop keeps this path out of the hot code)
         if (band <= kBandMax) {
-#pragma unroll
+#pragma unroll 1
           for (int e = 0; e < 32; ++e) {
-            const float tt = fmaf(__uint_as_float(sh[q][e]), cc, -m_new);
+            const float tt = fmaf(__uint_as_float(pick32(sh[q], e)), cc, -m_new);
             const float xv = ex2(tt) * 448.f;
             if (band_key(xv) <= kBandMax && (!masked_tile || q * 32 + e < hl)) {
-              const uint32_t code = exact_p_code(tt);
-              w.w[e >> 2] = (w.w[e >> 2] & ~(0xffu << ((e & 3) * 8))) | (code << ((e & 3) * 8));
+              const int byte = 32 * c + e;  // key column in the row
+              prow[((((byte >> 4) ^ (t & 7)) << 4)) | (byte & 15)] = (uint8_t)exact_p_code(tt);
             }
           }
         }
-        const int c = 2 * h + q;  // 32-key chunk of the row: 16-byte units 2c, 2c+1
-        *reinterpret_cast<uint4*>(prow + (((2 * c) ^ (t & 7)) << 4)) = make_uint4(w.w[0], w.w[1], w.w[2], w.w[3]);
-        *reinterpret_cast<uint4*>(prow + (((2 * c + 1) ^ (t & 7)) << 4)) =
-            make_uint4(w.w[4], w.w[5], w.w[6], w.w[7]);
       }
     }
     if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
@@ -318,10 +334,10 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort = &sm.abort;
 
-  if (warp < 4) {
-    softmax_tile_loop<D, CAUSAL>(sm, prm, 0, qbA, bh, tmem, abort);
-  } else if (warp < 8) {
-    if (hasB) softmax_tile_loop<D, CAUSAL>(sm, prm, 1, qbB, bh, tmem, abort);
+  if (warp < 8) {
+    // one call site, so both warpgroups run (and share instruction-cache lines of) one copy
+    const int X = warp >> 2;
+    if (X == 0 || hasB) softmax_tile_loop<D, CAUSAL>(sm, prm, X, X ? qbB : qbA, bh, tmem, abort);
   } else if (warp == 8 && lane == 0) {
     // ---------------- producer: Q tiles once, then K and V tiles
     tma_prefetch_desc(&tm_q);
