@@ -65,18 +65,70 @@ __device__ __forceinline__ float ex2(float x) {
 // midpoint of e4m3: fp32 mantissa bit 19 set and bits 18..0 clear.  The fast
 // value 448 * ex2.approx(t) is within 2 ulps of x (measured over 2^26 values of
 // t in [-16, 0]), so a code is trusted unless the fast value lies within
-// kBandUlps of such a midpoint; those few are recomputed with a correctly
-// rounded exp2.  band_key(x) <= kBandMax marks them.
-constexpr uint32_t kBandUlps = 8;
+// kBandUlps (twice that error) of such a midpoint; those few are recomputed from
+// an accurate 2^t.  band_key(x) <= kBandMax marks them.  (Below 2^-6, e4m3 is
+// subnormal and its midpoints are coarser; a flip there moves P by 2^-9 / 448 at most.)
+constexpr uint32_t kBandUlps = 4;
 constexpr uint32_t kBandC = (kBandUlps - 0x80000u) << 12;
 constexpr uint32_t kBandMax = (2u * kBandUlps) << 12;
 __device__ __forceinline__ uint32_t band_key(float x) { return __float_as_uint(x) * 4096u + kBandC; }
 
+// Pairs of fp32 (hi + lo) as extended precision: error-free transformations of
+// Knuth (two-sum) and Dekker (fast two-sum, two-product via FMA).
+struct F2x {
+  float h, l;
+};
+__device__ __forceinline__ F2x fast_two_sum(float a, float b) {  // |a| >= |b|
+  const float s = __fadd_rn(a, b);
+  return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+__device__ __forceinline__ F2x two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  return {s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb))};
+}
+__device__ __forceinline__ F2x f2x_mul(F2x a, F2x b) {
+  const float p = __fmul_rn(a.h, b.h);
+  const float e = fmaf(a.h, b.h, -p) + fmaf(a.h, b.l, __fmul_rn(a.l, b.h));
+  return fast_two_sum(p, e);
+}
+__device__ __forceinline__ F2x f2x_add(F2x a, F2x b) {
+  const F2x s = two_sum(a.h, b.h);
+  return fast_two_sum(s.h, __fadd_rn(s.l, __fadd_rn(a.l, b.l)));
+}
 
-// e4m3 code of RN(448 * RN(2^t)) with 2^t evaluated in fp64 and rounded once.
-// Out of line with a scalar argument: the rare path adds little code.
-__device__ __noinline__ uint32_t exact_p_code(float t) {
-  const float pt = (float)exp2((double)t);
+// e4m3 code of RN(448 * RN(2^t)).  t = n + f with n = rint(t) and |f| <= 1/2 (exact);
+// 2^f = e^y, y = f ln 2, from the Taylor series of e^y to degree 12 (truncation below
+// 2^-50 for |y| < 0.35): degrees 7..12 in fp32, 0..6 in fp32 pairs, so 2^f carries about
+// 2^-45 relative error and its leading fp32 is RN(2^f) except within that distance of
+// an fp32 midpoint.  Scaling by 2^n is exact in the normal range.
+__device__ __forceinline__ uint32_t exact_p_code(float t) {
+  if (!(t >= -125.f)) return 0u;  // 448 * 2^t is far below the smallest e4m3 subnormal
+  const float n = rintf(t);
+  const float f = __fsub_rn(t, n);
+  const float kLn2Hi = 0x1.62e430p-1f, kLn2Lo = -0x1.05c610p-29f;
+  const float yh0 = __fmul_rn(f, kLn2Hi);
+  const F2x y = fast_two_sum(yh0, fmaf(f, kLn2Hi, -yh0) + __fmul_rn(f, kLn2Lo));
+  // 1/k! for k = 7..12 (fp32) and k = 0..6 (hi, lo)
+  const float c12 = 2.0876755879584152e-09f, c11 = 2.5052107943679403e-08f, c10 = 2.755731998149713e-07f,
+              c9 = 2.7557318844628753e-06f, c8 = 2.4801587642286904e-05f, c7 = 0.00019841270113829523f;
+  float q = c12;
+  q = fmaf(q, y.h, c11);
+  q = fmaf(q, y.h, c10);
+  q = fmaf(q, y.h, c9);
+  q = fmaf(q, y.h, c8);
+  q = fmaf(q, y.h, c7);
+  const F2x c[7] = {{1.0f, 0.0f},
+                    {1.0f, 0.0f},
+                    {0.5f, 0.0f},
+                    {0.1666666716337204f, -4.967053879312289e-09f},
+                    {0.0416666679084301f, -1.2417634698280722e-09f},
+                    {0.008333333767950535f, -4.34617203337595e-10f},
+                    {0.0013888889225199819f, -3.3631094437103215e-11f}};
+  F2x r = {q, 0.0f};
+#pragma unroll
+  for (int k = 6; k >= 0; --k) r = f2x_add(f2x_mul(r, y), c[k]);
+  const float pt = __fmul_rn(r.h, __int_as_float(((int)n + 127) << 23));
   return (uint32_t)__nv_cvt_float_to_fp8(__fmul_rn(448.0f, pt), __NV_SATFINITE, __NV_E4M3);
 }
 
@@ -188,10 +240,10 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
       const float cc = h == 0 ? c0 : c1;
       const uint64_t cc2 = f2(cc, cc);
       const int hl = lim - h * 64;
+      uint32_t band = ~0u;  // smallest band key of the 64 codes of this half
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         uint32_t w[8];
-        uint32_t band = ~0u;
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
           float x[4];
@@ -213,18 +265,29 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
         const int c = 2 * h + q;  // 32-key chunk of the row: 16-byte units 2c, 2c+1
         *reinterpret_cast<uint4*>(prow + (((2 * c) ^ (t & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         *reinterpret_cast<uint4*>(prow + (((2 * c + 1) ^ (t & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
-        // rare: codes whose fast value is near an e4m3 midpoint are redone exactly and
-        // patched in shared memory (a short loop keeps this path out of the hot code)
-        if (band <= kBandMax) {
-#pragma unroll 1
-          for (int e = 0; e < 32; ++e) {
-            const float tt = fmaf(__uint_as_float(pick32(sh[q], e)), cc, -m_new);
-            const float xv = ex2(tt) * 448.f;
-            if (band_key(xv) <= kBandMax && (!masked_tile || q * 32 + e < hl)) {
-              const int byte = 32 * c + e;  // key column in the row
-              prow[((((byte >> 4) ^ (t & 7)) << 4)) | (byte & 15)] = (uint8_t)exact_p_code(tt);
-            }
-          }
+      }
+      // rare: codes whose fast value is near an e4m3 midpoint are redone exactly and
+      // patched in shared memory (one site for the half's 64 codes)
+      if (band <= kBandMax) {
+        uint64_t flags = 0;
+        // the fast values are recomputed with the very instruction sequence of the loop above
+#pragma unroll
+        for (int e = 0; e < 64; e += 2) {
+          float t0, t1, x0, x1;
+          f2split(ffma2(f2(__uint_as_float(sh[e >> 5][e & 31]), __uint_as_float(sh[e >> 5][(e & 31) + 1])), cc2,
+                        neg_m2),
+                  t0, t1);
+          f2split(fmul2(f2(ex2(t0), ex2(t1)), k448), x0, x1);
+          if (band_key(x0) <= kBandMax && (!masked_tile || e < hl)) flags |= 1ull << e;
+          if (band_key(x1) <= kBandMax && (!masked_tile || e + 1 < hl)) flags |= 1ull << (e + 1);
+        }
+        while (flags) {
+          const int e = __ffsll((long long)flags) - 1;
+          flags &= flags - 1;
+          const uint32_t v = (e & 32) ? pick32(sh[1], e & 31) : pick32(sh[0], e & 31);
+          const int byte = 64 * h + e;  // key column in the row
+          prow[((((byte >> 4) ^ (t & 7)) << 4)) | (byte & 15)] =
+              (uint8_t)exact_p_code(fmaf(__uint_as_float(v), cc, -m_new));
         }
       }
     }
