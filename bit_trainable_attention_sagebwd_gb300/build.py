@@ -7,13 +7,16 @@ from __future__ import annotations
 
 import concurrent.futures as cf
 import glob
+import hashlib
 import os
+import platform
 import subprocess
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsage_attn.so")
+STAMP = os.path.join(OUT_DIR, "libsage_attn.stamp")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I" + os.path.join(os.path.dirname(HERE), "include")]
@@ -35,11 +38,24 @@ def _deps():
         [os.path.join(os.path.dirname(HERE), "include", "sage_attn.h")]
 
 
+def _fingerprint() -> str:
+    """Hash of every source byte, the flags and the host machine: a library built from
+    other sources, with other flags or for another CPU architecture is rebuilt."""
+    h = hashlib.sha256()
+    for p in sorted(_deps()):
+        h.update(os.path.basename(p).encode())
+        with open(p, "rb") as f:
+            h.update(f.read())
+    h.update(" ".join(ARCH + FLAGS[:-1]).encode())
+    h.update(platform.machine().encode())
+    return h.hexdigest()
+
+
 def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+    if not (os.path.exists(LIB) and os.path.exists(STAMP)):
         return False
-    t = os.path.getmtime(LIB)
-    return all(os.path.getmtime(p) <= t for p in _deps())
+    with open(STAMP) as f:
+        return f.read().strip() == _fingerprint()
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
@@ -69,6 +85,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(STAMP, "w") as f:
+        f.write(_fingerprint() + "\n")
     return LIB
 
 

@@ -26,15 +26,32 @@ _lock = threading.Lock()
 _lib = None
 
 
+_CMD = ["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fno-fast-math", "-fexcess-precision=standard", "-fPIC",
+        "-shared"]
+
+
+def _fingerprint() -> str:
+    """Source bytes, flags and host machine: a library built otherwise is rebuilt."""
+    import hashlib
+    import platform
+    h = hashlib.sha256(open(_SRC, "rb").read())
+    h.update(" ".join(_CMD).encode())
+    h.update(platform.machine().encode())
+    return h.hexdigest()
+
+
 def build(force: bool = False) -> str:
     """Compile the oracle (plain C, OpenMP, IEEE operations only)."""
     os.makedirs(os.path.dirname(_OUT), exist_ok=True)
-    if force or not os.path.exists(_OUT) or os.path.getmtime(_OUT) < os.path.getmtime(_SRC):
+    stamp = _OUT + ".stamp"
+    fp = _fingerprint()
+    fresh = os.path.exists(_OUT) and os.path.exists(stamp) and open(stamp).read().strip() == fp
+    if force or not fresh:
         tmp = _OUT + f".{os.getpid()}.tmp"
-        cmd = ["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
-               "-fexcess-precision=standard", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
-        subprocess.run(cmd, check=True)
+        subprocess.run(_CMD + ["-o", tmp, _SRC, "-lm"], check=True)
         os.replace(tmp, _OUT)
+        with open(stamp, "w") as f:
+            f.write(fp + "\n")
     return _OUT
 
 
