@@ -29,6 +29,7 @@
 #include <cuda_fp8.h>
 
 #include "../../include/sage_attn.h"
+#include "codes.cuh"
 #include "kernels.h"
 #include "layout.h"
 #include "ptx.cuh"
@@ -133,9 +134,12 @@ __global__ void __launch_bounds__(kPreThreads) bwd_do8_kernel(const __nv_bfloat1
   const int tid = threadIdx.x, g = tid % TPR, ro = tid / TPR;
   const size_t head = (size_t)bh * N * D;
   __shared__ __align__(16) uint8_t s8[D][128];
-  float sc[8];
+  float sc[8], inv[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) sc[i] = sdo[(size_t)bh * D + g * 8 + i];
+  for (int i = 0; i < 8; ++i) {
+    sc[i] = sdo[(size_t)bh * D + g * 8 + i];
+    inv[i] = sc[i] > 0.f ? __frcp_rn(sc[i]) : 0.f;
+  }
 #pragma unroll
   for (int p = 0; p < PASSES; ++p) {
     const int row = p * RPP + ro, t = blk * 128 + row;
@@ -146,8 +150,7 @@ __global__ void __launch_bounds__(kPreThreads) bwd_do8_kernel(const __nv_bfloat1
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int d = g * 8 + i;
-      const float y = sc[i] > 0.f ? __fdiv_rn(x[i], sc[i]) : 0.f;
-      s8[d][row ^ (((d >> 3) & 15) << 2)] = __nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3);
+      s8[d][row ^ (((d >> 3) & 15) << 2)] = (uint8_t)e4m3_code(x[i], sc[i], inv[i]);
     }
   }
   __syncthreads();

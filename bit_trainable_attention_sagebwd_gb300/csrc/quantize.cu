@@ -12,6 +12,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
+#include "codes.cuh"
 #include "kernels.h"
 #include "layout.h"
 #include "timer.h"
@@ -87,12 +88,6 @@ __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, m));
   return v;
-}
-
-__device__ __forceinline__ int int8_code(float x, float s) {
-  if (s == 0.f) return 0;
-  int c = __float2int_rn(__fdiv_rn(x, s));
-  return c > 127 ? 127 : (c < -127 ? -127 : c);
 }
 
 // ---------------------------------------------------------------------------
@@ -205,9 +200,12 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(
 
   if (which == 2) {
     // ---- V: e4m3 codes with channel scales, transposed through shared memory
-    float svv[8];
+    float svv[8], inv[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) svv[i] = sv[(size_t)bh * D + g * 8 + i];
+    for (int i = 0; i < 8; ++i) {
+      svv[i] = sv[(size_t)bh * D + g * 8 + i];
+      inv[i] = svv[i] > 0.f ? __frcp_rn(svv[i]) : 0.f;
+    }
 #pragma unroll
     for (int p = 0; p < PASSES; ++p) {
       const int row = p * RPP + ro;
@@ -215,10 +213,9 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(
       unpack8(raw[p], v);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float y = svv[i] > 0.f ? __fdiv_rn(v[i], svv[i]) : 0.f;
         const int d = g * 8 + i;
-        // round to nearest even, saturating to +-448
-        s_v8[d][row ^ (((d >> 3) & 15) << 2)] = __nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3);
+        // e4m3(RN(v / s_v)): round to nearest even, saturating to +-448
+        s_v8[d][row ^ (((d >> 3) & 15) << 2)] = (uint8_t)e4m3_code(v[i], svv[i], inv[i]);
       }
     }
     __syncthreads();
@@ -269,13 +266,14 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(
     s_red[1][warp] = am[1];
   }
   __syncthreads();
-  float sc[2];
+  float sc[2], inv[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     float a = 0.f;
 #pragma unroll
     for (int w = 0; w < kThreads / 32; ++w) a = fmaxf(a, s_red[h][w]);
     sc[h] = a > 0.f ? __fdiv_rn(a, 127.0f) : 0.f;
+    inv[h] = sc[h] > 0.f ? __frcp_rn(sc[h]) : 0.f;
   }
   if (!isk) {
     if (tid == 0) sq[(size_t)bh * nb + blk] = sc[0];
@@ -285,10 +283,11 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(
   __nv_bfloat16* dst = isk ? kc : qc;
 #pragma unroll
   for (int p = 0; p < PASSES; ++p) {
-    const float s = isk ? sc[(p * RPP + ro) >= 64] : sc[0];
+    const int hs = isk && (p * RPP + ro) >= 64;
+    const float s = sc[hs], si = inv[hs];
     float c[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) c[i] = (float)int8_code(x[p][i], s);
+    for (int i = 0; i < 8; ++i) c[i] = int_code(x[p][i], s, si);
     reinterpret_cast<uint4*>(dst + phead + (size_t)(blk * 128 + p * RPP + ro) * D)[g] = pack8_bf16(c);
   }
 }

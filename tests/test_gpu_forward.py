@@ -68,3 +68,34 @@ def test_forward_p_codes_exact(w):
         b, h = divmod(bh, w.H)
         err = float(np.abs(g["O32"][b, h].cpu().numpy().astype(np.float64) - r["O32"]).max())
         assert err <= O_EXACT_ATOL, f"O32 error {err} at head {bh}: a P code differs from the oracle's"
+
+
+def _boundary_inputs():
+    """Q, K and V values whose quotients by their scales sit exactly on rounding boundaries:
+    INT8 half-integers (k + 1/2) and e4m3 midpoints, normal and subnormal."""
+    import numpy as np
+    w = wl.custom(1, 1, 256, 128, False, k_smooth=False, seed=31, name="boundaries")
+    x = wl.all_inputs(w)
+    rng = np.random.default_rng(5)
+    # INT8: block max 127/8 gives the scale 1/8 exactly; (k + 1/2)/8 are exact bf16 values
+    half = (np.arange(-127, 127) + 0.5) / 8.0
+    for name in ("q", "k"):
+        t = rng.choice(half, size=(256, 128))
+        t[0, 0] = t[64, 0] = t[128, 0] = t[192, 0] = 127.0 / 8.0
+        x[name][0, 0] = wl.f32_to_bf16_bits(t.astype(np.float32))
+    # e4m3: channel max 28 gives the scale 1/16 exactly; midpoints / 16 are exact bf16 values
+    mids = [(1 + (m + 0.5) / 8) * 2.0 ** e for e in range(-6, 9) for m in range(8)]
+    mids = [v for v in mids if v < 448] + [(k + 0.5) * 2.0 ** -9 for k in range(8)]
+    vals = np.array(mids + [-v for v in mids]) / 16.0
+    t = rng.choice(vals, size=(256, 128))
+    t[0, :] = 28.0
+    x["v"][0, 0] = wl.f32_to_bf16_bits(t.astype(np.float32))
+    return w, x
+
+
+def test_codes_on_rounding_boundaries():
+    import parity
+    w, x = _boundary_inputs()
+    g = parity.run_gpu(w, x, backward=False)
+    r = parity.oracle_head(w, x, 0, backward=False)
+    parity.check_quantize_head(w, g, 0, r)
