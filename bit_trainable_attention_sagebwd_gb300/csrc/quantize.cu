@@ -14,6 +14,7 @@
 
 #include "codes.cuh"
 #include "kernels.h"
+#include "ptx.cuh"
 #include "layout.h"
 #include "timer.h"
 
@@ -91,64 +92,106 @@ __device__ __forceinline__ float warp_max(float v) {
 }
 
 // ---------------------------------------------------------------------------
-// kstats: per (head, 128-token block): partial fp64 column sums of k' and the
-// partial channel maxima of |V|.
+// A 128-token block of one head is contiguous in memory ([token][channel] bf16 rows).
+// Each CTA stages its block in shared memory with one bulk copy (issued by thread 0,
+// completion on an mbarrier) and computes from there: no data stays in registers across
+// the block reductions, so several CTAs per SM keep well over 100 KB in flight.
+struct BlockStage {
+  uint64_t bar;
+  int abort;
+};
+
+// Copy `bytes` (a multiple of 16) from src to dst and wait; false for every thread of the
+// CTA when the wait ran out (then the workspace status is set).
+__device__ __forceinline__ bool stage_block(BlockStage& st, void* dst, const void* src, uint32_t bytes,
+                                            int* status) {
+  if (threadIdx.x == 0) {
+    mbar_init(&st.bar, 1);
+    st.abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(&st.bar, bytes);
+    bulk_load(dst, src, bytes, &st.bar);
+  }
+  mbar_wait(&st.bar, 0, &st.abort);
+  __syncthreads();  // every thread sees the same outcome
+  if (st.abort) {
+    if (threadIdx.x == 0) atomicExch(status, kDevTimeout);
+    return false;
+  }
+  return true;
+}
+
+// row `row` (token) of a staged block, channels [8g, 8g+8); zero past the sequence end
+template <int D>
+__device__ __forceinline__ uint4 staged(const uint8_t* buf, int row, int rows, int g) {
+  return row < rows ? reinterpret_cast<const uint4*>(buf + (size_t)row * D * 2)[g] : make_uint4(0, 0, 0, 0);
+}
+
+// ---------------------------------------------------------------------------
+// kstats: per (head, 128-token block): blockIdx.z = 0: partial fp64 column sums of k';
+// blockIdx.z = 1: partial channel maxima of |V|.
 template <int D>
 __global__ void __launch_bounds__(kThreads) kstats_kernel(const __nv_bfloat16* __restrict__ K,
                                                            const __nv_bfloat16* __restrict__ V, int N,
                                                            int qk_norm, double* __restrict__ kpart,
-                                                           float* __restrict__ vpart) {
+                                                           float* __restrict__ vpart, int* __restrict__ status) {
   constexpr int TPR = D / 8, RPP = kThreads / TPR, PASSES = 128 / RPP;
   const int blk = blockIdx.x, bh = blockIdx.y, nb = gridDim.x;
   const int tid = threadIdx.x, g = tid % TPR, ro = tid / TPR;
-  const size_t head = (size_t)bh * N * D;
-  DF cs[8];
-  float vm[8];
+  const int rows = min(128, N - blk * 128);
+  extern __shared__ __align__(128) uint8_t stage_buf[];
+  __shared__ BlockStage st;
+  const __nv_bfloat16* src = (blockIdx.z == 0 ? K : V) + (size_t)bh * N * D + (size_t)blk * 128 * D;
+  if (!stage_block(st, stage_buf, src, (uint32_t)rows * D * 2, status)) return;
+  if (blockIdx.z == 0) {
+    DF cs[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    cs[i] = {0.f, 0.f};
-    vm[i] = 0.f;
-  }
+    for (int i = 0; i < 8; ++i) cs[i] = {0.f, 0.f};
 #pragma unroll
-  for (int p = 0; p < PASSES; ++p) {
-    const int t = blk * 128 + p * RPP + ro;
-    float k[8], v[8];
-    uint4 uk = make_uint4(0, 0, 0, 0), uv = make_uint4(0, 0, 0, 0);
-    if (t < N) {
-      uk = __ldg(reinterpret_cast<const uint4*>(K + head + (size_t)t * D) + g);
-      uv = __ldg(reinterpret_cast<const uint4*>(V + head + (size_t)t * D) + g);
+    for (int p = 0; p < PASSES; ++p) {
+      float k[8];
+      unpack8(staged<D>(stage_buf, p * RPP + ro, rows, g), k);
+      if (qk_norm) {
+        const float r = inv_norm<TPR>(k);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) k[i] = __fmul_rn(k[i], r);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) cs[i] = df_add(cs[i], k[i]);
     }
-    unpack8(uk, k);
-    unpack8(uv, v);
-    if (qk_norm) {
-      const float r = inv_norm<TPR>(k);
+    // combine the RPP row groups per channel in fp64, fixed order
+    __shared__ double s_sum[RPP][D];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) k[i] = __fmul_rn(k[i], r);
+    for (int i = 0; i < 8; ++i) s_sum[ro][g * 8 + i] = (double)cs[i].hi + (double)cs[i].lo;
+    __syncthreads();
+    if (tid < D) {
+      double s = 0.0;
+      for (int r = 0; r < RPP; ++r) s += s_sum[r][tid];
+      kpart[((size_t)bh * nb + blk) * D + tid] = s;
     }
+  } else {
+    float vm[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      cs[i] = df_add(cs[i], k[i]);
-      vm[i] = fmaxf(vm[i], fabsf(v[i]));
-    }
-  }
-  // combine the RPP row groups per channel in fp64, fixed order
-  __shared__ double s_sum[RPP][D];
-  __shared__ float s_max[RPP][D];
+    for (int i = 0; i < 8; ++i) vm[i] = 0.f;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    s_sum[ro][g * 8 + i] = (double)cs[i].hi + (double)cs[i].lo;
-    s_max[ro][g * 8 + i] = vm[i];
-  }
-  __syncthreads();
-  if (tid < D) {
-    double s = 0.0;
-    float m = 0.f;
-    for (int r = 0; r < RPP; ++r) {
-      s += s_sum[r][tid];
-      m = fmaxf(m, s_max[r][tid]);
+    for (int p = 0; p < PASSES; ++p) {
+      float v[8];
+      unpack8(staged<D>(stage_buf, p * RPP + ro, rows, g), v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) vm[i] = fmaxf(vm[i], fabsf(v[i]));
     }
-    kpart[((size_t)bh * nb + blk) * D + tid] = s;
-    vpart[((size_t)bh * nb + blk) * D + tid] = m;
+    __shared__ float s_max[RPP][D];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s_max[ro][g * 8 + i] = vm[i];
+    __syncthreads();
+    if (tid < D) {
+      float m = 0.f;
+      for (int r = 0; r < RPP; ++r) m = fmaxf(m, s_max[r][tid]);
+      vpart[((size_t)bh * nb + blk) * D + tid] = m;
+    }
   }
 }
 
@@ -170,8 +213,6 @@ __global__ void kcombine_kernel(const double* __restrict__ kpart, const float* _
 }
 
 // quantize: per (head, 128-token block, tensor): blockIdx.z = 0 for Q, 1 for K, 2 for V.
-// Each thread issues all of its 128-bit loads before any arithmetic (values stay
-// packed bf16 until used) so that a CTA keeps a whole 32 KB block in flight.
 template <int D>
 __global__ void __launch_bounds__(kThreads) quantize_kernel(
     const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K,
@@ -182,21 +223,17 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(
   constexpr int TPR = D / 8, RPP = kThreads / TPR, PASSES = 128 / RPP;
   const int blk = blockIdx.x, bh = blockIdx.y, which = blockIdx.z, nb = gridDim.x, np = nb * 128;
   const int tid = threadIdx.x, g = tid % TPR, ro = tid / TPR, warp = tid >> 5, lane = tid & 31;
-  const size_t head = (size_t)bh * N * D;
   const size_t phead = (size_t)bh * np * D;
+  const int rows = min(128, N - blk * 128);
+  extern __shared__ __align__(128) uint8_t stage_buf[];
+  __shared__ BlockStage st;
   __shared__ float s_red[2][kThreads / 32];
   // V codes transposed: row d holds the block's 128 tokens; 4-byte groups are
   // permuted by (d / 8) so the byte stores of one warp fall in distinct banks
   __shared__ __align__(16) uint8_t s_v8[D][128];
-  if (blk == 0 && bh == 0 && which == 0 && tid == 0) *status = 0;
 
-  const __nv_bfloat16* src = which == 0 ? Q : (which == 1 ? K : V);
-  uint4 raw[PASSES];
-#pragma unroll
-  for (int p = 0; p < PASSES; ++p) {
-    const int t = blk * 128 + p * RPP + ro;
-    raw[p] = t < N ? __ldg(reinterpret_cast<const uint4*>(src + head + (size_t)t * D) + g) : make_uint4(0, 0, 0, 0);
-  }
+  const __nv_bfloat16* src = (which == 0 ? Q : (which == 1 ? K : V)) + (size_t)bh * N * D + (size_t)blk * 128 * D;
+  if (!stage_block(st, stage_buf, src, (uint32_t)rows * D * 2, status)) return;
 
   if (which == 2) {
     // ---- V: e4m3 codes with channel scales, transposed through shared memory
@@ -210,7 +247,7 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(
     for (int p = 0; p < PASSES; ++p) {
       const int row = p * RPP + ro;
       float v[8];
-      unpack8(raw[p], v);
+      unpack8(staged<D>(stage_buf, row, rows, g), v);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int d = g * 8 + i;
@@ -233,31 +270,43 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(
   }
 
   // ---- Q (which == 0): optional norm, one 128-token block max;
-  //      K (which == 1): optional norm, minus the channel mean, two 64-token block maxima
+  //      K (which == 1): optional norm, minus the channel mean, two 64-token block maxima.
+  // The staged block is read twice: for the maxima, then for the codes.
   const bool isk = which == 1;
   float km[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) km[i] = (isk && k_smooth) ? kmean[(size_t)bh * D + g * 8 + i] : 0.f;
   float* rout = isk ? kr : qr;
-  float x[PASSES][8];
+  float rn[PASSES];
+  // x' = x r - m for keys inside the sequence (x r for queries), 0 past its end
+  auto prep = [&](int p, float (&x)[8]) {
+    const int row = p * RPP + ro;
+    unpack8(staged<D>(stage_buf, row, rows, g), x);
+    if (qk_norm) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[i] = __fmul_rn(x[i], rn[p]);
+    }
+    if (isk) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[i] = (row < rows) ? (k_smooth ? __fsub_rn(x[i], km[i]) : x[i]) : 0.f;
+    }
+  };
   float am[2] = {0.f, 0.f};
 #pragma unroll
   for (int p = 0; p < PASSES; ++p) {
-    const int t = blk * 128 + p * RPP + ro;
-    unpack8(raw[p], x[p]);
-    float r = 1.f;
+    const int row = p * RPP + ro;
+    float x[8];
     if (qk_norm) {
-      r = inv_norm<TPR>(x[p]);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) x[p][i] = __fmul_rn(x[p][i], r);
+      unpack8(staged<D>(stage_buf, row, rows, g), x);
+      rn[p] = inv_norm<TPR>(x);
+    } else {
+      rn[p] = 1.f;
     }
-    if (g == 0) rout[(size_t)bh * np + blk * 128 + p * RPP + ro] = r;
-    const int hsel = isk && (p * RPP + ro) >= 64;
+    if (g == 0) rout[(size_t)bh * np + blk * 128 + row] = rn[p];
+    prep(p, x);
+    const int hsel = isk && row >= 64;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      if (isk) x[p][i] = (t < N) ? (k_smooth ? __fsub_rn(x[p][i], km[i]) : x[p][i]) : 0.f;
-      am[hsel] = fmaxf(am[hsel], fabsf(x[p][i]));
-    }
+    for (int i = 0; i < 8; ++i) am[hsel] = fmaxf(am[hsel], fabsf(x[i]));
   }
   am[0] = warp_max(am[0]);
   am[1] = warp_max(am[1]);
@@ -283,12 +332,13 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(
   __nv_bfloat16* dst = isk ? kc : qc;
 #pragma unroll
   for (int p = 0; p < PASSES; ++p) {
-    const int hs = isk && (p * RPP + ro) >= 64;
-    const float s = sc[hs], si = inv[hs];
-    float c[8];
+    const int row = p * RPP + ro;
+    const int hs = isk && row >= 64;
+    float x[8], c[8];
+    prep(p, x);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) c[i] = int_code(x[p][i], s, si);
-    reinterpret_cast<uint4*>(dst + phead + (size_t)(blk * 128 + p * RPP + ro) * D)[g] = pack8_bf16(c);
+    for (int i = 0; i < 8; ++i) c[i] = int_code(x[i], sc[hs], inv[hs]);
+    reinterpret_cast<uint4*>(dst + phead + (size_t)(blk * 128 + row) * D)[g] = pack8_bf16(c);
   }
 }
 
@@ -299,7 +349,6 @@ int launch_quantize(const void* Q, const void* K, const void* V, int B, int H, i
   const QuantWs L = quant_ws_layout(B, H, N, D);
   uint8_t* w = static_cast<uint8_t*>(ws);
   const int nb = L.np / 128;
-  const dim3 grid(nb, B * H);
   const dim3 qgrid(nb, B * H, 3);
   auto* q = static_cast<const __nv_bfloat16*>(Q);
   auto* k = static_cast<const __nv_bfloat16*>(K);
@@ -308,24 +357,23 @@ int launch_quantize(const void* Q, const void* K, const void* V, int B, int H, i
   float* vpart = reinterpret_cast<float*>(w + L.vpart);
   float* kmean = reinterpret_cast<float*>(w + L.kmean);
   float* sv = reinterpret_cast<float*>(w + L.sv);
+  int* status = reinterpret_cast<int*>(w + L.status);
+  const size_t stage = (size_t)128 * D * 2;  // one staged token block
   ScopedTimer timer("quantize", st);
-  if (D == 128)
-    kstats_kernel<128><<<grid, kThreads, 0, st>>>(k, v, N, qk_norm, kpart, vpart);
-  else
-    kstats_kernel<64><<<grid, kThreads, 0, st>>>(k, v, N, qk_norm, kpart, vpart);
+  // the status word is cleared before the kernels that may set it
+  if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return 3;
+  auto stats = D == 128 ? kstats_kernel<128> : kstats_kernel<64>;
+  auto quant = D == 128 ? quantize_kernel<128> : quantize_kernel<64>;
+  if (cudaFuncSetAttribute(stats, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)stage) != cudaSuccess ||
+      cudaFuncSetAttribute(quant, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)stage) != cudaSuccess)
+    return 3;
+  stats<<<dim3(nb, B * H, 2), kThreads, stage, st>>>(k, v, N, qk_norm, kpart, vpart, status);
   kcombine_kernel<<<B * H, 128, 0, st>>>(kpart, vpart, N, D, nb, k_smooth, kmean, sv);
-  auto args = [&](auto kern) {
-    kern<<<qgrid, kThreads, 0, st>>>(q, k, v, N, qk_norm, k_smooth, kmean, sv,
-                                    reinterpret_cast<__nv_bfloat16*>(w + L.qc),
-                                    reinterpret_cast<__nv_bfloat16*>(w + L.kc), w + L.v8t,
-                                    reinterpret_cast<float*>(w + L.sq), reinterpret_cast<float*>(w + L.sk),
-                                    reinterpret_cast<float*>(w + L.qr), reinterpret_cast<float*>(w + L.kr),
-                                    reinterpret_cast<int*>(w + L.status));
-  };
-  if (D == 128)
-    args(quantize_kernel<128>);
-  else
-    args(quantize_kernel<64>);
+  quant<<<qgrid, kThreads, stage, st>>>(q, k, v, N, qk_norm, k_smooth, kmean, sv,
+                                        reinterpret_cast<__nv_bfloat16*>(w + L.qc),
+                                        reinterpret_cast<__nv_bfloat16*>(w + L.kc), w + L.v8t,
+                                        reinterpret_cast<float*>(w + L.sq), reinterpret_cast<float*>(w + L.sk),
+                                        reinterpret_cast<float*>(w + L.qr), reinterpret_cast<float*>(w + L.kr), status);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 
