@@ -5,7 +5,7 @@
 // q = RN(x * inv) is within 2 ulps of x / s, and so within 2.5 ulps of RN(x / s).  Both
 // round to the same code unless a rounding boundary (a half-integer, or an e4m3 midpoint)
 // lies within that distance of q; such elements (a few in a million) are recomputed with
-// the IEEE division, out of line.
+// the IEEE division.
 #pragma once
 
 #include <cuda_fp8.h>
@@ -13,21 +13,6 @@
 
 namespace sage {
 namespace {  // internal linkage: each translation unit keeps its own copy
-
-__device__ __noinline__ float int_code_exact(float x, float s) {
-  const float c = rintf(__fdiv_rn(x, s));
-  return fminf(fmaxf(c, -127.f), 127.f);
-}
-
-// rint(RN(x / s)) clamped to [-127, 127]; inv = RN(1 / s), or 0 when s == 0 (then x == 0)
-__device__ __forceinline__ float int_code(float x, float s, float inv) {
-  const float q = __fmul_rn(x, inv);
-  const float r = rintf(q);
-  // |q| <= 128 has ulp <= 2^-16, so 4 ulps < 2^-14: only q within 2^-14 of a half-integer is
-  // in doubt (q - r is exact)
-  if (fabsf(__fsub_rn(q, r)) > 0.49993896484375f) return int_code_exact(x, s);
-  return fminf(fmaxf(r, -127.f), 127.f);
-}
 
 __device__ __noinline__ uint32_t e4m3_code_exact(float x, float s) {
   return (uint32_t)__nv_cvt_float_to_fp8(__fdiv_rn(x, s), __NV_SATFINITE, __NV_E4M3);
@@ -44,6 +29,42 @@ __device__ __forceinline__ uint32_t e4m3_code(float x, float s, float inv) {
   const float aq = fabsf(q);
   if (key <= (16u << 12) || (aq < 0.015625f && aq != 0.f)) return e4m3_code_exact(x, s);
   return (uint32_t)__nv_cvt_float_to_fp8(q, __NV_SATFINITE, __NV_E4M3);
+}
+
+// Eight INT8 codes with one scale: the doubt test costs no branch per element; when any of
+// the eight is in doubt all eight take the (inlined) division, which is rare.
+__device__ __forceinline__ void int_codes8(const float (&x)[8], float s, float inv, float (&c)[8]) {
+  bool doubt = false;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float q = __fmul_rn(x[i], inv);
+    const float r = rintf(q);
+    doubt |= fabsf(__fsub_rn(q, r)) > 0.49993896484375f;
+    c[i] = fminf(fmaxf(r, -127.f), 127.f);
+  }
+  if (doubt) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) c[i] = fminf(fmaxf(rintf(__fdiv_rn(x[i], s)), -127.f), 127.f);
+  }
+}
+
+// Eight e4m3 codes with per-element scales, same scheme as e4m3_code.
+__device__ __forceinline__ void e4m3_codes8(const float (&x)[8], const float (&s)[8], const float (&inv)[8],
+                                            uint32_t (&c)[8]) {
+  bool doubt = false;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float q = __fmul_rn(x[i], inv[i]);
+    const uint32_t key = __float_as_uint(q) * 4096u + ((8u - 0x80000u) << 12);
+    const float aq = fabsf(q);
+    doubt |= (key <= (16u << 12)) | ((aq < 0.015625f) & (aq != 0.f));
+    c[i] = (uint32_t)__nv_cvt_float_to_fp8(q, __NV_SATFINITE, __NV_E4M3);
+  }
+  if (doubt) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      c[i] = (uint32_t)__nv_cvt_float_to_fp8(__fdiv_rn(x[i], s[i]), __NV_SATFINITE, __NV_E4M3);
+  }
 }
 
 }  // namespace

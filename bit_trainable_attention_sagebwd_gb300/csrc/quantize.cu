@@ -202,11 +202,28 @@ __global__ void kcombine_kernel(const double* __restrict__ kpart, const float* _
                                 float* __restrict__ sv) {
   const int bh = blockIdx.x, d = threadIdx.x;
   if (d >= D) return;
+  // partials summed in block order; their loads are issued 8 at a time
   double s = 0.0;
   float m = 0.f;
-  for (int b = 0; b < nb; ++b) {
-    s += kpart[((size_t)bh * nb + b) * D + d];
-    m = fmaxf(m, vpart[((size_t)bh * nb + b) * D + d]);
+  const size_t base = (size_t)bh * nb * D + d;
+  int b = 0;
+  for (; b + 8 <= nb; b += 8) {
+    double ks[8];
+    float vs[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      ks[i] = kpart[base + (size_t)(b + i) * D];
+      vs[i] = vpart[base + (size_t)(b + i) * D];
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      s += ks[i];
+      m = fmaxf(m, vs[i]);
+    }
+  }
+  for (; b < nb; ++b) {
+    s += kpart[base + (size_t)b * D];
+    m = fmaxf(m, vpart[base + (size_t)b * D]);
   }
   kmean[(size_t)bh * D + d] = k_smooth ? (float)(s / (double)N) : 0.f;
   sv[(size_t)bh * D + d] = m > 0.f ? __fdiv_rn(m, 448.0f) : 0.f;
@@ -247,12 +264,14 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(
     for (int p = 0; p < PASSES; ++p) {
       const int row = p * RPP + ro;
       float v[8];
+      uint32_t c8[8];
       unpack8(staged<D>(stage_buf, row, rows, g), v);
+      // e4m3(RN(v / s_v)): round to nearest even, saturating to +-448
+      e4m3_codes8(v, svv, inv, c8);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int d = g * 8 + i;
-        // e4m3(RN(v / s_v)): round to nearest even, saturating to +-448
-        s_v8[d][row ^ (((d >> 3) & 15) << 2)] = (uint8_t)e4m3_code(v[i], svv[i], inv[i]);
+        s_v8[d][row ^ (((d >> 3) & 15) << 2)] = (uint8_t)c8[i];
       }
     }
     __syncthreads();
@@ -336,8 +355,7 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(
     const int hs = isk && row >= 64;
     float x[8], c[8];
     prep(p, x);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) c[i] = int_code(x[i], sc[hs], inv[hs]);
+    int_codes8(x, sc[hs], inv[hs], c);
     reinterpret_cast<uint4*>(dst + phead + (size_t)(blk * 128 + row) * D)[g] = pack8_bf16(c);
   }
 }
