@@ -146,6 +146,21 @@ __device__ __forceinline__ uint32_t pick32(const uint32_t (&a)[32], int e) {
   return (e & 1) ? f[1] : f[0];
 }
 
+// Masked keys of a tile (padding, or after the query on the causal diagonal): their S values
+// become -inf right after the TMEM load, so the max and exp passes need no per-element test
+// (2^-inf = 0).  Columns [0, valid) of the 64 held in s stay.
+__device__ __forceinline__ void mask_half(uint32_t (&s)[2][32], int valid) {
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+      if (q * 32 + e >= valid) s[q][e] = 0xff800000u;
+}
+
+// A zero logit scale (an all-zero Q or K block, so every unmasked S there is 0) becomes the
+// smallest subnormal: -inf * scale stays -inf, and 0 * scale - m is still exactly -m.
+__device__ __forceinline__ float logit_scale(float c) { return c > 0.f ? c : __uint_as_float(1u); }
+
 __device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float d) {
   const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
   const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
@@ -179,8 +194,8 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
       break;
     }
     tc_fence_after();
-    const float c0 = __fmul_rn(__fmul_rn(s_q, skj.x), prm.alpha);
-    const float c1 = __fmul_rn(__fmul_rn(s_q, skj.y), prm.alpha);
+    const float c0 = logit_scale(__fmul_rn(__fmul_rn(s_q, skj.x), prm.alpha));
+    const float c1 = logit_scale(__fmul_rn(__fmul_rn(s_q, skj.y), prm.alpha));
     const int kbase = j * 128;
     const bool masked_tile = (kbase + 128 > prm.N) || (CAUSAL && j == qb);
     int lim = prm.N - kbase;  // keys [0, lim) of the tile are valid
@@ -196,19 +211,12 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
       tmem_ld_wait();
       reg_fence32(sh[0]);
       reg_fence32(sh[1]);
+      if (masked_tile) mask_half(sh, lim - h * 64);
       float a = -INFINITY;
-      const int hl = lim - h * 64;  // valid keys of this half (masked tiles)
 #pragma unroll
       for (int q = 0; q < 2; ++q)
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float v0 = __uint_as_float(sh[q][e]), v1 = __uint_as_float(sh[q][e + 1]);
-          if (masked_tile) {
-            v0 = (q * 32 + e < hl) ? v0 : -INFINITY;
-            v1 = (q * 32 + e + 1 < hl) ? v1 : -INFINITY;
-          }
-          a = max3(a, v0, v1);
-        }
+        for (int e = 0; e < 32; e += 2) a = max3(a, __uint_as_float(sh[q][e]), __uint_as_float(sh[q][e + 1]));
       mxh[h] = a;
     }
     // the log2-domain logit is acc * c with c >= 0, so its maximum is max(acc) * c
@@ -236,10 +244,10 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
         tmem_ld_wait();
         reg_fence32(sh[0]);
         reg_fence32(sh[1]);
+        if (masked_tile) mask_half(sh, lim);
       }
       const float cc = h == 0 ? c0 : c1;
       const uint64_t cc2 = f2(cc, cc);
-      const int hl = lim - h * 64;
       uint32_t band = ~0u;  // smallest band key of the 64 codes of this half
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
@@ -253,10 +261,6 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
             f2split(ffma2(f2(__uint_as_float(sh[q][e + u]), __uint_as_float(sh[q][e + u + 1])), cc2, neg_m2), t0,
                     t1);
             f2split(fmul2(f2(ex2(t0), ex2(t1)), k448), x[u], x[u + 1]);
-            if (masked_tile) {
-              x[u] = (q * 32 + e + u < hl) ? x[u] : 0.f;
-              x[u + 1] = (q * 32 + e + u + 1 < hl) ? x[u + 1] : 0.f;
-            }
             lsum = fadd2(lsum, f2(x[u], x[u + 1]));
             band = min(band, min(band_key(x[u]), band_key(x[u + 1])));
           }
@@ -278,8 +282,8 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
                         neg_m2),
                   t0, t1);
           f2split(fmul2(f2(ex2(t0), ex2(t1)), k448), x0, x1);
-          if (band_key(x0) <= kBandMax && (!masked_tile || e < hl)) flags |= 1ull << e;
-          if (band_key(x1) <= kBandMax && (!masked_tile || e + 1 < hl)) flags |= 1ull << (e + 1);
+          if (band_key(x0) <= kBandMax) flags |= 1ull << e;
+          if (band_key(x1) <= kBandMax) flags |= 1ull << (e + 1);
         }
         while (flags) {
           const int e = __ffsll((long long)flags) - 1;
