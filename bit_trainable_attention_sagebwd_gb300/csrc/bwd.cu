@@ -423,7 +423,10 @@ __global__ void __launch_bounds__(384, 1)
       // this query row's scalars: P = 2^(S2 - LSE2) is formed as 2^(S2 + bias) / 448
       const float bias_t = sm.bias[qs][t];
       const float dvec_t = sm.dvec[qs][t];
-      const float cs = __fmul_rn(__fmul_rn(sqI, sk_mine), prm.alpha);
+      // a zero logit scale (all-zero Q or K block: every unmasked S there is 0) becomes the
+      // smallest subnormal, so that a masked -inf times it stays -inf
+      const float cs_raw = __fmul_rn(__fmul_rn(sqI, sk_mine), prm.alpha);
+      const float cs = cs_raw > 0.f ? cs_raw : __uint_as_float(1u);
       // masked key columns kc >= klim: padding, and keys after this query on the diagonal block
       const int klim = (prm.causal && I == kb) ? min(klim_pad, t + 1) : klim_pad;
       const bool any_mask = __any_sync(0xffffffffu, klim < (int)kcol + 64);
@@ -438,6 +441,14 @@ __global__ void __launch_bounds__(384, 1)
       tmem_ld_wait();
 #pragma unroll
       for (int c = 0; c < 2; ++c) reg_fence32(buf[c]);
+      if (any_mask) {
+        // masked keys: S = -inf, so 2^(S2 + bias) = 0 without a test per element below
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if ((int)kcol + 32 * c + e >= klim) buf[c][e] = 0xff800000u;
+      }
       {
         const uint64_t cs2 = f2(cs, cs), b2 = f2(bias_t, bias_t);
 #pragma unroll
@@ -449,11 +460,6 @@ __global__ void __launch_bounds__(384, 1)
             f2split(ffma2(f2(__uint_as_float(buf[c][e + 2]), __uint_as_float(buf[c][e + 3])), cs2, b2), p[2], p[3]);
 #pragma unroll
             for (int u = 0; u < 4; ++u) p[u] = ex2(p[u]);
-            if (any_mask) {
-#pragma unroll
-              for (int u = 0; u < 4; ++u)
-                if ((int)kcol + 32 * c + e + u >= klim) p[u] = 0.f;
-            }
             const __nv_fp8x2_storage_t lo =
                 __nv_cvt_float2_to_fp8x2(make_float2(p[0], p[1]), __NV_SATFINITE, __NV_E4M3);
             const __nv_fp8x2_storage_t hi =
