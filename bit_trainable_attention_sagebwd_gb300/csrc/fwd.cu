@@ -47,6 +47,9 @@ struct FwdSmem {
 struct FwdParams {
   int N, np, nqb, npairs;
   float alpha;  // RN(sm_scale * log2 e)
+  // 4096, passed at run time so that the band key stays one integer multiply-add (FMA pipe)
+  // instead of a shift and an add on the busier ALU pipe
+  uint32_t band_mult;
   const float* sq;
   const float* sk;
   const float* sv;
@@ -71,7 +74,9 @@ __device__ __forceinline__ float ex2(float x) {
 constexpr uint32_t kBandUlps = 4;
 constexpr uint32_t kBandC = (kBandUlps - 0x80000u) << 12;
 constexpr uint32_t kBandMax = (2u * kBandUlps) << 12;
-__device__ __forceinline__ uint32_t band_key(float x) { return __float_as_uint(x) * 4096u + kBandC; }
+__device__ __forceinline__ uint32_t band_key(float x, uint32_t mult4096) {
+  return __float_as_uint(x) * mult4096 + kBandC;
+}
 
 // Pairs of fp32 (hi + lo) as extended precision: error-free transformations of
 // Knuth (two-sum) and Dekker (fast two-sum, two-product via FMA).
@@ -212,12 +217,13 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
       reg_fence32(sh[0]);
       reg_fence32(sh[1]);
       if (masked_tile) mask_half(sh, lim - h * 64);
-      float a = -INFINITY;
+      // one running maximum per 32-column load: two independent chains
+      float a[2] = {-INFINITY, -INFINITY};
 #pragma unroll
       for (int q = 0; q < 2; ++q)
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) a = max3(a, __uint_as_float(sh[q][e]), __uint_as_float(sh[q][e + 1]));
-      mxh[h] = a;
+        for (int e = 0; e < 32; e += 2) a[q] = max3(a[q], __uint_as_float(sh[q][e]), __uint_as_float(sh[q][e + 1]));
+      mxh[h] = fmaxf(a[0], a[1]);
     }
     // the log2-domain logit is acc * c with c >= 0, so its maximum is max(acc) * c
     const float mt0 = mxh[0] == -INFINITY ? -INFINITY : __fmul_rn(mxh[0], c0);
@@ -235,7 +241,8 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
     // ---- t = RN(acc*c - m_new) (one FMA), x = 448 * 2^t, e4m3 codes -> shared memory
     const uint64_t neg_m2 = f2(-m_new, -m_new);
     const uint64_t k448 = f2(448.f, 448.f);
-    uint64_t lsum = f2(0.f, 0.f);
+    uint64_t lsum[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};  // two independent chains
+    const uint32_t bm = prm.band_mult;
 #pragma unroll 1
     for (int h = 1; h >= 0; --h) {
       if (h == 0) {
@@ -248,7 +255,7 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
       }
       const float cc = h == 0 ? c0 : c1;
       const uint64_t cc2 = f2(cc, cc);
-      uint32_t band = ~0u;  // smallest band key of the 64 codes of this half
+      uint32_t band[2] = {~0u, ~0u};  // smallest band keys of the 64 codes of this half
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         uint32_t w[8];
@@ -261,8 +268,8 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
             f2split(ffma2(f2(__uint_as_float(sh[q][e + u]), __uint_as_float(sh[q][e + u + 1])), cc2, neg_m2), t0,
                     t1);
             f2split(fmul2(f2(ex2(t0), ex2(t1)), k448), x[u], x[u + 1]);
-            lsum = fadd2(lsum, f2(x[u], x[u + 1]));
-            band = min(band, min(band_key(x[u]), band_key(x[u + 1])));
+            lsum[u >> 1] = fadd2(lsum[u >> 1], f2(x[u], x[u + 1]));
+            band[u >> 1] = min(band[u >> 1], min(band_key(x[u], bm), band_key(x[u + 1], bm)));
           }
           w[e >> 2] = pack4_e4m3(x[0], x[1], x[2], x[3]);
         }
@@ -272,7 +279,7 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
       }
       // rare: codes whose fast value is near an e4m3 midpoint are redone exactly and
       // patched in shared memory (one site for the half's 64 codes)
-      if (band <= kBandMax) {
+      if (min(band[0], band[1]) <= kBandMax) {
         uint64_t flags = 0;
         // the fast values are recomputed with the very instruction sequence of the loop above
 #pragma unroll
@@ -282,8 +289,8 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
                         neg_m2),
                   t0, t1);
           f2split(fmul2(f2(ex2(t0), ex2(t1)), k448), x0, x1);
-          if (band_key(x0) <= kBandMax) flags |= 1ull << e;
-          if (band_key(x1) <= kBandMax) flags |= 1ull << (e + 1);
+          if (band_key(x0, bm) <= kBandMax) flags |= 1ull << e;
+          if (band_key(x1, bm) <= kBandMax) flags |= 1ull << (e + 1);
         }
         while (flags) {
           const int e = __ffsll((long long)flags) - 1;
@@ -302,13 +309,15 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
         tmem_ld32(o_col + c, o);
         tmem_wait32(o);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+        for (int i = 0; i < 32; i += 2)
+          f2split(fmul2(f2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), f2(corr, corr)),
+                  *reinterpret_cast<float*>(&o[i]), *reinterpret_cast<float*>(&o[i + 1]));
         tmem_st32(o_col + c, o);
       }
       tmem_st_wait();
     }
     float la, lb;
-    f2split(lsum, la, lb);
+    f2split(fadd2(lsum[0], lsum[1]), la, lb);
     l = fmaf(l, corr, la + lb);
     m = m_new;
     fence_proxy_async_smem();
@@ -514,6 +523,7 @@ int launch_fwd(const void* ws, void* O, float* LSE, float* O32, int B, int H, in
   p.nqb = np / 128;
   p.npairs = (p.nqb + 1) / 2;
   p.alpha = (float)((double)sm_scale * 1.4426950408889634074);
+  p.band_mult = 4096u;
   p.sq = reinterpret_cast<const float*>(w + L.sq);
   p.sk = reinterpret_cast<const float*>(w + L.sk);
   p.sv = reinterpret_cast<const float*>(w + L.sv);
