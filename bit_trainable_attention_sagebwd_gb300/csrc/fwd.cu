@@ -4,15 +4,16 @@
 // QK^T and PV run quantized.  "ThriftAttention" (gist.science summary),
 // Methodology step 2: FlashAttention-2 online softmax over key tiles.
 //
-// One CTA per (head, 128-query block); keys in 128-token tiles.
-//   warp 0 lane 0 : TMA producer for Q and the K tiles (bf16 containers of INT8 codes)
-//   warp 2 lane 0 : TMA producer for the V tiles (e4m3, channel-major)
-//   warp 1        : TMEM allocator; lane 0 issues the UMMAs
+// One CTA per (head, pair of 128-query tiles A and B); keys in 128-token tiles.
+//   warps 0..15   : softmax, four warpgroups.  Warpgroup 2X + hh serves query tile X and the
+//                   64-key half hh of every key tile; thread t owns query row t (TMEM lane t).
+//   warp 16 lane 0: TMA producer for Q, the K tiles (bf16 containers of INT8 codes) and the
+//                   V tiles (e4m3, channel-major)
+//   warp 17       : TMEM allocator; lane 0 issues the UMMAs
 //       S_j = Q8 K8_j^T   kind::f16 on bf16-held integers -> exact int sums in fp32
 //       O  += P8_j V8_j   kind::f8f6f4 e4m3 x e4m3 -> fp32
-//   warps 4..7    : softmax, thread t owns query row t (TMEM lane t)
-// TMEM: S double buffer (2 x 128 columns) + O (D columns).  S_{j+1} is computed
-// while the softmax warps work on S_j.
+// TMEM: S_A, S_B (128 columns each) + O_A, O_B (D columns each).  The tensor core works on one
+// tile while the softmax of the other runs.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -36,6 +37,8 @@ struct FwdSmem {
   uint8_t k[kKStages][128 * D * 2];  // key tiles
   uint8_t v[kVStages][D * 128];      // value tiles (e4m3, channel-major)
   uint8_t p[2][128 * 128];           // P of tiles A and B (e4m3, 128B-swizzled K-major)
+  float xmax[2][2][128];             // per tile and key half: row maxima of the current key tile
+  float xsum[2][2][128];             // per tile and key half: row sums, exchanged at the end
   uint64_t bar_q;
   uint64_t bar_k_full[kKStages], bar_k_empty[kKStages];
   uint64_t bar_v_full[kVStages], bar_v_empty[kVStages];
@@ -162,9 +165,19 @@ __device__ __forceinline__ void mask_half(uint32_t (&s)[2][32], int valid) {
       if (q * 32 + e >= valid) s[q][e] = 0xff800000u;
 }
 
+// the same for one 32-column chunk: columns [0, valid) stay
+__device__ __forceinline__ void mask_chunk(uint32_t (&s)[32], int valid) {
+#pragma unroll
+  for (int e = 0; e < 32; ++e)
+    if (e >= valid) s[e] = 0xff800000u;
+}
+
 // A zero logit scale (an all-zero Q or K block, so every unmasked S there is 0) becomes the
 // smallest subnormal: -inf * scale stays -inf, and 0 * scale - m is still exactly -m.
 __device__ __forceinline__ float logit_scale(float c) { return c > 0.f ? c : __uint_as_float(1u); }
+
+// named barrier 1 + X over the two warpgroups of tile X
+__device__ __forceinline__ void named_bar_tile(int X) { asm volatile("bar.sync %0, 256;" ::"r"(1 + X) : "memory"); }
 
 __device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float d) {
   const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
@@ -172,92 +185,83 @@ __device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float 
   return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
-// Softmax of one 128-query tile (tile X of the CTA), run by one warpgroup.
-// Thread t owns query row t (TMEM lane t).
+// Softmax of one 128-query tile (tile X of the CTA) by two warpgroups: thread t of half hh
+// owns query row t (TMEM lane t) and the 64 keys [64 hh, 64 hh + 64) of every key tile, which
+// is exactly one K scale block.  The two halves exchange their row maxima once per tile and
+// their row sums at the end; each rescales and writes half of the O columns.
 template <int D, bool CAUSAL>
-__device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParams& prm, int X, int qb, int bh,
-                                                  uint32_t tmem, volatile int* abort) {
-  const int t = threadIdx.x - 128 * X;
+__device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParams& prm, int X, int hh, int qb,
+                                                  int bh, uint32_t tmem, volatile int* abort) {
+  constexpr int DH = D / 2;  // O columns of this half
+  const int t = threadIdx.x & 127;
   const int warp_in_wg = t >> 5;
   const int row = qb * 128 + t;
   const uint32_t lane_base = (uint32_t)(warp_in_wg * 32) << 16;
-  const uint32_t s_col = tmem + lane_base + (uint32_t)(X * 128);
-  const uint32_t o_col = tmem + lane_base + 256u + (uint32_t)(X * D);
+  const uint32_t s_col = tmem + lane_base + (uint32_t)(X * 128 + hh * 64);
+  const uint32_t o_col = tmem + lane_base + 256u + (uint32_t)(X * D + hh * DH);
   const int n_tiles = CAUSAL ? qb + 1 : prm.nqb;
   const float s_q = prm.sq[(size_t)bh * prm.nqb + qb];
-  const float* skh = prm.sk + (size_t)bh * prm.nqb * 2;
+  const float* skh = prm.sk + (size_t)bh * prm.nqb * 2 + hh;  // this half's K block scale
   uint8_t* prow = sm.p[X] + (t >> 3) * 1024 + (t & 7) * 128;
-  float m = -INFINITY, l = 0.f;
+  float m = -INFINITY, l = 0.f;  // l: this half's share of the row sum
+  // a wait that runs out raises the abort flag; from then on this thread skips its waits but
+  // still runs every tile, so neither half is left behind at a named barrier
   bool ok = true;
-  // the K-block scales of a tile are fetched one tile early (global latency off the path)
-  float2 sk_next = *reinterpret_cast<const float2*>(skh);
+  // the K-block scale of a tile is fetched one tile early (global latency off the path)
+  float sk_next = skh[0];
   for (int j = 0; j < n_tiles; ++j) {
-    const float2 skj = sk_next;
-    if (j + 1 < n_tiles) sk_next = *reinterpret_cast<const float2*>(skh + 2 * (j + 1));
-    if (!mbar_wait(&sm.bar_s_full[X], j & 1, abort)) {
-      ok = false;
-      break;
-    }
+    const float skj = sk_next;
+    if (j + 1 < n_tiles) sk_next = skh[2 * (j + 1)];
+    ok = ok && mbar_wait(&sm.bar_s_full[X], j & 1, abort);
     tc_fence_after();
-    const float c0 = logit_scale(__fmul_rn(__fmul_rn(s_q, skj.x), prm.alpha));
-    const float c1 = logit_scale(__fmul_rn(__fmul_rn(s_q, skj.y), prm.alpha));
+    const float cc = logit_scale(__fmul_rn(__fmul_rn(s_q, skj), prm.alpha));
     const int kbase = j * 128;
     const bool masked_tile = (kbase + 128 > prm.N) || (CAUSAL && j == qb);
     int lim = prm.N - kbase;  // keys [0, lim) of the tile are valid
     if (CAUSAL && j == qb) lim = min(lim, t + 1);
-    // ---- S row in two 64-key halves (sh = two 32-column loads): the max pass ends
-    // with half 1 in registers; the exp pass uses it, then reloads half 0
-    uint32_t sh[2][32];
-    float mxh[2];
-#pragma unroll 1
-    for (int h = 0; h < 2; ++h) {
-      tmem_ld32(s_col + h * 64, sh[0]);
-      tmem_ld32(s_col + h * 64 + 32, sh[1]);
+    // ---- max pass over this half's 64 S values (two 32-column loads)
+    float mx;
+    {
+      uint32_t sh[2][32];
+      tmem_ld32(s_col, sh[0]);
+      tmem_ld32(s_col + 32, sh[1]);
       tmem_ld_wait();
       reg_fence32(sh[0]);
       reg_fence32(sh[1]);
-      if (masked_tile) mask_half(sh, lim - h * 64);
-      // one running maximum per 32-column load: two independent chains
-      float a[2] = {-INFINITY, -INFINITY};
+      if (masked_tile) mask_half(sh, lim - hh * 64);
+      float a[2] = {-INFINITY, -INFINITY};  // one running maximum per load: two chains
 #pragma unroll
       for (int q = 0; q < 2; ++q)
 #pragma unroll
         for (int e = 0; e < 32; e += 2) a[q] = max3(a[q], __uint_as_float(sh[q][e]), __uint_as_float(sh[q][e + 1]));
-      mxh[h] = fmaxf(a[0], a[1]);
+      mx = fmaxf(a[0], a[1]);
     }
-    // the log2-domain logit is acc * c with c >= 0, so its maximum is max(acc) * c
-    const float mt0 = mxh[0] == -INFINITY ? -INFINITY : __fmul_rn(mxh[0], c0);
-    const float mt1 = mxh[1] == -INFINITY ? -INFINITY : __fmul_rn(mxh[1], c1);
-    const float m_new = max3(m, mt0, mt1);
+    // the log2-domain logit is acc * c with c > 0, so its maximum is max(acc) * c
+    const float mt = mx == -INFINITY ? -INFINITY : __fmul_rn(mx, cc);
+    sm.xmax[X][hh][t] = mt;
+    named_bar_tile(X);
+    const float m_new = max3(m, sm.xmax[X][0][t], sm.xmax[X][1][t]);
     const float corr = (m == -INFINITY) ? 0.f : ex2(m - m_new);
     // ---- PV of the previous tile must be complete before P is overwritten and O rescaled
     if (j > 0) {
-      if (!mbar_wait(&sm.bar_o_done[X], (j - 1) & 1, abort)) {
-        ok = false;
-        break;
-      }
+      ok = ok && mbar_wait(&sm.bar_o_done[X], (j - 1) & 1, abort);
       tc_fence_after();
     }
-    // ---- t = RN(acc*c - m_new) (one FMA), x = 448 * 2^t, e4m3 codes -> shared memory
-    const uint64_t neg_m2 = f2(-m_new, -m_new);
-    const uint64_t k448 = f2(448.f, 448.f);
-    uint64_t lsum[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};  // two independent chains
-    const uint32_t bm = prm.band_mult;
-#pragma unroll 1
-    for (int h = 1; h >= 0; --h) {
-      if (h == 0) {
-        tmem_ld32(s_col, sh[0]);
-        tmem_ld32(s_col + 32, sh[1]);
-        tmem_ld_wait();
-        reg_fence32(sh[0]);
-        reg_fence32(sh[1]);
-        if (masked_tile) mask_half(sh, lim);
-      }
-      const float cc = h == 0 ? c0 : c1;
+    // ---- t = RN(acc*c - m_new) (one FMA), x = 448 * 2^t, e4m3 codes -> shared memory; one
+    // 32-column chunk at a time (reloaded from TMEM), so few registers stay live
+    {
+      const uint64_t neg_m2 = f2(-m_new, -m_new);
+      const uint64_t k448 = f2(448.f, 448.f);
       const uint64_t cc2 = f2(cc, cc);
-      uint32_t band[2] = {~0u, ~0u};  // smallest band keys of the 64 codes of this half
-#pragma unroll
+      const uint32_t bm = prm.band_mult;
+      uint64_t lsum[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};  // two independent chains
+#pragma unroll 1
       for (int q = 0; q < 2; ++q) {
+        uint32_t sv[32];
+        tmem_ld32(s_col + 32 * q, sv);
+        tmem_wait32(sv);
+        if (masked_tile) mask_chunk(sv, lim - hh * 64 - 32 * q);
+        uint32_t band[2] = {~0u, ~0u};  // smallest band keys of the chunk's codes
         uint32_t w[8];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
@@ -265,46 +269,46 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
 #pragma unroll
           for (int u = 0; u < 4; u += 2) {
             float t0, t1;
-            f2split(ffma2(f2(__uint_as_float(sh[q][e + u]), __uint_as_float(sh[q][e + u + 1])), cc2, neg_m2), t0,
-                    t1);
+            f2split(ffma2(f2(__uint_as_float(sv[e + u]), __uint_as_float(sv[e + u + 1])), cc2, neg_m2), t0, t1);
             f2split(fmul2(f2(ex2(t0), ex2(t1)), k448), x[u], x[u + 1]);
             lsum[u >> 1] = fadd2(lsum[u >> 1], f2(x[u], x[u + 1]));
             band[u >> 1] = min(band[u >> 1], min(band_key(x[u], bm), band_key(x[u + 1], bm)));
           }
           w[e >> 2] = pack4_e4m3(x[0], x[1], x[2], x[3]);
         }
-        const int c = 2 * h + q;  // 32-key chunk of the row: 16-byte units 2c, 2c+1
+        const int c = 2 * hh + q;  // 32-key chunk of the row: 16-byte units 2c, 2c+1
         *reinterpret_cast<uint4*>(prow + (((2 * c) ^ (t & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         *reinterpret_cast<uint4*>(prow + (((2 * c + 1) ^ (t & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
-      }
-      // rare: codes whose fast value is near an e4m3 midpoint are redone exactly and
-      // patched in shared memory (one site for the half's 64 codes)
-      if (min(band[0], band[1]) <= kBandMax) {
-        uint64_t flags = 0;
-        // the fast values are recomputed with the very instruction sequence of the loop above
+        // rare: codes whose fast value is near an e4m3 midpoint are redone exactly and
+        // patched in shared memory
+        if (min(band[0], band[1]) <= kBandMax) {
+          uint32_t flags = 0;
+          // the fast values are recomputed with the very instruction sequence of the loop above
 #pragma unroll
-        for (int e = 0; e < 64; e += 2) {
-          float t0, t1, x0, x1;
-          f2split(ffma2(f2(__uint_as_float(sh[e >> 5][e & 31]), __uint_as_float(sh[e >> 5][(e & 31) + 1])), cc2,
-                        neg_m2),
-                  t0, t1);
-          f2split(fmul2(f2(ex2(t0), ex2(t1)), k448), x0, x1);
-          if (band_key(x0, bm) <= kBandMax) flags |= 1ull << e;
-          if (band_key(x1, bm) <= kBandMax) flags |= 1ull << (e + 1);
-        }
-        while (flags) {
-          const int e = __ffsll((long long)flags) - 1;
-          flags &= flags - 1;
-          const uint32_t v = (e & 32) ? pick32(sh[1], e & 31) : pick32(sh[0], e & 31);
-          const int byte = 64 * h + e;  // key column in the row
-          prow[((((byte >> 4) ^ (t & 7)) << 4)) | (byte & 15)] =
-              (uint8_t)exact_p_code(fmaf(__uint_as_float(v), cc, -m_new));
+          for (int e = 0; e < 32; e += 2) {
+            float t0, t1, x0, x1;
+            f2split(ffma2(f2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), cc2, neg_m2), t0, t1);
+            f2split(fmul2(f2(ex2(t0), ex2(t1)), k448), x0, x1);
+            if (band_key(x0, bm) <= kBandMax) flags |= 1u << e;
+            if (band_key(x1, bm) <= kBandMax) flags |= 1u << (e + 1);
+          }
+          while (flags) {
+            const int e = __ffs(flags) - 1;
+            flags &= flags - 1;
+            const int byte = 32 * c + e;  // key column in the row
+            prow[((((byte >> 4) ^ (t & 7)) << 4)) | (byte & 15)] =
+                (uint8_t)exact_p_code(fmaf(__uint_as_float(pick32(sv, e)), cc, -m_new));
+          }
         }
       }
+      float la, lb;
+      f2split(fadd2(lsum[0], lsum[1]), la, lb);
+      l = fmaf(l, corr, la + lb);
     }
+    // ---- this half's O columns are rescaled when the row maximum moved (any lane of the warp)
     if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
 #pragma unroll 1
-      for (int c = 0; c < D; c += 32) {
+      for (int c = 0; c < DH; c += 32) {
         uint32_t o[32];
         tmem_ld32(o_col + c, o);
         tmem_wait32(o);
@@ -316,23 +320,24 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
       }
       tmem_st_wait();
     }
-    float la, lb;
-    f2split(fadd2(lsum[0], lsum[1]), la, lb);
-    l = fmaf(l, corr, la + lb);
     m = m_new;
     fence_proxy_async_smem();
     tc_fence_before();
     mbar_arrive(&sm.bar_p_full[X]);
   }
-  // ---- epilogue: O = A * sv / l (l sums 448 p~), LSE = ln2 (m + log2(l / 448))
-  if (ok && mbar_wait(&sm.bar_o_done[X], (n_tiles - 1) & 1, abort)) {
-    tc_fence_after();
+  // ---- epilogue: O = A * sv / l (l sums 448 p~ over both halves), LSE = ln2 (m + log2(l / 448))
+  ok = ok && mbar_wait(&sm.bar_o_done[X], (n_tiles - 1) & 1, abort);
+  tc_fence_after();
+  sm.xsum[X][hh][t] = l;
+  named_bar_tile(X);
+  l = sm.xsum[X][0][t] + sm.xsum[X][1][t];  // the same order in both halves
+  if (ok) {
     const float inv_l = 1.0f / l;
     const bool live = row < prm.N;
-    const size_t obase = ((size_t)bh * prm.N + row) * D;
-    const float* svh = prm.sv + (size_t)bh * D;
+    const size_t obase = ((size_t)bh * prm.N + row) * D + hh * DH;
+    const float* svh = prm.sv + (size_t)bh * D + hh * DH;
 #pragma unroll 1
-    for (int c = 0; c < D; c += 32) {
+    for (int c = 0; c < DH; c += 32) {
       uint32_t o[32];
       tmem_ld32(o_col + c, o);
       tmem_wait32(o);
@@ -356,18 +361,19 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
         }
       }
     }
-    if (live) prm.LSE[(size_t)bh * prm.N + row] = (m + (log2f(l) - kLog2_448)) * 0.69314718055994531f;
+    if (live && hh == 0) prm.LSE[(size_t)bh * prm.N + row] = (m + (log2f(l) - kLog2_448)) * 0.69314718055994531f;
   }
 }
 
-// One CTA per (head, pair of 128-query blocks A = 2c, B = 2c + 1).  Warpgroups
-// 0 and 1 run the softmax of tiles A and B; warp 8 loads K and V tiles with
-// TMA; warp 9 allocates TMEM and issues the UMMAs in the order
+// One CTA per (head, pair of 128-query blocks A = 2c, B = 2c + 1).  Warpgroups 0-1 run
+// the softmax of tile A (keys [0,64) and [64,128) of each key tile), 2-3 that of tile B;
+// warp 16 loads K and V tiles with TMA; warp 17 allocates TMEM and issues the UMMAs in
+// the order
 //   S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) ...
 // so the tensor core works on one tile while the other tile's softmax runs.
 // TMEM columns: S_A [0,128), S_B [128,256), O_A [256,256+D), O_B [256+D,256+2D).
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(640, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdParams prm) {
   extern __shared__ uint8_t smem_raw[];
@@ -395,13 +401,13 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&sm.bar_s_full[x], 1);
-      mbar_init(&sm.bar_p_full[x], 128);
+      mbar_init(&sm.bar_p_full[x], 256);
       mbar_init(&sm.bar_o_done[x], 1);
     }
     sm.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == 17) {
     tmem_alloc(&sm.tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -410,87 +416,95 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort = &sm.abort;
 
-  if (warp < 8) {
-    // one call site, so both warpgroups run (and share instruction-cache lines of) one copy
-    const int X = warp >> 2;
-    if (X == 0 || hasB) softmax_tile_loop<D, CAUSAL>(sm, prm, X, X ? qbB : qbA, bh, tmem, abort);
-  } else if (warp == 8 && lane == 0) {
-    // ---------------- producer: Q tiles once, then K and V tiles
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
-    mbar_arrive_expect_tx(&sm.bar_q, (hasB ? 2 : 1) * 128 * D * 2);
-#pragma unroll
-    for (int c = 0; c < D / 64; ++c) {
-      tma_load_3d(sm.q[0] + c * 16384, &tm_q, c * 64, qbA * 128, bh, &sm.bar_q);
-      if (hasB) tma_load_3d(sm.q[1] + c * 16384, &tm_q, c * 64, qbB * 128, bh, &sm.bar_q);
-    }
-    for (int j = 0; j < n_kv; ++j) {
-      const int s = j % kKStages;
-      if (j >= kKStages && !mbar_wait(&sm.bar_k_empty[s], ((j / kKStages) - 1) & 1, abort)) break;
-      mbar_arrive_expect_tx(&sm.bar_k_full[s], 128 * D * 2);
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_3d(sm.k[s] + c * 16384, &tm_k, c * 64, j * 128, bh, &sm.bar_k_full[s]);
-      const int vs = j % kVStages;
-      if (j >= kVStages && !mbar_wait(&sm.bar_v_empty[vs], ((j / kVStages) - 1) & 1, abort)) break;
-      mbar_arrive_expect_tx(&sm.bar_v_full[vs], D * 128);
-      tma_load_3d(sm.v[vs], &tm_v, j * 128, 0, bh, &sm.bar_v_full[vs]);
-    }
-  } else if (warp == 9 && lane == 0) {
-    // ---------------- UMMA issuer
-    constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
-    constexpr uint32_t idesc_o = idesc_e4m3(128, D);
-    auto issue_s = [&](int X, int j) {
-      const uint32_t q_addr = smem_u32(sm.q[X]);
-      const uint32_t k_addr = smem_u32(sm.k[j % kKStages]);
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-        umma_bf16(tmem + (uint32_t)(X * 128), sdesc_sw128(q_addr + off, 16, 1024),
-                  sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0);
+  // the producer/MMA warpgroup needs few registers: hand them to the softmax groups
+  // (launch: 96 x 640; after: 56 x 128 + 104 x 512)
+  constexpr uint32_t kRegsIssue = 56, kRegsSoftmax = 104;
+  static_assert(kRegsIssue * 128 + kRegsSoftmax * 512 <= 96 * 640, "register split exceeds the launch budget");
+  if (warp >= 16) {
+    regs_decrease<kRegsIssue>();
+    if (warp == 16 && lane == 0) {
+      // ---------------- producer: Q tiles once, then K and V tiles
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(&sm.bar_q, (hasB ? 2 : 1) * 128 * D * 2);
+  #pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_3d(sm.q[0] + c * 16384, &tm_q, c * 64, qbA * 128, bh, &sm.bar_q);
+        if (hasB) tma_load_3d(sm.q[1] + c * 16384, &tm_q, c * 64, qbB * 128, bh, &sm.bar_q);
       }
-      umma_commit(&sm.bar_s_full[X]);
-    };
-    auto issue_pv = [&](int X, int j, int first) {
-      const uint32_t p_addr = smem_u32(sm.p[X]);
-      const uint32_t v_addr = smem_u32(sm.v[j % kVStages]);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        umma_f8(tmem + 256u + (uint32_t)(X * D), sdesc_sw128(p_addr + kk * 32, 16, 1024),
-                sdesc_sw128(v_addr + kk * 32, 16, 1024), idesc_o, (!first || kk > 0));
-      umma_commit(&sm.bar_o_done[X]);
-    };
-    bool ok = mbar_wait(&sm.bar_q, 0, abort) && mbar_wait(&sm.bar_k_full[0], 0, abort);
-    if (ok) {
-      tc_fence_after();
-      issue_s(0, 0);
-      if (lastB >= 0) issue_s(1, 0);
-      umma_commit(&sm.bar_k_empty[0]);
-    }
-    for (int j = 0; ok && j < n_kv; ++j) {
-      const bool nextk = j + 1 < n_kv;
-      if (nextk && !mbar_wait(&sm.bar_k_full[(j + 1) % kKStages], ((j + 1) / kKStages) & 1, abort)) break;
-      if (!mbar_wait(&sm.bar_v_full[j % kVStages], (j / kVStages) & 1, abort)) break;
-      for (int X = 0; X < 2; ++X) {
-        const int last = X == 0 ? lastA : lastB;
-        if (j > last) continue;
-        if (!mbar_wait(&sm.bar_p_full[X], j & 1, abort)) {
-          ok = false;
-          break;
+      for (int j = 0; j < n_kv; ++j) {
+        const int s = j % kKStages;
+        if (j >= kKStages && !mbar_wait(&sm.bar_k_empty[s], ((j / kKStages) - 1) & 1, abort)) break;
+        mbar_arrive_expect_tx(&sm.bar_k_full[s], 128 * D * 2);
+  #pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(sm.k[s] + c * 16384, &tm_k, c * 64, j * 128, bh, &sm.bar_k_full[s]);
+        const int vs = j % kVStages;
+        if (j >= kVStages && !mbar_wait(&sm.bar_v_empty[vs], ((j / kVStages) - 1) & 1, abort)) break;
+        mbar_arrive_expect_tx(&sm.bar_v_full[vs], D * 128);
+        tma_load_3d(sm.v[vs], &tm_v, j * 128, 0, bh, &sm.bar_v_full[vs]);
+      }
+    } else if (warp == 17 && lane == 0) {
+      // ---------------- UMMA issuer
+      constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idesc_o = idesc_e4m3(128, D);
+      auto issue_s = [&](int X, int j) {
+        const uint32_t q_addr = smem_u32(sm.q[X]);
+        const uint32_t k_addr = smem_u32(sm.k[j % kKStages]);
+  #pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          umma_bf16(tmem + (uint32_t)(X * 128), sdesc_sw128(q_addr + off, 16, 1024),
+                    sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0);
         }
+        umma_commit(&sm.bar_s_full[X]);
+      };
+      auto issue_pv = [&](int X, int j, int first) {
+        const uint32_t p_addr = smem_u32(sm.p[X]);
+        const uint32_t v_addr = smem_u32(sm.v[j % kVStages]);
+  #pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_f8(tmem + 256u + (uint32_t)(X * D), sdesc_sw128(p_addr + kk * 32, 16, 1024),
+                  sdesc_sw128(v_addr + kk * 32, 16, 1024), idesc_o, (!first || kk > 0));
+        umma_commit(&sm.bar_o_done[X]);
+      };
+      bool ok = mbar_wait(&sm.bar_q, 0, abort) && mbar_wait(&sm.bar_k_full[0], 0, abort);
+      if (ok) {
         tc_fence_after();
-        issue_pv(X, j, j == 0);
-        if (j + 1 <= last) issue_s(X, j + 1);
+        issue_s(0, 0);
+        if (lastB >= 0) issue_s(1, 0);
+        umma_commit(&sm.bar_k_empty[0]);
       }
-      if (!ok) break;
-      umma_commit(&sm.bar_v_empty[j % kVStages]);
-      if (nextk) umma_commit(&sm.bar_k_empty[(j + 1) % kKStages]);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const bool nextk = j + 1 < n_kv;
+        if (nextk && !mbar_wait(&sm.bar_k_full[(j + 1) % kKStages], ((j + 1) / kKStages) & 1, abort)) break;
+        if (!mbar_wait(&sm.bar_v_full[j % kVStages], (j / kVStages) & 1, abort)) break;
+        for (int X = 0; X < 2; ++X) {
+          const int last = X == 0 ? lastA : lastB;
+          if (j > last) continue;
+          if (!mbar_wait(&sm.bar_p_full[X], j & 1, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_pv(X, j, j == 0);
+          if (j + 1 <= last) issue_s(X, j + 1);
+        }
+        if (!ok) break;
+        umma_commit(&sm.bar_v_empty[j % kVStages]);
+        if (nextk) umma_commit(&sm.bar_k_empty[(j + 1) % kKStages]);
+      }
     }
+  } else {
+    regs_increase<kRegsSoftmax>();
+    // one call site, so the four warpgroups run (and share instruction-cache lines of) one copy
+    const int X = warp >> 3, hh = (warp >> 2) & 1;
+    if (X == 0 || hasB) softmax_tile_loop<D, CAUSAL>(sm, prm, X, hh, X ? qbB : qbA, bh, tmem, abort);
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 17) tmem_dealloc(tmem, kTmemCols);
   if (tid == 0 && sm.abort) atomicExch(prm.status, kDevTimeout);
 }
 
@@ -502,7 +516,7 @@ int launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
   auto kern = fwd_kernel<D, CAUSAL>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 3;
   ScopedTimer timer("fwd", st);
-  kern<<<dim3(p.npairs, BH), 384, smem, st>>>(tq, tk, tv, p);
+  kern<<<dim3(p.npairs, BH), 640, smem, st>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 
