@@ -22,7 +22,7 @@
 //                dQ_part = dS8 K8      kind::f16 per 64-key half, scaled, staged in shared
 //                                      memory and added to the fp32 accumulator by TMA reduce
 //              dV and dK (x sm_scale, through QK-norm) written at the end
-//   bwd_dq     per query row: dQ = sm_scale * acc, through QK-norm, to bf16
+//   bwd_dq     (bwd_dq.cu) dQ = sm_scale * acc, through QK-norm, to bf16
 #include <cstddef>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -33,6 +33,7 @@
 #include "kernels.h"
 #include "layout.h"
 #include "ptx.cuh"
+#include "stage.cuh"
 #include "timer.h"
 #include "tmap.h"
 
@@ -66,11 +67,12 @@ __global__ void __launch_bounds__(kPreThreads) bwd_pre_kernel(const __nv_bfloat1
                                                                const float* __restrict__ LSE, int N,
                                                                float* __restrict__ dvec, float* __restrict__ bias,
                                                                float* __restrict__ dopart,
-                                                               float* __restrict__ dqacc) {
+                                                               float* __restrict__ dqacc, int* __restrict__ ticket) {
   constexpr int TPR = D / 8, RPP = kPreThreads / TPR, PASSES = 128 / RPP;
   const int blk = blockIdx.x, bh = blockIdx.y, nb = gridDim.x, np = nb * 128;
   const int tid = threadIdx.x, g = tid % TPR, ro = tid / TPR;
   const size_t head = (size_t)bh * N * D;
+  if (blk == 0 && bh == 0 && tid == 0) *ticket = 0;  // the dQ pass claims its work from it
   float am[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) am[i] = 0.f;
@@ -125,44 +127,20 @@ __global__ void bwd_docomb_kernel(const float* __restrict__ dopart, int D, int n
   sdo[(size_t)bh * D + d] = m > 0.f ? __fdiv_rn(m, 448.0f) : 0.f;
 }
 
+// e4m3 codes of one 128-query block of dO with the head's channel scales, written
+// channel-major [BH, D, Np]; the rows are read straight from global memory
 template <int D>
-__global__ void __launch_bounds__(kPreThreads) bwd_do8_kernel(const __nv_bfloat16* __restrict__ dO, int N,
+__global__ void __launch_bounds__(kPreThreads, 4) bwd_do8_kernel(const __nv_bfloat16* __restrict__ dO, int N,
                                                                const float* __restrict__ sdo,
                                                                uint8_t* __restrict__ do8t) {
-  constexpr int TPR = D / 8, RPP = kPreThreads / TPR, PASSES = 128 / RPP;
-  const int blk = blockIdx.x, bh = blockIdx.y, nb = gridDim.x, np = nb * 128;
-  const int tid = threadIdx.x, g = tid % TPR, ro = tid / TPR;
-  const size_t head = (size_t)bh * N * D;
-  __shared__ __align__(16) uint8_t s8[D][128];
-  float sc[8], inv[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    sc[i] = sdo[(size_t)bh * D + g * 8 + i];
-    inv[i] = sc[i] > 0.f ? __frcp_rn(sc[i]) : 0.f;
-  }
-#pragma unroll
-  for (int p = 0; p < PASSES; ++p) {
-    const int row = p * RPP + ro, t = blk * 128 + row;
-    uint4 u = make_uint4(0, 0, 0, 0);
-    if (t < N) u = __ldg(reinterpret_cast<const uint4*>(dO + head + (size_t)t * D) + g);
-    float x[8];
-    unpack8(u, x);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int d = g * 8 + i;
-      s8[d][row ^ (((d >> 3) & 15) << 2)] = (uint8_t)e4m3_code(x[i], sc[i], inv[i]);
-    }
-  }
-  __syncthreads();
-  for (int idx = tid; idx < D * 8; idx += kPreThreads) {
-    const int d = idx >> 3, c = idx & 7, f = ((d >> 3) & 15) << 2;
-    uint4 val;
-    val.x = *reinterpret_cast<const uint32_t*>(&s8[d][(c * 16 + 0) ^ f]);
-    val.y = *reinterpret_cast<const uint32_t*>(&s8[d][(c * 16 + 4) ^ f]);
-    val.z = *reinterpret_cast<const uint32_t*>(&s8[d][(c * 16 + 8) ^ f]);
-    val.w = *reinterpret_cast<const uint32_t*>(&s8[d][(c * 16 + 12) ^ f]);
-    reinterpret_cast<uint4*>(do8t + ((size_t)bh * D + d) * np + blk * 128)[c] = val;
-  }
+  constexpr int TPR = D / 8;
+  const int blk = blockIdx.x, bh = blockIdx.y, np = gridDim.x * 128;
+  const int rows = min(128, N - blk * 128);
+  __shared__ __align__(16) uint8_t s8[D * 128];
+  const uint4* src = reinterpret_cast<const uint4*>(dO + ((size_t)bh * N + (size_t)blk * 128) * D);
+  e4m3_block_codes<D, kPreThreads>(
+      [&](int t, int g) { return t < rows ? __ldg(src + t * TPR + g) : make_uint4(0, 0, 0, 0); },
+      sdo + (size_t)bh * D, s8, do8t + (size_t)bh * D * np + blk * 128, np);
 }
 
 // ------------------------------------------------------------------ bwd_main
@@ -708,51 +686,6 @@ __global__ void __launch_bounds__(384, 1)
 // ------------------------------------------------------------------ bwd_dq
 // 64 tokens per CTA: the feature-major accumulator is read along tokens (coalesced),
 // transposed through shared memory, scaled, passed through QK-norm, written as bf16 rows.
-template <int D>
-__global__ void __launch_bounds__(kPreThreads) bwd_dq_kernel(const float* __restrict__ dqacc,
-                                                              const __nv_bfloat16* __restrict__ Q,
-                                                              const float* __restrict__ qr, int N, int np,
-                                                              int qk_norm, float sm_scale,
-                                                              __nv_bfloat16* __restrict__ dQ) {
-  constexpr int TPR = D / 8, RPP = kPreThreads / TPR, TOK = 64;
-  __shared__ float tile[D][TOK + 1];
-  const int bh = blockIdx.y, t0 = blockIdx.x * TOK;
-  const int tid = threadIdx.x, g = tid % TPR, ro = tid / TPR;
-  for (int idx = tid; idx < D * TOK; idx += kPreThreads) {
-    const int d = idx / TOK, c = idx % TOK;
-    tile[d][c] = dqacc[((size_t)bh * D + d) * np + t0 + c];
-  }
-  __syncthreads();
-#pragma unroll
-  for (int p = 0; p < TOK / RPP; ++p) {
-    const int r = p * RPP + ro, t = t0 + r;
-    const bool live = t < N;  // no early exit: the row's lanes shuffle together below
-    float x[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) x[i] = tile[g * 8 + i][r] * sm_scale;
-    const size_t row = ((size_t)bh * N + t) * D;
-    if (qk_norm) {
-      const float rr = live ? qr[(size_t)bh * np + t] : 0.f;
-      float qn[8];
-      unpack8(live ? __ldg(reinterpret_cast<const uint4*>(Q + row) + g) : make_uint4(0, 0, 0, 0), qn);
-      float dot = 0.f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        qn[i] = __fmul_rn(qn[i], rr);
-        dot = fmaf(qn[i], x[i], dot);
-      }
-#pragma unroll
-      for (int m = TPR / 2; m >= 1; m >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, m, TPR);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) x[i] = rr * (x[i] - qn[i] * dot);
-    }
-    uint4 u;
-    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) h[e] = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
-    if (live) reinterpret_cast<uint4*>(dQ + row)[g] = u;
-  }
-}
 
 template <int D>
 int launch_main_t(const CUtensorMap& tk, const CUtensorMap& tq, const CUtensorMap& tv, const CUtensorMap& tdo,
@@ -783,15 +716,16 @@ int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const
   float* sdo = reinterpret_cast<float*>(bw + BL.sdo);
   float* dqacc = reinterpret_cast<float*>(bw + BL.dqacc);
   uint8_t* do8t = bw + BL.do8t;
+  int* ticket = reinterpret_cast<int*>(bw + BL.sync);
   auto* o = static_cast<const __nv_bfloat16*>(O);
   auto* dob = static_cast<const __nv_bfloat16*>(dO);
   const dim3 g(nb, BH);
   {
   ScopedTimer timer("bwd_pre", st);
   if (D == 128) {
-    bwd_pre_kernel<128><<<g, kPreThreads, 0, st>>>(o, dob, LSE, N, dvec, biasv, dopart, dqacc);
+    bwd_pre_kernel<128><<<g, kPreThreads, 0, st>>>(o, dob, LSE, N, dvec, biasv, dopart, dqacc, ticket);
   } else {
-    bwd_pre_kernel<64><<<g, kPreThreads, 0, st>>>(o, dob, LSE, N, dvec, biasv, dopart, dqacc);
+    bwd_pre_kernel<64><<<g, kPreThreads, 0, st>>>(o, dob, LSE, N, dvec, biasv, dopart, dqacc, ticket);
   }
   bwd_docomb_kernel<<<BH, 128, 0, st>>>(dopart, D, nb, sdo);
   if (D == 128)
@@ -832,15 +766,9 @@ int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const
   int rc = D == 128 ? launch_main_t<128>(tk, tq, tv, tdo, tdo8, tdq, p, BH, st)
                     : launch_main_t<64>(tk, tq, tv, tdo, tdo8, tdq, p, BH, st);
   if (rc) return rc;
-  const float* qr = reinterpret_cast<const float*>(w + QL.qr);
-  auto* q = static_cast<const __nv_bfloat16*>(Q);
-  auto* dq = static_cast<__nv_bfloat16*>(dQ);
   ScopedTimer timer("bwd_dq", st);
-  if (D == 128)
-    bwd_dq_kernel<128><<<dim3(np / 64, BH), kPreThreads, 0, st>>>(dqacc, q, qr, N, np, qk_norm, sm_scale, dq);
-  else
-    bwd_dq_kernel<64><<<dim3(np / 64, BH), kPreThreads, 0, st>>>(dqacc, q, qr, N, np, qk_norm, sm_scale, dq);
-  return cudaGetLastError() == cudaSuccess ? 0 : 3;
+  return launch_bwd_dq(Q, reinterpret_cast<const float*>(w + QL.qr), bwd_ws, dQ, B, H, N, D, qk_norm, sm_scale,
+                       p.status, st);
 }
 
 }  // namespace sage

@@ -12,6 +12,9 @@ int launch_fwd(const void* ws, void* O, float* LSE, float* O32, int B, int H, in
 int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO,
                void* dQ, void* dK, void* dV, const void* ws, void* bwd_ws, int B, int H, int N, int D,
                int causal, int qk_norm, int k_smooth, float sm_scale, cudaStream_t st);
+// dQ epilogue of the backward (the work ticket in the backward workspace must be zero)
+int launch_bwd_dq(const void* Q, const float* qr, void* bwd_ws, void* dQ, int B, int H, int N, int D, int qk_norm,
+                  float sm_scale, int* status, cudaStream_t st);
 int launch_selftest_wait(void* ws, unsigned long long budget_ns, cudaStream_t st);
 
 }  // namespace sage

@@ -12,7 +12,7 @@ inline int pad128(int n) { return (n + 127) / 128 * 128; }
 
 struct QuantWs {
   // byte offsets
-  size_t status, qc, kc, v8t, sq, sk, sv, kmean, qr, kr, kpart, vpart, total;
+  size_t status, sync, qc, kc, v8t, sq, sk, sv, kmean, qr, kr, kpart, vpart, total;
   int np;
 };
 
@@ -25,6 +25,7 @@ inline QuantWs quant_ws_layout(int B, int H, int N, int D) {
   const size_t nb = np / 128;
   size_t o = 0;
   L.status = o; o = align256(o + 256);
+  L.sync = o;   o = align256(o + 2 * bh * 4);  // per-head counters of finished statistics blocks
   L.qc = o;     o = align256(o + bh * np * D * 2);
   L.kc = o;     o = align256(o + bh * np * D * 2);
   L.v8t = o;    o = align256(o + bh * D * np);
@@ -42,11 +43,11 @@ inline QuantWs quant_ws_layout(int B, int H, int N, int D) {
 }
 
 struct BwdWs {
-  size_t dvec, bias, do8t, sdo, dopart, dqacc, total;
+  size_t sync, dvec, bias, do8t, sdo, dopart, dqacc, total;
   int np;
 };
 
-// backward scratch: D_i, log2(448) - LSE*log2(e) (-inf on padded rows), FP8 dO codes
+// backward scratch: the dQ pass's work ticket, D_i, log2(448) - LSE*log2(e) (-inf on padded rows), FP8 dO codes
 // (channel-major), their channel scales and partial maxima, fp32 dQ accumulator
 // (feature-major [BH, D, Np] so that reductions from query rows coalesce)
 inline BwdWs bwd_ws_layout(int B, int H, int N, int D) {
@@ -55,6 +56,7 @@ inline BwdWs bwd_ws_layout(int B, int H, int N, int D) {
   const int np = pad128(N);
   const size_t nb = np / 128;
   size_t o = 0;
+  L.sync = o;   o = align256(o + 16);
   L.dvec = o;   o = align256(o + bh * np * 4);
   L.bias = o;   o = align256(o + bh * np * 4);
   L.do8t = o;   o = align256(o + bh * D * np);

@@ -1,9 +1,12 @@
 // Quantize pass of the SageBwd scheme ("SageBwd: A Trainable Low-bit Attention",
 // Methodology 1 and 4): QK-norm, K-smoothing, per-block INT8 codes of Q (128
 // tokens) and K (64 tokens), per-channel FP8 e4m3 codes of V (stored
-// channel-major for the PV matmul).  HBM-bound: 128-bit loads and stores, one CTA
-// per (head, 128-token block), values held in registers between the block
-// maximum and the code computation.
+// channel-major for the PV matmul).
+//
+// HBM-bound, two launches: kstats (V channel maxima, column sums of k'; the last block
+// of a head combines them into the V scales and the smoothing mean), then quantize (the
+// codes).  Each CTA stages one 128-token block in shared memory with a bulk copy.
+// Without QK-norm the maxima run on packed bf16 pairs and the codes on fp32 pairs.
 //
 // Bit-exactness rules: every operation the scheme states in fp32 is a single
 // correctly rounded intrinsic (__fmul_rn, __fdiv_rn, ...), so no FMA contraction
@@ -16,6 +19,7 @@
 #include "kernels.h"
 #include "ptx.cuh"
 #include "layout.h"
+#include "stage.cuh"
 #include "timer.h"
 
 namespace sage {
@@ -91,154 +95,220 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// ---------------------------------------------------------------------------
-// A 128-token block of one head is contiguous in memory ([token][channel] bf16 rows).
-// Each CTA stages its block in shared memory with one bulk copy (issued by thread 0,
-// completion on an mbarrier) and computes from there: no data stays in registers across
-// the block reductions, so several CTAs per SM keep well over 100 KB in flight.
-struct BlockStage {
-  uint64_t bar;
-  int abort;
-};
+// ---- packed pairs: two bf16 in a 32-bit word, or two fp32 in a 64-bit register
 
-// Copy `bytes` (a multiple of 16) from src to dst and wait; false for every thread of the
-// CTA when the wait ran out (then the workspace status is set).
-__device__ __forceinline__ bool stage_block(BlockStage& st, void* dst, const void* src, uint32_t bytes,
-                                            int* status) {
-  if (threadIdx.x == 0) {
-    mbar_init(&st.bar, 1);
-    st.abort = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    mbar_arrive_expect_tx(&st.bar, bytes);
-    bulk_load(dst, src, bytes, &st.bar);
-  }
-  mbar_wait(&st.bar, 0, &st.abort);
-  __syncthreads();  // every thread sees the same outcome
-  if (st.abort) {
-    if (threadIdx.x == 0) atomicExch(status, kDevTimeout);
-    return false;
-  }
-  return true;
+// max of two pairs of non-negative bf16 bit patterns (ordered like unsigned integers)
+__device__ __forceinline__ uint32_t umax2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t bmin2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("min.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// largest |x| of the bf16 of a staged row slice (4 words), folded into m (bit patterns)
+__device__ __forceinline__ uint32_t absmax_bits(uint32_t m, const uint4& u) {
+  m = umax2(m, u.x & 0x7fff7fffu);
+  m = umax2(m, u.y & 0x7fff7fffu);
+  m = umax2(m, u.z & 0x7fff7fffu);
+  return umax2(m, u.w & 0x7fff7fffu);
 }
 
-// row `row` (token) of a staged block, channels [8g, 8g+8); zero past the sequence end
-template <int D>
-__device__ __forceinline__ uint4 staged(const uint8_t* buf, int row, int rows, int g) {
-  return row < rows ? reinterpret_cast<const uint4*>(buf + (size_t)row * D * 2)[g] : make_uint4(0, 0, 0, 0);
+// Knuth's two-sum on fp32 pairs: s + e == a + b exactly in each lane
+__device__ __forceinline__ void two_sum2(uint64_t a, uint64_t b, uint64_t& s, uint64_t& e) {
+  s = fadd2(a, b);
+  const uint64_t bb = fsub2(s, a);
+  e = fadd2(fsub2(a, fsub2(s, bb)), fsub2(b, bb));
 }
 
 // ---------------------------------------------------------------------------
-// kstats: per (head, 128-token block): blockIdx.z = 0: partial fp64 column sums of k';
-// blockIdx.z = 1: partial channel maxima of |V|.
-template <int D>
+// ---------------------------------------------------------------------------
+// kstats: per (head, 128-token block): blockIdx.z = 0: partial channel maxima of |V|;
+// blockIdx.z = 1 (with smoothing only): partial fp64 column sums of k'.  The last block
+// of a head to finish (a counter per head and tensor, zeroed before the launch) combines
+// the partials: the V channel scales max|V| / 448, and the smoothing mean as the fp32
+// rounding of (sum over the head's tokens) / N (0 without smoothing).
+template <int D, bool QKN>
 __global__ void __launch_bounds__(kThreads) kstats_kernel(const __nv_bfloat16* __restrict__ K,
                                                            const __nv_bfloat16* __restrict__ V, int N,
-                                                           int qk_norm, double* __restrict__ kpart,
-                                                           float* __restrict__ vpart, int* __restrict__ status) {
+                                                           int k_smooth, double* __restrict__ kpart,
+                                                           float* __restrict__ vpart, int* __restrict__ cnt,
+                                                           float* __restrict__ kmean, float* __restrict__ sv,
+                                                           int* __restrict__ status) {
   constexpr int TPR = D / 8, RPP = kThreads / TPR, PASSES = 128 / RPP;
+  constexpr int J = kThreads / D;  // threads per channel in the combine
   const int blk = blockIdx.x, bh = blockIdx.y, nb = gridDim.x;
+  const bool isk = blockIdx.z == 1;
   const int tid = threadIdx.x, g = tid % TPR, ro = tid / TPR;
   const int rows = min(128, N - blk * 128);
   extern __shared__ __align__(128) uint8_t stage_buf[];
   __shared__ BlockStage st;
-  const __nv_bfloat16* src = (blockIdx.z == 0 ? K : V) + (size_t)bh * N * D + (size_t)blk * 128 * D;
+  __shared__ int s_last;
+  const __nv_bfloat16* src = (isk ? K : V) + (size_t)bh * N * D + (size_t)blk * 128 * D;
   if (!stage_block(st, stage_buf, src, (uint32_t)rows * D * 2, status)) return;
-  if (blockIdx.z == 0) {
-    DF cs[8];
+  if (isk) {
+    DF cs[8];  // this thread's column sums of its channels (double-float)
+    if constexpr (!QKN) {
+      // k' = k: the double-float sums run on channel pairs straight from the bf16 words
+      uint64_t hi[4], lo[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) cs[i] = {0.f, 0.f};
+      for (int w = 0; w < 4; ++w) hi[w] = lo[w] = 0;
 #pragma unroll
-    for (int p = 0; p < PASSES; ++p) {
-      float k[8];
-      unpack8(staged<D>(stage_buf, p * RPP + ro, rows, g), k);
-      if (qk_norm) {
+      for (int p = 0; p < PASSES; ++p) {
+        const uint4 u = staged<D>(stage_buf, p * RPP + ro, rows, g);
+        const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          uint64_t sum, err;
+          two_sum2(hi[w], bf2f2(wv[w]), sum, err);
+          hi[w] = sum;
+          lo[w] = fadd2(lo[w], err);
+        }
+      }
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        cs[2 * w] = {f2lo(hi[w]), f2lo(lo[w])};
+        cs[2 * w + 1] = {f2hi(hi[w]), f2hi(lo[w])};
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) cs[i] = {0.f, 0.f};
+#pragma unroll
+      for (int p = 0; p < PASSES; ++p) {
+        float k[8];
+        unpack8(staged<D>(stage_buf, p * RPP + ro, rows, g), k);
         const float r = inv_norm<TPR>(k);
 #pragma unroll
         for (int i = 0; i < 8; ++i) k[i] = __fmul_rn(k[i], r);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) cs[i] = df_add(cs[i], k[i]);
       }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) cs[i] = df_add(cs[i], k[i]);
     }
-    // combine the RPP row groups per channel in fp64, fixed order
-    __shared__ double s_sum[RPP][D];
+    // combine the rows per channel: the lanes of a warp that hold the same channels (in
+    // double-float), then the warps in fp64 in a fixed order
 #pragma unroll
-    for (int i = 0; i < 8; ++i) s_sum[ro][g * 8 + i] = (double)cs[i].hi + (double)cs[i].lo;
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int m = TPR; m < 32; m <<= 1) cs[i] = df_add(cs[i], df_shfl_xor(cs[i], m));
+    __shared__ double s_sum[kThreads / 32][D];
+    if ((tid & 31) < TPR) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s_sum[tid >> 5][g * 8 + i] = (double)cs[i].hi + (double)cs[i].lo;
+    }
     __syncthreads();
     if (tid < D) {
       double s = 0.0;
-      for (int r = 0; r < RPP; ++r) s += s_sum[r][tid];
+      for (int r = 0; r < kThreads / 32; ++r) s += s_sum[r][tid];
       kpart[((size_t)bh * nb + blk) * D + tid] = s;
     }
   } else {
-    float vm[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) vm[i] = 0.f;
+    // |v| maxima on the bf16 bit patterns, two channels per word
+    uint32_t vb[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
     for (int p = 0; p < PASSES; ++p) {
-      float v[8];
-      unpack8(staged<D>(stage_buf, p * RPP + ro, rows, g), v);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) vm[i] = fmaxf(vm[i], fabsf(v[i]));
+      const uint4 u = staged<D>(stage_buf, p * RPP + ro, rows, g);
+      vb[0] = umax2(vb[0], u.x & 0x7fff7fffu);
+      vb[1] = umax2(vb[1], u.y & 0x7fff7fffu);
+      vb[2] = umax2(vb[2], u.z & 0x7fff7fffu);
+      vb[3] = umax2(vb[3], u.w & 0x7fff7fffu);
     }
-    __shared__ float s_max[RPP][D];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) s_max[ro][g * 8 + i] = vm[i];
+    for (int w = 0; w < 4; ++w)
+#pragma unroll
+      for (int m = TPR; m < 32; m <<= 1) vb[w] = umax2(vb[w], __shfl_xor_sync(0xffffffffu, vb[w], m));
+    __shared__ float s_max[kThreads / 32][D];
+    if ((tid & 31) < TPR) {
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        s_max[tid >> 5][g * 8 + 2 * w] = bf_lo(vb[w]);
+        s_max[tid >> 5][g * 8 + 2 * w + 1] = bf_hi(vb[w]);
+      }
+    }
     __syncthreads();
     if (tid < D) {
       float m = 0.f;
-      for (int r = 0; r < RPP; ++r) m = fmaxf(m, s_max[r][tid]);
+      for (int r = 0; r < kThreads / 32; ++r) m = fmaxf(m, s_max[r][tid]);
       vpart[((size_t)bh * nb + blk) * D + tid] = m;
     }
   }
-}
-
-// kcombine: per head: channel mean of k' (fp32 rounding of the fp64 sum / N) and
-// the V channel scales max|V|/448.
-__global__ void kcombine_kernel(const double* __restrict__ kpart, const float* __restrict__ vpart, int N,
-                                int D, int nb, int k_smooth, float* __restrict__ kmean,
-                                float* __restrict__ sv) {
-  const int bh = blockIdx.x, d = threadIdx.x;
-  if (d >= D) return;
-  // partials summed in block order; their loads are issued 8 at a time
-  double s = 0.0;
-  float m = 0.f;
-  const size_t base = (size_t)bh * nb * D + d;
-  int b = 0;
-  for (; b + 8 <= nb; b += 8) {
-    double ks[8];
-    float vs[8];
+  // count this block; the head's last block combines.  The barrier orders the partial's
+  // stores before thread 0's fence, which releases them to the other blocks with the count.
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    s_last = atomicAdd(cnt + (isk ? gridDim.y : 0) + bh, 1) == nb - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // channel tid % D over the blocks j, j + J, ... (j = tid / D), eight loads in flight,
+  // then the J results of a channel in a fixed order
+  const int d = tid % D, j = tid / D;
+  if (isk) {
+    __shared__ double s_comb[J][D];
+    const double* part = kpart + (size_t)bh * nb * D + d;
+    double s = 0.0;
+    int b = j;
+    for (; b + 7 * J < nb; b += 8 * J) {
+      double v[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      ks[i] = kpart[base + (size_t)(b + i) * D];
-      vs[i] = vpart[base + (size_t)(b + i) * D];
+      for (int u = 0; u < 8; ++u) v[u] = __ldcg(part + (size_t)(b + u * J) * D);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) s += v[u];
     }
+    for (; b < nb; b += J) s += __ldcg(part + (size_t)b * D);
+    s_comb[j][d] = s;
+    __syncthreads();
+    if (tid < D) {
+      double t = 0.0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      s += ks[i];
-      m = fmaxf(m, vs[i]);
+      for (int u = 0; u < J; ++u) t += s_comb[u][tid];
+      kmean[(size_t)bh * D + tid] = (float)(t / (double)N);
+    }
+  } else {
+    __shared__ float f_comb[J][D];
+    const float* part = vpart + (size_t)bh * nb * D + d;
+    float m = 0.f;
+    int b = j;
+    for (; b + 7 * J < nb; b += 8 * J) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = __ldcg(part + (size_t)(b + u * J) * D);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) m = fmaxf(m, v[u]);
+    }
+    for (; b < nb; b += J) m = fmaxf(m, __ldcg(part + (size_t)b * D));
+    f_comb[j][d] = m;
+    __syncthreads();
+    if (tid < D) {
+#pragma unroll
+      for (int u = 0; u < J; ++u) m = fmaxf(m, f_comb[u][tid]);
+      sv[(size_t)bh * D + tid] = m > 0.f ? __fdiv_rn(m, 448.0f) : 0.f;
+      if (!k_smooth) kmean[(size_t)bh * D + tid] = 0.f;
     }
   }
-  for (; b < nb; ++b) {
-    s += kpart[base + (size_t)b * D];
-    m = fmaxf(m, vpart[base + (size_t)b * D]);
-  }
-  kmean[(size_t)bh * D + d] = k_smooth ? (float)(s / (double)N) : 0.f;
-  sv[(size_t)bh * D + d] = m > 0.f ? __fdiv_rn(m, 448.0f) : 0.f;
 }
 
-// quantize: per (head, 128-token block, tensor): blockIdx.z = 0 for Q, 1 for K, 2 for V.
-template <int D>
+// quantize: per (head, 128-token block, tensor): which = 0 for Q, 1 for K, 2 for V.
+template <int D, bool QKN>
 __global__ void __launch_bounds__(kThreads) quantize_kernel(
     const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K,
-    const __nv_bfloat16* __restrict__ V, int N, int qk_norm, int k_smooth, const float* __restrict__ kmean,
+    const __nv_bfloat16* __restrict__ V, int N, int k_smooth, const float* __restrict__ kmean,
     const float* __restrict__ sv, __nv_bfloat16* __restrict__ qc, __nv_bfloat16* __restrict__ kc,
     uint8_t* __restrict__ v8t, float* __restrict__ sq, float* __restrict__ sk, float* __restrict__ qr,
     float* __restrict__ kr, int* __restrict__ status) {
   constexpr int TPR = D / 8, RPP = kThreads / TPR, PASSES = 128 / RPP;
-  const int blk = blockIdx.x, bh = blockIdx.y, which = blockIdx.z, nb = gridDim.x, np = nb * 128;
+  // grid z runs K, V, then Q: the keys and values the statistics pass has just read are
+  // re-read while they are still in L2
+  const int which = blockIdx.z == 2 ? 0 : (int)blockIdx.z + 1;
+  const int blk = blockIdx.x, bh = blockIdx.y, nb = gridDim.x, np = nb * 128;
   const int tid = threadIdx.x, g = tid % TPR, ro = tid / TPR, warp = tid >> 5, lane = tid & 31;
   const size_t phead = (size_t)bh * np * D;
   const int rows = min(128, N - blk * 128);
@@ -253,79 +323,109 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(
   if (!stage_block(st, stage_buf, src, (uint32_t)rows * D * 2, status)) return;
 
   if (which == 2) {
-    // ---- V: e4m3 codes with channel scales, transposed through shared memory
-    float svv[8], inv[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      svv[i] = sv[(size_t)bh * D + g * 8 + i];
-      inv[i] = svv[i] > 0.f ? __frcp_rn(svv[i]) : 0.f;
-    }
-#pragma unroll
-    for (int p = 0; p < PASSES; ++p) {
-      const int row = p * RPP + ro;
-      float v[8];
-      uint32_t c8[8];
-      unpack8(staged<D>(stage_buf, row, rows, g), v);
-      // e4m3(RN(v / s_v)): round to nearest even, saturating to +-448
-      e4m3_codes8(v, svv, inv, c8);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int d = g * 8 + i;
-        s_v8[d][row ^ (((d >> 3) & 15) << 2)] = (uint8_t)c8[i];
-      }
-    }
-    __syncthreads();
-    // D rows of 128 bytes: 16 bytes per thread per step
-    for (int idx = tid; idx < D * 8; idx += kThreads) {
-      const int d = idx >> 3, c = idx & 7, f = ((d >> 3) & 15) << 2;
-      uint4 val;
-      val.x = *reinterpret_cast<const uint32_t*>(&s_v8[d][(c * 16 + 0) ^ f]);
-      val.y = *reinterpret_cast<const uint32_t*>(&s_v8[d][(c * 16 + 4) ^ f]);
-      val.z = *reinterpret_cast<const uint32_t*>(&s_v8[d][(c * 16 + 8) ^ f]);
-      val.w = *reinterpret_cast<const uint32_t*>(&s_v8[d][(c * 16 + 12) ^ f]);
-      reinterpret_cast<uint4*>(v8t + ((size_t)bh * D + d) * np + blk * 128)[c] = val;
-    }
+    // ---- V: e4m3 codes with channel scales, channel-major
+    e4m3_block_codes<D, kThreads>([&](int t, int gg) { return staged<D>(stage_buf, t, rows, gg); },
+                                  sv + (size_t)bh * D, &s_v8[0][0], v8t + (size_t)bh * D * np + blk * 128, np);
     return;
   }
 
   // ---- Q (which == 0): optional norm, one 128-token block max;
   //      K (which == 1): optional norm, minus the channel mean, two 64-token block maxima.
-  // The staged block is read twice: for the maxima, then for the codes.
+  // The staged block is read twice: for the maxima, then for the codes.  Without QK-norm
+  // both passes run on bf16 pairs (packed maxima, fp32-pair arithmetic); with it, or for a
+  // smoothed key block shorter than 128 tokens, the maxima take the general path.
   const bool isk = which == 1;
+  const bool smooth = isk && k_smooth;
   float km[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) km[i] = (isk && k_smooth) ? kmean[(size_t)bh * D + g * 8 + i] : 0.f;
+  for (int i = 0; i < 8; ++i) km[i] = smooth ? kmean[(size_t)bh * D + g * 8 + i] : 0.f;
   float* rout = isk ? kr : qr;
   float rn[PASSES];
   // x' = x r - m for keys inside the sequence (x r for queries), 0 past its end
-  auto prep = [&](int p, float (&x)[8]) {
+  auto prep = [&](int p, float r, float (&x)[8]) {
     const int row = p * RPP + ro;
     unpack8(staged<D>(stage_buf, row, rows, g), x);
-    if (qk_norm) {
+    if constexpr (QKN) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) x[i] = __fmul_rn(x[i], rn[p]);
+      for (int i = 0; i < 8; ++i) x[i] = __fmul_rn(x[i], r);
     }
     if (isk) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) x[i] = (row < rows) ? (k_smooth ? __fsub_rn(x[i], km[i]) : x[i]) : 0.f;
     }
   };
+  // rows [0, 64) of the block are passes [0, PASSES / 2): the key half of a pass is uniform
   float am[2] = {0.f, 0.f};
+  if (!QKN && !smooth) {
+    // x' = x (zero past the end): largest |x| on the bf16 bit patterns
+    uint32_t mb[2] = {0u, 0u};
 #pragma unroll
-  for (int p = 0; p < PASSES; ++p) {
-    const int row = p * RPP + ro;
-    float x[8];
-    if (qk_norm) {
-      unpack8(staged<D>(stage_buf, row, rows, g), x);
-      rn[p] = inv_norm<TPR>(x);
-    } else {
-      rn[p] = 1.f;
+    for (int p = 0; p < PASSES; ++p) {
+      // the key half of a pass is uniform: isk selects between two registers
+      const uint4 u = staged<D>(stage_buf, p * RPP + ro, rows, g);
+      if (isk && p >= PASSES / 2)
+        mb[1] = absmax_bits(mb[1], u);
+      else
+        mb[0] = absmax_bits(mb[0], u);
     }
-    if (g == 0) rout[(size_t)bh * np + blk * 128 + row] = rn[p];
-    prep(p, x);
-    const int hsel = isk && row >= 64;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) am[hsel] = fmaxf(am[hsel], fabsf(x[i]));
+    for (int h = 0; h < 2; ++h) am[h] = fmaxf(bf_lo(mb[h]), bf_hi(mb[h]));
+  } else if (!QKN && rows == 128) {
+    // x' = RN(k - m): |x'| is largest at a channel's largest or smallest k, and rounding
+    // is monotonic, so max |x'| = max over channels of RN(kmax - m), RN(m - kmin)
+    uint32_t mx[2][4], mn[2][4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        mx[h][w] = 0xff80ff80u;  // -inf, -inf
+        mn[h][w] = 0x7f807f80u;  // +inf, +inf
+      }
+#pragma unroll
+    for (int p = 0; p < PASSES; ++p) {
+      const int h = p >= PASSES / 2;
+      const uint4 u = staged<D>(stage_buf, p * RPP + ro, rows, g);
+      const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        mx[h][w] = bmax2(mx[h][w], wv[w]);
+        mn[h][w] = bmin2(mn[h][w], wv[w]);
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        am[h] = max3(am[h], __fsub_rn(bf_lo(mx[h][w]), km[2 * w]), __fsub_rn(km[2 * w], bf_lo(mn[h][w])));
+        am[h] = max3(am[h], __fsub_rn(bf_hi(mx[h][w]), km[2 * w + 1]), __fsub_rn(km[2 * w + 1], bf_hi(mn[h][w])));
+      }
+  }
+  if constexpr (!QKN) {
+#pragma unroll
+    for (int p = 0; p < PASSES; ++p) {
+      rn[p] = 1.f;
+      if (g == 0) rout[(size_t)bh * np + blk * 128 + p * RPP + ro] = 1.f;
+    }
+  }
+  if (QKN || (smooth && rows < 128)) {
+#pragma unroll
+    for (int p = 0; p < PASSES; ++p) {
+      const int row = p * RPP + ro;
+      float x[8];
+      if constexpr (QKN) {
+        unpack8(staged<D>(stage_buf, row, rows, g), x);
+        rn[p] = inv_norm<TPR>(x);
+        if (g == 0) rout[(size_t)bh * np + blk * 128 + row] = rn[p];
+      }
+      prep(p, rn[p], x);
+      float a = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(x[i]));
+      if (isk && row >= 64)
+        am[1] = fmaxf(am[1], a);
+      else
+        am[0] = fmaxf(am[0], a);
+    }
   }
   am[0] = warp_max(am[0]);
   am[1] = warp_max(am[1]);
@@ -335,6 +435,7 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(
   }
   __syncthreads();
   float sc[2], inv[2];
+  bool exact[2];  // a scale whose reciprocal is not a finite number: every code divides
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     float a = 0.f;
@@ -342,21 +443,71 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(
     for (int w = 0; w < kThreads / 32; ++w) a = fmaxf(a, s_red[h][w]);
     sc[h] = a > 0.f ? __fdiv_rn(a, 127.0f) : 0.f;
     inv[h] = sc[h] > 0.f ? __frcp_rn(sc[h]) : 0.f;
+    exact[h] = !(sc[h] < INFINITY && inv[h] < INFINITY);
   }
   if (!isk) {
     if (tid == 0) sq[(size_t)bh * nb + blk] = sc[0];
   } else if (tid < 2) {
-    sk[(size_t)bh * nb * 2 + blk * 2 + tid] = sc[tid];
+    sk[(size_t)bh * nb * 2 + blk * 2 + tid] = tid ? sc[1] : sc[0];
   }
   __nv_bfloat16* dst = isk ? kc : qc;
+  if constexpr (QKN) {
 #pragma unroll
-  for (int p = 0; p < PASSES; ++p) {
-    const int row = p * RPP + ro;
-    const int hs = isk && row >= 64;
-    float x[8], c[8];
-    prep(p, x);
-    int_codes8(x, sc[hs], inv[hs], c);
-    reinterpret_cast<uint4*>(dst + phead + (size_t)(blk * 128 + row) * D)[g] = pack8_bf16(c);
+    for (int p = 0; p < PASSES; ++p) {
+      const int row = p * RPP + ro;
+      const bool hs = isk && row >= 64;
+      float x[8], c[8];
+      prep(p, rn[p], x);
+      int_codes8(x, hs ? sc[1] : sc[0], hs ? inv[1] : inv[0], c);
+      reinterpret_cast<uint4*>(dst + phead + (size_t)(blk * 128 + row) * D)[g] = pack8_bf16(c);
+    }
+  } else {
+    // codes on fp32 pairs: q = RN(x' inv), code = rint(q); q is within 2 ulps of x' / s, so
+    // the code is that of the division unless q is within 2^-14 of a half-integer.  With a
+    // finite reciprocal |q| <= RN(a inv) < 127.5: no clamp is needed.
+    uint64_t km2[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) km2[w] = f2(km[2 * w], km[2 * w + 1]);
+#pragma unroll
+    for (int p = 0; p < PASSES; ++p) {
+      const int row = p * RPP + ro;
+      const bool hs = isk && p >= PASSES / 2;
+      const float sch = hs ? sc[1] : sc[0], invh = hs ? inv[1] : inv[0];
+      const bool exacth = hs ? exact[1] : exact[0];
+      uint4 out = make_uint4(0u, 0u, 0u, 0u);  // past the end: zero codes
+      if (row < rows) {
+        const uint4 u = staged<D>(stage_buf, row, rows, g);
+        const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+        uint32_t ow[4];
+        const uint64_t inv2 = f2(invh, invh);
+        float dm = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          uint64_t x = bf2f2(wv[w]);
+          if (smooth) x = fsub2(x, km2[w]);
+          const uint64_t q = fmul2(x, inv2);
+          const float r0 = rintf(f2lo(q)), r1 = rintf(f2hi(q));
+          const uint64_t d = fsub2(q, f2(r0, r1));
+          dm = max3(dm, fabsf(f2lo(d)), fabsf(f2hi(d)));
+          __nv_bfloat162 h = __floats2bfloat162_rn(r0, r1);
+          ow[w] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        if (dm > 0.49993896484375f || exacth) {
+          // rare: the division decides (and clamps, for non-finite scales)
+          float x[8], c[8];
+          unpack8(u, x);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (smooth) x[i] = __fsub_rn(x[i], km[i]);
+            c[i] = fminf(fmaxf(rintf(__fdiv_rn(x[i], sch)), -127.f), 127.f);
+          }
+          out = pack8_bf16(c);
+        } else {
+          out = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+        }
+      }
+      reinterpret_cast<uint4*>(dst + phead + (size_t)(blk * 128 + row) * D)[g] = out;
+    }
   }
 }
 
@@ -378,16 +529,19 @@ int launch_quantize(const void* Q, const void* K, const void* V, int B, int H, i
   int* status = reinterpret_cast<int*>(w + L.status);
   const size_t stage = (size_t)128 * D * 2;  // one staged token block
   ScopedTimer timer("quantize", st);
-  // the status word is cleared before the kernels that may set it
-  if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return 3;
-  auto stats = D == 128 ? kstats_kernel<128> : kstats_kernel<64>;
-  auto quant = D == 128 ? quantize_kernel<128> : quantize_kernel<64>;
+  // the status word and the per-head counters are cleared before the kernels that use them
+  if (cudaMemsetAsync(w + L.status, 0, L.qc - L.status, st) != cudaSuccess) return 3;
+  auto stats = D == 128 ? (qk_norm ? kstats_kernel<128, true> : kstats_kernel<128, false>)
+                        : (qk_norm ? kstats_kernel<64, true> : kstats_kernel<64, false>);
+  auto quant = D == 128 ? (qk_norm ? quantize_kernel<128, true> : quantize_kernel<128, false>)
+                        : (qk_norm ? quantize_kernel<64, true> : quantize_kernel<64, false>);
   if (cudaFuncSetAttribute(stats, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)stage) != cudaSuccess ||
       cudaFuncSetAttribute(quant, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)stage) != cudaSuccess)
     return 3;
-  stats<<<dim3(nb, B * H, 2), kThreads, stage, st>>>(k, v, N, qk_norm, kpart, vpart, status);
-  kcombine_kernel<<<B * H, 128, 0, st>>>(kpart, vpart, N, D, nb, k_smooth, kmean, sv);
-  quant<<<qgrid, kThreads, stage, st>>>(q, k, v, N, qk_norm, k_smooth, kmean, sv,
+  stats<<<dim3(nb, B * H, k_smooth ? 2 : 1), kThreads, stage, st>>>(k, v, N, k_smooth, kpart, vpart,
+                                                                   reinterpret_cast<int*>(w + L.sync), kmean, sv,
+                                                                   status);
+  quant<<<qgrid, kThreads, stage, st>>>(q, k, v, N, k_smooth, kmean, sv,
                                         reinterpret_cast<__nv_bfloat16*>(w + L.qc),
                                         reinterpret_cast<__nv_bfloat16*>(w + L.kc), w + L.v8t,
                                         reinterpret_cast<float*>(w + L.sq), reinterpret_cast<float*>(w + L.sk),
