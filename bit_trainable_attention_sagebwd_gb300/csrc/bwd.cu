@@ -31,6 +31,7 @@
 #include "../../include/sage_attn.h"
 #include "codes.cuh"
 #include "kernels.h"
+#include "launch.h"
 #include "layout.h"
 #include "ptx.cuh"
 #include "stage.cuh"
@@ -72,6 +73,8 @@ __global__ void __launch_bounds__(kPreThreads) bwd_pre_kernel(const __nv_bfloat1
   const int blk = blockIdx.x, bh = blockIdx.y, nb = gridDim.x, np = nb * 128;
   const int tid = threadIdx.x, g = tid % TPR, ro = tid / TPR;
   const size_t head = (size_t)bh * N * D;
+  pdl_wait();  // O and LSE come from the forward
+  pdl_trigger();
   if (blk == 0 && bh == 0 && tid == 0) *ticket = 0;  // the dQ pass claims its work from it
   float am[8];
 #pragma unroll
@@ -121,6 +124,8 @@ __global__ void __launch_bounds__(kPreThreads) bwd_pre_kernel(const __nv_bfloat1
 
 __global__ void bwd_docomb_kernel(const float* __restrict__ dopart, int D, int nb, float* __restrict__ sdo) {
   const int bh = blockIdx.x, d = threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
   if (d >= D) return;
   float m = 0.f;
   for (int b = 0; b < nb; ++b) m = fmaxf(m, dopart[((size_t)bh * nb + b) * D + d]);
@@ -138,6 +143,8 @@ __global__ void __launch_bounds__(kPreThreads, 4) bwd_do8_kernel(const __nv_bflo
   const int rows = min(128, N - blk * 128);
   __shared__ __align__(16) uint8_t s8[D * 128];
   const uint4* src = reinterpret_cast<const uint4*>(dO + ((size_t)bh * N + (size_t)blk * 128) * D);
+  pdl_wait();  // the channel scales come from bwd_docomb
+  pdl_trigger();
   e4m3_block_codes<D, kPreThreads>(
       [&](int t, int g) { return t < rows ? __ldg(src + t * TPR + g) : make_uint4(0, 0, 0, 0); },
       sdo + (size_t)bh * D, s8, do8t + (size_t)bh * D * np + blk * 128, np);
@@ -256,6 +263,8 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort = &sm.abort;
+  pdl_wait();  // dO codes, scales and the zeroed accumulator come from the preparation
+  pdl_trigger();
   // the producer/MMA warpgroup needs few registers: hand them to the compute groups
   // (launch: 168 x 384; after: 80 x 128 + 208 x 256)
   constexpr uint32_t kRegsIssue = 80, kRegsCompute = 208;
@@ -683,10 +692,6 @@ __global__ void __launch_bounds__(384, 1)
   if (tid == 0 && sm.abort) atomicExch(prm.status, kDevTimeout);
 }
 
-// ------------------------------------------------------------------ bwd_dq
-// 64 tokens per CTA: the feature-major accumulator is read along tokens (coalesced),
-// transposed through shared memory, scaled, passed through QK-norm, written as bf16 rows.
-
 template <int D>
 int launch_main_t(const CUtensorMap& tk, const CUtensorMap& tq, const CUtensorMap& tv, const CUtensorMap& tdo,
                   const CUtensorMap& tdo8, const CUtensorMap& tdq, const BwdParams& p, int BH, cudaStream_t st) {
@@ -695,7 +700,7 @@ int launch_main_t(const CUtensorMap& tk, const CUtensorMap& tq, const CUtensorMa
   auto kern = bwd_main_kernel<D>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 3;
   ScopedTimer timer("bwd_main", st);
-  kern<<<dim3(p.nqb, BH), 384, smem, st>>>(tk, tq, tv, tdo, tdo8, tdq, p);
+  if (launch_pdl(kern, dim3(p.nqb, BH), dim3(384), smem, st, tk, tq, tv, tdo, tdo8, tdq, p) != cudaSuccess) return 3;
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 
@@ -722,16 +727,12 @@ int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const
   const dim3 g(nb, BH);
   {
   ScopedTimer timer("bwd_pre", st);
-  if (D == 128) {
-    bwd_pre_kernel<128><<<g, kPreThreads, 0, st>>>(o, dob, LSE, N, dvec, biasv, dopart, dqacc, ticket);
-  } else {
-    bwd_pre_kernel<64><<<g, kPreThreads, 0, st>>>(o, dob, LSE, N, dvec, biasv, dopart, dqacc, ticket);
-  }
-  bwd_docomb_kernel<<<BH, 128, 0, st>>>(dopart, D, nb, sdo);
-  if (D == 128)
-    bwd_do8_kernel<128><<<g, kPreThreads, 0, st>>>(dob, N, sdo, do8t);
-  else
-    bwd_do8_kernel<64><<<g, kPreThreads, 0, st>>>(dob, N, sdo, do8t);
+  if (launch_pdl(D == 128 ? bwd_pre_kernel<128> : bwd_pre_kernel<64>, g, dim3(kPreThreads), 0, st, o, dob, LSE, N,
+                 dvec, biasv, dopart, dqacc, ticket) != cudaSuccess ||
+      launch_pdl(bwd_docomb_kernel, dim3(BH), dim3(128), 0, st, (const float*)dopart, D, nb, sdo) != cudaSuccess ||
+      launch_pdl(D == 128 ? bwd_do8_kernel<128> : bwd_do8_kernel<64>, g, dim3(kPreThreads), 0, st, dob, N,
+                 (const float*)sdo, do8t) != cudaSuccess)
+    return 3;
   }
   if (cudaGetLastError() != cudaSuccess) return 3;
 

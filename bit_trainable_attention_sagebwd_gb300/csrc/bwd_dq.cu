@@ -10,6 +10,7 @@
 #include <cuda_bf16.h>
 
 #include "kernels.h"
+#include "launch.h"
 #include "layout.h"
 #include "ptx.cuh"
 #include "stream.cuh"
@@ -58,6 +59,8 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_kernel(const __grid_consta
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int tl = (warp & 1) * 32 + lane, fg = warp >> 1;
   if (tid == 0) tma_prefetch_desc(&tacc);
+  pdl_wait();  // the accumulator comes from the main backward kernel
+  pdl_trigger();
   auto issue = [&](int item, uint8_t* stage, uint64_t* bar) {
     mbar_arrive_expect_tx(bar, kStage);
     tma_load_3d(stage, &tacc, (item % p.nc) * kChunk, 0, item / p.nc, bar);
@@ -137,7 +140,9 @@ int launch_bwd_dq(const void* Q, const float* qr, void* bwd_ws, void* dQ, int B,
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 3;
     attr[D == 128] = true;
   }
-  kern<<<persistent_grid(kern, kThreads, smem, nitems), kThreads, smem, st>>>(tacc, p);
+  if (launch_pdl(kern, dim3(persistent_grid(kern, kThreads, smem, nitems)), dim3(kThreads), smem, st, tacc, p) !=
+      cudaSuccess)
+    return 3;
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 

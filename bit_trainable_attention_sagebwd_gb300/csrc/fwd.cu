@@ -18,6 +18,7 @@
 #include <cuda_fp8.h>
 
 #include "kernels.h"
+#include "launch.h"
 #include "layout.h"
 #include "ptx.cuh"
 #include "timer.h"
@@ -415,6 +416,8 @@ __global__ void __launch_bounds__(640, 1)
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort = &sm.abort;
+  pdl_wait();  // the codes and scales come from the quantize pass
+  pdl_trigger();
 
   // the producer/MMA warpgroup needs few registers: hand them to the softmax groups
   // (launch: 96 x 640; after: 56 x 128 + 104 x 512)
@@ -516,7 +519,7 @@ int launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
   auto kern = fwd_kernel<D, CAUSAL>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 3;
   ScopedTimer timer("fwd", st);
-  kern<<<dim3(p.npairs, BH), 640, smem, st>>>(tq, tk, tv, p);
+  if (launch_pdl(kern, dim3(p.npairs, BH), dim3(640), smem, st, tq, tk, tv, p) != cudaSuccess) return 3;
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 

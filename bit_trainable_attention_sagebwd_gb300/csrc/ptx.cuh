@@ -75,6 +75,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// ------------------------------------------------ programmatic dependent launch
+// Kernels of one pass follow each other on a stream with programmatic serialization:
+// the next kernel's CTAs may start while this one drains.  Each kernel waits for its
+// predecessor (completion and memory) before touching anything the predecessor writes or
+// reads, then lets its own successor launch.  Without the launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ----------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
   asm volatile(

@@ -18,6 +18,7 @@
 #include "codes.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
+#include "launch.h"
 #include "layout.h"
 #include "stage.cuh"
 #include "timer.h"
@@ -153,6 +154,8 @@ __global__ void __launch_bounds__(kThreads) kstats_kernel(const __nv_bfloat16* _
   __shared__ int s_last;
   const __nv_bfloat16* src = (isk ? K : V) + (size_t)bh * N * D + (size_t)blk * 128 * D;
   if (!stage_block(st, stage_buf, src, (uint32_t)rows * D * 2, status)) return;
+  pdl_wait();  // the input block is staged; the partials and counters come after the predecessor
+  pdl_trigger();
   if (isk) {
     DF cs[8];  // this thread's column sums of its channels (double-float)
     if constexpr (!QKN) {
@@ -321,6 +324,8 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(
 
   const __nv_bfloat16* src = (which == 0 ? Q : (which == 1 ? K : V)) + (size_t)bh * N * D + (size_t)blk * 128 * D;
   if (!stage_block(st, stage_buf, src, (uint32_t)rows * D * 2, status)) return;
+  pdl_wait();  // the scales and the mean come from kstats
+  pdl_trigger();
 
   if (which == 2) {
     // ---- V: e4m3 codes with channel scales, channel-major
@@ -538,14 +543,15 @@ int launch_quantize(const void* Q, const void* K, const void* V, int B, int H, i
   if (cudaFuncSetAttribute(stats, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)stage) != cudaSuccess ||
       cudaFuncSetAttribute(quant, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)stage) != cudaSuccess)
     return 3;
-  stats<<<dim3(nb, B * H, k_smooth ? 2 : 1), kThreads, stage, st>>>(k, v, N, k_smooth, kpart, vpart,
-                                                                   reinterpret_cast<int*>(w + L.sync), kmean, sv,
-                                                                   status);
-  quant<<<qgrid, kThreads, stage, st>>>(q, k, v, N, k_smooth, kmean, sv,
-                                        reinterpret_cast<__nv_bfloat16*>(w + L.qc),
-                                        reinterpret_cast<__nv_bfloat16*>(w + L.kc), w + L.v8t,
-                                        reinterpret_cast<float*>(w + L.sq), reinterpret_cast<float*>(w + L.sk),
-                                        reinterpret_cast<float*>(w + L.qr), reinterpret_cast<float*>(w + L.kr), status);
+  int* cnt = reinterpret_cast<int*>(w + L.sync);
+  if (launch_pdl(stats, dim3(nb, B * H, k_smooth ? 2 : 1), dim3(kThreads), stage, st, k, v, N, k_smooth, kpart, vpart,
+                 cnt, kmean, sv, status) != cudaSuccess)
+    return 3;
+  if (launch_pdl(quant, qgrid, dim3(kThreads), stage, st, q, k, v, N, k_smooth, (const float*)kmean, (const float*)sv,
+                 reinterpret_cast<__nv_bfloat16*>(w + L.qc), reinterpret_cast<__nv_bfloat16*>(w + L.kc), w + L.v8t,
+                 reinterpret_cast<float*>(w + L.sq), reinterpret_cast<float*>(w + L.sk),
+                 reinterpret_cast<float*>(w + L.qr), reinterpret_cast<float*>(w + L.kr), status) != cudaSuccess)
+    return 3;
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 
