@@ -24,7 +24,8 @@ SAGE_OK, SAGE_ERR_INVALID_ARG, SAGE_ERR_UNSUPPORTED, SAGE_ERR_CUDA, SAGE_ERR_TIM
 ABI_FUNCTIONS = ("sage_attn_ws_bytes", "sage_attn_bwd_ws_bytes", "sage_attn_quantize", "sage_attn_fwd",
                  "sage_attn_bwd", "sage_attn_ws_views", "sage_attn_get_status", "sage_attn_selftest_wait",
                  "sage_attn_status_str", "sage_attn_timer_enable", "sage_attn_timer_read",
-                 "sage_attn_bwd_noalloc")
+                 "sage_attn_bwd_noalloc", "sage_attn_step_host_bytes", "sage_attn_step_host",
+                 "sage_attn_timer_only")
 
 
 class SageError(RuntimeError):
@@ -64,7 +65,11 @@ def lib():
             L.sage_attn_get_status.argtypes = [vp, vp]
             L.sage_attn_selftest_wait.argtypes = [vp, u64, vp]
             L.sage_attn_bwd_noalloc.argtypes = [vp] * 10 + [i] * 7 + [fp, vp]
+            L.sage_attn_step_host_bytes.restype = sz
+            L.sage_attn_step_host_bytes.argtypes = [i, i, i, i, i]
+            L.sage_attn_step_host.argtypes = [vp] * 10 + [sz] + [i] * 7 + [fp, i, vp]
             L.sage_attn_timer_enable.argtypes = [i]
+            L.sage_attn_timer_only.argtypes = [ctypes.c_char_p]
             L.sage_attn_timer_read.argtypes = [ctypes.c_char_p, ctypes.POINTER(ctypes.c_double),
                                                ctypes.POINTER(ctypes.c_int)]
             L.sage_attn_status_str.restype = ctypes.c_char_p
@@ -103,6 +108,16 @@ def sage_attn_bwd_noalloc(Q, K, V, O, LSE, dO, dQ, dK, dV, ws, B, H, N, D, causa
                                        int(qk_norm), int(k_smooth), float(sm_scale), stream)
 
 
+def sage_attn_step_host_bytes(B, H, N, D, groups):
+    return lib().sage_attn_step_host_bytes(B, H, N, D, int(groups))
+
+
+def sage_attn_step_host(Q, K, V, dO, O, LSE, dQ, dK, dV, dev, dev_bytes, B, H, N, D, causal, qk_norm, k_smooth,
+                        sm_scale, groups, stream):
+    return lib().sage_attn_step_host(Q, K, V, dO, O, LSE, dQ, dK, dV, dev, dev_bytes, B, H, N, D, int(causal),
+                                     int(qk_norm), int(k_smooth), float(sm_scale), int(groups), stream)
+
+
 def sage_attn_ws_views(ws, B, H, N, D) -> sage_ws_views:
     v = sage_ws_views()
     rc = lib().sage_attn_ws_views(ws, B, H, N, D, ctypes.byref(v))
@@ -121,6 +136,11 @@ def sage_attn_selftest_wait(ws, budget_ns, stream):
 
 def sage_attn_timer_enable(on):
     return lib().sage_attn_timer_enable(int(on))
+
+
+def sage_attn_timer_only(kernel):
+    """Time only the launch group `kernel` (None: every group)."""
+    return lib().sage_attn_timer_only(kernel.encode() if kernel else None)
 
 
 def sage_attn_timer_read(kernel: str):
@@ -218,6 +238,30 @@ def backward(q, k, v, o, lse, do, ws, causal, qk_norm=False, k_smooth=True, sm_s
                                           _ptr(dk), _ptr(dv), _ptr(ws), _ptr(bwd_ws), bwd_ws.numel(), B, H, N,
                                           D, causal, qk_norm, k_smooth, sm_scale, _stream_ptr(stream)))
     return dq, dk, dv
+
+
+def alloc_step_host(B, H, N, D, groups=0, device="cuda"):
+    """Device scratch for step_host (its status word: get_status(scratch))."""
+    import torch
+    n = sage_attn_step_host_bytes(B, H, N, D, groups)
+    if n == 0:
+        raise SageError("sage_attn_step_host_bytes", SAGE_ERR_UNSUPPORTED)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def step_host(q, k, v, do, out, scratch, causal, qk_norm=False, k_smooth=True, sm_scale=None, groups=0,
+              stream=None):
+    """Quantize + forward + backward of host (CPU, ideally pinned) bf16 [B, H, N, D] tensors with the copies
+    overlapped with the computation.  `out` holds host tensors o, lse, dq, dk, dv that receive the results;
+    they are complete once `stream` has completed."""
+    B, H, N, D = _shape(q)
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    _check("sage_attn_step_host",
+           sage_attn_step_host(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(out["o"]), _ptr(out["lse"]),
+                               _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(scratch), scratch.numel(),
+                               B, H, N, D, causal, qk_norm, k_smooth, sm_scale, groups, _stream_ptr(stream)))
+    return out
 
 
 def get_status(ws, stream=None) -> int:

@@ -135,6 +135,11 @@ int sage_attn_timer_enable(int on) {
   return SAGE_OK;
 }
 
+int sage_attn_timer_only(const char* kernel) {
+  sage::timer_only(kernel);
+  return SAGE_OK;
+}
+
 int sage_attn_timer_read(const char* kernel, double* total_ms, int* launches) {
   if (kernel == nullptr) return SAGE_ERR_INVALID_ARG;
   return sage::timer_read(kernel, total_ms, launches) == 0 ? SAGE_OK : SAGE_ERR_CUDA;

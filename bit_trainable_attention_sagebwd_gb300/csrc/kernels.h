@@ -5,8 +5,9 @@
 
 namespace sage {
 
+// clear_status = false keeps the workspace status word (errors of earlier launches)
 int launch_quantize(const void* Q, const void* K, const void* V, int B, int H, int N, int D, int qk_norm,
-                    int k_smooth, void* ws, cudaStream_t st);
+                    int k_smooth, void* ws, cudaStream_t st, bool clear_status = true);
 int launch_fwd(const void* ws, void* O, float* LSE, float* O32, int B, int H, int N, int D, int causal,
                float sm_scale, cudaStream_t st);
 int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO,

@@ -519,7 +519,7 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(
 }  // namespace
 
 int launch_quantize(const void* Q, const void* K, const void* V, int B, int H, int N, int D, int qk_norm,
-                    int k_smooth, void* ws, cudaStream_t st) {
+                    int k_smooth, void* ws, cudaStream_t st, bool clear_status) {
   const QuantWs L = quant_ws_layout(B, H, N, D);
   uint8_t* w = static_cast<uint8_t*>(ws);
   const int nb = L.np / 128;
@@ -534,8 +534,9 @@ int launch_quantize(const void* Q, const void* K, const void* V, int B, int H, i
   int* status = reinterpret_cast<int*>(w + L.status);
   const size_t stage = (size_t)128 * D * 2;  // one staged token block
   ScopedTimer timer("quantize", st);
-  // the status word and the per-head counters are cleared before the kernels that use them
-  if (cudaMemsetAsync(w + L.status, 0, L.qc - L.status, st) != cudaSuccess) return 3;
+  // the per-head counters (and normally the status word) are cleared before the kernels
+  const size_t clear_from = clear_status ? L.status : L.sync;
+  if (cudaMemsetAsync(w + clear_from, 0, L.qc - clear_from, st) != cudaSuccess) return 3;
   auto stats = D == 128 ? (qk_norm ? kstats_kernel<128, true> : kstats_kernel<128, false>)
                         : (qk_norm ? kstats_kernel<64, true> : kstats_kernel<64, false>);
   auto quant = D == 128 ? (qk_norm ? quantize_kernel<128, true> : quantize_kernel<128, false>)

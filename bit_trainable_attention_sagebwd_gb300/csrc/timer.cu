@@ -17,6 +17,7 @@ struct Rec {
 
 std::mutex g_mu;
 bool g_on = false;
+std::string g_only;  // empty: every group
 std::vector<Rec> g_recs;
 std::vector<cudaEvent_t> g_pool;
 
@@ -36,6 +37,16 @@ cudaEvent_t take_event() {
 bool timer_enabled() {
   std::lock_guard<std::mutex> g(g_mu);
   return g_on;
+}
+
+bool timer_enabled_for(const char* name) {
+  std::lock_guard<std::mutex> g(g_mu);
+  return g_on && (g_only.empty() || g_only == name);
+}
+
+void timer_only(const char* name) {
+  std::lock_guard<std::mutex> g(g_mu);
+  g_only = name ? name : "";
 }
 
 void timer_set(bool on) {

@@ -7,7 +7,11 @@
 namespace sage {
 
 bool timer_enabled();
+// enabled, and `name` passes the filter (timer_only)
+bool timer_enabled_for(const char* name);
 void timer_set(bool on);
+// record only the launch group `name` (nullptr: every group)
+void timer_only(const char* name);
 // record the start event of a timed launch group; returns a handle for timer_stop
 int timer_start(const char* name, cudaStream_t st);
 void timer_stop(int handle, cudaStream_t st);
@@ -18,7 +22,7 @@ int timer_read(const char* name, double* total_ms, int* launches);
 struct ScopedTimer {
   int h;
   cudaStream_t st;
-  ScopedTimer(const char* name, cudaStream_t s) : h(timer_enabled() ? timer_start(name, s) : -1), st(s) {}
+  ScopedTimer(const char* name, cudaStream_t s) : h(timer_enabled_for(name) ? timer_start(name, s) : -1), st(s) {}
   ~ScopedTimer() {
     if (h >= 0) timer_stop(h, st);
   }

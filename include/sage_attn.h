@@ -43,8 +43,8 @@
  *  - Every device-side wait is bounded; a wait that runs out records
  *    SAGE_ERR_TIMEOUT in the workspace status word (read with
  *    sage_attn_get_status) and the kernel returns.
- *  - The forward is deterministic.  dQ is accumulated with fp32 atomics across
- *    key blocks, so its last bits depend on the order of those atomics.
+ *  - The forward is deterministic.  dQ is accumulated with fp32 additions in L2
+ *    (TMA reductions) across key blocks, so its last bits depend on their order.
  */
 #ifndef SAGE_ATTN_H
 #define SAGE_ATTN_H
@@ -171,11 +171,46 @@ int sage_attn_bwd_noalloc(const void *Q, const void *K, const void *V, const voi
                           int N, int D, int causal, int qk_norm, int k_smooth, float sm_scale,
                           void *stream);
 
+/*
+ * One training step of the attention block on HOST-resident tensors: the quantize
+ * pass, the forward and the backward above, with the host<->device copies overlapped
+ * with the computation.  Every pass of the scheme treats heads independently, so the
+ * B*H heads are split into `groups` contiguous ranges (groups <= 0: automatic, at most
+ * 4; at most 64): the inputs of all ranges are copied in on one copy stream, range g
+ * runs on `stream` once its inputs have landed, and its outputs are copied out on a
+ * second copy stream while range g+1 runs.  The results equal those of the three calls
+ * on device tensors.
+ *  - Q, K, V, dO: host bf16 [B, H, N, D] (read).  O, dQ, dK, dV: host bf16 [B, H, N, D]
+ *    and LSE: host fp32 [B, H, N] (written).  Page-locked host memory lets the copies
+ *    run asynchronously; with pageable memory the call is correct but the copies do
+ *    not overlap the computation.
+ *  - dev: device scratch, 256-byte aligned, of sage_attn_step_host_bytes(B, H, N, D,
+ *    groups) bytes (the same `groups`): device copies of the inputs and outputs and
+ *    the workspaces of one head range.  It begins with a quantize workspace whose
+ *    status word collects the errors of every range: read it with
+ *    sage_attn_get_status(dev, stream).
+ *  - Returns once everything is enqueued; the outputs are in host memory when work
+ *    enqueued on `stream` before the next call completes (e.g. after
+ *    cudaStreamSynchronize(stream)).  The library's two copy streams are shared by all
+ *    calls of the process: calls from several host threads at once are not supported.
+ */
+size_t sage_attn_step_host_bytes(int B, int H, int N, int D, int groups);
+int sage_attn_step_host(const void *Q, const void *K, const void *V, const void *dO, void *O, float *LSE,
+                        void *dQ, void *dK, void *dV, void *dev, size_t dev_bytes, int B, int H, int N,
+                        int D, int causal, int qk_norm, int k_smooth, float sm_scale, int groups,
+                        void *stream);
+
 /* Kernel timing for benchmarks.  While enabled (on != 0) the library brackets
  * each launch group with CUDA events recorded on the launching stream: "quantize"
- * (the three quantize kernels), "fwd", "bwd_pre" (D_i, LSE*log2e, dO codes),
+ * (the two quantize kernels), "fwd", "bwd_pre" (D_i, LSE*log2e, dO codes),
  * "bwd_main" and "bwd_dq".  Costs two event records per group; off by default. */
 int sage_attn_timer_enable(int on);
+
+/* Restrict the timing to the launch group `kernel` (one of the names above; NULL:
+ * every group).  An event recorded between two launches orders the second after the
+ * first's completion, so timing every group removes the overlap of each launch with
+ * its predecessor's tail; timing one group keeps it everywhere else. */
+int sage_attn_timer_only(const char *kernel);
 
 /* Synchronise the events recorded for `kernel` since the last read, store their
  * summed duration (ms) and number of launches, and forget them.  Unknown names
