@@ -23,10 +23,27 @@ constexpr int kMaxGroups = 64;
 
 struct StepHostLayout {
   size_t ws, bwd_ws, q, k, v, dO, o, dq, dk, dv, lse, total;
-  int groups, hg;  // head ranges and heads per range (the last range may hold fewer)
+  int groups, hg;              // head ranges and the largest range
+  int start[kMaxGroups + 1];   // range g holds heads [start[g], start[g+1])
 };
 
-int auto_groups(int bh) { return bh < 4 ? bh : 4; }
+int auto_groups(int bh) { return bh < 5 ? bh : 5; }
+
+// Range sizes: with three ranges or more the first and the last take half the share of
+// the others, so the computation starts early and the last copies out are short.
+void split_heads(int bh, int g, int* start) {
+  const double total = g >= 3 ? g - 1.0 : (double)g;
+  double acc = 0.0;
+  start[0] = 0;
+  for (int i = 0; i < g; ++i) {
+    acc += (g >= 3 && (i == 0 || i == g - 1)) ? 0.5 : 1.0;
+    int e = (int)(acc / total * bh + 0.5);
+    if (e < start[i] + 1) e = start[i] + 1;          // every range holds a head
+    if (e > bh - (g - 1 - i)) e = bh - (g - 1 - i);  // ... and leaves one for each later range
+    start[i + 1] = e;
+  }
+  start[g] = bh;
+}
 
 StepHostLayout step_host_layout(int B, int H, int N, int D, int groups) {
   StepHostLayout L{};
@@ -34,8 +51,11 @@ StepHostLayout step_host_layout(int B, int H, int N, int D, int groups) {
   int g = groups > 0 ? groups : auto_groups(bh);
   if (g > bh) g = bh;
   if (g > kMaxGroups) g = kMaxGroups;
-  L.hg = (bh + g - 1) / g;
-  L.groups = (bh + L.hg - 1) / L.hg;
+  L.groups = g;
+  split_heads(bh, g, L.start);
+  L.hg = 0;
+  for (int i = 0; i < g; ++i)
+    if (L.start[i + 1] - L.start[i] > L.hg) L.hg = L.start[i + 1] - L.start[i];
   const size_t t = (size_t)bh * N * D * 2;  // one bf16 [B, H, N, D] tensor
   size_t o = 0;
   L.ws = o;     o = align256(o + quant_ws_layout(1, L.hg, N, D).total);  // first: its status word
@@ -57,7 +77,7 @@ StepHostLayout step_host_layout(int B, int H, int N, int D, int groups) {
 struct CopyEngines {
   int device = -1;
   cudaStream_t h2d = nullptr, d2h = nullptr;
-  std::vector<cudaEvent_t> ev;  // [0] start, [1] end, then in/out per range
+  std::vector<cudaEvent_t> ev;  // [0] start, [1] end, then inputs in / forward done / backward done per range
 };
 
 CopyEngines* copy_engines() {
@@ -69,7 +89,7 @@ CopyEngines* copy_engines() {
     if (cudaStreamCreateWithFlags(&e.h2d, cudaStreamNonBlocking) != cudaSuccess ||
         cudaStreamCreateWithFlags(&e.d2h, cudaStreamNonBlocking) != cudaSuccess)
       return nullptr;
-    e.ev.resize(2 + 2 * kMaxGroups);
+    e.ev.resize(2 + 3 * kMaxGroups);
     for (auto& x : e.ev)
       if (cudaEventCreateWithFlags(&x, cudaEventDisableTiming) != cudaSuccess) return nullptr;
     e.device = dev;
@@ -84,7 +104,6 @@ int launch_step_host(const void* Q, const void* K, const void* V, const void* dO
   CopyEngines* E = copy_engines();
   if (E == nullptr) return 3;
   uint8_t* d = static_cast<uint8_t*>(dev);
-  const int bh = B * H;
   const size_t head = (size_t)N * D * 2, head_lse = (size_t)N * 4;
   const uint8_t* hin[4] = {static_cast<const uint8_t*>(Q), static_cast<const uint8_t*>(K),
                            static_cast<const uint8_t*>(V), static_cast<const uint8_t*>(dO)};
@@ -98,36 +117,40 @@ int launch_step_host(const void* Q, const void* K, const void* V, const void* dO
       cudaStreamWaitEvent(E->d2h, ev_start, 0) != cudaSuccess)
     return 3;
   for (int g = 0; g < L.groups; ++g) {
-    const int h0 = g * L.hg, n = bh - h0 < L.hg ? bh - h0 : L.hg;
+    const int h0 = L.start[g], n = L.start[g + 1] - h0;
     for (int t = 0; t < 4; ++t)
       if (cudaMemcpyAsync(din[t] + h0 * head, hin[t] + h0 * head, n * head, cudaMemcpyHostToDevice, E->h2d) !=
           cudaSuccess)
         return 3;
-    if (cudaEventRecord(E->ev[2 + 2 * g], E->h2d) != cudaSuccess) return 3;
+    if (cudaEventRecord(E->ev[2 + 3 * g], E->h2d) != cudaSuccess) return 3;
   }
   for (int g = 0; g < L.groups; ++g) {
-    const int h0 = g * L.hg, n = bh - h0 < L.hg ? bh - h0 : L.hg;
+    const int h0 = L.start[g], n = L.start[g + 1] - h0;
     const size_t off = h0 * head;
     float* lse = reinterpret_cast<float*>(d + L.lse) + (size_t)h0 * N;
-    if (cudaStreamWaitEvent(st, E->ev[2 + 2 * g], 0) != cudaSuccess) return 3;
+    if (cudaStreamWaitEvent(st, E->ev[2 + 3 * g], 0) != cudaSuccess) return 3;
     // one workspace serves every range in turn; its status word collects their errors
     if (int rc = launch_quantize(din[0] + off, din[1] + off, din[2] + off, 1, n, N, D, qk_norm, k_smooth, d + L.ws,
                                  st, g == 0))
       return rc;
     if (int rc = launch_fwd(d + L.ws, dout[0] + off, lse, nullptr, 1, n, N, D, causal, sm_scale, st)) return rc;
+    // O and LSE go out while the range's backward runs
+    if (cudaEventRecord(E->ev[3 + 3 * g], st) != cudaSuccess ||
+        cudaStreamWaitEvent(E->d2h, E->ev[3 + 3 * g], 0) != cudaSuccess ||
+        cudaMemcpyAsync(hout[0] + off, dout[0] + off, n * head, cudaMemcpyDeviceToHost, E->d2h) != cudaSuccess ||
+        cudaMemcpyAsync(reinterpret_cast<uint8_t*>(LSE) + h0 * head_lse, lse, n * head_lse, cudaMemcpyDeviceToHost,
+                        E->d2h) != cudaSuccess)
+      return 3;
     if (int rc = launch_bwd(din[0] + off, din[1] + off, din[2] + off, dout[0] + off, lse, din[3] + off,
                             dout[1] + off, dout[2] + off, dout[3] + off, d + L.ws, d + L.bwd_ws, 1, n, N, D, causal,
                             qk_norm, k_smooth, sm_scale, st))
       return rc;
-    if (cudaEventRecord(E->ev[3 + 2 * g], st) != cudaSuccess ||
-        cudaStreamWaitEvent(E->d2h, E->ev[3 + 2 * g], 0) != cudaSuccess)
+    if (cudaEventRecord(E->ev[4 + 3 * g], st) != cudaSuccess ||
+        cudaStreamWaitEvent(E->d2h, E->ev[4 + 3 * g], 0) != cudaSuccess)
       return 3;
-    for (int t = 0; t < 4; ++t)
+    for (int t = 1; t < 4; ++t)
       if (cudaMemcpyAsync(hout[t] + off, dout[t] + off, n * head, cudaMemcpyDeviceToHost, E->d2h) != cudaSuccess)
         return 3;
-    if (cudaMemcpyAsync(reinterpret_cast<uint8_t*>(LSE) + h0 * head_lse, lse, n * head_lse, cudaMemcpyDeviceToHost,
-                        E->d2h) != cudaSuccess)
-      return 3;
   }
   // the caller's stream completes once the outputs are in host memory
   if (cudaEventRecord(ev_end, E->d2h) != cudaSuccess || cudaStreamWaitEvent(st, ev_end, 0) != cudaSuccess) return 3;

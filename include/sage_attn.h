@@ -175,8 +175,9 @@ int sage_attn_bwd_noalloc(const void *Q, const void *K, const void *V, const voi
  * One training step of the attention block on HOST-resident tensors: the quantize
  * pass, the forward and the backward above, with the host<->device copies overlapped
  * with the computation.  Every pass of the scheme treats heads independently, so the
- * B*H heads are split into `groups` contiguous ranges (groups <= 0: automatic, at most
- * 4; at most 64): the inputs of all ranges are copied in on one copy stream, range g
+ * B*H heads are split into `groups` contiguous ranges (groups <= 0: automatic, 5 or
+ * fewer; at most 64; with 3 ranges or more the first and last hold half the heads of the
+ * others): the inputs of all ranges are copied in on one copy stream, range g
  * runs on `stream` once its inputs have landed, and its outputs are copied out on a
  * second copy stream while range g+1 runs.  The results equal those of the three calls
  * on device tensors.
