@@ -173,6 +173,7 @@ struct BwdSmem {
 
 struct BwdParams {
   int N, np, nqb, causal, qk_norm;
+  int BH, hgroup;  // heads, and heads per CTA-order group (tile_head_order)
   float alpha, sm_scale;
   const float* sq;
   const float* sk;
@@ -226,7 +227,8 @@ __global__ void __launch_bounds__(384, 1)
   constexpr int DG = D / 2;  // output columns per compute thread
   constexpr int WPROD = 8, WMMA = 9;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int kb = blockIdx.x, bh = blockIdx.y;
+  int kb, bh;  // one CTA per (key block, head)
+  tile_head_order((int)blockIdx.x, prm.nqb, prm.BH, prm.hgroup, kb, bh);
   const int I0 = prm.causal ? kb : 0;
   const int n_it = prm.nqb - I0;
   constexpr uint32_t kCols = 512;
@@ -700,7 +702,7 @@ int launch_main_t(const CUtensorMap& tk, const CUtensorMap& tq, const CUtensorMa
   auto kern = bwd_main_kernel<D>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 3;
   ScopedTimer timer("bwd_main", st);
-  if (launch_pdl(kern, dim3(p.nqb, BH), dim3(384), smem, st, tk, tq, tv, tdo, tdo8, tdq, p) != cudaSuccess) return 3;
+  if (launch_pdl(kern, dim3(p.nqb * BH), dim3(384), smem, st, tk, tq, tv, tdo, tdo8, tdq, p) != cudaSuccess) return 3;
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 
@@ -750,6 +752,8 @@ int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const
   p.N = N;
   p.np = np;
   p.nqb = nb;
+  p.BH = BH;
+  p.hgroup = l2_head_group((size_t)np * D * 5, BH);  // Q codes, dO (bf16 and e4m3) of a head
   p.causal = causal;
   p.qk_norm = qk_norm;
   p.alpha = (float)((double)sm_scale * 1.4426950408889634074);

@@ -50,6 +50,7 @@ struct FwdSmem {
 
 struct FwdParams {
   int N, np, nqb, npairs;
+  int BH, hgroup;  // heads, and heads per CTA-order group (tile_head_order)
   float alpha;  // RN(sm_scale * log2 e)
   // 4096, passed at run time so that the band key stays one integer multiply-add (FMA pipe)
   // instead of a shift and an add on the busier ALU pipe
@@ -380,8 +381,9 @@ __global__ void __launch_bounds__(640, 1)
   extern __shared__ uint8_t smem_raw[];
   FwdSmem<D>& sm = *reinterpret_cast<FwdSmem<D>*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bh = blockIdx.y;
-  const int pc = CAUSAL ? (prm.npairs - 1 - (int)blockIdx.x) : (int)blockIdx.x;
+  int px, bh;  // one CTA per (pair of query blocks, head); causal: the longest pairs first
+  tile_head_order((int)blockIdx.x, prm.npairs, prm.BH, prm.hgroup, px, bh);
+  const int pc = CAUSAL ? (prm.npairs - 1 - px) : px;
   const int qbA = 2 * pc, qbB = 2 * pc + 1;
   const bool hasB = qbB < prm.nqb;
   // KV tiles: tile A needs [0, lastA], tile B [0, lastB]
@@ -519,7 +521,7 @@ int launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
   auto kern = fwd_kernel<D, CAUSAL>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 3;
   ScopedTimer timer("fwd", st);
-  if (launch_pdl(kern, dim3(p.npairs, BH), dim3(640), smem, st, tq, tk, tv, p) != cudaSuccess) return 3;
+  if (launch_pdl(kern, dim3(p.npairs * BH), dim3(640), smem, st, tq, tk, tv, p) != cudaSuccess) return 3;
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 
@@ -539,6 +541,8 @@ int launch_fwd(const void* ws, void* O, float* LSE, float* O32, int B, int H, in
   p.np = np;
   p.nqb = np / 128;
   p.npairs = (p.nqb + 1) / 2;
+  p.BH = BH;
+  p.hgroup = l2_head_group((size_t)p.np * D * 3, BH);  // K codes and V codes of a head
   p.alpha = (float)((double)sm_scale * 1.4426950408889634074);
   p.band_mult = 4096u;
   p.sq = reinterpret_cast<const float*>(w + L.sq);

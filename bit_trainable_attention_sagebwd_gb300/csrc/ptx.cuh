@@ -75,6 +75,29 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// ------------------------------------------------------------ CTA order
+// Linear CTA index -> (tile index t in [0, ntile), head bh).  Heads go in groups of
+// `hgroup` whose per-head operands fit in L2 together; inside a group the tile index is
+// major, so in a causal pass the longest CTAs of the group (t = 0) start first and the
+// short ones fill the tail.
+__device__ __forceinline__ void tile_head_order(int idx, int ntile, int BH, int hgroup, int& t, int& bh) {
+  const int s = idx / (ntile * hgroup);
+  const int h0 = s * hgroup;
+  const int r = idx - h0 * ntile;
+  const int gs = BH - h0 < hgroup ? BH - h0 : hgroup;
+  t = r / gs;
+  bh = h0 + r % gs;
+}
+
+// heads per group for tile_head_order: as many as keep `bytes_per_head` within ~96 MB of L2
+inline int l2_head_group(size_t bytes_per_head, int BH) {
+  const size_t budget = (size_t)96 << 20;
+  size_t g = bytes_per_head > 0 ? budget / bytes_per_head : (size_t)BH;
+  if (g < 1) g = 1;
+  if (g > (size_t)BH) g = BH;
+  return (int)g;
+}
+
 // ------------------------------------------------ programmatic dependent launch
 // Kernels of one pass follow each other on a stream with programmatic serialization:
 // the next kernel's CTAs may start while this one drains.  Each kernel waits for its
