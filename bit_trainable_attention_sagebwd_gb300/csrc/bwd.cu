@@ -351,22 +351,18 @@ __global__ void __launch_bounds__(384, 1)
           umma_f8(tmem + cDV, sdesc_sw128(a_p + kk * 4096, 16384, 1024), sdesc_sw128(a_do8 + kk * 32, 16, 1024),
                   id_dv, (it > 0 || kk > 0));
         umma_commit(&sm.bar_do8_free);
-        // dQ of keys [0,64) once group 0's codes are in: [q, d] = sum_key dS[q, key] K[key, d]
-        if (!mbar_wait(&sm.bar_ds[0], ph, abort)) break;
+        // dK first, once both groups' codes are in, so its readout starts as early as possible
+        if (!mbar_wait(&sm.bar_ds[0], ph, abort) || !mbar_wait(&sm.bar_ds[1], ph, abort)) break;
         tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma_bf16(tmem + cDQ0, sdesc_sw128(a_ds + kk * 32, 16, 1024), sdesc_sw128(a_k + kk * 2048, 16384, 1024),
-                    id_dq, kk > 0);
-        if (!mbar_wait(&sm.bar_ds[1], ph, abort)) break;
-        tc_fence_after();
-        // dK_part[key, d] = sum_q dS[q, key] Q[q, d]
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           umma_bf16(tmem + cS, sdesc_sw128(a_ds + kk * 2048, 16384, 1024), sdesc_sw128(a_q + kk * 2048, 16384, 1024),
                     id_dk, kk > 0);
         umma_commit(&sm.bar_dk);
-        // dQ of keys [64,128), into the dP columns (both groups have read dP by now)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16(tmem + cDQ0, sdesc_sw128(a_ds + kk * 32, 16, 1024), sdesc_sw128(a_k + kk * 2048, 16384, 1024),
+                    id_dq, kk > 0);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           umma_bf16(tmem + cDQ1, sdesc_sw128(a_ds + 16384 + kk * 32, 16, 1024),

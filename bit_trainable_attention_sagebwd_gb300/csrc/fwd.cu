@@ -493,8 +493,10 @@ __global__ void __launch_bounds__(640, 1)
             break;
           }
           tc_fence_after();
-          issue_pv(X, j, j == 0);
+          // the tile's next S first: its softmax waits for it, while PV only has to be done
+          // before that softmax rescales O (the S columns are free: P went to shared memory)
           if (j + 1 <= last) issue_s(X, j + 1);
+          issue_pv(X, j, j == 0);
         }
         if (!ok) break;
         umma_commit(&sm.bar_v_empty[j % kVStages]);
