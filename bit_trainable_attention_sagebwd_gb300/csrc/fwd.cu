@@ -43,7 +43,7 @@ struct FwdSmem {
   uint64_t bar_q;
   uint64_t bar_k_full[kKStages], bar_k_empty[kKStages];
   uint64_t bar_v_full[kVStages], bar_v_empty[kVStages];
-  uint64_t bar_s_full[2], bar_p_full[2], bar_o_done[2];
+  uint64_t bar_s_full[2], bar_s_free[2], bar_p_full[2], bar_o_done[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -262,6 +262,11 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
         uint32_t sv[32];
         tmem_ld32(s_col + 32 * q, sv);
         tmem_wait32(sv);
+        if (q == 1) {
+          // every S value of this half is in registers: the tile's next S may overwrite them
+          tc_fence_before();
+          mbar_arrive(&sm.bar_s_free[X]);
+        }
         if (masked_tile) mask_chunk(sv, lim - hh * 64 - 32 * q);
         uint32_t band[2] = {~0u, ~0u};  // smallest band keys of the chunk's codes
         uint32_t w[8];
@@ -404,6 +409,7 @@ __global__ void __launch_bounds__(640, 1)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&sm.bar_s_full[x], 1);
+      mbar_init(&sm.bar_s_free[x], 256);
       mbar_init(&sm.bar_p_full[x], 256);
       mbar_init(&sm.bar_o_done[x], 1);
     }
@@ -485,6 +491,19 @@ __global__ void __launch_bounds__(640, 1)
         const bool nextk = j + 1 < n_kv;
         if (nextk && !mbar_wait(&sm.bar_k_full[(j + 1) % kKStages], ((j + 1) / kKStages) & 1, abort)) break;
         if (!mbar_wait(&sm.bar_v_full[j % kVStages], (j / kVStages) & 1, abort)) break;
+        // the next S of a tile as soon as its softmax has read this S into registers (halfway
+        // through its exp pass), then the PVs once the P codes are in shared memory
+        for (int X = 0; X < 2; ++X) {
+          const int last = X == 0 ? lastA : lastB;
+          if (j + 1 > last) continue;
+          if (!mbar_wait(&sm.bar_s_free[X], j & 1, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_s(X, j + 1);
+        }
+        if (!ok) break;
         for (int X = 0; X < 2; ++X) {
           const int last = X == 0 ? lastA : lastB;
           if (j > last) continue;
@@ -493,9 +512,6 @@ __global__ void __launch_bounds__(640, 1)
             break;
           }
           tc_fence_after();
-          // the tile's next S first: its softmax waits for it, while PV only has to be done
-          // before that softmax rescales O (the S columns are free: P went to shared memory)
-          if (j + 1 <= last) issue_s(X, j + 1);
           issue_pv(X, j, j == 0);
         }
         if (!ok) break;
