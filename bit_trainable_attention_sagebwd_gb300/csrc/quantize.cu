@@ -131,8 +131,8 @@ __device__ __forceinline__ void two_sum2(uint64_t a, uint64_t b, uint64_t& s, ui
 
 // ---------------------------------------------------------------------------
 // ---------------------------------------------------------------------------
-// kstats: per (head, 128-token block): blockIdx.z = 0: partial channel maxima of |V|;
-// blockIdx.z = 1 (with smoothing only): partial fp64 column sums of k'.  The last block
+// kstats: per (head, 128-token block): partial fp64 column sums of k' (with smoothing only:
+// blockIdx.z = 0) and partial channel maxima of |V| (the last z).  The last block
 // of a head to finish (a counter per head and tensor, zeroed before the launch) combines
 // the partials: the V channel scales max|V| / 448, and the smoothing mean as the fp32
 // rounding of (sum over the head's tokens) / N (0 without smoothing).
@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(kThreads) kstats_kernel(const __nv_bfloat16* _
   constexpr int TPR = D / 8, RPP = kThreads / TPR, PASSES = 128 / RPP;
   constexpr int J = kThreads / D;  // threads per channel in the combine
   const int blk = blockIdx.x, bh = blockIdx.y, nb = gridDim.x;
-  const bool isk = blockIdx.z == 1;
+  const bool isk = gridDim.z == 2 && blockIdx.z == 0;  // keys first (with smoothing), then values
   const int tid = threadIdx.x, g = tid % TPR, ro = tid / TPR;
   const int rows = min(128, N - blk * 128);
   extern __shared__ __align__(128) uint8_t stage_buf[];
@@ -308,9 +308,9 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(
     uint8_t* __restrict__ v8t, float* __restrict__ sq, float* __restrict__ sk, float* __restrict__ qr,
     float* __restrict__ kr, int* __restrict__ status) {
   constexpr int TPR = D / 8, RPP = kThreads / TPR, PASSES = 128 / RPP;
-  // grid z runs K, V, then Q: the keys and values the statistics pass has just read are
-  // re-read while they are still in L2
-  const int which = blockIdx.z == 2 ? 0 : (int)blockIdx.z + 1;
+  // grid z runs V, K, then Q: kstats reads K first, then V, so the values it read last are
+  // re-read first, then the keys, while they are still in L2
+  const int which = blockIdx.z == 2 ? 0 : 2 - (int)blockIdx.z;
   const int blk = blockIdx.x, bh = blockIdx.y, nb = gridDim.x, np = nb * 128;
   const int tid = threadIdx.x, g = tid % TPR, ro = tid / TPR, warp = tid >> 5, lane = tid & 31;
   const size_t phead = (size_t)bh * np * D;

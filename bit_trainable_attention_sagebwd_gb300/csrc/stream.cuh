@@ -47,7 +47,6 @@ struct StreamCtl {
   uint64_t full[NS];
   int item[NS];  // item held by each stage (>= nitems: none)
   int abort;
-  int flag;      // scratch word for block-uniform decisions of the item bodies
 };
 
 // Runs body(item, stage) on every item this CTA claims, with all threads of the CTA.
