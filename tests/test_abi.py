@@ -74,3 +74,36 @@ def test_ws_views_offsets(lib):
     ptrs = [v.status, v.qc, v.kc, v.v8t, v.sq, v.sk, v.sv, v.kmean, v.qr, v.kr]
     assert ptrs == sorted(ptrs) and all((p - base) % 256 == 0 for p in ptrs)
     assert v.kc - v.qc >= 6 * 384 * 128 * 2
+
+
+def test_step_host_sizes_and_argument_errors(lib):
+    """Scratch of the host-tensor step: inputs and outputs of the whole batch plus the
+    workspaces of the largest head range; smaller ranges need less; bad arguments are
+    refused before any CUDA call."""
+    B, H, N, D = 4, 16, 2048, 128
+    t = B * H * N * D * 2
+    sizes = {g: sa.sage_attn_step_host_bytes(B, H, N, D, g) for g in (1, 2, 5, 8, 64)}
+    for g, n in sizes.items():
+        assert n >= 8 * t + B * H * N * 4 and n % 256 == 0
+    assert sizes[1] > sizes[2] > sizes[5] > sizes[8] > sizes[64]
+    assert sa.sage_attn_step_host_bytes(B, H, N, D, 0) == sizes[5]  # automatic: five ranges
+    assert sa.sage_attn_step_host_bytes(1, 1, 128, 96, 0) == 0
+    n = sizes[5]
+    null = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(0x10000)
+    host = [fake] * 9
+    assert sa.sage_attn_step_host(*host, null, n, B, H, N, D, 1, 0, 1, 0.0, 0, null) == sa.SAGE_ERR_INVALID_ARG
+    assert sa.sage_attn_step_host(*host, ctypes.c_void_p(0x10010), n, B, H, N, D, 1, 0, 1, 0.0, 0,
+                                  null) == sa.SAGE_ERR_INVALID_ARG  # scratch not 256-byte aligned
+    assert sa.sage_attn_step_host(*host, fake, n - 256, B, H, N, D, 1, 0, 1, 0.0, 0, null) == sa.SAGE_ERR_INVALID_ARG
+    assert sa.sage_attn_step_host(*host, fake, n, B, H, N, D, 1, 0, 1, float("inf"), 0,
+                                  null) == sa.SAGE_ERR_INVALID_ARG
+    assert sa.sage_attn_step_host(*host, fake, n, B, H, N, 96, 1, 0, 1, 0.0, 0, null) == sa.SAGE_ERR_UNSUPPORTED
+    host[4] = null  # no O buffer
+    assert sa.sage_attn_step_host(*host, fake, n, B, H, N, D, 1, 0, 1, 0.0, 0, null) == sa.SAGE_ERR_INVALID_ARG
+
+
+def test_timer_filter_needs_no_gpu(lib):
+    assert sa.sage_attn_timer_only("bwd_main") == sa.SAGE_OK
+    assert sa.sage_attn_timer_only(None) == sa.SAGE_OK
+    assert sa.sage_attn_timer_read("bwd_main") == (0.0, 0)

@@ -45,12 +45,3 @@ def test_step_host_matches_device_calls(w, groups):
     rel = float((out["dq"].float() - ref).norm() / ref.norm())
     assert rel < 1e-5, rel
 
-
-def test_step_host_rejects_bad_arguments():
-    import bit_trainable_attention_sagebwd_gb300 as sa
-    n = sa.sage_attn_step_host_bytes(1, 2, 256, 128, 0)
-    assert n > 0
-    assert sa.sage_attn_step_host_bytes(1, 2, 256, 96, 0) == 0
-    rc = sa.sage_attn_step_host(None, None, None, None, None, None, None, None, None, None, n, 1, 2, 256, 128,
-                                1, 0, 1, 0.0, 0, None)
-    assert rc == sa.SAGE_ERR_INVALID_ARG
