@@ -9,9 +9,10 @@
 //
 // Kernels (all on the caller's stream):
 //   bwd_pre    per (head, 128-query block): D_i = sum_d dO*O, log2(448) - LSE*log2(e)
-//              (-inf on padded rows), partial channel maxima of |dO|, zeroed dQ accumulator
+//              (-inf on padded rows), partial channel maxima of |dO|
 //   bwd_docomb per head: dO channel scales max|dO|/448
-//   bwd_do8    per (head, 128-query block): e4m3 codes of dO, channel-major
+//   bwd_do8    per (head, 128-query block): e4m3 codes of dO, channel-major; zeroed dQ
+//              accumulator
 //   bwd_main   per (head, 128-key block), looping over query blocks:
 //                S  = Q8 K8^T          kind::f16 (bf16-held INT8 codes, exact)
 //                dP = dO V^T           kind::f16 (bf16)
@@ -106,11 +107,6 @@ __global__ void __launch_bounds__(kPreThreads) bwd_pre_kernel(const __nv_bfloat1
           t < N ? kLog2_448 - (float)((double)LSE[(size_t)bh * N + t] * 1.4426950408889634074) : -INFINITY;
     }
   }
-  // zero this block's columns of the feature-major dQ accumulator [bh][d][token]
-  for (int idx = tid; idx < D * 32; idx += kPreThreads) {
-    const int d = idx >> 5, c = idx & 31;
-    reinterpret_cast<float4*>(dqacc + ((size_t)bh * D + d) * np + blk * 128)[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
   __shared__ float s_max[RPP][D];
 #pragma unroll
   for (int i = 0; i < 8; ++i) s_max[ro][g * 8 + i] = am[i];
@@ -133,13 +129,17 @@ __global__ void bwd_docomb_kernel(const float* __restrict__ dopart, int D, int n
 }
 
 // e4m3 codes of one 128-query block of dO with the head's channel scales, written
-// channel-major [BH, D, Np]; the rows are read straight from global memory
+// channel-major [BH, D, Np]; the rows are read straight from global memory.  The block's
+// columns of the dQ accumulator are zeroed here rather than in bwd_pre, whose dO reads then
+// stay in L2 for this kernel.
 template <int D>
 __global__ void __launch_bounds__(kPreThreads, 4) bwd_do8_kernel(const __nv_bfloat16* __restrict__ dO, int N,
                                                                const float* __restrict__ sdo,
-                                                               uint8_t* __restrict__ do8t) {
+                                                               uint8_t* __restrict__ do8t, float* __restrict__ dqacc) {
   constexpr int TPR = D / 8;
-  const int blk = blockIdx.x, bh = blockIdx.y, np = gridDim.x * 128;
+  const int tid = threadIdx.x;
+  // blocks in the reverse order of bwd_pre: the dO blocks it read last are re-read first
+  const int blk = gridDim.x - 1 - blockIdx.x, bh = gridDim.y - 1 - blockIdx.y, np = gridDim.x * 128;
   const int rows = min(128, N - blk * 128);
   __shared__ __align__(16) uint8_t s8[D * 128];
   const uint4* src = reinterpret_cast<const uint4*>(dO + ((size_t)bh * N + (size_t)blk * 128) * D);
@@ -148,6 +148,11 @@ __global__ void __launch_bounds__(kPreThreads, 4) bwd_do8_kernel(const __nv_bflo
   e4m3_block_codes<D, kPreThreads>(
       [&](int t, int g) { return t < rows ? __ldg(src + t * TPR + g) : make_uint4(0, 0, 0, 0); },
       sdo + (size_t)bh * D, s8, do8t + (size_t)bh * D * np + blk * 128, np);
+  // zero this block's columns of the feature-major dQ accumulator [bh][d][token]
+  for (int idx = tid; idx < D * 32; idx += kPreThreads) {
+    const int d = idx >> 5, c = idx & 31;
+    reinterpret_cast<float4*>(dqacc + ((size_t)bh * D + d) * np + blk * 128)[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
 }
 
 // ------------------------------------------------------------------ bwd_main
@@ -729,7 +734,7 @@ int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const
                  dvec, biasv, dopart, dqacc, ticket) != cudaSuccess ||
       launch_pdl(bwd_docomb_kernel, dim3(BH), dim3(128), 0, st, (const float*)dopart, D, nb, sdo) != cudaSuccess ||
       launch_pdl(D == 128 ? bwd_do8_kernel<128> : bwd_do8_kernel<64>, g, dim3(kPreThreads), 0, st, dob, N,
-                 (const float*)sdo, do8t) != cudaSuccess)
+                 (const float*)sdo, do8t, dqacc) != cudaSuccess)
     return 3;
   }
   if (cudaGetLastError() != cudaSuccess) return 3;
