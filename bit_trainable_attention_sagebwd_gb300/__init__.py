@@ -25,7 +25,7 @@ ABI_FUNCTIONS = ("sage_attn_ws_bytes", "sage_attn_bwd_ws_bytes", "sage_attn_quan
                  "sage_attn_bwd", "sage_attn_ws_views", "sage_attn_get_status", "sage_attn_selftest_wait",
                  "sage_attn_status_str", "sage_attn_timer_enable", "sage_attn_timer_read",
                  "sage_attn_bwd_noalloc", "sage_attn_step_host_bytes", "sage_attn_step_host",
-                 "sage_attn_timer_only")
+                 "sage_attn_timer_only", "sage_attn_bwd_o32")
 
 
 class SageError(RuntimeError):
@@ -61,6 +61,7 @@ def lib():
             L.sage_attn_quantize.argtypes = [vp, vp, vp, i, i, i, i, i, i, vp, sz, vp]
             L.sage_attn_fwd.argtypes = [vp, vp, vp, vp, i, i, i, i, i, fp, vp]
             L.sage_attn_bwd.argtypes = [vp] * 11 + [sz] + [i] * 7 + [fp, vp]
+            L.sage_attn_bwd_o32.argtypes = [vp] * 11 + [sz] + [i] * 7 + [fp, vp]
             L.sage_attn_ws_views.argtypes = [vp, i, i, i, i, ctypes.POINTER(sage_ws_views)]
             L.sage_attn_get_status.argtypes = [vp, vp]
             L.sage_attn_selftest_wait.argtypes = [vp, u64, vp]
@@ -100,6 +101,12 @@ def sage_attn_bwd(Q, K, V, O, LSE, dO, dQ, dK, dV, ws, bwd_ws, bwd_ws_bytes, B, 
                   k_smooth, sm_scale, stream):
     return lib().sage_attn_bwd(Q, K, V, O, LSE, dO, dQ, dK, dV, ws, bwd_ws, bwd_ws_bytes, B, H, N, D,
                                int(causal), int(qk_norm), int(k_smooth), float(sm_scale), stream)
+
+
+def sage_attn_bwd_o32(Q, K, V, O32, LSE, dO, dQ, dK, dV, ws, bwd_ws, bwd_ws_bytes, B, H, N, D, causal, qk_norm,
+                      k_smooth, sm_scale, stream):
+    return lib().sage_attn_bwd_o32(Q, K, V, O32, LSE, dO, dQ, dK, dV, ws, bwd_ws, bwd_ws_bytes, B, H, N, D,
+                                   int(causal), int(qk_norm), int(k_smooth), float(sm_scale), stream)
 
 
 def sage_attn_bwd_noalloc(Q, K, V, O, LSE, dO, dQ, dK, dV, ws, B, H, N, D, causal, qk_norm, k_smooth, sm_scale,
@@ -223,8 +230,9 @@ def forward(ws, B, H, N, D, causal, sm_scale=None, o=None, lse=None, o32=False, 
 
 
 def backward(q, k, v, o, lse, do, ws, causal, qk_norm=False, k_smooth=True, sm_scale=None, bwd_ws=None,
-             dq=None, dk=None, dv=None, stream=None):
-    """Backward; returns (dQ, dK, dV) bf16."""
+             dq=None, dk=None, dv=None, stream=None, o32=None):
+    """Backward; returns (dQ, dK, dV) bf16.  With o32 (the forward's fp32 output) the row
+    terms D_i take it instead of the bf16 o (sage_attn_bwd_o32)."""
     import torch
     B, H, N, D = _shape(q)
     if sm_scale is None:
@@ -234,6 +242,12 @@ def backward(q, k, v, o, lse, do, ws, causal, qk_norm=False, k_smooth=True, sm_s
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    if o32 is not None:
+        _check("sage_attn_bwd_o32",
+               sage_attn_bwd_o32(_ptr(q), _ptr(k), _ptr(v), _ptr(o32), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk),
+                                 _ptr(dv), _ptr(ws), _ptr(bwd_ws), bwd_ws.numel(), B, H, N, D, causal, qk_norm,
+                                 k_smooth, sm_scale, _stream_ptr(stream)))
+        return dq, dk, dv
     _check("sage_attn_bwd", sage_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq),
                                           _ptr(dk), _ptr(dv), _ptr(ws), _ptr(bwd_ws), bwd_ws.numel(), B, H, N,
                                           D, causal, qk_norm, k_smooth, sm_scale, _stream_ptr(stream)))

@@ -90,6 +90,22 @@ int sage_attn_bwd(const void* Q, const void* K, const void* V, const void* O, co
                           k_smooth != 0, resolve_scale(sm_scale, D), static_cast<cudaStream_t>(stream));
 }
 
+int sage_attn_bwd_o32(const void* Q, const void* K, const void* V, const float* O32, const float* LSE,
+                      const void* dO, void* dQ, void* dK, void* dV, const void* ws, void* bwd_ws, size_t bwd_ws_bytes,
+                      int B, int H, int N, int D, int causal, int qk_norm, int k_smooth, float sm_scale,
+                      void* stream) {
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O32) || !aligned16(dO) || !aligned16(dQ) ||
+      !aligned16(dK) || !aligned16(dV) || !aligned16(ws) || !aligned16(bwd_ws) || LSE == nullptr ||
+      ((uintptr_t)LSE & 3u))
+    return SAGE_ERR_INVALID_ARG;
+  if (!(sm_scale == sm_scale) || isinf(sm_scale)) return SAGE_ERR_INVALID_ARG;
+  if (!shape_ok(B, H, N, D)) return SAGE_ERR_UNSUPPORTED;
+  if (bwd_ws_bytes < sage::bwd_ws_layout(B, H, N, D).total) return SAGE_ERR_INVALID_ARG;
+  return sage::launch_bwd(Q, K, V, nullptr, LSE, dO, dQ, dK, dV, ws, bwd_ws, B, H, N, D, causal != 0,
+                          qk_norm != 0, k_smooth != 0, resolve_scale(sm_scale, D), static_cast<cudaStream_t>(stream),
+                          O32);
+}
+
 int sage_attn_ws_views(void* ws, int B, int H, int N, int D, sage_ws_views* v) {
   if (ws == nullptr || v == nullptr) return SAGE_ERR_INVALID_ARG;
   if (!shape_ok(B, H, N, D)) return SAGE_ERR_UNSUPPORTED;

@@ -63,8 +63,11 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
 }
 
 // ------------------------------------------------------------------ bwd_pre
+// O32 (fp32, the forward's output before its bf16 rounding) replaces O in D_i when it is not
+// null: the high-precision auxiliary output of the Attn-QAT backward
 template <int D>
 __global__ void __launch_bounds__(kPreThreads) bwd_pre_kernel(const __nv_bfloat16* __restrict__ O,
+                                                               const float* __restrict__ O32,
                                                                const __nv_bfloat16* __restrict__ dO,
                                                                const float* __restrict__ LSE, int N,
                                                                float* __restrict__ dvec, float* __restrict__ bias,
@@ -84,12 +87,23 @@ __global__ void __launch_bounds__(kPreThreads) bwd_pre_kernel(const __nv_bfloat1
   for (int p = 0; p < PASSES; ++p) {
     const int r = p * RPP + ro, t = blk * 128 + r;
     uint4 uo = make_uint4(0, 0, 0, 0), ud = make_uint4(0, 0, 0, 0);
+    float4 oa = make_float4(0.f, 0.f, 0.f, 0.f), ob = oa;
     if (t < N) {
-      uo = __ldg(reinterpret_cast<const uint4*>(O + head + (size_t)t * D) + g);
+      if (O32) {
+        const float4* o32 = reinterpret_cast<const float4*>(O32 + head + (size_t)t * D) + 2 * g;
+        oa = __ldg(o32);
+        ob = __ldg(o32 + 1);
+      } else {
+        uo = __ldg(reinterpret_cast<const uint4*>(O + head + (size_t)t * D) + g);
+      }
       ud = __ldg(reinterpret_cast<const uint4*>(dO + head + (size_t)t * D) + g);
     }
     float o[8], d[8];
-    unpack8(uo, o);
+    if (O32) {
+      o[0] = oa.x, o[1] = oa.y, o[2] = oa.z, o[3] = oa.w, o[4] = ob.x, o[5] = ob.y, o[6] = ob.z, o[7] = ob.w;
+    } else {
+      unpack8(uo, o);
+    }
     unpack8(ud, d);
     float s = 0.f;
 #pragma unroll
@@ -711,7 +725,7 @@ int launch_main_t(const CUtensorMap& tk, const CUtensorMap& tq, const CUtensorMa
 
 int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO,
                void* dQ, void* dK, void* dV, const void* ws, void* bwd_ws, int B, int H, int N, int D, int causal,
-               int qk_norm, int k_smooth, float sm_scale, cudaStream_t st) {
+               int qk_norm, int k_smooth, float sm_scale, cudaStream_t st, const float* O32) {
   (void)k_smooth;  // the smoothing Jacobian is applied as the identity (dS rows sum to zero)
   const QuantWs QL = quant_ws_layout(B, H, N, D);
   const BwdWs BL = bwd_ws_layout(B, H, N, D);
@@ -730,7 +744,7 @@ int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const
   const dim3 g(nb, BH);
   {
   ScopedTimer timer("bwd_pre", st);
-  if (launch_pdl(D == 128 ? bwd_pre_kernel<128> : bwd_pre_kernel<64>, g, dim3(kPreThreads), 0, st, o, dob, LSE, N,
+  if (launch_pdl(D == 128 ? bwd_pre_kernel<128> : bwd_pre_kernel<64>, g, dim3(kPreThreads), 0, st, o, O32, dob, LSE, N,
                  dvec, biasv, dopart, dqacc, ticket) != cudaSuccess ||
       launch_pdl(bwd_docomb_kernel, dim3(BH), dim3(128), 0, st, (const float*)dopart, D, nb, sdo) != cudaSuccess ||
       launch_pdl(D == 128 ? bwd_do8_kernel<128> : bwd_do8_kernel<64>, g, dim3(kPreThreads), 0, st, dob, N,

@@ -132,6 +132,19 @@ int sage_attn_bwd(const void *Q, const void *K, const void *V, const void *O, co
                   size_t bwd_ws_bytes, int B, int H, int N, int D, int causal, int qk_norm,
                   int k_smooth, float sm_scale, void *stream);
 
+/*
+ * Backward with the high-precision auxiliary output ("Attn-QAT: 4-Bit Attention With
+ * Quantization-Aware Training" (gist.science summary), Methodology, principle 2): the same
+ * as sage_attn_bwd, except that the row terms D_i = sum_d dO_id O'_id take O' = O32, the
+ * forward's fp32 output before its bf16 rounding (the O32 output of sage_attn_fwd), instead
+ * of the bf16 O.  O32: fp32 [B, H, N, D], device memory, 16-byte aligned.  The bf16 O is
+ * not read.  Errors as for sage_attn_bwd.
+ */
+int sage_attn_bwd_o32(const void *Q, const void *K, const void *V, const float *O32, const float *LSE,
+                      const void *dO, void *dQ, void *dK, void *dV, const void *ws, void *bwd_ws,
+                      size_t bwd_ws_bytes, int B, int H, int N, int D, int causal, int qk_norm,
+                      int k_smooth, float sm_scale, void *stream);
+
 /* Fill `views` with the device pointers inside a quantize workspace. */
 int sage_attn_ws_views(void *ws, int B, int H, int N, int D, sage_ws_views *views);
 

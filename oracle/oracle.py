@@ -149,12 +149,15 @@ def backward(qz: dict, v, do, O, LSE, causal, sm_scale, qk_norm, qmask=QM_ALL) -
 
 
 def run_head(q, k, v, do, causal, sm_scale, qk_norm=False, k_smooth=True, qmask=QM_ALL,
-             backward_pass=True) -> dict:
+             backward_pass=True, o_aux="bf16") -> dict:
     """Quantize, forward and (optionally) backward of one head.
 
     In the low-bit scheme (F32 bit on) the backward consumes the forward's bf16 O
     and fp32 LSE, as a training step would; with exact arithmetic it consumes
-    the fp64 values.
+    the fp64 values.  o_aux="fp32" gives the backward the forward's fp32 O instead
+    of the bf16 one for D_i = rowsum(dO * O): the high-precision auxiliary output of
+    "Attn-QAT: 4-Bit Attention With Quantization-Aware Training" (gist.science
+    summary), Methodology, principle 2.
     """
     qz = quantize(q, k, v, qk_norm, k_smooth, qmask)
     fw = forward(qz, causal, sm_scale, qmask)
@@ -162,7 +165,8 @@ def run_head(q, k, v, do, causal, sm_scale, qk_norm=False, k_smooth=True, qmask=
     out.update(fw)
     if backward_pass:
         if qmask & QM_F32:
-            O_used, L_used = fw["Obf"], fw["LSE32"].astype(np.float64)
+            O_used = fw["O32"].astype(np.float64) if o_aux == "fp32" else fw["Obf"]
+            L_used = fw["LSE32"].astype(np.float64)
         else:
             O_used, L_used = fw["O64"], fw["LSE64"]
         out.update(backward(qz, v, do, O_used, L_used, causal, sm_scale, qk_norm, qmask))

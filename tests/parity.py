@@ -28,7 +28,7 @@ def e4m3_decode(u8: torch.Tensor) -> np.ndarray:
     return u8.view(torch.float8_e4m3fn).float().cpu().numpy().astype(np.float64)
 
 
-def run_gpu(w, x: dict, backward=True) -> dict:
+def run_gpu(w, x: dict, backward=True, o32_aux=False) -> dict:
     t = to_dev(x)
     B, H, N, D = w.B, w.H, w.N, w.D
     ws = sa.quantize(t["q"], t["k"], t["v"], w.qk_norm, w.k_smooth)
@@ -36,7 +36,7 @@ def run_gpu(w, x: dict, backward=True) -> dict:
     out = {"ws": ws, "O": o, "LSE": lse, "O32": o32, "in": t}
     if backward:
         dq, dk, dv = sa.backward(t["q"], t["k"], t["v"], o, lse, t["do"], ws, w.causal, w.qk_norm,
-                                 w.k_smooth, w.sm_scale)
+                                 w.k_smooth, w.sm_scale, o32=o32 if o32_aux else None)
         out.update(dQ=dq, dK=dk, dV=dv)
     torch.cuda.synchronize()
     st = sa.get_status(ws)
@@ -96,7 +96,7 @@ def check_backward_head(w, g: dict, bh: int, r: dict) -> dict:
     return out
 
 
-def oracle_head(w, x, bh, backward=True) -> dict:
+def oracle_head(w, x, bh, backward=True, o_aux="bf16", qmask=None) -> dict:
     hx = head_f64(x, w, bh)
     return orc.run_head(hx["q"], hx["k"], hx["v"], hx["do"], w.causal, w.sm_scale, w.qk_norm, w.k_smooth,
-                        qmask=orc.QM_ALL, backward_pass=backward)
+                        qmask=orc.QM_ALL if qmask is None else qmask, backward_pass=backward, o_aux=o_aux)

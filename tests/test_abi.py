@@ -62,6 +62,12 @@ def test_argument_errors_return_before_launch(lib):
     a2 = list(args)
     a2[6] = odd
     assert sa.sage_attn_bwd(*a2[:10], fake, 1 << 40, 1, 1, 128, 64, 1, 0, 1, 0.125, null) == sa.SAGE_ERR_INVALID_ARG
+    # the fp32-auxiliary backward: same checks, O32 in place of O
+    assert sa.sage_attn_bwd_o32(*args[:3], null, *args[4:10], fake, 1 << 40, 1, 1, 128, 64, 1, 0, 1, 0.125,
+                                null) == sa.SAGE_ERR_INVALID_ARG
+    assert sa.sage_attn_bwd_o32(*args[:10], fake, 16, 1, 1, 128, 64, 1, 0, 1, 0.125, null) == sa.SAGE_ERR_INVALID_ARG
+    assert sa.sage_attn_bwd_o32(*args[:10], fake, 1 << 40, 1, 1, 128, 80, 1, 0, 1, 0.125,
+                                null) == sa.SAGE_ERR_UNSUPPORTED
     with pytest.raises(sa.SageError):
         sa.sage_attn_ws_views(fake, 1, 1, 128, 96)
     assert sa.status_str(sa.SAGE_ERR_TIMEOUT) == "device wait timed out"

@@ -357,3 +357,19 @@ def test_full_scheme_error_is_modest():
     assert rel(a["O64"], b["O64"]) < 0.05
     for n in ("dQ64", "dK64", "dV64"):
         assert rel(a[n], b[n]) < 0.1, n
+
+
+def test_fp32_auxiliary_output_feeds_the_row_terms():
+    """o_aux="fp32" ("Attn-QAT" summary, Methodology, principle 2): the backward's row terms
+    are rowsum(dO * O) with the forward's fp32 O instead of its bf16 rounding; dV does not
+    depend on them, dQ and dK do."""
+    rng = np.random.default_rng(27)
+    N, D = 192, 64
+    q, k, v, do = (_rand(rng, N, D) for _ in range(4))
+    a = orc.run_head(q, k, v, do, True, 0.125, False, True)
+    b = orc.run_head(q, k, v, do, True, 0.125, False, True, o_aux="fp32")
+    np.testing.assert_allclose(a["Dvec"], (do * a["Obf"]).sum(1), rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(b["Dvec"], (do * b["O32"].astype(np.float64)).sum(1), rtol=1e-12, atol=1e-14)
+    assert not np.allclose(a["Dvec"], b["Dvec"], rtol=1e-6, atol=0)
+    np.testing.assert_array_equal(a["dV64"], b["dV64"])
+    assert not np.array_equal(a["dQ64"], b["dQ64"]) and not np.array_equal(a["dK64"], b["dK64"])
