@@ -71,6 +71,7 @@ def lib():
             L.sage_oracle_quantize.argtypes = [i, i, dp, dp, dp, i, i, i] + [dp] * 11
             L.sage_oracle_fwd.argtypes = [i, i, i, ctypes.c_double, i] + [dp] * 6 + [dp, fp, dp]
             L.sage_oracle_bwd.argtypes = [i, i, i, ctypes.c_double, i, i] + [dp] * 12 + [dp] * 4
+            L.sage_oracle_bwd_sdo.argtypes = [i, i, i, ctypes.c_double, i, i] + [dp] * 12 + [dp] * 5
             _lib = L
     return _lib
 
@@ -132,16 +133,22 @@ def forward(qz: dict, causal, sm_scale, qmask=QM_ALL) -> dict:
             "LSE32": L.astype(np.float32)}
 
 
-def backward(qz: dict, v, do, O, LSE, causal, sm_scale, qk_norm, qmask=QM_ALL) -> dict:
+def backward(qz: dict, v, do, O, LSE, causal, sm_scale, qk_norm, qmask=QM_ALL, sdo=None) -> dict:
+    """One head's backward; sdo (optional, [D]) gives the e4m3 channel scales of dO instead of
+    taking them from this head's dO (grouped-query attention, see run_group)."""
     v, do, O, LSE = _c64(v), _c64(do), _c64(O), _c64(LSE)
     N, D = v.shape
     dQ, dK, dV = np.zeros((N, D)), np.zeros((N, D)), np.zeros((N, D))
     Dv = np.zeros(N)
-    rc = lib().sage_oracle_bwd(N, D, int(causal), float(sm_scale), int(qk_norm), int(qmask),
-                               _d(v), _d(do), _d(O), _d(LSE),
-                               _d(qz["qx"]), _d(qz["sq"]), _d(qz["kx"]), _d(qz["sk"]),
-                               _d(qz["qn"]), _d(qz["qr"]), _d(qz["kn"]), _d(qz["kr"]),
-                               _d(dQ), _d(dK), _d(dV), _d(Dv))
+    common = (N, D, int(causal), float(sm_scale), int(qk_norm), int(qmask),
+              _d(v), _d(do), _d(O), _d(LSE),
+              _d(qz["qx"]), _d(qz["sq"]), _d(qz["kx"]), _d(qz["sk"]),
+              _d(qz["qn"]), _d(qz["qr"]), _d(qz["kn"]), _d(qz["kr"]))
+    if sdo is None:
+        rc = lib().sage_oracle_bwd(*common, _d(dQ), _d(dK), _d(dV), _d(Dv))
+    else:
+        sdo = _c64(sdo)
+        rc = lib().sage_oracle_bwd_sdo(*common, _d(sdo), _d(dQ), _d(dK), _d(dV), _d(Dv))
     if rc:
         raise RuntimeError(f"oracle backward failed ({rc})")
     return {"dQ64": dQ, "dK64": dK, "dV64": dV, "dQbf": to_bf16(dQ), "dKbf": to_bf16(dK),
@@ -171,3 +178,39 @@ def run_head(q, k, v, do, causal, sm_scale, qk_norm=False, k_smooth=True, qmask=
             O_used, L_used = fw["O64"], fw["LSE64"]
         out.update(backward(qz, v, do, O_used, L_used, causal, sm_scale, qk_norm, qmask))
     return out
+
+
+def run_group(qs, k, v, dos, causal, sm_scale, qk_norm=False, k_smooth=True, qmask=QM_ALL) -> dict:
+    """Grouped-query attention: the G query heads qs[g] (with upstream gradients dos[g])
+    share the key/value head k, v.  Each query head is quantized (Q block scales of its
+    own; K and V codes, the same for every head of the group), run forward and backward
+    as one head, except that the e4m3 channel scale of dO spans the group's tokens: dV of
+    the shared head sums P^T dO over all of them, so one scale per channel keeps that sum
+    a single FP8 accumulation.  dK and dV of the shared head are the sums over the group.
+    Returns {"heads": [run_head-like dicts], "dK64", "dV64", "dKbf", "dVbf", "sdo"}.
+    """
+    qs = [_c64(q) for q in qs]
+    dos = [_c64(d) for d in dos]
+    N, D = _c64(v).shape
+    if qmask & QM_DO:
+        a = np.max(np.abs(np.stack(dos)), axis=(0, 1))  # per channel over the group's tokens
+        s = (a / 448.0).astype(np.float32).astype(np.float64) if qmask & QM_F32 else a / 448.0
+        sdo = np.where(a > 0.0, s, 0.0)
+    else:
+        sdo = np.ones(D)
+    heads = []
+    dK, dV = np.zeros((N, D)), np.zeros((N, D))
+    for q, do in zip(qs, dos):
+        qz = quantize(q, k, v, qk_norm, k_smooth, qmask)
+        fw = forward(qz, causal, sm_scale, qmask)
+        out = dict(qz)
+        out.update(fw)
+        if qmask & QM_F32:
+            O_used, L_used = fw["Obf"], fw["LSE32"].astype(np.float64)
+        else:
+            O_used, L_used = fw["O64"], fw["LSE64"]
+        out.update(backward(qz, v, do, O_used, L_used, causal, sm_scale, qk_norm, qmask, sdo=sdo))
+        heads.append(out)
+        dK += out["dK64"]
+        dV += out["dV64"]
+    return {"heads": heads, "dK64": dK, "dV64": dV, "dKbf": to_bf16(dK), "dVbf": to_bf16(dV), "sdo": sdo}

@@ -367,11 +367,43 @@ static void l2_normalise_grad(double *g, const double *xn, const double *r, int 
  * rows sum to zero, so the smoothed-K gradient already has zero token mean.
  * Outputs dQ, dK, dV [N, D] and Dvec [N] in fp64.
  */
+static int bwd_head(int N, int D, int causal, double sm_scale, int qk_norm, int qmask,
+                    const double *V, const double *dO, const double *O, const double *LSE,
+                    const double *qx, const double *sq, const double *kx, const double *sk,
+                    const double *qn, const double *qr, const double *kn, const double *kr,
+                    const double *sdo_in, double *dQ, double *dK, double *dV, double *Dvec);
+
 int sage_oracle_bwd(int N, int D, int causal, double sm_scale, int qk_norm, int qmask,
                     const double *V, const double *dO, const double *O, const double *LSE,
                     const double *qx, const double *sq, const double *kx, const double *sk,
                     const double *qn, const double *qr, const double *kn, const double *kr,
                     double *dQ, double *dK, double *dV, double *Dvec)
+{
+    return bwd_head(N, D, causal, sm_scale, qk_norm, qmask, V, dO, O, LSE, qx, sq, kx, sk, qn, qr, kn, kr,
+                    NULL, dQ, dK, dV, Dvec);
+}
+
+/*
+ * The same backward with the channel scales of dO given (sdo_in[D]) instead of taken
+ * from this head's dO.  Grouped-query attention: the query heads that share one
+ * key/value head put their dO tokens on one axis for dV = sum_i P_ij dO_i, so its
+ * e4m3 channel scale spans all of them (the caller computes it as for one head).
+ */
+int sage_oracle_bwd_sdo(int N, int D, int causal, double sm_scale, int qk_norm, int qmask,
+                        const double *V, const double *dO, const double *O, const double *LSE,
+                        const double *qx, const double *sq, const double *kx, const double *sk,
+                        const double *qn, const double *qr, const double *kn, const double *kr,
+                        const double *sdo_in, double *dQ, double *dK, double *dV, double *Dvec)
+{
+    return bwd_head(N, D, causal, sm_scale, qk_norm, qmask, V, dO, O, LSE, qx, sq, kx, sk, qn, qr, kn, kr,
+                    sdo_in, dQ, dK, dV, Dvec);
+}
+
+static int bwd_head(int N, int D, int causal, double sm_scale, int qk_norm, int qmask,
+                    const double *V, const double *dO, const double *O, const double *LSE,
+                    const double *qx, const double *sq, const double *kx, const double *sk,
+                    const double *qn, const double *qr, const double *kn, const double *kr,
+                    const double *sdo_in, double *dQ, double *dK, double *dV, double *Dvec)
 {
     if (N < 0 || D <= 0) return 1;
     int f32 = (qmask & QM_F32) != 0;
@@ -388,7 +420,18 @@ int sage_oracle_bwd(int N, int D, int causal, double sm_scale, int qk_norm, int 
         Dvec[i] = s;
         lse2[i] = r32(f32, LSE[i] * LOG2E);
     }
-    channel_e4m3(dO, N, D, (qmask & QM_DO) != 0, f32, do8, sdo);
+    if (sdo_in && (qmask & QM_DO)) {
+        /* e4m3(x / s) with the given channel scale, as channel_e4m3 forms it */
+        for (int d = 0; d < D; ++d) {
+            sdo[d] = sdo_in[d];
+            for (int t = 0; t < N; ++t) {
+                size_t i = (size_t)t * D + d;
+                do8[i] = sdo[d] > 0.0 ? sage_oracle_e4m3(r32(f32, dO[i] / sdo[d])) : 0.0;
+            }
+        }
+    } else {
+        channel_e4m3(dO, N, D, (qmask & QM_DO) != 0, f32, do8, sdo);
+    }
     memset(dQ, 0, sizeof(double) * E);
     memset(dK, 0, sizeof(double) * E);
     memset(dV, 0, sizeof(double) * E);

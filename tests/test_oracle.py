@@ -373,3 +373,45 @@ def test_fp32_auxiliary_output_feeds_the_row_terms():
     assert not np.allclose(a["Dvec"], b["Dvec"], rtol=1e-6, atol=0)
     np.testing.assert_array_equal(a["dV64"], b["dV64"])
     assert not np.array_equal(a["dQ64"], b["dQ64"]) and not np.array_equal(a["dK64"], b["dK64"])
+
+
+# ---------------------------------------------------------------- grouped-query attention
+
+@pytest.mark.parametrize("causal,qk_norm", [(True, False), (False, True)])
+def test_group_exact_mode_matches_library_attention(causal, qk_norm):
+    """Exact arithmetic: G query heads on one key/value head equal torch attention with the
+    key/value head repeated, and dK, dV are the sums of the per-head gradients."""
+    rng = np.random.default_rng(40)
+    G, N, D = 3, 160, 64
+    qs = [_rand(rng, N, D) for _ in range(G)]
+    dos = [_rand(rng, N, D) for _ in range(G)]
+    k, v = _rand(rng, N, D), _rand(rng, N, D)
+    r = orc.run_group(qs, k, v, dos, causal, 0.2, qk_norm, True, qmask=0)
+    dK, dV = np.zeros((N, D)), np.zeros((N, D))
+    for g in range(G):
+        O, lse, dq, dk, dv = ref_grads(qs[g], k, v, dos[g], causal, 0.2, qk_norm, True)
+        np.testing.assert_allclose(r["heads"][g]["O64"], O, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(r["heads"][g]["dQ64"], dq, rtol=0, atol=1e-10)
+        dK += dk
+        dV += dv
+    np.testing.assert_allclose(r["dK64"], dK, rtol=0, atol=1e-10)
+    np.testing.assert_allclose(r["dV64"], dV, rtol=0, atol=1e-10)
+
+
+def test_group_do_scale_spans_the_group():
+    """In the low-bit scheme the group's dO channel scale is max |dO| over all of its heads'
+    tokens / 448 (fp32): with one head the group is that head, and a head with larger dO
+    sets the scale of the others."""
+    rng = np.random.default_rng(41)
+    N, D = 128, 64
+    q, k, v, do = (_rand(rng, N, D) for _ in range(4))
+    one = orc.run_group([q], k, v, [do], True, 0.125)
+    single = orc.run_head(q, k, v, do, True, 0.125)
+    for n in ("dQ64", "dK64", "dV64"):
+        np.testing.assert_array_equal(one["heads"][0][n], single[n])
+    np.testing.assert_array_equal(one["dV64"], single["dV64"])
+    big = 8.0 * do
+    two = orc.run_group([q, q], k, v, [do, big], True, 0.125)
+    np.testing.assert_array_equal(two["sdo"], (np.abs(big).max(0) / 448.0).astype(np.float32).astype(np.float64))
+    # the first head's dO is coded with the larger scale: its dV differs from the lone head's
+    assert not np.array_equal(two["heads"][0]["dV64"], single["dV64"])
