@@ -25,7 +25,9 @@ ABI_FUNCTIONS = ("sage_attn_ws_bytes", "sage_attn_bwd_ws_bytes", "sage_attn_quan
                  "sage_attn_bwd", "sage_attn_ws_views", "sage_attn_get_status", "sage_attn_selftest_wait",
                  "sage_attn_status_str", "sage_attn_timer_enable", "sage_attn_timer_read",
                  "sage_attn_bwd_noalloc", "sage_attn_step_host_bytes", "sage_attn_step_host",
-                 "sage_attn_timer_only", "sage_attn_bwd_o32")
+                 "sage_attn_timer_only", "sage_attn_bwd_o32", "sage_attn_gqa_ws_bytes",
+                 "sage_attn_gqa_bwd_ws_bytes", "sage_attn_gqa_quantize", "sage_attn_gqa_fwd", "sage_attn_gqa_bwd",
+                 "sage_attn_gqa_ws_views")
 
 
 class SageError(RuntimeError):
@@ -62,6 +64,14 @@ def lib():
             L.sage_attn_fwd.argtypes = [vp, vp, vp, vp, i, i, i, i, i, fp, vp]
             L.sage_attn_bwd.argtypes = [vp] * 11 + [sz] + [i] * 7 + [fp, vp]
             L.sage_attn_bwd_o32.argtypes = [vp] * 11 + [sz] + [i] * 7 + [fp, vp]
+            L.sage_attn_gqa_ws_bytes.restype = sz
+            L.sage_attn_gqa_ws_bytes.argtypes = [i] * 5
+            L.sage_attn_gqa_bwd_ws_bytes.restype = sz
+            L.sage_attn_gqa_bwd_ws_bytes.argtypes = [i] * 5
+            L.sage_attn_gqa_quantize.argtypes = [vp, vp, vp] + [i] * 7 + [vp, sz, vp]
+            L.sage_attn_gqa_fwd.argtypes = [vp, vp, vp, vp] + [i] * 6 + [fp, vp]
+            L.sage_attn_gqa_bwd.argtypes = [vp] * 11 + [sz] + [i] * 8 + [fp, vp]
+            L.sage_attn_gqa_ws_views.argtypes = [vp] + [i] * 5 + [ctypes.POINTER(sage_ws_views)]
             L.sage_attn_ws_views.argtypes = [vp, i, i, i, i, ctypes.POINTER(sage_ws_views)]
             L.sage_attn_get_status.argtypes = [vp, vp]
             L.sage_attn_selftest_wait.argtypes = [vp, u64, vp]
@@ -123,6 +133,36 @@ def sage_attn_step_host(Q, K, V, dO, O, LSE, dQ, dK, dV, dev, dev_bytes, B, H, N
                         sm_scale, groups, stream):
     return lib().sage_attn_step_host(Q, K, V, dO, O, LSE, dQ, dK, dV, dev, dev_bytes, B, H, N, D, int(causal),
                                      int(qk_norm), int(k_smooth), float(sm_scale), int(groups), stream)
+
+
+def sage_attn_gqa_ws_bytes(B, H, Hkv, N, D):
+    return lib().sage_attn_gqa_ws_bytes(B, H, Hkv, N, D)
+
+
+def sage_attn_gqa_bwd_ws_bytes(B, H, Hkv, N, D):
+    return lib().sage_attn_gqa_bwd_ws_bytes(B, H, Hkv, N, D)
+
+
+def sage_attn_gqa_quantize(Q, K, V, B, H, Hkv, N, D, qk_norm, k_smooth, ws, ws_bytes, stream):
+    return lib().sage_attn_gqa_quantize(Q, K, V, B, H, Hkv, N, D, int(qk_norm), int(k_smooth), ws, ws_bytes, stream)
+
+
+def sage_attn_gqa_fwd(ws, O, LSE, O32, B, H, Hkv, N, D, causal, sm_scale, stream):
+    return lib().sage_attn_gqa_fwd(ws, O, LSE, O32, B, H, Hkv, N, D, int(causal), float(sm_scale), stream)
+
+
+def sage_attn_gqa_bwd(Q, K, V, O, LSE, dO, dQ, dK, dV, ws, bwd_ws, bwd_ws_bytes, B, H, Hkv, N, D, causal, qk_norm,
+                      k_smooth, sm_scale, stream):
+    return lib().sage_attn_gqa_bwd(Q, K, V, O, LSE, dO, dQ, dK, dV, ws, bwd_ws, bwd_ws_bytes, B, H, Hkv, N, D,
+                                   int(causal), int(qk_norm), int(k_smooth), float(sm_scale), stream)
+
+
+def sage_attn_gqa_ws_views(ws, B, H, Hkv, N, D) -> sage_ws_views:
+    v = sage_ws_views()
+    rc = lib().sage_attn_gqa_ws_views(ws, B, H, Hkv, N, D, ctypes.byref(v))
+    if rc:
+        raise SageError("sage_attn_gqa_ws_views", rc)
+    return v
 
 
 def sage_attn_ws_views(ws, B, H, N, D) -> sage_ws_views:
@@ -188,34 +228,43 @@ def _shape(q):
     return B, H, N, D
 
 
-def alloc_ws(B, H, N, D, device="cuda"):
+def alloc_ws(B, H, N, D, device="cuda", hkv=None):
     import torch
-    n = sage_attn_ws_bytes(B, H, N, D)
+    n = sage_attn_ws_bytes(B, H, N, D) if hkv in (None, H) else sage_attn_gqa_ws_bytes(B, H, hkv, N, D)
     if n == 0:
         raise SageError("sage_attn_ws_bytes", SAGE_ERR_UNSUPPORTED)
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
-def alloc_bwd_ws(B, H, N, D, device="cuda"):
+def alloc_bwd_ws(B, H, N, D, device="cuda", hkv=None):
     import torch
-    n = sage_attn_bwd_ws_bytes(B, H, N, D)
+    n = sage_attn_bwd_ws_bytes(B, H, N, D) if hkv in (None, H) else sage_attn_gqa_bwd_ws_bytes(B, H, hkv, N, D)
     if n == 0:
         raise SageError("sage_attn_bwd_ws_bytes", SAGE_ERR_UNSUPPORTED)
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
 def quantize(q, k, v, qk_norm=False, k_smooth=True, ws=None, stream=None):
-    """Quantize pass on bf16 [B, H, N, D] CUDA tensors; returns the workspace tensor."""
+    """Quantize pass on bf16 [B, H, N, D] CUDA tensors (k, v: [B, Hkv, N, D], Hkv dividing H, for
+    grouped-query attention); returns the workspace tensor."""
     B, H, N, D = _shape(q)
+    hkv = k.shape[1]
     if ws is None:
-        ws = alloc_ws(B, H, N, D, q.device)
-    _check("sage_attn_quantize", sage_attn_quantize(_ptr(q), _ptr(k), _ptr(v), B, H, N, D, qk_norm, k_smooth,
-                                                    _ptr(ws), ws.numel(), _stream_ptr(stream)))
+        ws = alloc_ws(B, H, N, D, q.device, hkv)
+    if hkv == H:
+        _check("sage_attn_quantize", sage_attn_quantize(_ptr(q), _ptr(k), _ptr(v), B, H, N, D, qk_norm, k_smooth,
+                                                        _ptr(ws), ws.numel(), _stream_ptr(stream)))
+    else:
+        _check("sage_attn_gqa_quantize",
+               sage_attn_gqa_quantize(_ptr(q), _ptr(k), _ptr(v), B, H, hkv, N, D, qk_norm, k_smooth, _ptr(ws),
+                                      ws.numel(), _stream_ptr(stream)))
     return ws
 
 
-def forward(ws, B, H, N, D, causal, sm_scale=None, o=None, lse=None, o32=False, device="cuda", stream=None):
-    """Forward from a quantize workspace; returns (O bf16, LSE fp32[, O32 fp32])."""
+def forward(ws, B, H, N, D, causal, sm_scale=None, o=None, lse=None, o32=False, device="cuda", stream=None,
+            hkv=None):
+    """Forward from a quantize workspace; returns (O bf16, LSE fp32[, O32 fp32]).  hkv: key/value
+    heads of a grouped-query workspace."""
     import torch
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
@@ -224,8 +273,12 @@ def forward(ws, B, H, N, D, causal, sm_scale=None, o=None, lse=None, o32=False, 
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
     O32 = torch.empty((B, H, N, D), dtype=torch.float32, device=device) if o32 is True else (o32 or None)
-    _check("sage_attn_fwd", sage_attn_fwd(_ptr(ws), _ptr(o), _ptr(lse), _ptr(O32), B, H, N, D, causal,
-                                          sm_scale, _stream_ptr(stream)))
+    if hkv in (None, H):
+        _check("sage_attn_fwd", sage_attn_fwd(_ptr(ws), _ptr(o), _ptr(lse), _ptr(O32), B, H, N, D, causal,
+                                              sm_scale, _stream_ptr(stream)))
+    else:
+        _check("sage_attn_gqa_fwd", sage_attn_gqa_fwd(_ptr(ws), _ptr(o), _ptr(lse), _ptr(O32), B, H, hkv, N, D,
+                                                      causal, sm_scale, _stream_ptr(stream)))
     return (o, lse, O32) if O32 is not None else (o, lse)
 
 
@@ -235,13 +288,22 @@ def backward(q, k, v, o, lse, do, ws, causal, qk_norm=False, k_smooth=True, sm_s
     terms D_i take it instead of the bf16 o (sage_attn_bwd_o32)."""
     import torch
     B, H, N, D = _shape(q)
+    hkv = k.shape[1]
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
     if bwd_ws is None:
-        bwd_ws = alloc_bwd_ws(B, H, N, D, q.device)
+        bwd_ws = alloc_bwd_ws(B, H, N, D, q.device, hkv)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    if hkv != H:
+        if o32 is not None:
+            raise ValueError("the fp32 auxiliary output is not offered with grouped key/value heads")
+        _check("sage_attn_gqa_bwd",
+               sage_attn_gqa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk),
+                                 _ptr(dv), _ptr(ws), _ptr(bwd_ws), bwd_ws.numel(), B, H, hkv, N, D, causal,
+                                 qk_norm, k_smooth, sm_scale, _stream_ptr(stream)))
+        return dq, dk, dv
     if o32 is not None:
         _check("sage_attn_bwd_o32",
                sage_attn_bwd_o32(_ptr(q), _ptr(k), _ptr(v), _ptr(o32), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk),
@@ -282,13 +344,15 @@ def get_status(ws, stream=None) -> int:
     return sage_attn_get_status(_ptr(ws), _stream_ptr(stream))
 
 
-def ws_tensors(ws, B, H, N, D) -> dict:
-    """Views of a quantize workspace as torch tensors (for inspection and tests)."""
+def ws_tensors(ws, B, H, N, D, hkv=None) -> dict:
+    """Views of a quantize workspace as torch tensors (for inspection and tests); hkv: key/value
+    heads of a grouped-query workspace (K and V sections then hold B*hkv heads)."""
     import torch
-    v = sage_attn_ws_views(_ptr(ws), B, H, N, D)
+    hk = H if hkv is None else hkv
+    v = sage_attn_ws_views(_ptr(ws), B, H, N, D) if hk == H else sage_attn_gqa_ws_views(_ptr(ws), B, H, hk, N, D)
     base = ws.data_ptr()
     np_ = v.n_pad
-    bh = B * H
+    bh, bk = B * H, B * hk
 
     def view(ptr, n_bytes, dtype, shape):
         off = ptr - base
@@ -296,13 +360,13 @@ def ws_tensors(ws, B, H, N, D) -> dict:
 
     return {
         "qc": view(v.qc, bh * np_ * D * 2, torch.bfloat16, (B, H, np_, D)),
-        "kc": view(v.kc, bh * np_ * D * 2, torch.bfloat16, (B, H, np_, D)),
-        "v8t": view(v.v8t, bh * D * np_, torch.uint8, (B, H, D, np_)),
+        "kc": view(v.kc, bk * np_ * D * 2, torch.bfloat16, (B, hk, np_, D)),
+        "v8t": view(v.v8t, bk * D * np_, torch.uint8, (B, hk, D, np_)),
         "sq": view(v.sq, bh * (np_ // 128) * 4, torch.float32, (B, H, np_ // 128)),
-        "sk": view(v.sk, bh * (np_ // 64) * 4, torch.float32, (B, H, np_ // 64)),
-        "sv": view(v.sv, bh * D * 4, torch.float32, (B, H, D)),
-        "kmean": view(v.kmean, bh * D * 4, torch.float32, (B, H, D)),
+        "sk": view(v.sk, bk * (np_ // 64) * 4, torch.float32, (B, hk, np_ // 64)),
+        "sv": view(v.sv, bk * D * 4, torch.float32, (B, hk, D)),
+        "kmean": view(v.kmean, bk * D * 4, torch.float32, (B, hk, D)),
         "qr": view(v.qr, bh * np_ * 4, torch.float32, (B, H, np_)),
-        "kr": view(v.kr, bh * np_ * 4, torch.float32, (B, H, np_)),
+        "kr": view(v.kr, bk * np_ * 4, torch.float32, (B, hk, np_)),
         "n_pad": np_,
     }

@@ -132,14 +132,17 @@ __global__ void __launch_bounds__(kPreThreads) bwd_pre_kernel(const __nv_bfloat1
   }
 }
 
-__global__ void bwd_docomb_kernel(const float* __restrict__ dopart, int D, int nb, float* __restrict__ sdo) {
-  const int bh = blockIdx.x, d = threadIdx.x;
+// per key/value head: the channel maxima of |dO| over the blocks of its `group` query heads
+// (one scale per channel for all of them: dV sums P^T dO over their tokens)
+__global__ void bwd_docomb_kernel(const float* __restrict__ dopart, int D, int nb, int group,
+                                  float* __restrict__ sdo) {
+  const int kvh = blockIdx.x, d = threadIdx.x;
   pdl_wait();
   pdl_trigger();
   if (d >= D) return;
   float m = 0.f;
-  for (int b = 0; b < nb; ++b) m = fmaxf(m, dopart[((size_t)bh * nb + b) * D + d]);
-  sdo[(size_t)bh * D + d] = m > 0.f ? __fdiv_rn(m, 448.0f) : 0.f;
+  for (int b = 0; b < nb * group; ++b) m = fmaxf(m, dopart[((size_t)kvh * group * nb + b) * D + d]);
+  sdo[(size_t)kvh * D + d] = m > 0.f ? __fdiv_rn(m, 448.0f) : 0.f;
 }
 
 // e4m3 codes of one 128-query block of dO with the head's channel scales, written
@@ -148,7 +151,7 @@ __global__ void bwd_docomb_kernel(const float* __restrict__ dopart, int D, int n
 // stay in L2 for this kernel.
 template <int D>
 __global__ void __launch_bounds__(kPreThreads, 4) bwd_do8_kernel(const __nv_bfloat16* __restrict__ dO, int N,
-                                                               const float* __restrict__ sdo,
+                                                               const float* __restrict__ sdo, int group,
                                                                uint8_t* __restrict__ do8t, float* __restrict__ dqacc) {
   constexpr int TPR = D / 8;
   const int tid = threadIdx.x;
@@ -161,7 +164,7 @@ __global__ void __launch_bounds__(kPreThreads, 4) bwd_do8_kernel(const __nv_bflo
   pdl_trigger();
   e4m3_block_codes<D, kPreThreads>(
       [&](int t, int g) { return t < rows ? __ldg(src + t * TPR + g) : make_uint4(0, 0, 0, 0); },
-      sdo + (size_t)bh * D, s8, do8t + (size_t)bh * D * np + blk * 128, np);
+      sdo + (size_t)(bh / group) * D, s8, do8t + (size_t)bh * D * np + blk * 128, np);
   // zero this block's columns of the feature-major dQ accumulator [bh][d][token]
   for (int idx = tid; idx < D * 32; idx += kPreThreads) {
     const int d = idx >> 5, c = idx & 31;
@@ -192,7 +195,8 @@ struct BwdSmem {
 
 struct BwdParams {
   int N, np, nqb, causal, qk_norm;
-  int BH, hgroup;  // heads, and heads per CTA-order group (tile_head_order)
+  int BH, hgroup;  // key/value heads, and heads per CTA-order group (tile_head_order)
+  int group;       // query heads per key/value head (grouped-query attention; 1 otherwise)
   float alpha, sm_scale;
   const float* sq;
   const float* sk;
@@ -246,10 +250,13 @@ __global__ void __launch_bounds__(384, 1)
   constexpr int DG = D / 2;  // output columns per compute thread
   constexpr int WPROD = 8, WMMA = 9;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  int kb, bh;  // one CTA per (key block, head)
+  int kb, bh;  // one CTA per (key block, key/value head)
   tile_head_order((int)blockIdx.x, prm.nqb, prm.BH, prm.hgroup, kb, bh);
   const int I0 = prm.causal ? kb : 0;
-  const int n_it = prm.nqb - I0;
+  // iteration it: query block I0 + it % nq of query head bh * group + it / nq (grouped-query
+  // attention: every query head of the group sees this key block)
+  const int nq = prm.nqb - I0;
+  const int n_it = prm.group * nq;
   constexpr uint32_t kCols = 512;
   constexpr uint32_t cS = 0, cDP = 128, cDV = 256, cDQ0 = 384, cDQ1 = 128;  // TMEM column bases
   constexpr uint32_t kTile = 128 * D * 2;
@@ -308,24 +315,24 @@ __global__ void __launch_bounds__(384, 1)
         tma_load_3d(sm.v + c * 16384, &tm_v, c * 64, kb * 128, bh, &sm.bar_kv);
       }
       for (int it = 0; it < n_it; ++it) {
-        const int I = I0 + it;
+        const int I = I0 + it % nq, qh = bh * prm.group + it / nq;
         if (it > 0 && !mbar_wait(&sm.bar_do_free, (it - 1) & 1, abort)) break;
         mbar_arrive_expect_tx(&sm.bar_do_full, kTile);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sm.dob + c * 16384, &tm_do, c * 64, I * 128, bh, &sm.bar_do_full);
+          tma_load_3d(sm.dob + c * 16384, &tm_do, c * 64, I * 128, qh, &sm.bar_do_full);
         if (it > 0 && !mbar_wait(&sm.bar_do8_free, (it - 1) & 1, abort)) break;
         mbar_arrive_expect_tx(&sm.bar_do8_full, D * 128);
-        tma_load_3d(sm.do8, &tm_do8, I * 128, 0, bh, &sm.bar_do8_full);
+        tma_load_3d(sm.do8, &tm_do8, I * 128, 0, qh, &sm.bar_do8_full);
         const int qs = it & 1;
         if (it > 1 && !mbar_wait(&sm.bar_q_free[qs], ((it >> 1) - 1) & 1, abort)) break;
         mbar_arrive_expect_tx(&sm.bar_q_full[qs], kTile + 1024);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sm.q[qs] + c * 16384, &tm_q, c * 64, I * 128, bh, &sm.bar_q_full[qs]);
+          tma_load_3d(sm.q[qs] + c * 16384, &tm_q, c * 64, I * 128, qh, &sm.bar_q_full[qs]);
         // the query block's bias and D_i rows travel with its Q tile
-        bulk_load(sm.bias[qs], prm.bias + (size_t)bh * prm.np + I * 128, 512, &sm.bar_q_full[qs]);
-        bulk_load(sm.dvec[qs], prm.dvec + (size_t)bh * prm.np + I * 128, 512, &sm.bar_q_full[qs]);
+        bulk_load(sm.bias[qs], prm.bias + (size_t)qh * prm.np + I * 128, 512, &sm.bar_q_full[qs]);
+        bulk_load(sm.dvec[qs], prm.dvec + (size_t)qh * prm.np + I * 128, 512, &sm.bar_q_full[qs]);
       }
     } else if (warp == WMMA && lane == 0) {
       // ---------------- UMMA issuer
@@ -415,13 +422,14 @@ __global__ void __launch_bounds__(384, 1)
     // a wait that times out raises the abort flag; from then on this thread skips its waits
     // but still runs every iteration, so no thread is left behind at a named barrier
     bool ok = true;
-    float sq_next = prm.sq[(size_t)bh * prm.nqb + I0];
+    float sq_next = prm.sq[(size_t)bh * prm.group * prm.nqb + I0];
     for (int it = 0; it < n_it; ++it) {
-      const int I = I0 + it;
+      const int I = I0 + it % nq, qh = bh * prm.group + it / nq;
       const uint32_t ph = it & 1;
       // the query block's scale was fetched an iteration early (global latency off the path)
       const float sqI = sq_next;
-      if (it + 1 < n_it) sq_next = prm.sq[(size_t)bh * prm.nqb + I + 1];
+      if (it + 1 < n_it)
+        sq_next = prm.sq[(size_t)(bh * prm.group + (it + 1) / nq) * prm.nqb + I0 + (it + 1) % nq];
       const int qs = it & 1;
       ok = ok && mbar_wait(&sm.bar_q_full[qs], (it >> 1) & 1, abort);
       // this query row's scalars: P = 2^(S2 - LSE2) is formed as 2^(S2 + bias) / 448
@@ -622,7 +630,7 @@ __global__ void __launch_bounds__(384, 1)
         named_bar_group(g);
         if (t == 0) {
 #pragma unroll
-          for (int b = 0; b < DG / 32; ++b) tma_reduce_add_3d(&tm_dq, slot(b), I * 128, (int)dcol + 32 * b, bh);
+          for (int b = 0; b < DG / 32; ++b) tma_reduce_add_3d(&tm_dq, slot(b), I * 128, (int)dcol + 32 * b, qh);
           bulk_commit();
           pending_qs = qs;
         }
@@ -725,13 +733,14 @@ int launch_main_t(const CUtensorMap& tk, const CUtensorMap& tq, const CUtensorMa
 
 int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO,
                void* dQ, void* dK, void* dV, const void* ws, void* bwd_ws, int B, int H, int N, int D, int causal,
-               int qk_norm, int k_smooth, float sm_scale, cudaStream_t st, const float* O32) {
+               int qk_norm, int k_smooth, float sm_scale, cudaStream_t st, const float* O32, int Hkv) {
   (void)k_smooth;  // the smoothing Jacobian is applied as the identity (dS rows sum to zero)
-  const QuantWs QL = quant_ws_layout(B, H, N, D);
-  const BwdWs BL = bwd_ws_layout(B, H, N, D);
+  const QuantWs QL = quant_ws_layout(B, H, N, D, Hkv);
+  const BwdWs BL = bwd_ws_layout(B, H, N, D, Hkv);
   const uint8_t* w = static_cast<const uint8_t*>(ws);
   uint8_t* bw = static_cast<uint8_t*>(bwd_ws);
-  const int BH = B * H, np = QL.np, nb = np / 128;
+  // BH query heads, BHk key/value heads, `group` query heads per key/value head
+  const int BH = B * H, BHk = B * (Hkv > 0 ? Hkv : H), group = BH / BHk, np = QL.np, nb = np / 128;
   float* dvec = reinterpret_cast<float*>(bw + BL.dvec);
   float* biasv = reinterpret_cast<float*>(bw + BL.bias);
   float* dopart = reinterpret_cast<float*>(bw + BL.dopart);
@@ -746,17 +755,18 @@ int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const
   ScopedTimer timer("bwd_pre", st);
   if (launch_pdl(D == 128 ? bwd_pre_kernel<128> : bwd_pre_kernel<64>, g, dim3(kPreThreads), 0, st, o, O32, dob, LSE, N,
                  dvec, biasv, dopart, dqacc, ticket) != cudaSuccess ||
-      launch_pdl(bwd_docomb_kernel, dim3(BH), dim3(128), 0, st, (const float*)dopart, D, nb, sdo) != cudaSuccess ||
+      launch_pdl(bwd_docomb_kernel, dim3(BHk), dim3(128), 0, st, (const float*)dopart, D, nb, group, sdo) !=
+          cudaSuccess ||
       launch_pdl(D == 128 ? bwd_do8_kernel<128> : bwd_do8_kernel<64>, g, dim3(kPreThreads), 0, st, dob, N,
-                 (const float*)sdo, do8t, dqacc) != cudaSuccess)
+                 (const float*)sdo, group, do8t, dqacc) != cudaSuccess)
     return 3;
   }
   if (cudaGetLastError() != cudaSuccess) return 3;
 
   CUtensorMap tk, tq, tv, tdo, tdo8;
-  if (!make_tmap_3d(&tk, w + QL.kc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, np, BH, 64, 128)) return 3;
+  if (!make_tmap_3d(&tk, w + QL.kc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, np, BHk, 64, 128)) return 3;
   if (!make_tmap_3d(&tq, w + QL.qc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, np, BH, 64, 128)) return 3;
-  if (!make_tmap_3d(&tv, V, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, N, BH, 64, 128)) return 3;
+  if (!make_tmap_3d(&tv, V, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, N, BHk, 64, 128)) return 3;
   if (!make_tmap_3d(&tdo, dO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, N, BH, 64, 128)) return 3;
   if (!make_tmap_3d(&tdo8, do8t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, np, D, BH, 128, D)) return 3;
   // dQ accumulator [BH][D][np] fp32, boxes of 32 features x 128 queries, unswizzled
@@ -767,8 +777,10 @@ int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const
   p.N = N;
   p.np = np;
   p.nqb = nb;
-  p.BH = BH;
-  p.hgroup = l2_head_group((size_t)np * D * 5, BH);  // Q codes, dO (bf16 and e4m3) of a head
+  p.BH = BHk;  // one CTA per (key block, key/value head)
+  p.group = group;
+  // Q codes, dO (bf16 and e4m3) of the query heads of a key/value head
+  p.hgroup = l2_head_group((size_t)np * D * 5 * group, BHk);
   p.causal = causal;
   p.qk_norm = qk_norm;
   p.alpha = (float)((double)sm_scale * 1.4426950408889634074);
@@ -783,12 +795,12 @@ int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const
   p.dK = static_cast<__nv_bfloat16*>(dK);
   p.dV = static_cast<__nv_bfloat16*>(dV);
   p.status = reinterpret_cast<int*>(const_cast<uint8_t*>(w) + QL.status);
-  int rc = D == 128 ? launch_main_t<128>(tk, tq, tv, tdo, tdo8, tdq, p, BH, st)
-                    : launch_main_t<64>(tk, tq, tv, tdo, tdo8, tdq, p, BH, st);
+  int rc = D == 128 ? launch_main_t<128>(tk, tq, tv, tdo, tdo8, tdq, p, BHk, st)
+                    : launch_main_t<64>(tk, tq, tv, tdo, tdo8, tdq, p, BHk, st);
   if (rc) return rc;
   ScopedTimer timer("bwd_dq", st);
   return launch_bwd_dq(Q, reinterpret_cast<const float*>(w + QL.qr), bwd_ws, dQ, B, H, N, D, qk_norm, sm_scale,
-                       p.status, st);
+                       p.status, st, Hkv);
 }
 
 }  // namespace sage

@@ -110,8 +110,8 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_kernel(const __grid_consta
 }  // namespace
 
 int launch_bwd_dq(const void* Q, const float* qr, void* bwd_ws, void* dQ, int B, int H, int N, int D, int qk_norm,
-                  float sm_scale, int* status, cudaStream_t st) {
-  const BwdWs L = bwd_ws_layout(B, H, N, D);
+                  float sm_scale, int* status, cudaStream_t st, int Hkv) {
+  const BwdWs L = bwd_ws_layout(B, H, N, D, Hkv);
   uint8_t* bw = static_cast<uint8_t*>(bwd_ws);
   const int BH = B * H;
   CUtensorMap tacc;

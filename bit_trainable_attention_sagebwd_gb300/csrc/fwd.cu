@@ -51,6 +51,7 @@ struct FwdSmem {
 struct FwdParams {
   int N, np, nqb, npairs;
   int BH, hgroup;  // heads, and heads per CTA-order group (tile_head_order)
+  int group;       // query heads per key/value head (grouped-query attention; 1 otherwise)
   float alpha;  // RN(sm_scale * log2 e)
   // 4096, passed at run time so that the band key stays one integer multiply-add (FMA pipe)
   // instead of a shift and an add on the busier ALU pipe
@@ -203,7 +204,8 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
   const uint32_t o_col = tmem + lane_base + 256u + (uint32_t)(X * D + hh * DH);
   const int n_tiles = CAUSAL ? qb + 1 : prm.nqb;
   const float s_q = prm.sq[(size_t)bh * prm.nqb + qb];
-  const float* skh = prm.sk + (size_t)bh * prm.nqb * 2 + hh;  // this half's K block scale
+  const int kvh = bh / prm.group;  // the key/value head of this query head
+  const float* skh = prm.sk + (size_t)kvh * prm.nqb * 2 + hh;  // this half's K block scale
   uint8_t* prow = sm.p[X] + (t >> 3) * 1024 + (t & 7) * 128;
   float m = -INFINITY, l = 0.f;  // l: this half's share of the row sum
   // a wait that runs out raises the abort flag; from then on this thread skips its waits but
@@ -342,7 +344,7 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
     const float inv_l = 1.0f / l;
     const bool live = row < prm.N;
     const size_t obase = ((size_t)bh * prm.N + row) * D + hh * DH;
-    const float* svh = prm.sv + (size_t)bh * D + hh * DH;
+    const float* svh = prm.sv + (size_t)kvh * D + hh * DH;
 #pragma unroll 1
     for (int c = 0; c < DH; c += 32) {
       uint32_t o[32];
@@ -450,11 +452,11 @@ __global__ void __launch_bounds__(640, 1)
         mbar_arrive_expect_tx(&sm.bar_k_full[s], 128 * D * 2);
   #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sm.k[s] + c * 16384, &tm_k, c * 64, j * 128, bh, &sm.bar_k_full[s]);
+          tma_load_3d(sm.k[s] + c * 16384, &tm_k, c * 64, j * 128, bh / prm.group, &sm.bar_k_full[s]);
         const int vs = j % kVStages;
         if (j >= kVStages && !mbar_wait(&sm.bar_v_empty[vs], ((j / kVStages) - 1) & 1, abort)) break;
         mbar_arrive_expect_tx(&sm.bar_v_full[vs], D * 128);
-        tma_load_3d(sm.v[vs], &tm_v, j * 128, 0, bh, &sm.bar_v_full[vs]);
+        tma_load_3d(sm.v[vs], &tm_v, j * 128, 0, bh / prm.group, &sm.bar_v_full[vs]);
       }
     } else if (warp == 17 && lane == 0) {
       // ---------------- UMMA issuer
@@ -546,21 +548,23 @@ int launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
 }  // namespace
 
 int launch_fwd(const void* ws, void* O, float* LSE, float* O32, int B, int H, int N, int D, int causal,
-               float sm_scale, cudaStream_t st) {
-  const QuantWs L = quant_ws_layout(B, H, N, D);
+               float sm_scale, cudaStream_t st, int Hkv) {
+  const QuantWs L = quant_ws_layout(B, H, N, D, Hkv);
   const uint8_t* w = static_cast<const uint8_t*>(ws);
-  const int BH = B * H, np = L.np;
+  const int BH = B * H, BHk = B * (Hkv > 0 ? Hkv : H), np = L.np;
   CUtensorMap tq, tk, tv;
   if (!make_tmap_3d(&tq, w + L.qc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, np, BH, 64, 128)) return 3;
-  if (!make_tmap_3d(&tk, w + L.kc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, np, BH, 64, 128)) return 3;
-  if (!make_tmap_3d(&tv, w + L.v8t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, np, D, BH, 128, D)) return 3;
+  if (!make_tmap_3d(&tk, w + L.kc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, np, BHk, 64, 128)) return 3;
+  if (!make_tmap_3d(&tv, w + L.v8t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, np, D, BHk, 128, D)) return 3;
   FwdParams p;
   p.N = N;
   p.np = np;
   p.nqb = np / 128;
   p.npairs = (p.nqb + 1) / 2;
   p.BH = BH;
-  p.hgroup = l2_head_group((size_t)p.np * D * 3, BH);  // K codes and V codes of a head
+  p.group = BH / BHk;
+  // K codes and V codes of a head (shared by a group of query heads, which are adjacent)
+  p.hgroup = l2_head_group((size_t)p.np * D * 3 / p.group, BH);
   p.alpha = (float)((double)sm_scale * 1.4426950408889634074);
   p.band_mult = 4096u;
   p.sq = reinterpret_cast<const float*>(w + L.sq);

@@ -17,26 +17,28 @@ struct QuantWs {
 };
 
 // quantize workspace: codes and scales the forward and backward read, and the
-// per-128-token partial sums that the smoothing mean and the V scales come from
-inline QuantWs quant_ws_layout(int B, int H, int N, int D) {
+// per-128-token partial sums that the smoothing mean and the V scales come from.
+// Hkv key/value heads per batch entry (Hkv divides H; 0 means Hkv = H): the Q sections hold
+// B*H heads, the K and V sections B*Hkv.
+inline QuantWs quant_ws_layout(int B, int H, int N, int D, int Hkv = 0) {
   QuantWs L{};
-  const size_t bh = (size_t)B * H;
+  const size_t bh = (size_t)B * H, bk = (size_t)B * (Hkv > 0 ? Hkv : H);
   const int np = pad128(N);
   const size_t nb = np / 128;
   size_t o = 0;
   L.status = o; o = align256(o + 256);
-  L.sync = o;   o = align256(o + 2 * bh * 4);  // per-head counters of finished statistics blocks
+  L.sync = o;   o = align256(o + 2 * bk * 4);  // per-head counters of finished statistics blocks
   L.qc = o;     o = align256(o + bh * np * D * 2);
-  L.kc = o;     o = align256(o + bh * np * D * 2);
-  L.v8t = o;    o = align256(o + bh * D * np);
+  L.kc = o;     o = align256(o + bk * np * D * 2);
+  L.v8t = o;    o = align256(o + bk * D * np);
   L.sq = o;     o = align256(o + bh * nb * 4);
-  L.sk = o;     o = align256(o + bh * nb * 2 * 4);
-  L.sv = o;     o = align256(o + bh * D * 4);
-  L.kmean = o;  o = align256(o + bh * D * 4);
+  L.sk = o;     o = align256(o + bk * nb * 2 * 4);
+  L.sv = o;     o = align256(o + bk * D * 4);
+  L.kmean = o;  o = align256(o + bk * D * 4);
   L.qr = o;     o = align256(o + bh * np * 4);
-  L.kr = o;     o = align256(o + bh * np * 4);
-  L.kpart = o;  o = align256(o + bh * nb * D * 8);  // fp64 partial column sums of k'
-  L.vpart = o;  o = align256(o + bh * nb * D * 4);  // partial channel max |V|
+  L.kr = o;     o = align256(o + bk * np * 4);
+  L.kpart = o;  o = align256(o + bk * nb * D * 8);  // fp64 partial column sums of k'
+  L.vpart = o;  o = align256(o + bk * nb * D * 4);  // partial channel max |V|
   L.total = o;
   L.np = np;
   return L;
@@ -48,11 +50,12 @@ struct BwdWs {
 };
 
 // backward scratch: the dQ pass's work ticket, D_i, log2(448) - LSE*log2(e) (-inf on padded rows), FP8 dO codes
-// (channel-major), their channel scales and partial maxima, fp32 dQ accumulator
-// (feature-major [BH, D, Np] so that reductions from query rows coalesce)
-inline BwdWs bwd_ws_layout(int B, int H, int N, int D) {
+// (channel-major), their channel scales (one set per key/value head: the query heads that
+// share it share the scale) and partial maxima, fp32 dQ accumulator (feature-major
+// [BH, D, Np] so that reductions from query rows coalesce)
+inline BwdWs bwd_ws_layout(int B, int H, int N, int D, int Hkv = 0) {
   BwdWs L{};
-  const size_t bh = (size_t)B * H;
+  const size_t bh = (size_t)B * H, bk = (size_t)B * (Hkv > 0 ? Hkv : H);
   const int np = pad128(N);
   const size_t nb = np / 128;
   size_t o = 0;
@@ -60,7 +63,7 @@ inline BwdWs bwd_ws_layout(int B, int H, int N, int D) {
   L.dvec = o;   o = align256(o + bh * np * 4);
   L.bias = o;   o = align256(o + bh * np * 4);
   L.do8t = o;   o = align256(o + bh * D * np);
-  L.sdo = o;    o = align256(o + bh * D * 4);
+  L.sdo = o;    o = align256(o + bk * D * 4);
   L.dopart = o; o = align256(o + bh * nb * D * 4);
   L.dqacc = o;  o = align256(o + bh * np * D * 4);
   L.total = o;

@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(
     const __nv_bfloat16* __restrict__ V, int N, int k_smooth, const float* __restrict__ kmean,
     const float* __restrict__ sv, __nv_bfloat16* __restrict__ qc, __nv_bfloat16* __restrict__ kc,
     uint8_t* __restrict__ v8t, float* __restrict__ sq, float* __restrict__ sk, float* __restrict__ qr,
-    float* __restrict__ kr, int* __restrict__ status) {
+    float* __restrict__ kr, int* __restrict__ status, int bhk) {
   constexpr int TPR = D / 8, RPP = kThreads / TPR, PASSES = 128 / RPP;
   // grid z runs V, K, then Q: kstats reads K first, then V, so the values it read last are
   // re-read first, then the keys, while they are still in L2
@@ -322,6 +322,9 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(
   // permuted by (d / 8) so the byte stores of one warp fall in distinct banks
   __shared__ __align__(16) uint8_t s_v8[D][128];
 
+  // grid y spans the query heads; key/value blocks of heads past bhk (grouped-query
+  // attention: fewer key/value heads) have nothing to do
+  if (which != 0 && bh >= bhk) return;
   const __nv_bfloat16* src = (which == 0 ? Q : (which == 1 ? K : V)) + (size_t)bh * N * D + (size_t)blk * 128 * D;
   if (!stage_block(st, stage_buf, src, (uint32_t)rows * D * 2, status)) return;
   pdl_wait();  // the scales and the mean come from kstats
@@ -519,8 +522,9 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(
 }  // namespace
 
 int launch_quantize(const void* Q, const void* K, const void* V, int B, int H, int N, int D, int qk_norm,
-                    int k_smooth, void* ws, cudaStream_t st, bool clear_status) {
-  const QuantWs L = quant_ws_layout(B, H, N, D);
+                    int k_smooth, void* ws, cudaStream_t st, bool clear_status, int Hkv) {
+  const QuantWs L = quant_ws_layout(B, H, N, D, Hkv);
+  const int BHk = B * (Hkv > 0 ? Hkv : H);
   uint8_t* w = static_cast<uint8_t*>(ws);
   const int nb = L.np / 128;
   const dim3 qgrid(nb, B * H, 3);
@@ -545,13 +549,13 @@ int launch_quantize(const void* Q, const void* K, const void* V, int B, int H, i
       cudaFuncSetAttribute(quant, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)stage) != cudaSuccess)
     return 3;
   int* cnt = reinterpret_cast<int*>(w + L.sync);
-  if (launch_pdl(stats, dim3(nb, B * H, k_smooth ? 2 : 1), dim3(kThreads), stage, st, k, v, N, k_smooth, kpart, vpart,
+  if (launch_pdl(stats, dim3(nb, BHk, k_smooth ? 2 : 1), dim3(kThreads), stage, st, k, v, N, k_smooth, kpart, vpart,
                  cnt, kmean, sv, status) != cudaSuccess)
     return 3;
   if (launch_pdl(quant, qgrid, dim3(kThreads), stage, st, q, k, v, N, k_smooth, (const float*)kmean, (const float*)sv,
                  reinterpret_cast<__nv_bfloat16*>(w + L.qc), reinterpret_cast<__nv_bfloat16*>(w + L.kc), w + L.v8t,
                  reinterpret_cast<float*>(w + L.sq), reinterpret_cast<float*>(w + L.sk),
-                 reinterpret_cast<float*>(w + L.qr), reinterpret_cast<float*>(w + L.kr), status) != cudaSuccess)
+                 reinterpret_cast<float*>(w + L.qr), reinterpret_cast<float*>(w + L.kr), status, BHk) != cudaSuccess)
     return 3;
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }

@@ -145,6 +145,35 @@ int sage_attn_bwd_o32(const void *Q, const void *K, const void *V, const float *
                       size_t bwd_ws_bytes, int B, int H, int N, int D, int causal, int qk_norm,
                       int k_smooth, float sm_scale, void *stream);
 
+/*
+ * Grouped-query attention: Hkv key/value heads per batch entry, each shared by G = H / Hkv
+ * consecutive query heads (query head h reads key/value head h / G; Hkv = 1 is multi-query
+ * attention).  The pages leave grouped heads unvalidated ("SageBwd: A Trainable Low-bit
+ * Attention" (euno.news summary), Limitations); these calls extend the scheme as follows.
+ *  - K, V, dK, dV are bf16 [B, Hkv, N, D]; Q, O, dO, dQ bf16 [B, H, N, D]; LSE [B, H, N].
+ *  - Quantize: Q per query head as above; K (smoothing mean, block scales) and V (channel
+ *    scales) per key/value head.
+ *  - Forward: each query head against its key/value head, exactly as above.
+ *  - Backward: dK and dV of a key/value head sum over its G query heads.  The e4m3 channel
+ *    scale of dO spans the G query heads' tokens (one scale per key/value head and channel),
+ *    so dV stays one FP8 accumulation over all of them.
+ * With Hkv = H every call equals its counterpart above.  Hkv must divide H
+ * (else SAGE_ERR_UNSUPPORTED).
+ */
+size_t sage_attn_gqa_ws_bytes(int B, int H, int Hkv, int N, int D);
+size_t sage_attn_gqa_bwd_ws_bytes(int B, int H, int Hkv, int N, int D);
+int sage_attn_gqa_quantize(const void *Q, const void *K, const void *V, int B, int H, int Hkv, int N, int D,
+                           int qk_norm, int k_smooth, void *ws, size_t ws_bytes, void *stream);
+int sage_attn_gqa_fwd(const void *ws, void *O, float *LSE, float *O32, int B, int H, int Hkv, int N, int D,
+                      int causal, float sm_scale, void *stream);
+int sage_attn_gqa_bwd(const void *Q, const void *K, const void *V, const void *O, const float *LSE,
+                      const void *dO, void *dQ, void *dK, void *dV, const void *ws, void *bwd_ws,
+                      size_t bwd_ws_bytes, int B, int H, int Hkv, int N, int D, int causal, int qk_norm,
+                      int k_smooth, float sm_scale, void *stream);
+/* Workspace views for the grouped layout: qc, sq, qr hold B*H heads; kc, v8t, sk, sv,
+ * kmean, kr hold B*Hkv. */
+int sage_attn_gqa_ws_views(void *ws, int B, int H, int Hkv, int N, int D, sage_ws_views *views);
+
 /* Fill `views` with the device pointers inside a quantize workspace. */
 int sage_attn_ws_views(void *ws, int B, int H, int N, int D, sage_ws_views *views);
 
