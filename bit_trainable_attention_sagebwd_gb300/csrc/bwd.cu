@@ -219,7 +219,9 @@ __device__ __forceinline__ void named_bar_group(int g) {
 
 constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23: x + M - M rounds x to an integer (ties to even)
 
-// One CTA per (head, 128-key block), looping over the query blocks that see it.
+// One CTA per (key/value head, 128-key block), looping over the query blocks that see it: of
+// every query head of the group that shares the key/value head (one query head without
+// grouped-query attention).
 //   warps 0-7 : two compute warpgroups.  In the P and dS phases thread t of group g owns query
 //               row t (TMEM lane t of S and dP) and the keys of K block g (columns [64g, 64g+64)):
 //               the row's LSE and D_i are then scalars, and each group's dS tile (128 queries x
