@@ -316,8 +316,9 @@ __global__ void __launch_bounds__(384, 1)
         tma_load_3d(sm.k + c * 16384, &tm_k, c * 64, kb * 128, bh, &sm.bar_kv);
         tma_load_3d(sm.v + c * 16384, &tm_v, c * 64, kb * 128, bh, &sm.bar_kv);
       }
-      for (int it = 0; it < n_it; ++it) {
-        const int I = I0 + it % nq, qh = bh * prm.group + it / nq;
+      // (query block I, query head qh) of iteration it, advanced without a division
+      for (int it = 0, I = I0, qh = bh * prm.group; it < n_it; ++it, I = I + 1 < prm.nqb ? I + 1 : I0,
+               qh = I == I0 ? qh + 1 : qh) {
         if (it > 0 && !mbar_wait(&sm.bar_do_free, (it - 1) & 1, abort)) break;
         mbar_arrive_expect_tx(&sm.bar_do_full, kTile);
 #pragma unroll
@@ -425,13 +426,14 @@ __global__ void __launch_bounds__(384, 1)
     // but still runs every iteration, so no thread is left behind at a named barrier
     bool ok = true;
     float sq_next = prm.sq[(size_t)bh * prm.group * prm.nqb + I0];
+    // (query block I, query head qh) of iteration it, and of the next, advanced without a division
+    int I = I0, qh = bh * prm.group;
+    int In = I0 + 1 < prm.nqb ? I0 + 1 : I0, qhn = I0 + 1 < prm.nqb ? qh : qh + 1;
     for (int it = 0; it < n_it; ++it) {
-      const int I = I0 + it % nq, qh = bh * prm.group + it / nq;
       const uint32_t ph = it & 1;
       // the query block's scale was fetched an iteration early (global latency off the path)
       const float sqI = sq_next;
-      if (it + 1 < n_it)
-        sq_next = prm.sq[(size_t)(bh * prm.group + (it + 1) / nq) * prm.nqb + I0 + (it + 1) % nq];
+      if (it + 1 < n_it) sq_next = prm.sq[(size_t)qhn * prm.nqb + In];
       const int qs = it & 1;
       ok = ok && mbar_wait(&sm.bar_q_full[qs], (it >> 1) & 1, abort);
       // this query row's scalars: P = 2^(S2 - LSE2) is formed as 2^(S2 + bias) / 448
@@ -636,6 +638,14 @@ __global__ void __launch_bounds__(384, 1)
           bulk_commit();
           pending_qs = qs;
         }
+      }
+      I = In;
+      qh = qhn;
+      if (In + 1 < prm.nqb) {
+        ++In;
+      } else {
+        In = I0;
+        ++qhn;
       }
     }
     // the last reductions must complete before the CTA's shared memory goes away
