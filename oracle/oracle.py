@@ -72,6 +72,9 @@ def lib():
             L.sage_oracle_fwd.argtypes = [i, i, i, ctypes.c_double, i] + [dp] * 6 + [dp, fp, dp]
             L.sage_oracle_bwd.argtypes = [i, i, i, ctypes.c_double, i, i] + [dp] * 12 + [dp] * 4
             L.sage_oracle_bwd_sdo.argtypes = [i, i, i, ctypes.c_double, i, i] + [dp] * 12 + [dp] * 5
+            L.sage_oracle_quantize_qs.argtypes = [i, i, dp, dp, dp, i, i, i] + [dp] * 13
+            L.sage_oracle_fwd_qs.argtypes = [i, i, i, ctypes.c_double, i] + [dp] * 7 + [dp, fp, dp]
+            L.sage_oracle_bwd_qs.argtypes = [i, i, i, ctypes.c_double, i, i] + [dp] * 12 + [dp] * 7
             _lib = L
     return _lib
 
@@ -104,29 +107,41 @@ def to_bf16(x: np.ndarray) -> np.ndarray:
     return y
 
 
-def quantize(q, k, v, qk_norm, k_smooth, qmask=QM_ALL) -> dict:
+def quantize(q, k, v, qk_norm, k_smooth, qmask=QM_ALL, q_smooth=False) -> dict:
+    """One head's codes and scales.  q_smooth adds "qmean" [ceil(N/128), D] (the query
+    blocks' channel means, removed before the INT8 quantizer) and "dsb" [ceil(N/128), N]
+    (the logit term they carry back), see sage_oracle.c."""
     q, k, v = _c64(q), _c64(k), _c64(v)
     N, D = q.shape
+    nI = max(1, -(-N // 128))
     o = {n: np.zeros((N, D)) for n in ("qn", "kn", "qx", "kx", "vx")}
     o.update(qr=np.zeros(N), kr=np.zeros(N), kmean=np.zeros(D),
-             sq=np.zeros(max(1, -(-N // 128))), sk=np.zeros(max(1, -(-N // 64))), sv=np.zeros(D))
-    rc = lib().sage_oracle_quantize(N, D, _d(q), _d(k), _d(v), int(qk_norm), int(k_smooth), int(qmask),
-                                    _d(o["qn"]), _d(o["qr"]), _d(o["kn"]), _d(o["kr"]), _d(o["kmean"]),
-                                    _d(o["qx"]), _d(o["sq"]), _d(o["kx"]), _d(o["sk"]),
-                                    _d(o["vx"]), _d(o["sv"]))
+             sq=np.zeros(nI), sk=np.zeros(max(1, -(-N // 64))), sv=np.zeros(D))
+    args = [N, D, _d(q), _d(k), _d(v), int(qk_norm), int(k_smooth), int(qmask),
+            _d(o["qn"]), _d(o["qr"]), _d(o["kn"]), _d(o["kr"]), _d(o["kmean"]),
+            _d(o["qx"]), _d(o["sq"]), _d(o["kx"]), _d(o["sk"]), _d(o["vx"]), _d(o["sv"])]
+    if q_smooth:
+        o.update(qmean=np.zeros((nI, D)), dsb=np.zeros((nI, max(N, 1))))
+        rc = lib().sage_oracle_quantize_qs(*args, _d(o["qmean"]), _d(o["dsb"]))
+    else:
+        rc = lib().sage_oracle_quantize(*args)
     if rc:
         raise RuntimeError(f"oracle quantize failed ({rc})")
     return o
 
 
 def forward(qz: dict, causal, sm_scale, qmask=QM_ALL) -> dict:
+    """One head's forward; with Q-smoothing when qz carries "dsb"."""
     N, D = qz["qx"].shape
     O64 = np.zeros((N, D))
     O32 = np.zeros((N, D), dtype=np.float32)
     L = np.zeros(N)
-    rc = lib().sage_oracle_fwd(N, D, int(causal), float(sm_scale), int(qmask),
-                               _d(qz["qx"]), _d(qz["sq"]), _d(qz["kx"]), _d(qz["sk"]),
-                               _d(qz["vx"]), _d(qz["sv"]), _d(O64), _f(O32), _d(L))
+    args = [N, D, int(causal), float(sm_scale), int(qmask), _d(qz["qx"]), _d(qz["sq"]), _d(qz["kx"]),
+            _d(qz["sk"]), _d(qz["vx"]), _d(qz["sv"])]
+    if "dsb" in qz:
+        rc = lib().sage_oracle_fwd_qs(*args, _d(qz["dsb"]), _d(O64), _f(O32), _d(L))
+    else:
+        rc = lib().sage_oracle_fwd(*args, _d(O64), _f(O32), _d(L))
     if rc:
         raise RuntimeError(f"oracle forward failed ({rc})")
     return {"O64": O64, "O32": O32, "Obf": to_bf16(O64), "LSE64": L,
@@ -135,7 +150,8 @@ def forward(qz: dict, causal, sm_scale, qmask=QM_ALL) -> dict:
 
 def backward(qz: dict, v, do, O, LSE, causal, sm_scale, qk_norm, qmask=QM_ALL, sdo=None) -> dict:
     """One head's backward; sdo (optional, [D]) gives the e4m3 channel scales of dO instead of
-    taking them from this head's dO (grouped-query attention, see run_group)."""
+    taking them from this head's dO (grouped-query attention, see run_group).  With
+    Q-smoothing when qz carries "dsb" and "qmean"."""
     v, do, O, LSE = _c64(v), _c64(do), _c64(O), _c64(LSE)
     N, D = v.shape
     dQ, dK, dV = np.zeros((N, D)), np.zeros((N, D)), np.zeros((N, D))
@@ -144,7 +160,11 @@ def backward(qz: dict, v, do, O, LSE, causal, sm_scale, qk_norm, qmask=QM_ALL, s
               _d(v), _d(do), _d(O), _d(LSE),
               _d(qz["qx"]), _d(qz["sq"]), _d(qz["kx"]), _d(qz["sk"]),
               _d(qz["qn"]), _d(qz["qr"]), _d(qz["kn"]), _d(qz["kr"]))
-    if sdo is None:
+    if "dsb" in qz:
+        sdo_a = _c64(sdo) if sdo is not None else None
+        rc = lib().sage_oracle_bwd_qs(*common, _d(sdo_a) if sdo_a is not None else None, _d(qz["dsb"]),
+                                      _d(qz["qmean"]), _d(dQ), _d(dK), _d(dV), _d(Dv))
+    elif sdo is None:
         rc = lib().sage_oracle_bwd(*common, _d(dQ), _d(dK), _d(dV), _d(Dv))
     else:
         sdo = _c64(sdo)
@@ -156,7 +176,7 @@ def backward(qz: dict, v, do, O, LSE, causal, sm_scale, qk_norm, qmask=QM_ALL, s
 
 
 def run_head(q, k, v, do, causal, sm_scale, qk_norm=False, k_smooth=True, qmask=QM_ALL,
-             backward_pass=True, o_aux="bf16") -> dict:
+             backward_pass=True, o_aux="bf16", q_smooth=False) -> dict:
     """Quantize, forward and (optionally) backward of one head.
 
     In the low-bit scheme (F32 bit on) the backward consumes the forward's bf16 O
@@ -164,9 +184,9 @@ def run_head(q, k, v, do, causal, sm_scale, qk_norm=False, k_smooth=True, qmask=
     the fp64 values.  o_aux="fp32" gives the backward the forward's fp32 O instead
     of the bf16 one for D_i = rowsum(dO * O): the high-precision auxiliary output of
     "Attn-QAT: 4-Bit Attention With Quantization-Aware Training" (gist.science
-    summary), Methodology, principle 2.
+    summary), Methodology, principle 2.  q_smooth: Q-smoothing (see quantize).
     """
-    qz = quantize(q, k, v, qk_norm, k_smooth, qmask)
+    qz = quantize(q, k, v, qk_norm, k_smooth, qmask, q_smooth)
     fw = forward(qz, causal, sm_scale, qmask)
     out = dict(qz)
     out.update(fw)
@@ -180,7 +200,8 @@ def run_head(q, k, v, do, causal, sm_scale, qk_norm=False, k_smooth=True, qmask=
     return out
 
 
-def run_group(qs, k, v, dos, causal, sm_scale, qk_norm=False, k_smooth=True, qmask=QM_ALL) -> dict:
+def run_group(qs, k, v, dos, causal, sm_scale, qk_norm=False, k_smooth=True, qmask=QM_ALL,
+              q_smooth=False) -> dict:
     """Grouped-query attention: the G query heads qs[g] (with upstream gradients dos[g])
     share the key/value head k, v.  Each query head is quantized (Q block scales of its
     own; K and V codes, the same for every head of the group), run forward and backward
@@ -201,7 +222,7 @@ def run_group(qs, k, v, dos, causal, sm_scale, qk_norm=False, k_smooth=True, qma
     heads = []
     dK, dV = np.zeros((N, D)), np.zeros((N, D))
     for q, do in zip(qs, dos):
-        qz = quantize(q, k, v, qk_norm, k_smooth, qmask)
+        qz = quantize(q, k, v, qk_norm, k_smooth, qmask, q_smooth)
         fw = forward(qz, causal, sm_scale, qmask)
         out = dict(qz)
         out.update(fw)

@@ -168,12 +168,52 @@ static void l2_normalise(const double *x, int N, int D, int f32, double *xn, dou
  * factors [N] (1 when QK-norm is off); kmean [D] (0 when smoothing is off);
  * qx/kx INT8 codes [N, D] with scales sq [ceil(N/128)], sk [ceil(N/64)];
  * vx e4m3 codes [N, D] with per-channel scales sv [D].
+ *
+ * Q-smoothing (q_smooth; "SageBwd: A Trainable Low-bit Attention", euno.news
+ * summary, Methodology 4, names it as the optional companion of K-smoothing and
+ * prints no formula).  Read as the query-side smoothing of the SageAttention
+ * line: each 128-token query block I loses its channel mean before the INT8
+ * quantizer, and the logits get back what the mean carries as a per-(block, key)
+ * term kept in high precision:
+ *   qmean_I,d = RN32(sum_{t in I} q'_td / |I|)      (valid tokens of the block)
+ *   qs_td     = RN32(q'_td - qmean_I,d)             -> INT8 codes qx, scales sq
+ *   dsb_I,j   = RN32(sum_d qmean_I,d k''_jd)        (k'' = the smoothed k' that K's
+ *                                                    quantizer takes)
+ * so that qs.k'' + dsb = q'.k'' exactly in exact arithmetic.  qmean is
+ * [ceil(N/128), D], dsb [ceil(N/128), N].
  */
+static int quantize_head(int N, int D, const double *Q, const double *K, const double *V,
+                         int qk_norm, int k_smooth, int q_smooth, int qmask,
+                         double *qn, double *qr, double *kn, double *kr, double *kmean,
+                         double *qx, double *sq, double *kx, double *sk,
+                         double *vx, double *sv, double *qmean, double *dsb);
+
 int sage_oracle_quantize(int N, int D, const double *Q, const double *K, const double *V,
                          int qk_norm, int k_smooth, int qmask,
                          double *qn, double *qr, double *kn, double *kr, double *kmean,
                          double *qx, double *sq, double *kx, double *sk,
                          double *vx, double *sv)
+{
+    return quantize_head(N, D, Q, K, V, qk_norm, k_smooth, 0, qmask, qn, qr, kn, kr, kmean,
+                         qx, sq, kx, sk, vx, sv, NULL, NULL);
+}
+
+int sage_oracle_quantize_qs(int N, int D, const double *Q, const double *K, const double *V,
+                            int qk_norm, int k_smooth, int qmask,
+                            double *qn, double *qr, double *kn, double *kr, double *kmean,
+                            double *qx, double *sq, double *kx, double *sk,
+                            double *vx, double *sv, double *qmean, double *dsb)
+{
+    if (!qmean || !dsb) return 1;
+    return quantize_head(N, D, Q, K, V, qk_norm, k_smooth, 1, qmask, qn, qr, kn, kr, kmean,
+                         qx, sq, kx, sk, vx, sv, qmean, dsb);
+}
+
+static int quantize_head(int N, int D, const double *Q, const double *K, const double *V,
+                         int qk_norm, int k_smooth, int q_smooth, int qmask,
+                         double *qn, double *qr, double *kn, double *kr, double *kmean,
+                         double *qx, double *sq, double *kx, double *sk,
+                         double *vx, double *sv, double *qmean, double *dsb)
 {
     if (N < 0 || D <= 0) return 1;
     int f32 = (qmask & QM_F32) != 0;
@@ -201,7 +241,30 @@ int sage_oracle_quantize(int N, int D, const double *Q, const double *K, const d
             ks[i] = k_smooth ? r32(f32, kn[i] - m) : kn[i];
         }
     }
-    block_int8(qn, N, D, QBLK, (qmask & QM_QK) != 0, f32, qx, sq);
+    if (q_smooth) {
+        double *qs = (double *)malloc(sizeof(double) * (E ? E : 1));
+        if (!qs) { free(ks); return 2; }
+        int nI = (N + QBLK - 1) / QBLK;
+        for (int I = 0; I < nI; ++I) {
+            int t0 = I * QBLK, t1 = t0 + QBLK < N ? t0 + QBLK : N;
+            for (int d = 0; d < D; ++d) {
+                double s = 0.0;
+                for (int t = t0; t < t1; ++t) s += qn[(size_t)t * D + d];
+                double m = r32(f32, s / (t1 - t0));
+                qmean[(size_t)I * D + d] = m;
+                for (int t = t0; t < t1; ++t) qs[(size_t)t * D + d] = r32(f32, qn[(size_t)t * D + d] - m);
+            }
+            for (int j = 0; j < N; ++j) {
+                double a = 0.0;
+                for (int d = 0; d < D; ++d) a += qmean[(size_t)I * D + d] * ks[(size_t)j * D + d];
+                dsb[(size_t)I * N + j] = r32(f32, a);
+            }
+        }
+        block_int8(qs, N, D, QBLK, (qmask & QM_QK) != 0, f32, qx, sq);
+        free(qs);
+    } else {
+        block_int8(qn, N, D, QBLK, (qmask & QM_QK) != 0, f32, qx, sq);
+    }
     block_int8(ks, N, D, KBLK, (qmask & QM_QK) != 0, f32, kx, sk);
     channel_e4m3(V, N, D, (qmask & QM_V) != 0, f32, vx, sv);
     free(ks);
@@ -235,11 +298,51 @@ static inline double qk_factor(double sqI, double skJ, double alpha, int f32)
  *   p~ = RN32(2^t) (fp64 exp2);  p8 = e4m3(RN32(448 p~));
  *   l = l 2^(m - m') + sum p~;  A = A 2^(m - m') + sum p8 v8.
  * Finish: O = A sv / (448 l), LSE = ln2 (m + log2 l).
+ * With Q-smoothing (dsb given, [ceil(N/128), N]) the logit of query i in block I
+ * first takes back the block mean's term in natural units,
+ *   u_ij = RN32(acc_ij RN32(sq_I sk_J) + dsb_Ij),
+ * and u_ij alpha plays the part of acc_ij c above (alpha = RN32(sm_scale log2 e)).
  * Outputs O64 [N, D], O32 [N, D] (float), LSE64 [N].
  */
+static int fwd_head(int N, int D, int causal, double sm_scale, int qmask,
+                    const double *qx, const double *sq, const double *kx, const double *sk,
+                    const double *vx, const double *sv, const double *dsb,
+                    double *O64, float *O32, double *LSE64);
+
 int sage_oracle_fwd(int N, int D, int causal, double sm_scale, int qmask,
                     const double *qx, const double *sq, const double *kx, const double *sk,
                     const double *vx, const double *sv,
+                    double *O64, float *O32, double *LSE64)
+{
+    return fwd_head(N, D, causal, sm_scale, qmask, qx, sq, kx, sk, vx, sv, NULL, O64, O32, LSE64);
+}
+
+int sage_oracle_fwd_qs(int N, int D, int causal, double sm_scale, int qmask,
+                       const double *qx, const double *sq, const double *kx, const double *sk,
+                       const double *vx, const double *sv, const double *dsb,
+                       double *O64, float *O32, double *LSE64)
+{
+    if (!dsb) return 1;
+    return fwd_head(N, D, causal, sm_scale, qmask, qx, sq, kx, sk, vx, sv, dsb, O64, O32, LSE64);
+}
+
+/* The log2-domain logit of query i and key j is RN32(x f) for the value x and
+ * factor f this returns: x = acc, f = c without Q-smoothing; x = u, f = alpha
+ * with it (see fwd_head). */
+static inline double logit_parts(double acc, double sqI, double skJ, double alpha, int f32,
+                                 const double *dsb_row, int j, double *f)
+{
+    if (!dsb_row) {
+        *f = qk_factor(sqI, skJ, alpha, f32);
+        return acc;
+    }
+    *f = alpha;
+    return r32(f32, acc * r32(f32, sqI * skJ) + dsb_row[j]);
+}
+
+static int fwd_head(int N, int D, int causal, double sm_scale, int qmask,
+                    const double *qx, const double *sq, const double *kx, const double *sk,
+                    const double *vx, const double *sv, const double *dsb,
                     double *O64, float *O32, double *LSE64)
 {
     if (N < 0 || D <= 0) return 1;
@@ -250,7 +353,7 @@ int sage_oracle_fwd(int N, int D, int causal, double sm_scale, int qmask,
 #pragma omp parallel
     {
         double *A = (double *)malloc(sizeof(double) * D);
-        double *s2 = (double *)malloc(sizeof(double) * 2 * TILE);  /* acc, c per key */
+        double *s2 = (double *)malloc(sizeof(double) * 2 * TILE);  /* x, f per key (logit_parts) */
         if (!A || !s2) {
 #pragma omp atomic write
             err = 2;
@@ -267,9 +370,11 @@ int sage_oracle_fwd(int N, int D, int causal, double sm_scale, int qmask,
                 if (j1 <= j0) break;
                 double mt = -INFINITY;
                 double *acc = s2, *cj = s2 + TILE;
+                const double *dsb_row = dsb ? dsb + (size_t)(i / QBLK) * N : NULL;
                 for (int j = j0; j < j1; ++j) {
-                    double c = qk_factor(sq[i / QBLK], sk[j / KBLK], alpha, f32);
-                    acc[j - j0] = dot(qrow, kx + (size_t)j * D, D);
+                    double c;
+                    acc[j - j0] = logit_parts(dot(qrow, kx + (size_t)j * D, D), sq[i / QBLK], sk[j / KBLK],
+                                              alpha, f32, dsb_row, j, &c);
                     cj[j - j0] = c;
                     mt = fmax(mt, r32(f32, acc[j - j0] * c));
                 }
@@ -304,24 +409,27 @@ int sage_oracle_fwd(int N, int D, int causal, double sm_scale, int qmask,
  * P = RN32(2^RN32(acc c - RN32(LSE log2 e))), p8 = e4m3(RN32(448 P)), P^ = p8 / 448,
  * dP = dO V^T (fp64, unquantized), dS = RN32(P^ (dP - Dvec)),
  * dS8 = INT8 of dS with one scale max|dS|/127 for the tile.
+ * With Q-smoothing (dsb given) the logit is formed as in the forward (logit_parts).
  * p8t/ds8t are [QBLK][KBLK]; returns the tile's dS scale. */
 static double bwd_tile(int I, int J, int N, int D, int causal, double alpha, int qmask,
                        const double *qx, const double *sq, const double *kx, const double *sk,
                        const double *V, const double *dO, const double *lse2, const double *Dv,
-                       double *p8t, double *ds8t)
+                       const double *dsb, double *p8t, double *ds8t)
 {
     int f32 = (qmask & QM_F32) != 0;
     int i0 = I * QBLK, i1 = i0 + QBLK < N ? i0 + QBLK : N;
     int j0 = J * KBLK, j1 = j0 + KBLK < N ? j0 + KBLK : N;
     double amax = 0.0;
-    double c = qk_factor(sq[I], sk[J], alpha, f32);
+    const double *dsb_row = dsb ? dsb + (size_t)I * N : NULL;
     for (int i = i0; i < i1; ++i) {
         for (int j = j0; j < j1; ++j) {
             double *pp = p8t + (size_t)(i - i0) * KBLK + (j - j0);
             double *dd = ds8t + (size_t)(i - i0) * KBLK + (j - j0);
             if (causal && j > i) { *pp = 0.0; *dd = 0.0; continue; }
-            double acc = dot(qx + (size_t)i * D, kx + (size_t)j * D, D);
-            double P = r32(f32, exp2(r32(f32, acc * c - lse2[i])));
+            double c;
+            double x = logit_parts(dot(qx + (size_t)i * D, kx + (size_t)j * D, D), sq[I], sk[J], alpha, f32,
+                                   dsb_row, j, &c);
+            double P = r32(f32, exp2(r32(f32, x * c - lse2[i])));
             double p8 = (qmask & QM_P) ? sage_oracle_e4m3(r32(f32, 448.0 * P)) : 448.0 * P;
             double dp = 0.0;
             for (int d = 0; d < D; ++d) dp += dO[(size_t)i * D + d] * V[(size_t)j * D + d];
@@ -365,13 +473,20 @@ static void l2_normalise_grad(double *g, const double *xn, const double *r, int 
  * then dQ, dK scaled by sm_scale, and passed back through QK-norm; the
  * K-smoothing Jacobian (I - 11^T/N) is applied as the identity: the exact dS
  * rows sum to zero, so the smoothed-K gradient already has zero token mean.
+ * With Q-smoothing (dsb and qmean given) the codes qx are those of q' - qmean_I,
+ * and the keys' gradient takes back the mean's share of S = (q' - qmean) k'' +
+ * qmean k'', per tile:
+ *   dK_j += s_dS (sum_i dS8_ij) qmean_I
+ * (the dequantized dS of the tile, summed over its queries).  dQ needs no such
+ * term: the mean's gradient through qmean_I and through q' - qmean_I cancel.
  * Outputs dQ, dK, dV [N, D] and Dvec [N] in fp64.
  */
 static int bwd_head(int N, int D, int causal, double sm_scale, int qk_norm, int qmask,
                     const double *V, const double *dO, const double *O, const double *LSE,
                     const double *qx, const double *sq, const double *kx, const double *sk,
                     const double *qn, const double *qr, const double *kn, const double *kr,
-                    const double *sdo_in, double *dQ, double *dK, double *dV, double *Dvec);
+                    const double *sdo_in, const double *dsb, const double *qmean,
+                    double *dQ, double *dK, double *dV, double *Dvec);
 
 int sage_oracle_bwd(int N, int D, int causal, double sm_scale, int qk_norm, int qmask,
                     const double *V, const double *dO, const double *O, const double *LSE,
@@ -380,7 +495,7 @@ int sage_oracle_bwd(int N, int D, int causal, double sm_scale, int qk_norm, int 
                     double *dQ, double *dK, double *dV, double *Dvec)
 {
     return bwd_head(N, D, causal, sm_scale, qk_norm, qmask, V, dO, O, LSE, qx, sq, kx, sk, qn, qr, kn, kr,
-                    NULL, dQ, dK, dV, Dvec);
+                    NULL, NULL, NULL, dQ, dK, dV, Dvec);
 }
 
 /*
@@ -396,14 +511,29 @@ int sage_oracle_bwd_sdo(int N, int D, int causal, double sm_scale, int qk_norm, 
                         const double *sdo_in, double *dQ, double *dK, double *dV, double *Dvec)
 {
     return bwd_head(N, D, causal, sm_scale, qk_norm, qmask, V, dO, O, LSE, qx, sq, kx, sk, qn, qr, kn, kr,
-                    sdo_in, dQ, dK, dV, Dvec);
+                    sdo_in, NULL, NULL, dQ, dK, dV, Dvec);
+}
+
+/* The backward with Q-smoothing: dsb [ceil(N/128), N] and qmean [ceil(N/128), D] as
+ * sage_oracle_quantize_qs returns them; sdo_in as in sage_oracle_bwd_sdo, or NULL. */
+int sage_oracle_bwd_qs(int N, int D, int causal, double sm_scale, int qk_norm, int qmask,
+                       const double *V, const double *dO, const double *O, const double *LSE,
+                       const double *qx, const double *sq, const double *kx, const double *sk,
+                       const double *qn, const double *qr, const double *kn, const double *kr,
+                       const double *sdo_in, const double *dsb, const double *qmean,
+                       double *dQ, double *dK, double *dV, double *Dvec)
+{
+    if (!dsb || !qmean) return 1;
+    return bwd_head(N, D, causal, sm_scale, qk_norm, qmask, V, dO, O, LSE, qx, sq, kx, sk, qn, qr, kn, kr,
+                    sdo_in, dsb, qmean, dQ, dK, dV, Dvec);
 }
 
 static int bwd_head(int N, int D, int causal, double sm_scale, int qk_norm, int qmask,
                     const double *V, const double *dO, const double *O, const double *LSE,
                     const double *qx, const double *sq, const double *kx, const double *sk,
                     const double *qn, const double *qr, const double *kn, const double *kr,
-                    const double *sdo_in, double *dQ, double *dK, double *dV, double *Dvec)
+                    const double *sdo_in, const double *dsb, const double *qmean,
+                    double *dQ, double *dK, double *dV, double *Dvec)
 {
     if (N < 0 || D <= 0) return 1;
     int f32 = (qmask & QM_F32) != 0;
@@ -456,7 +586,7 @@ static int bwd_head(int N, int D, int causal, double sm_scale, int qk_norm, int 
             for (int J = 0; J < nJ; ++J) {
                 if (causal && J * KBLK > i1 - 1) break;
                 double s = bwd_tile(I, J, N, D, causal, alpha, qmask, qx, sq, kx, sk, V, dO,
-                                    lse2, Dvec, p8t, ds8t);
+                                    lse2, Dvec, dsb, p8t, ds8t);
                 double c = r32(f32, s * sk[J]);
                 int j0 = J * KBLK, j1 = j0 + KBLK < N ? j0 + KBLK : N;
                 for (int i = i0; i < i1; ++i) {
@@ -495,15 +625,17 @@ static int bwd_head(int N, int D, int causal, double sm_scale, int qk_norm, int 
                 int i0 = I * QBLK, i1 = i0 + QBLK < N ? i0 + QBLK : N;
                 if (causal && j0 > i1 - 1) continue;
                 double s = bwd_tile(I, J, N, D, causal, alpha, qmask, qx, sq, kx, sk, V, dO,
-                                    lse2, Dvec, p8t, ds8t);
+                                    lse2, Dvec, dsb, p8t, ds8t);
                 double c = r32(f32, s * sq[I]);
                 for (int j = j0; j < j1; ++j) {
                     /* acck_d = sum_i dS8_ij qx_id, accv_d = sum_i p8_ij dO8_id, i ascending */
                     for (int d = 0; d < D; ++d) { acc[d] = 0.0; acc2[d] = 0.0; }
+                    double colsum = 0.0;
                     for (int i = i0; i < i1; ++i) {
                         size_t t = (size_t)(i - i0) * KBLK + (j - j0);
                         double a = ds8t[t], p = p8t[t];
                         const double *qrow = qx + (size_t)i * D, *orow = do8 + (size_t)i * D;
+                        colsum += a;
                         for (int d = 0; d < D; ++d) {
                             acc[d] += a * qrow[d];
                             acc2[d] += p * orow[d];
@@ -511,6 +643,7 @@ static int bwd_head(int N, int D, int causal, double sm_scale, int qk_norm, int 
                     }
                     for (int d = 0; d < D; ++d) {
                         dK[(size_t)j * D + d] += c * acc[d];
+                        if (qmean) dK[(size_t)j * D + d] += s * colsum * qmean[(size_t)I * D + d];
                         dV[(size_t)j * D + d] += (sdo[d] / 448.0) * acc2[d];
                     }
                 }

@@ -415,3 +415,115 @@ def test_group_do_scale_spans_the_group():
     np.testing.assert_array_equal(two["sdo"], (np.abs(big).max(0) / 448.0).astype(np.float32).astype(np.float64))
     # the first head's dO is coded with the larger scale: its dV differs from the lone head's
     assert not np.array_equal(two["heads"][0]["dV64"], single["dV64"])
+
+
+# ---------------------------------------------------------------- Q-smoothing
+
+def _bf16(x):
+    return torch.tensor(x).to(torch.bfloat16).to(torch.float64).numpy()
+
+
+@pytest.mark.parametrize("causal,qk_norm", [(False, False), (True, False), (True, True)])
+def test_q_smoothing_exact_mode_matches_library_attention(causal, qk_norm):
+    """Exact arithmetic: (q' - qmean_I) k'' + qmean_I k'' is q' k'', so the Q-smoothed path
+    equals torch attention, and its dK (the per-tile qmean term included) equals autograd's.
+    N = 300 leaves a ragged last query block of 44 tokens, whose mean is over those alone."""
+    rng = np.random.default_rng(50)
+    N, D = 300, 64
+    q, k, v, do = (_rand(rng, N, D) for _ in range(4))
+    q = q + rng.normal(0, 3.0, size=(1, D))  # a common query component for the mean to carry
+    sm = 0.125 if not qk_norm else 4.0
+    r = orc.run_head(q, k, v, do, causal, sm, qk_norm, True, qmask=0, q_smooth=True)
+    O, lse, dq, dk, dv = ref_grads(q, k, v, do, causal, sm, qk_norm, True)
+    np.testing.assert_allclose(r["O64"], O, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(r["LSE64"], lse, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(r["dQ64"], dq, rtol=0, atol=1e-10)
+    np.testing.assert_allclose(r["dK64"], dk, rtol=0, atol=1e-10)
+    np.testing.assert_allclose(r["dV64"], dv, rtol=0, atol=1e-10)
+
+
+def test_q_smoothing_quantizer_parts():
+    """The block means are fp32 roundings of the exact means over each block's valid
+    tokens; the INT8 codes reconstruct q' - qmean to half a step; dsb is qmean . k'' with
+    k'' the smoothed keys K's quantizer takes (fp32 rounding of the fp64 dot product)."""
+    rng = np.random.default_rng(51)
+    N, D = 200, 64
+    q = _bf16(_rand(rng, N, D, offset=2.0))
+    k, v = _bf16(_rand(rng, N, D)), _bf16(_rand(rng, N, D))
+    z = orc.quantize(q, k, v, False, True, q_smooth=True)
+    assert z["qmean"].shape == (2, D) and z["dsb"].shape == (2, N)
+    for I, (t0, t1) in enumerate([(0, 128), (128, 200)]):
+        exact = np.array([math.fsum(q[t0:t1, d]) / (t1 - t0) for d in range(D)])
+        np.testing.assert_array_equal(z["qmean"][I], exact.astype(np.float32).astype(np.float64))
+        qs = (q[t0:t1] - z["qmean"][I]).astype(np.float32).astype(np.float64)
+        s = z["sq"][I]
+        assert s == np.float32(np.abs(qs).max() / 127.0)
+        assert np.abs(z["qx"][t0:t1]).max() == 127
+        assert np.all(np.abs(z["qx"][t0:t1] * s - qs) <= 0.5 * s * (1 + 1e-6))
+    ks = (k - z["kmean"]).astype(np.float32).astype(np.float64)
+    want = (z["qmean"] @ ks.T).astype(np.float32).astype(np.float64)
+    np.testing.assert_allclose(z["dsb"], want, rtol=2 ** -22, atol=1e-12)
+    # no Q-smoothing: the same K, V codes, and the unsmoothed Q codes
+    z0 = orc.quantize(q, k, v, False, True)
+    for n in ("kx", "sk", "vx", "sv", "kmean"):
+        np.testing.assert_array_equal(z[n], z0[n])
+    assert not np.array_equal(z["qx"], z0["qx"])
+
+
+def test_q_smoothing_zero_mean_blocks_keep_the_codes():
+    """Query blocks whose channel means are exactly zero (each token paired with its
+    negation) keep their unsmoothed codes and scales, and dsb is zero; the outputs then differ
+    from the plain scheme only by where the logit rounds (RN(acc RN(sq sk)) alpha against
+    acc RN(RN(sq sk) alpha))."""
+    rng = np.random.default_rng(52)
+    N, D = 256, 64
+    half = _bf16(_rand(rng, 64, D))
+    q = np.concatenate([half, -half, half[::-1], -half[::-1]])
+    k, v, do = (_bf16(_rand(rng, N, D)) for _ in range(3))
+    zq = orc.quantize(q, k, v, False, True, q_smooth=True)
+    z0 = orc.quantize(q, k, v, False, True)
+    assert np.all(zq["qmean"] == 0) and np.all(zq["dsb"] == 0)
+    np.testing.assert_array_equal(zq["qx"], z0["qx"])
+    np.testing.assert_array_equal(zq["sq"], z0["sq"])
+    a = orc.run_head(q, k, v, do, True, 0.125, q_smooth=True)
+    b = orc.run_head(q, k, v, do, True, 0.125)
+    for n in ("O64", "dQ64", "dK64", "dV64"):
+        rel = np.linalg.norm(a[n] - b[n]) / np.linalg.norm(b[n])
+        assert rel < 2e-3, (n, rel)
+
+
+def test_q_smoothing_constant_blocks_reduce_to_high_precision_logits():
+    """Every token of a query block equal: q' - qmean = 0, so the block's scale and codes are
+    0 and its logits are dsb alone, a high-precision product.  With only the Q/K quantizer on,
+    the forward then equals exact attention to fp32 rounding, however coarse K's codes."""
+    rng = np.random.default_rng(53)
+    N, D = 256, 64
+    q = np.repeat(_bf16(_rand(rng, 2, D, offset=1.0)), 128, axis=0)
+    k, v, do = (_bf16(_rand(rng, N, D)) for _ in range(3))
+    qm = orc.QM_QK | orc.QM_F32
+    r = orc.run_head(q, k, v, do, False, 0.125, qmask=qm, backward_pass=False, q_smooth=True)
+    assert np.all(r["sq"] == 0) and np.all(r["qx"] == 0)
+    O, lse, *_ = ref_grads(q, k, v, do, False, 0.125, False, True)
+    np.testing.assert_allclose(r["O64"], O, rtol=0, atol=1e-5)
+    np.testing.assert_allclose(r["LSE64"], lse, rtol=0, atol=1e-5)
+
+
+def test_q_smoothing_lowers_the_error_of_offset_queries():
+    """Queries with a large common component: removing each block's mean before INT8 leaves
+    the codes the varying part.  With the quantizer that Q-smoothing acts on (Q/K INT8) as the
+    only one on, O and dK (which reads the Q codes) land several times closer to exact
+    attention, and dQ no farther.  (With every quantizer on, the e4m3 P and dO codes dominate
+    the gradients' error, and the difference drowns in it.)"""
+    rel = lambda a, b: np.linalg.norm(a - b) / np.linalg.norm(b)  # noqa: E731
+    qm = orc.QM_QK | orc.QM_F32
+    for seed in (54, 55, 56):
+        rng = np.random.default_rng(seed)
+        N, D = 256, 64
+        q, k, v, do = (_rand(rng, N, D) for _ in range(4))
+        q = q + 6.0
+        ex = orc.run_head(q, k, v, do, True, 0.125, qmask=0)
+        plain = orc.run_head(q, k, v, do, True, 0.125, qmask=qm)
+        smooth = orc.run_head(q, k, v, do, True, 0.125, qmask=qm, q_smooth=True)
+        for n in ("O64", "dK64"):
+            assert rel(smooth[n], ex[n]) < 0.5 * rel(plain[n], ex[n]), (seed, n)
+        assert rel(smooth["dQ64"], ex["dQ64"]) <= rel(plain["dQ64"], ex["dQ64"]), seed
