@@ -27,7 +27,8 @@ ABI_FUNCTIONS = ("sage_attn_ws_bytes", "sage_attn_bwd_ws_bytes", "sage_attn_quan
                  "sage_attn_bwd_noalloc", "sage_attn_step_host_bytes", "sage_attn_step_host",
                  "sage_attn_timer_only", "sage_attn_bwd_o32", "sage_attn_gqa_ws_bytes",
                  "sage_attn_gqa_bwd_ws_bytes", "sage_attn_gqa_quantize", "sage_attn_gqa_fwd", "sage_attn_gqa_bwd",
-                 "sage_attn_gqa_ws_views")
+                 "sage_attn_gqa_ws_views", "sage_attn_qs_ws_bytes", "sage_attn_qs_quantize", "sage_attn_qs_fwd",
+                 "sage_attn_qs_bwd", "sage_attn_qs_ws_views")
 
 
 class SageError(RuntimeError):
@@ -40,7 +41,8 @@ class sage_ws_views(ctypes.Structure):
     _fields_ = [("qc", ctypes.c_void_p), ("kc", ctypes.c_void_p), ("v8t", ctypes.c_void_p),
                 ("sq", ctypes.c_void_p), ("sk", ctypes.c_void_p), ("sv", ctypes.c_void_p),
                 ("kmean", ctypes.c_void_p), ("qr", ctypes.c_void_p), ("kr", ctypes.c_void_p),
-                ("status", ctypes.c_void_p), ("n_pad", ctypes.c_int)]
+                ("status", ctypes.c_void_p), ("n_pad", ctypes.c_int), ("qmean", ctypes.c_void_p),
+                ("dsb", ctypes.c_void_p)]
 
 
 _lib = None
@@ -72,6 +74,12 @@ def lib():
             L.sage_attn_gqa_fwd.argtypes = [vp, vp, vp, vp] + [i] * 6 + [fp, vp]
             L.sage_attn_gqa_bwd.argtypes = [vp] * 11 + [sz] + [i] * 8 + [fp, vp]
             L.sage_attn_gqa_ws_views.argtypes = [vp] + [i] * 5 + [ctypes.POINTER(sage_ws_views)]
+            L.sage_attn_qs_ws_bytes.restype = sz
+            L.sage_attn_qs_ws_bytes.argtypes = [i] * 5
+            L.sage_attn_qs_quantize.argtypes = [vp, vp, vp] + [i] * 7 + [vp, sz, vp]
+            L.sage_attn_qs_fwd.argtypes = [vp, vp, vp, vp] + [i] * 6 + [fp, vp]
+            L.sage_attn_qs_bwd.argtypes = [vp] * 11 + [sz] + [i] * 8 + [fp, vp]
+            L.sage_attn_qs_ws_views.argtypes = [vp] + [i] * 5 + [ctypes.POINTER(sage_ws_views)]
             L.sage_attn_ws_views.argtypes = [vp, i, i, i, i, ctypes.POINTER(sage_ws_views)]
             L.sage_attn_get_status.argtypes = [vp, vp]
             L.sage_attn_selftest_wait.argtypes = [vp, u64, vp]
@@ -165,6 +173,32 @@ def sage_attn_gqa_ws_views(ws, B, H, Hkv, N, D) -> sage_ws_views:
     return v
 
 
+def sage_attn_qs_ws_bytes(B, H, Hkv, N, D):
+    return lib().sage_attn_qs_ws_bytes(B, H, Hkv, N, D)
+
+
+def sage_attn_qs_quantize(Q, K, V, B, H, Hkv, N, D, qk_norm, k_smooth, ws, ws_bytes, stream):
+    return lib().sage_attn_qs_quantize(Q, K, V, B, H, Hkv, N, D, int(qk_norm), int(k_smooth), ws, ws_bytes, stream)
+
+
+def sage_attn_qs_fwd(ws, O, LSE, O32, B, H, Hkv, N, D, causal, sm_scale, stream):
+    return lib().sage_attn_qs_fwd(ws, O, LSE, O32, B, H, Hkv, N, D, int(causal), float(sm_scale), stream)
+
+
+def sage_attn_qs_bwd(Q, K, V, O, LSE, dO, dQ, dK, dV, ws, bwd_ws, bwd_ws_bytes, B, H, Hkv, N, D, causal, qk_norm,
+                     k_smooth, sm_scale, stream):
+    return lib().sage_attn_qs_bwd(Q, K, V, O, LSE, dO, dQ, dK, dV, ws, bwd_ws, bwd_ws_bytes, B, H, Hkv, N, D,
+                                  int(causal), int(qk_norm), int(k_smooth), float(sm_scale), stream)
+
+
+def sage_attn_qs_ws_views(ws, B, H, Hkv, N, D) -> sage_ws_views:
+    v = sage_ws_views()
+    rc = lib().sage_attn_qs_ws_views(ws, B, H, Hkv, N, D, ctypes.byref(v))
+    if rc != SAGE_OK:
+        raise SageError("sage_attn_qs_ws_views", rc)
+    return v
+
+
 def sage_attn_ws_views(ws, B, H, N, D) -> sage_ws_views:
     v = sage_ws_views()
     rc = lib().sage_attn_ws_views(ws, B, H, N, D, ctypes.byref(v))
@@ -228,9 +262,12 @@ def _shape(q):
     return B, H, N, D
 
 
-def alloc_ws(B, H, N, D, device="cuda", hkv=None):
+def alloc_ws(B, H, N, D, device="cuda", hkv=None, q_smooth=False):
     import torch
-    n = sage_attn_ws_bytes(B, H, N, D) if hkv in (None, H) else sage_attn_gqa_ws_bytes(B, H, hkv, N, D)
+    if q_smooth:
+        n = sage_attn_qs_ws_bytes(B, H, H if hkv is None else hkv, N, D)
+    else:
+        n = sage_attn_ws_bytes(B, H, N, D) if hkv in (None, H) else sage_attn_gqa_ws_bytes(B, H, hkv, N, D)
     if n == 0:
         raise SageError("sage_attn_ws_bytes", SAGE_ERR_UNSUPPORTED)
     return torch.empty(n, dtype=torch.uint8, device=device)
@@ -244,14 +281,19 @@ def alloc_bwd_ws(B, H, N, D, device="cuda", hkv=None):
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
-def quantize(q, k, v, qk_norm=False, k_smooth=True, ws=None, stream=None):
+def quantize(q, k, v, qk_norm=False, k_smooth=True, ws=None, stream=None, q_smooth=False):
     """Quantize pass on bf16 [B, H, N, D] CUDA tensors (k, v: [B, Hkv, N, D], Hkv dividing H, for
-    grouped-query attention); returns the workspace tensor."""
+    grouped-query attention); returns the workspace tensor.  q_smooth: Q-smoothing
+    (sage_attn_qs_quantize; forward and backward then take q_smooth=True too)."""
     B, H, N, D = _shape(q)
     hkv = k.shape[1]
     if ws is None:
-        ws = alloc_ws(B, H, N, D, q.device, hkv)
-    if hkv == H:
+        ws = alloc_ws(B, H, N, D, q.device, hkv, q_smooth)
+    if q_smooth:
+        _check("sage_attn_qs_quantize",
+               sage_attn_qs_quantize(_ptr(q), _ptr(k), _ptr(v), B, H, hkv, N, D, qk_norm, k_smooth, _ptr(ws),
+                                     ws.numel(), _stream_ptr(stream)))
+    elif hkv == H:
         _check("sage_attn_quantize", sage_attn_quantize(_ptr(q), _ptr(k), _ptr(v), B, H, N, D, qk_norm, k_smooth,
                                                         _ptr(ws), ws.numel(), _stream_ptr(stream)))
     else:
@@ -262,9 +304,9 @@ def quantize(q, k, v, qk_norm=False, k_smooth=True, ws=None, stream=None):
 
 
 def forward(ws, B, H, N, D, causal, sm_scale=None, o=None, lse=None, o32=False, device="cuda", stream=None,
-            hkv=None):
+            hkv=None, q_smooth=False):
     """Forward from a quantize workspace; returns (O bf16, LSE fp32[, O32 fp32]).  hkv: key/value
-    heads of a grouped-query workspace."""
+    heads of a grouped-query workspace; q_smooth: a workspace quantized with Q-smoothing."""
     import torch
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
@@ -273,7 +315,11 @@ def forward(ws, B, H, N, D, causal, sm_scale=None, o=None, lse=None, o32=False, 
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
     O32 = torch.empty((B, H, N, D), dtype=torch.float32, device=device) if o32 is True else (o32 or None)
-    if hkv in (None, H):
+    if q_smooth:
+        _check("sage_attn_qs_fwd", sage_attn_qs_fwd(_ptr(ws), _ptr(o), _ptr(lse), _ptr(O32), B, H,
+                                                    H if hkv is None else hkv, N, D, causal, sm_scale,
+                                                    _stream_ptr(stream)))
+    elif hkv in (None, H):
         _check("sage_attn_fwd", sage_attn_fwd(_ptr(ws), _ptr(o), _ptr(lse), _ptr(O32), B, H, N, D, causal,
                                               sm_scale, _stream_ptr(stream)))
     else:
@@ -283,9 +329,10 @@ def forward(ws, B, H, N, D, causal, sm_scale=None, o=None, lse=None, o32=False, 
 
 
 def backward(q, k, v, o, lse, do, ws, causal, qk_norm=False, k_smooth=True, sm_scale=None, bwd_ws=None,
-             dq=None, dk=None, dv=None, stream=None, o32=None):
+             dq=None, dk=None, dv=None, stream=None, o32=None, q_smooth=False):
     """Backward; returns (dQ, dK, dV) bf16.  With o32 (the forward's fp32 output) the row
-    terms D_i take it instead of the bf16 o (sage_attn_bwd_o32)."""
+    terms D_i take it instead of the bf16 o (sage_attn_bwd_o32); q_smooth: a workspace quantized
+    with Q-smoothing (sage_attn_qs_bwd)."""
     import torch
     B, H, N, D = _shape(q)
     hkv = k.shape[1]
@@ -296,6 +343,14 @@ def backward(q, k, v, o, lse, do, ws, causal, qk_norm=False, k_smooth=True, sm_s
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    if q_smooth:
+        if o32 is not None:
+            raise ValueError("the fp32 auxiliary output is not offered with Q-smoothing")
+        _check("sage_attn_qs_bwd",
+               sage_attn_qs_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk),
+                                _ptr(dv), _ptr(ws), _ptr(bwd_ws), bwd_ws.numel(), B, H, hkv, N, D, causal,
+                                qk_norm, k_smooth, sm_scale, _stream_ptr(stream)))
+        return dq, dk, dv
     if hkv != H:
         if o32 is not None:
             raise ValueError("the fp32 auxiliary output is not offered with grouped key/value heads")
@@ -344,12 +399,18 @@ def get_status(ws, stream=None) -> int:
     return sage_attn_get_status(_ptr(ws), _stream_ptr(stream))
 
 
-def ws_tensors(ws, B, H, N, D, hkv=None) -> dict:
+def ws_tensors(ws, B, H, N, D, hkv=None, q_smooth=False) -> dict:
     """Views of a quantize workspace as torch tensors (for inspection and tests); hkv: key/value
-    heads of a grouped-query workspace (K and V sections then hold B*hkv heads)."""
+    heads of a grouped-query workspace (K and V sections then hold B*hkv heads); q_smooth: a
+    Q-smoothing workspace (adds qmean [B, H, Np/128, D] and dsb [B, H, Np/128, Np])."""
     import torch
     hk = H if hkv is None else hkv
-    v = sage_attn_ws_views(_ptr(ws), B, H, N, D) if hk == H else sage_attn_gqa_ws_views(_ptr(ws), B, H, hk, N, D)
+    if q_smooth:
+        v = sage_attn_qs_ws_views(_ptr(ws), B, H, hk, N, D)
+    elif hk == H:
+        v = sage_attn_ws_views(_ptr(ws), B, H, N, D)
+    else:
+        v = sage_attn_gqa_ws_views(_ptr(ws), B, H, hk, N, D)
     base = ws.data_ptr()
     np_ = v.n_pad
     bh, bk = B * H, B * hk
@@ -358,7 +419,12 @@ def ws_tensors(ws, B, H, N, D, hkv=None) -> dict:
         off = ptr - base
         return ws[off:off + n_bytes].view(dtype).view(shape)
 
-    return {
+    extra = {}
+    if q_smooth:
+        nb = np_ // 128
+        extra = {"qmean": view(v.qmean, bh * nb * D * 4, torch.float32, (B, H, nb, D)),
+                 "dsb": view(v.dsb, bh * nb * np_ * 4, torch.float32, (B, H, nb, np_))}
+    return extra | {
         "qc": view(v.qc, bh * np_ * D * 2, torch.bfloat16, (B, H, np_, D)),
         "kc": view(v.kc, bk * np_ * D * 2, torch.bfloat16, (B, hk, np_, D)),
         "v8t": view(v.v8t, bk * D * np_, torch.uint8, (B, hk, D, np_)),

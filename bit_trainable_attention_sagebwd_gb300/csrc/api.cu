@@ -152,11 +152,8 @@ int sage_attn_gqa_bwd(const void* Q, const void* K, const void* V, const void* O
                           Hkv);
 }
 
-int sage_attn_gqa_ws_views(void* ws, int B, int H, int Hkv, int N, int D, sage_ws_views* v) {
-  if (ws == nullptr || v == nullptr) return SAGE_ERR_INVALID_ARG;
-  if (!shape_ok(B, H, N, D) || !groups_ok(H, Hkv)) return SAGE_ERR_UNSUPPORTED;
-  const sage::QuantWs L = sage::quant_ws_layout(B, H, N, D, Hkv);
-  uint8_t* w = static_cast<uint8_t*>(ws);
+namespace {
+void fill_views(uint8_t* w, const sage::QuantWs& L, bool qs, sage_ws_views* v) {
   v->qc = w + L.qc;
   v->kc = w + L.kc;
   v->v8t = w + L.v8t;
@@ -168,25 +165,68 @@ int sage_attn_gqa_ws_views(void* ws, int B, int H, int Hkv, int N, int D, sage_w
   v->kr = reinterpret_cast<float*>(w + L.kr);
   v->status = reinterpret_cast<int*>(w + L.status);
   v->n_pad = L.np;
+  v->qmean = qs ? reinterpret_cast<float*>(w + L.qmean) : nullptr;
+  v->dsb = qs ? reinterpret_cast<float*>(w + L.dsb) : nullptr;
+}
+}  // namespace
+
+size_t sage_attn_qs_ws_bytes(int B, int H, int Hkv, int N, int D) {
+  if (!shape_ok(B, H, N, D) || !groups_ok(H, Hkv)) return 0;
+  return sage::quant_ws_layout(B, H, N, D, Hkv, true).total;
+}
+
+int sage_attn_qs_quantize(const void* Q, const void* K, const void* V, int B, int H, int Hkv, int N, int D,
+                          int qk_norm, int k_smooth, void* ws, size_t ws_bytes, void* stream) {
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(ws)) return SAGE_ERR_INVALID_ARG;
+  if (!shape_ok(B, H, N, D) || !groups_ok(H, Hkv)) return SAGE_ERR_UNSUPPORTED;
+  if (ws_bytes < sage::quant_ws_layout(B, H, N, D, Hkv, true).total) return SAGE_ERR_INVALID_ARG;
+  return sage::launch_quantize(Q, K, V, B, H, N, D, qk_norm != 0, k_smooth != 0, ws,
+                               static_cast<cudaStream_t>(stream), true, Hkv, true);
+}
+
+int sage_attn_qs_fwd(const void* ws, void* O, float* LSE, float* O32, int B, int H, int Hkv, int N, int D,
+                     int causal, float sm_scale, void* stream) {
+  if (!aligned16(ws) || !aligned16(O) || LSE == nullptr || ((uintptr_t)LSE & 3u)) return SAGE_ERR_INVALID_ARG;
+  if (O32 != nullptr && !aligned16(O32)) return SAGE_ERR_INVALID_ARG;
+  if (!(sm_scale == sm_scale) || isinf(sm_scale)) return SAGE_ERR_INVALID_ARG;
+  if (!shape_ok(B, H, N, D) || !groups_ok(H, Hkv)) return SAGE_ERR_UNSUPPORTED;
+  return sage::launch_fwd(ws, O, LSE, O32, B, H, N, D, causal != 0, resolve_scale(sm_scale, D),
+                          static_cast<cudaStream_t>(stream), Hkv, true);
+}
+
+int sage_attn_qs_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO,
+                     void* dQ, void* dK, void* dV, const void* ws, void* bwd_ws, size_t bwd_ws_bytes, int B, int H,
+                     int Hkv, int N, int D, int causal, int qk_norm, int k_smooth, float sm_scale, void* stream) {
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(dO) || !aligned16(dQ) ||
+      !aligned16(dK) || !aligned16(dV) || !aligned16(ws) || !aligned16(bwd_ws) || LSE == nullptr ||
+      ((uintptr_t)LSE & 3u))
+    return SAGE_ERR_INVALID_ARG;
+  if (!(sm_scale == sm_scale) || isinf(sm_scale)) return SAGE_ERR_INVALID_ARG;
+  if (!shape_ok(B, H, N, D) || !groups_ok(H, Hkv)) return SAGE_ERR_UNSUPPORTED;
+  if (bwd_ws_bytes < sage::bwd_ws_layout(B, H, N, D, Hkv).total) return SAGE_ERR_INVALID_ARG;
+  return sage::launch_bwd(Q, K, V, O, LSE, dO, dQ, dK, dV, ws, bwd_ws, B, H, N, D, causal != 0, qk_norm != 0,
+                          k_smooth != 0, resolve_scale(sm_scale, D), static_cast<cudaStream_t>(stream), nullptr,
+                          Hkv, true);
+}
+
+int sage_attn_qs_ws_views(void* ws, int B, int H, int Hkv, int N, int D, sage_ws_views* v) {
+  if (ws == nullptr || v == nullptr) return SAGE_ERR_INVALID_ARG;
+  if (!shape_ok(B, H, N, D) || !groups_ok(H, Hkv)) return SAGE_ERR_UNSUPPORTED;
+  fill_views(static_cast<uint8_t*>(ws), sage::quant_ws_layout(B, H, N, D, Hkv, true), true, v);
+  return SAGE_OK;
+}
+
+int sage_attn_gqa_ws_views(void* ws, int B, int H, int Hkv, int N, int D, sage_ws_views* v) {
+  if (ws == nullptr || v == nullptr) return SAGE_ERR_INVALID_ARG;
+  if (!shape_ok(B, H, N, D) || !groups_ok(H, Hkv)) return SAGE_ERR_UNSUPPORTED;
+  fill_views(static_cast<uint8_t*>(ws), sage::quant_ws_layout(B, H, N, D, Hkv), false, v);
   return SAGE_OK;
 }
 
 int sage_attn_ws_views(void* ws, int B, int H, int N, int D, sage_ws_views* v) {
   if (ws == nullptr || v == nullptr) return SAGE_ERR_INVALID_ARG;
   if (!shape_ok(B, H, N, D)) return SAGE_ERR_UNSUPPORTED;
-  const sage::QuantWs L = sage::quant_ws_layout(B, H, N, D);
-  uint8_t* w = static_cast<uint8_t*>(ws);
-  v->qc = w + L.qc;
-  v->kc = w + L.kc;
-  v->v8t = w + L.v8t;
-  v->sq = reinterpret_cast<float*>(w + L.sq);
-  v->sk = reinterpret_cast<float*>(w + L.sk);
-  v->sv = reinterpret_cast<float*>(w + L.sv);
-  v->kmean = reinterpret_cast<float*>(w + L.kmean);
-  v->qr = reinterpret_cast<float*>(w + L.qr);
-  v->kr = reinterpret_cast<float*>(w + L.kr);
-  v->status = reinterpret_cast<int*>(w + L.status);
-  v->n_pad = L.np;
+  fill_views(static_cast<uint8_t*>(ws), sage::quant_ws_layout(B, H, N, D), false, v);
   return SAGE_OK;
 }
 

@@ -182,16 +182,24 @@ struct BwdSmem {
   uint8_t do8[D * 128];      // dO e4m3 codes, channel-major
   uint8_t p[128 * 128];      // P e4m3, query rows of 128 keys
   uint8_t ds[128 * 128 * 2]; // dS INT8 codes in bf16, query rows; keys [0,64) then [64,128)
+  // Q-smoothing: bf16 ones, the B operand (16 x 16, unswizzled) of the dS column sums
+  __align__(128) uint16_t ones[256];
   __align__(16) float bias[2][128];  // log2(448) - LSE_i log2(e), per Q buffer
-  __align__(16) float dvec[2][128];  // D_i, per Q buffer
+  union {
+    __align__(16) float dvec[2][128];  // D_i, per Q buffer
+    __align__(16) float dsb[2][128];   // Q-smoothing: the logit terms of the block's keys (D_i then
+                                       // comes from global memory)
+  };
   float smax[8];             // per compute warp: max |448 dS| over its rows of its group's keys
   uint64_t bar_kv;
   uint64_t bar_q_full[2], bar_do_full, bar_do8_full;
   uint64_t bar_q_free[2], bar_do_free, bar_do8_free;
-  uint64_t bar_s, bar_dp, bar_p, bar_ds[2], bar_dk, bar_part, bar_free_s, bar_free_dp;
+  uint64_t bar_s, bar_dp, bar_p, bar_ds[2], bar_dk, bar_part, bar_free_s, bar_free_dp, bar_cs;
   uint32_t tmem_base;
   int abort;
 };
+
+static_assert(sizeof(BwdSmem<128>) <= 227 * 1024, "the backward's shared memory exceeds 227 KB");
 
 struct BwdParams {
   int N, np, nqb, causal, qk_norm;
@@ -203,6 +211,8 @@ struct BwdParams {
   const float* sdo;
   const float* bias;
   const float* dvec;
+  const float* dsb;    // Q-smoothing: [BH query heads][nqb][np] logit terms (nullptr without)
+  const float* qmean;  // Q-smoothing: [BH query heads][nqb][D] query block means
   const __nv_bfloat16* K;
   const float* kr;
   __nv_bfloat16* dK;
@@ -235,7 +245,10 @@ constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23: x + M - M rounds x to
 // boxes (16 KB) into shared memory the next MMAs do not read (its own dS block, then half
 // of the Q buffer just consumed); one thread per group adds them to the feature-major
 // accumulator with TMA reduce and, once the boxes are read, frees the Q buffer.
-template <int D>
+// QS (Q-smoothing): the logit is u = RN(acc RN(s_q s_k) + dsb_j) and P = 2^(u alpha + bias);
+// the dS codes' column sums (an extra MMA against ones into TMEM columns [128,144), read
+// before dQ1 overwrites them) give dK its term s_dS (sum_i dS8_ij) qmean_I.
+template <int D, bool QS>
 __global__ void __launch_bounds__(384, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -282,8 +295,13 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&sm.bar_part, 1);
     mbar_init(&sm.bar_free_s, 256);
     mbar_init(&sm.bar_free_dp, 256);
+    mbar_init(&sm.bar_cs, 256);
     sm.abort = 0;
     fence_mbar_init();
+  }
+  if (QS && tid < 128) {
+    reinterpret_cast<uint32_t*>(sm.ones)[tid] = 0x3f803f80u;  // bf16 1.0, 1.0
+    fence_proxy_async_smem();  // read by the tensor core
   }
   if (warp == WMMA) {
     tmem_alloc(&sm.tmem_base, kCols);
@@ -333,9 +351,13 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d(sm.q[qs] + c * 16384, &tm_q, c * 64, I * 128, qh, &sm.bar_q_full[qs]);
-        // the query block's bias and D_i rows travel with its Q tile
+        // the query block's bias and D_i rows (with Q-smoothing: its logit terms for this key
+        // block) travel with its Q tile
         bulk_load(sm.bias[qs], prm.bias + (size_t)qh * prm.np + I * 128, 512, &sm.bar_q_full[qs]);
-        bulk_load(sm.dvec[qs], prm.dvec + (size_t)qh * prm.np + I * 128, 512, &sm.bar_q_full[qs]);
+        if constexpr (QS)
+          bulk_load(sm.dsb[qs], prm.dsb + ((size_t)qh * prm.nqb + I) * prm.np + kb * 128, 512, &sm.bar_q_full[qs]);
+        else
+          bulk_load(sm.dvec[qs], prm.dvec + (size_t)qh * prm.np + I * 128, 512, &sm.bar_q_full[qs]);
       }
     } else if (warp == WMMA && lane == 0) {
       // ---------------- UMMA issuer
@@ -343,6 +365,7 @@ __global__ void __launch_bounds__(384, 1)
       constexpr uint32_t id_dv = idesc_e4m3(128, D, true);            // dV = P^T dO8: A from query rows
       constexpr uint32_t id_dk = idesc_bf16(128, D, true, true);      // dK = dS^T Q: A from query rows
       constexpr uint32_t id_dq = idesc_bf16(128, D, false, true);     // dQ = dS K: B from key rows
+      constexpr uint32_t id_cs = idesc_bf16(128, 16, true, false);    // dS^T ones: column sums
       const uint32_t a_k = smem_u32(sm.k), a_v = smem_u32(sm.v), a_do = smem_u32(sm.dob);
       const uint32_t a_do8 = smem_u32(sm.do8), a_p = smem_u32(sm.p), a_ds = smem_u32(sm.ds);
       bool ok = mbar_wait(&sm.bar_kv, 0, abort);
@@ -387,11 +410,23 @@ __global__ void __launch_bounds__(384, 1)
         for (int kk = 0; kk < 8; ++kk)
           umma_bf16(tmem + cS, sdesc_sw128(a_ds + kk * 2048, 16384, 1024), sdesc_sw128(a_q + kk * 2048, 16384, 1024),
                     id_dk, kk > 0);
+        if constexpr (QS) {
+          // column sums of the dS codes (exact integers) into the dP columns, which are free
+          // until dQ1: 16 identical columns, every step reads the same 16 x 16 ones
+          const uint64_t b1 = sdesc_none(smem_u32(sm.ones), 128, 256);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma_bf16(tmem + cDQ1, sdesc_sw128(a_ds + kk * 2048, 16384, 1024), b1, id_cs, kk > 0);
+        }
         umma_commit(&sm.bar_dk);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           umma_bf16(tmem + cDQ0, sdesc_sw128(a_ds + kk * 32, 16, 1024), sdesc_sw128(a_k + kk * 2048, 16384, 1024),
                     id_dq, kk > 0);
+        if constexpr (QS) {
+          if (!mbar_wait(&sm.bar_cs, ph, abort)) break;  // the column sums are read
+          tc_fence_after();
+        }
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           umma_bf16(tmem + cDQ1, sdesc_sw128(a_ds + 16384 + kk * 32, 16, 1024),
@@ -426,6 +461,8 @@ __global__ void __launch_bounds__(384, 1)
     // but still runs every iteration, so no thread is left behind at a named barrier
     bool ok = true;
     float sq_next = prm.sq[(size_t)bh * prm.group * prm.nqb + I0];
+    // with Q-smoothing D_i comes from global memory, also an iteration early
+    float dvec_next = QS ? prm.dvec[(size_t)bh * prm.group * prm.np + I0 * 128 + t] : 0.f;
     // (query block I, query head qh) of iteration it, and of the next, advanced without a division
     int I = I0, qh = bh * prm.group;
     int In = I0 + 1 < prm.nqb ? I0 + 1 : I0, qhn = I0 + 1 < prm.nqb ? qh : qh + 1;
@@ -434,14 +471,17 @@ __global__ void __launch_bounds__(384, 1)
       // the query block's scale was fetched an iteration early (global latency off the path)
       const float sqI = sq_next;
       if (it + 1 < n_it) sq_next = prm.sq[(size_t)qhn * prm.nqb + In];
+      float dvec_t = dvec_next;
+      if (QS && it + 1 < n_it) dvec_next = prm.dvec[(size_t)qhn * prm.np + In * 128 + t];
       const int qs = it & 1;
       ok = ok && mbar_wait(&sm.bar_q_full[qs], (it >> 1) & 1, abort);
       // this query row's scalars: P = 2^(S2 - LSE2) is formed as 2^(S2 + bias) / 448
       const float bias_t = sm.bias[qs][t];
-      const float dvec_t = sm.dvec[qs][t];
+      if constexpr (!QS) dvec_t = sm.dvec[qs][t];
       // a zero logit scale (all-zero Q or K block: every unmasked S there is 0) becomes the
-      // smallest subnormal, so that a masked -inf times it stays -inf
-      const float cs_raw = __fmul_rn(__fmul_rn(sqI, sk_mine), prm.alpha);
+      // smallest subnormal, so that a masked -inf times it stays -inf.  With Q-smoothing the
+      // scale leaves alpha out: it multiplies u = acc c + dsb.
+      const float cs_raw = QS ? __fmul_rn(sqI, sk_mine) : __fmul_rn(__fmul_rn(sqI, sk_mine), prm.alpha);
       const float cs = cs_raw > 0.f ? cs_raw : __uint_as_float(1u);
       // masked key columns kc >= klim: padding, and keys after this query on the diagonal block
       const int klim = (prm.causal && I == kb) ? min(klim_pad, t + 1) : klim_pad;
@@ -466,14 +506,25 @@ __global__ void __launch_bounds__(384, 1)
             if ((int)kcol + 32 * c + e >= klim) buf[c][e] = 0xff800000u;
       }
       {
-        const uint64_t cs2 = f2(cs, cs), b2 = f2(bias_t, bias_t);
+        const uint64_t cs2 = f2(cs, cs), b2 = f2(bias_t, bias_t), al2 = f2(prm.alpha, prm.alpha);
+        const float* drow = &sm.dsb[qs][kcol];  // Q-smoothing: this group's 64 keys
+        // exponent of 448 P: acc cs + bias, or (acc cs + dsb) alpha + bias
+        auto arg = [&](uint32_t s0, uint32_t s1, int e) -> uint64_t {
+          const uint64_t a2 = f2(__uint_as_float(s0), __uint_as_float(s1));
+          if constexpr (QS) {
+            const float2 d = *reinterpret_cast<const float2*>(drow + e);
+            return ffma2(ffma2(a2, cs2, f2(d.x, d.y)), al2, b2);
+          } else {
+            return ffma2(a2, cs2, b2);
+          }
+        };
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
 #pragma unroll
           for (int e = 0; e < 32; e += 4) {
             float p[4];
-            f2split(ffma2(f2(__uint_as_float(buf[c][e]), __uint_as_float(buf[c][e + 1])), cs2, b2), p[0], p[1]);
-            f2split(ffma2(f2(__uint_as_float(buf[c][e + 2]), __uint_as_float(buf[c][e + 3])), cs2, b2), p[2], p[3]);
+            f2split(arg(buf[c][e], buf[c][e + 1], 32 * c + e), p[0], p[1]);
+            f2split(arg(buf[c][e + 2], buf[c][e + 3], 32 * c + e + 2), p[2], p[3]);
 #pragma unroll
             for (int u = 0; u < 4; ++u) p[u] = ex2(p[u]);
             const __nv_fp8x2_storage_t lo =
@@ -563,6 +614,17 @@ __global__ void __launch_bounds__(384, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&sm.bar_ds[g]);
+      // Q-smoothing: this query block's mean over this group's features, for the dK term
+      // (loaded while the dK MMA runs)
+      float qb[QS ? DG : 1];
+      if constexpr (QS) {
+        const float4* src = reinterpret_cast<const float4*>(prm.qmean + ((size_t)qh * prm.nqb + I) * D + dcol);
+#pragma unroll
+        for (int c = 0; c < DG / 4; ++c) {
+          const float4 v = __ldg(src + c);
+          qb[4 * c] = v.x, qb[4 * c + 1] = v.y, qb[4 * c + 2] = v.z, qb[4 * c + 3] = v.w;
+        }
+      }
       // ---- dK += RN(s_dS * s_q) * part (key row t);  dQ (query row t) += ca * part0 + cb * part1
       ok = ok && mbar_wait(&sm.bar_dk, ph, abort);
       tc_fence_after();
@@ -576,6 +638,17 @@ __global__ void __launch_bounds__(384, 1)
       const float sds1 = a1 > 0.f ? __fdiv_rn(a1 * (1.0f / 448.0f), 127.0f) : 0.f;
       const float ck = __fmul_rn(t >> 6 ? sds1 : sds0, sqI);
       const float ca = __fmul_rn(sds0, sk0), cb = __fmul_rn(sds1, sk1);
+      // Q-smoothing: dK row t += RN(s_dS * sum_i dS8_it) * qmean (the sum is exact in TMEM)
+      float cq = 0.f;
+      if constexpr (QS) {
+        uint32_t csum;
+        tmem_ld1(tmem + lane_base + cDQ1, csum);
+        tmem_ld_wait();
+        asm volatile("" : "+r"(csum));
+        cq = __fmul_rn(t >> 6 ? sds1 : sds0, __uint_as_float(csum));
+        tc_fence_before();
+        mbar_arrive(&sm.bar_cs);  // dQ1 may overwrite the column sums
+      }
       {
         uint32_t kA[16], kB[16];
         tmem_ld16(tmem + lane_base + cS + dcol, kA);
@@ -584,11 +657,17 @@ __global__ void __launch_bounds__(384, 1)
         for (int c = 0; c < DG; c += 32) {
           tmem_ld16(tmem + lane_base + cS + dcol + c + 16, kB);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) dk[c + e] = fmaf(ck, __uint_as_float(kA[e]), dk[c + e]);
+          for (int e = 0; e < 16; ++e) {
+            dk[c + e] = fmaf(ck, __uint_as_float(kA[e]), dk[c + e]);
+            if constexpr (QS) dk[c + e] = fmaf(cq, qb[c + e], dk[c + e]);
+          }
           tmem_wait16(kB);
           if (c + 32 < DG) tmem_ld16(tmem + lane_base + cS + dcol + c + 32, kA);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) dk[c + 16 + e] = fmaf(ck, __uint_as_float(kB[e]), dk[c + 16 + e]);
+          for (int e = 0; e < 16; ++e) {
+            dk[c + 16 + e] = fmaf(ck, __uint_as_float(kB[e]), dk[c + 16 + e]);
+            if constexpr (QS) dk[c + 16 + e] = fmaf(cq, qb[c + 16 + e], dk[c + 16 + e]);
+          }
           if (c + 32 < DG) tmem_wait16(kA);
         }
       }
@@ -729,12 +808,12 @@ __global__ void __launch_bounds__(384, 1)
   if (tid == 0 && sm.abort) atomicExch(prm.status, kDevTimeout);
 }
 
-template <int D>
+template <int D, bool QS>
 int launch_main_t(const CUtensorMap& tk, const CUtensorMap& tq, const CUtensorMap& tv, const CUtensorMap& tdo,
                   const CUtensorMap& tdo8, const CUtensorMap& tdq, const BwdParams& p, int BH, cudaStream_t st) {
   size_t smem = sizeof(BwdSmem<D>);
   if (smem < 120 * 1024) smem = 120 * 1024;  // one CTA per SM: it holds all 512 TMEM columns
-  auto kern = bwd_main_kernel<D>;
+  auto kern = bwd_main_kernel<D, QS>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 3;
   ScopedTimer timer("bwd_main", st);
   if (launch_pdl(kern, dim3(p.nqb * BH), dim3(384), smem, st, tk, tq, tv, tdo, tdo8, tdq, p) != cudaSuccess) return 3;
@@ -745,9 +824,10 @@ int launch_main_t(const CUtensorMap& tk, const CUtensorMap& tq, const CUtensorMa
 
 int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO,
                void* dQ, void* dK, void* dV, const void* ws, void* bwd_ws, int B, int H, int N, int D, int causal,
-               int qk_norm, int k_smooth, float sm_scale, cudaStream_t st, const float* O32, int Hkv) {
+               int qk_norm, int k_smooth, float sm_scale, cudaStream_t st, const float* O32, int Hkv,
+               bool q_smooth) {
   (void)k_smooth;  // the smoothing Jacobian is applied as the identity (dS rows sum to zero)
-  const QuantWs QL = quant_ws_layout(B, H, N, D, Hkv);
+  const QuantWs QL = quant_ws_layout(B, H, N, D, Hkv, q_smooth);
   const BwdWs BL = bwd_ws_layout(B, H, N, D, Hkv);
   const uint8_t* w = static_cast<const uint8_t*>(ws);
   uint8_t* bw = static_cast<uint8_t*>(bwd_ws);
@@ -802,13 +882,17 @@ int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const
   p.sdo = sdo;
   p.bias = biasv;
   p.dvec = dvec;
+  p.dsb = q_smooth ? reinterpret_cast<const float*>(w + QL.dsb) : nullptr;
+  p.qmean = q_smooth ? reinterpret_cast<const float*>(w + QL.qmean) : nullptr;
   p.K = static_cast<const __nv_bfloat16*>(K);
   p.kr = reinterpret_cast<const float*>(w + QL.kr);
   p.dK = static_cast<__nv_bfloat16*>(dK);
   p.dV = static_cast<__nv_bfloat16*>(dV);
   p.status = reinterpret_cast<int*>(const_cast<uint8_t*>(w) + QL.status);
-  int rc = D == 128 ? launch_main_t<128>(tk, tq, tv, tdo, tdo8, tdq, p, BHk, st)
-                    : launch_main_t<64>(tk, tq, tv, tdo, tdo8, tdq, p, BHk, st);
+  int rc = q_smooth ? (D == 128 ? launch_main_t<128, true>(tk, tq, tv, tdo, tdo8, tdq, p, BHk, st)
+                                : launch_main_t<64, true>(tk, tq, tv, tdo, tdo8, tdq, p, BHk, st))
+                     : (D == 128 ? launch_main_t<128, false>(tk, tq, tv, tdo, tdo8, tdq, p, BHk, st)
+                                 : launch_main_t<64, false>(tk, tq, tv, tdo, tdo8, tdq, p, BHk, st));
   if (rc) return rc;
   ScopedTimer timer("bwd_dq", st);
   return launch_bwd_dq(Q, reinterpret_cast<const float*>(w + QL.qr), bwd_ws, dQ, B, H, N, D, qk_norm, sm_scale,

@@ -40,6 +40,8 @@ struct FwdSmem {
   uint8_t p[2][128 * 128];           // P of tiles A and B (e4m3, 128B-swizzled K-major)
   float xmax[2][2][128];             // per tile and key half: row maxima of the current key tile
   float xsum[2][2][128];             // per tile and key half: row sums, exchanged at the end
+  // Q-smoothing: the logit terms of tiles A and B for the keys of each value stage
+  __align__(16) float dsb[kVStages][2][128];
   uint64_t bar_q;
   uint64_t bar_k_full[kKStages], bar_k_empty[kKStages];
   uint64_t bar_v_full[kVStages], bar_v_empty[kVStages];
@@ -59,6 +61,7 @@ struct FwdParams {
   const float* sq;
   const float* sk;
   const float* sv;
+  const float* dsb;  // Q-smoothing: [BH][nqb][np] logit terms (nullptr without)
   __nv_bfloat16* O;
   float* O32;
   float* LSE;
@@ -192,7 +195,9 @@ __device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float 
 // owns query row t (TMEM lane t) and the 64 keys [64 hh, 64 hh + 64) of every key tile, which
 // is exactly one K scale block.  The two halves exchange their row maxima once per tile and
 // their row sums at the end; each rescales and writes half of the O columns.
-template <int D, bool CAUSAL>
+// QS (Q-smoothing): the logit first takes back the query block mean's term in natural units,
+// u = RN(acc RN(s_q s_k) + dsb_j), and u alpha stands where acc c stands otherwise.
+template <int D, bool CAUSAL, bool QS>
 __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParams& prm, int X, int hh, int qb,
                                                   int bh, uint32_t tmem, volatile int* abort) {
   constexpr int DH = D / 2;  // O columns of this half
@@ -218,7 +223,10 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
     if (j + 1 < n_tiles) sk_next = skh[2 * (j + 1)];
     ok = ok && mbar_wait(&sm.bar_s_full[X], j & 1, abort);
     tc_fence_after();
-    const float cc = logit_scale(__fmul_rn(__fmul_rn(s_q, skj), prm.alpha));
+    // with Q-smoothing the tile's logit terms travel with its value tile
+    const float* brow = &sm.dsb[j % kVStages][X][hh * 64];
+    if constexpr (QS) ok = ok && mbar_wait(&sm.bar_v_full[j % kVStages], (j / kVStages) & 1, abort);
+    const float cc = QS ? logit_scale(__fmul_rn(s_q, skj)) : logit_scale(__fmul_rn(__fmul_rn(s_q, skj), prm.alpha));
     const int kbase = j * 128;
     const bool masked_tile = (kbase + 128 > prm.N) || (CAUSAL && j == qb);
     int lim = prm.N - kbase;  // keys [0, lim) of the tile are valid
@@ -234,14 +242,28 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
       reg_fence32(sh[1]);
       if (masked_tile) mask_half(sh, lim - hh * 64);
       float a[2] = {-INFINITY, -INFINITY};  // one running maximum per load: two chains
+      if constexpr (QS) {
 #pragma unroll
-      for (int q = 0; q < 2; ++q)
+        for (int q = 0; q < 2; ++q)
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) a[q] = max3(a[q], __uint_as_float(sh[q][e]), __uint_as_float(sh[q][e + 1]));
+          for (int e = 0; e < 32; e += 4) {
+            const float4 b = *reinterpret_cast<const float4*>(brow + 32 * q + e);
+            const float u0 = fmaf(__uint_as_float(sh[q][e]), cc, b.x), u1 = fmaf(__uint_as_float(sh[q][e + 1]), cc, b.y);
+            const float u2 = fmaf(__uint_as_float(sh[q][e + 2]), cc, b.z), u3 = fmaf(__uint_as_float(sh[q][e + 3]), cc, b.w);
+            a[q] = max3(a[q], u0, u1);
+            a[q] = max3(a[q], u2, u3);
+          }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) a[q] = max3(a[q], __uint_as_float(sh[q][e]), __uint_as_float(sh[q][e + 1]));
+      }
       mx = fmaxf(a[0], a[1]);
     }
-    // the log2-domain logit is acc * c with c > 0, so its maximum is max(acc) * c
-    const float mt = mx == -INFINITY ? -INFINITY : __fmul_rn(mx, cc);
+    // the log2-domain logit is acc * c with c > 0, so its maximum is max(acc) * c (with
+    // Q-smoothing: u * alpha, alpha > 0)
+    const float mt = mx == -INFINITY ? -INFINITY : __fmul_rn(mx, QS ? prm.alpha : cc);
     sm.xmax[X][hh][t] = mt;
     named_bar_tile(X);
     const float m_new = max3(m, sm.xmax[X][0][t], sm.xmax[X][1][t]);
@@ -256,8 +278,18 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
     {
       const uint64_t neg_m2 = f2(-m_new, -m_new);
       const uint64_t k448 = f2(448.f, 448.f);
-      const uint64_t cc2 = f2(cc, cc);
+      const uint64_t cc2 = f2(cc, cc), al2 = f2(prm.alpha, prm.alpha);
       const uint32_t bm = prm.band_mult;
+      // t = RN(acc c - m) (one FMA), or RN(u alpha - m) with u = RN(acc c + dsb_e)
+      auto targ = [&](uint32_t s0, uint32_t s1, int e) -> uint64_t {
+        const uint64_t a2 = f2(__uint_as_float(s0), __uint_as_float(s1));
+        if constexpr (QS) {
+          const float2 b = *reinterpret_cast<const float2*>(brow + e);
+          return ffma2(ffma2(a2, cc2, f2(b.x, b.y)), al2, neg_m2);
+        } else {
+          return ffma2(a2, cc2, neg_m2);
+        }
+      };
       uint64_t lsum[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};  // two independent chains
 #pragma unroll 1
       for (int q = 0; q < 2; ++q) {
@@ -278,7 +310,7 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
 #pragma unroll
           for (int u = 0; u < 4; u += 2) {
             float t0, t1;
-            f2split(ffma2(f2(__uint_as_float(sv[e + u]), __uint_as_float(sv[e + u + 1])), cc2, neg_m2), t0, t1);
+            f2split(targ(sv[e + u], sv[e + u + 1], 32 * q + e + u), t0, t1);
             f2split(fmul2(f2(ex2(t0), ex2(t1)), k448), x[u], x[u + 1]);
             lsum[u >> 1] = fadd2(lsum[u >> 1], f2(x[u], x[u + 1]));
             band[u >> 1] = min(band[u >> 1], min(band_key(x[u], bm), band_key(x[u + 1], bm)));
@@ -296,7 +328,7 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             float t0, t1, x0, x1;
-            f2split(ffma2(f2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), cc2, neg_m2), t0, t1);
+            f2split(targ(sv[e], sv[e + 1], 32 * q + e), t0, t1);
             f2split(fmul2(f2(ex2(t0), ex2(t1)), k448), x0, x1);
             if (band_key(x0, bm) <= kBandMax) flags |= 1u << e;
             if (band_key(x1, bm) <= kBandMax) flags |= 1u << (e + 1);
@@ -305,8 +337,9 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
             const int e = __ffs(flags) - 1;
             flags &= flags - 1;
             const int byte = 32 * c + e;  // key column in the row
-            prow[((((byte >> 4) ^ (t & 7)) << 4)) | (byte & 15)] =
-                (uint8_t)exact_p_code(fmaf(__uint_as_float(pick32(sv, e)), cc, -m_new));
+            const float acc = __uint_as_float(pick32(sv, e));
+            const float targ1 = QS ? fmaf(fmaf(acc, cc, brow[32 * q + e]), prm.alpha, -m_new) : fmaf(acc, cc, -m_new);
+            prow[((((byte >> 4) ^ (t & 7)) << 4)) | (byte & 15)] = (uint8_t)exact_p_code(targ1);
           }
         }
       }
@@ -381,7 +414,7 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
 //   S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) ...
 // so the tensor core works on one tile while the other tile's softmax runs.
 // TMEM columns: S_A [0,128), S_B [128,256), O_A [256,256+D), O_B [256+D,256+2D).
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool QS>
 __global__ void __launch_bounds__(640, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdParams prm) {
@@ -455,8 +488,14 @@ __global__ void __launch_bounds__(640, 1)
           tma_load_3d(sm.k[s] + c * 16384, &tm_k, c * 64, j * 128, bh / prm.group, &sm.bar_k_full[s]);
         const int vs = j % kVStages;
         if (j >= kVStages && !mbar_wait(&sm.bar_v_empty[vs], ((j / kVStages) - 1) & 1, abort)) break;
-        mbar_arrive_expect_tx(&sm.bar_v_full[vs], D * 128);
+        mbar_arrive_expect_tx(&sm.bar_v_full[vs], D * 128 + (QS ? (hasB ? 1024 : 512) : 0));
         tma_load_3d(sm.v[vs], &tm_v, j * 128, 0, bh / prm.group, &sm.bar_v_full[vs]);
+        if constexpr (QS) {
+          // the logit terms of both query tiles for this key tile
+          const float* b = prm.dsb + ((size_t)bh * prm.nqb + qbA) * prm.np + j * 128;
+          bulk_load(sm.dsb[vs][0], b, 512, &sm.bar_v_full[vs]);
+          if (hasB) bulk_load(sm.dsb[vs][1], b + prm.np, 512, &sm.bar_v_full[vs]);
+        }
       }
     } else if (warp == 17 && lane == 0) {
       // ---------------- UMMA issuer
@@ -525,7 +564,7 @@ __global__ void __launch_bounds__(640, 1)
     regs_increase<kRegsSoftmax>();
     // one call site, so the four warpgroups run (and share instruction-cache lines of) one copy
     const int X = warp >> 3, hh = (warp >> 2) & 1;
-    if (X == 0 || hasB) softmax_tile_loop<D, CAUSAL>(sm, prm, X, hh, X ? qbB : qbA, bh, tmem, abort);
+    if (X == 0 || hasB) softmax_tile_loop<D, CAUSAL, QS>(sm, prm, X, hh, X ? qbB : qbA, bh, tmem, abort);
   }
   tc_fence_before();
   __syncthreads();
@@ -533,12 +572,12 @@ __global__ void __launch_bounds__(640, 1)
   if (tid == 0 && sm.abort) atomicExch(prm.status, kDevTimeout);
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool QS>
 int launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                  int BH, cudaStream_t st) {
   // at least 120 KB so that one CTA (which takes all 512 TMEM columns) runs per SM
   const size_t smem = sizeof(FwdSmem<D>) + 1024 > 120 * 1024 ? sizeof(FwdSmem<D>) + 1024 : 120 * 1024;
-  auto kern = fwd_kernel<D, CAUSAL>;
+  auto kern = fwd_kernel<D, CAUSAL, QS>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 3;
   ScopedTimer timer("fwd", st);
   if (launch_pdl(kern, dim3(p.npairs * BH), dim3(640), smem, st, tq, tk, tv, p) != cudaSuccess) return 3;
@@ -548,8 +587,8 @@ int launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
 }  // namespace
 
 int launch_fwd(const void* ws, void* O, float* LSE, float* O32, int B, int H, int N, int D, int causal,
-               float sm_scale, cudaStream_t st, int Hkv) {
-  const QuantWs L = quant_ws_layout(B, H, N, D, Hkv);
+               float sm_scale, cudaStream_t st, int Hkv, bool q_smooth) {
+  const QuantWs L = quant_ws_layout(B, H, N, D, Hkv, q_smooth);
   const uint8_t* w = static_cast<const uint8_t*>(ws);
   const int BH = B * H, BHk = B * (Hkv > 0 ? Hkv : H), np = L.np;
   CUtensorMap tq, tk, tv;
@@ -570,12 +609,22 @@ int launch_fwd(const void* ws, void* O, float* LSE, float* O32, int B, int H, in
   p.sq = reinterpret_cast<const float*>(w + L.sq);
   p.sk = reinterpret_cast<const float*>(w + L.sk);
   p.sv = reinterpret_cast<const float*>(w + L.sv);
+  p.dsb = q_smooth ? reinterpret_cast<const float*>(w + L.dsb) : nullptr;
   p.O = static_cast<__nv_bfloat16*>(O);
   p.O32 = O32;
   p.LSE = LSE;
   p.status = reinterpret_cast<int*>(const_cast<uint8_t*>(w) + L.status);
-  if (D == 128) return causal ? launch_fwd_t<128, true>(tq, tk, tv, p, BH, st) : launch_fwd_t<128, false>(tq, tk, tv, p, BH, st);
-  return causal ? launch_fwd_t<64, true>(tq, tk, tv, p, BH, st) : launch_fwd_t<64, false>(tq, tk, tv, p, BH, st);
+  if (q_smooth) {
+    if (D == 128)
+      return causal ? launch_fwd_t<128, true, true>(tq, tk, tv, p, BH, st)
+                    : launch_fwd_t<128, false, true>(tq, tk, tv, p, BH, st);
+    return causal ? launch_fwd_t<64, true, true>(tq, tk, tv, p, BH, st)
+                  : launch_fwd_t<64, false, true>(tq, tk, tv, p, BH, st);
+  }
+  if (D == 128)
+    return causal ? launch_fwd_t<128, true, false>(tq, tk, tv, p, BH, st)
+                  : launch_fwd_t<128, false, false>(tq, tk, tv, p, BH, st);
+  return causal ? launch_fwd_t<64, true, false>(tq, tk, tv, p, BH, st) : launch_fwd_t<64, false, false>(tq, tk, tv, p, BH, st);
 }
 
 }  // namespace sage

@@ -7,16 +7,20 @@ namespace sage {
 
 // Grouped-query attention: Hkv key/value heads per batch entry, Hkv divides H (0: Hkv = H);
 // query head h reads key/value head h / (H / Hkv).
-// clear_status = false keeps the workspace status word (errors of earlier launches)
+// clear_status = false keeps the workspace status word (errors of earlier launches).
+// q_smooth: Q-smoothing (the query blocks' channel means leave the INT8 codes and come back as
+// a logit term); the workspace then has the layout quant_ws_layout(..., qs = true), and the
+// forward and backward on it take q_smooth too.
 int launch_quantize(const void* Q, const void* K, const void* V, int B, int H, int N, int D, int qk_norm,
-                    int k_smooth, void* ws, cudaStream_t st, bool clear_status = true, int Hkv = 0);
+                    int k_smooth, void* ws, cudaStream_t st, bool clear_status = true, int Hkv = 0,
+                    bool q_smooth = false);
 int launch_fwd(const void* ws, void* O, float* LSE, float* O32, int B, int H, int N, int D, int causal,
-               float sm_scale, cudaStream_t st, int Hkv = 0);
+               float sm_scale, cudaStream_t st, int Hkv = 0, bool q_smooth = false);
 // O32 (optional, fp32 [B,H,N,D]) replaces O in the row terms D_i = sum_d dO O
 int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO,
                void* dQ, void* dK, void* dV, const void* ws, void* bwd_ws, int B, int H, int N, int D,
                int causal, int qk_norm, int k_smooth, float sm_scale, cudaStream_t st, const float* O32 = nullptr,
-               int Hkv = 0);
+               int Hkv = 0, bool q_smooth = false);
 // dQ epilogue of the backward (the work ticket in the backward workspace must be zero)
 int launch_bwd_dq(const void* Q, const float* qr, void* bwd_ws, void* dQ, int B, int H, int N, int D, int qk_norm,
                   float sm_scale, int* status, cudaStream_t st, int Hkv = 0);

@@ -12,15 +12,16 @@ inline int pad128(int n) { return (n + 127) / 128 * 128; }
 
 struct QuantWs {
   // byte offsets
-  size_t status, sync, qc, kc, v8t, sq, sk, sv, kmean, qr, kr, kpart, vpart, total;
+  size_t status, sync, qc, kc, v8t, sq, sk, sv, kmean, qr, kr, kpart, vpart, qmean, dsb, total;
   int np;
 };
 
 // quantize workspace: codes and scales the forward and backward read, and the
 // per-128-token partial sums that the smoothing mean and the V scales come from.
 // Hkv key/value heads per batch entry (Hkv divides H; 0 means Hkv = H): the Q sections hold
-// B*H heads, the K and V sections B*Hkv.
-inline QuantWs quant_ws_layout(int B, int H, int N, int D, int Hkv = 0) {
+// B*H heads, the K and V sections B*Hkv.  With Q-smoothing (qs) two more sections per query
+// head: the query blocks' channel means [nb][D] and the logit terms they carry [nb][Np].
+inline QuantWs quant_ws_layout(int B, int H, int N, int D, int Hkv = 0, bool qs = false) {
   QuantWs L{};
   const size_t bh = (size_t)B * H, bk = (size_t)B * (Hkv > 0 ? Hkv : H);
   const int np = pad128(N);
@@ -39,6 +40,8 @@ inline QuantWs quant_ws_layout(int B, int H, int N, int D, int Hkv = 0) {
   L.kr = o;     o = align256(o + bk * np * 4);
   L.kpart = o;  o = align256(o + bk * nb * D * 8);  // fp64 partial column sums of k'
   L.vpart = o;  o = align256(o + bk * nb * D * 4);  // partial channel max |V|
+  L.qmean = o;  o = align256(o + (qs ? bh * nb * D * 4 : 0));
+  L.dsb = o;    o = align256(o + (qs ? bh * nb * np * 4 : 0));
   L.total = o;
   L.np = np;
   return L;

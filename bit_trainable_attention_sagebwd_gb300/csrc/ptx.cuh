@@ -261,6 +261,10 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         "=r"(r[15])
       : "r"(taddr));
 }
+// one 32-bit column: thread t of the warp gets lane (warp's lane quarter + t)
+__device__ __forceinline__ void tmem_ld1(uint32_t taddr, uint32_t& r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
@@ -317,6 +321,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   d |= 1ull << 46;  // descriptor version for tcgen05
   d |= 2ull << 61;  // 128-byte swizzle
   return d;
+}
+
+// Shared-memory matrix descriptor without swizzle: the tile is made of core matrices of
+// 8 rows x 16 bytes (128 contiguous bytes); lbo and sbo are the byte distances between
+// core matrices adjacent along K and along M (or N).
+__device__ __forceinline__ uint64_t sdesc_none(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;  // descriptor version for tcgen05
+  return d;         // layout type 0: no swizzle
 }
 
 // Instruction descriptors (kind::f16 with bf16 inputs / kind::f8f6f4 with

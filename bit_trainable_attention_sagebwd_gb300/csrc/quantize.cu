@@ -519,15 +519,199 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(
   }
 }
 
+// ---------------------------------------------------------------------------
+// Q-smoothing ("SageBwd: A Trainable Low-bit Attention", Methodology 4 names it beside
+// K-smoothing): a 128-token query block loses its channel mean before the INT8 quantizer,
+//   qmean_d = RN(sum over the block's tokens of q'_d / tokens),   qs = RN(q' - qmean),
+// and the codes and the block scale are those of qs.  The sums are carried in double-float
+// and combined in fp64, so the mean is the fp32 rounding of the exact one (as the smoothing
+// mean of K in kstats).
+template <int D, bool QKN>
+__global__ void __launch_bounds__(kThreads) qsmooth_q_kernel(const __nv_bfloat16* __restrict__ Q, int N,
+                                                              __nv_bfloat16* __restrict__ qc, float* __restrict__ sq,
+                                                              float* __restrict__ qr, float* __restrict__ qmean,
+                                                              int* __restrict__ status) {
+  constexpr int TPR = D / 8, RPP = kThreads / TPR, PASSES = 128 / RPP;
+  const int blk = blockIdx.x, bh = blockIdx.y, nb = gridDim.x, np = nb * 128;
+  const int tid = threadIdx.x, g = tid % TPR, ro = tid / TPR, warp = tid >> 5, lane = tid & 31;
+  const int rows = min(128, N - blk * 128);
+  extern __shared__ __align__(128) uint8_t stage_buf[];
+  __shared__ BlockStage st;
+  __shared__ double s_sum[kThreads / 32][D];
+  __shared__ float s_mean[D];
+  __shared__ float s_red[kThreads / 32];
+  const __nv_bfloat16* src = Q + (size_t)bh * N * D + (size_t)blk * 128 * D;
+  if (!stage_block(st, stage_buf, src, (uint32_t)rows * D * 2, status)) return;
+  pdl_wait();
+  pdl_trigger();
+  // q' of pass p (zero past the end of the sequence)
+  float rn[PASSES];
+  auto load = [&](int p, float (&x)[8]) {
+    unpack8(staged<D>(stage_buf, p * RPP + ro, rows, g), x);
+    if constexpr (QKN) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[i] = __fmul_rn(x[i], rn[p]);
+    }
+  };
+  DF cs[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) cs[i] = {0.f, 0.f};
+#pragma unroll
+  for (int p = 0; p < PASSES; ++p) {
+    const int row = p * RPP + ro;
+    float x[8];
+    if constexpr (QKN) {
+      unpack8(staged<D>(stage_buf, row, rows, g), x);
+      rn[p] = inv_norm<TPR>(x);
+    } else {
+      rn[p] = 1.f;
+    }
+    if (g == 0) qr[(size_t)bh * np + blk * 128 + row] = rn[p];
+    load(p, x);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) cs[i] = df_add(cs[i], x[i]);  // zero past the end
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int m = TPR; m < 32; m <<= 1) cs[i] = df_add(cs[i], df_shfl_xor(cs[i], m));
+  if (lane < TPR) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s_sum[warp][g * 8 + i] = (double)cs[i].hi + (double)cs[i].lo;
+  }
+  __syncthreads();
+  if (tid < D) {
+    double t = 0.0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) t += s_sum[w][tid];
+    const float m = (float)(t / (double)rows);
+    s_mean[tid] = m;
+    qmean[((size_t)bh * nb + blk) * D + tid] = m;
+  }
+  __syncthreads();
+  float qm[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) qm[i] = s_mean[g * 8 + i];
+  // qs = RN(q' - qmean) for tokens of the sequence, 0 past its end
+  auto smoothed = [&](int p, float (&x)[8]) {
+    load(p, x);
+    const bool live = p * RPP + ro < rows;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = live ? __fsub_rn(x[i], qm[i]) : 0.f;
+  };
+  float am = 0.f;
+#pragma unroll
+  for (int p = 0; p < PASSES; ++p) {
+    float x[8];
+    smoothed(p, x);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(x[i]));
+  }
+  am = warp_max(am);
+  if (lane == 0) s_red[warp] = am;
+  __syncthreads();
+  float a = 0.f;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) a = fmaxf(a, s_red[w]);
+  const float sc = a > 0.f ? __fdiv_rn(a, 127.0f) : 0.f;
+  const float inv = sc > 0.f ? __frcp_rn(sc) : 0.f;
+  const bool exact = !(sc < INFINITY && inv < INFINITY);  // every code divides
+  if (tid == 0) sq[(size_t)bh * nb + blk] = sc;
+#pragma unroll
+  for (int p = 0; p < PASSES; ++p) {
+    const int row = p * RPP + ro;
+    float x[8], c[8];
+    smoothed(p, x);
+    if (exact) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) c[i] = sc > 0.f ? fminf(fmaxf(rintf(__fdiv_rn(x[i], sc)), -127.f), 127.f) : 0.f;
+    } else {
+      int_codes8(x, sc, inv, c);
+    }
+    reinterpret_cast<uint4*>(qc + (size_t)bh * np * D + (size_t)(blk * 128 + row) * D)[g] = pack8_bf16(c);
+  }
+}
+
+// The logit term of Q-smoothing, dsb[qh][I][j] = sum_d qmean[qh][I][d] k''[kvh][j][d] (fp32
+// products and sums, d ascending), for the 128 keys j of block kb and every query block I.
+// k'' is recomputed as K's quantizer forms it: RN(k r) with QK-norm, minus the smoothing mean.
+// One CTA per (key block, query head); a warp takes 4 query blocks at a time, a lane 4 keys.
+template <int D, bool QKN>
+__global__ void __launch_bounds__(kThreads) qs_bias_kernel(const __nv_bfloat16* __restrict__ K, int N,
+                                                            int k_smooth, const float* __restrict__ kmean,
+                                                            const float* __restrict__ kr,
+                                                            const float* __restrict__ qmean, float* __restrict__ dsb,
+                                                            int group) {
+  constexpr int IC = 32;  // query blocks per chunk: 8 warps x 4
+  const int kb = blockIdx.x, qh = blockIdx.y, nb = gridDim.x, np = nb * 128;
+  const int kvh = qh / group;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  extern __shared__ __align__(16) float ks[];  // [D][128]: k'' transposed
+  __shared__ __align__(16) float qt[D][IC + 4];  // qmean of a chunk of query blocks, transposed
+  pdl_wait();  // kmean, the key norms and the query means come from the quantize passes
+  pdl_trigger();
+  {
+    // thread: key t of the block, channels [h D/2, h D/2 + D/2)
+    const int t = tid & 127, h = tid >> 7;
+    const int key = kb * 128 + t;
+    const bool live = key < N;
+    const float r = (QKN && live) ? kr[(size_t)kvh * np + key] : 1.f;
+    const uint4* row = reinterpret_cast<const uint4*>(K + ((size_t)kvh * N + (live ? key : 0)) * D + h * (D / 2));
+#pragma unroll
+    for (int c = 0; c < D / 16; ++c) {
+      float x[8];
+      unpack8(live ? __ldg(row + c) : make_uint4(0u, 0u, 0u, 0u), x);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int d = h * (D / 2) + c * 8 + i;
+        float v = QKN ? __fmul_rn(x[i], r) : x[i];
+        if (k_smooth) v = __fsub_rn(v, kmean[(size_t)kvh * D + d]);
+        ks[d * 128 + t] = live ? v : 0.f;
+      }
+    }
+  }
+  for (int I0 = 0; I0 < nb; I0 += IC) {
+    __syncthreads();  // ks is written; the previous chunk's qt is read
+    for (int idx = tid; idx < IC * D; idx += kThreads) {
+      const int i = idx / D, d = idx % D;
+      qt[d][i] = I0 + i < nb ? qmean[((size_t)qh * nb + I0 + i) * D + d] : 0.f;
+    }
+    __syncthreads();
+    float acc[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+#pragma unroll 4
+    for (int d = 0; d < D; ++d) {
+      const float4 kv = *reinterpret_cast<const float4*>(&ks[d * 128 + 4 * lane]);
+      const float4 qv = *reinterpret_cast<const float4*>(&qt[d][4 * warp]);
+      const float kk[4] = {kv.x, kv.y, kv.z, kv.w}, qq[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(qq[a], kk[b], acc[a][b]);
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const int I = I0 + 4 * warp + a;
+      if (I < nb)
+        *reinterpret_cast<float4*>(dsb + ((size_t)qh * nb + I) * np + kb * 128 + 4 * lane) =
+            make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+    }
+  }
+}
+
 }  // namespace
 
 int launch_quantize(const void* Q, const void* K, const void* V, int B, int H, int N, int D, int qk_norm,
-                    int k_smooth, void* ws, cudaStream_t st, bool clear_status, int Hkv) {
-  const QuantWs L = quant_ws_layout(B, H, N, D, Hkv);
+                    int k_smooth, void* ws, cudaStream_t st, bool clear_status, int Hkv, bool q_smooth) {
+  const QuantWs L = quant_ws_layout(B, H, N, D, Hkv, q_smooth);
   const int BHk = B * (Hkv > 0 ? Hkv : H);
   uint8_t* w = static_cast<uint8_t*>(ws);
   const int nb = L.np / 128;
-  const dim3 qgrid(nb, B * H, 3);
+  // grid z: V, K, then Q (with Q-smoothing the query blocks take their own kernel)
+  const dim3 qgrid(nb, B * H, q_smooth ? 2 : 3);
   auto* q = static_cast<const __nv_bfloat16*>(Q);
   auto* k = static_cast<const __nv_bfloat16*>(K);
   auto* v = static_cast<const __nv_bfloat16*>(V);
@@ -557,6 +741,26 @@ int launch_quantize(const void* Q, const void* K, const void* V, int B, int H, i
                  reinterpret_cast<float*>(w + L.sq), reinterpret_cast<float*>(w + L.sk),
                  reinterpret_cast<float*>(w + L.qr), reinterpret_cast<float*>(w + L.kr), status, BHk) != cudaSuccess)
     return 3;
+  if (q_smooth) {
+    auto qsq = D == 128 ? (qk_norm ? qsmooth_q_kernel<128, true> : qsmooth_q_kernel<128, false>)
+                        : (qk_norm ? qsmooth_q_kernel<64, true> : qsmooth_q_kernel<64, false>);
+    auto bias = D == 128 ? (qk_norm ? qs_bias_kernel<128, true> : qs_bias_kernel<128, false>)
+                         : (qk_norm ? qs_bias_kernel<64, true> : qs_bias_kernel<64, false>);
+    const size_t ks_bytes = (size_t)D * 128 * 4;
+    if (cudaFuncSetAttribute(qsq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)stage) != cudaSuccess ||
+        cudaFuncSetAttribute(bias, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ks_bytes) != cudaSuccess)
+      return 3;
+    float* qmean = reinterpret_cast<float*>(w + L.qmean);
+    if (launch_pdl(qsq, dim3(nb, B * H), dim3(kThreads), stage, st, q, N,
+                   reinterpret_cast<__nv_bfloat16*>(w + L.qc), reinterpret_cast<float*>(w + L.sq),
+                   reinterpret_cast<float*>(w + L.qr), qmean, status) != cudaSuccess)
+      return 3;
+    // after the Q blocks (their means) and, through them, the K blocks (their norms)
+    if (launch_pdl(bias, dim3(nb, B * H), dim3(kThreads), ks_bytes, st, k, N, k_smooth, (const float*)kmean,
+                   reinterpret_cast<const float*>(w + L.kr), (const float*)qmean, reinterpret_cast<float*>(w + L.dsb),
+                   H / (Hkv > 0 ? Hkv : H)) != cudaSuccess)
+      return 3;
+  }
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 

@@ -119,6 +119,8 @@ def head_inputs(w: Workload, bh: int) -> dict:
         k = k + ex.normal(0.0, 2.0, size=(1, D))
     elif w.kind == "k_offset3":
         k = k + ex.normal(0.0, 3.0, size=(1, D))
+    elif w.kind == "q_offset3":
+        q = q + ex.normal(0.0, 3.0, size=(1, D))  # a common query component (Q-smoothing cases)
     elif w.kind == "k_outlier20":
         ch = ex.permutation(D)[:4]
         k[:, ch] *= 20.0

@@ -78,6 +78,8 @@ typedef struct sage_ws_views {
   float *kr;     /* [B*H, Np]     1/||k|| per token (1 without QK-norm)              */
   int *status;   /* device status word                                               */
   int n_pad;     /* Np                                                               */
+  float *qmean;  /* Q-smoothing: [B*H, Np/128, D] query block means (else NULL)      */
+  float *dsb;    /* Q-smoothing: [B*H, Np/128, Np] logit terms (else NULL)           */
 } sage_ws_views;
 
 /* Bytes of the quantize workspace for this shape (0 if unsupported). It holds the
@@ -174,7 +176,37 @@ int sage_attn_gqa_bwd(const void *Q, const void *K, const void *V, const void *O
  * kmean, kr hold B*Hkv. */
 int sage_attn_gqa_ws_views(void *ws, int B, int H, int Hkv, int N, int D, sage_ws_views *views);
 
-/* Fill `views` with the device pointers inside a quantize workspace. */
+/*
+ * Q-smoothing (the optional companion of K-smoothing that "SageBwd: A Trainable Low-bit
+ * Attention" (euno.news summary), Methodology 4, names without a formula), with grouped
+ * heads as the sage_attn_gqa_* calls (Hkv = H: one key/value head per query head).
+ *  - Quantize: each 128-token query block I loses its channel mean before the INT8
+ *    quantizer: qmean_I = RN32(sum of the block's q' / its token count) (the fp32 rounding of
+ *    the exact mean), qs = RN32(q' - qmean_I), codes and block scale of qs.  The logit terms
+ *    dsb[I][j] = qmean_I . k''_j (fp32 products and sums, k'' the smoothed keys of the query
+ *    head's key/value head) are stored for every (query block, key).  Workspace:
+ *    sage_attn_qs_ws_bytes; it adds 4*B*H*Np/128*(D + Np) bytes to the grouped layout.
+ *  - Forward: the logit of query i (block I) and key j is u = RN32(acc * RN32(s_q s_k) +
+ *    dsb[I][j]) in natural units; u * RN32(sm_scale log2 e) enters the online softmax.
+ *  - Backward (scratch: sage_attn_gqa_bwd_ws_bytes): P is recomputed with the same u, and
+ *    dK of each key gets, per (query block, 64-key block) tile, s_dS (sum over the tile's
+ *    queries of the dS codes) qmean_I: the mean's share of S = qs k'' + qmean k''.
+ * Arguments, layouts, ownership and errors as in the sage_attn_gqa_* calls; a workspace
+ * quantized with Q-smoothing is read only by sage_attn_qs_fwd and sage_attn_qs_bwd.
+ */
+size_t sage_attn_qs_ws_bytes(int B, int H, int Hkv, int N, int D);
+int sage_attn_qs_quantize(const void *Q, const void *K, const void *V, int B, int H, int Hkv, int N, int D,
+                          int qk_norm, int k_smooth, void *ws, size_t ws_bytes, void *stream);
+int sage_attn_qs_fwd(const void *ws, void *O, float *LSE, float *O32, int B, int H, int Hkv, int N, int D,
+                     int causal, float sm_scale, void *stream);
+int sage_attn_qs_bwd(const void *Q, const void *K, const void *V, const void *O, const float *LSE,
+                     const void *dO, void *dQ, void *dK, void *dV, const void *ws, void *bwd_ws,
+                     size_t bwd_ws_bytes, int B, int H, int Hkv, int N, int D, int causal, int qk_norm,
+                     int k_smooth, float sm_scale, void *stream);
+/* Workspace views of the Q-smoothing layout, qmean and dsb included. */
+int sage_attn_qs_ws_views(void *ws, int B, int H, int Hkv, int N, int D, sage_ws_views *views);
+
+/* Fill `views` with the device pointers inside a quantize workspace (qmean, dsb: NULL). */
 int sage_attn_ws_views(void *ws, int B, int H, int N, int D, sage_ws_views *views);
 
 /* Synchronise `stream`, read and clear the workspace status word.  Returns SAGE_OK

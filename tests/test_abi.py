@@ -113,3 +113,38 @@ def test_timer_filter_needs_no_gpu(lib):
     assert sa.sage_attn_timer_only("bwd_main") == sa.SAGE_OK
     assert sa.sage_attn_timer_only(None) == sa.SAGE_OK
     assert sa.sage_attn_timer_read("bwd_main") == (0.0, 0)
+
+
+def test_q_smoothing_workspace_and_argument_errors(lib):
+    """The Q-smoothing workspace is the grouped one plus the query block means and the logit
+    terms (4 bytes each, [B*H][Np/128][D] and [B*H][Np/128][Np]); its views point into it in
+    order, and its calls refuse bad arguments before any launch."""
+    for (B, H, Hkv, N, D) in [(1, 2, 2, 256, 64), (4, 16, 4, 2048, 128), (2, 3, 1, 333, 128)]:
+        np_ = (N + 127) // 128 * 128
+        nb = np_ // 128
+        base = sa.sage_attn_gqa_ws_bytes(B, H, Hkv, N, D)
+        n = sa.sage_attn_qs_ws_bytes(B, H, Hkv, N, D)
+        extra = B * H * nb * (D + np_) * 4
+        assert base + extra <= n <= base + extra + 512 and n % 256 == 0
+        v = sa.sage_attn_qs_ws_views(ctypes.c_void_p(1 << 20), B, H, Hkv, N, D)
+        ptrs = [v.status, v.qc, v.kc, v.v8t, v.sq, v.sk, v.sv, v.kmean, v.qr, v.kr, v.qmean, v.dsb]
+        assert ptrs == sorted(ptrs) and v.dsb - v.qmean >= B * H * nb * D * 4
+        assert (1 << 20) + n - v.dsb >= B * H * nb * np_ * 4
+    # the other layouts have no Q-smoothing sections
+    v = sa.sage_attn_ws_views(ctypes.c_void_p(1 << 20), 1, 2, 256, 64)
+    assert v.qmean is None and v.dsb is None
+    assert sa.sage_attn_qs_ws_bytes(1, 4, 3, 128, 64) == 0  # Hkv must divide H
+    null = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(0x10000)
+    n = sa.sage_attn_qs_ws_bytes(1, 4, 2, 256, 64)
+    assert sa.sage_attn_qs_quantize(null, fake, fake, 1, 4, 2, 256, 64, 0, 1, fake, n, null) == sa.SAGE_ERR_INVALID_ARG
+    assert sa.sage_attn_qs_quantize(fake, fake, fake, 1, 4, 2, 256, 64, 0, 1, fake, n - 256,
+                                    null) == sa.SAGE_ERR_INVALID_ARG
+    assert sa.sage_attn_qs_quantize(fake, fake, fake, 1, 4, 3, 256, 64, 0, 1, fake, n, null) == sa.SAGE_ERR_UNSUPPORTED
+    assert sa.sage_attn_qs_fwd(fake, fake, null, null, 1, 4, 2, 256, 64, 1, 0.125, null) == sa.SAGE_ERR_INVALID_ARG
+    assert sa.sage_attn_qs_fwd(fake, fake, fake, null, 1, 4, 2, 256, 96, 1, 0.125, null) == sa.SAGE_ERR_UNSUPPORTED
+    nbw = sa.sage_attn_gqa_bwd_ws_bytes(1, 4, 2, 256, 64)
+    args = [fake] * 11
+    assert sa.sage_attn_qs_bwd(*args, nbw - 256, 1, 4, 2, 256, 64, 1, 0, 1, 0.125, null) == sa.SAGE_ERR_INVALID_ARG
+    assert sa.sage_attn_qs_bwd(*args, nbw, 1, 4, 2, 256, 64, 1, 0, 1, float("nan"), null) == sa.SAGE_ERR_INVALID_ARG
+    assert sa.sage_attn_qs_bwd(*args, nbw, 1, 4, 3, 256, 64, 1, 0, 1, 0.125, null) == sa.SAGE_ERR_UNSUPPORTED
