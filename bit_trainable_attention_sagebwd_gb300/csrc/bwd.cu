@@ -148,11 +148,15 @@ __global__ void bwd_docomb_kernel(const float* __restrict__ dopart, int D, int n
 // e4m3 codes of one 128-query block of dO with the head's channel scales, written
 // channel-major [BH, D, Np]; the rows are read straight from global memory.  The block's
 // columns of the dQ accumulator are zeroed here rather than in bwd_pre, whose dO reads then
-// stay in L2 for this kernel.
+// stay in L2 for this kernel.  With the query heads of a key/value head split over several
+// backward CTAs (kvacc not null), the first query head of each key/value head also zeroes
+// the block's rows of the dK and dV sums and the block's counter.
 template <int D>
 __global__ void __launch_bounds__(kPreThreads, 4) bwd_do8_kernel(const __nv_bfloat16* __restrict__ dO, int N,
                                                                const float* __restrict__ sdo, int group,
-                                                               uint8_t* __restrict__ do8t, float* __restrict__ dqacc) {
+                                                               uint8_t* __restrict__ do8t, float* __restrict__ dqacc,
+                                                               float* __restrict__ kvacc, int* __restrict__ kvcnt,
+                                                               size_t kv_stride) {
   constexpr int TPR = D / 8;
   const int tid = threadIdx.x;
   // blocks in the reverse order of bwd_pre: the dO blocks it read last are re-read first
@@ -169,6 +173,17 @@ __global__ void __launch_bounds__(kPreThreads, 4) bwd_do8_kernel(const __nv_bflo
   for (int idx = tid; idx < D * 32; idx += kPreThreads) {
     const int d = idx >> 5, c = idx & 31;
     reinterpret_cast<float4*>(dqacc + ((size_t)bh * D + d) * np + blk * 128)[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  if (kvacc != nullptr && bh % group == 0) {
+    // dK sums then dV sums (kv_stride floats apart): rows [128 blk, 128 blk + 128) of the head
+    const int kvh = bh / group;
+    float4* a = reinterpret_cast<float4*>(kvacc + ((size_t)kvh * np + blk * 128) * D);
+    float4* b = reinterpret_cast<float4*>(kvacc + kv_stride + ((size_t)kvh * np + blk * 128) * D);
+    for (int idx = tid; idx < 32 * D; idx += kPreThreads) {
+      a[idx] = make_float4(0.f, 0.f, 0.f, 0.f);
+      b[idx] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (tid == 0) kvcnt[(size_t)kvh * (np / 128) + blk] = 0;
   }
 }
 
@@ -197,6 +212,7 @@ struct BwdSmem {
   uint64_t bar_s, bar_dp, bar_p, bar_ds[2], bar_dk, bar_part, bar_free_s, bar_free_dp, bar_cs;
   uint32_t tmem_base;
   int abort;
+  int last;  // split query heads: this CTA is the last of its key block to finish
 };
 
 static_assert(sizeof(BwdSmem<128>) <= 227 * 1024, "the backward's shared memory exceeds 227 KB");
@@ -213,6 +229,12 @@ struct BwdParams {
   const float* dvec;
   const float* dsb;    // Q-smoothing: [BH query heads][nqb][np] logit terms (nullptr without)
   const float* qmean;  // Q-smoothing: [BH query heads][nqb][D] query block means
+  // grouped heads: the query heads of a key/value head are split over `split` CTAs per key
+  // block, which add dK and dV into fp32 sums [BH][np][D]; the last to count finishes them
+  int split;
+  float* dkacc;
+  float* dvacc;
+  int* kvcnt;
   const __nv_bfloat16* K;
   const float* kr;
   __nv_bfloat16* dK;
@@ -265,13 +287,16 @@ __global__ void __launch_bounds__(384, 1)
   constexpr int DG = D / 2;  // output columns per compute thread
   constexpr int WPROD = 8, WMMA = 9;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  int kb, bh;  // one CTA per (key block, key/value head)
-  tile_head_order((int)blockIdx.x, prm.nqb, prm.BH, prm.hgroup, kb, bh);
+  int kb, bh;  // one CTA per (key block, key/value head, share of its query heads)
+  const int tile = (int)blockIdx.x / prm.split, sp = (int)blockIdx.x - tile * prm.split;
+  tile_head_order(tile, prm.nqb, prm.BH, prm.hgroup, kb, bh);
   const int I0 = prm.causal ? kb : 0;
-  // iteration it: query block I0 + it % nq of query head bh * group + it / nq (grouped-query
-  // attention: every query head of the group sees this key block)
+  // iteration it: query block I0 + it % nq of query head qh0 + it / nq (grouped-query
+  // attention: every query head of the group sees this key block; this CTA takes gs of them)
   const int nq = prm.nqb - I0;
-  const int n_it = prm.group * nq;
+  const int gs = prm.group / prm.split;
+  const int qh0 = bh * prm.group + sp * gs;
+  const int n_it = gs * nq;
   constexpr uint32_t kCols = 512;
   constexpr uint32_t cS = 0, cDP = 128, cDV = 256, cDQ0 = 384, cDQ1 = 128;  // TMEM column bases
   constexpr uint32_t kTile = 128 * D * 2;
@@ -335,7 +360,7 @@ __global__ void __launch_bounds__(384, 1)
         tma_load_3d(sm.v + c * 16384, &tm_v, c * 64, kb * 128, bh, &sm.bar_kv);
       }
       // (query block I, query head qh) of iteration it, advanced without a division
-      for (int it = 0, I = I0, qh = bh * prm.group; it < n_it; ++it, I = I + 1 < prm.nqb ? I + 1 : I0,
+      for (int it = 0, I = I0, qh = qh0; it < n_it; ++it, I = I + 1 < prm.nqb ? I + 1 : I0,
                qh = I == I0 ? qh + 1 : qh) {
         if (it > 0 && !mbar_wait(&sm.bar_do_free, (it - 1) & 1, abort)) break;
         mbar_arrive_expect_tx(&sm.bar_do_full, kTile);
@@ -460,11 +485,11 @@ __global__ void __launch_bounds__(384, 1)
     // a wait that times out raises the abort flag; from then on this thread skips its waits
     // but still runs every iteration, so no thread is left behind at a named barrier
     bool ok = true;
-    float sq_next = prm.sq[(size_t)bh * prm.group * prm.nqb + I0];
+    float sq_next = prm.sq[(size_t)qh0 * prm.nqb + I0];
     // with Q-smoothing D_i comes from global memory, also an iteration early
-    float dvec_next = QS ? prm.dvec[(size_t)bh * prm.group * prm.np + I0 * 128 + t] : 0.f;
+    float dvec_next = QS ? prm.dvec[(size_t)qh0 * prm.np + I0 * 128 + t] : 0.f;
     // (query block I, query head qh) of iteration it, and of the next, advanced without a division
-    int I = I0, qh = bh * prm.group;
+    int I = I0, qh = qh0;
     int In = I0 + 1 < prm.nqb ? I0 + 1 : I0, qhn = I0 + 1 < prm.nqb ? qh : qh + 1;
     for (int it = 0; it < n_it; ++it) {
       const uint32_t ph = it & 1;
@@ -737,8 +762,50 @@ __global__ void __launch_bounds__(384, 1)
       const size_t orow = ((size_t)bh * prm.N + key) * D;
 #pragma unroll
       for (int d = 0; d < DG; ++d) dk[d] *= prm.sm_scale;
+      const float* sdoh = prm.sdo + (size_t)bh * D;
+      // split query heads: add this CTA's dK and (scaled) dV rows to the fp32 sums; the last
+      // CTA of the key block to count reads the sums back and finishes them below
+      const size_t arow = ((size_t)bh * prm.np + key) * D + dcol;
+      bool fin = true;
+      if (prm.split > 1) {
+        if (key_ok && ok) {
+#pragma unroll
+          for (int c = 0; c < DG; c += 4) red_add_v4(prm.dkacc + arow + c, dk[c], dk[c + 1], dk[c + 2], dk[c + 3]);
+        }
+#pragma unroll 1
+        for (int c = 0; c < DG; c += 16) {
+          uint32_t v[16];
+          tmem_ld16(tmem + lane_base + cDV + dcol + c, v);
+          tmem_wait16(v);
+          if (key_ok && ok) {
+#pragma unroll
+            for (int i = 0; i < 16; i += 4) {
+              float f[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                f[e] = __uint_as_float(v[i + e]) * (sdoh[dcol + c + i + e] * (1.0f / 448.0f));
+              red_add_v4(prm.dvacc + arow + c + i, f[0], f[1], f[2], f[3]);
+            }
+          }
+        }
+        __threadfence();
+        named_bar_compute();
+        if (tid == 0) sm.last = atomicAdd(prm.kvcnt + (size_t)bh * prm.nqb + kb, 1) == prm.split - 1;
+        named_bar_compute();
+        fin = sm.last != 0;
+        if (fin) {
+          __threadfence();
+          if (key_ok) {
+#pragma unroll
+            for (int c = 0; c < DG; c += 4) {
+              const float4 a = __ldcg(reinterpret_cast<const float4*>(prm.dkacc + arow + c));
+              dk[c] = a.x, dk[c + 1] = a.y, dk[c + 2] = a.z, dk[c + 3] = a.w;
+            }
+          }
+        }
+      }
       const uint4* krow = reinterpret_cast<const uint4*>(prm.K + orow + dcol);
-      if (prm.qk_norm) {
+      if (fin && prm.qk_norm) {
         // dk = r (dk' - k' (k' . dk')), k' = RN(k r): the dot spans both groups' columns
         const float r = key_ok ? prm.kr[(size_t)bh * prm.np + key] : 0.f;
         float dot = 0.f;
@@ -767,7 +834,7 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
       }
-      if (key_ok && ok) {
+      if (fin && key_ok && ok) {
         uint4* dstk = reinterpret_cast<uint4*>(prm.dK + orow + dcol);
 #pragma unroll
         for (int c = 0; c < DG / 8; ++c) {
@@ -778,12 +845,24 @@ __global__ void __launch_bounds__(384, 1)
           dstk[c] = u;
         }
       }
-      const float* sdoh = prm.sdo + (size_t)bh * D;
 #pragma unroll
-      for (int c = 0; c < DG; c += 16) {
-        uint32_t v[16];
-        tmem_ld16(tmem + lane_base + cDV + dcol + c, v);
-        tmem_wait16(v);
+      for (int c = 0; fin && c < DG; c += 16) {
+        float f[16];
+        if (prm.split > 1) {
+          // the finished sums, already scaled
+#pragma unroll
+          for (int i = 0; i < 16; i += 4) {
+            const float4 a = key_ok ? __ldcg(reinterpret_cast<const float4*>(prm.dvacc + arow + c + i))
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+            f[i] = a.x, f[i + 1] = a.y, f[i + 2] = a.z, f[i + 3] = a.w;
+          }
+        } else {
+          uint32_t v[16];
+          tmem_ld16(tmem + lane_base + cDV + dcol + c, v);
+          tmem_wait16(v);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) f[e] = __uint_as_float(v[e]) * (sdoh[dcol + c + e] * (1.0f / 448.0f));
+        }
         if (key_ok && ok) {
           uint4* dstv = reinterpret_cast<uint4*>(prm.dV + orow + dcol + c);
 #pragma unroll
@@ -791,11 +870,7 @@ __global__ void __launch_bounds__(384, 1)
             uint4 u;
             __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int d0 = dcol + c + 8 * i + 2 * e;
-              h[e] = __floats2bfloat162_rn(__uint_as_float(v[8 * i + 2 * e]) * (sdoh[d0] * (1.0f / 448.0f)),
-                                           __uint_as_float(v[8 * i + 2 * e + 1]) * (sdoh[d0 + 1] * (1.0f / 448.0f)));
-            }
+            for (int e = 0; e < 4; ++e) h[e] = __floats2bfloat162_rn(f[8 * i + 2 * e], f[8 * i + 2 * e + 1]);
             dstv[i] = u;
           }
         }
@@ -816,7 +891,8 @@ int launch_main_t(const CUtensorMap& tk, const CUtensorMap& tq, const CUtensorMa
   auto kern = bwd_main_kernel<D, QS>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 3;
   ScopedTimer timer("bwd_main", st);
-  if (launch_pdl(kern, dim3(p.nqb * BH), dim3(384), smem, st, tk, tq, tv, tdo, tdo8, tdq, p) != cudaSuccess) return 3;
+  if (launch_pdl(kern, dim3(p.nqb * BH * p.split), dim3(384), smem, st, tk, tq, tv, tdo, tdo8, tdq, p) != cudaSuccess)
+    return 3;
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 
@@ -843,6 +919,24 @@ int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const
   auto* o = static_cast<const __nv_bfloat16*>(O);
   auto* dob = static_cast<const __nv_bfloat16*>(dO);
   const dim3 g(nb, BH);
+  // Grouped heads with too few (key block, key/value head) tiles to fill the GPU twice over
+  // split each tile's query heads over `split` CTAs (a divisor of the group); their dK and dV
+  // meet in fp32 sums.  One query head per key/value head never splits.
+  int split = 1;
+  if (group > 1) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return 3;
+    const int want = (2 * sms) / (BHk * nb);
+    for (int s = want < group ? want : group; s > 1; --s)
+      if (group % s == 0) {
+        split = s;
+        break;
+      }
+  }
+  float* kvacc = split > 1 ? reinterpret_cast<float*>(bw + BL.dkacc) : nullptr;
+  int* kvcnt = reinterpret_cast<int*>(bw + BL.kvcnt);
   {
   ScopedTimer timer("bwd_pre", st);
   if (launch_pdl(D == 128 ? bwd_pre_kernel<128> : bwd_pre_kernel<64>, g, dim3(kPreThreads), 0, st, o, O32, dob, LSE, N,
@@ -850,7 +944,8 @@ int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const
       launch_pdl(bwd_docomb_kernel, dim3(BHk), dim3(128), 0, st, (const float*)dopart, D, nb, group, sdo) !=
           cudaSuccess ||
       launch_pdl(D == 128 ? bwd_do8_kernel<128> : bwd_do8_kernel<64>, g, dim3(kPreThreads), 0, st, dob, N,
-                 (const float*)sdo, group, do8t, dqacc) != cudaSuccess)
+                 (const float*)sdo, group, do8t, dqacc, kvacc, kvcnt, (size_t)(BL.dvacc - BL.dkacc) / 4) !=
+          cudaSuccess)
     return 3;
   }
   if (cudaGetLastError() != cudaSuccess) return 3;
@@ -883,6 +978,10 @@ int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const
   p.bias = biasv;
   p.dvec = dvec;
   p.dsb = q_smooth ? reinterpret_cast<const float*>(w + QL.dsb) : nullptr;
+  p.split = split;
+  p.dkacc = reinterpret_cast<float*>(bw + BL.dkacc);
+  p.dvacc = reinterpret_cast<float*>(bw + BL.dvacc);
+  p.kvcnt = kvcnt;
   p.qmean = q_smooth ? reinterpret_cast<const float*>(w + QL.qmean) : nullptr;
   p.K = static_cast<const __nv_bfloat16*>(K);
   p.kr = reinterpret_cast<const float*>(w + QL.kr);

@@ -48,7 +48,7 @@ inline QuantWs quant_ws_layout(int B, int H, int N, int D, int Hkv = 0, bool qs 
 }
 
 struct BwdWs {
-  size_t sync, dvec, bias, do8t, sdo, dopart, dqacc, total;
+  size_t sync, dvec, bias, do8t, sdo, dopart, dqacc, dkacc, dvacc, kvcnt, total;
   int np;
 };
 
@@ -69,6 +69,12 @@ inline BwdWs bwd_ws_layout(int B, int H, int N, int D, int Hkv = 0) {
   L.sdo = o;    o = align256(o + bk * D * 4);
   L.dopart = o; o = align256(o + bh * nb * D * 4);
   L.dqacc = o;  o = align256(o + bh * np * D * 4);
+  // grouped heads: fp32 sums of dK and dV [Bk, Np, D] for key blocks whose query heads are
+  // split over several CTAs, and a counter per (key/value head, key block)
+  const bool grouped = bk < bh;
+  L.dkacc = o;  o = align256(o + (grouped ? bk * np * D * 4 : 0));
+  L.dvacc = o;  o = align256(o + (grouped ? bk * np * D * 4 : 0));
+  L.kvcnt = o;  o = align256(o + (grouped ? bk * nb * 4 : 0));
   L.total = o;
   L.np = np;
   return L;
