@@ -320,6 +320,52 @@ def run_ours(args, w):
     ktimes = {name: sa.sage_attn_timer_read(name) for name in ("quantize", "fwd", "bwd_pre", "bwd_main", "bwd_dq")}
 
     ops = w.ops()
+
+    # ---- the same shape through grouped key/value heads and through Q-smoothing (not part of
+    # `value`): median of 20 steps, L2 flushed before each
+    def time_variant(fn, ws_status):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for i in range(20):
+            flush.fill_(float(i))
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        if sa.get_status(ws_status) != sa.SAGE_OK:
+            raise SystemExit("device status not ok after a variant's steps")
+        ms = sorted(ts)[len(ts) // 2]
+        return {"ms_per_step": ms, "tops": ops["fwd_bwd"] / (ms * 1e-3) / 1e12}
+
+    variants = {}
+    for hkv in sorted({H // 4, 1}, reverse=True):
+        if hkv < 1 or H % hkv or hkv == H:
+            continue
+        kg, vg = t["k"][:, :hkv].contiguous(), t["v"][:, :hkv].contiguous()
+        wsg, bwsg = sa.alloc_ws(B, H, N, D, dev, hkv), sa.alloc_bwd_ws(B, H, N, D, dev, hkv)
+        dkg, dvg = torch.empty_like(kg), torch.empty_like(vg)
+
+        def gstep():
+            sa.quantize(t["q"], kg, vg, w.qk_norm, w.k_smooth, ws=wsg)
+            sa.forward(wsg, B, H, N, D, w.causal, w.sm_scale, o=o, lse=lse, device=dev, hkv=hkv)
+            sa.backward(t["q"], kg, vg, o, lse, t["do"], wsg, w.causal, w.qk_norm, w.k_smooth, w.sm_scale,
+                        bwd_ws=bwsg, dq=dq, dk=dkg, dv=dvg)
+        variants[f"kv_heads_{hkv}"] = dict(time_variant(gstep, wsg), query_heads_per_kv_head=H // hkv)
+        del wsg, bwsg, kg, vg, dkg, dvg
+    wsq = sa.alloc_ws(B, H, N, D, dev, None, True)
+
+    def qstep():
+        sa.quantize(t["q"], t["k"], t["v"], w.qk_norm, w.k_smooth, ws=wsq, q_smooth=True)
+        sa.forward(wsq, B, H, N, D, w.causal, w.sm_scale, o=o, lse=lse, device=dev, q_smooth=True)
+        sa.backward(t["q"], t["k"], t["v"], o, lse, t["do"], wsq, w.causal, w.qk_norm, w.k_smooth, w.sm_scale,
+                    bwd_ws=bws, dq=dq, dk=dk, dv=dv, q_smooth=True)
+    variants["q_smooth"] = time_variant(qstep, wsq)
+    del wsq
+
     tmax = total_ms
     if dist:
         tt = torch.tensor([total_ms], device=dev)
@@ -394,6 +440,9 @@ def run_ours(args, w):
         "fwd_bwd_frac_fp8_peak": value / world / fp8_peak,
         "kernel_ms_per_step": {n: ms / max(1, c) for n, (ms, c) in ktimes.items()},
         "kernel_ms_note": "per launch group, from 20 untimed steps with every group bracketed by events",
+        "variants": variants,
+        "variants_note": "the workload's shape with fewer key/value heads (grouped-query attention) and with "
+                         "Q-smoothing: quantize + forward + backward, median of 20 steps, L2 flushed",
         "wall_s": wall,
     }
 
