@@ -3,7 +3,7 @@
 on GB300: causal-adjusted fwd+bwd TOPS and the fraction of the tensor peak.
 
 One step = the whole hot path on one batch: sage_attn_quantize, sage_attn_fwd,
-sage_attn_bwd (9 kernel launches).  Inputs are synthetic, seeded, resident in
+sage_attn_bwd (8 kernel launches).  Inputs are synthetic, seeded, resident in
 HBM; L2 is flushed (256 MiB write) between timed steps, outside the events.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -47,6 +47,17 @@ def parse():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
+
+
+def max_over_ranks(v: float, dist, device) -> float:
+    """The largest of every rank's v (v itself without a process group): the job's time is
+    its slowest rank's."""
+    if dist is None:
+        return v
+    import torch
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 def measured_peaks():
@@ -366,11 +377,7 @@ def run_ours(args, w):
     variants["q_smooth"] = time_variant(qstep, wsq)
     del wsq
 
-    tmax = total_ms
-    if dist:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        tmax = float(tt.item())
+    tmax = max_over_ranks(total_ms, dist, dev)
     value = world * ops["fwd_bwd"] * K / (tmax * 1e-3) / 1e12
 
     # ---- end to end through the public API, host buffers, copies inside the timed region:
@@ -398,11 +405,7 @@ def run_ours(args, w):
         raise SystemExit("device status not ok after the end-to-end steps")
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = sum(v.numel() * v.element_size() for v in pin_out.values())
-    e2e_total = sum(e2e_ms)
-    if dist:
-        tt = torch.tensor([e2e_total], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_total = float(tt.item())
+    e2e_total = max_over_ranks(sum(e2e_ms), dist, dev)
     e2e_value = world * ops["fwd_bwd"] * Ke / (e2e_total * 1e-3) / 1e12
 
     # ---- roofline of the dominant kernel (backward main: the five backward matmuls)
