@@ -47,6 +47,25 @@ int launch_selftest_wait(void* ws, unsigned long long budget_ns, cudaStream_t st
 }
 }  // namespace sage
 
+namespace {
+// the device pointers of a quantize workspace's sections (qmean, dsb: Q-smoothing layouts only)
+void fill_views(uint8_t* w, const sage::QuantWs& L, bool qs, sage_ws_views* v) {
+  v->qc = w + L.qc;
+  v->kc = w + L.kc;
+  v->v8t = w + L.v8t;
+  v->sq = reinterpret_cast<float*>(w + L.sq);
+  v->sk = reinterpret_cast<float*>(w + L.sk);
+  v->sv = reinterpret_cast<float*>(w + L.sv);
+  v->kmean = reinterpret_cast<float*>(w + L.kmean);
+  v->qr = reinterpret_cast<float*>(w + L.qr);
+  v->kr = reinterpret_cast<float*>(w + L.kr);
+  v->status = reinterpret_cast<int*>(w + L.status);
+  v->n_pad = L.np;
+  v->qmean = qs ? reinterpret_cast<float*>(w + L.qmean) : nullptr;
+  v->dsb = qs ? reinterpret_cast<float*>(w + L.dsb) : nullptr;
+}
+}  // namespace
+
 extern "C" {
 
 size_t sage_attn_ws_bytes(int B, int H, int N, int D) {
@@ -151,24 +170,6 @@ int sage_attn_gqa_bwd(const void* Q, const void* K, const void* V, const void* O
                           k_smooth != 0, resolve_scale(sm_scale, D), static_cast<cudaStream_t>(stream), nullptr,
                           Hkv);
 }
-
-namespace {
-void fill_views(uint8_t* w, const sage::QuantWs& L, bool qs, sage_ws_views* v) {
-  v->qc = w + L.qc;
-  v->kc = w + L.kc;
-  v->v8t = w + L.v8t;
-  v->sq = reinterpret_cast<float*>(w + L.sq);
-  v->sk = reinterpret_cast<float*>(w + L.sk);
-  v->sv = reinterpret_cast<float*>(w + L.sv);
-  v->kmean = reinterpret_cast<float*>(w + L.kmean);
-  v->qr = reinterpret_cast<float*>(w + L.qr);
-  v->kr = reinterpret_cast<float*>(w + L.kr);
-  v->status = reinterpret_cast<int*>(w + L.status);
-  v->n_pad = L.np;
-  v->qmean = qs ? reinterpret_cast<float*>(w + L.qmean) : nullptr;
-  v->dsb = qs ? reinterpret_cast<float*>(w + L.dsb) : nullptr;
-}
-}  // namespace
 
 size_t sage_attn_qs_ws_bytes(int B, int H, int Hkv, int N, int D) {
   if (!shape_ok(B, H, N, D) || !groups_ok(H, Hkv)) return 0;
