@@ -18,6 +18,7 @@ import numpy as np
 
 QM_QK, QM_V, QM_P, QM_DO, QM_DS, QM_F32 = 1, 2, 4, 8, 16, 32
 QM_ALL = 63
+QM_FP4 = 64  # NVFP4 for V and P (with QM_ALL: the FP4 variant of the scheme)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "sage_oracle.c")
@@ -67,6 +68,9 @@ def lib():
             L.sage_oracle_e4m3.restype = ctypes.c_double
             L.sage_oracle_e4m3.argtypes = [ctypes.c_double]
             L.sage_oracle_e4m3_f32.argtypes = [fp, fp, ctypes.c_long]
+            L.sage_oracle_e2m1.restype = ctypes.c_double
+            L.sage_oracle_e2m1.argtypes = [ctypes.c_double]
+            L.sage_oracle_e2m1_f64.argtypes = [dp, dp, ctypes.c_long]
             L.sage_oracle_to_bf16.argtypes = [dp, dp, ctypes.c_long]
             L.sage_oracle_quantize.argtypes = [i, i, dp, dp, dp, i, i, i] + [dp] * 11
             L.sage_oracle_fwd.argtypes = [i, i, i, ctypes.c_double, i] + [dp] * 6 + [dp, fp, dp]
@@ -96,6 +100,14 @@ def e4m3(x: np.ndarray) -> np.ndarray:
     x = np.ascontiguousarray(x, dtype=np.float32)
     y = np.empty_like(x)
     lib().sage_oracle_e4m3_f32(_f(x), _f(y), x.size)
+    return y
+
+
+def e2m1(x: np.ndarray) -> np.ndarray:
+    """e2m1 (FP4) rounding (nearest, ties to the even mantissa, saturating at 6)."""
+    x = _c64(x)
+    y = np.empty_like(x)
+    lib().sage_oracle_e2m1_f64(_d(x), _d(y), x.size)
     return y
 
 

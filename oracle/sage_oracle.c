@@ -31,7 +31,9 @@
  *
  * Quantizer mask (qmask): each bit switches one quantizer on; all bits off
  * turns the same code into exact fp64 attention, which the tests compare with
- * textbook attention and finite differences.
+ * textbook attention and finite differences.  QM_FP4 selects the NVFP4 variant
+ * (P and V in block-scaled FP4 instead of e4m3; "Attn-QAT" trains attention in
+ * FP4 and recomputes P in the backward in the forward's precision, principle 1).
  *
  * Parity status: every function below is pinned by the CPU tests (e4m3 rounding
  * exhaustively against a library cast; the quantizers-off path against library
@@ -50,6 +52,7 @@
 #define QM_DO 8   /* e4m3 codes for dO (backward dV) */
 #define QM_DS 16  /* INT8 codes for dS (backward dQ, dK) */
 #define QM_F32 32 /* fp32 rounding of the stored intermediate values */
+#define QM_FP4 64 /* NVFP4 in place of e4m3 for V and P (the forward PV, P^ in the backward) */
 
 #define QBLK 128  /* Q tokens per INT8 scale */
 #define KBLK 64   /* K tokens per INT8 scale */
@@ -76,6 +79,25 @@ double sage_oracle_e4m3(double x)
     double r = nearbyint(a / quantum) * quantum;
     if (r > 448.0) r = 448.0;
     return copysign(r, x);
+}
+
+/* e2m1 (FP4) rounding: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 (one exponent pair of bits,
+ * one mantissa bit, subnormal 0.5); round to nearest with ties to the even mantissa,
+ * saturating at 6.  The spacing is 0.5 below 2, 1 in [2, 4) and 2 from 4, and the parity
+ * of the count of spacings is the mantissa bit. */
+double sage_oracle_e2m1(double x)
+{
+    double a = fabs(x);
+    if (a != a) return x;
+    double quantum = a < 2.0 ? 0.5 : (a < 4.0 ? 1.0 : 2.0);
+    double r = nearbyint(a / quantum) * quantum;
+    if (r > 6.0) r = 6.0;
+    return copysign(r, x);
+}
+
+void sage_oracle_e2m1_f64(const double *x, double *y, long n)
+{
+    for (long i = 0; i < n; ++i) y[i] = sage_oracle_e2m1(x[i]);
 }
 
 void sage_oracle_e4m3_f32(const float *x, float *y, long n)
@@ -145,6 +167,50 @@ static void channel_e4m3(const double *x, int N, int D, int on, int f32,
             codes[i] = a > 0.0 ? sage_oracle_e4m3(r32(f32, x[i] / s)) : 0.0;
         }
     }
+}
+
+/* NVFP4 (the block-scaled FP4 that Blackwell's tensor cores take; "ThriftAttention"
+ * (gist.science summary), Methodology step 2, names it for the low-precision path, and the
+ * Attn-QAT summary trains attention in FP4): e2m1 codes, one e4m3 scale per 16 consecutive
+ * values along the contraction axis, and one fp32 scale for the tensor.
+ *
+ * V (contracted over keys in PV): per head, g = RN32(max|V| / (448 * 6)); per channel d and
+ * block of 16 tokens, s = e4m3(RN32(amax / RN32(6 g))); code = e2m1(RN32(v / RN32(s g))).
+ * vx receives the values the matmul sees, code * s * g, and sv = 1 (so that the forward's
+ * O = A sv / (448 l) holds with A summing 448 P^ times them). */
+static void channel_nvfp4(const double *x, int N, int D, int f32, double *vx, double *sv)
+{
+    double amax = 0.0;
+    for (size_t i = 0; i < (size_t)N * D; ++i) amax = fmax(amax, fabs(x[i]));
+    double g = r32(f32, amax / 2688.0);
+    double g6 = r32(f32, 6.0 * g);
+    for (int d = 0; d < D; ++d) {
+        sv[d] = 1.0;
+        for (int t0 = 0; t0 < N; t0 += 16) {
+            int t1 = t0 + 16 < N ? t0 + 16 : N;
+            double a = 0.0;
+            for (int t = t0; t < t1; ++t) a = fmax(a, fabs(x[(size_t)t * D + d]));
+            double sb = (a > 0.0 && g6 > 0.0) ? sage_oracle_e4m3(r32(f32, a / g6)) : 0.0;
+            double sg = r32(f32, sb * g);
+            for (int t = t0; t < t1; ++t) {
+                size_t i = (size_t)t * D + d;
+                vx[i] = sg > 0.0 ? sage_oracle_e2m1(r32(f32, x[i] / sg)) * sb * g : 0.0;
+            }
+        }
+    }
+}
+
+/* P in NVFP4 along keys: the values p[k] (k < n <= 16: one block of a row, P or the
+ * forward's p~, both <= 1) take the static tensor scale 1 / (448 * 6): with
+ * y = RN32(2688 p), s = e4m3(RN32(max y / 6)), code = e2m1(RN32(y / s)).  p8[k] receives
+ * 448 P^ = code * s / 6, the scale the e4m3 path's codes carry. */
+static void p_block_nvfp4(const double *p, int n, int f32, double *p8)
+{
+    double ym = 0.0;
+    for (int k = 0; k < n; ++k) ym = fmax(ym, r32(f32, 2688.0 * p[k]));
+    double sb = ym > 0.0 ? sage_oracle_e4m3(r32(f32, ym / 6.0)) : 0.0;
+    for (int k = 0; k < n; ++k)
+        p8[k] = sb > 0.0 ? sage_oracle_e2m1(r32(f32, r32(f32, 2688.0 * p[k]) / sb)) * sb / 6.0 : 0.0;
 }
 
 /* Per-token L2 normalisation: sigma = sum x^2 (fp64, exact for bf16 inputs),
@@ -266,7 +332,10 @@ static int quantize_head(int N, int D, const double *Q, const double *K, const d
         block_int8(qn, N, D, QBLK, (qmask & QM_QK) != 0, f32, qx, sq);
     }
     block_int8(ks, N, D, KBLK, (qmask & QM_QK) != 0, f32, kx, sk);
-    channel_e4m3(V, N, D, (qmask & QM_V) != 0, f32, vx, sv);
+    if (qmask & QM_FP4)
+        channel_nvfp4(V, N, D, f32, vx, sv);
+    else
+        channel_e4m3(V, N, D, (qmask & QM_V) != 0, f32, vx, sv);
     free(ks);
     return 0;
 }
@@ -353,7 +422,8 @@ static int fwd_head(int N, int D, int causal, double sm_scale, int qmask,
 #pragma omp parallel
     {
         double *A = (double *)malloc(sizeof(double) * D);
-        double *s2 = (double *)malloc(sizeof(double) * 2 * TILE);  /* x, f per key (logit_parts) */
+        /* x, f per key (logit_parts); with NVFP4 also p~ and 448 P^ per key */
+        double *s2 = (double *)malloc(sizeof(double) * 4 * TILE);
         if (!A || !s2) {
 #pragma omp atomic write
             err = 2;
@@ -382,13 +452,29 @@ static int fwd_head(int N, int D, int causal, double sm_scale, int qmask,
                 double corr = (m == -INFINITY) ? 0.0 : exp2(m - mn);
                 l *= corr;
                 for (int d = 0; d < D; ++d) A[d] *= corr;
-                for (int j = j0; j < j1; ++j) {
-                    double t = r32(f32, acc[j - j0] * cj[j - j0] - mn);
-                    double pt = r32(f32, exp2(t));
-                    double p8 = qp ? sage_oracle_e4m3(r32(f32, 448.0 * pt)) : 448.0 * pt;
-                    l += pt;
-                    const double *vrow = vx + (size_t)j * D;
-                    for (int d = 0; d < D; ++d) A[d] += p8 * vrow[d];
+                if (qmask & QM_FP4) {
+                    /* p~ of the tile's keys, then NVFP4 per block of 16 keys (blocks start at
+                     * multiples of 16; keys past the causal limit are not in any block) */
+                    double *ptv = s2 + 2 * TILE, *p8v = s2 + 3 * TILE;
+                    for (int j = j0; j < j1; ++j) {
+                        ptv[j - j0] = r32(f32, exp2(r32(f32, acc[j - j0] * cj[j - j0] - mn)));
+                        l += ptv[j - j0];
+                    }
+                    for (int b0 = j0; b0 < j1; b0 += 16)
+                        p_block_nvfp4(ptv + (b0 - j0), (b0 + 16 < j1 ? b0 + 16 : j1) - b0, f32, p8v + (b0 - j0));
+                    for (int j = j0; j < j1; ++j) {
+                        const double *vrow = vx + (size_t)j * D;
+                        for (int d = 0; d < D; ++d) A[d] += p8v[j - j0] * vrow[d];
+                    }
+                } else {
+                    for (int j = j0; j < j1; ++j) {
+                        double t = r32(f32, acc[j - j0] * cj[j - j0] - mn);
+                        double pt = r32(f32, exp2(t));
+                        double p8 = qp ? sage_oracle_e4m3(r32(f32, 448.0 * pt)) : 448.0 * pt;
+                        l += pt;
+                        const double *vrow = vx + (size_t)j * D;
+                        for (int d = 0; d < D; ++d) A[d] += p8 * vrow[d];
+                    }
                 }
                 m = mn;
             }
@@ -422,15 +508,28 @@ static double bwd_tile(int I, int J, int N, int D, int causal, double alpha, int
     double amax = 0.0;
     const double *dsb_row = dsb ? dsb + (size_t)I * N : NULL;
     for (int i = i0; i < i1; ++i) {
+        /* the row's P on this key block (0 past the causal limit), then 448 P^: e4m3 codes, or
+         * NVFP4 per 16 keys as in the forward */
+        double Pr[KBLK], p8r[KBLK];
+        for (int j = j0; j < j1; ++j) {
+            if (causal && j > i) { Pr[j - j0] = 0.0; continue; }
+            double c;
+            double x = logit_parts(dot(qx + (size_t)i * D, kx + (size_t)j * D, D), sq[I], sk[J], alpha, f32,
+                                   dsb_row, j, &c);
+            Pr[j - j0] = r32(f32, exp2(r32(f32, x * c - lse2[i])));
+        }
+        if (qmask & QM_FP4) {
+            for (int b0 = j0; b0 < j1; b0 += 16)
+                p_block_nvfp4(Pr + (b0 - j0), (b0 + 16 < j1 ? b0 + 16 : j1) - b0, f32, p8r + (b0 - j0));
+        } else {
+            for (int j = j0; j < j1; ++j)
+                p8r[j - j0] = (qmask & QM_P) ? sage_oracle_e4m3(r32(f32, 448.0 * Pr[j - j0])) : 448.0 * Pr[j - j0];
+        }
         for (int j = j0; j < j1; ++j) {
             double *pp = p8t + (size_t)(i - i0) * KBLK + (j - j0);
             double *dd = ds8t + (size_t)(i - i0) * KBLK + (j - j0);
             if (causal && j > i) { *pp = 0.0; *dd = 0.0; continue; }
-            double c;
-            double x = logit_parts(dot(qx + (size_t)i * D, kx + (size_t)j * D, D), sq[I], sk[J], alpha, f32,
-                                   dsb_row, j, &c);
-            double P = r32(f32, exp2(r32(f32, x * c - lse2[i])));
-            double p8 = (qmask & QM_P) ? sage_oracle_e4m3(r32(f32, 448.0 * P)) : 448.0 * P;
+            double p8 = p8r[j - j0];
             double dp = 0.0;
             for (int d = 0; d < D; ++d) dp += dO[(size_t)i * D + d] * V[(size_t)j * D + d];
             double ds = r32(f32, (p8 / 448.0) * (dp - Dv[i]));

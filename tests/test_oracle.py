@@ -527,3 +527,122 @@ def test_q_smoothing_lowers_the_error_of_offset_queries():
         for n in ("O64", "dK64"):
             assert rel(smooth[n], ex[n]) < 0.5 * rel(plain[n], ex[n]), (seed, n)
         assert rel(smooth["dQ64"], ex["dQ64"]) <= rel(plain["dQ64"], ex["dQ64"]), seed
+
+
+# ---------------------------------------------------------------- NVFP4 (the FP4 variant)
+
+def _e2m1_brute(x):
+    """Nearest value of the e2m1 magnitude grid; a tie takes the value whose mantissa bit is
+    0 (0, 1, 2, 4); beyond 6, 6."""
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    even = {0.0, 1.0, 2.0, 4.0}
+    out = np.empty_like(x)
+    for i, v in enumerate(x):
+        a = abs(v)
+        d = np.abs(grid - a)
+        best = grid[d == d.min()]
+        r = best[0] if len(best) == 1 else [b for b in best if b in even][0]
+        out[i] = math.copysign(min(r, 6.0), v)
+    return out
+
+
+def test_e2m1_rounding_against_the_grid():
+    """Every multiple of 1/128 in [-8, 8] (all midpoints included) and random values: the
+    oracle's arithmetic rounding equals the nearest-grid-value definition."""
+    x = np.concatenate([np.arange(-1024, 1025) / 128.0, np.random.default_rng(60).normal(0, 3, 4000)])
+    np.testing.assert_array_equal(orc.e2m1(x), _e2m1_brute(x))
+
+
+def _nvfp4_exact_values(rng, N, D, m):
+    """Values that NVFP4 holds exactly: per (channel, 16-token block) e2m1 grid values times
+    2^k (k per block, the block's largest magnitude 6 * 2^k), the tensor's largest 2688 * 2^m."""
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    v = rng.choice(grid, size=(N, D)) * rng.choice([-1.0, 1.0], size=(N, D))
+    for t0 in range(0, N, 16):
+        v[t0, :] = 6.0  # every block's largest magnitude is 6 before its power of two
+    k = rng.integers(-6, 3, size=(N // 16, D))
+    v *= np.repeat(2.0 ** k, 16, axis=0)
+    v[0, 0] = 2688.0 * 2.0 ** m  # the tensor scale becomes 2^m; its block's scale is 448
+    v[1:16, 0] = rng.choice(grid, size=15) * 448.0 * 2.0 ** m
+    return v
+
+
+def test_nvfp4_v_keeps_representable_values_and_its_block_axis():
+    """V whose 16-token blocks (per channel) are e2m1 values times a power of two per block,
+    with the head's largest |V| = 2688 * 2^m: the tensor scale is 2^m, every block scale is
+    exact, and the quantized V equals V.  The blocks' powers of two differ along tokens, so
+    blocks taken along another axis, or one scale per channel, would not reproduce it."""
+    rng = np.random.default_rng(61)
+    N, D = 64, 64
+    v = _nvfp4_exact_values(rng, N, D, -4)
+    q, k = _rand(rng, N, D), _rand(rng, N, D)
+    z = orc.quantize(q, k, v, False, True, qmask=orc.QM_ALL | orc.QM_FP4)
+    np.testing.assert_array_equal(z["vx"], v)
+    assert np.all(z["sv"] == 1.0)
+    # generic values: each value within one e2m1 half-spacing (at most 1) of its block's step
+    w = _rand(rng, N, D)
+    zw = orc.quantize(q, k, w, False, True, qmask=orc.QM_ALL | orc.QM_FP4)
+    blk = np.abs(w).reshape(N // 16, 16, D).max(axis=1)
+    step = np.repeat(blk / 6.0 * (1 + 1.0 / 16), 16, axis=0)
+    assert np.all(np.abs(zw["vx"] - w) <= step * 1.0 + 1e-12)
+    assert np.mean(zw["vx"] == 0.0) < 0.2
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_nvfp4_uniform_rows_reduce_to_means(causal):
+    """Identical keys: every visible logit of a row is equal, so p~ = 1 on each of them, its
+    block scale is 448 and its code 6: P^ is exact.  With V exactly representable, O is the
+    mean of V over the visible keys (with causal masking, the running mean) to rounding."""
+    rng = np.random.default_rng(62)
+    N, D = 64, 64
+    v = _nvfp4_exact_values(rng, N, D, -3)
+    q = _rand(rng, N, D)
+    k = np.repeat(_rand(rng, 1, D), N, axis=0)
+    r = orc.run_head(q, k, v, _rand(rng, N, D), causal, 0.125, qmask=orc.QM_FP4 | orc.QM_F32,
+                     backward_pass=False)
+    want = np.cumsum(v, axis=0) / np.arange(1, N + 1)[:, None] if causal else np.repeat(v.mean(0, keepdims=True), N, 0)
+    np.testing.assert_allclose(r["O64"], want, rtol=1e-12, atol=1e-12)
+
+
+def test_nvfp4_backward_exact_when_p_is_representable():
+    """Non-causal, identical keys, 64 keys: P = 1/64 everywhere, which NVFP4 holds exactly
+    (block scale e4m3(448/64) = 7, code 6), and V is representable.  The FP4 variant (only
+    that quantizer on) then computes what the unquantized path computes: O, LSE, dK, dV agree
+    with it to fp32 rounding.  (The backward's P is 2^-6 (1 + ~1e-6) from the fp32 LSE, which
+    the block scale rounds back to 2^-6; dQ, zero in exact arithmetic for identical keys, is
+    all cancellation here and is left out.)"""
+    rng = np.random.default_rng(63)
+    N, D = 64, 64
+    v = _nvfp4_exact_values(rng, N, D, -3)
+    q, do = _rand(rng, N, D), _rand(rng, N, D)
+    k = np.repeat(_rand(rng, 1, D), N, axis=0)
+    r = orc.run_head(q, k, v, do, False, 0.125, k_smooth=False, qmask=orc.QM_FP4 | orc.QM_F32)
+    p = orc.run_head(q, k, v, do, False, 0.125, k_smooth=False, qmask=orc.QM_F32)
+    for name in ("O64", "LSE64", "dK64", "dV64"):
+        scale = float(np.abs(p[name]).max())
+        assert float(np.abs(r[name] - p[name]).max()) <= 1e-5 * scale, name
+    # and a P that NVFP4 cannot hold (1/48: block scale 9.333 rounds to 9) moves dV by percents
+    r48 = orc.run_head(q[:48], k[:48], v[:48], do[:48], False, 0.125, k_smooth=False, qmask=orc.QM_FP4 | orc.QM_F32)
+    p48 = orc.run_head(q[:48], k[:48], v[:48], do[:48], False, 0.125, k_smooth=False, qmask=orc.QM_F32)
+    assert np.linalg.norm(r48["dV64"] - p48["dV64"]) > 1e-3 * np.linalg.norm(p48["dV64"])
+
+
+def test_nvfp4_p_blocks_follow_the_keys():
+    """Keys 0-15 with large logits and keys 16-31 with logits 10 lower, V = 1 on the second
+    block only: that block's own scale keeps its small P (about 2^-10 of the first block's),
+    so O's channel stays within a few percent of exact attention; one scale for the whole row
+    would flush those P to zero."""
+    rng = np.random.default_rng(64)
+    N, D = 32, 64
+    q = np.zeros((N, D))
+    q[:, 0] = 1.0
+    k = np.zeros((N, D))
+    k[:16, 0] = 80.0
+    k[16:, 0] = 80.0 - 10.0 / (0.125 * math.log2(math.e))
+    v = np.zeros((N, D))
+    v[16:, 1] = 1.0
+    ex = orc.run_head(q, k, v, _rand(rng, N, D), False, 0.125, k_smooth=False, qmask=0, backward_pass=False)
+    r = orc.run_head(q, k, v, _rand(rng, N, D), False, 0.125, k_smooth=False, qmask=orc.QM_FP4 | orc.QM_F32,
+                     backward_pass=False)
+    assert ex["O64"][0, 1] > 1e-4
+    np.testing.assert_allclose(r["O64"][:, 1], ex["O64"][:, 1], rtol=0.05)
