@@ -10,6 +10,7 @@ quantizer mask selects which quantizers are on (QM_ALL = the low-bit scheme,
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import subprocess
 import threading
@@ -71,6 +72,9 @@ def lib():
             L.sage_oracle_e2m1.restype = ctypes.c_double
             L.sage_oracle_e2m1.argtypes = [ctypes.c_double]
             L.sage_oracle_e2m1_f64.argtypes = [dp, dp, ctypes.c_long]
+            L.sage_oracle_fp16_f64.argtypes = [dp, dp, ctypes.c_long]
+            L.sage_oracle_fwd_thrift.argtypes = ([i, i, i, ctypes.c_double, i] + [dp] * 6 +
+                                                 [ctypes.POINTER(ctypes.c_ubyte)] + [dp] * 3 + [dp, fp, dp])
             L.sage_oracle_to_bf16.argtypes = [dp, dp, ctypes.c_long]
             L.sage_oracle_quantize.argtypes = [i, i, dp, dp, dp, i, i, i] + [dp] * 11
             L.sage_oracle_fwd.argtypes = [i, i, i, ctypes.c_double, i] + [dp] * 6 + [dp, fp, dp]
@@ -111,6 +115,42 @@ def e2m1(x: np.ndarray) -> np.ndarray:
     return y
 
 
+def fp16(x: np.ndarray) -> np.ndarray:
+    """fp16 rounding (nearest even) as the oracle forms it."""
+    x = _c64(x)
+    y = np.empty_like(x)
+    lib().sage_oracle_fp16_f64(_d(x), _d(y), x.size)
+    return y
+
+
+def thrift_select(q, k, causal, budget) -> np.ndarray:
+    """ThriftAttention's selection ("ThriftAttention" (gist.science summary), Methodology
+    step 1): the importance of the pair (128-query block I, 128-key tile J) is the dot
+    product of the blocks' token means, qbar_I . kbar_J, over the raw inputs; the
+    ceil(budget * pairs) most important of the pairs the mask lets through (causal: J <= I)
+    are promoted, ties taken in (I, J) order.  Returns uint8 [nI, nJ], 1 = promoted."""
+    q, k = _c64(q), _c64(k)
+    N = q.shape[0]
+    nb = -(-N // 128)
+    qm = np.stack([q[b * 128:(b + 1) * 128].mean(0) for b in range(nb)])
+    km = np.stack([k[b * 128:(b + 1) * 128].mean(0) for b in range(nb)])
+    score = qm @ km.T
+    vis = np.tril(np.ones((nb, nb), dtype=bool)) if causal else np.ones((nb, nb), dtype=bool)
+    idx = np.flatnonzero(vis.ravel())
+    n = int(math.ceil(budget * idx.size - 1e-12))
+    order = idx[np.lexsort((idx, -score.ravel()[idx]))]
+    sel = np.zeros(nb * nb, dtype=np.uint8)
+    sel[order[:n]] = 1
+    return sel.reshape(nb, nb)
+
+
+def thrift_inputs(qz: dict, v) -> dict:
+    """The high-precision path's operands: the softmax's q' and k'' (the smoothed keys,
+    RN32(k' - kmean), which K's quantizer takes) and V, rounded to fp16."""
+    ks = (qz["kn"] - qz["kmean"]).astype(np.float32).astype(np.float64)
+    return {"qh": fp16(qz["qn"]), "kh": fp16(ks), "vh": fp16(_c64(v))}
+
+
 def to_bf16(x: np.ndarray) -> np.ndarray:
     """fp64 -> fp32 -> bf16 (both nearest even), returned as float64 values."""
     x = _c64(x)
@@ -142,15 +182,23 @@ def quantize(q, k, v, qk_norm, k_smooth, qmask=QM_ALL, q_smooth=False) -> dict:
     return o
 
 
-def forward(qz: dict, causal, sm_scale, qmask=QM_ALL) -> dict:
-    """One head's forward; with Q-smoothing when qz carries "dsb"."""
+def forward(qz: dict, causal, sm_scale, qmask=QM_ALL, thrift=None) -> dict:
+    """One head's forward; with Q-smoothing when qz carries "dsb".  thrift: ThriftAttention's
+    mixed precision, {"sel": thrift_select(...), **thrift_inputs(...)}."""
     N, D = qz["qx"].shape
     O64 = np.zeros((N, D))
     O32 = np.zeros((N, D), dtype=np.float32)
     L = np.zeros(N)
     args = [N, D, int(causal), float(sm_scale), int(qmask), _d(qz["qx"]), _d(qz["sq"]), _d(qz["kx"]),
             _d(qz["sk"]), _d(qz["vx"]), _d(qz["sv"])]
-    if "dsb" in qz:
+    if thrift is not None:
+        if "dsb" in qz:
+            raise ValueError("ThriftAttention is not combined with Q-smoothing")
+        sel = np.ascontiguousarray(thrift["sel"], dtype=np.uint8)
+        th = {n: _c64(thrift[n]) for n in ("qh", "kh", "vh")}
+        rc = lib().sage_oracle_fwd_thrift(*args, sel.ctypes.data_as(ctypes.POINTER(ctypes.c_ubyte)),
+                                          _d(th["qh"]), _d(th["kh"]), _d(th["vh"]), _d(O64), _f(O32), _d(L))
+    elif "dsb" in qz:
         rc = lib().sage_oracle_fwd_qs(*args, _d(qz["dsb"]), _d(O64), _f(O32), _d(L))
     else:
         rc = lib().sage_oracle_fwd(*args, _d(O64), _f(O32), _d(L))

@@ -373,17 +373,60 @@ static inline double qk_factor(double sqI, double skJ, double alpha, int f32)
  * and u_ij alpha plays the part of acc_ij c above (alpha = RN32(sm_scale log2 e)).
  * Outputs O64 [N, D], O32 [N, D] (float), LSE64 [N].
  */
+/* ThriftAttention's promoted tiles ("ThriftAttention" (gist.science summary), Methodology
+ * steps 1-2): sel[I * nkt + J] != 0 computes the pair (128-query block I, 128-key tile J) in
+ * the high-precision path from qh, kh, vh (the softmax's q', k'' and V rounded to fp16):
+ * x = RN32(qh . kh) (fp16 products, one rounding of the sum), the log2 logit RN32(x alpha),
+ * P16 = fp16(p~) times vh into an fp32 accumulator of its own; the other tiles take the
+ * low-bit path; both merge in the one online softmax (shared m and l). */
+struct thrift {
+    const unsigned char *sel;
+    int nkt;
+    const double *qh, *kh, *vh;
+};
+
 static int fwd_head(int N, int D, int causal, double sm_scale, int qmask,
                     const double *qx, const double *sq, const double *kx, const double *sk,
-                    const double *vx, const double *sv, const double *dsb,
+                    const double *vx, const double *sv, const double *dsb, const struct thrift *th,
                     double *O64, float *O32, double *LSE64);
+
+/* fp16 rounding: 11-bit significand, nearest even, subnormal below 2^-14, saturating at the
+ * largest finite 65504 (inputs here stay far below it) */
+static double fp16_round(double x)
+{
+    double a = fabs(x);
+    if (a != a || a == 0.0) return x;
+    if (a >= 65504.0) return copysign(65504.0, x);
+    int e;
+    frexp(a, &e);
+    int E = e - 1;
+    if (E < -14) E = -14;
+    double quantum = ldexp(1.0, E - 10);
+    return copysign(nearbyint(a / quantum) * quantum, x);
+}
+
+void sage_oracle_fp16_f64(const double *x, double *y, long n)
+{
+    for (long i = 0; i < n; ++i) y[i] = fp16_round(x[i]);
+}
+
+int sage_oracle_fwd_thrift(int N, int D, int causal, double sm_scale, int qmask,
+                           const double *qx, const double *sq, const double *kx, const double *sk,
+                           const double *vx, const double *sv, const unsigned char *sel,
+                           const double *qh, const double *kh, const double *vh,
+                           double *O64, float *O32, double *LSE64)
+{
+    if (!sel || !qh || !kh || !vh) return 1;
+    struct thrift th = {sel, (N + TILE - 1) / TILE, qh, kh, vh};
+    return fwd_head(N, D, causal, sm_scale, qmask, qx, sq, kx, sk, vx, sv, NULL, &th, O64, O32, LSE64);
+}
 
 int sage_oracle_fwd(int N, int D, int causal, double sm_scale, int qmask,
                     const double *qx, const double *sq, const double *kx, const double *sk,
                     const double *vx, const double *sv,
                     double *O64, float *O32, double *LSE64)
 {
-    return fwd_head(N, D, causal, sm_scale, qmask, qx, sq, kx, sk, vx, sv, NULL, O64, O32, LSE64);
+    return fwd_head(N, D, causal, sm_scale, qmask, qx, sq, kx, sk, vx, sv, NULL, NULL, O64, O32, LSE64);
 }
 
 int sage_oracle_fwd_qs(int N, int D, int causal, double sm_scale, int qmask,
@@ -392,7 +435,7 @@ int sage_oracle_fwd_qs(int N, int D, int causal, double sm_scale, int qmask,
                        double *O64, float *O32, double *LSE64)
 {
     if (!dsb) return 1;
-    return fwd_head(N, D, causal, sm_scale, qmask, qx, sq, kx, sk, vx, sv, dsb, O64, O32, LSE64);
+    return fwd_head(N, D, causal, sm_scale, qmask, qx, sq, kx, sk, vx, sv, dsb, NULL, O64, O32, LSE64);
 }
 
 /* The log2-domain logit of query i and key j is RN32(x f) for the value x and
@@ -411,7 +454,7 @@ static inline double logit_parts(double acc, double sqI, double skJ, double alph
 
 static int fwd_head(int N, int D, int causal, double sm_scale, int qmask,
                     const double *qx, const double *sq, const double *kx, const double *sk,
-                    const double *vx, const double *sv, const double *dsb,
+                    const double *vx, const double *sv, const double *dsb, const struct thrift *th,
                     double *O64, float *O32, double *LSE64)
 {
     if (N < 0 || D <= 0) return 1;
@@ -421,7 +464,8 @@ static int fwd_head(int N, int D, int causal, double sm_scale, int qmask,
     int err = 0;
 #pragma omp parallel
     {
-        double *A = (double *)malloc(sizeof(double) * D);
+        double *A = (double *)malloc(sizeof(double) * 2 * D);
+        double *A16 = A ? A + D : NULL;  /* the high-precision tiles' accumulator (true units) */
         /* x, f per key (logit_parts); with NVFP4 also p~ and 448 P^ per key */
         double *s2 = (double *)malloc(sizeof(double) * 4 * TILE);
         if (!A || !s2) {
@@ -433,26 +477,43 @@ static int fwd_head(int N, int D, int causal, double sm_scale, int qmask,
             if (!A || !s2) continue;
             const double *qrow = qx + (size_t)i * D;
             double m = -INFINITY, l = 0.0;
-            for (int d = 0; d < D; ++d) A[d] = 0.0;
+            for (int d = 0; d < D; ++d) A[d] = A16[d] = 0.0;
             for (int j0 = 0; j0 < N; j0 += TILE) {
                 int j1 = j0 + TILE < N ? j0 + TILE : N;
                 if (causal && j1 > i + 1) j1 = i + 1;
                 if (j1 <= j0) break;
+                const int hp = th && th->sel[(size_t)(i / QBLK) * th->nkt + j0 / TILE];
                 double mt = -INFINITY;
                 double *acc = s2, *cj = s2 + TILE;
                 const double *dsb_row = dsb ? dsb + (size_t)(i / QBLK) * N : NULL;
                 for (int j = j0; j < j1; ++j) {
                     double c;
-                    acc[j - j0] = logit_parts(dot(qrow, kx + (size_t)j * D, D), sq[i / QBLK], sk[j / KBLK],
-                                              alpha, f32, dsb_row, j, &c);
+                    if (hp) {
+                        acc[j - j0] = r32(f32, dot(th->qh + (size_t)i * D, th->kh + (size_t)j * D, D));
+                        c = alpha;
+                    } else {
+                        acc[j - j0] = logit_parts(dot(qrow, kx + (size_t)j * D, D), sq[i / QBLK], sk[j / KBLK],
+                                                  alpha, f32, dsb_row, j, &c);
+                    }
                     cj[j - j0] = c;
                     mt = fmax(mt, r32(f32, acc[j - j0] * c));
                 }
                 double mn = fmax(m, mt);
                 double corr = (m == -INFINITY) ? 0.0 : exp2(m - mn);
                 l *= corr;
-                for (int d = 0; d < D; ++d) A[d] *= corr;
-                if (qmask & QM_FP4) {
+                for (int d = 0; d < D; ++d) {
+                    A[d] *= corr;
+                    A16[d] *= corr;
+                }
+                if (hp) {
+                    for (int j = j0; j < j1; ++j) {
+                        double pt = r32(f32, exp2(r32(f32, acc[j - j0] * cj[j - j0] - mn)));
+                        double p16 = fp16_round(pt);
+                        l += pt;
+                        const double *vrow = th->vh + (size_t)j * D;
+                        for (int d = 0; d < D; ++d) A16[d] += p16 * vrow[d];
+                    }
+                } else if (qmask & QM_FP4) {
                     /* p~ of the tile's keys, then NVFP4 per block of 16 keys (blocks start at
                      * multiples of 16; keys past the causal limit are not in any block) */
                     double *ptv = s2 + 2 * TILE, *p8v = s2 + 3 * TILE;
@@ -479,7 +540,7 @@ static int fwd_head(int N, int D, int causal, double sm_scale, int qmask,
                 m = mn;
             }
             for (int d = 0; d < D; ++d) {
-                double o = A[d] * sv[d] / (448.0 * l);
+                double o = (A[d] * sv[d] / 448.0 + A16[d]) / l;
                 O64[(size_t)i * D + d] = o;
                 O32[(size_t)i * D + d] = (float)o;
             }

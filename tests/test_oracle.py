@@ -646,3 +646,83 @@ def test_nvfp4_p_blocks_follow_the_keys():
                      backward_pass=False)
     assert ex["O64"][0, 1] > 1e-4
     np.testing.assert_allclose(r["O64"][:, 1], ex["O64"][:, 1], rtol=0.05)
+
+
+# ---------------------------------------------------------------- ThriftAttention
+
+def _thrift_case(seed, N=640, D=64):
+    rng = np.random.default_rng(seed)
+    q, k, v = (_rand(rng, N, D) for _ in range(3))
+    k = k + rng.normal(0, 2.0, size=(1, D))
+    return q, k, v
+
+
+def test_thrift_selection_invariants():
+    """The promoted pairs are the ceil(budget * visible) pairs of largest block-mean score
+    qbar_I . kbar_J among the pairs the causal mask lets through, ties in index order."""
+    q, k, _ = _thrift_case(70)
+    nb = 5
+    qm = np.stack([q[b * 128:(b + 1) * 128].mean(0) for b in range(nb)])
+    km = np.stack([k[b * 128:(b + 1) * 128].mean(0) for b in range(nb)])
+    score = qm @ km.T
+    for causal in (False, True):
+        vis = np.tril(np.ones((nb, nb), bool)) if causal else np.ones((nb, nb), bool)
+        for budget in (0.0, 0.05, 0.3, 1.0):
+            sel = orc.thrift_select(q, k, causal, budget).astype(bool)
+            assert sel.sum() == math.ceil(budget * vis.sum() - 1e-12)
+            assert not np.any(sel & ~vis)
+            if 0 < sel.sum() < vis.sum():
+                assert score[sel].min() >= score[vis & ~sel].max()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_thrift_budget_zero_is_the_low_bit_forward(causal):
+    q, k, v = _thrift_case(71)
+    qz = orc.quantize(q, k, v, False, True)
+    plain = orc.forward(qz, causal, 0.125)
+    th = dict(sel=orc.thrift_select(q, k, causal, 0.0), **orc.thrift_inputs(qz, v))
+    mixed = orc.forward(qz, causal, 0.125, thrift=th)
+    np.testing.assert_array_equal(mixed["O64"], plain["O64"])
+    np.testing.assert_array_equal(mixed["LSE64"], plain["LSE64"])
+
+
+def _fp16_attention(qh, kh, vh, causal, sm_scale):
+    s = (qh @ kh.T) * sm_scale
+    if causal:
+        s = np.where(np.tril(np.ones(s.shape, bool)), s, -np.inf)
+    s = s - s.max(1, keepdims=True)
+    p = np.exp(s)
+    return (p @ vh) / p.sum(1, keepdims=True)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_thrift_promoted_tiles_are_fp16_attention(causal):
+    """Every pair promoted: the forward is attention on the fp16-rounded q', k'', V, whose
+    only other rounding is P's fp16 rounding (relative 2^-11): O within 2^-11 max|V|."""
+    q, k, v = _thrift_case(72)
+    qz = orc.quantize(q, k, v, False, True)
+    th = dict(sel=orc.thrift_select(q, k, causal, 1.0), **orc.thrift_inputs(qz, v))
+    r = orc.forward(qz, causal, 0.125, thrift=th)
+    ref = _fp16_attention(th["qh"], th["kh"], th["vh"], causal, 0.125)
+    assert np.abs(r["O64"] - ref).max() <= 2.0 ** -11 * np.abs(th["vh"]).max() * 1.01 + 1e-6
+
+
+@pytest.mark.parametrize("budget", [0.1, 0.4])
+def test_thrift_mixed_tiles_merge_in_one_softmax(budget):
+    """With the low-bit path made exact (quantizers off) any mix of promoted and other tiles
+    must give exact attention up to the promoted tiles' fp16 rounding: the two paths share
+    the running maximum and row sum.  The low-bit scheme then moves toward exact attention
+    as the budget grows."""
+    q, k, v = _thrift_case(73)
+    ex = orc.run_head(q, k, v, v, True, 0.125, qmask=0, backward_pass=False)
+    qz0 = orc.quantize(q, k, v, False, True, qmask=0)
+    th0 = dict(sel=orc.thrift_select(q, k, True, budget), **orc.thrift_inputs(qz0, v))
+    r0 = orc.forward(qz0, True, 0.125, qmask=0, thrift=th0)
+    assert np.abs(r0["O64"] - ex["O64"]).max() <= 2.0 ** -10 * np.abs(v).max()
+    rel = lambda a, b: np.linalg.norm(a - b) / np.linalg.norm(b)  # noqa: E731
+    qz = orc.quantize(q, k, v, False, True)
+    errs = []
+    for b in (0.0, budget, 1.0):
+        th = dict(sel=orc.thrift_select(q, k, True, b), **orc.thrift_inputs(qz, v))
+        errs.append(rel(orc.forward(qz, True, 0.125, thrift=th)["O64"], ex["O64"]))
+    assert errs[0] > errs[1] > errs[2]
