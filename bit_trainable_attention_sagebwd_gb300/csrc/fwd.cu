@@ -411,8 +411,9 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
 // the softmax of tile A (keys [0,64) and [64,128) of each key tile), 2-3 that of tile B;
 // warp 16 loads K and V tiles with TMA; warp 17 allocates TMEM and issues the UMMAs in
 // the order
-//   S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) ...
-// so the tensor core works on one tile while the other tile's softmax runs.
+//   S_A(0) S_B(0) | S_A(j+1) S_B(j+1) PV_A(j) PV_B(j) ...
+// (each next S once its tile's softmax holds the current S in registers, each PV once its
+// P is written), so the tensor core works on one tile while the other tile's softmax runs.
 // TMEM columns: S_A [0,128), S_B [128,256), O_A [256,256+D), O_B [256+D,256+2D).
 template <int D, bool CAUSAL, bool QS>
 __global__ void __launch_bounds__(640, 1)
