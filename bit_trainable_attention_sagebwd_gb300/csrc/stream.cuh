@@ -6,32 +6,13 @@
 // one item, the bulk copies of the following ones are under way.  A few CTAs per SM
 // then hold well over 100 KB of reads in flight, and compute overlaps the copies.
 //
-// Because claims go in increasing order and every CTA works on its claims in order, an
-// item may wait for results of items before it in the list: each of those was claimed by
-// a running CTA that has no unfinished wait of its own ahead of it.  No co-residency of
-// the grid is assumed.
+// Items are independent: no CTA waits on another, and no co-residency of the grid is
+// assumed.
 #pragma once
 
 #include "ptx.cuh"
 
 namespace sage {
-
-__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Wait until *p >= target (a counter other CTAs raise); false when the budget runs out.
-__device__ __forceinline__ bool wait_counter(const int* p, int target, uint64_t budget_ns = SAGE_WAIT_NS) {
-  if (ld_acquire_gpu(p) >= target) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (;;) {
-    __nanosleep(100);
-    if (ld_acquire_gpu(p) >= target) return true;
-    if (globaltimer_ns() - t0 > budget_ns) return false;
-  }
-}
 
 // Wait for an mbarrier phase without looking at any abort flag (draining copies in flight).
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t budget_ns = SAGE_WAIT_NS) {
