@@ -3,6 +3,10 @@
 - e4m3 rounding: exhaustive over every positive fp32 in [2^-11, 448] against
   torch's float8_e4m3fn cast (a library routine), plus signs, underflow and
   saturation.
+- bf16 and fp16 rounding (every bf16 output and reference gradient, the D_i of
+  the backward, the fp16 path of ThriftAttention): every mantissa of every fp32
+  binade where the rounding rule changes, against torch's bfloat16 / float16
+  casts (library routines), plus a random sample over all bit patterns.
 - exact mode (every quantizer off): forward against torch scaled-dot-product
   attention in float64, backward against torch autograd, and against central
   finite differences of the oracle's own forward.
@@ -63,6 +67,58 @@ def test_e4m3_exhaustive_against_torch_cast():
         t = torch.from_numpy(x).to(torch.float8_e4m3fn).to(torch.float32).numpy()
         assert np.array_equal(y, t), f"mismatch in chunk starting at {start:#x}"
         assert np.array_equal(orc.e4m3(-x), -t)
+
+
+def _binade(e: int, sign: int = 0) -> np.ndarray:
+    """Every fp32 with biased exponent e (all 2^23 mantissas) and the given sign."""
+    bits = (np.uint32(sign) << np.uint32(31)) | (np.uint32(e) << np.uint32(23)) | \
+        np.arange(1 << 23, dtype=np.uint32)
+    return bits.view(np.float32)
+
+
+def _same(a: np.ndarray, b: np.ndarray) -> bool:
+    return bool(np.all((a == b) | (np.isnan(a) & np.isnan(b))))
+
+
+def test_bf16_rounding_against_torch_cast():
+    """The oracle's bf16 rounding (nearest even; inf and NaN kept) equals torch's fp32 ->
+    bfloat16 cast on every mantissa of the binades where the rule changes (subnormals, the
+    smallest normals, around 1, the two largest finite binades, where rounding reaches
+    infinity, and inf/NaN), both signs, and on 2^24 random bit patterns."""
+    for e in (0, 1, 2, 126, 127, 128, 253, 254, 255):
+        for sign in (0, 1):
+            x = _binade(e, sign)
+            y = orc.to_bf16(x.astype(np.float64))
+            t = torch.from_numpy(x).to(torch.bfloat16).to(torch.float32).numpy().astype(np.float64)
+            assert _same(y, t), f"bf16 rounding differs in binade {e}, sign {sign}"
+    x = np.random.default_rng(1).integers(0, 1 << 32, size=1 << 24, dtype=np.uint64).astype(np.uint32)
+    x = x.view(np.float32)
+    t = torch.from_numpy(x).to(torch.bfloat16).to(torch.float32).numpy().astype(np.float64)
+    assert _same(orc.to_bf16(x.astype(np.float64)), t)
+
+
+def test_fp16_rounding_against_torch_cast():
+    """The oracle's fp16 rounding (nearest even, subnormal below 2^-14) equals torch's
+    fp32 -> float16 cast on every positive fp32 from 2^-26 (below it both give 0) up to the
+    largest finite binade [2^15, 2^16) except past 65520 (where IEEE rounds to infinity and
+    the oracle saturates at 65504, a range its inputs never reach), on negative values, and
+    on 2^24 random bit patterns with |x| < 65520."""
+    for e in range(101, 143):
+        x = _binade(e)
+        if e == 142:
+            x = x[x < 65520.0]
+        y = orc.fp16(x.astype(np.float64))
+        t = torch.from_numpy(x).to(torch.float16).to(torch.float32).numpy().astype(np.float64)
+        assert np.array_equal(y, t), f"fp16 rounding differs in binade {e}"
+        assert np.array_equal(orc.fp16(-x.astype(np.float64)), -t)
+    tiny = _binade(100)
+    assert np.all(orc.fp16(tiny.astype(np.float64)) == 0.0)
+    x = np.random.default_rng(2).integers(0, 1 << 32, size=1 << 24, dtype=np.uint64).astype(np.uint32)
+    x = x.view(np.float32)
+    x = x[np.abs(x) < 65520.0]
+    t = torch.from_numpy(x).to(torch.float16).to(torch.float32).numpy().astype(np.float64)
+    assert np.array_equal(orc.fp16(x.astype(np.float64)), t)
+    assert np.all(orc.fp16(np.array([65520.0, 1e6, 3e38])) == 65504.0)
 
 
 def test_e4m3_underflow_and_saturation():
