@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include "../../include/sage_attn.h"
+#include "args.h"
 #include "kernels.h"
 #include "layout.h"
 #include "ptx.cuh"
@@ -19,7 +20,6 @@ bool shape_ok(int B, int H, int N, int D) {
 bool aligned16(const void* p) { return p != nullptr && ((uintptr_t)p & 15u) == 0; }
 // grouped-query attention: Hkv key/value heads, each shared by H / Hkv query heads
 bool groups_ok(int H, int Hkv) { return Hkv >= 1 && Hkv <= H && H % Hkv == 0; }
-float resolve_scale(float sm_scale, int D) { return sm_scale > 0.f ? sm_scale : 1.0f / sqrtf((float)D); }
 
 // One CTA waits on a barrier that nothing arrives at; the bounded wait gives up
 // after budget_ns and the kernel records the timeout in the status word.
@@ -91,9 +91,9 @@ int sage_attn_fwd(const void* ws, void* O, float* LSE, float* O32, int B, int H,
                   float sm_scale, void* stream) {
   if (!aligned16(ws) || !aligned16(O) || LSE == nullptr || ((uintptr_t)LSE & 3u)) return SAGE_ERR_INVALID_ARG;
   if (O32 != nullptr && !aligned16(O32)) return SAGE_ERR_INVALID_ARG;
-  if (!(sm_scale == sm_scale) || isinf(sm_scale)) return SAGE_ERR_INVALID_ARG;
+  if (!sage::scale_ok(sm_scale)) return SAGE_ERR_INVALID_ARG;
   if (!shape_ok(B, H, N, D)) return SAGE_ERR_UNSUPPORTED;
-  return sage::launch_fwd(ws, O, LSE, O32, B, H, N, D, causal != 0, resolve_scale(sm_scale, D),
+  return sage::launch_fwd(ws, O, LSE, O32, B, H, N, D, causal != 0, sage::resolve_scale(sm_scale, D),
                           static_cast<cudaStream_t>(stream));
 }
 
@@ -104,11 +104,11 @@ int sage_attn_bwd(const void* Q, const void* K, const void* V, const void* O, co
       !aligned16(dK) || !aligned16(dV) || !aligned16(ws) || !aligned16(bwd_ws) || LSE == nullptr ||
       ((uintptr_t)LSE & 3u))
     return SAGE_ERR_INVALID_ARG;
-  if (!(sm_scale == sm_scale) || isinf(sm_scale)) return SAGE_ERR_INVALID_ARG;
+  if (!sage::scale_ok(sm_scale)) return SAGE_ERR_INVALID_ARG;
   if (!shape_ok(B, H, N, D)) return SAGE_ERR_UNSUPPORTED;
   if (bwd_ws_bytes < sage::bwd_ws_layout(B, H, N, D).total) return SAGE_ERR_INVALID_ARG;
   return sage::launch_bwd(Q, K, V, O, LSE, dO, dQ, dK, dV, ws, bwd_ws, B, H, N, D, causal != 0, qk_norm != 0,
-                          k_smooth != 0, resolve_scale(sm_scale, D), static_cast<cudaStream_t>(stream));
+                          k_smooth != 0, sage::resolve_scale(sm_scale, D), static_cast<cudaStream_t>(stream));
 }
 
 int sage_attn_bwd_o32(const void* Q, const void* K, const void* V, const float* O32, const float* LSE,
@@ -119,11 +119,11 @@ int sage_attn_bwd_o32(const void* Q, const void* K, const void* V, const float* 
       !aligned16(dK) || !aligned16(dV) || !aligned16(ws) || !aligned16(bwd_ws) || LSE == nullptr ||
       ((uintptr_t)LSE & 3u))
     return SAGE_ERR_INVALID_ARG;
-  if (!(sm_scale == sm_scale) || isinf(sm_scale)) return SAGE_ERR_INVALID_ARG;
+  if (!sage::scale_ok(sm_scale)) return SAGE_ERR_INVALID_ARG;
   if (!shape_ok(B, H, N, D)) return SAGE_ERR_UNSUPPORTED;
   if (bwd_ws_bytes < sage::bwd_ws_layout(B, H, N, D).total) return SAGE_ERR_INVALID_ARG;
   return sage::launch_bwd(Q, K, V, nullptr, LSE, dO, dQ, dK, dV, ws, bwd_ws, B, H, N, D, causal != 0,
-                          qk_norm != 0, k_smooth != 0, resolve_scale(sm_scale, D), static_cast<cudaStream_t>(stream),
+                          qk_norm != 0, k_smooth != 0, sage::resolve_scale(sm_scale, D), static_cast<cudaStream_t>(stream),
                           O32);
 }
 
@@ -150,9 +150,9 @@ int sage_attn_gqa_fwd(const void* ws, void* O, float* LSE, float* O32, int B, in
                       int causal, float sm_scale, void* stream) {
   if (!aligned16(ws) || !aligned16(O) || LSE == nullptr || ((uintptr_t)LSE & 3u)) return SAGE_ERR_INVALID_ARG;
   if (O32 != nullptr && !aligned16(O32)) return SAGE_ERR_INVALID_ARG;
-  if (!(sm_scale == sm_scale) || isinf(sm_scale)) return SAGE_ERR_INVALID_ARG;
+  if (!sage::scale_ok(sm_scale)) return SAGE_ERR_INVALID_ARG;
   if (!shape_ok(B, H, N, D) || !groups_ok(H, Hkv)) return SAGE_ERR_UNSUPPORTED;
-  return sage::launch_fwd(ws, O, LSE, O32, B, H, N, D, causal != 0, resolve_scale(sm_scale, D),
+  return sage::launch_fwd(ws, O, LSE, O32, B, H, N, D, causal != 0, sage::resolve_scale(sm_scale, D),
                           static_cast<cudaStream_t>(stream), Hkv);
 }
 
@@ -163,11 +163,11 @@ int sage_attn_gqa_bwd(const void* Q, const void* K, const void* V, const void* O
       !aligned16(dK) || !aligned16(dV) || !aligned16(ws) || !aligned16(bwd_ws) || LSE == nullptr ||
       ((uintptr_t)LSE & 3u))
     return SAGE_ERR_INVALID_ARG;
-  if (!(sm_scale == sm_scale) || isinf(sm_scale)) return SAGE_ERR_INVALID_ARG;
+  if (!sage::scale_ok(sm_scale)) return SAGE_ERR_INVALID_ARG;
   if (!shape_ok(B, H, N, D) || !groups_ok(H, Hkv)) return SAGE_ERR_UNSUPPORTED;
   if (bwd_ws_bytes < sage::bwd_ws_layout(B, H, N, D, Hkv).total) return SAGE_ERR_INVALID_ARG;
   return sage::launch_bwd(Q, K, V, O, LSE, dO, dQ, dK, dV, ws, bwd_ws, B, H, N, D, causal != 0, qk_norm != 0,
-                          k_smooth != 0, resolve_scale(sm_scale, D), static_cast<cudaStream_t>(stream), nullptr,
+                          k_smooth != 0, sage::resolve_scale(sm_scale, D), static_cast<cudaStream_t>(stream), nullptr,
                           Hkv);
 }
 
@@ -189,9 +189,9 @@ int sage_attn_qs_fwd(const void* ws, void* O, float* LSE, float* O32, int B, int
                      int causal, float sm_scale, void* stream) {
   if (!aligned16(ws) || !aligned16(O) || LSE == nullptr || ((uintptr_t)LSE & 3u)) return SAGE_ERR_INVALID_ARG;
   if (O32 != nullptr && !aligned16(O32)) return SAGE_ERR_INVALID_ARG;
-  if (!(sm_scale == sm_scale) || isinf(sm_scale)) return SAGE_ERR_INVALID_ARG;
+  if (!sage::scale_ok(sm_scale)) return SAGE_ERR_INVALID_ARG;
   if (!shape_ok(B, H, N, D) || !groups_ok(H, Hkv)) return SAGE_ERR_UNSUPPORTED;
-  return sage::launch_fwd(ws, O, LSE, O32, B, H, N, D, causal != 0, resolve_scale(sm_scale, D),
+  return sage::launch_fwd(ws, O, LSE, O32, B, H, N, D, causal != 0, sage::resolve_scale(sm_scale, D),
                           static_cast<cudaStream_t>(stream), Hkv, true);
 }
 
@@ -202,11 +202,11 @@ int sage_attn_qs_bwd(const void* Q, const void* K, const void* V, const void* O,
       !aligned16(dK) || !aligned16(dV) || !aligned16(ws) || !aligned16(bwd_ws) || LSE == nullptr ||
       ((uintptr_t)LSE & 3u))
     return SAGE_ERR_INVALID_ARG;
-  if (!(sm_scale == sm_scale) || isinf(sm_scale)) return SAGE_ERR_INVALID_ARG;
+  if (!sage::scale_ok(sm_scale)) return SAGE_ERR_INVALID_ARG;
   if (!shape_ok(B, H, N, D) || !groups_ok(H, Hkv)) return SAGE_ERR_UNSUPPORTED;
   if (bwd_ws_bytes < sage::bwd_ws_layout(B, H, N, D, Hkv).total) return SAGE_ERR_INVALID_ARG;
   return sage::launch_bwd(Q, K, V, O, LSE, dO, dQ, dK, dV, ws, bwd_ws, B, H, N, D, causal != 0, qk_norm != 0,
-                          k_smooth != 0, resolve_scale(sm_scale, D), static_cast<cudaStream_t>(stream), nullptr,
+                          k_smooth != 0, sage::resolve_scale(sm_scale, D), static_cast<cudaStream_t>(stream), nullptr,
                           Hkv, true);
 }
 

@@ -135,11 +135,8 @@ int launch_bwd_dq(const void* Q, const float* qr, void* bwd_ws, void* dQ, int B,
   if (nitems == 0) return 0;
   auto kern = D == 128 ? bwd_dq_kernel<128> : bwd_dq_kernel<64>;
   const size_t smem = (size_t)(D == 128 ? 3 : 4) * kChunk * D * 4;
-  static bool attr[2] = {false, false};
-  if (!attr[D == 128]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 3;
-    attr[D == 128] = true;
-  }
+  // the attribute is per device: set on every launch, so a second GPU of the process gets it too
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 3;
   if (launch_pdl(kern, dim3(persistent_grid(kern, kThreads, smem, nitems)), dim3(kThreads), smem, st, tacc, p) !=
       cudaSuccess)
     return 3;

@@ -9,6 +9,7 @@
 #include <mutex>
 
 #include "../../include/sage_attn.h"
+#include "args.h"
 #include "kernels.h"
 #include "layout.h"
 
@@ -46,14 +47,14 @@ extern "C" int sage_attn_bwd_noalloc(const void* Q, const void* K, const void* V
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(dO) || !aligned16(dQ) ||
       !aligned16(dK) || !aligned16(dV) || !aligned16(ws) || LSE == nullptr || ((uintptr_t)LSE & 3u))
     return SAGE_ERR_INVALID_ARG;
-  if (!(sm_scale == sm_scale) || sm_scale > 3.0e38f || sm_scale < -3.0e38f) return SAGE_ERR_INVALID_ARG;
+  if (!sage::scale_ok(sm_scale)) return SAGE_ERR_INVALID_ARG;
   const size_t need = sage_attn_bwd_ws_bytes(B, H, N, D);
   if (need == 0) return SAGE_ERR_UNSUPPORTED;
   if (need > (size_t)SAGE_ATTN_NOALLOC_SCRATCH_BYTES) return SAGE_ERR_UNSUPPORTED;  // too large for the array
   void* scratch = nullptr;
   const int rc = scratch_address(&scratch);
   if (rc != SAGE_OK) return rc;
-  const float scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf((float)D);
+  const float scale = sage::resolve_scale(sm_scale, D);
   // the launcher zeroes the dQ accumulator and writes every other scratch section
   // before reading it, so nothing left from an earlier call leaks into this one
   return sage::launch_bwd(Q, K, V, O, LSE, dO, dQ, dK, dV, ws, scratch, B, H, N, D, causal != 0, qk_norm != 0,

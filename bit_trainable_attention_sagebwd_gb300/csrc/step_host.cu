@@ -10,9 +10,11 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <mutex>
 #include <vector>
 
 #include "../../include/sage_attn.h"
+#include "args.h"
 #include "kernels.h"
 #include "layout.h"
 
@@ -80,12 +82,18 @@ struct CopyEngines {
   std::vector<cudaEvent_t> ev;  // [0] start, [1] end, then inputs in / forward done / backward done per range
 };
 
+// One set per device, created on the first step on that device and kept until exit; the
+// mutex guards creation only (a set in use is never replaced).
+constexpr int kMaxDevices = 64;
+std::mutex g_engines_mu;
+CopyEngines g_engines[kMaxDevices];
+
 CopyEngines* copy_engines() {
-  static CopyEngines e;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_engines_mu);
+  CopyEngines& e = g_engines[dev];
   if (e.device != dev) {
-    e = CopyEngines();  // a new device: fresh streams and events (the old ones stay with it)
     if (cudaStreamCreateWithFlags(&e.h2d, cudaStreamNonBlocking) != cudaSuccess ||
         cudaStreamCreateWithFlags(&e.d2h, cudaStreamNonBlocking) != cudaSuccess)
       return nullptr;
@@ -177,12 +185,12 @@ int sage_attn_step_host(const void* Q, const void* K, const void* V, const void*
                         int qk_norm, int k_smooth, float sm_scale, int groups, void* stream) {
   if (!Q || !K || !V || !dO || !O || !LSE || !dQ || !dK || !dV || !dev || ((uintptr_t)dev & 255u))
     return SAGE_ERR_INVALID_ARG;
-  if (!(sm_scale == sm_scale) || isinf(sm_scale)) return SAGE_ERR_INVALID_ARG;
+  if (!sage::scale_ok(sm_scale)) return SAGE_ERR_INVALID_ARG;
   if (!sage::shape_ok(B, H, N, D)) return SAGE_ERR_UNSUPPORTED;
   if (dev_bytes < sage::step_host_layout(B, H, N, D, groups).total) return SAGE_ERR_INVALID_ARG;
-  const float scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf((float)D);
   return sage::launch_step_host(Q, K, V, dO, O, LSE, dQ, dK, dV, dev, B, H, N, D, causal != 0, qk_norm != 0,
-                                k_smooth != 0, scale, groups, static_cast<cudaStream_t>(stream));
+                                k_smooth != 0, sage::resolve_scale(sm_scale, D), groups,
+                                static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -10,6 +10,8 @@
 // assumed.
 #pragma once
 
+#include <atomic>
+
 #include "ptx.cuh"
 
 namespace sage {
@@ -84,15 +86,19 @@ __device__ __forceinline__ bool stream_items(StreamCtl<NS>& c, uint8_t* stages, 
   return ok;
 }
 
-// number of SMs of the current device (cached per process)
+// number of SMs of the current device (looked up once per device)
 inline int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
   }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+  if (dev >= 0 && dev < kMaxDevices) cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
