@@ -81,6 +81,17 @@ def check_forward_head(w, g: dict, bh: int, r: dict) -> dict:
     return {"o_err": err, "lse_err": lerr}
 
 
+def full_size_heads(w) -> list:
+    """Heads the full-size checks compare: every head of a small workload; otherwise the first,
+    the last and one in the middle.  The forward and backward launch their CTAs in groups of
+    heads whose operands fit in L2 (heads in order, longest tiles first within a group), so
+    the first and last heads sit in the first and last groups and B*H/2 + 1 in a middle one
+    (long_32k: backward groups of 4 heads, forward groups of 7)."""
+    if w.bh <= 4:
+        return list(range(w.bh))
+    return sorted({0, w.bh // 2 + 1, w.bh - 1})
+
+
 def rel_l2(got: np.ndarray, ref: np.ndarray) -> float:
     return float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30))
 

@@ -32,14 +32,13 @@ def test_backward_small(w):
 
 @pytest.mark.parametrize("name", list(wl.WORKLOADS))
 def test_backward_full_size(name):
-    """Full-size workloads in the bench's launch configuration; the oracle computes
-    one head (two for the small workload)."""
+    """Full-size workloads in the bench's launch configuration; the oracle computes the
+    first, a middle and the last head (every head of the small workload)."""
     import parity
     w = wl.WORKLOADS[name]
     x = wl.all_inputs(w)
     g = parity.run_gpu(w, x, backward=True)
-    heads = range(w.bh) if w.bh <= 4 else [w.bh - 1]
-    for bh in heads:
+    for bh in parity.full_size_heads(w):
         r = parity.oracle_head(w, x, bh, backward=True)
         parity.check_backward_head(w, g, bh, r)
 

@@ -33,14 +33,13 @@ def test_quantize_forward_small(w):
 
 @pytest.mark.parametrize("name", list(wl.WORKLOADS))
 def test_quantize_forward_full_size(name):
-    """Full-size workloads in the bench's launch configuration; the oracle computes
-    the first and last head (every head for the small one)."""
+    """Full-size workloads in the bench's launch configuration; the oracle computes the
+    first, a middle and the last head (every head of the small workload)."""
     import parity
     w = wl.WORKLOADS[name]
     x = wl.all_inputs(w)
     g = parity.run_gpu(w, x, backward=False)
-    heads = range(w.bh) if w.bh <= 4 else [0, w.bh - 1]
-    for bh in heads:
+    for bh in parity.full_size_heads(w):
         r = parity.oracle_head(w, x, bh, backward=False)
         parity.check_quantize_head(w, g, bh, r)
         parity.check_forward_head(w, g, bh, r)
