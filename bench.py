@@ -40,12 +40,14 @@ FLUSH_BYTES = 256 << 20
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=None)
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-workloads", action="store_true", help="skip the per-kernel runs of the other "
+                    "full-size workloads")
     return ap.parse_args()
 
 
@@ -240,6 +242,67 @@ def run_reference(args, w):
 
 
 # -------------------------------------------------------------------- ours
+def kernel_fractions(flops: dict, fwd_ms: float, bwd_main_ms: float, peaks: dict) -> dict:
+    """Achieved TFLOP/s of fwd_kernel and bwd_main_kernel and their fractions of the FP8-equivalent
+    peak (2 x measured bf16, the benchmark spec's INT8/FP8 denominator) and of the executed formats
+    (S, dP, dQ, dK on bf16 tensor cores; PV, dV on FP8)."""
+    fp8 = 2.0 * peaks["bf16"]
+    fa = flops["fwd"] / (fwd_ms * 1e-3) / 1e12
+    ba = flops["bwd"] / (bwd_main_ms * 1e-3) / 1e12
+    t_exec_fwd = (0.5 * flops["fwd"]) / (peaks["bf16"] * 1e12) + (0.5 * flops["fwd"]) / (fp8 * 1e12)
+    t_exec_bwd = (0.8 * flops["bwd"]) / (peaks["bf16"] * 1e12) + (0.2 * flops["bwd"]) / (fp8 * 1e12)
+    return {"fwd_kernel": {"achieved": fa, "frac": fa / fp8, "frac_executed_formats": t_exec_fwd / (fwd_ms * 1e-3),
+                           "flops_per_launch": flops["fwd"], "avg_launch_ms": fwd_ms},
+            "bwd_main_kernel": {"achieved": ba, "frac": ba / fp8,
+                                "frac_executed_formats": t_exec_bwd / (bwd_main_ms * 1e-3),
+                                "flops_per_launch": flops["bwd"], "avg_launch_ms": bwd_main_ms}}
+
+
+def other_workload(sa, wl, name, dev, flush, peaks, steps=20):
+    """Every launch group of another workload bracketed by events (after 3 warm-up steps, L2
+    flushed before each step): per-group ms, step TOPS and the two main kernels' fractions."""
+    import numpy as np
+    import torch
+    w = wl.WORKLOADS[name]
+    B, H, N, D = w.B, w.H, w.N, w.D
+    x = wl.all_inputs(w)
+    t = {n: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev) for n, a in x.items()}
+    del x
+    ws, bws = sa.alloc_ws(B, H, N, D, dev), sa.alloc_bwd_ws(B, H, N, D, dev)
+    o = torch.empty((B, H, N, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(o) for _ in range(3))
+
+    def step():
+        sa.quantize(t["q"], t["k"], t["v"], w.qk_norm, w.k_smooth, ws=ws)
+        sa.forward(ws, B, H, N, D, w.causal, w.sm_scale, o=o, lse=lse, device=dev)
+        sa.backward(t["q"], t["k"], t["v"], o, lse, t["do"], ws, w.causal, w.qk_norm, w.k_smooth, w.sm_scale,
+                    bwd_ws=bws, dq=dq, dk=dk, dv=dv)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    groups = ("quantize", "fwd", "bwd_pre", "bwd_main", "bwd_dq")
+    for g in groups:
+        sa.sage_attn_timer_read(g)
+    sa.sage_attn_timer_only(None)
+    sa.sage_attn_timer_enable(1)
+    for i in range(steps):
+        flush.fill_(float(i))
+        step()
+    torch.cuda.synchronize()
+    sa.sage_attn_timer_enable(0)
+    if sa.get_status(ws) != sa.SAGE_OK:
+        raise SystemExit(f"device status not ok after the {name} steps")
+    ms = {g: (lambda r: r[0] / max(1, r[1]))(sa.sage_attn_timer_read(g)) for g in groups}
+    ops = w.ops()
+    step_ms = sum(ms.values())
+    out = {"workload": f"{w.name}: {w.note}", "steps": steps, "kernel_ms_per_step": ms,
+           "tops_sum_of_groups": ops["fwd_bwd"] / (step_ms * 1e-3) / 1e12}
+    out.update(kernel_fractions(ops, ms["fwd"], ms["bwd_main"], peaks))
+    return out
+
+
 def run_ours(args, w):
     import numpy as np
     import torch
@@ -431,6 +494,21 @@ def run_ours(args, w):
             "peak_note": f"{peaks['source']} bf16 {peaks['bf16']:.1f} TF/s (burst) x 2, the nominal fp8/bf16 ratio",
             "frac_executed_formats": t_exec_bwd / (bm_avg * 1e-3),
             "flops_per_launch": bwd_flops, "avg_launch_ms": bm_avg}
+    # the forward kernel's block, from the breakdown steps (every launch group bracketed)
+    ff = kernel_fractions(ops, fw_avg, bm_avg, peaks)["fwd_kernel"]
+    roof_fwd = {"kernel": "fwd_kernel", "bound": "tensor", "achieved": ff["achieved"], "peak": fp8_peak,
+                "unit": "TFLOP/s", "frac": ff["frac"],
+                "traffic": profiled_traffic("fwd", w.name, os.path.join(ROOT, "bit_trainable_attention_sagebwd_gb300",
+                                                                        "csrc", "fwd.cu")),
+                "peak_note": roof["peak_note"], "frac_executed_formats": ff["frac_executed_formats"],
+                "flops_per_launch": fwd_flops, "avg_launch_ms": fw_avg}
+    others = {}
+    if not args.no_other_workloads:
+        for name in wl.WORKLOADS:
+            if name in (w.name, "pr1_ref"):
+                continue
+            others[name] = other_workload(sa, wl, name, dev, flush, peaks)
+            torch.cuda.empty_cache()
     fwd_tops = fwd_flops / ((q_ms + fw_ms) / max(1, fw_n) * 1e-3) / 1e12
     bk_ms, bk_n = ktimes["bwd_main"]
     bwd_tops = bwd_flops / ((bp_ms + bk_ms + bd_ms) / max(1, bk_n) * 1e-3) / 1e12
@@ -443,6 +521,9 @@ def run_ours(args, w):
         "fwd_bwd_frac_fp8_peak": value / world / fp8_peak,
         "kernel_ms_per_step": {n: ms / max(1, c) for n, (ms, c) in ktimes.items()},
         "kernel_ms_note": "per launch group, from 20 untimed steps with every group bracketed by events",
+        "other_workloads": others,
+        "other_workloads_note": "the other full-size workloads, 20 steps each after 3 warm-up, L2 flushed, "
+                                "every launch group bracketed by events (not part of value)",
         "variants": variants,
         "variants_note": "the workload's shape with fewer key/value heads (grouped-query attention) and with "
                          "Q-smoothing: quantize + forward + backward, median of 20 steps, L2 flushed",
@@ -462,6 +543,7 @@ def run_ours(args, w):
                        "l2": "flushed between timed steps (256 MiB write, outside the events)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "roofline": roof,
+            "roofline_fwd": roof_fwd,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_total / Ke,

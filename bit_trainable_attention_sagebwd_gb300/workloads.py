@@ -76,7 +76,7 @@ WORKLOADS = {
                           "k_offset3", 4, "B2 H24 N16384 D64, non-causal, K offset N(0,3^2)"),
 }
 
-BENCH_WORKLOAD = "pretrain_8k"
+BENCH_WORKLOAD = "long_32k"
 
 
 def custom(B, H, N, D, causal, qk_norm=False, k_smooth=True, sm_scale=None,
@@ -134,14 +134,28 @@ def head_inputs(w: Workload, bh: int) -> dict:
 
 
 def all_inputs(w: Workload) -> dict:
-    """bf16 bit patterns (uint16 [B, H, N, D]) of q, k, v, do for every head."""
+    """bf16 bit patterns (uint16 [B, H, N, D]) of q, k, v, do for every head.
+
+    Heads are drawn on a thread pool (numpy's generators release the GIL while they fill
+    arrays); every head has its own stream, so the result does not depend on the order."""
+    import concurrent.futures as cf
+    import os
     shape = (w.B, w.H, w.N, w.D)
     out = {n: np.empty(shape, dtype=np.uint16) for n in ("q", "k", "v", "do")}
-    for bh in range(w.bh):
+
+    def one(bh):
         hi = head_inputs(w, bh)
         b, h = divmod(bh, w.H)
         for n in out:
             out[n][b, h] = hi[n]
+
+    workers = min(16, os.cpu_count() or 1, w.bh)
+    if workers <= 1 or w.N * w.D < (1 << 16):
+        for bh in range(w.bh):
+            one(bh)
+    else:
+        with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+            list(ex.map(one, range(w.bh)))
     return out
 
 
