@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=None)
+    ap.add_argument("--heads", type=int, default=None, help="run the workload with this many heads per batch "
+                    "entry (a smaller case of the same kernels, for profiling)")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-other-workloads", action="store_true", help="skip the per-kernel runs of the other "
@@ -564,6 +566,9 @@ def main():
     args = parse()
     from bit_trainable_attention_sagebwd_gb300 import workloads as wl
     w = wl.WORKLOADS[args.workload or wl.BENCH_WORKLOAD]
+    if args.heads:
+        import dataclasses
+        w = dataclasses.replace(w, H=args.heads, note=f"{w.note}, {args.heads} heads")
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)
