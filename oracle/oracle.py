@@ -123,6 +123,21 @@ def fp16(x: np.ndarray) -> np.ndarray:
     return y
 
 
+def _block_means(x: np.ndarray) -> np.ndarray:
+    """Channel means of the 128-token blocks [ceil(N/128), D]: fp64 sums over the block's
+    tokens in token order, divided by the block's token count."""
+    N, D = x.shape
+    nb = -(-N // 128)
+    out = np.empty((nb, D))
+    for b in range(nb):
+        blk = x[b * 128:(b + 1) * 128]
+        s = np.zeros(D)
+        for t in range(blk.shape[0]):
+            s = s + blk[t]
+        out[b] = s / blk.shape[0]
+    return out
+
+
 def thrift_select(q, k, causal, budget) -> np.ndarray:
     """ThriftAttention's selection ("ThriftAttention" (gist.science summary), Methodology
     step 1): the importance of the pair (128-query block I, 128-key tile J) is the dot
@@ -132,9 +147,11 @@ def thrift_select(q, k, causal, budget) -> np.ndarray:
     q, k = _c64(q), _c64(k)
     N = q.shape[0]
     nb = -(-N // 128)
-    qm = np.stack([q[b * 128:(b + 1) * 128].mean(0) for b in range(nb)])
-    km = np.stack([k[b * 128:(b + 1) * 128].mean(0) for b in range(nb)])
-    score = qm @ km.T
+    qm, km = _block_means(q), _block_means(k)
+    # the dot products in a fixed order: fp64 products added over the channels one by one
+    score = np.zeros((nb, nb))
+    for d in range(q.shape[1]):
+        score = score + qm[:, d, None] * km[None, :, d]
     vis = np.tril(np.ones((nb, nb), dtype=bool)) if causal else np.ones((nb, nb), dtype=bool)
     idx = np.flatnonzero(vis.ravel())
     n = int(math.ceil(budget * idx.size - 1e-12))

@@ -378,7 +378,11 @@ static inline double qk_factor(double sqI, double skJ, double alpha, int f32)
  * the high-precision path from qh, kh, vh (the softmax's q', k'' and V rounded to fp16):
  * x = RN32(qh . kh) (fp16 products, one rounding of the sum), the log2 logit RN32(x alpha),
  * P16 = fp16(p~) times vh into an fp32 accumulator of its own; the other tiles take the
- * low-bit path; both merge in the one online softmax (shared m and l). */
+ * low-bit path; both merge in the one online softmax (shared m and l).  A row takes its
+ * low-bit tiles first and its promoted tiles after them, as the page's kernel does (the
+ * non-selected blocks through the low-precision path, then the promoted blocks in a
+ * separate high-precision routine); since P is quantized relative to the running maximum,
+ * the order is part of the result. */
 struct thrift {
     const unsigned char *sel;
     int nkt;
@@ -478,11 +482,15 @@ static int fwd_head(int N, int D, int causal, double sm_scale, int qmask,
             const double *qrow = qx + (size_t)i * D;
             double m = -INFINITY, l = 0.0;
             for (int d = 0; d < D; ++d) A[d] = A16[d] = 0.0;
+            /* ThriftAttention: the low-bit tiles first, then the promoted ones (pass 1), each
+             * pass in ascending key order; without it one pass over every tile */
+            for (int pass = 0; pass < (th ? 2 : 1); ++pass)
             for (int j0 = 0; j0 < N; j0 += TILE) {
                 int j1 = j0 + TILE < N ? j0 + TILE : N;
                 if (causal && j1 > i + 1) j1 = i + 1;
                 if (j1 <= j0) break;
                 const int hp = th && th->sel[(size_t)(i / QBLK) * th->nkt + j0 / TILE];
+                if (th && hp != pass) continue;
                 double mt = -INFINITY;
                 double *acc = s2, *cj = s2 + TILE;
                 const double *dsb_row = dsb ? dsb + (size_t)(i / QBLK) * N : NULL;
