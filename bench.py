@@ -442,6 +442,29 @@ def run_ours(args, w):
     variants["q_smooth"] = time_variant(qstep, wsq)
     del wsq
 
+    # ThriftAttention (forward only, the page's 5 % budget) against the plain forward: quantize +
+    # forward, median of 20 steps each, L2 flushed
+    tws = None
+
+    def pstep():
+        sa.quantize(t["q"], t["k"], t["v"], w.qk_norm, w.k_smooth, ws=ws)
+        sa.forward(ws, B, H, N, D, w.causal, w.sm_scale, o=o, lse=lse, device=dev)
+
+    def tstep():
+        nonlocal tws
+        _, tws = sa.thrift_quantize(t["q"], t["k"], t["v"], w.causal, 0.05, w.qk_norm, w.k_smooth, ws=ws,
+                                    tws=tws)
+        sa.thrift_forward(ws, tws, B, H, N, D, w.causal, w.sm_scale, o=o, lse=lse, device=dev)
+    plain_fwd = time_variant(pstep, ws)
+    thr = time_variant(tstep, ws)
+    fwd_ops = ops["fwd"]
+    variants["thrift_5pct_forward"] = {
+        "ms_per_step": thr["ms_per_step"], "fwd_tops": fwd_ops / (thr["ms_per_step"] * 1e-3) / 1e12,
+        "plain_forward_ms_per_step": plain_fwd["ms_per_step"],
+        "plain_fwd_tops": fwd_ops / (plain_fwd["ms_per_step"] * 1e-3) / 1e12,
+        "note": "quantize + forward; 5 % of the visible (query block, key tile) pairs in fp16"}
+    del tws
+
     tmax = max_over_ranks(total_ms, dist, dev)
     value = world * ops["fwd_bwd"] * K / (tmax * 1e-3) / 1e12
 

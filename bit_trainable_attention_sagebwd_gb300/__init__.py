@@ -28,7 +28,8 @@ ABI_FUNCTIONS = ("sage_attn_ws_bytes", "sage_attn_bwd_ws_bytes", "sage_attn_quan
                  "sage_attn_timer_only", "sage_attn_bwd_o32", "sage_attn_gqa_ws_bytes",
                  "sage_attn_gqa_bwd_ws_bytes", "sage_attn_gqa_quantize", "sage_attn_gqa_fwd", "sage_attn_gqa_bwd",
                  "sage_attn_gqa_ws_views", "sage_attn_qs_ws_bytes", "sage_attn_qs_quantize", "sage_attn_qs_fwd",
-                 "sage_attn_qs_bwd", "sage_attn_qs_ws_views")
+                 "sage_attn_qs_bwd", "sage_attn_qs_ws_views", "sage_attn_thrift_ws_bytes",
+                 "sage_attn_thrift_quantize", "sage_attn_thrift_fwd", "sage_attn_thrift_sel")
 
 
 class SageError(RuntimeError):
@@ -80,6 +81,12 @@ def lib():
             L.sage_attn_qs_fwd.argtypes = [vp, vp, vp, vp] + [i] * 6 + [fp, vp]
             L.sage_attn_qs_bwd.argtypes = [vp] * 11 + [sz] + [i] * 8 + [fp, vp]
             L.sage_attn_qs_ws_views.argtypes = [vp] + [i] * 5 + [ctypes.POINTER(sage_ws_views)]
+            L.sage_attn_thrift_ws_bytes.restype = sz
+            L.sage_attn_thrift_ws_bytes.argtypes = [i] * 4
+            L.sage_attn_thrift_quantize.argtypes = [vp, vp, vp] + [i] * 7 + [ctypes.c_double, vp, sz, vp, sz, vp]
+            L.sage_attn_thrift_fwd.argtypes = [vp] * 5 + [i] * 5 + [fp, vp]
+            L.sage_attn_thrift_sel.restype = vp
+            L.sage_attn_thrift_sel.argtypes = [vp] + [i] * 4
             L.sage_attn_ws_views.argtypes = [vp, i, i, i, i, ctypes.POINTER(sage_ws_views)]
             L.sage_attn_get_status.argtypes = [vp, vp]
             L.sage_attn_selftest_wait.argtypes = [vp, u64, vp]
@@ -125,6 +132,24 @@ def sage_attn_bwd_o32(Q, K, V, O32, LSE, dO, dQ, dK, dV, ws, bwd_ws, bwd_ws_byte
                       k_smooth, sm_scale, stream):
     return lib().sage_attn_bwd_o32(Q, K, V, O32, LSE, dO, dQ, dK, dV, ws, bwd_ws, bwd_ws_bytes, B, H, N, D,
                                    int(causal), int(qk_norm), int(k_smooth), float(sm_scale), stream)
+
+
+def sage_attn_thrift_ws_bytes(B, H, N, D):
+    return lib().sage_attn_thrift_ws_bytes(B, H, N, D)
+
+
+def sage_attn_thrift_quantize(Q, K, V, B, H, N, D, qk_norm, k_smooth, causal, budget, ws, ws_bytes, tws, tws_bytes,
+                              stream):
+    return lib().sage_attn_thrift_quantize(Q, K, V, B, H, N, D, int(qk_norm), int(k_smooth), int(causal),
+                                           float(budget), ws, ws_bytes, tws, tws_bytes, stream)
+
+
+def sage_attn_thrift_fwd(ws, tws, O, LSE, O32, B, H, N, D, causal, sm_scale, stream):
+    return lib().sage_attn_thrift_fwd(ws, tws, O, LSE, O32, B, H, N, D, int(causal), float(sm_scale), stream)
+
+
+def sage_attn_thrift_sel(tws, B, H, N, D):
+    return lib().sage_attn_thrift_sel(tws, B, H, N, D)
 
 
 def sage_attn_bwd_noalloc(Q, K, V, O, LSE, dO, dQ, dK, dV, ws, B, H, N, D, causal, qk_norm, k_smooth, sm_scale,
@@ -326,6 +351,48 @@ def forward(ws, B, H, N, D, causal, sm_scale=None, o=None, lse=None, o32=False, 
         _check("sage_attn_gqa_fwd", sage_attn_gqa_fwd(_ptr(ws), _ptr(o), _ptr(lse), _ptr(O32), B, H, hkv, N, D,
                                                       causal, sm_scale, _stream_ptr(stream)))
     return (o, lse, O32) if O32 is not None else (o, lse)
+
+
+def thrift_quantize(q, k, v, causal, budget, qk_norm=False, k_smooth=True, ws=None, tws=None, stream=None):
+    """ThriftAttention's quantize pass: the low-bit codes (ws) and the selection of ceil(budget x
+    visible pairs) promoted (query block, key tile) pairs with the fp16 operands of the
+    high-precision path (tws).  Returns (ws, tws)."""
+    import torch
+    B, H, N, D = _shape(q)
+    if ws is None:
+        ws = alloc_ws(B, H, N, D, q.device)
+    if tws is None:
+        n = sage_attn_thrift_ws_bytes(B, H, N, D)
+        if n == 0:
+            raise SageError("sage_attn_thrift_ws_bytes", SAGE_ERR_UNSUPPORTED)
+        tws = torch.empty(n, dtype=torch.uint8, device=q.device)
+    _check("sage_attn_thrift_quantize",
+           sage_attn_thrift_quantize(_ptr(q), _ptr(k), _ptr(v), B, H, N, D, qk_norm, k_smooth, causal, budget,
+                                     _ptr(ws), ws.numel(), _ptr(tws), tws.numel(), _stream_ptr(stream)))
+    return ws, tws
+
+
+def thrift_forward(ws, tws, B, H, N, D, causal, sm_scale=None, o=None, lse=None, o32=False, device="cuda",
+                   stream=None):
+    """ThriftAttention's forward; returns (O bf16, LSE fp32[, O32 fp32])."""
+    import torch
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    if o is None:
+        o = torch.empty((B, H, N, D), dtype=torch.bfloat16, device=device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    O32 = torch.empty((B, H, N, D), dtype=torch.float32, device=device) if o32 is True else (o32 or None)
+    _check("sage_attn_thrift_fwd", sage_attn_thrift_fwd(_ptr(ws), _ptr(tws), _ptr(o), _ptr(lse), _ptr(O32), B, H, N,
+                                                        D, causal, sm_scale, _stream_ptr(stream)))
+    return (o, lse, O32) if O32 is not None else (o, lse)
+
+
+def thrift_sel(tws, B, H, N, D):
+    """The promoted pairs as a uint8 CUDA tensor [B*H, nb, nb] viewing the scratch."""
+    nb = (N + 127) // 128
+    off = sage_attn_thrift_sel(_ptr(tws), B, H, N, D) - tws.data_ptr()
+    return tws[off:off + B * H * nb * nb].view(B * H, nb, nb)
 
 
 def backward(q, k, v, o, lse, do, ws, causal, qk_norm=False, k_smooth=True, sm_scale=None, bwd_ws=None,

@@ -224,6 +224,45 @@ int sage_attn_gqa_ws_views(void* ws, int B, int H, int Hkv, int N, int D, sage_w
   return SAGE_OK;
 }
 
+size_t sage_attn_thrift_ws_bytes(int B, int H, int N, int D) {
+  if (!shape_ok(B, H, N, D)) return 0;
+  return sage::thrift_ws_layout(B, H, N, D).total;
+}
+
+int sage_attn_thrift_quantize(const void* Q, const void* K, const void* V, int B, int H, int N, int D, int qk_norm,
+                              int k_smooth, int causal, double budget, void* ws, size_t ws_bytes, void* tws,
+                              size_t tws_bytes, void* stream) {
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(ws) || !aligned16(tws))
+    return SAGE_ERR_INVALID_ARG;
+  if (!(budget >= 0.0 && budget <= 1.0)) return SAGE_ERR_INVALID_ARG;
+  if (!shape_ok(B, H, N, D)) return SAGE_ERR_UNSUPPORTED;
+  if (ws_bytes < sage::quant_ws_layout(B, H, N, D).total || tws_bytes < sage::thrift_ws_layout(B, H, N, D).total)
+    return SAGE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (int rc = sage::launch_quantize(Q, K, V, B, H, N, D, qk_norm != 0, k_smooth != 0, ws, st)) return rc;
+  return sage::launch_thrift_prepare(Q, K, V, B, H, N, D, qk_norm != 0, causal != 0, budget, ws, tws, st);
+}
+
+int sage_attn_thrift_fwd(const void* ws, const void* tws, void* O, float* LSE, float* O32, int B, int H, int N,
+                         int D, int causal, float sm_scale, void* stream) {
+  if (!aligned16(ws) || !aligned16(tws) || !aligned16(O) || LSE == nullptr || ((uintptr_t)LSE & 3u))
+    return SAGE_ERR_INVALID_ARG;
+  if (O32 != nullptr && !aligned16(O32)) return SAGE_ERR_INVALID_ARG;
+  if (!sage::scale_ok(sm_scale)) return SAGE_ERR_INVALID_ARG;
+  if (!shape_ok(B, H, N, D)) return SAGE_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const float scale = sage::resolve_scale(sm_scale, D);
+  if (int rc = sage::launch_fwd(ws, O, LSE, O32, B, H, N, D, causal != 0, scale, st, 0, false,
+                                const_cast<void*>(tws)))
+    return rc;
+  return sage::launch_thrift_hp(ws, tws, O, LSE, O32, B, H, N, D, causal != 0, scale, st);
+}
+
+uint8_t* sage_attn_thrift_sel(void* tws, int B, int H, int N, int D) {
+  if (tws == nullptr || !shape_ok(B, H, N, D)) return nullptr;
+  return static_cast<uint8_t*>(tws) + sage::thrift_ws_layout(B, H, N, D).sel;
+}
+
 int sage_attn_ws_views(void* ws, int B, int H, int N, int D, sage_ws_views* v) {
   if (ws == nullptr || v == nullptr) return SAGE_ERR_INVALID_ARG;
   if (!shape_ok(B, H, N, D)) return SAGE_ERR_UNSUPPORTED;

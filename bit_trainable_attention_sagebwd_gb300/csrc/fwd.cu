@@ -62,6 +62,12 @@ struct FwdParams {
   const float* sk;
   const float* sv;
   const float* dsb;  // Q-smoothing: [BH][nqb][np] logit terms (nullptr without)
+  // ThriftAttention: the promoted (query block, key tile) pairs [BH][nqb][nqb], skipped here;
+  // query tiles with any hand their unnormalised output (true units, [BH][np][D]) and per row
+  // the running maximum and 448 x the row sum ([BH][np][2]) to the high-precision pass
+  const uint8_t* sel;
+  float* oacc;
+  float* ml;
   __nv_bfloat16* O;
   float* O32;
   float* LSE;
@@ -197,7 +203,9 @@ __device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float 
 // their row sums at the end; each rescales and writes half of the O columns.
 // QS (Q-smoothing): the logit first takes back the query block mean's term in natural units,
 // u = RN(acc RN(s_q s_k) + dsb_j), and u alpha stands where acc c stands otherwise.
-template <int D, bool CAUSAL, bool QS>
+// TH (ThriftAttention): the promoted key tiles of this query tile are skipped (the barriers
+// count processed tiles), and a tile with any promoted pair ends with its unnormalised output.
+template <int D, bool CAUSAL, bool QS, bool TH>
 __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParams& prm, int X, int hh, int qb,
                                                   int bh, uint32_t tmem, volatile int* abort) {
   constexpr int DH = D / 2;  // O columns of this half
@@ -216,12 +224,22 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
   // a wait that runs out raises the abort flag; from then on this thread skips its waits but
   // still runs every tile, so neither half is left behind at a named barrier
   bool ok = true;
+  const uint8_t* srow = TH ? prm.sel + ((size_t)bh * prm.nqb + qb) * prm.nqb : nullptr;
+  int cnt = 0;  // tiles processed (with TH the promoted ones are not)
+  bool hp_any = false;
   // the K-block scale of a tile is fetched one tile early (global latency off the path)
   float sk_next = skh[0];
   for (int j = 0; j < n_tiles; ++j) {
+    if constexpr (TH) {
+      if (srow[j]) {
+        hp_any = true;
+        continue;
+      }
+      sk_next = skh[2 * j];
+    }
     const float skj = sk_next;
-    if (j + 1 < n_tiles) sk_next = skh[2 * (j + 1)];
-    ok = ok && mbar_wait(&sm.bar_s_full[X], j & 1, abort);
+    if (!TH && j + 1 < n_tiles) sk_next = skh[2 * (j + 1)];
+    ok = ok && mbar_wait(&sm.bar_s_full[X], cnt & 1, abort);
     tc_fence_after();
     // with Q-smoothing the tile's logit terms travel with its value tile
     const float* brow = &sm.dsb[j % kVStages][X][hh * 64];
@@ -269,8 +287,8 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
     const float m_new = max3(m, sm.xmax[X][0][t], sm.xmax[X][1][t]);
     const float corr = (m == -INFINITY) ? 0.f : ex2(m - m_new);
     // ---- PV of the previous tile must be complete before P is overwritten and O rescaled
-    if (j > 0) {
-      ok = ok && mbar_wait(&sm.bar_o_done[X], (j - 1) & 1, abort);
+    if (cnt > 0) {
+      ok = ok && mbar_wait(&sm.bar_o_done[X], (cnt - 1) & 1, abort);
       tc_fence_after();
     }
     // ---- t = RN(acc*c - m_new) (one FMA), x = 448 * 2^t, e4m3 codes -> shared memory; one
@@ -348,7 +366,7 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
       l = fmaf(l, corr, la + lb);
     }
     // ---- this half's O columns are rescaled when the row maximum moved (any lane of the warp)
-    if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
+    if (cnt > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
 #pragma unroll 1
       for (int c = 0; c < DH; c += 32) {
         uint32_t o[32];
@@ -366,14 +384,37 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
     fence_proxy_async_smem();
     tc_fence_before();
     mbar_arrive(&sm.bar_p_full[X]);
+    ++cnt;
   }
   // ---- epilogue: O = A * sv / l (l sums 448 p~ over both halves), LSE = ln2 (m + log2(l / 448))
-  ok = ok && mbar_wait(&sm.bar_o_done[X], (n_tiles - 1) & 1, abort);
+  if (cnt > 0) ok = ok && mbar_wait(&sm.bar_o_done[X], (cnt - 1) & 1, abort);
   tc_fence_after();
   sm.xsum[X][hh][t] = l;
   named_bar_tile(X);
   l = sm.xsum[X][0][t] + sm.xsum[X][1][t];  // the same order in both halves
-  if (ok) {
+  if (TH && hp_any) {
+    // the high-precision pass finishes this tile: A sv / 448 (true units) and (m, l) of every row
+    float* dst = prm.oacc + ((size_t)bh * prm.np + row) * D + hh * DH;
+    const float* svh = prm.sv + (size_t)kvh * D + hh * DH;
+#pragma unroll 1
+    for (int c = 0; c < DH; c += 32) {
+      float f[32];
+      if (cnt > 0) {
+        uint32_t o[32];
+        tmem_ld32(o_col + c, o);
+        tmem_wait32(o);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(o[i]) * (svh[c + i] * (1.0f / 448.0f));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) f[i] = 0.f;
+      }
+      float4* d4 = reinterpret_cast<float4*>(dst + c);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) d4[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+    }
+    if (hh == 0) *reinterpret_cast<float2*>(prm.ml + ((size_t)bh * prm.np + row) * 2) = make_float2(m, l);
+  } else if (ok) {
     const float inv_l = 1.0f / l;
     const bool live = row < prm.N;
     const size_t obase = ((size_t)bh * prm.N + row) * D + hh * DH;
@@ -415,7 +456,7 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
 // (each next S once its tile's softmax holds the current S in registers, each PV once its
 // P is written), so the tensor core works on one tile while the other tile's softmax runs.
 // TMEM columns: S_A [0,128), S_B [128,256), O_A [256,256+D), O_B [256+D,256+2D).
-template <int D, bool CAUSAL, bool QS>
+template <int D, bool CAUSAL, bool QS, bool TH>
 __global__ void __launch_bounds__(640, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdParams prm) {
@@ -522,11 +563,24 @@ __global__ void __launch_bounds__(640, 1)
                   sdesc_sw128(v_addr + kk * 32, 16, 1024), idesc_o, (!first || kk > 0));
         umma_commit(&sm.bar_o_done[X]);
       };
+      // tile X takes key tile j (ThriftAttention: unless the pair is promoted); ns, np count
+      // the S and PV issued per tile, which the barrier phases follow
+      const uint8_t* selA = TH ? prm.sel + ((size_t)bh * prm.nqb + qbA) * prm.nqb : nullptr;
+      auto use = [&](int X, int j) -> bool {
+        const int last = X == 0 ? lastA : lastB;
+        if (j > last) return false;
+        if constexpr (TH) return selA[X * prm.nqb + j] == 0;  // tile B's row follows tile A's
+        return true;
+      };
+      int ns[2] = {0, 0}, npv[2] = {0, 0};
       bool ok = mbar_wait(&sm.bar_q, 0, abort) && mbar_wait(&sm.bar_k_full[0], 0, abort);
       if (ok) {
         tc_fence_after();
-        issue_s(0, 0);
-        if (lastB >= 0) issue_s(1, 0);
+        for (int X = 0; X < 2; ++X)
+          if (use(X, 0)) {
+            issue_s(X, 0);
+            ++ns[X];
+          }
         umma_commit(&sm.bar_k_empty[0]);
       }
       for (int j = 0; ok && j < n_kv; ++j) {
@@ -536,25 +590,25 @@ __global__ void __launch_bounds__(640, 1)
         // the next S of a tile as soon as its softmax has read this S into registers (halfway
         // through its exp pass), then the PVs once the P codes are in shared memory
         for (int X = 0; X < 2; ++X) {
-          const int last = X == 0 ? lastA : lastB;
-          if (j + 1 > last) continue;
-          if (!mbar_wait(&sm.bar_s_free[X], j & 1, abort)) {
+          if (!use(X, j + 1)) continue;
+          if (ns[X] > 0 && !mbar_wait(&sm.bar_s_free[X], (ns[X] - 1) & 1, abort)) {
             ok = false;
             break;
           }
           tc_fence_after();
           issue_s(X, j + 1);
+          ++ns[X];
         }
         if (!ok) break;
         for (int X = 0; X < 2; ++X) {
-          const int last = X == 0 ? lastA : lastB;
-          if (j > last) continue;
-          if (!mbar_wait(&sm.bar_p_full[X], j & 1, abort)) {
+          if (!use(X, j)) continue;
+          if (!mbar_wait(&sm.bar_p_full[X], npv[X] & 1, abort)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          issue_pv(X, j, j == 0);
+          issue_pv(X, j, npv[X] == 0);
+          ++npv[X];
         }
         if (!ok) break;
         umma_commit(&sm.bar_v_empty[j % kVStages]);
@@ -565,7 +619,7 @@ __global__ void __launch_bounds__(640, 1)
     regs_increase<kRegsSoftmax>();
     // one call site, so the four warpgroups run (and share instruction-cache lines of) one copy
     const int X = warp >> 3, hh = (warp >> 2) & 1;
-    if (X == 0 || hasB) softmax_tile_loop<D, CAUSAL, QS>(sm, prm, X, hh, X ? qbB : qbA, bh, tmem, abort);
+    if (X == 0 || hasB) softmax_tile_loop<D, CAUSAL, QS, TH>(sm, prm, X, hh, X ? qbB : qbA, bh, tmem, abort);
   }
   tc_fence_before();
   __syncthreads();
@@ -573,12 +627,12 @@ __global__ void __launch_bounds__(640, 1)
   if (tid == 0 && sm.abort) atomicExch(prm.status, kDevTimeout);
 }
 
-template <int D, bool CAUSAL, bool QS>
+template <int D, bool CAUSAL, bool QS, bool TH>
 int launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                  int BH, cudaStream_t st) {
   // at least 120 KB so that one CTA (which takes all 512 TMEM columns) runs per SM
   const size_t smem = sizeof(FwdSmem<D>) + 1024 > 120 * 1024 ? sizeof(FwdSmem<D>) + 1024 : 120 * 1024;
-  auto kern = fwd_kernel<D, CAUSAL, QS>;
+  auto kern = fwd_kernel<D, CAUSAL, QS, TH>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 3;
   ScopedTimer timer("fwd", st);
   if (launch_pdl(kern, dim3(p.npairs * BH), dim3(640), smem, st, tq, tk, tv, p) != cudaSuccess) return 3;
@@ -588,7 +642,7 @@ int launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
 }  // namespace
 
 int launch_fwd(const void* ws, void* O, float* LSE, float* O32, int B, int H, int N, int D, int causal,
-               float sm_scale, cudaStream_t st, int Hkv, bool q_smooth) {
+               float sm_scale, cudaStream_t st, int Hkv, bool q_smooth, void* tws) {
   const QuantWs L = quant_ws_layout(B, H, N, D, Hkv, q_smooth);
   const uint8_t* w = static_cast<const uint8_t*>(ws);
   const int BH = B * H, BHk = B * (Hkv > 0 ? Hkv : H), np = L.np;
@@ -615,17 +669,34 @@ int launch_fwd(const void* ws, void* O, float* LSE, float* O32, int B, int H, in
   p.O32 = O32;
   p.LSE = LSE;
   p.status = reinterpret_cast<int*>(const_cast<uint8_t*>(w) + L.status);
+  p.sel = nullptr;
+  p.oacc = p.ml = nullptr;
+  if (tws) {
+    // ThriftAttention (plain heads, no Q-smoothing): the low-bit tiles here, the promoted ones
+    // in the high-precision pass that follows
+    const ThriftWs T = thrift_ws_layout(B, H, N, D);
+    uint8_t* t = static_cast<uint8_t*>(tws);
+    p.sel = t + T.sel;
+    p.oacc = reinterpret_cast<float*>(t + T.oacc);
+    p.ml = reinterpret_cast<float*>(t + T.ml);
+    if (D == 128)
+      return causal ? launch_fwd_t<128, true, false, true>(tq, tk, tv, p, BH, st)
+                    : launch_fwd_t<128, false, false, true>(tq, tk, tv, p, BH, st);
+    return causal ? launch_fwd_t<64, true, false, true>(tq, tk, tv, p, BH, st)
+                  : launch_fwd_t<64, false, false, true>(tq, tk, tv, p, BH, st);
+  }
   if (q_smooth) {
     if (D == 128)
-      return causal ? launch_fwd_t<128, true, true>(tq, tk, tv, p, BH, st)
-                    : launch_fwd_t<128, false, true>(tq, tk, tv, p, BH, st);
-    return causal ? launch_fwd_t<64, true, true>(tq, tk, tv, p, BH, st)
-                  : launch_fwd_t<64, false, true>(tq, tk, tv, p, BH, st);
+      return causal ? launch_fwd_t<128, true, true, false>(tq, tk, tv, p, BH, st)
+                    : launch_fwd_t<128, false, true, false>(tq, tk, tv, p, BH, st);
+    return causal ? launch_fwd_t<64, true, true, false>(tq, tk, tv, p, BH, st)
+                  : launch_fwd_t<64, false, true, false>(tq, tk, tv, p, BH, st);
   }
   if (D == 128)
-    return causal ? launch_fwd_t<128, true, false>(tq, tk, tv, p, BH, st)
-                  : launch_fwd_t<128, false, false>(tq, tk, tv, p, BH, st);
-  return causal ? launch_fwd_t<64, true, false>(tq, tk, tv, p, BH, st) : launch_fwd_t<64, false, false>(tq, tk, tv, p, BH, st);
+    return causal ? launch_fwd_t<128, true, false, false>(tq, tk, tv, p, BH, st)
+                  : launch_fwd_t<128, false, false, false>(tq, tk, tv, p, BH, st);
+  return causal ? launch_fwd_t<64, true, false, false>(tq, tk, tv, p, BH, st)
+                : launch_fwd_t<64, false, false, false>(tq, tk, tv, p, BH, st);
 }
 
 }  // namespace sage

@@ -14,8 +14,17 @@ namespace sage {
 int launch_quantize(const void* Q, const void* K, const void* V, int B, int H, int N, int D, int qk_norm,
                     int k_smooth, void* ws, cudaStream_t st, bool clear_status = true, int Hkv = 0,
                     bool q_smooth = false);
+// tws (ThriftAttention scratch, thrift_ws_layout): skip the promoted pairs and hand the rows of
+// query tiles that have any to launch_thrift_hp (plain heads only)
 int launch_fwd(const void* ws, void* O, float* LSE, float* O32, int B, int H, int N, int D, int causal,
-               float sm_scale, cudaStream_t st, int Hkv = 0, bool q_smooth = false);
+               float sm_scale, cudaStream_t st, int Hkv = 0, bool q_smooth = false, void* tws = nullptr);
+// ThriftAttention: block means, pair scores and the promoted pairs of ceil(budget x visible
+// pairs) per head, and the fp16 operands of the high-precision path (after launch_quantize)
+int launch_thrift_prepare(const void* Q, const void* K, const void* V, int B, int H, int N, int D, int qk_norm,
+                          int causal, double budget, const void* ws, void* tws, cudaStream_t st);
+// ThriftAttention: the promoted tiles of every query tile that has any, after launch_fwd(..., tws)
+int launch_thrift_hp(const void* ws, const void* tws, void* O, float* LSE, float* O32, int B, int H, int N, int D,
+                     int causal, float sm_scale, cudaStream_t st);
 // O32 (optional, fp32 [B,H,N,D]) replaces O in the row terms D_i = sum_d dO O
 int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO,
                void* dQ, void* dK, void* dV, const void* ws, void* bwd_ws, int B, int H, int N, int D,

@@ -80,4 +80,34 @@ inline BwdWs bwd_ws_layout(int B, int H, int N, int D, int Hkv = 0) {
   return L;
 }
 
+struct ThriftWs {
+  size_t qbar, kbar, keys, sel, q16, k16, v16, oacc, ml, total;
+  int np;
+};
+
+// ThriftAttention scratch: the raw blocks' channel means (fp64), the pair scores as
+// order-preserving keys, the promoted pairs (uint8 [BH][nb][nb]), the high-precision path's
+// fp16 copies of q', k'' and V ([BH][Np][D], rows past N zero), and what the low-bit pass
+// hands over for query tiles with promoted pairs: the unnormalised output (fp32 [BH][Np][D])
+// and per row the running maximum and the row sum ([BH][Np][2])
+inline ThriftWs thrift_ws_layout(int B, int H, int N, int D) {
+  ThriftWs L{};
+  const size_t bh = (size_t)B * H;
+  const int np = pad128(N);
+  const size_t nb = np / 128;
+  size_t o = 0;
+  L.qbar = o;  o = align256(o + bh * nb * D * 8);
+  L.kbar = o;  o = align256(o + bh * nb * D * 8);
+  L.keys = o;  o = align256(o + bh * nb * nb * 8);
+  L.sel = o;   o = align256(o + bh * nb * nb);
+  L.q16 = o;   o = align256(o + bh * np * D * 2);
+  L.k16 = o;   o = align256(o + bh * np * D * 2);
+  L.v16 = o;   o = align256(o + bh * np * D * 2);
+  L.oacc = o;  o = align256(o + bh * np * D * 4);
+  L.ml = o;    o = align256(o + bh * np * 8);
+  L.total = o;
+  L.np = np;
+  return L;
+}
+
 }  // namespace sage

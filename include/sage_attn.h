@@ -206,6 +206,39 @@ int sage_attn_qs_bwd(const void *Q, const void *K, const void *V, const void *O,
 /* Workspace views of the Q-smoothing layout, qmean and dsb included. */
 int sage_attn_qs_ws_views(void *ws, int B, int H, int Hkv, int N, int D, sage_ws_views *views);
 
+/*
+ * ThriftAttention's selective mixed precision, forward only ("ThriftAttention"
+ * (gist.science summary), Methodology steps 1-2 and its implementation paragraph).
+ *  - Selection: the importance of the pair (128-query block I, 128-key tile J) is
+ *    qbar_I . kbar_J, the dot product of the blocks' channel means over the raw Q and K
+ *    (fp64: each mean sums the block's tokens in order and divides by their count; the
+ *    dot product adds the channel products in order).  Of the pairs the mask lets through
+ *    (causal: J <= I) the n = ceil(budget * pairs - 1e-12) largest are promoted, ties in
+ *    index order I * nb + J (nb = Np / 128), per head.
+ *  - Promoted pairs run in high precision: S = q16 . k16 (fp16 copies of q' and of the
+ *    smoothed keys k'' = RN32(k' - kmean), fp32 accumulation), P16 = fp16(p~), O += P16 v16
+ *    (v16 = fp16(V)) in fp32.  The others take the low-bit path of sage_attn_fwd.  A row
+ *    runs its low-bit tiles first and its promoted tiles after them, in one online softmax
+ *    (shared running maximum and row sum).
+ * sage_attn_thrift_ws_bytes: size of the scratch (device memory, caller-owned) that holds
+ *   the selection, the fp16 operands and the low-bit pass's hand-over; 0 for an unsupported
+ *   shape.
+ * sage_attn_thrift_quantize: the quantize pass of sage_attn_quantize into `ws`, then the
+ *   selection and the fp16 operands into `tws`; budget in [0, 1].
+ * sage_attn_thrift_fwd: the forward on `ws` and `tws` from that call; outputs, sm_scale
+ *   and errors as in sage_attn_fwd.
+ * sage_attn_thrift_sel: device pointer to the promoted pairs, uint8 [B*H, nb, nb] (1 =
+ *   promoted), inside `tws`; NULL for an unsupported shape.
+ * Q-smoothing and grouped heads are not combined with this path.
+ */
+size_t sage_attn_thrift_ws_bytes(int B, int H, int N, int D);
+int sage_attn_thrift_quantize(const void *Q, const void *K, const void *V, int B, int H, int N, int D,
+                              int qk_norm, int k_smooth, int causal, double budget, void *ws, size_t ws_bytes,
+                              void *tws, size_t tws_bytes, void *stream);
+int sage_attn_thrift_fwd(const void *ws, const void *tws, void *O, float *LSE, float *O32, int B, int H, int N,
+                         int D, int causal, float sm_scale, void *stream);
+uint8_t *sage_attn_thrift_sel(void *tws, int B, int H, int N, int D);
+
 /* Fill `views` with the device pointers inside a quantize workspace (qmean, dsb: NULL). */
 int sage_attn_ws_views(void *ws, int B, int H, int N, int D, sage_ws_views *views);
 
