@@ -29,7 +29,9 @@ ABI_FUNCTIONS = ("sage_attn_ws_bytes", "sage_attn_bwd_ws_bytes", "sage_attn_quan
                  "sage_attn_gqa_bwd_ws_bytes", "sage_attn_gqa_quantize", "sage_attn_gqa_fwd", "sage_attn_gqa_bwd",
                  "sage_attn_gqa_ws_views", "sage_attn_qs_ws_bytes", "sage_attn_qs_quantize", "sage_attn_qs_fwd",
                  "sage_attn_qs_bwd", "sage_attn_qs_ws_views", "sage_attn_thrift_ws_bytes",
-                 "sage_attn_thrift_quantize", "sage_attn_thrift_fwd", "sage_attn_thrift_sel")
+                 "sage_attn_thrift_quantize", "sage_attn_thrift_fwd", "sage_attn_thrift_sel",
+                 "sage_attn_fp4_ws_bytes", "sage_attn_fp4_quantize", "sage_attn_fp4_fwd",
+                 "sage_attn_fp4_ws_views")
 
 
 class SageError(RuntimeError):
@@ -43,7 +45,8 @@ class sage_ws_views(ctypes.Structure):
                 ("sq", ctypes.c_void_p), ("sk", ctypes.c_void_p), ("sv", ctypes.c_void_p),
                 ("kmean", ctypes.c_void_p), ("qr", ctypes.c_void_p), ("kr", ctypes.c_void_p),
                 ("status", ctypes.c_void_p), ("n_pad", ctypes.c_int), ("qmean", ctypes.c_void_p),
-                ("dsb", ctypes.c_void_p)]
+                ("dsb", ctypes.c_void_p), ("vg", ctypes.c_void_p), ("v4", ctypes.c_void_p),
+                ("v4sf", ctypes.c_void_p)]
 
 
 _lib = None
@@ -81,6 +84,11 @@ def lib():
             L.sage_attn_qs_fwd.argtypes = [vp, vp, vp, vp] + [i] * 6 + [fp, vp]
             L.sage_attn_qs_bwd.argtypes = [vp] * 11 + [sz] + [i] * 8 + [fp, vp]
             L.sage_attn_qs_ws_views.argtypes = [vp] + [i] * 5 + [ctypes.POINTER(sage_ws_views)]
+            L.sage_attn_fp4_ws_bytes.restype = sz
+            L.sage_attn_fp4_ws_bytes.argtypes = [i] * 4
+            L.sage_attn_fp4_quantize.argtypes = [vp, vp, vp] + [i] * 6 + [vp, sz, vp]
+            L.sage_attn_fp4_fwd.argtypes = [vp, vp, vp, vp] + [i] * 5 + [fp, vp]
+            L.sage_attn_fp4_ws_views.argtypes = [vp] + [i] * 4 + [ctypes.POINTER(sage_ws_views)]
             L.sage_attn_thrift_ws_bytes.restype = sz
             L.sage_attn_thrift_ws_bytes.argtypes = [i] * 4
             L.sage_attn_thrift_quantize.argtypes = [vp, vp, vp] + [i] * 7 + [ctypes.c_double, vp, sz, vp, sz, vp]
@@ -132,6 +140,26 @@ def sage_attn_bwd_o32(Q, K, V, O32, LSE, dO, dQ, dK, dV, ws, bwd_ws, bwd_ws_byte
                       k_smooth, sm_scale, stream):
     return lib().sage_attn_bwd_o32(Q, K, V, O32, LSE, dO, dQ, dK, dV, ws, bwd_ws, bwd_ws_bytes, B, H, N, D,
                                    int(causal), int(qk_norm), int(k_smooth), float(sm_scale), stream)
+
+
+def sage_attn_fp4_ws_bytes(B, H, N, D):
+    return lib().sage_attn_fp4_ws_bytes(B, H, N, D)
+
+
+def sage_attn_fp4_quantize(Q, K, V, B, H, N, D, qk_norm, k_smooth, ws, ws_bytes, stream):
+    return lib().sage_attn_fp4_quantize(Q, K, V, B, H, N, D, int(qk_norm), int(k_smooth), ws, ws_bytes, stream)
+
+
+def sage_attn_fp4_fwd(ws, O, LSE, O32, B, H, N, D, causal, sm_scale, stream):
+    return lib().sage_attn_fp4_fwd(ws, O, LSE, O32, B, H, N, D, int(causal), float(sm_scale), stream)
+
+
+def sage_attn_fp4_ws_views(ws, B, H, N, D) -> sage_ws_views:
+    v = sage_ws_views()
+    rc = lib().sage_attn_fp4_ws_views(ws, B, H, N, D, ctypes.byref(v))
+    if rc != SAGE_OK:
+        raise SageError("sage_attn_fp4_ws_views", rc)
+    return v
 
 
 def sage_attn_thrift_ws_bytes(B, H, N, D):
@@ -353,6 +381,36 @@ def forward(ws, B, H, N, D, causal, sm_scale=None, o=None, lse=None, o32=False, 
     return (o, lse, O32) if O32 is not None else (o, lse)
 
 
+def fp4_quantize(q, k, v, qk_norm=False, k_smooth=True, ws=None, stream=None):
+    """Quantize pass of the NVFP4 variant: the INT8 codes of Q and K and V's NVFP4 codes and
+    block scales; returns the workspace tensor."""
+    import torch
+    B, H, N, D = _shape(q)
+    if ws is None:
+        n = sage_attn_fp4_ws_bytes(B, H, N, D)
+        if n == 0:
+            raise SageError("sage_attn_fp4_ws_bytes", SAGE_ERR_UNSUPPORTED)
+        ws = torch.empty(n, dtype=torch.uint8, device=q.device)
+    _check("sage_attn_fp4_quantize", sage_attn_fp4_quantize(_ptr(q), _ptr(k), _ptr(v), B, H, N, D, qk_norm,
+                                                            k_smooth, _ptr(ws), ws.numel(), _stream_ptr(stream)))
+    return ws
+
+
+def fp4_forward(ws, B, H, N, D, causal, sm_scale=None, o=None, lse=None, o32=False, device="cuda", stream=None):
+    """Forward of the NVFP4 variant; returns (O bf16, LSE fp32[, O32 fp32])."""
+    import torch
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    if o is None:
+        o = torch.empty((B, H, N, D), dtype=torch.bfloat16, device=device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    O32 = torch.empty((B, H, N, D), dtype=torch.float32, device=device) if o32 is True else (o32 or None)
+    _check("sage_attn_fp4_fwd", sage_attn_fp4_fwd(_ptr(ws), _ptr(o), _ptr(lse), _ptr(O32), B, H, N, D, causal,
+                                                  sm_scale, _stream_ptr(stream)))
+    return (o, lse, O32) if O32 is not None else (o, lse)
+
+
 def thrift_quantize(q, k, v, causal, budget, qk_norm=False, k_smooth=True, ws=None, tws=None, stream=None):
     """ThriftAttention's quantize pass: the low-bit codes (ws) and the selection of ceil(budget x
     visible pairs) promoted (query block, key tile) pairs with the fp16 operands of the
@@ -466,13 +524,16 @@ def get_status(ws, stream=None) -> int:
     return sage_attn_get_status(_ptr(ws), _stream_ptr(stream))
 
 
-def ws_tensors(ws, B, H, N, D, hkv=None, q_smooth=False) -> dict:
+def ws_tensors(ws, B, H, N, D, hkv=None, q_smooth=False, fp4=False) -> dict:
     """Views of a quantize workspace as torch tensors (for inspection and tests); hkv: key/value
     heads of a grouped-query workspace (K and V sections then hold B*hkv heads); q_smooth: a
-    Q-smoothing workspace (adds qmean [B, H, Np/128, D] and dsb [B, H, Np/128, Np])."""
+    Q-smoothing workspace (adds qmean [B, H, Np/128, D] and dsb [B, H, Np/128, Np]); fp4: an
+    NVFP4 workspace (adds vg [B, H], v4 [B, H, D, Np/2] and v4sf [B, H, Np/64, 512])."""
     import torch
     hk = H if hkv is None else hkv
-    if q_smooth:
+    if fp4:
+        v = sage_attn_fp4_ws_views(_ptr(ws), B, H, N, D)
+    elif q_smooth:
         v = sage_attn_qs_ws_views(_ptr(ws), B, H, hk, N, D)
     elif hk == H:
         v = sage_attn_ws_views(_ptr(ws), B, H, N, D)
@@ -487,6 +548,10 @@ def ws_tensors(ws, B, H, N, D, hkv=None, q_smooth=False) -> dict:
         return ws[off:off + n_bytes].view(dtype).view(shape)
 
     extra = {}
+    if fp4:
+        extra = {"vg": view(v.vg, bk * 4, torch.float32, (B, hk)),
+                 "v4": view(v.v4, bk * D * np_ // 2, torch.uint8, (B, hk, D, np_ // 2)),
+                 "v4sf": view(v.v4sf, bk * (np_ // 64) * 512, torch.uint8, (B, hk, np_ // 64, 512))}
     if q_smooth:
         nb = np_ // 128
         extra = {"qmean": view(v.qmean, bh * nb * D * 4, torch.float32, (B, H, nb, D)),

@@ -63,6 +63,10 @@ void fill_views(uint8_t* w, const sage::QuantWs& L, bool qs, sage_ws_views* v) {
   v->n_pad = L.np;
   v->qmean = qs ? reinterpret_cast<float*>(w + L.qmean) : nullptr;
   v->dsb = qs ? reinterpret_cast<float*>(w + L.dsb) : nullptr;
+  const bool fp4 = L.v4sf > L.v4;
+  v->vg = fp4 ? reinterpret_cast<float*>(w + L.vg) : nullptr;
+  v->v4 = fp4 ? w + L.v4 : nullptr;
+  v->v4sf = fp4 ? w + L.v4sf : nullptr;
 }
 }  // namespace
 
@@ -221,6 +225,37 @@ int sage_attn_gqa_ws_views(void* ws, int B, int H, int Hkv, int N, int D, sage_w
   if (ws == nullptr || v == nullptr) return SAGE_ERR_INVALID_ARG;
   if (!shape_ok(B, H, N, D) || !groups_ok(H, Hkv)) return SAGE_ERR_UNSUPPORTED;
   fill_views(static_cast<uint8_t*>(ws), sage::quant_ws_layout(B, H, N, D, Hkv), false, v);
+  return SAGE_OK;
+}
+
+size_t sage_attn_fp4_ws_bytes(int B, int H, int N, int D) {
+  if (!shape_ok(B, H, N, D)) return 0;
+  return sage::quant_ws_layout(B, H, N, D, 0, false, true).total;
+}
+
+int sage_attn_fp4_quantize(const void* Q, const void* K, const void* V, int B, int H, int N, int D, int qk_norm,
+                           int k_smooth, void* ws, size_t ws_bytes, void* stream) {
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(ws)) return SAGE_ERR_INVALID_ARG;
+  if (!shape_ok(B, H, N, D)) return SAGE_ERR_UNSUPPORTED;
+  if (ws_bytes < sage::quant_ws_layout(B, H, N, D, 0, false, true).total) return SAGE_ERR_INVALID_ARG;
+  return sage::launch_quantize(Q, K, V, B, H, N, D, qk_norm != 0, k_smooth != 0, ws,
+                               static_cast<cudaStream_t>(stream), true, 0, false, true);
+}
+
+int sage_attn_fp4_fwd(const void* ws, void* O, float* LSE, float* O32, int B, int H, int N, int D, int causal,
+                      float sm_scale, void* stream) {
+  if (!aligned16(ws) || !aligned16(O) || LSE == nullptr || ((uintptr_t)LSE & 3u)) return SAGE_ERR_INVALID_ARG;
+  if (O32 != nullptr && !aligned16(O32)) return SAGE_ERR_INVALID_ARG;
+  if (!sage::scale_ok(sm_scale)) return SAGE_ERR_INVALID_ARG;
+  if (!shape_ok(B, H, N, D)) return SAGE_ERR_UNSUPPORTED;
+  return sage::launch_fwd(ws, O, LSE, O32, B, H, N, D, causal != 0, sage::resolve_scale(sm_scale, D),
+                          static_cast<cudaStream_t>(stream), 0, false, nullptr, true);
+}
+
+int sage_attn_fp4_ws_views(void* ws, int B, int H, int N, int D, sage_ws_views* v) {
+  if (ws == nullptr || v == nullptr) return SAGE_ERR_INVALID_ARG;
+  if (!shape_ok(B, H, N, D)) return SAGE_ERR_UNSUPPORTED;
+  fill_views(static_cast<uint8_t*>(ws), sage::quant_ws_layout(B, H, N, D, 0, false, true), false, v);
   return SAGE_OK;
 }
 

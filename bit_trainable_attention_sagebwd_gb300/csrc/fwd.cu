@@ -15,6 +15,7 @@
 // TMEM: S_A, S_B (128 columns each) + O_A, O_B (D columns each).  The tensor core works on one
 // tile while the softmax of the other runs.
 #include <cuda_bf16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 
 #include "kernels.h"
@@ -31,6 +32,7 @@ namespace {
 constexpr int kKStages = 2;
 constexpr int kVStages = 2;
 constexpr float kLog2_448 = 8.807354922057604f;  // log2(448)
+constexpr float kLog2_2688 = 11.392317422778761f;  // log2(448 * 6)
 
 template <int D>
 struct FwdSmem {
@@ -42,6 +44,10 @@ struct FwdSmem {
   float xsum[2][2][128];             // per tile and key half: row sums, exchanged at the end
   // Q-smoothing: the logit terms of tiles A and B for the keys of each value stage
   __align__(16) float dsb[kVStages][2][128];
+  // NVFP4: the block scales of P (one 512-byte atom per 64-key half, as the tensor core reads
+  // them) and of each value stage's V tile (two atoms)
+  __align__(128) uint8_t sfa[2][512];
+  __align__(128) uint8_t sfb[kVStages][1024];
   uint64_t bar_q;
   uint64_t bar_k_full[kKStages], bar_k_empty[kKStages];
   uint64_t bar_v_full[kVStages], bar_v_empty[kVStages];
@@ -68,6 +74,8 @@ struct FwdParams {
   const uint8_t* sel;
   float* oacc;
   float* ml;
+  const float* vg;  // NVFP4: V's tensor scale per key/value head
+  const uint8_t* v4sf;  // NVFP4: V's block-scale atoms [BHk][np/64][512]
   __nv_bfloat16* O;
   float* O32;
   float* LSE;
@@ -117,13 +125,13 @@ __device__ __forceinline__ F2x f2x_add(F2x a, F2x b) {
   return fast_two_sum(s.h, __fadd_rn(s.l, __fadd_rn(a.l, b.l)));
 }
 
-// e4m3 code of RN(448 * RN(2^t)).  t = n + f with n = rint(t) and |f| <= 1/2 (exact);
+// RN(2^t), and the e4m3 code of RN(448 * RN(2^t)).  t = n + f with n = rint(t) and |f| <= 1/2 (exact);
 // 2^f = e^y, y = f ln 2, from the Taylor series of e^y to degree 12 (truncation below
 // 2^-50 for |y| < 0.35): degrees 7..12 in fp32, 0..6 in fp32 pairs, so 2^f carries about
 // 2^-45 relative error and its leading fp32 is RN(2^f) except within that distance of
 // an fp32 midpoint.  Scaling by 2^n is exact in the normal range.
-__device__ __forceinline__ uint32_t exact_p_code(float t) {
-  if (!(t >= -125.f)) return 0u;  // 448 * 2^t is far below the smallest e4m3 subnormal
+__device__ __forceinline__ float exact_pt(float t) {
+  if (!(t >= -125.f)) return 0.f;  // far below anything a code can hold
   const float n = rintf(t);
   const float f = __fsub_rn(t, n);
   const float kLn2Hi = 0x1.62e430p-1f, kLn2Lo = -0x1.05c610p-29f;
@@ -148,8 +156,10 @@ __device__ __forceinline__ uint32_t exact_p_code(float t) {
   F2x r = {q, 0.0f};
 #pragma unroll
   for (int k = 6; k >= 0; --k) r = f2x_add(f2x_mul(r, y), c[k]);
-  const float pt = __fmul_rn(r.h, __int_as_float(((int)n + 127) << 23));
-  return (uint32_t)__nv_cvt_float_to_fp8(__fmul_rn(448.0f, pt), __NV_SATFINITE, __NV_E4M3);
+  return __fmul_rn(r.h, __int_as_float(((int)n + 127) << 23));
+}
+__device__ __forceinline__ uint32_t exact_p_code(float t) {
+  return (uint32_t)__nv_cvt_float_to_fp8(__fmul_rn(448.0f, exact_pt(t)), __NV_SATFINITE, __NV_E4M3);
 }
 
 // a[e] for a run-time e, by a tree of selects (a stays in registers)
@@ -191,6 +201,11 @@ __device__ __forceinline__ float logit_scale(float c) { return c > 0.f ? c : __u
 // named barrier 1 + X over the two warpgroups of tile X
 __device__ __forceinline__ void named_bar_tile(int X) { asm volatile("bar.sync %0, 256;" ::"r"(1 + X) : "memory"); }
 
+// e2m1 codes of two values, the first in the low nibble
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+  return (uint32_t)__nv_cvt_float2_to_fp4x2(make_float2(lo, hi), __NV_E2M1, cudaRoundNearest);
+}
+
 __device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float d) {
   const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
   const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
@@ -205,7 +220,10 @@ __device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float 
 // u = RN(acc RN(s_q s_k) + dsb_j), and u alpha stands where acc c stands otherwise.
 // TH (ThriftAttention): the promoted key tiles of this query tile are skipped (the barriers
 // count processed tiles), and a tile with any promoted pair ends with its unnormalised output.
-template <int D, bool CAUSAL, bool QS, bool TH>
+// F4 (NVFP4 PV): P takes e2m1 codes with an e4m3 scale per 16 keys: y = RN(2688 p~),
+// s = e4m3(RN(max y / 6)), code = e2m1(RN(y / s)); codes and scales near a rounding boundary
+// are redone from an accurate 2^t, so they equal the exact definition.  l sums y (2688 units).
+template <int D, bool CAUSAL, bool QS, bool TH, bool F4>
 __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParams& prm, int X, int hh, int qb,
                                                   int bh, uint32_t tmem, volatile int* abort) {
   constexpr int DH = D / 2;  // O columns of this half
@@ -293,7 +311,91 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
     }
     // ---- t = RN(acc*c - m_new) (one FMA), x = 448 * 2^t, e4m3 codes -> shared memory; one
     // 32-column chunk at a time (reloaded from TMEM), so few registers stay live
-    {
+    if constexpr (F4) {
+      // NVFP4: per 16-key block y = RN(2688 p~), s = e4m3(RN(max y / 6)), codes e2m1(RN(y / s)).
+      // A scale or code whose decision a few ulps could change (checked by rounding the value
+      // moved 2^-18 up and down) is redone from an accurate 2^t and a correctly rounded division.
+      const uint64_t neg_m2 = f2(-m_new, -m_new), cc2 = f2(cc, cc), k2688 = f2(2688.f, 2688.f);
+      constexpr float kUp = 1.0f + 0x1p-18f, kDn = 1.0f - 0x1p-18f;
+      uint64_t lsum2 = f2(0.f, 0.f);
+      uint32_t sfw = 0;  // this half's four block scales (e4m3), block 0 in the low byte
+      // row t of the P tile: 64 bytes (128 keys), 64-byte swizzle: 16-byte unit c at c ^ ((t & 7) >> 1)
+      uint8_t* prow4 = sm.p[X] + (t >> 3) * 512 + (t & 7) * 64;
+#pragma unroll 1
+      for (int q = 0; q < 2; ++q) {
+        uint32_t sv[32];
+        tmem_ld32(s_col + 32 * q, sv);
+        tmem_wait32(sv);
+        if (q == 1) {
+          tc_fence_before();
+          mbar_arrive(&sm.bar_s_free[X]);
+        }
+        if (masked_tile) mask_chunk(sv, lim - hh * 64 - 32 * q);
+        uint32_t cw[4];
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          float y[16];
+          float ym = 0.f;
+#pragma unroll
+          for (int e = 0; e < 16; e += 2) {
+            float t0, t1;
+            f2split(ffma2(f2(__uint_as_float(sv[16 * b + e]), __uint_as_float(sv[16 * b + e + 1])), cc2, neg_m2), t0, t1);
+            const uint64_t y2 = fmul2(f2(ex2(t0), ex2(t1)), k2688);
+            lsum2 = fadd2(lsum2, y2);
+            f2split(y2, y[e], y[e + 1]);
+            ym = max3(ym, y[e], y[e + 1]);
+          }
+          float qs = __fdiv_rn(ym, 6.0f);
+          uint32_t sb = (uint32_t)__nv_cvt_float_to_fp8(qs, __NV_SATFINITE, __NV_E4M3);
+          bool redo = sb != (uint32_t)__nv_cvt_float_to_fp8(qs * kUp, __NV_SATFINITE, __NV_E4M3) ||
+                      sb != (uint32_t)__nv_cvt_float_to_fp8(qs * kDn, __NV_SATFINITE, __NV_E4M3);
+          uint32_t w0 = 0, w1 = 0;
+          float sval = __half2float(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)sb, __NV_E4M3)));
+          if (sval > 0.f) {
+            const float inv = __frcp_rn(sval);
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+              const float q0 = y[e] * inv, q1 = y[e + 1] * inv;
+              const uint32_t c = e2m1x2(q0, q1);
+              redo = redo || c != e2m1x2(q0 * kUp, q1 * kUp) || c != e2m1x2(q0 * kDn, q1 * kDn);
+              if (e < 8) w0 |= c << (4 * e);
+              else w1 |= c << (4 * (e - 8));
+            }
+          }
+          if (redo) {
+            // the definition itself: RN(2^t) accurately, then the correctly rounded steps
+            ym = 0.f;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              y[e] = __fmul_rn(2688.0f, exact_pt(fmaf(__uint_as_float(sv[16 * b + e]), cc, -m_new)));
+              ym = fmaxf(ym, y[e]);
+            }
+            qs = __fdiv_rn(ym, 6.0f);
+            sb = (uint32_t)__nv_cvt_float_to_fp8(qs, __NV_SATFINITE, __NV_E4M3);
+            sval = __half2float(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)sb, __NV_E4M3)));
+            w0 = w1 = 0;
+            if (sval > 0.f) {
+#pragma unroll
+              for (int e = 0; e < 16; e += 2) {
+                const uint32_t c = e2m1x2(__fdiv_rn(y[e], sval), __fdiv_rn(y[e + 1], sval));
+                if (e < 8) w0 |= c << (4 * e);
+                else w1 |= c << (4 * (e - 8));
+              }
+            }
+          }
+          cw[2 * b] = w0;
+          cw[2 * b + 1] = w1;
+          sfw |= sb << (8 * (2 * q + b));
+        }
+        const int unit = 2 * hh + q;  // 32 keys = 16 bytes
+        *reinterpret_cast<uint4*>(prow4 + ((unit ^ ((t & 7) >> 1)) << 4)) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+      }
+      // this half's scales into its atom: row t at byte (t % 32) * 16 + (t / 32) * 4
+      *reinterpret_cast<uint32_t*>(sm.sfa[hh] + (t & 31) * 16 + (t >> 5) * 4) = sfw;
+      float la, lb;
+      f2split(lsum2, la, lb);
+      l = fmaf(l, corr, la + lb);
+    } else {
       const uint64_t neg_m2 = f2(-m_new, -m_new);
       const uint64_t k448 = f2(448.f, 448.f);
       const uint64_t cc2 = f2(cc, cc), al2 = f2(prm.alpha, prm.alpha);
@@ -419,6 +521,8 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
     const bool live = row < prm.N;
     const size_t obase = ((size_t)bh * prm.N + row) * D + hh * DH;
     const float* svh = prm.sv + (size_t)kvh * D + hh * DH;
+    // NVFP4: the accumulator holds sum (2688 P^)(V^ / g) and l sums 2688 p~, so O = acc g / l
+    const float g_l = F4 ? prm.vg[kvh] * inv_l : 0.f;
 #pragma unroll 1
     for (int c = 0; c < DH; c += 32) {
       uint32_t o[32];
@@ -426,7 +530,7 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
       tmem_wait32(o);
       float f[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(o[i]) * (svh[c + i] * inv_l);
+      for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(o[i]) * (F4 ? g_l : svh[c + i] * inv_l);
       if (live) {
         uint4* dst = reinterpret_cast<uint4*>(prm.O + obase + c);
 #pragma unroll
@@ -444,7 +548,8 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
         }
       }
     }
-    if (live && hh == 0) prm.LSE[(size_t)bh * prm.N + row] = (m + (log2f(l) - kLog2_448)) * 0.69314718055994531f;
+    if (live && hh == 0)
+      prm.LSE[(size_t)bh * prm.N + row] = (m + (log2f(l) - (F4 ? kLog2_2688 : kLog2_448))) * 0.69314718055994531f;
   }
 }
 
@@ -456,7 +561,10 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
 // (each next S once its tile's softmax holds the current S in registers, each PV once its
 // P is written), so the tensor core works on one tile while the other tile's softmax runs.
 // TMEM columns: S_A [0,128), S_B [128,256), O_A [256,256+D), O_B [256+D,256+2D).
-template <int D, bool CAUSAL, bool QS, bool TH>
+// F4 (NVFP4 PV): one query tile per CTA (tile A); the TMEM columns of tile B's S hold the
+// scale factors of P and V, two sets of 16 columns used in turn, and PV runs as two
+// kind::mxf4nvf4 MMAs (K = 64 keys each) on packed e2m1 operands with a 64-byte swizzle.
+template <int D, bool CAUSAL, bool QS, bool TH, bool F4>
 __global__ void __launch_bounds__(640, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdParams prm) {
@@ -466,7 +574,7 @@ __global__ void __launch_bounds__(640, 1)
   int px, bh;  // one CTA per (pair of query blocks, head); causal: the longest pairs first
   tile_head_order((int)blockIdx.x, prm.npairs, prm.BH, prm.hgroup, px, bh);
   const int pc = CAUSAL ? (prm.npairs - 1 - px) : px;
-  const int qbA = 2 * pc, qbB = 2 * pc + 1;
+  const int qbA = F4 ? pc : 2 * pc, qbB = F4 ? prm.nqb : 2 * pc + 1;
   const bool hasB = qbB < prm.nqb;
   // KV tiles: tile A needs [0, lastA], tile B [0, lastB]
   const int lastA = CAUSAL ? qbA : prm.nqb - 1;
@@ -530,8 +638,16 @@ __global__ void __launch_bounds__(640, 1)
           tma_load_3d(sm.k[s] + c * 16384, &tm_k, c * 64, j * 128, bh / prm.group, &sm.bar_k_full[s]);
         const int vs = j % kVStages;
         if (j >= kVStages && !mbar_wait(&sm.bar_v_empty[vs], ((j / kVStages) - 1) & 1, abort)) break;
-        mbar_arrive_expect_tx(&sm.bar_v_full[vs], D * 128 + (QS ? (hasB ? 1024 : 512) : 0));
-        tma_load_3d(sm.v[vs], &tm_v, j * 128, 0, bh / prm.group, &sm.bar_v_full[vs]);
+        if constexpr (F4) {
+          // packed e2m1 codes of V ([D][64 bytes], 64-byte swizzle) and their two scale atoms
+          const int kvh = bh / prm.group;
+          mbar_arrive_expect_tx(&sm.bar_v_full[vs], D * 64 + 1024);
+          tma_load_3d(sm.v[vs], &tm_v, j * 64, 0, kvh, &sm.bar_v_full[vs]);
+          bulk_load(sm.sfb[vs], prm.v4sf + ((size_t)kvh * (prm.np / 64) + 2 * j) * 512, 1024, &sm.bar_v_full[vs]);
+        } else {
+          mbar_arrive_expect_tx(&sm.bar_v_full[vs], D * 128 + (QS ? (hasB ? 1024 : 512) : 0));
+          tma_load_3d(sm.v[vs], &tm_v, j * 128, 0, bh / prm.group, &sm.bar_v_full[vs]);
+        }
         if constexpr (QS) {
           // the logit terms of both query tiles for this key tile
           const float* b = prm.dsb + ((size_t)bh * prm.nqb + qbA) * prm.np + j * 128;
@@ -554,13 +670,31 @@ __global__ void __launch_bounds__(640, 1)
         }
         umma_commit(&sm.bar_s_full[X]);
       };
+      int nf4 = 0;  // NVFP4: PVs issued, whose parity picks the scale-factor columns
       auto issue_pv = [&](int X, int j, int first) {
         const uint32_t p_addr = smem_u32(sm.p[X]);
         const uint32_t v_addr = smem_u32(sm.v[j % kVStages]);
+        if constexpr (F4) {
+          // scale factors to TMEM (P's two atoms, then V's), then two K = 64 MMAs; the columns
+          // alternate between PVs, so a copy never lands where an unfinished MMA reads
+          constexpr uint32_t idesc_f4 = idesc_nvf4(128, D);
+          const uint32_t sf = tmem + 128u + 16u * (uint32_t)(nf4 & 1);
+          ++nf4;
   #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma_f8(tmem + 256u + (uint32_t)(X * D), sdesc_sw128(p_addr + kk * 32, 16, 1024),
-                  sdesc_sw128(v_addr + kk * 32, 16, 1024), idesc_o, (!first || kk > 0));
+          for (int h = 0; h < 2; ++h) {
+            tmem_cp_32x128b_x4(sf + 4 * h, sdesc_none(smem_u32(sm.sfa[h]), 128, 128));
+            tmem_cp_32x128b_x4(sf + 8 + 4 * h, sdesc_none(smem_u32(sm.sfb[j % kVStages] + 512 * h), 128, 128));
+          }
+  #pragma unroll
+          for (int h = 0; h < 2; ++h)
+            umma_nvf4(tmem + 256u, sdesc_sw64(p_addr + 32 * h, 16, 512), sdesc_sw64(v_addr + 32 * h, 16, 512), idesc_f4,
+                      sf + 4 * h, sf + 8 + 4 * h, (!first || h > 0));
+        } else {
+  #pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_f8(tmem + 256u + (uint32_t)(X * D), sdesc_sw128(p_addr + kk * 32, 16, 1024),
+                    sdesc_sw128(v_addr + kk * 32, 16, 1024), idesc_o, (!first || kk > 0));
+        }
         umma_commit(&sm.bar_o_done[X]);
       };
       // tile X takes key tile j (ThriftAttention: unless the pair is promoted); ns, np count
@@ -619,7 +753,7 @@ __global__ void __launch_bounds__(640, 1)
     regs_increase<kRegsSoftmax>();
     // one call site, so the four warpgroups run (and share instruction-cache lines of) one copy
     const int X = warp >> 3, hh = (warp >> 2) & 1;
-    if (X == 0 || hasB) softmax_tile_loop<D, CAUSAL, QS, TH>(sm, prm, X, hh, X ? qbB : qbA, bh, tmem, abort);
+    if (X == 0 || hasB) softmax_tile_loop<D, CAUSAL, QS, TH, F4>(sm, prm, X, hh, X ? qbB : qbA, bh, tmem, abort);
   }
   tc_fence_before();
   __syncthreads();
@@ -627,12 +761,12 @@ __global__ void __launch_bounds__(640, 1)
   if (tid == 0 && sm.abort) atomicExch(prm.status, kDevTimeout);
 }
 
-template <int D, bool CAUSAL, bool QS, bool TH>
+template <int D, bool CAUSAL, bool QS, bool TH, bool F4 = false>
 int launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                  int BH, cudaStream_t st) {
   // at least 120 KB so that one CTA (which takes all 512 TMEM columns) runs per SM
   const size_t smem = sizeof(FwdSmem<D>) + 1024 > 120 * 1024 ? sizeof(FwdSmem<D>) + 1024 : 120 * 1024;
-  auto kern = fwd_kernel<D, CAUSAL, QS, TH>;
+  auto kern = fwd_kernel<D, CAUSAL, QS, TH, F4>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 3;
   ScopedTimer timer("fwd", st);
   if (launch_pdl(kern, dim3(p.npairs * BH), dim3(640), smem, st, tq, tk, tv, p) != cudaSuccess) return 3;
@@ -642,8 +776,8 @@ int launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
 }  // namespace
 
 int launch_fwd(const void* ws, void* O, float* LSE, float* O32, int B, int H, int N, int D, int causal,
-               float sm_scale, cudaStream_t st, int Hkv, bool q_smooth, void* tws) {
-  const QuantWs L = quant_ws_layout(B, H, N, D, Hkv, q_smooth);
+               float sm_scale, cudaStream_t st, int Hkv, bool q_smooth, void* tws, bool fp4) {
+  const QuantWs L = quant_ws_layout(B, H, N, D, Hkv, q_smooth, fp4);
   const uint8_t* w = static_cast<const uint8_t*>(ws);
   const int BH = B * H, BHk = B * (Hkv > 0 ? Hkv : H), np = L.np;
   CUtensorMap tq, tk, tv;
@@ -671,6 +805,21 @@ int launch_fwd(const void* ws, void* O, float* LSE, float* O32, int B, int H, in
   p.status = reinterpret_cast<int*>(const_cast<uint8_t*>(w) + L.status);
   p.sel = nullptr;
   p.oacc = p.ml = nullptr;
+  p.vg = reinterpret_cast<const float*>(w + L.vg);
+  p.v4sf = w + L.v4sf;
+  if (fp4) {
+    // NVFP4 PV (plain heads): one query tile per CTA; V's packed e2m1 codes [BHk][D][Np/2]
+    CUtensorMap tv4;
+    if (!make_tmap_3d(&tv4, w + L.v4, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, np / 2, D, BHk, 64, D,
+                      CU_TENSOR_MAP_SWIZZLE_64B))
+      return 3;
+    p.npairs = p.nqb;
+    if (D == 128)
+      return causal ? launch_fwd_t<128, true, false, false, true>(tq, tk, tv4, p, BH, st)
+                    : launch_fwd_t<128, false, false, false, true>(tq, tk, tv4, p, BH, st);
+    return causal ? launch_fwd_t<64, true, false, false, true>(tq, tk, tv4, p, BH, st)
+                  : launch_fwd_t<64, false, false, false, true>(tq, tk, tv4, p, BH, st);
+  }
   if (tws) {
     // ThriftAttention (plain heads, no Q-smoothing): the low-bit tiles here, the promoted ones
     // in the high-precision pass that follows

@@ -11,13 +11,18 @@ namespace sage {
 // q_smooth: Q-smoothing (the query blocks' channel means leave the INT8 codes and come back as
 // a logit term); the workspace then has the layout quant_ws_layout(..., qs = true), and the
 // forward and backward on it take q_smooth too.
+// fp4: also V's NVFP4 codes and block scales (quant_ws_layout(..., fp4 = true))
 int launch_quantize(const void* Q, const void* K, const void* V, int B, int H, int N, int D, int qk_norm,
                     int k_smooth, void* ws, cudaStream_t st, bool clear_status = true, int Hkv = 0,
-                    bool q_smooth = false);
+                    bool q_smooth = false, bool fp4 = false);
+struct QuantWs;
+int launch_vfp4(const void* V, int BHk, int N, int D, void* ws, const QuantWs& L, cudaStream_t st);
 // tws (ThriftAttention scratch, thrift_ws_layout): skip the promoted pairs and hand the rows of
 // query tiles that have any to launch_thrift_hp (plain heads only)
+// fp4: NVFP4 PV on a workspace quantized with fp4 (plain heads only)
 int launch_fwd(const void* ws, void* O, float* LSE, float* O32, int B, int H, int N, int D, int causal,
-               float sm_scale, cudaStream_t st, int Hkv = 0, bool q_smooth = false, void* tws = nullptr);
+               float sm_scale, cudaStream_t st, int Hkv = 0, bool q_smooth = false, void* tws = nullptr,
+               bool fp4 = false);
 // ThriftAttention: block means, pair scores and the promoted pairs of ceil(budget x visible
 // pairs) per head, and the fp16 operands of the high-precision path (after launch_quantize)
 int launch_thrift_prepare(const void* Q, const void* K, const void* V, int B, int H, int N, int D, int qk_norm,

@@ -12,7 +12,7 @@ inline int pad128(int n) { return (n + 127) / 128 * 128; }
 
 struct QuantWs {
   // byte offsets
-  size_t status, sync, qc, kc, v8t, sq, sk, sv, kmean, qr, kr, kpart, vpart, qmean, dsb, total;
+  size_t status, sync, qc, kc, v8t, sq, sk, sv, kmean, qr, kr, kpart, vpart, qmean, dsb, vg, v4, v4sf, total;
   int np;
 };
 
@@ -21,7 +21,11 @@ struct QuantWs {
 // Hkv key/value heads per batch entry (Hkv divides H; 0 means Hkv = H): the Q sections hold
 // B*H heads, the K and V sections B*Hkv.  With Q-smoothing (qs) two more sections per query
 // head: the query blocks' channel means [nb][D] and the logit terms they carry [nb][Np].
-inline QuantWs quant_ws_layout(int B, int H, int N, int D, int Hkv = 0, bool qs = false) {
+// With NVFP4 (fp4) three more per key/value head: V's tensor scale g (fp32), its e2m1 codes
+// packed two per byte [D][Np/2] (channel-major, the lower token in the low nibble) and their
+// e4m3 block scales, one per (channel, 16 tokens), as the tensor core reads them: per 64-token
+// chunk a 512-byte atom, byte (d % 32) * 16 + (d / 32) * 4 + (16-token block within the chunk).
+inline QuantWs quant_ws_layout(int B, int H, int N, int D, int Hkv = 0, bool qs = false, bool fp4 = false) {
   QuantWs L{};
   const size_t bh = (size_t)B * H, bk = (size_t)B * (Hkv > 0 ? Hkv : H);
   const int np = pad128(N);
@@ -42,6 +46,9 @@ inline QuantWs quant_ws_layout(int B, int H, int N, int D, int Hkv = 0, bool qs 
   L.vpart = o;  o = align256(o + bk * nb * D * 4);  // partial channel max |V|
   L.qmean = o;  o = align256(o + (qs ? bh * nb * D * 4 : 0));
   L.dsb = o;    o = align256(o + (qs ? bh * nb * np * 4 : 0));
+  L.vg = o;     o = align256(o + (fp4 ? bk * 4 : 0));
+  L.v4 = o;     o = align256(o + (fp4 ? bk * D * np / 2 : 0));
+  L.v4sf = o;   o = align256(o + (fp4 ? bk * (np / 64) * 512 : 0));
   L.total = o;
   L.np = np;
   return L;

@@ -229,6 +229,24 @@ __device__ __forceinline__ void umma_f8(uint32_t d, uint64_t a, uint64_t b, uint
       "l"(a), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
+// D[tmem] (+)= (A * scale A)[smem] * (B * scale B)[smem]^T: packed e2m1 operands (two per byte,
+// K-major), one ue4m3 scale per 16 values along K for each row of A and of B, read from TMEM
+// (sfa, sfb: four columns each, the 32 x 16-byte atom that tmem_cp_32x128b_x4 writes); fp32
+// accumulate; K = 64 per instruction
+__device__ __forceinline__ void umma_nvf4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                          uint32_t sfb, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+      : "memory");
+}
+// copy a 32-row x 16-byte shared-memory block (descriptor, no swizzle) to TMEM lanes 0-31,
+// columns [taddr, taddr + 4), and the same to lanes 32-63, 64-95 and 96-127
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // arrive once on *bar when every UMMA issued so far by this thread has completed
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -321,6 +339,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// Shared-memory matrix descriptor, 64-byte swizzle (K-major): blocks of 8 rows x 64 bytes
+// (512 B), the 16-byte chunk c of row r at chunk c ^ ((r & 7) >> 1); sbo = 512.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;  // descriptor version for tcgen05
+  d |= 4ull << 61;  // 64-byte swizzle
+  return d;
+}
+
 // Shared-memory matrix descriptor without swizzle: the tile is made of core matrices of
 // 8 rows x 16 bytes (128 contiguous bytes); lbo and sbo are the byte distances between
 // core matrices adjacent along K and along M (or N).
@@ -343,6 +373,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
          | ((b_mn_major ? 1u : 0u) << 16)      // B major-ness
          | ((uint32_t)(N >> 3) << 17)          // N / 8
          | ((uint32_t)(M >> 4) << 24);         // M / 16
+}
+// block-scaled kind::mxf4nvf4: A = B = e2m1, ue4m3 scales (format bit 0), K-major, scale
+// factor ids 0
+__host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
+  return (1u << 7)                     // A = E2M1
+         | (1u << 10)                  // B = E2M1
+         | ((uint32_t)(N >> 3) << 17)  // N / 8
+         | ((uint32_t)(M >> 4) << 24); // M / 16
 }
 __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool a_mn_major = false) {
   return (1u << 4)                         // D = F32

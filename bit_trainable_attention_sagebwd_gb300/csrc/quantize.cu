@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kThreads) kstats_kernel(const __nv_bfloat16* _
                                                            int k_smooth, double* __restrict__ kpart,
                                                            float* __restrict__ vpart, int* __restrict__ cnt,
                                                            float* __restrict__ kmean, float* __restrict__ sv,
-                                                           int* __restrict__ status) {
+                                                           int* __restrict__ status, float* __restrict__ vg) {
   constexpr int TPR = D / 8, RPP = kThreads / TPR, PASSES = 128 / RPP;
   constexpr int J = kThreads / D;  // threads per channel in the combine
   const int blk = blockIdx.x, bh = blockIdx.y, nb = gridDim.x;
@@ -295,6 +295,21 @@ __global__ void __launch_bounds__(kThreads) kstats_kernel(const __nv_bfloat16* _
       for (int u = 0; u < J; ++u) m = fmaxf(m, f_comb[u][tid]);
       sv[(size_t)bh * D + tid] = m > 0.f ? __fdiv_rn(m, 448.0f) : 0.f;
       if (!k_smooth) kmean[(size_t)bh * D + tid] = 0.f;
+    }
+    if (vg != nullptr) {
+      // NVFP4's tensor scale of V: the head's largest |V| / (448 * 6); every thread's m is at
+      // most its channel's maximum, and the threads below D hold the channel maxima
+      __shared__ float s_hm[kThreads / 32];
+      float hm = m;
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) hm = fmaxf(hm, __shfl_xor_sync(0xffffffffu, hm, o));
+      if ((tid & 31) == 0) s_hm[tid >> 5] = hm;
+      __syncthreads();
+      if (tid == 0) {
+        float a = 0.f;
+        for (int w = 0; w < kThreads / 32; ++w) a = fmaxf(a, s_hm[w]);
+        vg[bh] = a > 0.f ? __fdiv_rn(a, 2688.0f) : 0.f;
+      }
     }
   }
 }
@@ -705,8 +720,8 @@ __global__ void __launch_bounds__(kThreads) qs_bias_kernel(const __nv_bfloat16* 
 }  // namespace
 
 int launch_quantize(const void* Q, const void* K, const void* V, int B, int H, int N, int D, int qk_norm,
-                    int k_smooth, void* ws, cudaStream_t st, bool clear_status, int Hkv, bool q_smooth) {
-  const QuantWs L = quant_ws_layout(B, H, N, D, Hkv, q_smooth);
+                    int k_smooth, void* ws, cudaStream_t st, bool clear_status, int Hkv, bool q_smooth, bool fp4) {
+  const QuantWs L = quant_ws_layout(B, H, N, D, Hkv, q_smooth, fp4);
   const int BHk = B * (Hkv > 0 ? Hkv : H);
   uint8_t* w = static_cast<uint8_t*>(ws);
   const int nb = L.np / 128;
@@ -734,13 +749,16 @@ int launch_quantize(const void* Q, const void* K, const void* V, int B, int H, i
     return 3;
   int* cnt = reinterpret_cast<int*>(w + L.sync);
   if (launch_pdl(stats, dim3(nb, BHk, k_smooth ? 2 : 1), dim3(kThreads), stage, st, k, v, N, k_smooth, kpart, vpart,
-                 cnt, kmean, sv, status) != cudaSuccess)
+                 cnt, kmean, sv, status, fp4 ? reinterpret_cast<float*>(w + L.vg) : nullptr) != cudaSuccess)
     return 3;
   if (launch_pdl(quant, qgrid, dim3(kThreads), stage, st, q, k, v, N, k_smooth, (const float*)kmean, (const float*)sv,
                  reinterpret_cast<__nv_bfloat16*>(w + L.qc), reinterpret_cast<__nv_bfloat16*>(w + L.kc), w + L.v8t,
                  reinterpret_cast<float*>(w + L.sq), reinterpret_cast<float*>(w + L.sk),
                  reinterpret_cast<float*>(w + L.qr), reinterpret_cast<float*>(w + L.kr), status, BHk) != cudaSuccess)
     return 3;
+  // NVFP4 V codes after the quantize pass (its tensor scale comes from kstats)
+  if (fp4)
+    if (int rc = launch_vfp4(V, BHk, N, D, ws, L, st)) return rc;
   if (q_smooth) {
     auto qsq = D == 128 ? (qk_norm ? qsmooth_q_kernel<128, true> : qsmooth_q_kernel<128, false>)
                         : (qk_norm ? qsmooth_q_kernel<64, true> : qsmooth_q_kernel<64, false>);

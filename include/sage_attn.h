@@ -80,6 +80,11 @@ typedef struct sage_ws_views {
   int n_pad;     /* Np                                                               */
   float *qmean;  /* Q-smoothing: [B*H, Np/128, D] query block means (else NULL)      */
   float *dsb;    /* Q-smoothing: [B*H, Np/128, Np] logit terms (else NULL)           */
+  float *vg;     /* NVFP4: [B*H] V's tensor scale max|V| / 2688 (else NULL)          */
+  uint8_t *v4;   /* NVFP4: [B*H, D, Np/2] V's e2m1 codes, two per byte, the lower    */
+                 /*        token in the low nibble (else NULL)                       */
+  uint8_t *v4sf; /* NVFP4: [B*H, Np/64, 512] V's e4m3 block scales; in atom c (tokens */
+                 /*        64c ..) byte (d % 32) * 16 + (d / 32) * 4 + 16-token block */
 } sage_ws_views;
 
 /* Bytes of the quantize workspace for this shape (0 if unsupported). It holds the
@@ -238,6 +243,35 @@ int sage_attn_thrift_quantize(const void *Q, const void *K, const void *V, int B
 int sage_attn_thrift_fwd(const void *ws, const void *tws, void *O, float *LSE, float *O32, int B, int H, int N,
                          int D, int causal, float sm_scale, void *stream);
 uint8_t *sage_attn_thrift_sel(void *tws, int B, int H, int N, int D);
+
+/*
+ * NVFP4 variant of the forward PV ("Attn-QAT: 4-Bit Attention With Quantization-Aware
+ * Training" (gist.science summary), Methodology principle 1 and Implementation: attention
+ * trained in FP4 on Blackwell's FP4 path; "ThriftAttention" (gist.science summary),
+ * Methodology step 2: the NVFP4 format).  The pages print no recipe; this is NVFP4 for P and
+ * V with the rest of the scheme unchanged:
+ *  - e2m1 codes (0, 0.5, 1, 1.5, 2, 3, 4, 6, signed; nearest, ties to the even code,
+ *    saturating), one e4m3 scale per 16 consecutive values along the contracted axis (keys),
+ *    one fp32 scale per tensor;
+ *  - V, per head: g = RN32(max|V| / 2688); per channel and 16-token block
+ *    s = e4m3(RN32(amax / RN32(6 g))), code = e2m1(RN32(v / RN32(s g)));
+ *  - P, per row and 16-key block of the online softmax's p~ (relative to the running maximum):
+ *    y = RN32(2688 p~), s = e4m3(RN32(max y / 6)), code = e2m1(RN32(y / s)); P^ = code s / 2688;
+ *  - O = sum(P^ V^) / l with l the sum of the fp32 p~; QK^T stays INT8.
+ * The tensor core multiplies the e2m1 codes and their block scales
+ * (tcgen05.mma kind::mxf4nvf4.block_scale); the codes and scales equal the definition above
+ * bit for bit.
+ * sage_attn_fp4_ws_bytes: workspace size; sage_attn_fp4_quantize: the quantize pass plus V's
+ * NVFP4 codes and scales; sage_attn_fp4_fwd: the forward on that workspace (outputs, sm_scale
+ * and errors as in sage_attn_fwd); sage_attn_fp4_ws_views: the workspace's pointers, vg, v4
+ * and v4sf included.  Plain heads (no grouped heads, no Q-smoothing).
+ */
+size_t sage_attn_fp4_ws_bytes(int B, int H, int N, int D);
+int sage_attn_fp4_quantize(const void *Q, const void *K, const void *V, int B, int H, int N, int D, int qk_norm,
+                           int k_smooth, void *ws, size_t ws_bytes, void *stream);
+int sage_attn_fp4_fwd(const void *ws, void *O, float *LSE, float *O32, int B, int H, int N, int D, int causal,
+                      float sm_scale, void *stream);
+int sage_attn_fp4_ws_views(void *ws, int B, int H, int N, int D, sage_ws_views *views);
 
 /* Fill `views` with the device pointers inside a quantize workspace (qmean, dsb: NULL). */
 int sage_attn_ws_views(void *ws, int B, int H, int N, int D, sage_ws_views *views);
