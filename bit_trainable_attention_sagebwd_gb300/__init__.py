@@ -31,7 +31,7 @@ ABI_FUNCTIONS = ("sage_attn_ws_bytes", "sage_attn_bwd_ws_bytes", "sage_attn_quan
                  "sage_attn_qs_bwd", "sage_attn_qs_ws_views", "sage_attn_thrift_ws_bytes",
                  "sage_attn_thrift_quantize", "sage_attn_thrift_fwd", "sage_attn_thrift_sel",
                  "sage_attn_fp4_ws_bytes", "sage_attn_fp4_quantize", "sage_attn_fp4_fwd",
-                 "sage_attn_fp4_ws_views")
+                 "sage_attn_fp4_ws_views", "sage_attn_fp4_bwd_ws_bytes", "sage_attn_fp4_bwd")
 
 
 class SageError(RuntimeError):
@@ -89,6 +89,9 @@ def lib():
             L.sage_attn_fp4_quantize.argtypes = [vp, vp, vp] + [i] * 6 + [vp, sz, vp]
             L.sage_attn_fp4_fwd.argtypes = [vp, vp, vp, vp] + [i] * 5 + [fp, vp]
             L.sage_attn_fp4_ws_views.argtypes = [vp] + [i] * 4 + [ctypes.POINTER(sage_ws_views)]
+            L.sage_attn_fp4_bwd_ws_bytes.restype = sz
+            L.sage_attn_fp4_bwd_ws_bytes.argtypes = [i] * 4
+            L.sage_attn_fp4_bwd.argtypes = [vp] * 11 + [sz] + [i] * 7 + [fp, vp]
             L.sage_attn_thrift_ws_bytes.restype = sz
             L.sage_attn_thrift_ws_bytes.argtypes = [i] * 4
             L.sage_attn_thrift_quantize.argtypes = [vp, vp, vp] + [i] * 7 + [ctypes.c_double, vp, sz, vp, sz, vp]
@@ -152,6 +155,16 @@ def sage_attn_fp4_quantize(Q, K, V, B, H, N, D, qk_norm, k_smooth, ws, ws_bytes,
 
 def sage_attn_fp4_fwd(ws, O, LSE, O32, B, H, N, D, causal, sm_scale, stream):
     return lib().sage_attn_fp4_fwd(ws, O, LSE, O32, B, H, N, D, int(causal), float(sm_scale), stream)
+
+
+def sage_attn_fp4_bwd_ws_bytes(B, H, N, D):
+    return lib().sage_attn_fp4_bwd_ws_bytes(B, H, N, D)
+
+
+def sage_attn_fp4_bwd(Q, K, V, O, LSE, dO, dQ, dK, dV, ws, bwd_ws, bwd_ws_bytes, B, H, N, D, causal, qk_norm,
+                      k_smooth, sm_scale, stream):
+    return lib().sage_attn_fp4_bwd(Q, K, V, O, LSE, dO, dQ, dK, dV, ws, bwd_ws, bwd_ws_bytes, B, H, N, D,
+                                   int(causal), int(qk_norm), int(k_smooth), float(sm_scale), stream)
 
 
 def sage_attn_fp4_ws_views(ws, B, H, N, D) -> sage_ws_views:
@@ -409,6 +422,28 @@ def fp4_forward(ws, B, H, N, D, causal, sm_scale=None, o=None, lse=None, o32=Fal
     _check("sage_attn_fp4_fwd", sage_attn_fp4_fwd(_ptr(ws), _ptr(o), _ptr(lse), _ptr(O32), B, H, N, D, causal,
                                                   sm_scale, _stream_ptr(stream)))
     return (o, lse, O32) if O32 is not None else (o, lse)
+
+
+def fp4_backward(q, k, v, o, lse, do, ws, causal, qk_norm=False, k_smooth=True, sm_scale=None, bwd_ws=None,
+                 dq=None, dk=None, dv=None, stream=None):
+    """Backward of the NVFP4 variant (P^ recomputed in NVFP4); returns (dQ, dK, dV) bf16."""
+    import torch
+    B, H, N, D = _shape(q)
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    if bwd_ws is None:
+        n = sage_attn_fp4_bwd_ws_bytes(B, H, N, D)
+        if n == 0:
+            raise SageError("sage_attn_fp4_bwd_ws_bytes", SAGE_ERR_UNSUPPORTED)
+        bwd_ws = torch.empty(n, dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check("sage_attn_fp4_bwd",
+           sage_attn_fp4_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
+                             _ptr(ws), _ptr(bwd_ws), bwd_ws.numel(), B, H, N, D, causal, qk_norm, k_smooth, sm_scale,
+                             _stream_ptr(stream)))
+    return dq, dk, dv
 
 
 def thrift_quantize(q, k, v, causal, budget, qk_norm=False, k_smooth=True, ws=None, tws=None, stream=None):

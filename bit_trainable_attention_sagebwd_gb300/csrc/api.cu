@@ -252,6 +252,26 @@ int sage_attn_fp4_fwd(const void* ws, void* O, float* LSE, float* O32, int B, in
                           static_cast<cudaStream_t>(stream), 0, false, nullptr, true);
 }
 
+size_t sage_attn_fp4_bwd_ws_bytes(int B, int H, int N, int D) {
+  if (!shape_ok(B, H, N, D)) return 0;
+  return sage::bwd_ws_layout(B, H, N, D, 0, true).total;
+}
+
+int sage_attn_fp4_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO,
+                      void* dQ, void* dK, void* dV, const void* ws, void* bwd_ws, size_t bwd_ws_bytes, int B, int H,
+                      int N, int D, int causal, int qk_norm, int k_smooth, float sm_scale, void* stream) {
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(dO) || !aligned16(dQ) ||
+      !aligned16(dK) || !aligned16(dV) || !aligned16(ws) || !aligned16(bwd_ws) || LSE == nullptr ||
+      ((uintptr_t)LSE & 3u))
+    return SAGE_ERR_INVALID_ARG;
+  if (!sage::scale_ok(sm_scale)) return SAGE_ERR_INVALID_ARG;
+  if (!shape_ok(B, H, N, D)) return SAGE_ERR_UNSUPPORTED;
+  if (bwd_ws_bytes < sage::bwd_ws_layout(B, H, N, D, 0, true).total) return SAGE_ERR_INVALID_ARG;
+  return sage::launch_bwd(Q, K, V, O, LSE, dO, dQ, dK, dV, ws, bwd_ws, B, H, N, D, causal != 0, qk_norm != 0,
+                          k_smooth != 0, sage::resolve_scale(sm_scale, D), static_cast<cudaStream_t>(stream), nullptr,
+                          0, false, true);
+}
+
 int sage_attn_fp4_ws_views(void* ws, int B, int H, int N, int D, sage_ws_views* v) {
   if (ws == nullptr || v == nullptr) return SAGE_ERR_INVALID_ARG;
   if (!shape_ok(B, H, N, D)) return SAGE_ERR_UNSUPPORTED;

@@ -27,6 +27,7 @@
 #include <cstddef>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 
 #include "../../include/sage_attn.h"
@@ -44,7 +45,24 @@ namespace sage {
 namespace {
 
 constexpr float kLog2_448 = 8.807354922057604f;
+constexpr float kLog2_6 = 2.584962500721156f;
 constexpr int kPreThreads = 256;
+
+// e2m1 codes of two values, the first in the low nibble
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+  return (uint32_t)__nv_cvt_float2_to_fp4x2(make_float2(lo, hi), __NV_E2M1, cudaRoundNearest);
+}
+// the eight e2m1 codes of a word (low nibble first) times the e4m3 scale sbyte
+__device__ __forceinline__ void fp4_decode8(uint32_t w, uint32_t sbyte, float (&v)[8]) {
+  const float s = __half2float(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)sbyte, __NV_E4M3)));
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const __half2_raw h = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)((w >> (8 * b)) & 255u), __NV_E2M1);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+    v[2 * b] = f.x * s;
+    v[2 * b + 1] = f.y * s;
+  }
+}
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -187,6 +205,29 @@ __global__ void __launch_bounds__(kPreThreads, 4) bwd_do8_kernel(const __nv_bflo
   }
 }
 
+// NVFP4 backward: the e4m3 codes of dO ([BH][D][Np] bytes) as bf16 values (exact), 16 per thread
+__global__ void __launch_bounds__(256) do8_bf16_kernel(const uint8_t* __restrict__ do8t, size_t n16,
+                                                      __nv_bfloat16* __restrict__ do16) {
+  pdl_wait();  // the codes come from bwd_do8
+  pdl_trigger();
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x) {
+    const uint4 u = reinterpret_cast<const uint4*>(do8t)[i];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const __half2_raw h =
+          __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)((w[k >> 1] >> (16 * (k & 1))) & 0xffffu), __NV_E4M3);
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+      const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+      o[k] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(do16) + 2 * i;
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
 // ------------------------------------------------------------------ bwd_main
 template <int D>
 struct BwdSmem {
@@ -210,6 +251,7 @@ struct BwdSmem {
   uint64_t bar_q_full[2], bar_do_full, bar_do8_full;
   uint64_t bar_q_free[2], bar_do_free, bar_do8_free;
   uint64_t bar_s, bar_dp, bar_p, bar_ds[2], bar_dk, bar_part, bar_free_s, bar_free_dp, bar_cs;
+  uint64_t bar_dv;  // NVFP4: the dV MMA has read P^ (which shares the dS block)
   uint32_t tmem_base;
   int abort;
   int last;  // split query heads: this CTA is the last of its key block to finish
@@ -270,7 +312,12 @@ constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23: x + M - M rounds x to
 // QS (Q-smoothing): the logit is u = RN(acc RN(s_q s_k) + dsb_j) and P = 2^(u alpha + bias);
 // the dS codes' column sums (an extra MMA against ones into TMEM columns [128,144), read
 // before dQ1 overwrites them) give dK its term s_dS (sum_i dS8_ij) qmean_I.
-template <int D, bool QS>
+// F4 (NVFP4): P^ is recomputed in NVFP4 per 16-key block, y = 2688 P, s = e4m3(max y / 6),
+// code = e2m1(y / s); dS = P^ (dP - D) and dV = P^T dO8 use it, dV on bf16 tensor cores
+// (code s and the e4m3 codes of dO are exact in bf16; P^'s scales run along the keys, which
+// dV does not contract).  P^ (bf16) is written into the dS block, which the dS codes take
+// over once the dV MMA has read it; dO's codes come as bf16 in the dO8 and P regions.
+template <int D, bool QS, bool F4>
 __global__ void __launch_bounds__(384, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -321,6 +368,7 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&sm.bar_free_s, 256);
     mbar_init(&sm.bar_free_dp, 256);
     mbar_init(&sm.bar_cs, 256);
+    mbar_init(&sm.bar_dv, 1);
     sm.abort = 0;
     fence_mbar_init();
   }
@@ -368,8 +416,15 @@ __global__ void __launch_bounds__(384, 1)
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d(sm.dob + c * 16384, &tm_do, c * 64, I * 128, qh, &sm.bar_do_full);
         if (it > 0 && !mbar_wait(&sm.bar_do8_free, (it - 1) & 1, abort)) break;
-        mbar_arrive_expect_tx(&sm.bar_do8_full, D * 128);
-        tma_load_3d(sm.do8, &tm_do8, I * 128, 0, qh, &sm.bar_do8_full);
+        if constexpr (F4) {
+          // the e4m3 codes of dO as bf16, channel-major, in two 64-query boxes
+          mbar_arrive_expect_tx(&sm.bar_do8_full, D * 256);
+          tma_load_3d(sm.do8, &tm_do8, I * 128, 0, qh, &sm.bar_do8_full);
+          tma_load_3d(sm.do8 + D * 128, &tm_do8, I * 128 + 64, 0, qh, &sm.bar_do8_full);
+        } else {
+          mbar_arrive_expect_tx(&sm.bar_do8_full, D * 128);
+          tma_load_3d(sm.do8, &tm_do8, I * 128, 0, qh, &sm.bar_do8_full);
+        }
         const int qs = it & 1;
         if (it > 1 && !mbar_wait(&sm.bar_q_free[qs], ((it >> 1) - 1) & 1, abort)) break;
         mbar_arrive_expect_tx(&sm.bar_q_full[qs], kTile + 1024);
@@ -422,11 +477,23 @@ __global__ void __launch_bounds__(384, 1)
         umma_commit(&sm.bar_do_free);
         if (!mbar_wait(&sm.bar_p, ph, abort) || !mbar_wait(&sm.bar_do8_full, ph, abort)) break;
         tc_fence_after();
-        // dV[key, d] += sum_q P[q, key] dO8[q, d]: 32 query rows per step
+        if constexpr (F4) {
+          // dV[key, d] += sum_q (2688 P^)[q, key] dO8[q, d] on bf16: A read MN-major from the query
+          // rows of the dS block, B = dO8 codes K-major in two 64-query atoms; 16 queries per step
+          constexpr uint32_t id_dv16 = idesc_bf16(128, D, true, false);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma_f8(tmem + cDV, sdesc_sw128(a_p + kk * 4096, 16384, 1024), sdesc_sw128(a_do8 + kk * 32, 16, 1024),
-                  id_dv, (it > 0 || kk > 0));
+          for (int kk = 0; kk < 8; ++kk)
+            umma_bf16(tmem + cDV, sdesc_sw128(a_ds + kk * 2048, 16384, 1024),
+                      sdesc_sw128(a_do8 + (kk >> 2) * (D * 128) + (kk & 3) * 32, 16, 1024), id_dv16,
+                      (it > 0 || kk > 0));
+          umma_commit(&sm.bar_dv);
+        } else {
+          // dV[key, d] += sum_q P[q, key] dO8[q, d]: 32 query rows per step
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_f8(tmem + cDV, sdesc_sw128(a_p + kk * 4096, 16384, 1024), sdesc_sw128(a_do8 + kk * 32, 16, 1024),
+                    id_dv, (it > 0 || kk > 0));
+        }
         umma_commit(&sm.bar_do8_free);
         // dK first, once both groups' codes are in, so its readout starts as early as possible
         if (!mbar_wait(&sm.bar_ds[0], ph, abort) || !mbar_wait(&sm.bar_ds[1], ph, abort)) break;
@@ -517,6 +584,8 @@ __global__ void __launch_bounds__(384, 1)
       // to shared memory for the dV MMA and stay in registers for dS.
       uint32_t buf[2][32];
       uint32_t pw[2][8];
+      uint32_t pf[F4 ? 8 : 1];  // NVFP4: the 64 keys' e2m1 codes, key 8i + k at nibble k of pf[i]
+      uint32_t psc = 0;         // NVFP4: the four 16-key blocks' e4m3 scales, block 0 low
 #pragma unroll
       for (int c = 0; c < 2; ++c) tmem_ld32(tmem + lane_base + cS + kcol + 32 * c, buf[c]);
       tmem_ld_wait();
@@ -543,6 +612,65 @@ __global__ void __launch_bounds__(384, 1)
             return ffma2(a2, cs2, b2);
           }
         };
+        if constexpr (F4) {
+          // NVFP4 P^ per 16-key block: y = 2688 P (the exponent takes log2 6 more), codes e2m1(y / s)
+          // with s = e4m3(max y / 6); the codes and the four scales stay in registers for dS
+          const uint64_t b6 = f2(kLog2_6, kLog2_6);
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+              float y[16];
+              float ym = 0.f;
+#pragma unroll
+              for (int e = 0; e < 16; e += 2) {
+                float z0, z1;
+                f2split(fadd2(arg(buf[c][16 * b + e], buf[c][16 * b + e + 1], 32 * c + 16 * b + e), b6), z0, z1);
+                y[e] = ex2(z0);
+                y[e + 1] = ex2(z1);
+                ym = max3(ym, y[e], y[e + 1]);
+              }
+              const uint32_t sb = (uint32_t)__nv_cvt_float_to_fp8(ym * (1.0f / 6.0f), __NV_SATFINITE, __NV_E4M3);
+              const float sval = __half2float(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)sb, __NV_E4M3)));
+              uint32_t w0 = 0, w1 = 0;
+              if (sval > 0.f) {
+                const float inv = 1.0f / sval;
+#pragma unroll
+                for (int e = 0; e < 16; e += 2) {
+                  const uint32_t cd = e2m1x2(y[e] * inv, y[e + 1] * inv);
+                  if (e < 8) w0 |= cd << (4 * e);
+                  else w1 |= cd << (4 * (e - 8));
+                }
+              }
+              pf[4 * c + 2 * b] = w0;
+              pf[4 * c + 2 * b + 1] = w1;
+              psc |= sb << (8 * (2 * c + b));
+            }
+          }
+          // P^ (2688 units, bf16) into this group's dS block: the previous iteration's dQ boxes
+          // there must have been read first
+          if (t == 0 && pending_qs >= 0) {
+            bulk_wait_read_all();
+            mbar_arrive(&sm.bar_q_free[pending_qs]);
+            pending_qs = -1;
+          }
+          named_bar_group(g);
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              float v[8];
+              fp4_decode8(pf[4 * c + u], psc >> (8 * (2 * c + (u >> 1))) & 255u, v);
+              uint32_t h[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat162 hv = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+                h[e] = *reinterpret_cast<const uint32_t*>(&hv);
+              }
+              *reinterpret_cast<uint4*>(dsrow + (((4 * c + u) ^ (t & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+            }
+          }
+        } else {
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
 #pragma unroll
@@ -564,6 +692,7 @@ __global__ void __launch_bounds__(384, 1)
           *reinterpret_cast<uint4*>(prow + (((u0 + 1) ^ (t & 7)) << 4)) =
               make_uint4(pw[c][4], pw[c][5], pw[c][6], pw[c][7]);
         }
+        }
       }
       fence_proxy_async_smem();
       mbar_arrive(&sm.bar_p);
@@ -576,7 +705,28 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
       for (int c = 0; c < 2; ++c) reg_fence32(buf[c]);
       float amax = 0.f;
-      {
+      if constexpr (F4) {
+        // 2688 dS = (2688 P^) (dP - D_i)
+        const uint64_t d2 = f2(dvec_t, dvec_t);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            float pv[8];
+            fp4_decode8(pf[(32 * c + e) >> 3], (psc >> (8 * ((32 * c + e) >> 4))) & 255u, pv);
+#pragma unroll
+            for (int u = 0; u < 8; u += 2) {
+              float x0, x1;
+              f2split(fmul2(f2(pv[u], pv[u + 1]),
+                            fsub2(f2(__uint_as_float(buf[c][e + u]), __uint_as_float(buf[c][e + u + 1])), d2)),
+                      x0, x1);
+              amax = max3(amax, fabsf(x0), fabsf(x1));
+              buf[c][e + u] = __float_as_uint(x0);
+              buf[c][e + u + 1] = __float_as_uint(x1);
+            }
+          }
+        }
+      } else {
         const uint64_t d2 = f2(dvec_t, dvec_t);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -611,6 +761,11 @@ __global__ void __launch_bounds__(384, 1)
         pending_qs = -1;
       }
       named_bar_group(g);
+      // NVFP4: the dS codes take the block over once the dV MMA has read P^ from it
+      if constexpr (F4) {
+        ok = ok && mbar_wait(&sm.bar_dv, ph, abort);
+        tc_fence_after();
+      }
       // the group's tile (128 queries x 64 keys) max; values are 448 dS
       const float amine = fmaxf(fmaxf(sm.smax[4 * g], sm.smax[4 * g + 1]), fmaxf(sm.smax[4 * g + 2], sm.smax[4 * g + 3]));
       const float inv = amine > 0.f ? 127.0f / amine : 0.f;  // code = rint(448 dS * 127 / max|448 dS|)
@@ -659,8 +814,8 @@ __global__ void __launch_bounds__(384, 1)
       const float a0 = fmaxf(fmaxf(sm.smax[0], sm.smax[1]), fmaxf(sm.smax[2], sm.smax[3]));
       const float a1 = fmaxf(fmaxf(sm.smax[4], sm.smax[5]), fmaxf(sm.smax[6], sm.smax[7]));
       // values are 448 * dS: scale s_dS = max|dS| / 127
-      const float sds0 = a0 > 0.f ? __fdiv_rn(a0 * (1.0f / 448.0f), 127.0f) : 0.f;
-      const float sds1 = a1 > 0.f ? __fdiv_rn(a1 * (1.0f / 448.0f), 127.0f) : 0.f;
+      const float sds0 = a0 > 0.f ? __fdiv_rn(a0 * (F4 ? 1.0f / 2688.0f : 1.0f / 448.0f), 127.0f) : 0.f;
+      const float sds1 = a1 > 0.f ? __fdiv_rn(a1 * (F4 ? 1.0f / 2688.0f : 1.0f / 448.0f), 127.0f) : 0.f;
       const float ck = __fmul_rn(t >> 6 ? sds1 : sds0, sqI);
       const float ca = __fmul_rn(sds0, sk0), cb = __fmul_rn(sds1, sk1);
       // Q-smoothing: dK row t += RN(s_dS * sum_i dS8_it) * qmean (the sum is exact in TMEM)
@@ -783,7 +938,7 @@ __global__ void __launch_bounds__(384, 1)
               float f[4];
 #pragma unroll
               for (int e = 0; e < 4; ++e)
-                f[e] = __uint_as_float(v[i + e]) * (sdoh[dcol + c + i + e] * (1.0f / 448.0f));
+                f[e] = __uint_as_float(v[i + e]) * (sdoh[dcol + c + i + e] * (F4 ? 1.0f / 2688.0f : 1.0f / 448.0f));
               red_add_v4(prm.dvacc + arow + c + i, f[0], f[1], f[2], f[3]);
             }
           }
@@ -861,7 +1016,7 @@ __global__ void __launch_bounds__(384, 1)
           tmem_ld16(tmem + lane_base + cDV + dcol + c, v);
           tmem_wait16(v);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) f[e] = __uint_as_float(v[e]) * (sdoh[dcol + c + e] * (1.0f / 448.0f));
+          for (int e = 0; e < 16; ++e) f[e] = __uint_as_float(v[e]) * (sdoh[dcol + c + e] * (F4 ? 1.0f / 2688.0f : 1.0f / 448.0f));
         }
         if (key_ok && ok) {
           uint4* dstv = reinterpret_cast<uint4*>(prm.dV + orow + dcol + c);
@@ -883,12 +1038,12 @@ __global__ void __launch_bounds__(384, 1)
   if (tid == 0 && sm.abort) atomicExch(prm.status, kDevTimeout);
 }
 
-template <int D, bool QS>
+template <int D, bool QS, bool F4 = false>
 int launch_main_t(const CUtensorMap& tk, const CUtensorMap& tq, const CUtensorMap& tv, const CUtensorMap& tdo,
                   const CUtensorMap& tdo8, const CUtensorMap& tdq, const BwdParams& p, int BH, cudaStream_t st) {
   size_t smem = sizeof(BwdSmem<D>);
   if (smem < 120 * 1024) smem = 120 * 1024;  // one CTA per SM: it holds all 512 TMEM columns
-  auto kern = bwd_main_kernel<D, QS>;
+  auto kern = bwd_main_kernel<D, QS, F4>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 3;
   ScopedTimer timer("bwd_main", st);
   if (launch_pdl(kern, dim3(p.nqb * BH * p.split), dim3(384), smem, st, tk, tq, tv, tdo, tdo8, tdq, p) != cudaSuccess)
@@ -901,10 +1056,10 @@ int launch_main_t(const CUtensorMap& tk, const CUtensorMap& tq, const CUtensorMa
 int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO,
                void* dQ, void* dK, void* dV, const void* ws, void* bwd_ws, int B, int H, int N, int D, int causal,
                int qk_norm, int k_smooth, float sm_scale, cudaStream_t st, const float* O32, int Hkv,
-               bool q_smooth) {
+               bool q_smooth, bool fp4) {
   (void)k_smooth;  // the smoothing Jacobian is applied as the identity (dS rows sum to zero)
-  const QuantWs QL = quant_ws_layout(B, H, N, D, Hkv, q_smooth);
-  const BwdWs BL = bwd_ws_layout(B, H, N, D, Hkv);
+  const QuantWs QL = quant_ws_layout(B, H, N, D, Hkv, q_smooth, fp4);
+  const BwdWs BL = bwd_ws_layout(B, H, N, D, Hkv, fp4);
   const uint8_t* w = static_cast<const uint8_t*>(ws);
   uint8_t* bw = static_cast<uint8_t*>(bwd_ws);
   // BH query heads, BHk key/value heads, `group` query heads per key/value head
@@ -955,7 +1110,17 @@ int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const
   if (!make_tmap_3d(&tq, w + QL.qc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, np, BH, 64, 128)) return 3;
   if (!make_tmap_3d(&tv, V, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, N, BHk, 64, 128)) return 3;
   if (!make_tmap_3d(&tdo, dO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, N, BH, 64, 128)) return 3;
-  if (!make_tmap_3d(&tdo8, do8t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, np, D, BH, 128, D)) return 3;
+  if (fp4) {
+    // the codes as bf16 for the dV MMA: converted after bwd_do8, loaded in 64-query boxes
+    const size_t n16 = (size_t)BH * D * np / 16;
+    __nv_bfloat16* do16 = reinterpret_cast<__nv_bfloat16*>(bw + BL.do16);
+    if (launch_pdl(do8_bf16_kernel, dim3((unsigned)((n16 + 255) / 256 < 4096 ? (n16 + 255) / 256 : 4096)), dim3(256),
+                   0, st, (const uint8_t*)do8t, n16, do16) != cudaSuccess)
+      return 3;
+    if (!make_tmap_3d(&tdo8, do16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, np, D, BH, 64, D)) return 3;
+  } else if (!make_tmap_3d(&tdo8, do8t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, np, D, BH, 128, D)) {
+    return 3;
+  }
   // dQ accumulator [BH][D][np] fp32, boxes of 32 features x 128 queries, unswizzled
   CUtensorMap tdq;
   if (!make_tmap_3d(&tdq, dqacc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, np, D, BH, 128, 32, CU_TENSOR_MAP_SWIZZLE_NONE))
@@ -988,7 +1153,9 @@ int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const
   p.dK = static_cast<__nv_bfloat16*>(dK);
   p.dV = static_cast<__nv_bfloat16*>(dV);
   p.status = reinterpret_cast<int*>(const_cast<uint8_t*>(w) + QL.status);
-  int rc = q_smooth ? (D == 128 ? launch_main_t<128, true>(tk, tq, tv, tdo, tdo8, tdq, p, BHk, st)
+  int rc = fp4        ? (D == 128 ? launch_main_t<128, false, true>(tk, tq, tv, tdo, tdo8, tdq, p, BHk, st)
+                                 : launch_main_t<64, false, true>(tk, tq, tv, tdo, tdo8, tdq, p, BHk, st))
+           : q_smooth ? (D == 128 ? launch_main_t<128, true>(tk, tq, tv, tdo, tdo8, tdq, p, BHk, st)
                                 : launch_main_t<64, true>(tk, tq, tv, tdo, tdo8, tdq, p, BHk, st))
                      : (D == 128 ? launch_main_t<128, false>(tk, tq, tv, tdo, tdo8, tdq, p, BHk, st)
                                  : launch_main_t<64, false>(tk, tq, tv, tdo, tdo8, tdq, p, BHk, st));

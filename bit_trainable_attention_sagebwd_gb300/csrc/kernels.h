@@ -34,7 +34,7 @@ int launch_thrift_hp(const void* ws, const void* tws, void* O, float* LSE, float
 int launch_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO,
                void* dQ, void* dK, void* dV, const void* ws, void* bwd_ws, int B, int H, int N, int D,
                int causal, int qk_norm, int k_smooth, float sm_scale, cudaStream_t st, const float* O32 = nullptr,
-               int Hkv = 0, bool q_smooth = false);
+               int Hkv = 0, bool q_smooth = false, bool fp4 = false);
 // dQ epilogue of the backward (the work ticket in the backward workspace must be zero)
 int launch_bwd_dq(const void* Q, const float* qr, void* bwd_ws, void* dQ, int B, int H, int N, int D, int qk_norm,
                   float sm_scale, int* status, cudaStream_t st, int Hkv = 0);

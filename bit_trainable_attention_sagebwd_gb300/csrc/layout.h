@@ -55,7 +55,7 @@ inline QuantWs quant_ws_layout(int B, int H, int N, int D, int Hkv = 0, bool qs 
 }
 
 struct BwdWs {
-  size_t sync, dvec, bias, do8t, sdo, dopart, dqacc, dkacc, dvacc, kvcnt, total;
+  size_t sync, dvec, bias, do8t, sdo, dopart, dqacc, dkacc, dvacc, kvcnt, do16, total;
   int np;
 };
 
@@ -63,7 +63,8 @@ struct BwdWs {
 // (channel-major), their channel scales (one set per key/value head: the query heads that
 // share it share the scale) and partial maxima, fp32 dQ accumulator (feature-major
 // [BH, D, Np] so that reductions from query rows coalesce)
-inline BwdWs bwd_ws_layout(int B, int H, int N, int D, int Hkv = 0) {
+// fp4 (NVFP4 backward): the e4m3 codes of dO also as bf16 [BH, D, Np], the dV operand
+inline BwdWs bwd_ws_layout(int B, int H, int N, int D, int Hkv = 0, bool fp4 = false) {
   BwdWs L{};
   const size_t bh = (size_t)B * H, bk = (size_t)B * (Hkv > 0 ? Hkv : H);
   const int np = pad128(N);
@@ -82,6 +83,7 @@ inline BwdWs bwd_ws_layout(int B, int H, int N, int D, int Hkv = 0) {
   L.dkacc = o;  o = align256(o + (grouped ? bk * np * D * 4 : 0));
   L.dvacc = o;  o = align256(o + (grouped ? bk * np * D * 4 : 0));
   L.kvcnt = o;  o = align256(o + (grouped ? bk * nb * 4 : 0));
+  L.do16 = o;   o = align256(o + (fp4 ? bh * D * np * 2 : 0));
   L.total = o;
   L.np = np;
   return L;

@@ -272,6 +272,16 @@ int sage_attn_fp4_quantize(const void *Q, const void *K, const void *V, int B, i
 int sage_attn_fp4_fwd(const void *ws, void *O, float *LSE, float *O32, int B, int H, int N, int D, int causal,
                       float sm_scale, void *stream);
 int sage_attn_fp4_ws_views(void *ws, int B, int H, int N, int D, sage_ws_views *views);
+/* NVFP4 backward (Attn-QAT, principle 1: P recomputed at the forward's precision): P^ in
+ * NVFP4 from the saved LSE with the forward's 16-key blocks, used in dS = P^ (dP - D_i) and
+ * dV = P^T dO8; the rest as sage_attn_bwd.  dV runs on bf16 tensor cores with the exact
+ * values code * s and dO's e4m3 codes (P^'s scales vary along the keys, which dV does not
+ * contract).  Scratch: sage_attn_fp4_bwd_ws_bytes (it adds dO's codes as bf16).  `ws` comes
+ * from sage_attn_fp4_quantize. */
+size_t sage_attn_fp4_bwd_ws_bytes(int B, int H, int N, int D);
+int sage_attn_fp4_bwd(const void *Q, const void *K, const void *V, const void *O, const float *LSE, const void *dO,
+                      void *dQ, void *dK, void *dV, const void *ws, void *bwd_ws, size_t bwd_ws_bytes, int B, int H,
+                      int N, int D, int causal, int qk_norm, int k_smooth, float sm_scale, void *stream);
 
 /* Fill `views` with the device pointers inside a quantize workspace (qmean, dsb: NULL). */
 int sage_attn_ws_views(void *ws, int B, int H, int N, int D, sage_ws_views *views);

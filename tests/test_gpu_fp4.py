@@ -1,4 +1,4 @@
-"""NVFP4 variant of the forward on the GPU (sage_attn_fp4_*) against the CPU oracle's QM_FP4 mode
+"""NVFP4 variant (sage_attn_fp4_*) on the GPU against the CPU oracle's QM_FP4 mode
 ("Attn-QAT: 4-Bit Attention With Quantization-Aware Training" (gist.science summary),
 Methodology principle 1; "ThriftAttention" (gist.science summary), Methodology step 2).
 
@@ -13,6 +13,9 @@ import pytest
 from bit_trainable_attention_sagebwd_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
+
+# The backward recomputes P^ in NVFP4 from the saved LSE (the forward's blocks); dQ, dK, dV
+# are held to the backward's relative-L2 tolerance of 1e-2 against the oracle.
 
 SMALL = [
     wl.custom(1, 2, 333, 64, True, seed=90, kind="k_offset2", name="n333_d64_causal"),
@@ -43,7 +46,7 @@ def _v_values(views, b, h, N, D):
     return vals[:, :N].T
 
 
-def _run(w, x):
+def _run(w, x, backward=False):
     import torch
     import bit_trainable_attention_sagebwd_gb300 as sa
     import parity
@@ -51,16 +54,24 @@ def _run(w, x):
     B, H, N, D = w.B, w.H, w.N, w.D
     ws = sa.fp4_quantize(t["q"], t["k"], t["v"], w.qk_norm, w.k_smooth)
     o, lse, o32 = sa.fp4_forward(ws, B, H, N, D, w.causal, w.sm_scale, o32=True)
+    out = {"O": o, "LSE": lse, "O32": o32}
+    if backward:
+        dq, dk, dv = sa.fp4_backward(t["q"], t["k"], t["v"], o, lse, t["do"], ws, w.causal, w.qk_norm, w.k_smooth,
+                                     w.sm_scale)
+        out.update(dQ=dq, dK=dk, dV=dv)
     torch.cuda.synchronize()
     assert sa.get_status(ws) == sa.SAGE_OK
-    return {"O": o, "LSE": lse, "O32": o32, "views": sa.ws_tensors(ws, B, H, N, D, fp4=True)}
+    out["views"] = sa.ws_tensors(ws, B, H, N, D, fp4=True)
+    return out
 
 
-def _check_head(w, x, g, bh):
+def _check_head(w, x, g, bh, backward=False):
     import parity
     from oracle import oracle as orc
     b, h = divmod(bh, w.H)
-    r = parity.oracle_head(w, x, bh, backward=False, qmask=orc.QM_ALL | orc.QM_FP4)
+    r = parity.oracle_head(w, x, bh, backward=backward, qmask=orc.QM_ALL | orc.QM_FP4)
+    if backward:
+        parity.check_backward_head(w, g, bh, r)
     v = g["views"]
     N = w.N
     qc = v["qc"][b, h].float().cpu().numpy().astype(np.float64)
@@ -88,3 +99,22 @@ def test_fp4_forward_full_size(name):
     g = _run(w, x)
     for bh in parity.full_size_heads(w):
         _check_head(w, x, g, bh)
+
+
+@pytest.mark.parametrize("w", SMALL, ids=[w.name for w in SMALL])
+def test_fp4_backward_small(w):
+    x = wl.all_inputs(w)
+    g = _run(w, x, backward=True)
+    for bh in range(w.bh):
+        _check_head(w, x, g, bh, backward=True)
+
+
+@pytest.mark.parametrize("name", ["pretrain_8k", "long_32k"])
+def test_fp4_backward_full_size(name):
+    """Full-size workloads; the oracle computes the first, a middle and the last head."""
+    import parity
+    w = wl.WORKLOADS[name]
+    x = wl.all_inputs(w)
+    g = _run(w, x, backward=True)
+    for bh in parity.full_size_heads(w):
+        _check_head(w, x, g, bh, backward=True)
