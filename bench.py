@@ -442,6 +442,25 @@ def run_ours(args, w):
     variants["q_smooth"] = time_variant(qstep, wsq)
     del wsq
 
+    # NVFP4 PV (and P^ in the backward): the same step, and its quantize + forward alone
+    ws4 = torch.empty(sa.sage_attn_fp4_ws_bytes(B, H, N, D), dtype=torch.uint8, device=dev)
+    bws4 = torch.empty(sa.sage_attn_fp4_bwd_ws_bytes(B, H, N, D), dtype=torch.uint8, device=dev)
+
+    def f4step():
+        sa.fp4_quantize(t["q"], t["k"], t["v"], w.qk_norm, w.k_smooth, ws=ws4)
+        sa.fp4_forward(ws4, B, H, N, D, w.causal, w.sm_scale, o=o, lse=lse, device=dev)
+        sa.fp4_backward(t["q"], t["k"], t["v"], o, lse, t["do"], ws4, w.causal, w.qk_norm, w.k_smooth, w.sm_scale,
+                        bwd_ws=bws4, dq=dq, dk=dk, dv=dv)
+
+    def f4fwd():
+        sa.fp4_quantize(t["q"], t["k"], t["v"], w.qk_norm, w.k_smooth, ws=ws4)
+        sa.fp4_forward(ws4, B, H, N, D, w.causal, w.sm_scale, o=o, lse=lse, device=dev)
+    variants["nvfp4"] = time_variant(f4step, ws4)
+    f4f = time_variant(f4fwd, ws4)
+    variants["nvfp4"]["forward_ms_per_step"] = f4f["ms_per_step"]
+    variants["nvfp4"]["fwd_tops"] = ops["fwd"] / (f4f["ms_per_step"] * 1e-3) / 1e12
+    del ws4, bws4
+
     # ThriftAttention (forward only, the page's 5 % budget) against the plain forward: quantize +
     # forward, median of 20 steps each, L2 flushed
     tws = None
