@@ -44,9 +44,9 @@ struct FwdSmem {
   float xsum[2][2][128];             // per tile and key half: row sums, exchanged at the end
   // Q-smoothing: the logit terms of tiles A and B for the keys of each value stage
   __align__(16) float dsb[kVStages][2][128];
-  // NVFP4: the block scales of P (one 512-byte atom per 64-key half, as the tensor core reads
-  // them) and of each value stage's V tile (two atoms)
-  __align__(128) uint8_t sfa[2][512];
+  // NVFP4: the block scales of P (per tile, one 512-byte atom per 64-key half, as the tensor
+  // core reads them) and of each value stage's V tile (two atoms)
+  __align__(128) uint8_t sfa[2][2][512];
   __align__(128) uint8_t sfb[kVStages][1024];
   uint64_t bar_q;
   uint64_t bar_k_full[kKStages], bar_k_empty[kKStages];
@@ -391,7 +391,7 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
         *reinterpret_cast<uint4*>(prow4 + ((unit ^ ((t & 7) >> 1)) << 4)) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
       }
       // this half's scales into its atom: row t at byte (t % 32) * 16 + (t / 32) * 4
-      *reinterpret_cast<uint32_t*>(sm.sfa[hh] + (t & 31) * 16 + (t >> 5) * 4) = sfw;
+      *reinterpret_cast<uint32_t*>(sm.sfa[X][hh] + (t & 31) * 16 + (t >> 5) * 4) = sfw;
       float la, lb;
       f2split(lsum2, la, lb);
       l = fmaf(l, corr, la + lb);
@@ -561,9 +561,10 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
 // (each next S once its tile's softmax holds the current S in registers, each PV once its
 // P is written), so the tensor core works on one tile while the other tile's softmax runs.
 // TMEM columns: S_A [0,128), S_B [128,256), O_A [256,256+D), O_B [256+D,256+2D).
-// F4 (NVFP4 PV): one query tile per CTA (tile A); the TMEM columns of tile B's S hold the
-// scale factors of P and V, two sets of 16 columns used in turn, and PV runs as two
-// kind::mxf4nvf4 MMAs (K = 64 keys each) on packed e2m1 operands with a 64-byte swizzle.
+// F4 (NVFP4 PV): PV runs as two kind::mxf4nvf4 MMAs (K = 64 keys each) on packed e2m1
+// operands with a 64-byte swizzle; the scale factors of P and V go to the last 16 TMEM columns
+// of the tile's S, which its softmax has finished reading, and the tile's next S waits until
+// that PV has completed (instead of going ahead of it).
 template <int D, bool CAUSAL, bool QS, bool TH, bool F4>
 __global__ void __launch_bounds__(640, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -574,7 +575,7 @@ __global__ void __launch_bounds__(640, 1)
   int px, bh;  // one CTA per (pair of query blocks, head); causal: the longest pairs first
   tile_head_order((int)blockIdx.x, prm.npairs, prm.BH, prm.hgroup, px, bh);
   const int pc = CAUSAL ? (prm.npairs - 1 - px) : px;
-  const int qbA = F4 ? pc : 2 * pc, qbB = F4 ? prm.nqb : 2 * pc + 1;
+  const int qbA = 2 * pc, qbB = 2 * pc + 1;
   const bool hasB = qbB < prm.nqb;
   // KV tiles: tile A needs [0, lastA], tile B [0, lastB]
   const int lastA = CAUSAL ? qbA : prm.nqb - 1;
@@ -670,25 +671,23 @@ __global__ void __launch_bounds__(640, 1)
         }
         umma_commit(&sm.bar_s_full[X]);
       };
-      int nf4 = 0;  // NVFP4: PVs issued, whose parity picks the scale-factor columns
       auto issue_pv = [&](int X, int j, int first) {
         const uint32_t p_addr = smem_u32(sm.p[X]);
         const uint32_t v_addr = smem_u32(sm.v[j % kVStages]);
         if constexpr (F4) {
-          // scale factors to TMEM (P's two atoms, then V's), then two K = 64 MMAs; the columns
-          // alternate between PVs, so a copy never lands where an unfinished MMA reads
+          // scale factors to the last 16 columns of the tile's S (P's two atoms, then V's), then
+          // two K = 64 MMAs
           constexpr uint32_t idesc_f4 = idesc_nvf4(128, D);
-          const uint32_t sf = tmem + 128u + 16u * (uint32_t)(nf4 & 1);
-          ++nf4;
+          const uint32_t sf = tmem + (uint32_t)(X * 128) + 112u;
   #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            tmem_cp_32x128b_x4(sf + 4 * h, sdesc_none(smem_u32(sm.sfa[h]), 128, 128));
+            tmem_cp_32x128b_x4(sf + 4 * h, sdesc_none(smem_u32(sm.sfa[X][h]), 128, 128));
             tmem_cp_32x128b_x4(sf + 8 + 4 * h, sdesc_none(smem_u32(sm.sfb[j % kVStages] + 512 * h), 128, 128));
           }
   #pragma unroll
           for (int h = 0; h < 2; ++h)
-            umma_nvf4(tmem + 256u, sdesc_sw64(p_addr + 32 * h, 16, 512), sdesc_sw64(v_addr + 32 * h, 16, 512), idesc_f4,
-                      sf + 4 * h, sf + 8 + 4 * h, (!first || h > 0));
+            umma_nvf4(tmem + 256u + (uint32_t)(X * D), sdesc_sw64(p_addr + 32 * h, 16, 512),
+                      sdesc_sw64(v_addr + 32 * h, 16, 512), idesc_f4, sf + 4 * h, sf + 8 + 4 * h, (!first || h > 0));
         } else {
   #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
@@ -721,28 +720,51 @@ __global__ void __launch_bounds__(640, 1)
         const bool nextk = j + 1 < n_kv;
         if (nextk && !mbar_wait(&sm.bar_k_full[(j + 1) % kKStages], ((j + 1) / kKStages) & 1, abort)) break;
         if (!mbar_wait(&sm.bar_v_full[j % kVStages], (j / kVStages) & 1, abort)) break;
-        // the next S of a tile as soon as its softmax has read this S into registers (halfway
-        // through its exp pass), then the PVs once the P codes are in shared memory
-        for (int X = 0; X < 2; ++X) {
-          if (!use(X, j + 1)) continue;
-          if (ns[X] > 0 && !mbar_wait(&sm.bar_s_free[X], (ns[X] - 1) & 1, abort)) {
-            ok = false;
-            break;
+        if constexpr (F4) {
+          // per tile: its PV once the codes are in shared memory, then its next S once that PV
+          // has completed (the PV reads scale factors from the S columns)
+          for (int X = 0; X < 2; ++X) {
+            if (!use(X, j)) continue;
+            if (!mbar_wait(&sm.bar_p_full[X], npv[X] & 1, abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_pv(X, j, npv[X] == 0);
+            ++npv[X];
+            if (!use(X, j + 1)) continue;
+            if (!mbar_wait(&sm.bar_o_done[X], (npv[X] - 1) & 1, abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(X, j + 1);
+            ++ns[X];
           }
-          tc_fence_after();
-          issue_s(X, j + 1);
-          ++ns[X];
-        }
-        if (!ok) break;
-        for (int X = 0; X < 2; ++X) {
-          if (!use(X, j)) continue;
-          if (!mbar_wait(&sm.bar_p_full[X], npv[X] & 1, abort)) {
-            ok = false;
-            break;
+        } else {
+          // the next S of a tile as soon as its softmax has read this S into registers (halfway
+          // through its exp pass), then the PVs once the P codes are in shared memory
+          for (int X = 0; X < 2; ++X) {
+            if (!use(X, j + 1)) continue;
+            if (ns[X] > 0 && !mbar_wait(&sm.bar_s_free[X], (ns[X] - 1) & 1, abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(X, j + 1);
+            ++ns[X];
           }
-          tc_fence_after();
-          issue_pv(X, j, npv[X] == 0);
-          ++npv[X];
+          if (!ok) break;
+          for (int X = 0; X < 2; ++X) {
+            if (!use(X, j)) continue;
+            if (!mbar_wait(&sm.bar_p_full[X], npv[X] & 1, abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_pv(X, j, npv[X] == 0);
+            ++npv[X];
+          }
         }
         if (!ok) break;
         umma_commit(&sm.bar_v_empty[j % kVStages]);
@@ -808,12 +830,11 @@ int launch_fwd(const void* ws, void* O, float* LSE, float* O32, int B, int H, in
   p.vg = reinterpret_cast<const float*>(w + L.vg);
   p.v4sf = w + L.v4sf;
   if (fp4) {
-    // NVFP4 PV (plain heads): one query tile per CTA; V's packed e2m1 codes [BHk][D][Np/2]
+    // NVFP4 PV (plain heads); V's packed e2m1 codes [BHk][D][Np/2]
     CUtensorMap tv4;
     if (!make_tmap_3d(&tv4, w + L.v4, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, np / 2, D, BHk, 64, D,
                       CU_TENSOR_MAP_SWIZZLE_64B))
       return 3;
-    p.npairs = p.nqb;
     if (D == 128)
       return causal ? launch_fwd_t<128, true, false, false, true>(tq, tk, tv4, p, BH, st)
                     : launch_fwd_t<128, false, false, false, true>(tq, tk, tv4, p, BH, st);
