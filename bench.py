@@ -476,11 +476,24 @@ def run_ours(args, w):
         sa.thrift_forward(ws, tws, B, H, N, D, w.causal, w.sm_scale, o=o, lse=lse, device=dev)
     plain_fwd = time_variant(pstep, ws)
     thr = time_variant(tstep, ws)
+    # its launch groups, each bracketed by events over 5 more steps
+    tgroups = ("quantize", "thrift_prepare", "fwd", "thrift_hp")
+    for g in tgroups:
+        sa.sage_attn_timer_read(g)
+    sa.sage_attn_timer_only(None)
+    sa.sage_attn_timer_enable(1)
+    for i in range(5):
+        flush.fill_(float(i))
+        tstep()
+    torch.cuda.synchronize()
+    sa.sage_attn_timer_enable(0)
+    tms = {g: (lambda r: r[0] / max(1, r[1]))(sa.sage_attn_timer_read(g)) for g in tgroups}
     fwd_ops = ops["fwd"]
     variants["thrift_5pct_forward"] = {
         "ms_per_step": thr["ms_per_step"], "fwd_tops": fwd_ops / (thr["ms_per_step"] * 1e-3) / 1e12,
         "plain_forward_ms_per_step": plain_fwd["ms_per_step"],
         "plain_fwd_tops": fwd_ops / (plain_fwd["ms_per_step"] * 1e-3) / 1e12,
+        "kernel_ms_per_step": tms,
         "note": "quantize + forward; 5 % of the visible (query block, key tile) pairs in fp16"}
     del tws
 

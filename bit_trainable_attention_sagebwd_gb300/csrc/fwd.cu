@@ -345,22 +345,31 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
             f2split(y2, y[e], y[e + 1]);
             ym = max3(ym, y[e], y[e + 1]);
           }
-          float qs = __fdiv_rn(ym, 6.0f);
+          // the fast values are within a few ulps of RN(max y / 6) and RN(y / s); the 2^-18 band
+          // (32 ulps) covers the product with a rounded 1/6 and an approximate reciprocal
+          float qs = ym * (1.0f / 6.0f);
           uint32_t sb = (uint32_t)__nv_cvt_float_to_fp8(qs, __NV_SATFINITE, __NV_E4M3);
           bool redo = sb != (uint32_t)__nv_cvt_float_to_fp8(qs * kUp, __NV_SATFINITE, __NV_E4M3) ||
                       sb != (uint32_t)__nv_cvt_float_to_fp8(qs * kDn, __NV_SATFINITE, __NV_E4M3);
           uint32_t w0 = 0, w1 = 0;
           float sval = __half2float(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)sb, __NV_E4M3)));
           if (sval > 0.f) {
-            const float inv = __frcp_rn(sval);
+            const float inv = __fdividef(1.0f, sval);
+            const uint64_t inv2 = f2(inv, inv), up2 = f2(kUp, kUp), dn2 = f2(kDn, kDn);
+            uint32_t diff = 0;
 #pragma unroll
             for (int e = 0; e < 16; e += 2) {
-              const float q0 = y[e] * inv, q1 = y[e + 1] * inv;
+              const uint64_t q2 = fmul2(f2(y[e], y[e + 1]), inv2);
+              float q0, q1, u0, u1, d0, d1;
+              f2split(q2, q0, q1);
+              f2split(fmul2(q2, up2), u0, u1);
+              f2split(fmul2(q2, dn2), d0, d1);
               const uint32_t c = e2m1x2(q0, q1);
-              redo = redo || c != e2m1x2(q0 * kUp, q1 * kUp) || c != e2m1x2(q0 * kDn, q1 * kDn);
+              diff |= (c ^ e2m1x2(u0, u1)) | (c ^ e2m1x2(d0, d1));
               if (e < 8) w0 |= c << (4 * e);
               else w1 |= c << (4 * (e - 8));
             }
+            redo = redo || diff != 0;
           }
           if (redo) {
             // the definition itself: RN(2^t) accurately, then the correctly rounded steps
