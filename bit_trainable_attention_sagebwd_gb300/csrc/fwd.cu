@@ -670,14 +670,12 @@ __global__ void __launch_bounds__(640, 1)
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_o = idesc_e4m3(128, D);
       auto issue_s = [&](int X, int j) {
-        const uint32_t q_addr = smem_u32(sm.q[X]);
-        const uint32_t k_addr = smem_u32(sm.k[j % kKStages]);
+        // per 64-channel atom (16 KB) four K = 16 steps of 32 bytes
+        const uint64_t a = sdesc_sw128(smem_u32(sm.q[X]), 16, 1024);
+        const uint64_t b = sdesc_sw128(smem_u32(sm.k[j % kKStages]), 16, 1024);
   #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_bf16(tmem + (uint32_t)(X * 128), sdesc_sw128(q_addr + off, 16, 1024),
-                    sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0);
-        }
+        for (int h = 0; h < D / 64; ++h)
+          umma_bf16_x4<2, 2>(tmem + (uint32_t)(X * 128), a + 1024 * h, b + 1024 * h, idesc_s, h > 0);
         umma_commit(&sm.bar_s_full[X]);
       };
       auto issue_pv = [&](int X, int j, int first) {
@@ -698,10 +696,9 @@ __global__ void __launch_bounds__(640, 1)
             umma_nvf4(tmem + 256u + (uint32_t)(X * D), sdesc_sw64(p_addr + 32 * h, 16, 512),
                       sdesc_sw64(v_addr + 32 * h, 16, 512), idesc_f4, sf + 4 * h, sf + 8 + 4 * h, (!first || h > 0));
         } else {
-  #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_f8(tmem + 256u + (uint32_t)(X * D), sdesc_sw128(p_addr + kk * 32, 16, 1024),
-                    sdesc_sw128(v_addr + kk * 32, 16, 1024), idesc_o, (!first || kk > 0));
+          // four K = 32 steps of 32 bytes
+          umma_f8_x4<2, 2>(tmem + 256u + (uint32_t)(X * D), sdesc_sw128(p_addr, 16, 1024), sdesc_sw128(v_addr, 16, 1024),
+                           idesc_o, !first);
         }
         umma_commit(&sm.bar_o_done[X]);
       };

@@ -229,6 +229,33 @@ __device__ __forceinline__ void umma_f8(uint32_t d, uint64_t a, uint64_t b, uint
       "l"(a), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
+// Four MMAs along K into the same accumulator, in one asm block so that they issue back to
+// back: the k-th (k = 0..3) reads the descriptors a + k SA and b + k SB (steps in 16-byte units
+// of the start-address field, which never carries: shared addresses are below 256 KB).  The
+// first accumulates when acc != 0, the other three always.  An MMA issuer that shares its SM
+// sub-partition with busy warps spends about a third of the instructions per MMA this way.
+#define SAGE_UMMA_X4(KIND)                                                                          \
+  asm volatile(                                                                                     \
+      "{\n .reg .pred p, q;\n .reg .b64 a1, a2, a3, b1, b2, b3;\n"                                \
+      " setp.ne.b32 p, %4, 0;\n setp.eq.b32 q, %4, %4;\n"                                           \
+      " add.s64 a1, %1, %5;\n add.s64 a2, %1, %6;\n add.s64 a3, %1, %7;\n"                          \
+      " add.s64 b1, %2, %8;\n add.s64 b2, %2, %9;\n add.s64 b3, %2, %10;\n"                         \
+      " tcgen05.mma.cta_group::1.kind::" KIND " [%0], %1, %2, %3, p;\n"                            \
+      " tcgen05.mma.cta_group::1.kind::" KIND " [%0], a1, b1, %3, q;\n"                            \
+      " tcgen05.mma.cta_group::1.kind::" KIND " [%0], a2, b2, %3, q;\n"                            \
+      " tcgen05.mma.cta_group::1.kind::" KIND " [%0], a3, b3, %3, q;\n}\n" ::"r"(d),                \
+      "l"(a), "l"(b), "r"(idesc), "r"(acc), "n"(SA), "n"(2 * SA), "n"(3 * SA), "n"(SB), "n"(2 * SB), \
+      "n"(3 * SB)                                                                                   \
+      : "memory")
+template <int SA, int SB>
+__device__ __forceinline__ void umma_bf16_x4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  SAGE_UMMA_X4("f16");
+}
+template <int SA, int SB>
+__device__ __forceinline__ void umma_f8_x4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  SAGE_UMMA_X4("f8f6f4");
+}
+#undef SAGE_UMMA_X4
 // D[tmem] (+)= (A * scale A)[smem] * (B * scale B)[smem]^T: packed e2m1 operands (two per byte,
 // K-major), one ue4m3 scale per 16 values along K for each row of A and of B, read from TMEM
 // (sfa, sfb: four columns each, the 32 x 16-byte atom that tmem_cp_32x128b_x4 writes); fp32
