@@ -195,12 +195,16 @@ __global__ void __launch_bounds__(kThreads) kstats_kernel(const __nv_bfloat16* _
       }
     }
     // combine the rows per channel: the lanes of a warp that hold the same channels (in
-    // double-float), then the warps in fp64 in a fixed order
+    // double-float), then the warps in fp64 in a fixed order.  The per-warp sums go where the
+    // staged block was, once every warp is done with it: the block's shared memory is then
+    // the staged block alone, and more blocks fit on an SM (the pass is bound by the bytes in
+    // flight)
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
       for (int m = TPR; m < 32; m <<= 1) cs[i] = df_add(cs[i], df_shfl_xor(cs[i], m));
-    __shared__ double s_sum[kThreads / 32][D];
+    __syncthreads();
+    double(*s_sum)[D] = reinterpret_cast<double(*)[D]>(stage_buf);  // [kThreads / 32][D]
     if ((tid & 31) < TPR) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) s_sum[tid >> 5][g * 8 + i] = (double)cs[i].hi + (double)cs[i].lo;
@@ -226,7 +230,8 @@ __global__ void __launch_bounds__(kThreads) kstats_kernel(const __nv_bfloat16* _
     for (int w = 0; w < 4; ++w)
 #pragma unroll
       for (int m = TPR; m < 32; m <<= 1) vb[w] = umax2(vb[w], __shfl_xor_sync(0xffffffffu, vb[w], m));
-    __shared__ float s_max[kThreads / 32][D];
+    __syncthreads();  // the staged block is consumed: its space takes the per-warp maxima
+    float(*s_max)[D] = reinterpret_cast<float(*)[D]>(stage_buf);  // [kThreads / 32][D]
     if ((tid & 31) < TPR) {
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
@@ -255,7 +260,7 @@ __global__ void __launch_bounds__(kThreads) kstats_kernel(const __nv_bfloat16* _
   // then the J results of a channel in a fixed order
   const int d = tid % D, j = tid / D;
   if (isk) {
-    __shared__ double s_comb[J][D];
+    double(*s_comb)[D] = reinterpret_cast<double(*)[D]>(stage_buf);  // [J][D], staged block consumed
     const double* part = kpart + (size_t)bh * nb * D + d;
     double s = 0.0;
     int b = j;
@@ -276,7 +281,7 @@ __global__ void __launch_bounds__(kThreads) kstats_kernel(const __nv_bfloat16* _
       kmean[(size_t)bh * D + tid] = (float)(t / (double)N);
     }
   } else {
-    __shared__ float f_comb[J][D];
+    float(*f_comb)[D] = reinterpret_cast<float(*)[D]>(stage_buf);  // [J][D], staged block consumed
     const float* part = vpart + (size_t)bh * nb * D + d;
     float m = 0.f;
     int b = j;
@@ -299,7 +304,8 @@ __global__ void __launch_bounds__(kThreads) kstats_kernel(const __nv_bfloat16* _
     if (vg != nullptr) {
       // NVFP4's tensor scale of V: the head's largest |V| / (448 * 6); every thread's m is at
       // most its channel's maximum, and the threads below D hold the channel maxima
-      __shared__ float s_hm[kThreads / 32];
+      __syncthreads();  // f_comb is read: its space takes the per-warp maxima
+      float* s_hm = reinterpret_cast<float*>(stage_buf);
       float hm = m;
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) hm = fmaxf(hm, __shfl_xor_sync(0xffffffffu, hm, o));

@@ -39,19 +39,51 @@ namespace {
 constexpr float kLog2_448 = 8.807354922057604f;
 
 // ------------------------------------------------------------------ selection
-// channel means of one 128-token block of the raw input (tokens [0, cnt) of the block)
+// channel means of one 128-token block of the raw input (tokens [0, cnt) of the block): the
+// fp64 sum of the tokens in order, divided by cnt.  That sum is exact whenever every partial
+// sum is representable, which holds when the nonzero values' exponents span at most 38: a bf16
+// value is m 2^(e - 134) with an 8-bit m (e >= 1), so each partial sum is an integer multiple
+// of 2^(emin - 134) below 128 * 2^8 * 2^38 = 2^53 of them.  Then the sum is accumulated exactly
+// in a 64-bit integer (fp64 runs at 1/64 of the fp32 rate on this part); otherwise, or with an
+// infinity or NaN in the block, the fp64 sum is taken in order.
 template <int D>
 __global__ void __launch_bounds__(D) thrift_means_kernel(const __nv_bfloat16* __restrict__ Q,
                                                         const __nv_bfloat16* __restrict__ K, int N,
                                                         double* __restrict__ qbar, double* __restrict__ kbar) {
   const int blk = blockIdx.x, bh = blockIdx.y, d = threadIdx.x, nb = gridDim.x;
-  const __nv_bfloat16* x = (blockIdx.z == 0 ? Q : K) + ((size_t)bh * N + (size_t)blk * 128) * D + d;
+  const uint16_t* x = reinterpret_cast<const uint16_t*>(blockIdx.z == 0 ? Q : K) +
+                      ((size_t)bh * N + (size_t)blk * 128) * D + d;
   double* out = blockIdx.z == 0 ? qbar : kbar;
   pdl_wait();
   pdl_trigger();
   const int cnt = min(128, N - blk * 128);
-  double s = 0.0;
-  for (int t = 0; t < cnt; ++t) s = __dadd_rn(s, (double)__bfloat162float(x[(size_t)t * D]));
+  int emin = 255, emax = 0;
+  bool special = false;
+  for (int t = 0; t < cnt; ++t) {
+    const uint32_t u = x[(size_t)t * D];
+    const int e = (int)((u >> 7) & 0xFFu);
+    if (e == 0xFF) special = true;
+    if ((u & 0x7FFFu) != 0u) {
+      const int ee = e > 0 ? e : 1;
+      emin = min(emin, ee);
+      emax = max(emax, ee);
+    }
+  }
+  double s;
+  if (!special && emax - emin <= 38) {
+    long long acc = 0;
+    for (int t = 0; t < cnt; ++t) {
+      const uint32_t u = x[(size_t)t * D];
+      const uint32_t e = (u >> 7) & 0xFFu, f = u & 0x7Fu;
+      if ((u & 0x7FFFu) == 0u) continue;
+      const long long v = (long long)(e ? (f | 0x80u) : f) << ((e ? (int)e : 1) - emin);
+      acc += (u & 0x8000u) ? -v : v;
+    }
+    s = ldexp((double)acc, emin - 134);  // |acc| < 2^53: exact
+  } else {
+    s = 0.0;
+    for (int t = 0; t < cnt; ++t) s = __dadd_rn(s, (double)__bfloat162float(__ushort_as_bfloat16(x[(size_t)t * D])));
+  }
   out[((size_t)bh * nb + blk) * D + d] = __ddiv_rn(s, (double)cnt);
 }
 

@@ -124,6 +124,12 @@ def head_inputs(w: Workload, bh: int) -> dict:
     elif w.kind == "k_outlier20":
         ch = ex.permutation(D)[:4]
         k[:, ch] *= 20.0
+    elif w.kind == "exp_spread":
+        # Q and K magnitudes spread over about 48 binades (each element scaled down by 2^u, u a
+        # whole number in [0, 44)): block sums whose values span more than 38 binades, logits
+        # no larger than the plain recipe's
+        q = q * np.exp2(-ex.integers(0, 44, size=(N, D)))
+        k = k * np.exp2(-ex.integers(0, 44, size=(N, D)))
     elif w.kind in ("normal", "student_t3"):
         pass
     else:

@@ -20,6 +20,9 @@ CASES = [
     (wl.custom(1, 1, 129, 128, False, k_smooth=False, seed=83, name="n129_nosmooth"), 0.5),
     (wl.custom(1, 2, 512, 64, True, seed=84, name="n512_budget0"), 0.0),
     (wl.custom(1, 2, 384, 128, True, seed=85, kind="k_offset3", name="n384_budget1"), 1.0),
+    # block means whose values span more than 38 binades take the fp64 sum in order; the
+    # others the exact integer sum (the same bits either way)
+    (wl.custom(1, 2, 515, 128, True, seed=86, kind="exp_spread", name="n515_exp_spread"), 0.1),
 ]
 
 
