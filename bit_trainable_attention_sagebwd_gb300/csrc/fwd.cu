@@ -304,10 +304,9 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
     named_bar_tile(X);
     const float m_new = max3(m, sm.xmax[X][0][t], sm.xmax[X][1][t]);
     const float corr = (m == -INFINITY) ? 0.f : ex2(m - m_new);
-    // ---- PV of the previous tile must be complete before P is overwritten and O rescaled.
-    // Without NVFP4 the tensor core took that PV before this tile's S, whose completion
-    // (s_full) covers it; the NVFP4 order issues the next S only after the PV has completed
-    if (F4 && cnt > 0) {
+    // ---- PV of the previous tile must be complete before P is overwritten and O rescaled
+    // (the tensor core took it right after this tile's S, so it has normally finished by now)
+    if (cnt > 0) {
       ok = ok && mbar_wait(&sm.bar_o_done[X], (cnt - 1) & 1, abort);
       tc_fence_after();
     }
@@ -499,9 +498,8 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
     mbar_arrive(&sm.bar_p_full[X]);
     ++cnt;
   }
-  // ---- epilogue: O = A * sv / l (l sums 448 p~ over both halves), LSE = ln2 (m + log2(l / 448)).
-  // NVFP4 commits o_done after every PV; otherwise it is committed once, after the last MMA
-  if (cnt > 0) ok = ok && mbar_wait(&sm.bar_o_done[X], F4 ? (cnt - 1) & 1 : 0, abort);
+  // ---- epilogue: O = A * sv / l (l sums 448 p~ over both halves), LSE = ln2 (m + log2(l / 448))
+  if (cnt > 0) ok = ok && mbar_wait(&sm.bar_o_done[X], (cnt - 1) & 1, abort);
   tc_fence_after();
   sm.xsum[X][hh][t] = l;
   named_bar_tile(X);
@@ -569,13 +567,13 @@ __device__ __forceinline__ void softmax_tile_loop(FwdSmem<D>& sm, const FwdParam
 // the softmax of tile A (keys [0,64) and [64,128) of each key tile), 2-3 that of tile B;
 // warp 16 loads K and V tiles with TMA; warp 17 allocates TMEM and issues the UMMAs in
 // the order
-//   S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) ...
+//   S_A(0) S_B(0) | S_A(j+1) PV_A(j) S_B(j+1) PV_B(j) ...
 // (a tile's pair once its softmax has handed over P(j), and with it S(j)), so the tensor core
-// works on one tile's pair while the other tile's softmax runs.  A tile's softmax keeps
-// nothing of S for the rare exact-code path (it reloads S from TMEM), and the completion of
-// S(j+1) covers the PV before it.  Issuing S(j+1) earlier, as soon as S(j) is in registers,
-// measured slower on long_32k (7.80 ms against 7.15 ms): the softmax then had to hold the S
-// values for that path.
+// works on one tile's pair while the other tile's softmax runs.  The tile's next softmax waits
+// for its S; the PV behind it finishes during the max pass (o_done, waited before P is
+// rewritten).  A tile's softmax keeps nothing of S for the rare exact-code path (it reloads S
+// from TMEM).  Issuing S(j+1) earlier, as soon as S(j) is in registers, measured slower on
+// long_32k (7.80 ms against 7.09 ms): the softmax then had to hold the S values for that path.
 // TMEM columns: S_A [0,128), S_B [128,256), O_A [256,256+D), O_B [256+D,256+2D).
 // F4 (NVFP4 PV): PV runs as two kind::mxf4nvf4 MMAs (K = 64 keys each) on packed e2m1
 // operands with a 64-byte swizzle; the scale factors of P and V go to the last 16 TMEM columns
@@ -707,7 +705,7 @@ __global__ void __launch_bounds__(640, 1)
           umma_f8_x4<2, 2>(tmem + 256u + (uint32_t)(X * D), sdesc_sw128(p_addr, 16, 1024), sdesc_sw128(v_addr, 16, 1024),
                            idesc_o, !first);
         }
-        if constexpr (F4) umma_commit(&sm.bar_o_done[X]);
+        umma_commit(&sm.bar_o_done[X]);
       };
       // tile X takes key tile j (ThriftAttention: unless the pair is promoted); ns, np count
       // the S and PV issued per tile, which the barrier phases follow
@@ -755,33 +753,32 @@ __global__ void __launch_bounds__(640, 1)
             ++ns[X];
           }
         } else {
-          // per tile, once its softmax has handed over P (and so is done with S): its PV, then
-          // its next S behind it.  The tensor core works on one tile's pair while the other
-          // tile's softmax runs, and a completed S implies the tile's previous PV is complete.
+          // per tile, once its softmax has handed over P (and so is done with S): its next S,
+          // then its PV behind it.  The tile's next softmax waits only for the S; the PV finishes
+          // during its max pass.  The tensor core works on one tile's pair while the other tile's
+          // softmax runs.
           for (int X = 0; X < 2; ++X) {
-            if (use(X, j)) {
+            const bool pv = use(X, j);
+            if (pv) {
               if (!mbar_wait(&sm.bar_p_full[X], npv[X] & 1, abort)) {
                 ok = false;
                 break;
               }
               tc_fence_after();
-              issue_pv(X, j, npv[X] == 0);
-              ++npv[X];
             }
             if (use(X, j + 1)) {
               issue_s(X, j + 1);
               ++ns[X];
+            }
+            if (pv) {
+              issue_pv(X, j, npv[X] == 0);
+              ++npv[X];
             }
           }
         }
         if (!ok) break;
         umma_commit(&sm.bar_v_empty[j % kVStages]);
         if (nextk) umma_commit(&sm.bar_k_empty[(j + 1) % kKStages]);
-      }
-      if constexpr (!F4) {
-        // the softmax epilogues wait for every MMA of their tile
-        umma_commit(&sm.bar_o_done[0]);
-        umma_commit(&sm.bar_o_done[1]);
       }
     }
   } else {
