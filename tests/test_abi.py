@@ -148,3 +148,85 @@ def test_q_smoothing_workspace_and_argument_errors(lib):
     assert sa.sage_attn_qs_bwd(*args, nbw - 256, 1, 4, 2, 256, 64, 1, 0, 1, 0.125, null) == sa.SAGE_ERR_INVALID_ARG
     assert sa.sage_attn_qs_bwd(*args, nbw, 1, 4, 2, 256, 64, 1, 0, 1, float("nan"), null) == sa.SAGE_ERR_INVALID_ARG
     assert sa.sage_attn_qs_bwd(*args, nbw, 1, 4, 3, 256, 64, 1, 0, 1, 0.125, null) == sa.SAGE_ERR_UNSUPPORTED
+
+
+def test_nvfp4_workspace_and_argument_errors(lib):
+    """The NVFP4 workspace is the plain one plus V's packed e2m1 codes (half a byte per value),
+    their e4m3 block scales (one per 16 tokens, in 512-byte atoms of 128 channel rows x 4
+    blocks, as the tensor core reads them) and one fp32 tensor scale per head; its views point
+    there, the plain workspace's do not, and its calls refuse bad arguments before any launch."""
+    for (B, H, N, D) in [(1, 2, 256, 64), (4, 16, 2048, 128), (2, 3, 333, 128)]:
+        np_ = (N + 127) // 128 * 128
+        base = sa.sage_attn_ws_bytes(B, H, N, D)
+        n = sa.sage_attn_fp4_ws_bytes(B, H, N, D)
+        extra = B * H * (D * np_ // 2 + np_ // 64 * 512 + 4)
+        assert base + extra <= n <= base + extra + 1024 and n % 256 == 0
+        v = sa.sage_attn_fp4_ws_views(ctypes.c_void_p(1 << 20), B, H, N, D)
+        assert v.v4 is not None and v.v4sf is not None and v.vg is not None
+        assert v.v4sf - v.v4 >= B * H * D * np_ // 2
+        assert (1 << 20) + n - v.v4sf >= B * H * np_ // 64 * 512
+        assert sa.sage_attn_fp4_bwd_ws_bytes(B, H, N, D) >= sa.sage_attn_bwd_ws_bytes(B, H, N, D) + B * H * np_ * D * 2
+    v = sa.sage_attn_ws_views(ctypes.c_void_p(1 << 20), 1, 2, 256, 64)
+    assert v.v4 is None and v.v4sf is None and v.vg is None
+    assert sa.sage_attn_fp4_ws_bytes(1, 1, 128, 96) == 0 and sa.sage_attn_fp4_bwd_ws_bytes(1, 1, 128, 96) == 0
+    null = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10001)
+    n = sa.sage_attn_fp4_ws_bytes(1, 2, 256, 64)
+    assert sa.sage_attn_fp4_quantize(null, fake, fake, 1, 2, 256, 64, 0, 1, fake, n, null) == sa.SAGE_ERR_INVALID_ARG
+    assert sa.sage_attn_fp4_quantize(fake, fake, fake, 1, 2, 256, 64, 0, 1, fake, n - 256,
+                                     null) == sa.SAGE_ERR_INVALID_ARG
+    assert sa.sage_attn_fp4_quantize(fake, fake, fake, 1, 2, 256, 96, 0, 1, fake, n, null) == sa.SAGE_ERR_UNSUPPORTED
+    assert sa.sage_attn_fp4_fwd(fake, fake, null, null, 1, 2, 256, 64, 1, 0.125, null) == sa.SAGE_ERR_INVALID_ARG
+    assert sa.sage_attn_fp4_fwd(fake, fake, fake, odd, 1, 2, 256, 64, 1, 0.125, null) == sa.SAGE_ERR_INVALID_ARG
+    assert sa.sage_attn_fp4_fwd(fake, fake, fake, null, 1, 2, 256, 64, 1, float("inf"), null) == sa.SAGE_ERR_INVALID_ARG
+    assert sa.sage_attn_fp4_fwd(fake, fake, fake, null, 1, 2, 256, 80, 1, 0.125, null) == sa.SAGE_ERR_UNSUPPORTED
+    nbw = sa.sage_attn_fp4_bwd_ws_bytes(1, 2, 256, 64)
+    args = [fake] * 11
+    assert sa.sage_attn_fp4_bwd(*args, nbw - 256, 1, 2, 256, 64, 1, 0, 1, 0.125, null) == sa.SAGE_ERR_INVALID_ARG
+    assert sa.sage_attn_fp4_bwd(*args, nbw, 1, 2, 256, 64, 1, 0, 1, float("nan"), null) == sa.SAGE_ERR_INVALID_ARG
+    assert sa.sage_attn_fp4_bwd(*args, nbw, 1, 2, 256, 96, 1, 0, 1, 0.125, null) == sa.SAGE_ERR_UNSUPPORTED
+    bad = list(args)
+    bad[4] = null  # LSE
+    assert sa.sage_attn_fp4_bwd(*bad, nbw, 1, 2, 256, 64, 1, 0, 1, 0.125, null) == sa.SAGE_ERR_INVALID_ARG
+
+
+def test_thrift_workspace_and_argument_errors(lib):
+    """ThriftAttention's scratch holds the block means (fp64), the pair keys (8 bytes) and the
+    promoted pairs (1 byte) per (query block, key tile), the fp16 copies of q', k'' and V, and the
+    low-bit pass's hand-over (fp32 output and two fp32 per row); the selection pointer lies
+    after the means and keys; the calls refuse bad arguments (a budget outside [0, 1] too)."""
+    for (B, H, N, D) in [(1, 2, 256, 64), (4, 16, 2048, 128), (2, 3, 333, 128)]:
+        np_ = (N + 127) // 128 * 128
+        nb = np_ // 128
+        bh = B * H
+        need = 2 * bh * nb * D * 8 + bh * nb * nb * 9 + 3 * bh * np_ * D * 2 + bh * np_ * D * 4 + bh * np_ * 8
+        n = sa.sage_attn_thrift_ws_bytes(B, H, N, D)
+        assert need <= n <= need + 9 * 256 and n % 256 == 0
+        sel = sa.sage_attn_thrift_sel(ctypes.c_void_p(1 << 20), B, H, N, D)
+        assert sel - (1 << 20) >= 2 * bh * nb * D * 8 + bh * nb * nb * 8
+        assert (1 << 20) + n - sel >= bh * nb * nb
+    assert sa.sage_attn_thrift_ws_bytes(1, 1, 128, 96) == 0
+    assert sa.sage_attn_thrift_sel(ctypes.c_void_p(0), 1, 1, 128, 64) is None
+    assert sa.sage_attn_thrift_sel(ctypes.c_void_p(1 << 20), 1, 1, 128, 96) is None
+    null = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10001)
+    n = sa.sage_attn_ws_bytes(1, 2, 256, 64)
+    nt = sa.sage_attn_thrift_ws_bytes(1, 2, 256, 64)
+
+    def tq(q=fake, budget=0.05, D=64, ws_bytes=n, tws=fake, tws_bytes=nt):
+        return sa.sage_attn_thrift_quantize(q, fake, fake, 1, 2, 256, D, 0, 1, 1, budget, fake, ws_bytes, tws,
+                                            tws_bytes, null)
+    assert tq(q=null) == sa.SAGE_ERR_INVALID_ARG
+    assert tq(tws=odd) == sa.SAGE_ERR_INVALID_ARG
+    for budget in (-0.01, 1.01, float("nan")):
+        assert tq(budget=budget) == sa.SAGE_ERR_INVALID_ARG
+    assert tq(D=96) == sa.SAGE_ERR_UNSUPPORTED
+    assert tq(ws_bytes=n - 256) == sa.SAGE_ERR_INVALID_ARG
+    assert tq(tws_bytes=nt - 256) == sa.SAGE_ERR_INVALID_ARG
+    assert sa.sage_attn_thrift_fwd(fake, fake, fake, null, null, 1, 2, 256, 64, 1, 0.125, null) == sa.SAGE_ERR_INVALID_ARG
+    assert sa.sage_attn_thrift_fwd(fake, null, fake, fake, null, 1, 2, 256, 64, 1, 0.125, null) == sa.SAGE_ERR_INVALID_ARG
+    assert sa.sage_attn_thrift_fwd(fake, fake, fake, fake, null, 1, 2, 256, 64, 1, float("nan"),
+                                   null) == sa.SAGE_ERR_INVALID_ARG
+    assert sa.sage_attn_thrift_fwd(fake, fake, fake, fake, null, 1, 2, 256, 80, 1, 0.125, null) == sa.SAGE_ERR_UNSUPPORTED
