@@ -251,7 +251,7 @@ struct HpSmem {
   uint8_t k[2][128 * D * 2];  // K16 tiles
   uint8_t v[2][128 * D * 2];  // V16 tiles, [64-channel atom][128 keys][128 B] (MN-major B)
   uint8_t p[128 * 128 * 2];   // P16 (fp16), [64-key atom][128 rows][128 B] (K-major A)
-  uint64_t bar_q, bar_kv_full[2], bar_kv_empty[2], bar_s, bar_p, bar_o;
+  uint64_t bar_q, bar_kv_full[2], bar_kv_empty[2], bar_s[2], bar_p, bar_o;
   uint32_t tmem_base;
   int abort;
 };
@@ -282,7 +282,9 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn_major, 
 
 // One CTA per (128-query tile, head): warps 0-3 own the tile's rows (thread t = row t = TMEM
 // lane t, all 128 keys of a tile), warp 4 loads tiles with TMA, warp 5 allocates TMEM and
-// issues the MMAs.  TMEM: S [0, 128), O [128, 128 + D).
+// issues the MMAs in the order S(0) | S(i+1) PV(i) ...: S is double-buffered, so the next
+// promoted tile's S runs while the softmax works on this one.  TMEM: S of tile i at
+// [128 (i % 2), 128 (i % 2) + 128), O [256, 256 + D).
 template <int D>
 __global__ void __launch_bounds__(192, 1)
     fwd_hp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -297,14 +299,14 @@ __global__ void __launch_bounds__(192, 1)
   int nhp = 0;
   for (int j = 0; j < nJ; ++j) nhp += srow[j] != 0;
   if (nhp == 0) return;  // the low-bit pass has finished this tile's rows
-  constexpr uint32_t kCols = 256, cS = 0, cO = 128;
+  constexpr uint32_t kCols = 512, cO = 256;
   if (tid == 0) {
     mbar_init(&sm.bar_q, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sm.bar_kv_full[s], 1);
       mbar_init(&sm.bar_kv_empty[s], 1);
+      mbar_init(&sm.bar_s[s], 1);  // one phase per use of S buffer s
     }
-    mbar_init(&sm.bar_s, 1);
     mbar_init(&sm.bar_p, 128);
     mbar_init(&sm.bar_o, 1);
     sm.abort = 0;
@@ -345,33 +347,42 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else if (warp == 5) {
     if (lane == 0) {
-      // ---------------- MMA issuer: S16 of tile i, then (once P16 is in) PV16 of tile i
+      // ---------------- MMA issuer: S16 of tile i + 1 as soon as its K16 is in (its S buffer
+      // was freed when the softmax handed over P16 of tile i - 1, waited for below before PV16
+      // of tile i - 1), then PV16 of tile i once P16 is in
       constexpr uint32_t id_s = idesc_f16(128, 128, false, false);
       constexpr uint32_t id_o = idesc_f16(128, D, false, true);
       const uint32_t a_q = smem_u32(sm.q), a_p = smem_u32(sm.p);
-      bool ok = mbar_wait(&sm.bar_q, 0, abort);
-      for (int i = 0; ok && i < nhp; ++i) {
-        const int s = i & 1;
-        if (!mbar_wait(&sm.bar_kv_full[s], (i >> 1) & 1, abort)) break;
-        // S may be overwritten once the softmax has written P16 of the previous tile (it read S first)
-        if (i > 0 && !mbar_wait(&sm.bar_p, (i - 1) & 1, abort)) break;
-        tc_fence_after();
-        const uint32_t a_k = smem_u32(sm.k[s]);
+      auto issue_s = [&](int i) {
+        const uint32_t a_k = smem_u32(sm.k[i & 1]);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_bf16(tmem + cS, sdesc_sw128(a_q + off, 16, 1024), sdesc_sw128(a_k + off, 16, 1024), id_s, kk > 0);
+          umma_bf16(tmem + (uint32_t)((i & 1) * 128), sdesc_sw128(a_q + off, 16, 1024),
+                    sdesc_sw128(a_k + off, 16, 1024), id_s, kk > 0);
         }
-        umma_commit(&sm.bar_s);
+        umma_commit(&sm.bar_s[i & 1]);
+      };
+      bool ok = mbar_wait(&sm.bar_q, 0, abort) && mbar_wait(&sm.bar_kv_full[0], 0, abort);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+      }
+      for (int i = 0; ok && i < nhp; ++i) {
+        if (i + 1 < nhp) {
+          if (!mbar_wait(&sm.bar_kv_full[(i + 1) & 1], ((i + 1) >> 1) & 1, abort)) break;
+          tc_fence_after();
+          issue_s(i + 1);
+        }
         if (!mbar_wait(&sm.bar_p, i & 1, abort)) break;
         tc_fence_after();
-        const uint32_t a_v = smem_u32(sm.v[s]);
+        const uint32_t a_v = smem_u32(sm.v[i & 1]);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           umma_bf16(tmem + cO, sdesc_sw128(a_p + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
                     sdesc_sw128(a_v + kk * 2048, 16384, 1024), id_o, 1);
         umma_commit(&sm.bar_o);
-        umma_commit(&sm.bar_kv_empty[s]);
+        umma_commit(&sm.bar_kv_empty[i & 1]);
       }
     }
   } else {
@@ -379,7 +390,7 @@ __global__ void __launch_bounds__(192, 1)
     const int t = tid;
     const int row = qb * 128 + t;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const uint32_t s_col = tmem + lane_base + cS, o_col = tmem + lane_base + cO;
+    const uint32_t o_col = tmem + lane_base + cO;
     uint8_t* prow = sm.p + (t >> 3) * 1024 + (t & 7) * 128;
     const float* ml = prm.ml + ((size_t)bh * prm.np + row) * 2;
     float m = ml[0], l = ml[1];
@@ -404,9 +415,11 @@ __global__ void __launch_bounds__(192, 1)
     int i = 0;
     for (int j = 0; j < nJ; ++j) {
       if (!srow[j]) continue;
-      ok = ok && mbar_wait(&sm.bar_s, i & 1, abort);
+      ok = ok && mbar_wait(&sm.bar_s[i & 1], (i >> 1) & 1, abort);
       tc_fence_after();
-      // keys [0, lim) of the tile are valid
+      const uint32_t s_col = tmem + lane_base + (uint32_t)((i & 1) * 128);
+      // keys [0, lim) of the tile are valid; the others become -inf (2^-inf = 0 below), on the
+      // tiles that have any
       int lim = min(128, prm.N - j * 128);
       if (prm.causal && j == qb) lim = min(lim, t + 1);
       uint32_t sv[4][32];
@@ -415,12 +428,21 @@ __global__ void __launch_bounds__(192, 1)
       tmem_ld_wait();
 #pragma unroll
       for (int c = 0; c < 4; ++c) reg_fence32(sv[c]);
-      float mx = -INFINITY;
+      if (__any_sync(0xffffffffu, lim < 128)) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (32 * c + e >= lim) sv[c][e] = 0xff800000u;
+      }
+      // the maximum of RN(s alpha) is RN(max(s) alpha): alpha > 0 and rounding is monotone
+      float a[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (32 * c + e < lim) mx = fmaxf(mx, __fmul_rn(__uint_as_float(sv[c][e]), prm.alpha));
+        for (int e = 0; e < 32; e += 2) a[c] = max3(a[c], __uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]));
+      const float amax = fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3]));
+      const float mx = amax == -INFINITY ? -INFINITY : __fmul_rn(amax, prm.alpha);
       const float m_new = fmaxf(m, mx);
       const float corr = (m == -INFINITY) ? 0.f : ex2f(m - m_new);
       // the previous tile's PV must be done before O is rescaled (and P16 rewritten)
@@ -428,16 +450,17 @@ __global__ void __launch_bounds__(192, 1)
         ok = ok && mbar_wait(&sm.bar_o, (i - 1) & 1, abort);
         tc_fence_after();
       }
-      float ls = 0.f;
+      const uint64_t al2 = f2(prm.alpha, prm.alpha), nm2 = f2(-m_new, -m_new);
+      uint64_t ls2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};  // two independent chains
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float p0 = 0.f, p1 = 0.f;
-          if (32 * c + e < lim) p0 = ex2f(fmaf(__uint_as_float(sv[c][e]), prm.alpha, -m_new));
-          if (32 * c + e + 1 < lim) p1 = ex2f(fmaf(__uint_as_float(sv[c][e + 1]), prm.alpha, -m_new));
-          ls += p0 + p1;
+          float t0, t1;
+          f2split(ffma2(f2(__uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1])), al2, nm2), t0, t1);
+          const float p0 = ex2f(t0), p1 = ex2f(t1);
+          ls2[(e >> 1) & 1] = fadd2(ls2[(e >> 1) & 1], f2(p0, p1));
           const __half2 h = __floats2half2_rn(p0, p1);
           w[e >> 1] = *reinterpret_cast<const uint32_t*>(&h);
         }
@@ -450,7 +473,9 @@ __global__ void __launch_bounds__(192, 1)
               make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
         }
       }
-      l = fmaf(l, corr, 448.f * ls);
+      float la, lb;
+      f2split(fadd2(ls2[0], ls2[1]), la, lb);
+      l = fmaf(l, corr, 448.f * (la + lb));
       // O rescale when the maximum of any row of the warp moved (TMEM access is warp-wide)
       if (__any_sync(0xffffffffu, corr != 1.f)) {
 #pragma unroll 1
