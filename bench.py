@@ -246,7 +246,7 @@ def run_reference(args, w):
 # -------------------------------------------------------------------- ours
 def kernel_fractions(flops: dict, fwd_ms: float, bwd_main_ms: float, peaks: dict) -> dict:
     """Achieved TFLOP/s of fwd_kernel and bwd_main_kernel and their fractions of the FP8-equivalent
-    peak (2 x measured bf16, the benchmark spec's INT8/FP8 denominator) and of the executed formats
+    peak (2 x measured bf16: the dense INT8/FP8 tensor rate the targets use) and of the executed formats
     (S, dP, dQ, dK on bf16 tensor cores; PV, dV on FP8)."""
     fp8 = 2.0 * peaks["bf16"]
     fa = flops["fwd"] / (fwd_ms * 1e-3) / 1e12
