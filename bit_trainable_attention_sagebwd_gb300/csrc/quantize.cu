@@ -656,14 +656,16 @@ __global__ void __launch_bounds__(kThreads) qsmooth_q_kernel(const __nv_bfloat16
 // The logit term of Q-smoothing, dsb[qh][I][j] = sum_d qmean[qh][I][d] k''[kvh][j][d] (fp32
 // products and sums, d ascending), for the 128 keys j of block kb and every query block I.
 // k'' is recomputed as K's quantizer forms it: RN(k r) with QK-norm, minus the smoothing mean.
-// One CTA per (key block, query head); a warp takes 4 query blocks at a time, a lane 4 keys.
+// One CTA per (key block, query head); a warp takes 8 query blocks at a time, a lane 4 keys:
+// 32 FMAs per 16-byte shared load of keys (the query means are a broadcast), which keeps the
+// FMA pipe ahead of shared-memory bandwidth (with 4 query blocks it ran at half the FMA rate).
 template <int D, bool QKN>
 __global__ void __launch_bounds__(kThreads) qs_bias_kernel(const __nv_bfloat16* __restrict__ K, int N,
                                                             int k_smooth, const float* __restrict__ kmean,
                                                             const float* __restrict__ kr,
                                                             const float* __restrict__ qmean, float* __restrict__ dsb,
                                                             int group) {
-  constexpr int IC = 32;  // query blocks per chunk: 8 warps x 4
+  constexpr int IC = 64;  // query blocks per chunk: 8 warps x 8
   const int kb = blockIdx.x, qh = blockIdx.y, nb = gridDim.x, np = nb * 128;
   const int kvh = qh / group;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -698,24 +700,26 @@ __global__ void __launch_bounds__(kThreads) qs_bias_kernel(const __nv_bfloat16* 
       qt[d][i] = I0 + i < nb ? qmean[((size_t)qh * nb + I0 + i) * D + d] : 0.f;
     }
     __syncthreads();
-    float acc[4][4];
+    float acc[8][4];
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int a = 0; a < 8; ++a)
 #pragma unroll
       for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
 #pragma unroll 4
     for (int d = 0; d < D; ++d) {
       const float4 kv = *reinterpret_cast<const float4*>(&ks[d * 128 + 4 * lane]);
-      const float4 qv = *reinterpret_cast<const float4*>(&qt[d][4 * warp]);
-      const float kk[4] = {kv.x, kv.y, kv.z, kv.w}, qq[4] = {qv.x, qv.y, qv.z, qv.w};
+      const float4 qv0 = *reinterpret_cast<const float4*>(&qt[d][8 * warp]);
+      const float4 qv1 = *reinterpret_cast<const float4*>(&qt[d][8 * warp + 4]);
+      const float kk[4] = {kv.x, kv.y, kv.z, kv.w};
+      const float qq[8] = {qv0.x, qv0.y, qv0.z, qv0.w, qv1.x, qv1.y, qv1.z, qv1.w};
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
+      for (int a = 0; a < 8; ++a)
 #pragma unroll
         for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(qq[a], kk[b], acc[a][b]);
     }
 #pragma unroll
-    for (int a = 0; a < 4; ++a) {
-      const int I = I0 + 4 * warp + a;
+    for (int a = 0; a < 8; ++a) {
+      const int I = I0 + 8 * warp + a;
       if (I < nb)
         *reinterpret_cast<float4*>(dsb + ((size_t)qh * nb + I) * np + kb * 128 + 4 * lane) =
             make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
