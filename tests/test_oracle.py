@@ -731,6 +731,48 @@ def test_thrift_selection_invariants():
                 assert score[sel].min() >= score[vis & ~sel].max()
 
 
+def _bf16_values(rng, n, lo, hi):
+    """n bf16 values of random sign and significand whose biased exponents lie in [lo, hi],
+    with both ends present."""
+    e = rng.integers(lo, hi + 1, size=n)
+    e[0], e[1] = lo, hi
+    bits = (rng.integers(0, 2, size=n) << 15) | (e << 7) | rng.integers(0, 128, size=n)
+    return torch.from_numpy(bits.astype(np.int16)).view(torch.bfloat16).double().numpy()
+
+
+def test_thrift_block_means_are_exact_within_the_exponent_bound():
+    """The block means are fp64 sums in token order divided by the count.  When a 128-token
+    block's bf16 values span at most 38 binades every partial sum is an integer multiple of
+    the smallest value's ulp below 2^53 of them, so the in-order sum is the exact sum and the
+    mean is the exact mean rounded once (checked against rational arithmetic); one binade
+    more and an in-order sum can round."""
+    from fractions import Fraction
+    rng = np.random.default_rng(73)
+    for lo in (1, 60, 127 - 19, 254 - 38):
+        x = np.stack([_bf16_values(rng, 128, lo, lo + 38) for _ in range(4)], axis=1)
+        got = orc._block_means(x)
+        for d in range(x.shape[1]):
+            exact = sum(Fraction(float(t)) for t in x[:, d]) / 128
+            assert got[0, d] == float(exact)
+    # ragged tail block: the count is the block's own
+    x = np.stack([_bf16_values(rng, 128 + 37, 100, 138)], axis=1)
+    got = orc._block_means(x)
+    assert got[1, 0] == float(sum(Fraction(float(t)) for t in x[128:, 0]) / 37)
+    # 39 binades: 1.0078125 first (odd in units of its ulp 2^-7), then 127 copies of 255 * 2^32
+    # (exponent 39 above); the exact sum needs 54 significant bits
+    lead = float.fromhex("0x1.02p+0")
+    big = 255.0 * 2.0 ** 32
+    s = 0.0
+    for t in [lead] + [big] * 127:
+        s += t
+    assert Fraction(s) != Fraction(lead) + 127 * Fraction(big)
+    # and at 38 binades the same construction stays exact
+    s = 0.0
+    for t in [lead] + [big / 2] * 127:
+        s += t
+    assert Fraction(s) == Fraction(lead) + 127 * Fraction(big / 2)
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_thrift_budget_zero_is_the_low_bit_forward(causal):
     q, k, v = _thrift_case(71)
