@@ -234,10 +234,14 @@ struct BwdSmem {
   uint8_t k[128 * D * 2];    // K codes of this key block (resident)
   uint8_t v[128 * D * 2];    // V bf16 of this key block (resident)
   uint8_t q[2][128 * D * 2]; // Q codes of the current and next query blocks
-  uint8_t dob[128 * D * 2];  // dO bf16 of the current query block
+  // dO bf16 of the current query block; D = 64: two, by query block parity (pipelined order)
+  uint8_t dob[D == 64 ? 2 : 1][128 * D * 2];
   uint8_t do8[D * 128];      // dO e4m3 codes, channel-major
   uint8_t p[128 * 128];      // P e4m3, query rows of 128 keys
   uint8_t ds[128 * 128 * 2]; // dS INT8 codes in bf16, query rows; keys [0,64) then [64,128)
+  // D = 64 (pipelined order): the dQ boxes, [query block parity][group] x 16 KB, so that the dS
+  // codes need not wait for the previous block's reduce to read them
+  uint8_t dqst[D == 64 ? 4 * 16384 : 16];
   // Q-smoothing: bf16 ones, the B operand (16 x 16, unswizzled) of the dS column sums
   __align__(128) uint16_t ones[256];
   __align__(16) float bias[2][128];  // log2(448) - LSE_i log2(e), per Q buffer
@@ -246,11 +250,12 @@ struct BwdSmem {
     __align__(16) float dsb[2][128];   // Q-smoothing: the logit terms of the block's keys (D_i then
                                        // comes from global memory)
   };
-  float smax[8];             // per compute warp: max |448 dS| over its rows of its group's keys
+  // per query block parity and compute warp: max |448 dS| over its rows of its group's keys
+  float smax[2][8];
   uint64_t bar_kv;
-  uint64_t bar_q_full[2], bar_do_full, bar_do8_full;
-  uint64_t bar_q_free[2], bar_do_free, bar_do8_free;
-  uint64_t bar_s, bar_dp, bar_p, bar_ds[2], bar_dk, bar_part, bar_free_s, bar_free_dp, bar_cs;
+  uint64_t bar_q_full[2], bar_do_full[2], bar_do8_full;
+  uint64_t bar_q_free[2], bar_do_free[2], bar_do8_free;
+  uint64_t bar_s, bar_dp, bar_p, bar_ds[2][2], bar_dk, bar_part, bar_dk_read, bar_dq_read, bar_free_dp, bar_cs;
   uint64_t bar_dv;  // NVFP4: the dV MMA has read P^ (which shares the dS block)
   uint32_t tmem_base;
   int abort;
@@ -258,6 +263,7 @@ struct BwdSmem {
 };
 
 static_assert(sizeof(BwdSmem<128>) <= 227 * 1024, "the backward's shared memory exceeds 227 KB");
+static_assert(sizeof(BwdSmem<64>) <= 227 * 1024, "the backward's shared memory exceeds 227 KB");
 
 struct BwdParams {
   int N, np, nqb, causal, qk_norm;
@@ -304,7 +310,10 @@ constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23: x + M - M rounds x to
 //               [DG*g, DG*g + DG) (DG = D/2).
 //   warp 8 lane 0: TMA producer;  warp 9: TMEM allocator, lane 0 issues UMMAs.
 // TMEM columns: [0,128) S, then dK_part; [128,256) dP, then dQ of keys [64,128);
-// [256,256+D) dV; [384,384+D) dQ of keys [0,64).
+// [256,256+D) dV; [384,384+D) dQ of keys [0,64).  At D = 64 (plain e4m3 path) dK_part and the
+// dQ of keys [64,128) take the free columns [320,384) and [448,512) instead, so that S and dP
+// of the next query block can go in while this one's parts wait for their readout: the compute
+// warps then run P of block s + 1 between the dS codes of block s and its readouts (PIPE).
 // dQ staging: each group writes its scaled dQ part as [32 features][128 queries] fp32
 // boxes (16 KB) into shared memory the next MMAs do not read (its own dS block, then half
 // of the Q buffer just consumed); one thread per group adds them to the feature-major
@@ -344,28 +353,41 @@ __global__ void __launch_bounds__(384, 1)
   const int gs = prm.group / prm.split;
   const int qh0 = bh * prm.group + sp * gs;
   const int n_it = gs * nq;
+  // D = 64 without Q-smoothing or NVFP4: the software-pipelined order (dK, dQ and dP in TMEM
+  // columns of their own)
+  constexpr bool PIPE = D == 64 && !QS && !F4;
   constexpr uint32_t kCols = 512;
-  constexpr uint32_t cS = 0, cDP = 128, cDV = 256, cDQ0 = 384, cDQ1 = 128;  // TMEM column bases
+  // TMEM column bases
+  constexpr uint32_t cS = 0, cDP = 128, cDV = 256, cDQ0 = 384;
+  constexpr uint32_t cDK = PIPE ? 320 : cS, cDQ1 = PIPE ? 448 : cDP;
+  static_assert(!PIPE || cDQ1 + D <= kCols, "the pipelined TMEM layout exceeds 512 columns");
   constexpr uint32_t kTile = 128 * D * 2;
 
   if (tid == 0) {
     mbar_init(&sm.bar_kv, 1);
     mbar_init(&sm.bar_q_full[0], 1);
     mbar_init(&sm.bar_q_full[1], 1);
-    mbar_init(&sm.bar_do_full, 1);
+    mbar_init(&sm.bar_do_full[0], 1);
+    mbar_init(&sm.bar_do_full[1], 1);
     mbar_init(&sm.bar_do8_full, 1);
-    mbar_init(&sm.bar_q_free[0], 2);  // one arrival per group once its dQ boxes are read
-    mbar_init(&sm.bar_q_free[1], 2);
-    mbar_init(&sm.bar_do_free, 1);
+    // one arrival per group once its dQ boxes are read; PIPE: the dK MMA's commit (no dQ box
+    // goes into a Q buffer at D = 64)
+    mbar_init(&sm.bar_q_free[0], PIPE ? 1 : 2);
+    mbar_init(&sm.bar_q_free[1], PIPE ? 1 : 2);
+    mbar_init(&sm.bar_do_free[0], 1);
+    mbar_init(&sm.bar_do_free[1], 1);
     mbar_init(&sm.bar_do8_free, 1);
     mbar_init(&sm.bar_s, 1);
     mbar_init(&sm.bar_dp, 1);
     mbar_init(&sm.bar_p, 256);
-    mbar_init(&sm.bar_ds[0], 128);
-    mbar_init(&sm.bar_ds[1], 128);
+    mbar_init(&sm.bar_ds[0][0], 128);  // [query block parity][group]: the group's dS codes are in
+    mbar_init(&sm.bar_ds[0][1], 128);
+    mbar_init(&sm.bar_ds[1][0], 128);
+    mbar_init(&sm.bar_ds[1][1], 128);
     mbar_init(&sm.bar_dk, 1);
     mbar_init(&sm.bar_part, 1);
-    mbar_init(&sm.bar_free_s, 256);
+    mbar_init(&sm.bar_dk_read, 256);
+    mbar_init(&sm.bar_dq_read, 256);
     mbar_init(&sm.bar_free_dp, 256);
     mbar_init(&sm.bar_cs, 256);
     mbar_init(&sm.bar_dv, 1);
@@ -407,15 +429,13 @@ __global__ void __launch_bounds__(384, 1)
         tma_load_3d(sm.k + c * 16384, &tm_k, c * 64, kb * 128, bh, &sm.bar_kv);
         tma_load_3d(sm.v + c * 16384, &tm_v, c * 64, kb * 128, bh, &sm.bar_kv);
       }
-      // (query block I, query head qh) of iteration it, advanced without a division
-      for (int it = 0, I = I0, qh = qh0; it < n_it; ++it, I = I + 1 < prm.nqb ? I + 1 : I0,
-               qh = I == I0 ? qh + 1 : qh) {
-        if (it > 0 && !mbar_wait(&sm.bar_do_free, (it - 1) & 1, abort)) break;
-        mbar_arrive_expect_tx(&sm.bar_do_full, kTile);
+      auto load_do = [&](int b, int I, int qh) {
+        mbar_arrive_expect_tx(&sm.bar_do_full[b], kTile);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sm.dob + c * 16384, &tm_do, c * 64, I * 128, qh, &sm.bar_do_full);
-        if (it > 0 && !mbar_wait(&sm.bar_do8_free, (it - 1) & 1, abort)) break;
+          tma_load_3d(sm.dob[b] + c * 16384, &tm_do, c * 64, I * 128, qh, &sm.bar_do_full[b]);
+      };
+      auto load_do8 = [&](int I, int qh) {
         if constexpr (F4) {
           // the e4m3 codes of dO as bf16, channel-major, in two 64-query boxes
           mbar_arrive_expect_tx(&sm.bar_do8_full, D * 256);
@@ -425,8 +445,8 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive_expect_tx(&sm.bar_do8_full, D * 128);
           tma_load_3d(sm.do8, &tm_do8, I * 128, 0, qh, &sm.bar_do8_full);
         }
-        const int qs = it & 1;
-        if (it > 1 && !mbar_wait(&sm.bar_q_free[qs], ((it >> 1) - 1) & 1, abort)) break;
+      };
+      auto load_q = [&](int qs, int I, int qh) {
         mbar_arrive_expect_tx(&sm.bar_q_full[qs], kTile + 1024);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
@@ -438,6 +458,43 @@ __global__ void __launch_bounds__(384, 1)
           bulk_load(sm.dsb[qs], prm.dsb + ((size_t)qh * prm.nqb + I) * prm.np + kb * 128, 512, &sm.bar_q_full[qs]);
         else
           bulk_load(sm.dvec[qs], prm.dvec + (size_t)qh * prm.np + I * 128, 512, &sm.bar_q_full[qs]);
+      };
+      if constexpr (PIPE) {
+        // S(it + 1) goes in early in block it, so Q(it + 1) comes first: as soon as the dK MMA
+        // of block it - 1 has read its buffer; then dO of block it + 1 (once dP(it - 1) has read
+        // its buffer) and its codes (once dV(it) has read theirs)
+        load_q(0, I0, qh0);
+        load_do(0, I0, qh0);
+        load_do8(I0, qh0);
+        // (query block I, query head qh) of block j + 1, advanced without a division
+        int I = I0, qh = qh0;
+        for (int j = 0; j + 1 < n_it; ++j) {
+          if (I + 1 < prm.nqb) {
+            ++I;
+          } else {
+            I = I0;
+            ++qh;
+          }
+          const int q = j + 1;
+          if (q > 1 && !mbar_wait(&sm.bar_q_free[q & 1], ((q >> 1) - 1) & 1, abort)) break;
+          load_q(q & 1, I, qh);
+          if (q > 1 && !mbar_wait(&sm.bar_do_free[q & 1], ((q >> 1) - 1) & 1, abort)) break;
+          load_do(q & 1, I, qh);
+          if (!mbar_wait(&sm.bar_do8_free, j & 1, abort)) break;
+          load_do8(I, qh);
+        }
+      } else {
+        // (query block I, query head qh) of iteration it, advanced without a division
+        for (int it = 0, I = I0, qh = qh0; it < n_it; ++it, I = I + 1 < prm.nqb ? I + 1 : I0,
+                 qh = I == I0 ? qh + 1 : qh) {
+          if (it > 0 && !mbar_wait(&sm.bar_do_free[0], (it - 1) & 1, abort)) break;
+          load_do(0, I, qh);
+          if (it > 0 && !mbar_wait(&sm.bar_do8_free, (it - 1) & 1, abort)) break;
+          load_do8(I, qh);
+          const int qs = it & 1;
+          if (it > 1 && !mbar_wait(&sm.bar_q_free[qs], ((it >> 1) - 1) & 1, abort)) break;
+          load_q(qs, I, qh);
+        }
       }
     } else if (warp == WMMA && lane == 0) {
       // ---------------- UMMA issuer
@@ -446,27 +503,22 @@ __global__ void __launch_bounds__(384, 1)
       constexpr uint32_t id_dk = idesc_bf16(128, D, true, true);      // dK = dS^T Q: A from query rows
       constexpr uint32_t id_dq = idesc_bf16(128, D, false, true);     // dQ = dS K: B from key rows
       constexpr uint32_t id_cs = idesc_bf16(128, 16, true, false);    // dS^T ones: column sums
-      const uint32_t a_k = smem_u32(sm.k), a_v = smem_u32(sm.v), a_do = smem_u32(sm.dob);
+      const uint32_t a_k = smem_u32(sm.k), a_v = smem_u32(sm.v);
       const uint32_t a_do8 = smem_u32(sm.do8), a_p = smem_u32(sm.p), a_ds = smem_u32(sm.ds);
-      bool ok = mbar_wait(&sm.bar_kv, 0, abort);
-      for (int it = 0; ok && it < n_it; ++it) {
-        const uint32_t ph = it & 1;
+      // S(it) = Q(it) K^T
+      auto issue_s = [&](int it) {
         const uint32_t a_q = smem_u32(sm.q[it & 1]);
-        // S(it) goes in as soon as the previous dK part has been read out of its columns,
-        // dP(it) once the previous dQ halves have been read: both overlap the compute
-        // warps' work on iteration it - 1
-        if (!mbar_wait(&sm.bar_q_full[it & 1], (it >> 1) & 1, abort)) break;
-        if (it > 0 && !mbar_wait(&sm.bar_free_s, (it - 1) & 1, abort)) break;
-        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
           umma_bf16(tmem + cS, sdesc_sw128(a_q + off, 16, 1024), sdesc_sw128(a_k + off, 16, 1024), id_s, kk > 0);
         }
         umma_commit(&sm.bar_s);
-        if (!mbar_wait(&sm.bar_do_full, ph, abort)) break;
-        if (it > 0 && !mbar_wait(&sm.bar_free_dp, (it - 1) & 1, abort)) break;
-        tc_fence_after();
+      };
+      // dP(it) = dO(it) V^T; dO's bf16 buffer is free once it completes
+      auto issue_dp = [&](int it) {
+        const int b = PIPE ? it & 1 : 0;
+        const uint32_t a_do = smem_u32(sm.dob[b]);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -474,9 +526,10 @@ __global__ void __launch_bounds__(384, 1)
                     kk > 0);
         }
         umma_commit(&sm.bar_dp);
-        umma_commit(&sm.bar_do_free);
-        if (!mbar_wait(&sm.bar_p, ph, abort) || !mbar_wait(&sm.bar_do8_full, ph, abort)) break;
-        tc_fence_after();
+        umma_commit(&sm.bar_do_free[b]);
+      };
+      // dV += P^T dO8; dO's codes are free once it completes
+      auto issue_dv = [&](int it) {
         if constexpr (F4) {
           // dV[key, d] += sum_q (2688 P^)[q, key] dO8[q, d] on bf16: A read MN-major from the query
           // rows of the dS block, B = dO8 codes K-major in two 64-query atoms; 16 queries per step
@@ -495,12 +548,14 @@ __global__ void __launch_bounds__(384, 1)
                     id_dv, (it > 0 || kk > 0));
         }
         umma_commit(&sm.bar_do8_free);
-        // dK first, once both groups' codes are in, so its readout starts as early as possible
-        if (!mbar_wait(&sm.bar_ds[0], ph, abort) || !mbar_wait(&sm.bar_ds[1], ph, abort)) break;
-        tc_fence_after();
+      };
+      // dK part, then dQ of keys [0,64) and [64,128), once both groups' dS codes are in: dK
+      // first, so that its readout starts as early as possible
+      auto issue_dk_dq = [&](int it) -> bool {
+        const uint32_t a_q = smem_u32(sm.q[it & 1]);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_bf16(tmem + cS, sdesc_sw128(a_ds + kk * 2048, 16384, 1024), sdesc_sw128(a_q + kk * 2048, 16384, 1024),
+          umma_bf16(tmem + cDK, sdesc_sw128(a_ds + kk * 2048, 16384, 1024), sdesc_sw128(a_q + kk * 2048, 16384, 1024),
                     id_dk, kk > 0);
         if constexpr (QS) {
           // column sums of the dS codes (exact integers) into the dP columns, which are free
@@ -511,12 +566,13 @@ __global__ void __launch_bounds__(384, 1)
             umma_bf16(tmem + cDQ1, sdesc_sw128(a_ds + kk * 2048, 16384, 1024), b1, id_cs, kk > 0);
         }
         umma_commit(&sm.bar_dk);
+        if constexpr (PIPE) umma_commit(&sm.bar_q_free[it & 1]);  // dK was Q(it)'s last reader
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           umma_bf16(tmem + cDQ0, sdesc_sw128(a_ds + kk * 32, 16, 1024), sdesc_sw128(a_k + kk * 2048, 16384, 1024),
                     id_dq, kk > 0);
         if constexpr (QS) {
-          if (!mbar_wait(&sm.bar_cs, ph, abort)) break;  // the column sums are read
+          if (!mbar_wait(&sm.bar_cs, it & 1, abort)) return false;  // the column sums are read
           tc_fence_after();
         }
 #pragma unroll
@@ -524,6 +580,71 @@ __global__ void __launch_bounds__(384, 1)
           umma_bf16(tmem + cDQ1, sdesc_sw128(a_ds + 16384 + kk * 32, 16, 1024),
                     sdesc_sw128(a_k + 8192 + kk * 2048, 16384, 1024), id_dq, kk > 0);
         umma_commit(&sm.bar_part);
+        return true;
+      };
+      bool ok = mbar_wait(&sm.bar_kv, 0, abort);
+      if constexpr (PIPE) {
+        // S(it + 1) goes in once P(it) has read S(it), and dP(it + 1) once dS(it) has read dP(it),
+        // both while the compute warps still work on block it.  A group is then at most one dS
+        // phase ahead of the other's readout: the tile maxima and the dS barriers it reads there
+        // are kept per query block parity.
+        ok = ok && mbar_wait(&sm.bar_q_full[0], 0, abort) && mbar_wait(&sm.bar_do_full[0], 0, abort);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0);
+          issue_dp(0);
+        }
+        for (int it = 0; ok && it < n_it; ++it) {
+          const uint32_t ph = it & 1;
+          const bool more = it + 1 < n_it;
+          if (!mbar_wait(&sm.bar_p, ph, abort) || !mbar_wait(&sm.bar_do8_full, ph, abort)) break;
+          tc_fence_after();
+          // dV(it) before the wait for Q(it + 1): the producer loads that only after dO's codes
+          // of block it have been read
+          issue_dv(it);
+          if (more) {
+            if (!mbar_wait(&sm.bar_q_full[(it + 1) & 1], ((it + 1) >> 1) & 1, abort)) break;
+            tc_fence_after();
+            issue_s(it + 1);
+          }
+          if (!mbar_wait(&sm.bar_ds[ph][0], (it >> 1) & 1, abort) || !mbar_wait(&sm.bar_ds[ph][1], (it >> 1) & 1, abort))
+            break;
+          // the parts of block it - 1 have been read out of their columns
+          if (it > 0 && (!mbar_wait(&sm.bar_dk_read, (it - 1) & 1, abort) ||
+                         !mbar_wait(&sm.bar_dq_read, (it - 1) & 1, abort)))
+            break;
+          tc_fence_after();
+          if (!issue_dk_dq(it)) break;
+          if (more) {
+            if (!mbar_wait(&sm.bar_do_full[(it + 1) & 1], ((it + 1) >> 1) & 1, abort) ||
+                !mbar_wait(&sm.bar_free_dp, ph, abort))
+              break;
+            tc_fence_after();
+            issue_dp(it + 1);
+          }
+        }
+      } else {
+        for (int it = 0; ok && it < n_it; ++it) {
+          const uint32_t ph = it & 1;
+          // S(it) goes in as soon as the previous dK part has been read out of its columns,
+          // dP(it) once the previous dQ halves have been read: both overlap the compute
+          // warps' work on iteration it - 1
+          if (!mbar_wait(&sm.bar_q_full[it & 1], (it >> 1) & 1, abort)) break;
+          if (it > 0 && !mbar_wait(&sm.bar_dk_read, (it - 1) & 1, abort)) break;
+          tc_fence_after();
+          issue_s(it);
+          if (!mbar_wait(&sm.bar_do_full[0], ph, abort)) break;
+          if (it > 0 && !mbar_wait(&sm.bar_free_dp, (it - 1) & 1, abort)) break;
+          tc_fence_after();
+          issue_dp(it);
+          if (!mbar_wait(&sm.bar_p, ph, abort) || !mbar_wait(&sm.bar_do8_full, ph, abort)) break;
+          tc_fence_after();
+          issue_dv(it);
+          if (!mbar_wait(&sm.bar_ds[ph][0], (it >> 1) & 1, abort) || !mbar_wait(&sm.bar_ds[ph][1], (it >> 1) & 1, abort))
+            break;
+          tc_fence_after();
+          if (!issue_dk_dq(it)) break;
+        }
       }
     }
   } else {
@@ -552,40 +673,55 @@ __global__ void __launch_bounds__(384, 1)
     // a wait that times out raises the abort flag; from then on this thread skips its waits
     // but still runs every iteration, so no thread is left behind at a named barrier
     bool ok = true;
+    // one query block of the loop: iteration it, query block I of query head qh, the block's
+    // Q scale and (with Q-smoothing) this row's D_i, both fetched an iteration early
+    struct Blk {
+      int it, I, qh;
+      float sqI, dvec;
+    };
+    int cur_I = I0, cur_qh = qh0, taken = 0;
     float sq_next = prm.sq[(size_t)qh0 * prm.nqb + I0];
-    // with Q-smoothing D_i comes from global memory, also an iteration early
     float dvec_next = QS ? prm.dvec[(size_t)qh0 * prm.np + I0 * 128 + t] : 0.f;
-    // (query block I, query head qh) of iteration it, and of the next, advanced without a division
-    int I = I0, qh = qh0;
-    int In = I0 + 1 < prm.nqb ? I0 + 1 : I0, qhn = I0 + 1 < prm.nqb ? qh : qh + 1;
-    for (int it = 0; it < n_it; ++it) {
-      const uint32_t ph = it & 1;
-      // the query block's scale was fetched an iteration early (global latency off the path)
-      const float sqI = sq_next;
-      if (it + 1 < n_it) sq_next = prm.sq[(size_t)qhn * prm.nqb + In];
-      float dvec_t = dvec_next;
-      if (QS && it + 1 < n_it) dvec_next = prm.dvec[(size_t)qhn * prm.np + In * 128 + t];
-      const int qs = it & 1;
-      ok = ok && mbar_wait(&sm.bar_q_full[qs], (it >> 1) & 1, abort);
+    // the next block in loop order; (I, qh) advance without a division
+    auto take = [&]() -> Blk {
+      const Blk b{taken, cur_I, cur_qh, sq_next, dvec_next};
+      ++taken;
+      if (cur_I + 1 < prm.nqb) {
+        ++cur_I;
+      } else {
+        cur_I = I0;
+        ++cur_qh;
+      }
+      if (taken < n_it) {
+        sq_next = prm.sq[(size_t)cur_qh * prm.nqb + cur_I];
+        if (QS) dvec_next = prm.dvec[(size_t)cur_qh * prm.np + cur_I * 128 + t];
+      }
+      return b;
+    };
+    // P's codes of the block between its P and dS phases: e4m3 (pw), or NVFP4 (pf, psc)
+    uint32_t pw[2][8];
+    uint32_t pf[F4 ? 8 : 1];  // NVFP4: the 64 keys' e2m1 codes, key 8i + k at nibble k of pf[i]
+    uint32_t psc = 0;         // NVFP4: the four 16-key blocks' e4m3 scales, block 0 low
+    float ca = 0.f, cb = 0.f;  // dQ factors of keys [0,64) and [64,128), from the dK readout
+    // ---- P = e4m3(448 * 2^(S2 - LSE2)) on this row's 64 keys of block b, 32 per chunk.  The
+    // codes go to shared memory for the dV MMA and stay in registers for dS.
+    auto p_phase = [&](const Blk& b) {
+      const int qs = b.it & 1;
+      ok = ok && mbar_wait(&sm.bar_q_full[qs], (b.it >> 1) & 1, abort);
       // this query row's scalars: P = 2^(S2 - LSE2) is formed as 2^(S2 + bias) / 448
       const float bias_t = sm.bias[qs][t];
-      if constexpr (!QS) dvec_t = sm.dvec[qs][t];
       // a zero logit scale (all-zero Q or K block: every unmasked S there is 0) becomes the
       // smallest subnormal, so that a masked -inf times it stays -inf.  With Q-smoothing the
       // scale leaves alpha out: it multiplies u = acc c + dsb.
-      const float cs_raw = QS ? __fmul_rn(sqI, sk_mine) : __fmul_rn(__fmul_rn(sqI, sk_mine), prm.alpha);
+      const float cs_raw = QS ? __fmul_rn(b.sqI, sk_mine) : __fmul_rn(__fmul_rn(b.sqI, sk_mine), prm.alpha);
       const float cs = cs_raw > 0.f ? cs_raw : __uint_as_float(1u);
       // masked key columns kc >= klim: padding, and keys after this query on the diagonal block
-      const int klim = (prm.causal && I == kb) ? min(klim_pad, t + 1) : klim_pad;
+      const int klim = (prm.causal && b.I == kb) ? min(klim_pad, t + 1) : klim_pad;
       const bool any_mask = __any_sync(0xffffffffu, klim < (int)kcol + 64);
-      ok = ok && mbar_wait(&sm.bar_s, ph, abort);
+      ok = ok && mbar_wait(&sm.bar_s, b.it & 1, abort);
       tc_fence_after();
-      // ---- P = e4m3(448 * 2^(S2 - LSE2)) on this row's 64 keys, 32 per chunk.  The codes go
-      // to shared memory for the dV MMA and stay in registers for dS.
       uint32_t buf[2][32];
-      uint32_t pw[2][8];
-      uint32_t pf[F4 ? 8 : 1];  // NVFP4: the 64 keys' e2m1 codes, key 8i + k at nibble k of pf[i]
-      uint32_t psc = 0;         // NVFP4: the four 16-key blocks' e4m3 scales, block 0 low
+      psc = 0;
 #pragma unroll
       for (int c = 0; c < 2; ++c) tmem_ld32(tmem + lane_base + cS + kcol + 32 * c, buf[c]);
       tmem_ld_wait();
@@ -696,12 +832,22 @@ __global__ void __launch_bounds__(384, 1)
       }
       fence_proxy_async_smem();
       mbar_arrive(&sm.bar_p);
+    };
+    // ---- 448 dS = p8 (dP - D_i) of block b, then its INT8 codes into shared memory
+    auto ds_phase = [&](const Blk& b) {
       // ---- 448 dS = p8 (dP - D_i), kept in registers until the tile scale is known
-      ok = ok && mbar_wait(&sm.bar_dp, ph, abort);
+      const float dvec_t = QS ? b.dvec : sm.dvec[b.it & 1][t];
+      ok = ok && mbar_wait(&sm.bar_dp, b.it & 1, abort);
       tc_fence_after();
+      uint32_t buf[2][32];
 #pragma unroll
       for (int c = 0; c < 2; ++c) tmem_ld32(tmem + lane_base + cDP + kcol + 32 * c, buf[c]);
       tmem_ld_wait();
+      if constexpr (PIPE) {
+        // dP is in registers: the next dP may go in
+        tc_fence_before();
+        mbar_arrive(&sm.bar_free_dp);
+      }
 #pragma unroll
       for (int c = 0; c < 2; ++c) reg_fence32(buf[c]);
       float amax = 0.f;
@@ -752,10 +898,13 @@ __global__ void __launch_bounds__(384, 1)
       }
 #pragma unroll
       for (int m = 16; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
-      if (lane == 0) sm.smax[warp] = amax;
+      if (lane == 0) sm.smax[b.it & 1][warp] = amax;
       // the previous iteration's dQ boxes (this group's dS block and Q half) must be read
       // before the block is rewritten below and before the producer refills that Q buffer
-      if (t == 0 && pending_qs >= 0) {
+      if constexpr (PIPE) {
+        // the boxes of block it - 2, whose buffer block it's staging takes, must be read
+        if (t == 0) bulk_wait_read_but_last();
+      } else if (t == 0 && pending_qs >= 0) {
         bulk_wait_read_all();
         mbar_arrive(&sm.bar_q_free[pending_qs]);
         pending_qs = -1;
@@ -763,11 +912,12 @@ __global__ void __launch_bounds__(384, 1)
       named_bar_group(g);
       // NVFP4: the dS codes take the block over once the dV MMA has read P^ from it
       if constexpr (F4) {
-        ok = ok && mbar_wait(&sm.bar_dv, ph, abort);
+        ok = ok && mbar_wait(&sm.bar_dv, b.it & 1, abort);
         tc_fence_after();
       }
       // the group's tile (128 queries x 64 keys) max; values are 448 dS
-      const float amine = fmaxf(fmaxf(sm.smax[4 * g], sm.smax[4 * g + 1]), fmaxf(sm.smax[4 * g + 2], sm.smax[4 * g + 3]));
+      const float* smx = sm.smax[b.it & 1] + 4 * g;
+      const float amine = fmaxf(fmaxf(smx[0], smx[1]), fmaxf(smx[2], smx[3]));
       const float inv = amine > 0.f ? 127.0f / amine : 0.f;  // code = rint(448 dS * 127 / max|448 dS|)
       // ---- dS codes -> shared memory (bf16 containers, 128B-swizzled query rows).  Rounding to
       // the nearest integer (ties to even) stays in the fp32 pipe: RN(x * inv + 1.5 * 2^23) - 1.5 * 2^23;
@@ -793,12 +943,15 @@ __global__ void __launch_bounds__(384, 1)
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&sm.bar_ds[g]);
+      mbar_arrive(&sm.bar_ds[b.it & 1][g]);
+    };
+    // ---- dK += RN(s_dS * s_q) * part (key row t) of block b, and the dQ factors of its parts
+    auto readout = [&](const Blk& b) {
       // Q-smoothing: this query block's mean over this group's features, for the dK term
       // (loaded while the dK MMA runs)
       float qb[QS ? DG : 1];
       if constexpr (QS) {
-        const float4* src = reinterpret_cast<const float4*>(prm.qmean + ((size_t)qh * prm.nqb + I) * D + dcol);
+        const float4* src = reinterpret_cast<const float4*>(prm.qmean + ((size_t)b.qh * prm.nqb + b.I) * D + dcol);
 #pragma unroll
         for (int c = 0; c < DG / 4; ++c) {
           const float4 v = __ldg(src + c);
@@ -806,18 +959,21 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       // ---- dK += RN(s_dS * s_q) * part (key row t);  dQ (query row t) += ca * part0 + cb * part1
-      ok = ok && mbar_wait(&sm.bar_dk, ph, abort);
+      ok = ok && mbar_wait(&sm.bar_dk, b.it & 1, abort);
       tc_fence_after();
       // the other group's tile max: its codes are in (bar_dk completed after both groups' codes),
       // and the waits below make its smax writes visible here
-      ok = ok && mbar_wait(&sm.bar_ds[0], ph, abort) && mbar_wait(&sm.bar_ds[1], ph, abort);
-      const float a0 = fmaxf(fmaxf(sm.smax[0], sm.smax[1]), fmaxf(sm.smax[2], sm.smax[3]));
-      const float a1 = fmaxf(fmaxf(sm.smax[4], sm.smax[5]), fmaxf(sm.smax[6], sm.smax[7]));
+      ok = ok && mbar_wait(&sm.bar_ds[b.it & 1][0], (b.it >> 1) & 1, abort) &&
+           mbar_wait(&sm.bar_ds[b.it & 1][1], (b.it >> 1) & 1, abort);
+      const float* smx = sm.smax[b.it & 1];
+      const float a0 = fmaxf(fmaxf(smx[0], smx[1]), fmaxf(smx[2], smx[3]));
+      const float a1 = fmaxf(fmaxf(smx[4], smx[5]), fmaxf(smx[6], smx[7]));
       // values are 448 * dS: scale s_dS = max|dS| / 127
       const float sds0 = a0 > 0.f ? __fdiv_rn(a0 * (F4 ? 1.0f / 2688.0f : 1.0f / 448.0f), 127.0f) : 0.f;
       const float sds1 = a1 > 0.f ? __fdiv_rn(a1 * (F4 ? 1.0f / 2688.0f : 1.0f / 448.0f), 127.0f) : 0.f;
-      const float ck = __fmul_rn(t >> 6 ? sds1 : sds0, sqI);
-      const float ca = __fmul_rn(sds0, sk0), cb = __fmul_rn(sds1, sk1);
+      const float ck = __fmul_rn(t >> 6 ? sds1 : sds0, b.sqI);
+      ca = __fmul_rn(sds0, sk0);
+      cb = __fmul_rn(sds1, sk1);
       // Q-smoothing: dK row t += RN(s_dS * sum_i dS8_it) * qmean (the sum is exact in TMEM)
       float cq = 0.f;
       if constexpr (QS) {
@@ -831,18 +987,18 @@ __global__ void __launch_bounds__(384, 1)
       }
       {
         uint32_t kA[16], kB[16];
-        tmem_ld16(tmem + lane_base + cS + dcol, kA);
+        tmem_ld16(tmem + lane_base + cDK + dcol, kA);
         tmem_wait16(kA);
 #pragma unroll
         for (int c = 0; c < DG; c += 32) {
-          tmem_ld16(tmem + lane_base + cS + dcol + c + 16, kB);
+          tmem_ld16(tmem + lane_base + cDK + dcol + c + 16, kB);
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             dk[c + e] = fmaf(ck, __uint_as_float(kA[e]), dk[c + e]);
             if constexpr (QS) dk[c + e] = fmaf(cq, qb[c + e], dk[c + e]);
           }
           tmem_wait16(kB);
-          if (c + 32 < DG) tmem_ld16(tmem + lane_base + cS + dcol + c + 32, kA);
+          if (c + 32 < DG) tmem_ld16(tmem + lane_base + cDK + dcol + c + 32, kA);
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             dk[c + 16 + e] = fmaf(ck, __uint_as_float(kB[e]), dk[c + 16 + e]);
@@ -851,14 +1007,21 @@ __global__ void __launch_bounds__(384, 1)
           if (c + 32 < DG) tmem_wait16(kA);
         }
       }
-      // the dK part is in registers: the next S may overwrite its columns
+      // the dK part is in registers: its columns are free
       tc_fence_before();
-      mbar_arrive(&sm.bar_free_s);
-      ok = ok && mbar_wait(&sm.bar_part, ph, abort);
+      mbar_arrive(&sm.bar_dk_read);
+    };
+    // ---- dQ parts of block bk: ca * part0 + cb * part1 (query row t) staged as fp32 boxes and
+    // added to the accumulator by TMA reduce
+    auto staging = [&](const Blk& bk) {
+      const int qs = bk.it & 1;
+      ok = ok && mbar_wait(&sm.bar_part, bk.it & 1, abort);
       tc_fence_after();
       {
-        // staging slot of box b (features dcol + 32b ..): this group's dS block, then half g of q[qs]
+        // staging slot of box b (features dcol + 32b ..): this group's dS block, then half g of
+        // q[qs]; PIPE: this group's box of the block's parity
         auto slot = [&](int b) -> float* {
+          if constexpr (PIPE) return reinterpret_cast<float*>(sm.dqst + (2 * qs + g) * 16384);
           return reinterpret_cast<float*>(b == 0 ? sm.ds + g * 16384 : sm.q[qs] + g * 16384);
         };
         uint32_t va[2][16], vb[2][16];
@@ -874,9 +1037,10 @@ __global__ void __launch_bounds__(384, 1)
             tmem_ld16(tmem + lane_base + cDQ0 + dcol + c + 16, va[cur ^ 1]);
             tmem_ld16(tmem + lane_base + cDQ1 + dcol + c + 16, vb[cur ^ 1]);
           } else {
-            // every TMEM read of this iteration is done: the next dP may start
+            // every TMEM read of the block is done: the next dQ parts (and, with dQ1 in the
+            // dP columns, the next dP) may go in
             tc_fence_before();
-            mbar_arrive(&sm.bar_free_dp);
+            mbar_arrive(PIPE ? &sm.bar_dq_read : &sm.bar_free_dp);
           }
           // box row = feature, column = query row t: a warp stores 128 contiguous bytes
           float* box = slot(c >> 5) + (c & 31) * 128 + t;
@@ -893,18 +1057,33 @@ __global__ void __launch_bounds__(384, 1)
         named_bar_group(g);
         if (t == 0) {
 #pragma unroll
-          for (int b = 0; b < DG / 32; ++b) tma_reduce_add_3d(&tm_dq, slot(b), I * 128, (int)dcol + 32 * b, qh);
+          for (int bx = 0; bx < DG / 32; ++bx) tma_reduce_add_3d(&tm_dq, slot(bx), bk.I * 128, (int)dcol + 32 * bx, bk.qh);
           bulk_commit();
           pending_qs = qs;
         }
       }
-      I = In;
-      qh = qhn;
-      if (In + 1 < prm.nqb) {
-        ++In;
+    };
+    // Without PIPE each query block runs P, dS, the dK readout and the dQ staging in turn.  With
+    // PIPE (dK, dQ and dP in TMEM columns of their own) the order is software-pipelined: step s
+    // runs P of block s, then the readouts of block s - 1 (whose dK and dQ MMAs ran meanwhile),
+    // then dS of block s (whose dP went in after block s - 1's dK readout).
+    Blk cur{}, prev{};
+    for (int s = 0; s < n_it + (PIPE ? 1 : 0); ++s) {
+      if (s < n_it) {
+        cur = take();
+        p_phase(cur);
+      }
+      if constexpr (PIPE) {
+        if (s > 0) {
+          readout(prev);
+          staging(prev);
+        }
+        if (s < n_it) ds_phase(cur);
+        prev = cur;
       } else {
-        In = I0;
-        ++qhn;
+        ds_phase(cur);
+        readout(cur);
+        staging(cur);
       }
     }
     // the last reductions must complete before the CTA's shared memory goes away
