@@ -10,11 +10,16 @@ from bit_trainable_attention_sagebwd_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
 
-# (workload with H query heads, key/value heads Hkv)
+# (workload with H query heads, key/value heads Hkv).  The backward splits a key block's query
+# heads over `split` CTAs (a divisor of the group, at most 2 x SMs / key tiles); the last two
+# cases have enough key tiles (32 and 40 per head) that split stays below the group on 148 or
+# 152 SMs, so every CTA loops over two query heads (16 / 8 and 8 / 4).
 CASES = [
     (wl.custom(1, 4, 333, 64, True, seed=50, kind="k_offset2", name="h4_kv2_n333_d64_causal"), 2),
     (wl.custom(2, 3, 256, 128, False, qk_norm=True, sm_scale=16.0, seed=51, name="b2_h3_mqa_qknorm"), 1),
     (wl.custom(1, 8, 640, 128, True, seed=52, kind="student_t3", name="h8_kv2_n640_d128_causal"), 2),
+    (wl.custom(1, 16, 4000, 64, True, seed=53, kind="k_offset2", name="h16_mqa_n4000_d64_causal"), 1),
+    (wl.custom(1, 8, 5000, 128, True, seed=54, name="h8_mqa_n5000_d128_causal"), 1),
 ]
 
 
